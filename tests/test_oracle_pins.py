@@ -1,0 +1,447 @@
+"""Pins for the CPU oracle: each check ties the oracle to something other than its own formula
+(hand-worked values, published test vectors, closed forms, exact identities, finite differences,
+brute force), so that a dropped term, a wrong sign, index or transposed operand fails one of them.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+from oracle import lora_oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _rng(seed=0):
+    return np.random.default_rng(seed)
+
+
+# ------------------------------------------------------------------------------------------ hash
+def test_mix64_matches_published_splitmix64_outputs():
+    g = _golden("splitmix64_seed0.json")
+    state = 0
+    for want in g["outputs_hex"]:
+        state = (state + O.GOLDEN_GAMMA) & ((1 << 64) - 1)
+        assert O.mix64(state) == int(want, 16)
+
+
+def _inv_xorshift(y, sh):
+    x = y
+    for _ in range(64 // sh + 1):
+        x = y ^ (x >> sh)
+    return x
+
+
+def test_mix64_is_a_bijection_via_its_algebraic_inverse():
+    M = (1 << 64) - 1
+    i1 = pow(0xBF58476D1CE4E5B9, -1, 1 << 64)
+    i2 = pow(0x94D049BB133111EB, -1, 1 << 64)
+    rng = _rng(1)
+    for z in [0, 1, M] + [int(v) for v in rng.integers(0, 2**63, 200, dtype=np.int64)]:
+        y = O.mix64(z)
+        x = _inv_xorshift(y, 31)
+        x = (x * i2) & M
+        x = _inv_xorshift(x, 27)
+        x = (x * i1) & M
+        x = _inv_xorshift(x, 30)
+        assert x == z
+
+
+def test_mix64_array_and_scalar_forms_agree():
+    zs = _rng(2).integers(0, 2**63, 64, dtype=np.int64).astype(np.uint64)
+    arr = O.mix64(zs)
+    assert [int(v) for v in arr] == [O.mix64(int(z)) for z in zs]
+
+
+@pytest.mark.parametrize("p", [0.1, 0.5, 0.9])
+def test_dropout_rate_within_binomial_bounds(p):
+    keep = O.dropout_keep(p, 1234, 25, 0, 3, 2, 512, 768)
+    n = keep.size
+    dropped = n - keep.sum()
+    sigma = math.sqrt(n * p * (1 - p))
+    assert abs(dropped - n * p) < 6 * sigma
+
+
+def test_dropout_threshold_edges():
+    assert O.dropout_threshold(0.0) == 0
+    assert O.dropout_threshold(0.5) == 1 << 31
+    assert O.dropout_threshold(0.25) == 1 << 30
+    assert np.all(O.dropout_keep(0.0, 1, 2, 3, 4, 5, 7, 9) == 1.0)
+    assert O.dropout_q(0.5) == 2.0
+    assert O.dropout_q(0.1) == float(np.float32(1 / 0.9))
+
+
+def test_dropout_is_deterministic_and_every_key_field_matters():
+    base = dict(p=0.3, seed=42, opt_step=7, accum_ordinal=1, layer=5, proj=3, T=16, in_dim=64)
+    m0 = O.dropout_keep(**base)
+    assert np.array_equal(m0, O.dropout_keep(**base))
+    for field, val in [("seed", 43), ("opt_step", 8), ("accum_ordinal", 2), ("layer", 6),
+                       ("proj", 4)]:
+        other = dict(base, **{field: val})
+        assert not np.array_equal(m0, O.dropout_keep(**other)), field
+
+
+def test_dropout_chunked_call_equals_per_chunk_calls():
+    a = O.dropout_keep(0.2, 9, 3, 4, 1, 1, 24, 40, chunk_tokens=8)
+    parts = [O.dropout_keep(0.2, 9, 3, 4 + c, 1, 1, 8, 40) for c in range(3)]
+    assert np.array_equal(a, np.concatenate(parts))
+
+
+def test_dropout_hash_brute_force_single_element():
+    # element (t, i) of chunk `ordinal`: mix(key ^ (t*in + i)), dropped iff top 32 bits < tau
+    p, seed, step, ordinal, layer, proj, in_dim = 0.37, 77, 11, 3, 9, 4, 13
+    key = O.mix64(O.mix64(O.mix64(seed ^ O.GOLDEN_GAMMA) ^ step) ^ ((ordinal << 48) | (layer << 16) | proj))
+    keep = O.dropout_keep(p, seed, step, ordinal, layer, proj, 5, in_dim)
+    tau = int(p * 2**32)
+    for t in range(5):
+        for i in range(in_dim):
+            h = O.mix64(key ^ (t * in_dim + i))
+            assert keep[t, i] == (1.0 if (h >> 32) >= tau else 0.0)
+
+
+# ---------------------------------------------------------------------------------- forward/back
+def test_hand_worked_forward_backward():
+    g = _golden("hand_worked.json")["lora_1x2"]
+    s = O.lora_scale(g["alpha"], g["rank"], False)
+    f = O.lora_forward(g["X"], g["W"], g["A"], g["B"], s)
+    b = O.lora_backward(g["X"], g["W"], g["A"], g["B"], g["dY"], s)
+    np.testing.assert_array_equal(f.Y, g["Y"])
+    np.testing.assert_array_equal(b.dX, g["dX"])
+    np.testing.assert_array_equal(b.dA, g["dA"])
+    np.testing.assert_array_equal(b.dB, g["dB"])
+
+
+def test_scaling_standard_and_rslora():
+    assert O.lora_scale(16, 8, False) == 2.0
+    assert O.lora_scale(128, 64, True) == 16.0
+    assert O.lora_scale(8, 4, False) == 2.0
+
+
+def _problem(T=6, n_in=5, n_out=4, r=3, seed=3):
+    rng = _rng(seed)
+    return (rng.standard_normal((T, n_in)), rng.standard_normal((n_out, n_in)) / 2,
+            rng.standard_normal((r, n_in)), rng.standard_normal((n_out, r)),
+            rng.standard_normal((T, n_out)))
+
+
+def test_zero_adapter_is_a_noop_and_gives_zero_dA():
+    X, W, A, B, dY = _problem()
+    B0 = np.zeros_like(B)
+    f = O.lora_forward(X, W, A, B0, 2.0)
+    np.testing.assert_array_equal(f.Y, X @ W.T)
+    b = O.lora_backward(X, W, A, B0, dY, 2.0)
+    assert np.all(b.dA == 0.0)
+    np.testing.assert_array_equal(b.dX, dY @ W)
+
+
+def test_forward_equals_merged_weight():
+    X, W, A, B, _ = _problem(T=9, n_in=7, n_out=6, r=2)
+    s = 1.5
+    f = O.lora_forward(X, W, A, B, s)
+    merged = W + s * (B @ A)
+    np.testing.assert_allclose(f.Y, np.einsum("ti,oi->to", X, merged), rtol=1e-13, atol=1e-13)
+
+
+def _loss(Y, dY):
+    return float(np.sum(Y * dY))
+
+
+@pytest.mark.parametrize("p", [0.0, 0.4])
+def test_backward_matches_central_finite_differences(p):
+    X, W, A, B, dY = _problem(T=4, n_in=5, n_out=3, r=2, seed=5)
+    s = 1.25
+    keep = O.dropout_keep(p, 1, 2, 0, 0, 0, X.shape[0], X.shape[1]) if p > 0 else None
+    q = O.dropout_q(p) if p > 0 else 1.0
+    b = O.lora_backward(X, W, A, B, dY, s, keep, q)
+    h = 1e-3
+
+    def L(X_, A_, B_):
+        return _loss(O.lora_forward(X_, W, A_, B_, s, keep, q).Y, dY)
+
+    for name, arr, grad in [("X", X, b.dX), ("A", A, b.dA), ("B", B, b.dB)]:
+        fd = np.zeros_like(arr)
+        for idx in np.ndindex(arr.shape):
+            plus, minus = arr.copy(), arr.copy()
+            plus[idx] += h
+            minus[idx] -= h
+            args_p = {"X": X, "A": A, "B": B}
+            args_m = dict(args_p)
+            args_p[name], args_m[name] = plus, minus
+            fd[idx] = (L(args_p["X"], args_p["A"], args_p["B"]) -
+                       L(args_m["X"], args_m["A"], args_m["B"])) / (2 * h)
+        np.testing.assert_allclose(grad, fd, rtol=1e-8, atol=1e-9, err_msg=name)
+
+
+def test_dropout_masks_only_the_adapter_branch():
+    X, W, A, B, dY = _problem(T=5, n_in=6, n_out=4, r=2, seed=8)
+    keep = O.dropout_keep(0.5, 3, 0, 0, 0, 0, 5, 6)
+    f = O.lora_forward(X, W, A, B, 1.0, keep, 2.0)
+    # frozen part unmasked, adapter part sees the masked input scaled by q
+    np.testing.assert_allclose(f.Y, X @ W.T + 2.0 * ((keep * X) @ A.T) @ B.T, rtol=1e-13)
+    # with an all-zero mask the output is exactly the frozen product
+    f0 = O.lora_forward(X, W, A, B, 1.0, np.zeros_like(X), 2.0)
+    np.testing.assert_array_equal(f0.Y, X @ W.T)
+
+
+def test_adjointness_of_frozen_forward_and_transpose():
+    X, W, A, B, dY = _problem(T=7, n_in=6, n_out=5, r=2, seed=11)
+    B0 = np.zeros_like(B)
+    y = O.lora_forward(X, W, A, B0, 1.0).Y
+    dx = O.lora_backward(X, W, A, B0, dY, 1.0).dX
+    assert abs(np.sum(y * dY) - np.sum(X * dx)) < 1e-12 * max(1.0, abs(np.sum(y * dY)))
+
+
+# ---------------------------------------------------------------------------------------- DoRA
+def test_dora_row_norm_matches_expanded_identity():
+    _, W, A, B, _ = _problem(n_in=8, n_out=5, r=3, seed=12)
+    s = 0.7
+    n = O.dora_row_norm(W, A, B, s)
+    WAt = W @ A.T
+    AAt = A @ A.T
+    n2 = np.sum(W * W, 1) + 2 * s * np.sum(B * WAt, 1) + s * s * np.einsum("oj,jk,ok->o", B, AAt, B)
+    np.testing.assert_allclose(n, np.sqrt(n2), rtol=1e-12)
+
+
+def test_dora_with_zero_adapter_and_row_norm_magnitude_is_plain():
+    X, W, A, B, _ = _problem(seed=13)
+    B0 = np.zeros_like(B)
+    n = O.dora_row_norm(W, A, B0, 2.0)
+    np.testing.assert_allclose(n, np.linalg.norm(W, axis=1), rtol=1e-14)
+    f = O.lora_forward(X, W, A, B0, 2.0, mag=np.linalg.norm(W, axis=1), rownorm=n)
+    np.testing.assert_allclose(f.Y, X @ W.T, rtol=1e-13, atol=1e-14)
+
+
+def test_dora_backward_finite_differences_with_fixed_norm():
+    X, W, A, B, dY = _problem(T=3, n_in=4, n_out=3, r=2, seed=14)
+    s = 0.9
+    mag = np.abs(_rng(15).standard_normal(3)) + 0.5
+    n = O.dora_row_norm(W, A, B, s)
+    b = O.lora_backward(X, W, A, B, dY, s, mag=mag, rownorm=n)
+    h = 1e-3
+
+    def L(X_, A_, B_, m_):
+        return _loss(O.lora_forward(X_, W, A_, B_, s, mag=m_, rownorm=n).Y, dY)
+
+    for name, grad in [("X", b.dX), ("A", b.dA), ("B", b.dB), ("m", b.dm)]:
+        base = {"X": X, "A": A, "B": B, "m": mag}
+        arr = base[name]
+        fd = np.zeros_like(arr)
+        for idx in np.ndindex(arr.shape):
+            p_, m_ = dict(base), dict(base)
+            p_[name] = arr.copy(); p_[name][idx] += h
+            m_[name] = arr.copy(); m_[name][idx] -= h
+            fd[idx] = (L(p_["X"], p_["A"], p_["B"], p_["m"]) - L(m_["X"], m_["A"], m_["B"], m_["m"])) / (2 * h)
+        np.testing.assert_allclose(grad, fd, rtol=1e-8, atol=1e-9, err_msg=name)
+
+
+# ------------------------------------------------------------------------------ clip / optimizer
+def test_clip_hand_worked():
+    g = _golden("hand_worked.json")
+    for case in ("clip_3_4", "clip_normalise_only"):
+        c = g[case]
+        p = O.grad_prepare([np.array(c["grads"])], c["grad_scale"], c["max_norm"])
+        assert p.status == O.STATUS_OK
+        assert abs(p.scale - c["scale"]) < 1e-15 and abs(p.norm - c["norm"]) < 1e-15
+
+
+def test_clip_closed_form_constant_tensors():
+    # two constant tensors: S = n1 v1^2 + n2 v2^2
+    g1, g2 = np.full(300, 0.5, np.float32), np.full((20, 7), -2.0, np.float32)
+    S = 300 * 0.25 + 140 * 4.0
+    gamma = 1.0 / 64
+    for max_norm in (0.0, 0.1, 1e6):
+        p = O.grad_prepare([g1, g2], gamma, max_norm)
+        norm = gamma * math.sqrt(S)
+        assert abs(p.norm - norm) < 1e-15
+        want = gamma * min(1.0, max_norm / norm) if max_norm > 0 else gamma
+        assert abs(p.scale - want) < 1e-17
+    # a norm exactly at the limit is not clipped (strict test)
+    p = O.grad_prepare([np.array([3.0, 4.0])], 1.0, 5.0)
+    assert p.scale == 1.0
+
+
+@pytest.mark.parametrize("bad", [np.nan, np.inf, -np.inf])
+def test_clip_rejects_non_finite(bad):
+    g = np.ones(10, np.float32)
+    g[3] = bad
+    assert O.grad_prepare([np.ones(4), g], 1.0, 1.0).status == O.STATUS_NONFINITE
+
+
+def test_decay_touches_A_only_and_uses_pre_update_value():
+    rng = _rng(20)
+    A, B = rng.standard_normal(50).astype(np.float32), rng.standard_normal(50).astype(np.float32)
+    z = np.zeros(50, np.float32)
+    hp = O.AdamHP(lr=1e-2, wd=0.1, plus_ratio=4.0, step=0)
+    A1, _, _ = O.adamw_update(A, z, z, z, O.KIND_A, 1.0, hp)
+    B1, _, _ = O.adamw_update(B, z, z, z, O.KIND_B, 1.0, hp)
+    np.testing.assert_array_equal(A1, (A.astype(np.float64) * (1 - 1e-2 * 0.1)).astype(np.float32))
+    np.testing.assert_array_equal(B1, B)
+
+
+def test_decay_uses_scheduled_not_bias_corrected_lr():
+    # g = 0 with nonzero moments at step k: decay term is lr*wd*A regardless of 1/(1-b1^k)
+    A = np.full(4, 2.0, np.float32)
+    m = np.zeros(4, np.float32)
+    v = np.zeros(4, np.float32)
+    hp = O.AdamHP(lr=0.5, wd=0.2, step=3)
+    A1, _, _ = O.adamw_update(A, np.zeros(4), m, v, O.KIND_A, 1.0, hp)
+    np.testing.assert_array_equal(A1, np.full(4, 2.0 - 0.5 * 0.2 * 2.0, np.float32))
+
+
+def test_adam_first_step_is_normalised_sign_step():
+    # textbook Adam from zero moments: m_hat = g_hat, v_hat = g_hat^2, u = g_hat / (|g_hat| + eps)
+    g = np.array([1e-3, -2.0, 5e-9, 0.0], np.float64)
+    p = np.zeros(4, np.float32)
+    z = np.zeros(4, np.float32)
+    hp = O.AdamHP(lr=0.1, wd=0.0, step=0)
+    for kind, ratio in ((O.KIND_A, 1.0), (O.KIND_B, 1.0)):
+        p1, m1, v1 = O.adamw_update(p, g, z, z, kind, 1.0, hp)
+        want = -0.1 * ratio * g / (np.abs(g) + 1e-8)
+        np.testing.assert_allclose(p1, want.astype(np.float32), rtol=1e-6, atol=1e-30)
+        np.testing.assert_allclose(m1, 0.1 * g, rtol=1e-6)
+        np.testing.assert_allclose(v1, 0.001 * g * g, rtol=1e-6)
+
+
+def test_lora_plus_scales_B_update_exactly():
+    # from B = 0 a power-of-two ratio scales the fp32 result exactly, and decay never applies
+    rng = _rng(21)
+    B = np.zeros(64, np.float32)
+    g = rng.standard_normal(64)
+    m = (rng.standard_normal(64) * 1e-3).astype(np.float32)
+    v = (rng.random(64) * 1e-6).astype(np.float32)
+    d = {}
+    for rho in (1.0, 16.0):
+        hp = O.AdamHP(lr=1e-3, wd=0.5, plus_ratio=rho, step=4)
+        d[rho], _, _ = O.adamw_update(B, g, m, v, O.KIND_B, 0.3, hp)
+    np.testing.assert_array_equal(d[16.0], 16.0 * d[1.0])
+    assert np.all(d[1.0] != 0)
+
+
+def test_magnitude_update_has_no_decay_and_ratio_one():
+    mag = np.full(8, 3.0, np.float32)
+    z = np.zeros(8, np.float32)
+    hp = O.AdamHP(lr=0.5, wd=0.9, plus_ratio=10.0, step=0)
+    m1, _, _ = O.adamw_update(mag, np.zeros(8), z, z, O.KIND_MAG, 1.0, hp)
+    np.testing.assert_array_equal(m1, mag)
+    g = np.full(8, 2.0)
+    m2, _, _ = O.adamw_update(mag, g, z, z, O.KIND_MAG, 1.0, hp)
+    np.testing.assert_allclose(m2, 3.0 - 0.5 * 2.0 / (2.0 + 1e-8), rtol=1e-7)
+
+
+# ------------------------------------------------------------------------------------- schedule
+def test_schedule_closed_forms():
+    base, mn = 1e-4, 1e-6
+    assert O.lr_at("constant", base, 12345, 10, 100, mn) == base
+    assert O.lr_at("cosine", base, 0, 10, 100, mn) == pytest.approx(base / 10, rel=1e-15)
+    assert O.lr_at("cosine", base, 9, 10, 100, mn) == pytest.approx(base, rel=1e-15)
+    assert O.lr_at("cosine", base, 10, 10, 100, mn) == pytest.approx(base, rel=1e-15)
+    assert O.lr_at("cosine", base, 55, 10, 100, mn) == pytest.approx((base + mn) / 2, rel=1e-14)
+    assert O.lr_at("cosine", base, 100, 10, 100, mn) == pytest.approx(mn, rel=1e-12)
+    assert O.lr_at("cosine", base, 1000, 10, 100, mn) == pytest.approx(mn, rel=1e-12)
+    g = _golden("hand_worked.json")["cosine_at_25"]
+    assert O.lr_at("cosine", base, 25, 10, 100, mn) == pytest.approx(g["lr"], rel=1e-14)
+    seq = [O.lr_at("cosine", base, k, 10, 100, mn) for k in range(10, 101)]
+    assert all(a >= b for a, b in zip(seq, seq[1:]))
+
+
+# ---------------------------------------------------------------------------------- accumulation
+def _small_problems(T, seed, n_layers=2, dora=False):
+    rng = _rng(seed)
+    problems, state = {}, {}
+    for l in range(n_layers):
+        X = rng.standard_normal((T, 8))
+        W = rng.standard_normal((6, 8)) / 3
+        dY = rng.standard_normal((T, 6))
+        A = rng.uniform(-0.8, 0.8, (2, 8)).astype(np.float32)
+        B = (rng.standard_normal((6, 2)) * 0.1).astype(np.float32)
+        problems[l] = dict(X=X, W=W, dY=dY, layer=l, proj=0)
+        z = lambda a: np.zeros_like(a)
+        st = O.AdapterState(A, B, z(A), z(A), z(B), z(B))
+        if dora:
+            st.mag = np.linalg.norm(W, axis=1).astype(np.float32)
+            st.mM, st.vM = z(st.mag), z(st.mag)
+        state[l] = st
+    return problems, state
+
+
+def test_accumulated_chunks_equal_concatenated_batch():
+    problems, state = _small_problems(T=12, seed=30)
+    kw = dict(s=2.0, p=0.0, seed=0, opt_step=0, max_norm=1.0, hp=O.AdamHP(lr=1e-3))
+    r3 = O.run_single_step(problems, state, chunks=3, **kw)
+    r1 = O.run_single_step(problems, state, chunks=1, **kw)
+    for k in problems:
+        for a, b in zip(r3.grads[k][:2], r1.grads[k][:2]):
+            np.testing.assert_allclose(a, b, rtol=1e-6, atol=1e-6)
+    assert r3.prepared.scale == pytest.approx(r1.prepared.scale, rel=1e-6)
+    # gamma = 1 / total prediction tokens
+    sq = sum(float(np.sum(np.float64(g) ** 2)) for k in problems for g in r1.grads[k][:2])
+    assert r1.prepared.norm == pytest.approx(math.sqrt(sq) / 12, rel=1e-12)
+
+
+def test_step_rejects_non_finite_without_mutation():
+    problems, state = _small_problems(T=4, seed=31)
+    problems[1]["dY"] = problems[1]["dY"].copy()
+    problems[1]["dY"][2, 3] = np.nan
+    r = O.run_single_step(problems, state, s=1.0, chunks=2, p=0.0, seed=0, opt_step=0,
+                          max_norm=1.0, hp=O.AdamHP(lr=1e-3))
+    assert r.prepared.status == O.STATUS_NONFINITE
+    for k in problems:
+        assert r.new_state[k] is state[k]
+
+
+# ------------------------------------------------------------------------------------ multi-LoRA
+def test_token_slots_brute_force():
+    seg_start = [0, 3, 3, 7, 10]
+    seg_slot = [1, 0, 2, 9]
+    ts = O.token_slots(12, seg_start, seg_slot, 3)
+    assert list(ts) == [1, 1, 1, 2, 2, 2, 2, -1, -1, -1, -1, -1]
+
+
+def test_multi_single_slot_equals_single_lora():
+    X, W, A, B, dY = _problem(T=8, n_in=6, n_out=5, r=3, seed=40)
+    keep = O.dropout_keep(0.25, 1, 0, 0, 0, 0, 8, 6)
+    q = O.dropout_q(0.25)
+    slots = [O.SlotTensors(A, B, 1.5)]
+    ts = O.token_slots(8, [0, 8], [0], 1)
+    Y, H = O.multi_lora_forward(X, W, slots, ts, keep, q)
+    f = O.lora_forward(X, W, A, B, 1.5, keep, q)
+    np.testing.assert_allclose(Y, f.Y, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(H, f.H, rtol=1e-13, atol=1e-13)
+    dX, dA, dB = O.multi_lora_backward(X, W, dY, slots, ts, keep, q)
+    b = O.lora_backward(X, W, A, B, dY, 1.5, keep, q)
+    np.testing.assert_allclose(dX, b.dX, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(dA[0], b.dA, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(dB[0], b.dB, rtol=1e-12, atol=1e-12)
+
+
+def test_multi_slot_gradient_equals_that_slot_training_alone():
+    rng = _rng(41)
+    T, n_in, n_out = 20, 6, 4
+    X, W, dY = rng.standard_normal((T, n_in)), rng.standard_normal((n_out, n_in)), rng.standard_normal((T, n_out))
+    slots = [O.SlotTensors(rng.standard_normal((r, n_in)), rng.standard_normal((n_out, r)), s)
+             for r, s in ((2, 1.0), (3, 2.0), (1, 0.5))]
+    seg_start, seg_slot = [0, 5, 9, 14, 20], [2, 0, 2, 1]
+    ts = O.token_slots(T, seg_start, seg_slot, 3)
+    dX, dA, dB = O.multi_lora_backward(X, W, dY, slots, ts)
+    dXv, dAv, dBv = O.multi_lora_backward_vectorised(X, W, dY, slots, ts)
+    np.testing.assert_allclose(dX, dXv, rtol=1e-12, atol=1e-12)
+    for k, sl in enumerate(slots):
+        rows = ts == k
+        alone = O.lora_backward(X[rows], W, sl.A, sl.B, dY[rows], sl.s)
+        np.testing.assert_allclose(dA[k], alone.dA, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(dB[k], alone.dB, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(dAv[k], alone.dA, rtol=1e-12, atol=1e-12)
+    # the 1/adapter_global_batch_size scaled update of a slot is what it would get alone
+    gbs = 64
+    p_multi = O.grad_prepare([dA[1], dB[1]], 1.0 / gbs, 1.0)
+    p_alone = O.grad_prepare([O.lora_backward(X[ts == 1], W, slots[1].A, slots[1].B, dY[ts == 1], 2.0).dA,
+                              O.lora_backward(X[ts == 1], W, slots[1].A, slots[1].B, dY[ts == 1], 2.0).dB],
+                             1.0 / gbs, 1.0)
+    assert p_multi.scale == pytest.approx(p_alone.scale, rel=1e-12)
