@@ -1,0 +1,449 @@
+"""Benchmark: one optimizer step of LoRA-adapted linears (forward + backward over every
+accumulation chunk, two-pass clip, A-only AdamW) through the C ABI on GB300.
+
+Default workload: TinyLlama-1.1B-shaped wq + wv adapters over 22 layers, fp32 frozen W, rank 8,
+alpha 16, T = 1024 tokens per step in 4 accumulation chunks, clip 1.0, constant lr 2e-4.
+`--config c3|c4|c4dora|c5` selects the other workloads. Inputs are seeded synthetic tensors.
+
+Prints ONE JSON line (rank 0). `--impl reference` times the CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import lora_inputs as LI  # noqa: E402
+
+METRIC = "LoRA linear fwd+bwd+step tokens/s on 1 GB300; % of tensor/HBM roofline"
+UNIT = "tokens/s"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--config", default="c2", choices=sorted(LI.CONFIGS))
+    p.add_argument("--layers", type=int, default=0, help="override the layer count (0 = config's)")
+    p.add_argument("--streams", type=int, default=1)
+    p.add_argument("--no-graph", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--prof-class", type=int, default=0, help="kernel class to time (0 = auto)")
+    return p.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+# --------------------------------------------------------------------------------- algorithmic counts
+def counts(cfg: LI.LoraConfig, layers: int):
+    """Per-step algorithmic flops/bytes (stated in the design doc): frozen = 2 T in out per product,
+    fused LoRA terms = 2 T r out (forward) / 2 T r in (dX); optimizer = 32 B/param."""
+    T, r = cfg.tokens, cfg.rank
+    a = 4 if cfg.dtype == "f32" else 2
+    fwd = sum(2 * T * p.in_dim * p.out_dim + 2 * T * r * p.out_dim for p in cfg.projs) * layers
+    dx = sum(2 * T * p.in_dim * p.out_dim + 2 * T * r * p.in_dim for p in cfg.projs) * layers
+    lowrank = sum(6 * T * r * (p.in_dim + p.out_dim) for p in cfg.projs) * layers
+    params = sum(r * (p.in_dim + p.out_dim) for p in cfg.projs) * layers
+    return dict(fwd_flops_per_launch=fwd / (len(cfg.projs) * layers),
+                dx_flops_per_launch=dx / (len(cfg.projs) * layers),
+                fwd_flops=fwd, dx_flops=dx, lowrank_flops=lowrank, params=params,
+                opt_bytes=32 * params, act_bytes=a)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "sm_max_mhz": 2070.0}, "fallback"
+
+
+# --------------------------------------------------------------------------------- clocks sampler
+class Clocks:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------------- workload
+def _scale(cfg, L):
+    return L.lora_scale(cfg.alpha, cfg.rank, cfg.rslora)
+
+
+def make_single(cfg, layers, streams, device):
+    import torch
+    from bwd_adapter_adamw_gb300 import binding as L
+    from bwd_adapter_adamw_gb300.step import Linear, LoraStep
+    linears, xs = [], {}
+    for l in range(layers):
+        for pi, pr in enumerate(cfg.projs):
+            key = (l, pr.x_group)
+            if key not in xs:
+                xs[key] = LI.make_x(cfg, l, pr, device=device)
+            linears.append(Linear(l, pi, xs[key], LI.make_w(cfg, l, pr, device=device),
+                                  LI.make_dy(cfg, l, pr, device=device)))
+    hp = L.make_hp(cfg.beta1, cfg.beta2, cfg.eps, cfg.wd, cfg.plus_ratio)
+    step = LoraStep(linears, rank=cfg.rank, scale=_scale(cfg, L), dtype=cfg.dtype,
+                    tokens=cfg.tokens, chunks=cfg.chunks, dropout_p=cfg.dropout_p,
+                    seed=cfg.dropout_seed, dora=cfg.dora, max_norm=cfg.max_norm, hp=hp,
+                    n_streams=streams, device=device)
+    for lin in step.linears:
+        pr = cfg.projs[lin.proj_id]
+        lin.A.copy_(LI.make_a(cfg, lin.layer, pr, device=device))
+        lin.B.copy_(LI.make_b(cfg, lin.layer, pr, device=device))
+        if cfg.dora:
+            lin.mag.copy_(LI.dora_magnitude_init(lin.W))
+    m, v = LI.make_adam_state(cfg, step.arena.n, "all", device=device)
+    step.arena.m.copy_(m)
+    step.arena.v.copy_(v)
+    step.prepare_weights()
+    inputs = list(xs.values()) + [lin.dY for lin in step.linears]
+    lr = L.lora_lr_at(1 if cfg.sched == "cosine" else 0, cfg.lr, cfg.opt_step, cfg.warmup,
+                      cfg.total, cfg.min_lr)
+
+    def run():
+        step.run(cfg.opt_step, lr)
+
+    return step, run, inputs, [step.scale_norm, step.status]
+
+
+def make_multi(cfg, streams, device):
+    import torch
+    from bwd_adapter_adamw_gb300 import binding as L
+    from bwd_adapter_adamw_gb300.step import MultiLinear, MultiLoraStep
+    r = LI.make_routing(cfg)
+    xs, lins = {}, []
+    for pi, pr in enumerate(cfg.projs):
+        if pr.x_group not in xs:
+            xs[pr.x_group] = LI.make_x(cfg, 0, pr, device=device)
+        lins.append(MultiLinear(pi, xs[pr.x_group], LI.make_w(cfg, 0, pr, device=device),
+                                LI.make_dy(cfg, 0, pr, device=device)))
+    scales = [L.lora_scale(a, rk, cfg.rslora) for a, rk in zip(r.slot_alpha, r.slot_rank)]
+    hp = L.make_hp(cfg.beta1, cfg.beta2, cfg.eps, cfg.wd, cfg.plus_ratio)
+    step = MultiLoraStep(lins, slot_ranks=r.slot_rank, slot_scales=scales, dtype=cfg.dtype,
+                         tokens=cfg.tokens, seg_start=torch.tensor(r.seg_start, device=device),
+                         seg_slot=torch.tensor(r.seg_slot, device=device), max_norm=cfg.max_norm,
+                         hp=hp, n_streams=streams, device=device)
+    for lin in step.linears:
+        pr = cfg.projs[lin.proj_id]
+        for k, rk in enumerate(r.slot_rank):
+            lin.A[k].copy_(LI.make_a(cfg, 0, pr, rank=rk, tag=f"slot{k}", device=device))
+            lin.B[k].copy_(LI.make_b(cfg, 0, pr, rank=rk, tag=f"slot{k}", device=device))
+    step.prepare_weights()
+    ready = [k for k in range(len(r.slot_rank)) if LI.slot_ready(r, k)]
+    lrs = [cfg.lr] * len(r.slot_rank)
+
+    def run():
+        step.forward_backward(0)
+        step.optimizer_step(ready, r.slot_gbs, lrs, r.slot_step)
+
+    inputs = list(xs.values()) + [lin.dY for lin in step.linears]
+    return step, run, inputs, [step.scale_norm, step.status]
+
+
+# --------------------------------------------------------------------------------- CPU baseline
+def cpu_baseline(cfg: LI.LoraConfig, layers: int, budget_s: float = 20.0):
+    """The oracle, as it stands, on a bounded sample of the workload: whole steps over a subset of
+    the layers (all chunks, all projections), extrapolated to the full layer count."""
+    import numpy as np
+    from oracle import lora_oracle as O
+    s = O.lora_scale(cfg.alpha, cfg.rank, cfg.rslora)
+    hp = O.AdamHP(lr=O.lr_at(cfg.sched, cfg.lr, cfg.opt_step, cfg.warmup, cfg.total, cfg.min_lr),
+                  beta1=cfg.beta1, beta2=cfg.beta2, eps=cfg.eps, wd=cfg.wd,
+                  plus_ratio=cfg.plus_ratio, step=cfg.opt_step)
+    done_layers, elapsed = 0, 0.0
+    tokens = cfg.tokens
+    if cfg.multi or cfg.tokens * max(p.in_dim for p in cfg.projs) > 8192 * 4096:
+        tokens = 512   # large workloads: a token sample, scaled by tokens
+    t_all = time.perf_counter()
+    while done_layers < layers:
+        problems, state = {}, {}
+        for pi, pr in enumerate(cfg.projs):
+            X = LI.make_x(cfg, done_layers, pr, tokens=tokens)
+            A = LI.make_a(cfg, done_layers, pr)
+            B = LI.make_b(cfg, done_layers, pr)
+            problems[pi] = dict(X=X, W=LI.make_w(cfg, done_layers, pr),
+                                dY=LI.make_dy(cfg, done_layers, pr, tokens=tokens),
+                                layer=done_layers, proj=pi)
+            z = lambda a: np.zeros(tuple(a.shape), np.float32)
+            st = O.AdapterState(A.numpy(), B.numpy(), z(A), z(A), z(B), z(B))
+            if cfg.dora:
+                st.mag = LI.dora_magnitude_init(problems[pi]["W"]).numpy()
+                st.mM, st.vM = np.zeros_like(st.mag), np.zeros_like(st.mag)
+            state[pi] = st
+        chunks = cfg.chunks if tokens == cfg.tokens else 1
+        t0 = time.perf_counter()
+        O.run_single_step(problems, state, s=s, chunks=chunks, p=cfg.dropout_p,
+                          seed=cfg.dropout_seed, opt_step=cfg.opt_step, max_norm=cfg.max_norm,
+                          hp=hp, dora=cfg.dora, keep_outputs=False)
+        elapsed += time.perf_counter() - t0
+        done_layers += 1
+        if time.perf_counter() - t_all > budget_s:
+            break
+    per_step = elapsed / done_layers * layers * (cfg.tokens / tokens)
+    cores = len(os.sched_getaffinity(0))
+    return {"value": cfg.tokens / per_step, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": (f"{done_layers} of {layers} layers x {len(cfg.projs)} projections, "
+                       f"{tokens} of {cfg.tokens} tokens, float64 numpy oracle (BLAS threads "
+                       f"= all {cores} cores), whole step per layer, extrapolated linearly"),
+            "seconds": elapsed}
+
+
+# --------------------------------------------------------------------------------- reference arm
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    cfg = LI.CONFIGS[args.config]
+    layers = args.layers or cfg.layers
+    budget = 240.0 / max(1, args.steps + args.warmup)
+    vals = []
+    for i in range(args.warmup + args.steps):
+        r = cpu_baseline(cfg, layers, budget_s=min(budget, 20.0))
+        if i >= args.warmup:
+            vals.append(r)
+    value = statistics.median(v["value"] for v in vals)
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * cfg.tokens / value,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": workload_name(cfg, layers), "tokens_per_step": cfg.tokens},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": vals[0]["cores"],
+                             "kind": "oracle", "sample": vals[0]["sample"]},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_name(cfg, layers):
+    projs = "+".join(f"{p.name}:{p.in_dim}->{p.out_dim}" for p in cfg.projs)
+    extra = []
+    if cfg.multi:
+        extra.append(f"slots ranks {list(cfg.slot_ranks)}")
+    else:
+        extra.append(f"rank {cfg.rank} alpha {cfg.alpha:g}{' rsLoRA' if cfg.rslora else ''}")
+    if cfg.dora:
+        extra.append("DoRA")
+    if cfg.dropout_p:
+        extra.append(f"dropout {cfg.dropout_p}")
+    return (f"{cfg.name}: {layers} layers x [{projs}], {cfg.dtype} frozen W, "
+            f"{', '.join(extra)}, T={cfg.tokens} in {cfg.chunks} chunks")
+
+
+# --------------------------------------------------------------------------------- our arm
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    from bwd_adapter_adamw_gb300 import binding as L
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=device)
+    cfg = LI.CONFIGS[args.config]
+    layers = args.layers or cfg.layers
+    if cfg.multi:
+        step, run, inputs, results = make_multi(cfg, args.streams, device)
+    else:
+        step, run, inputs, results = make_single(cfg, layers, args.streams, device)
+    torch.cuda.synchronize()
+
+    # launches per step (eager), then warm-up
+    c0 = L.lora_launch_counter()
+    run()
+    torch.cuda.synchronize()
+    launches_per_step = L.lora_launch_counter() - c0
+    for _ in range(max(0, args.warmup - 1)):
+        run()
+    torch.cuda.synchronize()
+
+    # dominant kernel: event brackets around every launch of its class inside the timed step
+    prof_class = args.prof_class or L.LORA_PROF_FROZEN_FWD
+    n_prof = (layers if not cfg.multi else 1) * len(cfg.projs)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(n_prof)]
+    stops = [torch.cuda.Event(enable_timing=True) for _ in range(n_prof)]
+    L.lora_profile_arm(prof_class, starts, stops)
+    graph = None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream(device=device)
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(graph, stream=s):
+                run()
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        replay = graph.replay
+    else:
+        replay = run
+    used = L.lora_profile_used()
+    if graph is None:
+        L.lora_profile_arm(0, [], [])   # eager: only the warm-armed launches above were bracketed
+    for _ in range(2):
+        replay()
+    torch.cuda.synchronize()
+
+    # timed region
+    clocks = Clocks(local)
+    clocks.start()
+    time.sleep(0.3)
+    K = args.steps
+    stream = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for _ in range(K):
+        replay()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    ms = ev0.elapsed_time(ev1)
+    # dominant-kernel durations from the last replay
+    kern_ms = [a.elapsed_time(b) for a, b in zip(starts[:used], stops[:used])] if used else []
+    # end-to-end through host buffers: H2D of the step's inputs, the step, D2H of the result
+    pinned = [t.detach().to("cpu").pin_memory() for t in inputs]
+    res_host = [torch.empty(r.shape, dtype=r.dtype, pin_memory=True) for r in results]
+    h2d = sum(t.numel() * t.element_size() for t in pinned)
+    d2h = sum(t.numel() * t.element_size() for t in res_host)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    Ke = max(3, K // 2)
+    torch.cuda.synchronize()
+    t_host0 = time.perf_counter()
+    e0.record(stream)
+    for _ in range(Ke):
+        for dst, src in zip(inputs, pinned):
+            dst.copy_(src, non_blocking=True)
+        replay()
+        for dst, src in zip(res_host, results):
+            dst.copy_(src, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    clk = clocks.stop()
+
+    t = torch.tensor([ms, e2e_ms], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms, e2e_ms = float(t[0]), float(t[1])
+    tokens = cfg.tokens
+    value = world * K * tokens / (ms / 1e3)
+    e2e_value = world * Ke * tokens / (e2e_ms / 1e3)
+
+    if rank == 0:
+        peaks, peak_src = load_peaks()
+        cnt = counts(cfg, layers if not cfg.multi else 1)
+        per_launch = cnt["fwd_flops_per_launch"] if prof_class == L.LORA_PROF_FROZEN_FWD \
+            else cnt["dx_flops_per_launch"]
+        avg_kern = statistics.mean(kern_ms) if kern_ms else None
+        if cfg.dtype == "f32":
+            peak = 152 * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+            bound, punit = "alu", "TFLOP/s"
+            note = ("fp32 FMA peak derived: 152 SMs x 128 FP32 lanes x 2 flop x max SM clock "
+                    f"{peaks.get('sm_max_mhz', 2070.0):.0f} MHz")
+        else:
+            peak = peaks["bf16_tflops"]
+            bound, punit = "tensor", "TFLOP/s"
+            note = f"dense bf16 cuBLAS burst, {peak_src}"
+        achieved = per_launch / (avg_kern / 1e3) / 1e12 if avg_kern else None
+        cpu = None
+        if not args.no_cpu_baseline and world == 1:
+            cpu = cpu_baseline(cfg, layers)
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms / K, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32" if cfg.dtype == "f32" else "bf16", "data": "synthetic",
+            "config": {"workload": workload_name(cfg, layers), "tokens_per_step": tokens,
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "l2": "inputs larger than L2 (frozen W alone exceeds 129 MB)"
+                       if cfg.name != "c1" else "inputs fit in L2",
+                       "cuda_graph": graph is not None, "streams": args.streams},
+            "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": punit,
+                         "frac": (achieved / peak) if achieved else None, "traffic": None,
+                         "kernel": {1: "frozen forward GEMM", 2: "frozen dX GEMM"}.get(
+                             prof_class, f"class {prof_class}"),
+                         "launches_timed": len(kern_ms), "avg_launch_ms": avg_kern,
+                         "peak_source": note},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches_per_step * K,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,301 @@
+"""ctypes binding of liblora_gb300.so: argument marshalling only.
+
+Every function here has the name of the C entry point it calls, converts torch tensors to device
+pointers and Python values to the C structs, and raises LoraError on a nonzero status. All
+computation happens in the library's kernels; there is no fallback of any kind. If the library
+is missing the import fails loudly.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from typing import Optional, Sequence
+
+PKG_DIR = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG_DIR, "liblora_gb300.so")
+
+LORA_OK = 0
+LORA_ERR_INVALID = 1
+LORA_ERR_ALIGN = 2
+LORA_ERR_UNSUPPORTED = 3
+LORA_ERR_WORKSPACE = 4
+LORA_ERR_CUDA = 5
+LORA_ERR_NONFINITE = 6
+
+LORA_F32 = 0
+LORA_BF16 = 1
+LORA_SCHED_CONSTANT = 0
+LORA_SCHED_WARMUP_COSINE = 1
+LORA_MAX_RANK = 64
+LORA_MAX_SLOTS = 32
+LORA_MAX_GROUPS = 64
+
+
+class LoraError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+class lora_desc(C.Structure):
+    _fields_ = [("in_dim", C.c_int64), ("out_dim", C.c_int64), ("rank", C.c_int32),
+                ("scale", C.c_float), ("dtype", C.c_int32), ("dropout_p", C.c_float),
+                ("seed", C.c_uint64), ("layer_id", C.c_uint32), ("proj_id", C.c_uint32),
+                ("dora", C.c_int32)]
+
+
+class lora_ctx(C.Structure):
+    _fields_ = [("opt_step", C.c_uint64), ("accum_ordinal", C.c_uint32),
+                ("chunk_tokens", C.c_int64)]
+
+
+class lora_slot(C.Structure):
+    _fields_ = [("A", C.c_void_p), ("B", C.c_void_p), ("dA", C.c_void_p), ("dB", C.c_void_p),
+                ("rank", C.c_int32), ("scale", C.c_float)]
+
+
+class lora_group(C.Structure):
+    _fields_ = [("offset", C.c_int64), ("n_a", C.c_int64), ("n_b", C.c_int64),
+                ("n_mag", C.c_int64), ("grad_scale", C.c_double), ("max_norm", C.c_float),
+                ("lr", C.c_float), ("step", C.c_int64)]
+
+
+class lora_adamw_hp(C.Structure):
+    _fields_ = [("beta1", C.c_float), ("beta2", C.c_float), ("eps", C.c_float),
+                ("weight_decay", C.c_float), ("plus_ratio", C.c_float)]
+
+
+def _load() -> C.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is not built; run bwd_adapter_adamw_gb300.build.build() (nvcc, sm_103a)")
+    lib = C.CDLL(LIB_PATH)
+    P, I32, I64, U64, SZ, F, D = (C.c_void_p, C.c_int32, C.c_int64, C.c_uint64, C.c_size_t,
+                                  C.c_float, C.c_double)
+    DP, CP = C.POINTER(lora_desc), C.POINTER(lora_ctx)
+    sig = {
+        "lora_status_string": (C.c_char_p, [C.c_int]),
+        "lora_scale": (F, [F, I32, I32]),
+        "lora_lr_at": (D, [I32, D, U64, U64, U64, D]),
+        "lora_workspace_size": (SZ, [DP, I64]),
+        "lora_prepare_weight": (C.c_int, [DP, P, P, P]),
+        "lora_dora_norm": (C.c_int, [DP, P, P, P, P, P]),
+        "lora_forward": (C.c_int, [DP, CP, I64, P, P, P, P, P, P, P, P, P, SZ, P]),
+        "lora_backward": (C.c_int, [DP, CP, I64, P, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P]),
+        "lora_grad_prepare_workspace_size": (SZ, [I32, C.POINTER(lora_group)]),
+        "lora_grad_prepare": (C.c_int, [P, I32, C.POINTER(lora_group), P, P, P, SZ, P]),
+        "lora_adamw_step": (C.c_int, [P, P, P, P, I32, C.POINTER(lora_group),
+                                      C.POINTER(lora_adamw_hp), P, P, I32, P]),
+        "multi_lora_workspace_size": (SZ, [DP, I64, I32, I32, C.POINTER(lora_slot)]),
+        "multi_lora_forward": (C.c_int, [DP, CP, I64, P, P, I32, P, P, I32, C.POINTER(lora_slot),
+                                         P, P, P, SZ, P]),
+        "multi_lora_backward": (C.c_int, [DP, CP, I64, P, P, I32, P, P, I32,
+                                          C.POINTER(lora_slot), P, P, P, P, SZ, P]),
+        "lora_dropout_mask": (C.c_int, [DP, CP, I64, P, P]),
+        "multi_lora_token_slots": (C.c_int, [I64, I32, P, P, I32, P, P]),
+        "lora_profile_arm": (C.c_int, [I32, C.POINTER(C.c_void_p), C.POINTER(C.c_void_p), I32]),
+        "lora_profile_used": (I32, []),
+        "lora_launch_counter": (U64, []),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+_lib = _load()
+EXPORTED = ("lora_status_string", "lora_scale", "lora_lr_at", "lora_workspace_size",
+            "lora_prepare_weight", "lora_dora_norm", "lora_forward", "lora_backward",
+            "lora_grad_prepare_workspace_size", "lora_grad_prepare", "lora_adamw_step",
+            "multi_lora_workspace_size", "multi_lora_forward", "multi_lora_backward",
+            "lora_dropout_mask", "multi_lora_token_slots", "lora_profile_arm",
+            "lora_profile_used", "lora_launch_counter")
+
+LORA_PROF_NONE = 0
+LORA_PROF_FROZEN_FWD = 1
+LORA_PROF_FROZEN_DX = 2
+LORA_PROF_SHRINK = 3
+LORA_PROF_G = 4
+LORA_PROF_RED_DB = 5
+LORA_PROF_RED_DA = 6
+LORA_PROF_PREPARE = 7
+LORA_PROF_ADAMW = 8
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+# ------------------------------------------------------------------------------------ marshalling
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int, where: str) -> int:
+    if status != LORA_OK:
+        raise LoraError(status, where)
+    return status
+
+
+def status_string(status: int) -> str:
+    return _lib.lora_status_string(status).decode()
+
+
+def make_desc(in_dim, out_dim, rank, scale, dtype, dropout_p=0.0, seed=0, layer_id=0, proj_id=0,
+              dora=False) -> lora_desc:
+    return lora_desc(in_dim, out_dim, rank, scale, dtype, dropout_p, seed, layer_id, proj_id,
+                     1 if dora else 0)
+
+
+def make_ctx(opt_step=0, accum_ordinal=0, chunk_tokens=0) -> lora_ctx:
+    return lora_ctx(opt_step, accum_ordinal, chunk_tokens)
+
+
+def lora_scale(alpha: float, rank: int, rslora: bool) -> float:
+    return _lib.lora_scale(alpha, rank, 1 if rslora else 0)
+
+
+def lora_lr_at(kind: int, base: float, step: int, warmup: int, total: int, min_lr: float) -> float:
+    return _lib.lora_lr_at(kind, base, step, warmup, total, min_lr)
+
+
+def lora_workspace_size(d: lora_desc, T: int) -> int:
+    return _lib.lora_workspace_size(C.byref(d), T)
+
+
+def lora_prepare_weight(d: lora_desc, W, W_t, stream=None):
+    return _check(_lib.lora_prepare_weight(C.byref(d), _ptr(W), _ptr(W_t), _stream(stream)),
+                  "lora_prepare_weight")
+
+
+def lora_dora_norm(d: lora_desc, W, A, B, norm_out, stream=None):
+    return _check(_lib.lora_dora_norm(C.byref(d), _ptr(W), _ptr(A), _ptr(B), _ptr(norm_out),
+                                      _stream(stream)), "lora_dora_norm")
+
+
+def lora_forward(d: lora_desc, c: Optional[lora_ctx], T: int, X, W, A, B, dora_m, dora_n, Y,
+                 H_save, ws, ws_bytes: Optional[int] = None, stream=None, check=True):
+    nbytes = ws_bytes if ws_bytes is not None else ws.numel() * ws.element_size()
+    st = _lib.lora_forward(C.byref(d), C.byref(c) if c is not None else None, T, _ptr(X), _ptr(W),
+                           _ptr(A), _ptr(B), _ptr(dora_m), _ptr(dora_n), _ptr(Y), _ptr(H_save),
+                           _ptr(ws), nbytes, _stream(stream))
+    return _check(st, "lora_forward") if check else st
+
+
+def lora_backward(d: lora_desc, c: Optional[lora_ctx], T: int, X, W_t, A, B, dY, H_save, dora_m,
+                  dora_n, Y_save, dX, dA, dB, dm, ws, ws_bytes: Optional[int] = None, stream=None,
+                  check=True):
+    nbytes = ws_bytes if ws_bytes is not None else ws.numel() * ws.element_size()
+    st = _lib.lora_backward(C.byref(d), C.byref(c) if c is not None else None, T, _ptr(X),
+                            _ptr(W_t), _ptr(A), _ptr(B), _ptr(dY), _ptr(H_save), _ptr(dora_m),
+                            _ptr(dora_n), _ptr(Y_save), _ptr(dX), _ptr(dA), _ptr(dB), _ptr(dm),
+                            _ptr(ws), nbytes, _stream(stream))
+    return _check(st, "lora_backward") if check else st
+
+
+def make_groups(groups: Sequence[dict]):
+    arr = (lora_group * len(groups))()
+    for i, g in enumerate(groups):
+        arr[i] = lora_group(g["offset"], g.get("n_a", 0), g.get("n_b", 0), g.get("n_mag", 0),
+                            g["grad_scale"], g.get("max_norm", 0.0), g.get("lr", 0.0),
+                            g.get("step", 0))
+    return arr
+
+
+def lora_grad_prepare_workspace_size(groups) -> int:
+    return _lib.lora_grad_prepare_workspace_size(len(groups), groups)
+
+
+def lora_grad_prepare(grads, groups, d_scale_norm, d_status, ws, ws_bytes=None, stream=None,
+                      check=True):
+    nbytes = ws_bytes if ws_bytes is not None else ws.numel() * ws.element_size()
+    st = _lib.lora_grad_prepare(_ptr(grads), len(groups), groups, _ptr(d_scale_norm),
+                                _ptr(d_status), _ptr(ws), nbytes, _stream(stream))
+    return _check(st, "lora_grad_prepare") if check else st
+
+
+def make_hp(beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01, plus_ratio=1.0) -> lora_adamw_hp:
+    return lora_adamw_hp(beta1, beta2, eps, weight_decay, plus_ratio)
+
+
+def lora_adamw_step(params, grads, m, v, groups, hp: lora_adamw_hp, d_scale_norm, d_status,
+                    zero_grads=False, stream=None, check=True):
+    st = _lib.lora_adamw_step(_ptr(params), _ptr(grads), _ptr(m), _ptr(v), len(groups), groups,
+                              C.byref(hp), _ptr(d_scale_norm), _ptr(d_status),
+                              1 if zero_grads else 0, _stream(stream))
+    return _check(st, "lora_adamw_step") if check else st
+
+
+def make_slots(slots: Sequence[dict]):
+    arr = (lora_slot * len(slots))()
+    for i, s in enumerate(slots):
+        arr[i] = lora_slot(_ptr(s["A"]), _ptr(s["B"]), _ptr(s.get("dA")), _ptr(s.get("dB")),
+                           s["rank"], s["scale"])
+    return arr
+
+
+def multi_lora_workspace_size(d: lora_desc, T: int, n_seg: int, slots) -> int:
+    return _lib.multi_lora_workspace_size(C.byref(d), T, n_seg, len(slots), slots)
+
+
+def multi_lora_forward(d, c, T, X, W, n_seg, seg_start, seg_slot, slots, Y, H_save, ws,
+                       ws_bytes=None, stream=None, check=True):
+    nbytes = ws_bytes if ws_bytes is not None else ws.numel() * ws.element_size()
+    st = _lib.multi_lora_forward(C.byref(d), C.byref(c) if c is not None else None, T, _ptr(X),
+                                 _ptr(W), n_seg, _ptr(seg_start), _ptr(seg_slot), len(slots),
+                                 slots, _ptr(Y), _ptr(H_save), _ptr(ws), nbytes, _stream(stream))
+    return _check(st, "multi_lora_forward") if check else st
+
+
+def multi_lora_backward(d, c, T, X, W_t, n_seg, seg_start, seg_slot, slots, dY, H_save, dX, ws,
+                        ws_bytes=None, stream=None, check=True):
+    nbytes = ws_bytes if ws_bytes is not None else ws.numel() * ws.element_size()
+    st = _lib.multi_lora_backward(C.byref(d), C.byref(c) if c is not None else None, T, _ptr(X),
+                                  _ptr(W_t), n_seg, _ptr(seg_start), _ptr(seg_slot), len(slots),
+                                  slots, _ptr(dY), _ptr(H_save), _ptr(dX), _ptr(ws), nbytes,
+                                  _stream(stream))
+    return _check(st, "multi_lora_backward") if check else st
+
+
+def lora_dropout_mask(d: lora_desc, c: Optional[lora_ctx], T: int, mask, stream=None, check=True):
+    st = _lib.lora_dropout_mask(C.byref(d), C.byref(c) if c is not None else None, T, _ptr(mask),
+                                _stream(stream))
+    return _check(st, "lora_dropout_mask") if check else st
+
+
+def multi_lora_token_slots(T, n_seg, seg_start, seg_slot, n_slots, token_slot, stream=None,
+                           check=True):
+    st = _lib.multi_lora_token_slots(T, n_seg, _ptr(seg_start), _ptr(seg_slot), n_slots,
+                                     _ptr(token_slot), _stream(stream))
+    return _check(st, "multi_lora_token_slots") if check else st
+
+
+def lora_profile_arm(kernel_class: int, start_events: Sequence, stop_events: Sequence):
+    """Bracket the next len(start_events) launches of one kernel class with torch.cuda.Event
+    pairs (recorded on the launching stream)."""
+    n = len(start_events)
+    starts = (C.c_void_p * max(n, 1))(*[e.cuda_event for e in start_events])
+    stops = (C.c_void_p * max(n, 1))(*[e.cuda_event for e in stop_events])
+    return _check(_lib.lora_profile_arm(kernel_class, starts, stops, n), "lora_profile_arm")
+
+
+def lora_profile_used() -> int:
+    return _lib.lora_profile_used()
+
+
+def lora_launch_counter() -> int:
+    return _lib.lora_launch_counter()

@@ -1,0 +1,576 @@
+// C-ABI entry points: argument validation on the host, workspace carving, kernel orchestration.
+// Every entry point validates everything before enqueueing anything, so a nonzero status means
+// nothing was launched (except LORA_ERR_CUDA, which reports a failed launch).
+#include <cmath>
+#include <cstring>
+
+#include "lora_kernels.h"
+
+using namespace lora;
+
+namespace {
+
+constexpr size_t kWsAlign = 256;
+
+struct Carve {
+  char* base;
+  size_t off = 0;
+  explicit Carve(void* b) : base(static_cast<char*>(b)) {}
+  template <typename T>
+  T* take(size_t count) {
+    off = (off + kWsAlign - 1) / kWsAlign * kWsAlign;
+    T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+    off += count * sizeof(T);
+    return p;
+  }
+};
+
+inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? LORA_OK : LORA_ERR_CUDA; }
+
+#define LORA_TRY(expr)                         \
+  do {                                         \
+    cudaError_t _e = (expr);                   \
+    if (_e != cudaSuccess) return LORA_ERR_CUDA; \
+  } while (0)
+
+int64_t max_gemm_items(int64_t T, int32_t n_seg) {
+  if (n_seg < 1) n_seg = 1;
+  return (T + kGemmTileT - 1) / kGemmTileT + 2 * (int64_t)n_seg + 2;
+}
+int64_t max_red_items(int64_t T, int32_t n_seg) {
+  if (n_seg < 1) n_seg = 1;
+  return (T + kRedTileT - 1) / kRedTileT + (int64_t)n_seg + 1;
+}
+
+// Shape/dtype checks shared by every per-linear call.
+int check_desc(const lora_desc* d, int64_t T, bool multi) {
+  if (!d || T < 0) return LORA_ERR_INVALID;
+  if (d->in_dim <= 0 || d->out_dim <= 0) return LORA_ERR_INVALID;
+  if (d->dtype != LORA_F32 && d->dtype != LORA_BF16) return LORA_ERR_INVALID;
+  if (d->rank <= 0) return LORA_ERR_INVALID;
+  if (d->rank > LORA_MAX_RANK || (d->rank % 4) != 0) return LORA_ERR_UNSUPPORTED;
+  if ((d->in_dim % 8) != 0 || (d->out_dim % 8) != 0) return LORA_ERR_ALIGN;
+  if (!(d->dropout_p >= 0.f && d->dropout_p < 1.f)) return LORA_ERR_INVALID;
+  if (d->proj_id > 0xFFFFu) return LORA_ERR_INVALID;
+  if (d->dora != 0 && d->dora != 1) return LORA_ERR_INVALID;
+  if (multi && d->dora) return LORA_ERR_UNSUPPORTED;
+  if (!multi && !std::isfinite(d->scale)) return LORA_ERR_INVALID;
+  if (T >= (int64_t(1) << 31) - kRedTileT) return LORA_ERR_UNSUPPORTED;
+  return LORA_OK;
+}
+
+// Host side of the dropout hash: per-chunk keys of this call ("4.3. Training Guide", Dropout).
+int build_drop(const lora_desc* d, const lora_ctx* c, int64_t T, DropParams& dp) {
+  std::memset(&dp, 0, sizeof(dp));
+  const lora_ctx zero{0, 0, 0};
+  if (!c) c = &zero;
+  if (c->chunk_tokens < 0) return LORA_ERR_INVALID;
+  dp.in_dim = d->in_dim;
+  dp.chunk_tokens = c->chunk_tokens > 0 ? c->chunk_tokens : (T > 0 ? T : 1);
+  const int64_t n_chunks = T > 0 ? (T + dp.chunk_tokens - 1) / dp.chunk_tokens : 0;
+  if (n_chunks > LORA_MAX_CHUNKS_PER_CALL) return LORA_ERR_UNSUPPORTED;
+  if ((int64_t)c->accum_ordinal + n_chunks > 65536) return LORA_ERR_INVALID;
+  if (d->dropout_p <= 0.f) {
+    dp.enabled = 0;
+    dp.tau = 0;
+    return LORA_OK;
+  }
+  dp.enabled = 1;
+  const double t = std::floor((double)d->dropout_p * 4294967296.0);
+  dp.tau = t >= 4294967295.0 ? 0xFFFFFFFFu : (uint32_t)t;
+  const uint64_t k1 = mix64(mix64(d->seed ^ 0x9E3779B97F4A7C15ull) ^ c->opt_step);
+  for (int64_t i = 0; i < n_chunks; ++i) {
+    const uint64_t ord = (uint64_t)(c->accum_ordinal + i) & 0xFFFFull;
+    const uint64_t packed = (ord << 48) | ((uint64_t)d->layer_id << 16) | (uint64_t)d->proj_id;
+    dp.keys[i] = mix64(k1 ^ packed);
+  }
+  return LORA_OK;
+}
+
+float dropout_q(const lora_desc* d) {
+  return d->dropout_p > 0.f ? (float)(1.0 / (1.0 - (double)d->dropout_p)) : 1.f;
+}
+
+// Slot view shared by single-adapter and multi-adapter calls.
+struct Slots {
+  int n = 0;
+  const float* A[LORA_MAX_SLOTS];
+  const float* B[LORA_MAX_SLOTS];
+  float* dA[LORA_MAX_SLOTS];
+  float* dB[LORA_MAX_SLOTS];
+  int32_t rank[LORA_MAX_SLOTS];
+  float scale[LORA_MAX_SLOTS];
+  int64_t rank_sum = 0;
+};
+
+int slots_from_table(const lora_desc* d, int32_t n_slots, const lora_slot* tab, bool need_grads,
+                     Slots& s) {
+  if (!tab || n_slots < 1) return LORA_ERR_INVALID;
+  if (n_slots > LORA_MAX_SLOTS) return LORA_ERR_UNSUPPORTED;
+  s.n = n_slots;
+  s.rank_sum = 0;
+  for (int k = 0; k < n_slots; ++k) {
+    const lora_slot& e = tab[k];
+    if (!e.A || !e.B) return LORA_ERR_INVALID;
+    if (need_grads && (!e.dA || !e.dB)) return LORA_ERR_INVALID;
+    if (e.rank <= 0 || e.rank > d->rank) return LORA_ERR_INVALID;
+    if (e.rank % 4) return LORA_ERR_UNSUPPORTED;
+    if (!std::isfinite(e.scale)) return LORA_ERR_INVALID;
+    if (!al16(e.A) || !al16(e.B) || (need_grads && (!al16(e.dA) || !al16(e.dB))))
+      return LORA_ERR_ALIGN;
+    s.A[k] = e.A; s.B[k] = e.B; s.dA[k] = e.dA; s.dB[k] = e.dB;
+    s.rank[k] = e.rank; s.scale[k] = e.scale;
+    s.rank_sum += e.rank;
+  }
+  return LORA_OK;
+}
+
+void single_slot(const lora_desc* d, const float* A, const float* B, float* dA, float* dB, Slots& s) {
+  s.n = 1;
+  s.A[0] = A; s.B[0] = B; s.dA[0] = dA; s.dB[0] = dB;
+  s.rank[0] = d->rank; s.scale[0] = d->scale;
+  s.rank_sum = d->rank;
+}
+
+struct Layout {
+  TokenItem* gitems; int32_t* gcount;
+  TokenItem* ritems; int32_t* rcount;
+  int64_t gmax, rmax;
+  float* ratio;        // [out] DoRA m / n
+  float* Gs;           // [T, rmax]
+  float* At;           // per slot [in, r_s]
+  float* Bt;           // per slot [r_s, out]
+  float* partB;        // [rmax_items][out][rank]
+  float* partA;        // [rmax_items][in][rank]
+  size_t bytes;
+};
+
+Layout carve(const lora_desc* d, int64_t T, int32_t n_seg, int64_t rank_sum, bool backward, void* ws) {
+  Layout L{};
+  Carve c(ws);
+  L.gmax = max_gemm_items(T, n_seg);
+  L.rmax = max_red_items(T, n_seg);
+  L.gitems = c.take<TokenItem>((size_t)L.gmax);
+  L.gcount = c.take<int32_t>(4);
+  L.ritems = c.take<TokenItem>((size_t)L.rmax);
+  L.rcount = c.take<int32_t>(4);
+  L.ratio = c.take<float>((size_t)d->out_dim);
+  if (backward) {
+    L.Gs = c.take<float>((size_t)T * d->rank);
+    L.At = c.take<float>((size_t)rank_sum * d->in_dim);
+    L.Bt = c.take<float>((size_t)rank_sum * d->out_dim);
+    L.partB = c.take<float>((size_t)L.rmax * d->out_dim * d->rank);
+    L.partA = c.take<float>((size_t)L.rmax * d->in_dim * d->rank);
+  }
+  L.bytes = c.off + kWsAlign;
+  return L;
+}
+
+size_t ws_size(const lora_desc* d, int64_t T, int32_t n_seg, int64_t rank_sum) {
+  return carve(d, T, n_seg, rank_sum, true, nullptr).bytes;
+}
+
+// forward: shrink then the frozen product with the up-projection as extra K-steps
+int run_forward(const lora_desc* d, const DropParams& dp, int64_t T, const void* X, const void* W,
+                int32_t n_seg, const int32_t* seg_start, const int32_t* seg_slot, const Slots& s,
+                const float* ratio_src_m, const float* ratio_src_n, void* Y, float* H, void* ws,
+                cudaStream_t st) {
+  Layout L = carve(d, T, n_seg, s.rank_sum, false, ws);
+  LORA_TRY(launch_make_items(T, n_seg, seg_start, seg_slot, s.n, L.gitems, L.gcount, (int32_t)L.gmax,
+                             L.ritems, L.rcount, (int32_t)L.rmax, st));
+  const float q = dropout_q(d);
+  const float* ratio = nullptr;
+  if (ratio_src_m) {
+    LORA_TRY(launch_ratio(ratio_src_m, ratio_src_n, d->out_dim, L.ratio, st));
+    ratio = L.ratio;
+  }
+  // shrink: Hs[t, j] = s_k q sum_i M[t,i] X[t,i] A_k[j,i]   (columns j >= r_k written as 0)
+  {
+    TokGemmArgs a{};
+    a.items = L.gitems; a.n_items = L.gcount;
+    a.a = X; a.lda = d->in_dim; a.K = d->in_dim; a.a_mask = dp.enabled;
+    a.b_per_slot = 1;
+    for (int k = 0; k < s.n; ++k) {
+      a.bslot.p[k] = s.A[k]; a.bslot.ld[k] = d->in_dim; a.bslot.rank[k] = s.rank[k];
+      a.bslot.alpha[k] = s.scale[k] * q;
+    }
+    a.alpha_per_slot = 1;
+    a.out = H; a.ldo = d->rank; a.n_out = d->rank;
+    a.drop = dp;
+    LORA_TRY(launch_tok_gemm(d->dtype, LORA_F32, LORA_F32, 64, a, (int)L.gmax, st, LORA_PROF_SHRINK));
+  }
+  // frozen product + Hs B_k^T, times m/n per column in DoRA mode
+  {
+    TokGemmArgs a{};
+    a.items = L.gitems; a.n_items = L.gcount;
+    a.a = X; a.lda = d->in_dim; a.K = d->in_dim;
+    a.b = W; a.ldb = d->in_dim; a.n_rows = d->out_dim;
+    a.lora_phase = 1; a.lp = H; a.ldlp = d->rank;
+    for (int k = 0; k < s.n; ++k) {
+      a.lq.p[k] = s.B[k]; a.lq.ld[k] = s.rank[k]; a.lq.rank[k] = s.rank[k];
+    }
+    a.alpha = 1.f;
+    a.n_colscale = ratio;
+    a.out = Y; a.ldo = d->out_dim; a.n_out = d->out_dim;
+    a.drop = dp;
+    LORA_TRY(launch_tok_gemm(d->dtype, d->dtype, d->dtype, 128, a, (int)L.gmax, st, LORA_PROF_FROZEN_FWD));
+  }
+  return LORA_OK;
+}
+
+int run_backward(const lora_desc* d, const DropParams& dp, int64_t T, const void* X, const void* Wt,
+                 int32_t n_seg, const int32_t* seg_start, const int32_t* seg_slot, const Slots& s,
+                 const void* dY, const float* H, const float* dora_m, const float* dora_n,
+                 const void* Y_save, void* dX, float* dm, void* ws, cudaStream_t st) {
+  Layout L = carve(d, T, n_seg, s.rank_sum, true, ws);
+  LORA_TRY(launch_make_items(T, n_seg, seg_start, seg_slot, s.n, L.gitems, L.gcount, (int32_t)L.gmax,
+                             L.ritems, L.rcount, (int32_t)L.rmax, st));
+  const float q = dropout_q(d);
+  // transposed adapters: At_k = A_k^T [in, r_k], Bt_k = B_k^T [r_k, out]
+  float* At[LORA_MAX_SLOTS];
+  float* Bt[LORA_MAX_SLOTS];
+  {
+    TransposeTab ta{}, tb{};
+    int64_t oa = 0, ob = 0;
+    for (int k = 0; k < s.n; ++k) {
+      At[k] = L.At + oa; oa += (int64_t)s.rank[k] * d->in_dim;
+      Bt[k] = L.Bt + ob; ob += (int64_t)s.rank[k] * d->out_dim;
+      ta.src[k] = s.A[k]; ta.dst[k] = At[k]; ta.rows[k] = s.rank[k]; ta.cols[k] = d->in_dim;
+      tb.src[k] = s.B[k]; tb.dst[k] = Bt[k]; tb.rows[k] = d->out_dim; tb.cols[k] = s.rank[k];
+    }
+    LORA_TRY(launch_transpose_slots(ta, s.n, d->rank, d->in_dim, st));
+    LORA_TRY(launch_transpose_slots(tb, s.n, d->out_dim, d->rank, st));
+  }
+  const float* ratio = nullptr;
+  if (dora_m) {
+    LORA_TRY(launch_ratio(dora_m, dora_n, d->out_dim, L.ratio, st));
+    ratio = L.ratio;
+  }
+  // Gs[t, j] = s_k q sum_o dY'[t, o] B_k[o, j]
+  {
+    TokGemmArgs a{};
+    a.items = L.gitems; a.n_items = L.gcount;
+    a.a = dY; a.lda = d->out_dim; a.K = d->out_dim; a.a_colscale = ratio;
+    a.b_per_slot = 1;
+    for (int k = 0; k < s.n; ++k) {
+      a.bslot.p[k] = Bt[k]; a.bslot.ld[k] = d->out_dim; a.bslot.rank[k] = s.rank[k];
+      a.bslot.alpha[k] = s.scale[k] * q;
+    }
+    a.alpha_per_slot = 1;
+    a.out = L.Gs; a.ldo = d->rank; a.n_out = d->rank;
+    a.drop = dp;
+    LORA_TRY(launch_tok_gemm(d->dtype, LORA_F32, LORA_F32, 64, a, (int)L.gmax, st, LORA_PROF_G));
+  }
+  // dX = dY' W + (Gs A_k) * M
+  if (dX) {
+    TokGemmArgs a{};
+    a.items = L.gitems; a.n_items = L.gcount;
+    a.a = dY; a.lda = d->out_dim; a.K = d->out_dim; a.a_colscale = ratio;
+    a.b = Wt; a.ldb = d->out_dim; a.n_rows = d->in_dim;
+    a.lora_phase = 1; a.lp = L.Gs; a.ldlp = d->rank;
+    for (int k = 0; k < s.n; ++k) {
+      a.lq.p[k] = At[k]; a.lq.ld[k] = s.rank[k]; a.lq.rank[k] = s.rank[k];
+    }
+    a.mask_after_lora = dp.enabled;
+    a.alpha = 1.f;
+    a.out = dX; a.ldo = d->in_dim; a.n_out = d->in_dim;
+    a.drop = dp;
+    LORA_TRY(launch_tok_gemm(d->dtype, d->dtype, d->dtype, 128, a, (int)L.gmax, st, LORA_PROF_FROZEN_DX));
+  }
+  ReduceTab rt{};
+  for (int k = 0; k < s.n; ++k) rt.rank[k] = s.rank[k];
+  // dB_k += sum_t dY'[t, o] Hs[t, j]
+  {
+    RedGemmArgs a{};
+    a.items = L.ritems; a.n_items = L.rcount;
+    a.a = dY; a.lda = d->out_dim; a.M = d->out_dim; a.a_colscale = ratio;
+    a.b = H; a.ldb = d->rank;
+    for (int k = 0; k < s.n; ++k) a.rank[k] = s.rank[k];
+    a.part = L.partB; a.ldp = d->rank;
+    a.drop = dp;
+    LORA_TRY(launch_red_gemm(d->dtype, a, (int)L.rmax, st, LORA_PROF_RED_DB));
+    for (int k = 0; k < s.n; ++k) rt.out[k] = s.dB[k];
+    LORA_TRY(launch_reduce_parts(L.partB, L.ritems, L.rcount, (int)L.rmax, d->out_dim, d->rank, 0,
+                                 rt, s.n, st));
+  }
+  // dA_k += sum_t Gs[t, j] M[t, i] X[t, i]   (computed as dA^T partials)
+  {
+    RedGemmArgs a{};
+    a.items = L.ritems; a.n_items = L.rcount;
+    a.a = X; a.lda = d->in_dim; a.M = d->in_dim; a.a_mask = dp.enabled;
+    a.b = L.Gs; a.ldb = d->rank;
+    for (int k = 0; k < s.n; ++k) a.rank[k] = s.rank[k];
+    a.part = L.partA; a.ldp = d->rank;
+    a.drop = dp;
+    LORA_TRY(launch_red_gemm(d->dtype, a, (int)L.rmax, st, LORA_PROF_RED_DA));
+    for (int k = 0; k < s.n; ++k) rt.out[k] = s.dA[k];
+    LORA_TRY(launch_reduce_parts(L.partA, L.ritems, L.rcount, (int)L.rmax, d->in_dim, d->rank, 1,
+                                 rt, s.n, st));
+  }
+  if (dm) LORA_TRY(launch_dora_dm(d->dtype, dY, Y_save, dora_m, T, d->out_dim, dm, st));
+  return LORA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* lora_status_string(int status) {
+  switch (status) {
+    case LORA_OK: return "ok";
+    case LORA_ERR_INVALID: return "invalid argument";
+    case LORA_ERR_ALIGN: return "pointer or row stride not 16-byte aligned";
+    case LORA_ERR_UNSUPPORTED: return "unsupported dtype, rank or size";
+    case LORA_ERR_WORKSPACE: return "workspace too small";
+    case LORA_ERR_CUDA: return "CUDA launch or runtime error";
+    case LORA_ERR_NONFINITE: return "non-finite gradient: update rejected";
+    default: return "unknown status";
+  }
+}
+
+float lora_scale(float alpha, int32_t rank, int32_t rslora) {
+  if (rank <= 0) return 0.f;
+  return rslora ? (float)((double)alpha / std::sqrt((double)rank)) : (float)((double)alpha / rank);
+}
+
+double lora_lr_at(int32_t kind, double base, uint64_t step, uint64_t warmup, uint64_t total,
+                  double min_lr) {
+  if (kind == LORA_SCHED_CONSTANT) return base;
+  if (kind != LORA_SCHED_WARMUP_COSINE) return std::nan("");
+  if (step < warmup) return base * (double)(step + 1) / (double)warmup;
+  if (total <= warmup) return min_lr;
+  double progress = (double)(step - warmup) / (double)(total - warmup);
+  if (progress > 1.0) progress = 1.0;
+  return min_lr + 0.5 * (base - min_lr) * (1.0 + std::cos(M_PI * progress));
+}
+
+size_t lora_workspace_size(const lora_desc* d, int64_t T) {
+  if (check_desc(d, T, false) != LORA_OK) return 0;
+  return ws_size(d, T, -1, d->rank);
+}
+
+size_t multi_lora_workspace_size(const lora_desc* d, int64_t T, int32_t n_seg, int32_t n_slots,
+                                 const lora_slot* slots) {
+  if (check_desc(d, T, true) != LORA_OK || n_seg < 0) return 0;
+  Slots s;
+  if (slots_from_table(d, n_slots, slots, false, s) != LORA_OK) return 0;
+  return ws_size(d, T, n_seg, s.rank_sum);
+}
+
+int lora_prepare_weight(const lora_desc* d, const void* W, void* W_t, void* stream) {
+  int rc = check_desc(d, 0, false);
+  if (rc) return rc;
+  if (!W || !W_t) return LORA_ERR_INVALID;
+  if (!al16(W) || !al16(W_t)) return LORA_ERR_ALIGN;
+  return cuda_status(launch_transpose_weight(d->dtype, W, W_t, d->out_dim, d->in_dim,
+                                             (cudaStream_t)stream));
+}
+
+int lora_dora_norm(const lora_desc* d, const void* W, const float* A, const float* B,
+                   float* norm_out, void* stream) {
+  int rc = check_desc(d, 0, false);
+  if (rc) return rc;
+  if (!W || !A || !B || !norm_out) return LORA_ERR_INVALID;
+  if (!al16(W) || !al16(A) || !al16(B) || !al16(norm_out)) return LORA_ERR_ALIGN;
+  return cuda_status(launch_dora_norm(d->dtype, W, A, B, d->scale, d->out_dim, d->in_dim, d->rank,
+                                      norm_out, (cudaStream_t)stream));
+}
+
+int lora_forward(const lora_desc* d, const lora_ctx* c, int64_t T, const void* X, const void* W,
+                 const float* A, const float* B, const float* dora_m, const float* dora_n,
+                 void* Y, float* H_save, void* ws, size_t ws_bytes, void* stream) {
+  int rc = check_desc(d, T, false);
+  if (rc) return rc;
+  DropParams dp;
+  if ((rc = build_drop(d, c, T, dp))) return rc;
+  if (!X || !W || !A || !B || !Y || !H_save || !ws) return LORA_ERR_INVALID;
+  if (d->dora && (!dora_m || !dora_n)) return LORA_ERR_INVALID;
+  if (!al16(X) || !al16(W) || !al16(A) || !al16(B) || !al16(Y) || !al16(H_save) || !al16(ws))
+    return LORA_ERR_ALIGN;
+  if (d->dora && (!al16(dora_m) || !al16(dora_n))) return LORA_ERR_ALIGN;
+  if (ws_bytes < ws_size(d, T, -1, d->rank)) return LORA_ERR_WORKSPACE;
+  if (T == 0) return LORA_OK;
+  Slots s;
+  single_slot(d, A, B, nullptr, nullptr, s);
+  return run_forward(d, dp, T, X, W, -1, nullptr, nullptr, s, d->dora ? dora_m : nullptr,
+                     d->dora ? dora_n : nullptr, Y, H_save, ws, (cudaStream_t)stream);
+}
+
+int lora_backward(const lora_desc* d, const lora_ctx* c, int64_t T, const void* X,
+                  const void* W_t, const float* A, const float* B, const void* dY,
+                  const float* H_save, const float* dora_m, const float* dora_n,
+                  const void* Y_save, void* dX, float* dA, float* dB, float* dm, void* ws,
+                  size_t ws_bytes, void* stream) {
+  int rc = check_desc(d, T, false);
+  if (rc) return rc;
+  DropParams dp;
+  if ((rc = build_drop(d, c, T, dp))) return rc;
+  if (!X || !W_t || !A || !B || !dY || !H_save || !dA || !dB || !ws) return LORA_ERR_INVALID;
+  if (d->dora && (!dora_m || !dora_n || !Y_save || !dm)) return LORA_ERR_INVALID;
+  if (!al16(X) || !al16(W_t) || !al16(A) || !al16(B) || !al16(dY) || !al16(H_save) || !al16(dA) ||
+      !al16(dB) || !al16(ws) || (dX && !al16(dX)))
+    return LORA_ERR_ALIGN;
+  if (d->dora && (!al16(dora_m) || !al16(dora_n) || !al16(Y_save) || !al16(dm)))
+    return LORA_ERR_ALIGN;
+  if (ws_bytes < ws_size(d, T, -1, d->rank)) return LORA_ERR_WORKSPACE;
+  if (T == 0) return LORA_OK;
+  Slots s;
+  single_slot(d, A, B, dA, dB, s);
+  return run_backward(d, dp, T, X, W_t, -1, nullptr, nullptr, s, dY, H_save,
+                      d->dora ? dora_m : nullptr, d->dora ? dora_n : nullptr, Y_save, dX,
+                      d->dora ? dm : nullptr, ws, (cudaStream_t)stream);
+}
+
+int multi_lora_forward(const lora_desc* d, const lora_ctx* c, int64_t T, const void* X,
+                       const void* W, int32_t n_seg, const int32_t* d_seg_start,
+                       const int32_t* d_seg_slot, int32_t n_slots, const lora_slot* slots,
+                       void* Y, float* H_save, void* ws, size_t ws_bytes, void* stream) {
+  int rc = check_desc(d, T, true);
+  if (rc) return rc;
+  DropParams dp;
+  if ((rc = build_drop(d, c, T, dp))) return rc;
+  Slots s;
+  if ((rc = slots_from_table(d, n_slots, slots, false, s))) return rc;
+  if (n_seg < 0 || (n_seg > 0 && (!d_seg_start || !d_seg_slot))) return LORA_ERR_INVALID;
+  if (!X || !W || !Y || !H_save || !ws) return LORA_ERR_INVALID;
+  if (!al16(X) || !al16(W) || !al16(Y) || !al16(H_save) || !al16(ws)) return LORA_ERR_ALIGN;
+  if (ws_bytes < ws_size(d, T, n_seg, s.rank_sum)) return LORA_ERR_WORKSPACE;
+  if (T == 0) return LORA_OK;
+  return run_forward(d, dp, T, X, W, n_seg, n_seg ? d_seg_start : nullptr,
+                     n_seg ? d_seg_slot : nullptr, s, nullptr, nullptr, Y, H_save, ws,
+                     (cudaStream_t)stream);
+}
+
+int multi_lora_backward(const lora_desc* d, const lora_ctx* c, int64_t T, const void* X,
+                        const void* W_t, int32_t n_seg, const int32_t* d_seg_start,
+                        const int32_t* d_seg_slot, int32_t n_slots, const lora_slot* slots,
+                        const void* dY, const float* H_save, void* dX, void* ws,
+                        size_t ws_bytes, void* stream) {
+  int rc = check_desc(d, T, true);
+  if (rc) return rc;
+  DropParams dp;
+  if ((rc = build_drop(d, c, T, dp))) return rc;
+  Slots s;
+  if ((rc = slots_from_table(d, n_slots, slots, true, s))) return rc;
+  if (n_seg < 0 || (n_seg > 0 && (!d_seg_start || !d_seg_slot))) return LORA_ERR_INVALID;
+  if (!X || !W_t || !dY || !H_save || !ws) return LORA_ERR_INVALID;
+  if (!al16(X) || !al16(W_t) || !al16(dY) || !al16(H_save) || !al16(ws) || (dX && !al16(dX)))
+    return LORA_ERR_ALIGN;
+  if (ws_bytes < ws_size(d, T, n_seg, s.rank_sum)) return LORA_ERR_WORKSPACE;
+  if (T == 0) return LORA_OK;
+  return run_backward(d, dp, T, X, W_t, n_seg, n_seg ? d_seg_start : nullptr,
+                      n_seg ? d_seg_slot : nullptr, s, dY, H_save, nullptr, nullptr, nullptr, dX,
+                      nullptr, ws, (cudaStream_t)stream);
+}
+
+size_t lora_grad_prepare_workspace_size(int32_t n_groups, const lora_group* groups) {
+  if (!groups || n_groups < 1 || n_groups > LORA_MAX_GROUPS) return 0;
+  GroupTab g{};
+  g.n = n_groups;
+  for (int i = 0; i < n_groups; ++i) g.count[i] = groups[i].n_a + groups[i].n_b + groups[i].n_mag;
+  const int blocks = prepare_blocks(g);
+  Carve c(nullptr);
+  c.take<double>((size_t)(blocks > 0 ? blocks : 1));
+  c.take<uint32_t>(4);
+  return c.off + kWsAlign;
+}
+
+}  // extern "C"
+
+namespace {
+int build_groups(int32_t n_groups, const lora_group* groups, GroupTab& g, const lora_adamw_hp* hp) {
+  if (!groups || n_groups < 1) return LORA_ERR_INVALID;
+  if (n_groups > LORA_MAX_GROUPS) return LORA_ERR_UNSUPPORTED;
+  std::memset(&g, 0, sizeof(g));
+  g.n = n_groups;
+  for (int i = 0; i < n_groups; ++i) {
+    const lora_group& e = groups[i];
+    if (e.offset < 0 || e.n_a < 0 || e.n_b < 0 || e.n_mag < 0 || e.step < 0) return LORA_ERR_INVALID;
+    if (!(e.max_norm >= 0.f) || !std::isfinite(e.grad_scale) || !std::isfinite(e.lr))
+      return LORA_ERR_INVALID;
+    if (e.offset % 4) return LORA_ERR_ALIGN;
+    g.offset[i] = e.offset;
+    g.count[i] = e.n_a + e.n_b + e.n_mag;
+    g.n_a[i] = e.n_a;
+    g.n_b[i] = e.n_b;
+    g.gamma[i] = e.grad_scale;
+    g.max_norm[i] = e.max_norm;
+    g.lr[i] = e.lr;
+    if (hp) {
+      const double k = (double)e.step + 1.0;
+      g.bc1[i] = (float)(1.0 - std::pow((double)hp->beta1, k));
+      g.bc2[i] = (float)(1.0 - std::pow((double)hp->beta2, k));
+      if (!(g.bc1[i] > 0.f) || !(g.bc2[i] > 0.f)) return LORA_ERR_INVALID;
+    }
+  }
+  for (int i = 0; i < n_groups; ++i)
+    for (int j = i + 1; j < n_groups; ++j) {
+      const int64_t a0 = g.offset[i], a1 = a0 + g.count[i], b0 = g.offset[j], b1 = b0 + g.count[j];
+      if (a0 < b1 && b0 < a1 && g.count[i] > 0 && g.count[j] > 0) return LORA_ERR_INVALID;
+    }
+  return LORA_OK;
+}
+}  // namespace
+
+extern "C" {
+
+int lora_grad_prepare(const float* grads, int32_t n_groups, const lora_group* groups,
+                      double* d_scale_norm, int32_t* d_status, void* ws, size_t ws_bytes,
+                      void* stream) {
+  GroupTab g;
+  int rc = build_groups(n_groups, groups, g, nullptr);
+  if (rc) return rc;
+  if (!grads || !d_scale_norm || !d_status || !ws) return LORA_ERR_INVALID;
+  if (!al16(grads) || !al16(ws) || (reinterpret_cast<uintptr_t>(d_scale_norm) & 7u) ||
+      (reinterpret_cast<uintptr_t>(d_status) & 3u))
+    return LORA_ERR_ALIGN;
+  if (ws_bytes < lora_grad_prepare_workspace_size(n_groups, groups)) return LORA_ERR_WORKSPACE;
+  const int blocks = prepare_blocks(g);
+  Carve c(ws);
+  double* part = c.take<double>((size_t)(blocks > 0 ? blocks : 1));
+  uint32_t* counter = c.take<uint32_t>(4);
+  return cuda_status(launch_grad_prepare(grads, g, d_scale_norm, d_status, part, counter,
+                                         (cudaStream_t)stream));
+}
+
+int lora_adamw_step(float* params, float* grads, float* m, float* v, int32_t n_groups,
+                    const lora_group* groups, const lora_adamw_hp* hp, const double* d_scale_norm,
+                    const int32_t* d_status, int32_t zero_grads, void* stream) {
+  if (!hp) return LORA_ERR_INVALID;
+  if (!(hp->beta1 >= 0.f && hp->beta1 < 1.f && hp->beta2 >= 0.f && hp->beta2 < 1.f &&
+        hp->eps > 0.f && std::isfinite(hp->weight_decay) && std::isfinite(hp->plus_ratio)))
+    return LORA_ERR_INVALID;
+  GroupTab g;
+  int rc = build_groups(n_groups, groups, g, hp);
+  if (rc) return rc;
+  if (!params || !grads || !m || !v || !d_scale_norm || !d_status) return LORA_ERR_INVALID;
+  if (!al16(params) || !al16(grads) || !al16(m) || !al16(v)) return LORA_ERR_ALIGN;
+  return cuda_status(launch_adamw(params, grads, m, v, g, *hp, d_scale_norm, d_status, zero_grads,
+                                  (cudaStream_t)stream));
+}
+
+int lora_dropout_mask(const lora_desc* d, const lora_ctx* c, int64_t T, uint8_t* d_mask,
+                      void* stream) {
+  int rc = check_desc(d, T, false);
+  if (rc) return rc;
+  DropParams dp;
+  if ((rc = build_drop(d, c, T, dp))) return rc;
+  if (!d_mask) return LORA_ERR_INVALID;
+  return cuda_status(launch_dropout_mask(dp, T, d->in_dim, d_mask, (cudaStream_t)stream));
+}
+
+int multi_lora_token_slots(int64_t T, int32_t n_seg, const int32_t* d_seg_start,
+                           const int32_t* d_seg_slot, int32_t n_slots, int32_t* d_token_slot,
+                           void* stream) {
+  if (T < 0 || n_seg < 0 || n_slots < 1 || !d_token_slot) return LORA_ERR_INVALID;
+  if (n_seg > 0 && (!d_seg_start || !d_seg_slot)) return LORA_ERR_INVALID;
+  if (n_slots > LORA_MAX_SLOTS) return LORA_ERR_UNSUPPORTED;
+  if (T >= (int64_t(1) << 31) - kRedTileT) return LORA_ERR_UNSUPPORTED;
+  if (T == 0) return LORA_OK;
+  return cuda_status(launch_token_slots(T, n_seg, d_seg_start, d_seg_slot, n_slots, d_token_slot,
+                                        (cudaStream_t)stream));
+}
+
+}  // extern "C"

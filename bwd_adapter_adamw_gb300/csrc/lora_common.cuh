@@ -1,0 +1,88 @@
+// Shared device helpers for the LoRA-linear kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/lora_gb300.h"
+
+namespace lora {
+
+constexpr int kGemmTileT = 128;   // token rows per forward/dX/shrink/G work item
+constexpr int kRedTileT = 512;    // tokens per split of the token reductions (dA, dB)
+
+// ------------------------------------------------------------------------------------------
+// Stateless dropout hash ("4.3. Training Guide", Dropout: masks come from a stateless index
+// hash of seed, optimizer step, accumulation ordinal, token position, layer and projection).
+// Mixer: the SplitMix64 output finaliser (Steele, Lea & Flood 2014, Stafford variant 13).
+// key(chunk) = mix(mix(mix(seed ^ gamma) ^ step) ^ (ordinal << 48 | layer << 16 | proj)),
+// element (position t, column i): h = mix(key ^ (t * in + i)); kept iff (h >> 32) >= tau,
+// tau = floor(p * 2^32). The per-chunk keys are computed on the host.
+// ------------------------------------------------------------------------------------------
+__host__ __device__ __forceinline__ uint64_t mix64(uint64_t z) {
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+struct DropParams {
+  int32_t enabled;        // 0: every element kept, no hash evaluated
+  uint32_t tau;
+  int64_t chunk_tokens;   // tokens per accumulation chunk within the call (> 0)
+  int64_t in_dim;
+  uint64_t keys[LORA_MAX_CHUNKS_PER_CALL];
+};
+
+// Keep decision for token t (index within the call) and input column i.
+__device__ __forceinline__ bool drop_keep(const DropParams& d, int64_t t, int64_t i) {
+  const int64_t c = t / d.chunk_tokens;
+  const int64_t pos = t - c * d.chunk_tokens;
+  const uint64_t h = mix64(d.keys[c] ^ (uint64_t)(pos * d.in_dim + i));
+  return (uint32_t)(h >> 32) >= d.tau;
+}
+
+// ------------------------------------------------------------------------------------------
+// element loads
+// ------------------------------------------------------------------------------------------
+template <typename T> struct Vec;
+template <> struct Vec<float> { static constexpr int N = 4; };
+template <> struct Vec<__nv_bfloat16> { static constexpr int N = 8; };
+
+// Load VEC consecutive elements (16 bytes) as floats.
+__device__ __forceinline__ void load16(const float* p, float* out) {
+  const float4 v = __ldg(reinterpret_cast<const float4*>(p));
+  out[0] = v.x; out[1] = v.y; out[2] = v.z; out[3] = v.w;
+}
+__device__ __forceinline__ void load16(const __nv_bfloat16* p, float* out) {
+  const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    out[2 * j] = __uint_as_float(w[j] << 16);
+    out[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// Store 4 consecutive outputs.
+__device__ __forceinline__ void store4(float* p, const float* v) {
+  *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+}
+__device__ __forceinline__ void store4(__nv_bfloat16* p, const float* v) {
+  __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]);
+  __nv_bfloat162 b = __floats2bfloat162_rn(v[2], v[3]);
+  uint2 u;
+  u.x = *reinterpret_cast<uint32_t*>(&a);
+  u.y = *reinterpret_cast<uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(p) = u;
+}
+
+// A token range handled by one CTA, with the adapter slot of those tokens (-1: none).
+struct TokenItem {
+  int32_t t0, t1, slot, pad;
+};
+
+}  // namespace lora

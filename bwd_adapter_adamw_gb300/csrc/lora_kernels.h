@@ -1,0 +1,139 @@
+// Internal launch interface between the C-ABI layer (api.cu) and the kernels.
+#pragma once
+
+#include "lora_common.cuh"
+
+namespace lora {
+
+// profile.cu: launch counter and optional event brackets per kernel class (LORA_PROF_*).
+void prof_begin(int kind, cudaStream_t st);
+void prof_end(int kind, cudaStream_t st);
+
+// Per-slot operand table (fp32 adapters or their transposes).
+struct SlotTab {
+  const float* p[LORA_MAX_SLOTS];
+  int64_t ld[LORA_MAX_SLOTS];
+  int32_t rank[LORA_MAX_SLOTS];
+  float alpha[LORA_MAX_SLOTS];
+};
+
+struct TokGemmArgs {
+  const TokenItem* items;
+  const int32_t* n_items;
+  // main phase, A side: tokens x K, K-contiguous
+  const void* a;
+  int64_t lda;
+  int64_t K;
+  const float* a_colscale;   // multiply A[t, k] by a_colscale[k] (DoRA dY')
+  int32_t a_mask;            // zero A[t, k] where the dropout mask drops (t, k)
+  // main phase, B side: n_rows x K, K-contiguous; fixed or per slot
+  const void* b;
+  int64_t ldb;
+  int64_t n_rows;
+  int32_t b_per_slot;
+  SlotTab bslot;
+  // LoRA phase (extra K-steps): P [T, rank_slot] (row stride ldlp) times Q_slot [n_rows, rank_slot]
+  int32_t lora_phase;
+  const float* lp;
+  int64_t ldlp;
+  SlotTab lq;
+  int32_t mask_after_lora;   // multiply the LoRA phase result by the dropout mask at (t, n)
+  // epilogue
+  float alpha;
+  int32_t alpha_per_slot;    // alpha = bslot.alpha[slot]
+  const float* n_colscale;   // multiply column n by n_colscale[n] (DoRA m / n)
+  void* out;
+  int64_t ldo;
+  int64_t n_out;             // columns written
+  DropParams drop;
+};
+
+struct RedGemmArgs {
+  const TokenItem* items;
+  const int32_t* n_items;
+  const void* a;             // [T, lda], column m (M extent)
+  int64_t lda;
+  int64_t M;
+  const float* a_colscale;
+  int32_t a_mask;
+  const float* b;            // [T, ldb] fp32, column j < rank[slot]
+  int64_t ldb;
+  int32_t rank[LORA_MAX_SLOTS];
+  float* part;               // [items][M][ldp]
+  int64_t ldp;
+  DropParams drop;
+};
+
+cudaError_t launch_tok_gemm(int dtype_a, int dtype_b, int dtype_out, int bn, const TokGemmArgs& a,
+                            int max_items, cudaStream_t st, int prof_kind);
+cudaError_t launch_red_gemm(int dtype_a, const RedGemmArgs& a, int max_items, cudaStream_t st,
+                            int prof_kind);
+
+// ---- lowrank.cu ----
+cudaError_t launch_make_items(int64_t T, int32_t n_seg, const int32_t* seg_start,
+                              const int32_t* seg_slot, int32_t n_slots, TokenItem* gitems,
+                              int32_t* gcount, int32_t gmax, TokenItem* ritems, int32_t* rcount,
+                              int32_t rmax, cudaStream_t st);
+
+struct TransposeTab {
+  const float* src[LORA_MAX_SLOTS];
+  float* dst[LORA_MAX_SLOTS];
+  int64_t rows[LORA_MAX_SLOTS];   // src rows
+  int64_t cols[LORA_MAX_SLOTS];   // src cols
+};
+cudaError_t launch_transpose_slots(const TransposeTab& t, int n, int64_t max_rows, int64_t max_cols,
+                                   cudaStream_t st);
+cudaError_t launch_transpose_weight(int dtype, const void* W, void* Wt, int64_t rows, int64_t cols,
+                                    cudaStream_t st);
+
+// out_slot[j, i] (+)= sum over items of `slot` of part[item][...]; see lowrank.cu
+struct ReduceTab {
+  float* out[LORA_MAX_SLOTS];
+  int32_t rank[LORA_MAX_SLOTS];
+};
+cudaError_t launch_reduce_parts(const float* part, const TokenItem* items, const int32_t* n_items,
+                                int max_items, int64_t M, int64_t ldp, int transposed,
+                                const ReduceTab& tab, int n_slots, cudaStream_t st);
+
+cudaError_t launch_dropout_mask(const DropParams& dp, int64_t T, int64_t in_dim, uint8_t* mask,
+                                cudaStream_t st);
+cudaError_t launch_ratio(const float* num, const float* den, int64_t n, float* out, cudaStream_t st);
+cudaError_t launch_token_slots(int64_t T, int32_t n_seg, const int32_t* seg_start,
+                               const int32_t* seg_slot, int32_t n_slots, int32_t* token_slot,
+                               cudaStream_t st);
+
+// ---- dora.cu ----
+cudaError_t launch_dora_norm(int dtype, const void* W, const float* A, const float* B, float s,
+                             int64_t out_dim, int64_t in_dim, int32_t rank, float* norm_out,
+                             cudaStream_t st);
+cudaError_t launch_dora_dm(int dtype, const void* dY, const void* Y, const float* mag, int64_t T,
+                           int64_t out_dim, float* dm, cudaStream_t st);
+
+// ---- optim.cu ----
+struct GroupTab {
+  int32_t n;
+  int64_t offset[LORA_MAX_GROUPS];
+  int64_t count[LORA_MAX_GROUPS];
+  int64_t n_a[LORA_MAX_GROUPS];
+  int64_t n_b[LORA_MAX_GROUPS];
+  int32_t block_begin[LORA_MAX_GROUPS + 1];
+  double gamma[LORA_MAX_GROUPS];
+  float max_norm[LORA_MAX_GROUPS];
+  float lr[LORA_MAX_GROUPS];
+  float bc1[LORA_MAX_GROUPS];   // 1 - beta1^k
+  float bc2[LORA_MAX_GROUPS];   // 1 - beta2^k
+};
+constexpr int kPrepThreads = 256;
+constexpr int kPrepElemsPerBlock = kPrepThreads * 64;
+constexpr int kAdamThreads = 256;
+constexpr int kAdamElemsPerBlock = kAdamThreads * 16;
+
+// workspace: [blocks] double partials, [blocks] int flags, 1 int counter
+int prepare_blocks(const GroupTab& g);  // CTAs (and double partials) of one prepare launch
+cudaError_t launch_grad_prepare(const float* grads, const GroupTab& g, double* d_scale_norm,
+                                int32_t* d_status, double* part, uint32_t* counter, cudaStream_t st);
+cudaError_t launch_adamw(float* p, float* g, float* m, float* v, const GroupTab& gt,
+                         const lora_adamw_hp& hp, const double* d_scale_norm,
+                         const int32_t* d_status, int zero_grads, cudaStream_t st);
+
+}  // namespace lora

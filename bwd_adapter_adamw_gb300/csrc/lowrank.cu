@@ -1,0 +1,213 @@
+// Token work items, adapter transposes, ordered split reductions and the test hooks.
+#include "lora_kernels.h"
+
+namespace lora {
+
+namespace {
+
+// Token work items from the segment table ("Multi-LoRA Training Example (fully-async)", Design:
+// a batch holds contiguous per-adapter sample groups; here a segment is a contiguous token range
+// with one slot). Segments are taken in order; each covers [max(start, end of coverage so far),
+// end), clamped to [0, T). Uncovered tokens form items with slot -1 (frozen output only).
+// Items never cross a segment boundary, so every CTA works for exactly one slot.
+__global__ void k_make_items(int64_t T, int32_t n_seg, const int32_t* __restrict__ seg_start,
+                             const int32_t* __restrict__ seg_slot, int32_t n_slots,
+                             TokenItem* gitems, int32_t* gcount, int32_t gmax, TokenItem* ritems,
+                             int32_t* rcount, int32_t rmax) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  int32_t ng = 0, nr = 0;
+  int64_t cursor = 0;
+  auto emit = [&](int64_t a, int64_t b, int32_t slot) {
+    for (int64_t t = a; t < b; t += kGemmTileT)
+      if (ng < gmax) gitems[ng++] = TokenItem{(int32_t)t, (int32_t)min(b, t + kGemmTileT), slot, 0};
+    if (slot >= 0)
+      for (int64_t t = a; t < b; t += kRedTileT)
+        if (nr < rmax) ritems[nr++] = TokenItem{(int32_t)t, (int32_t)min(b, t + kRedTileT), slot, 0};
+  };
+  // n_seg < 0: one implicit segment [0, T) with slot 0 (single-adapter calls)
+  const int32_t nsegs = seg_start ? n_seg : (n_seg < 0 ? 1 : 0);
+  for (int32_t k = 0; k < nsegs; ++k) {
+    int64_t a = seg_start ? (int64_t)seg_start[k] : 0;
+    int64_t b = seg_start ? (int64_t)seg_start[k + 1] : T;
+    int32_t slot = seg_slot ? seg_slot[k] : 0;
+    if (slot < 0 || slot >= n_slots) slot = -1;
+    a = max((int64_t)0, min(a, T));
+    b = max((int64_t)0, min(b, T));
+    if (a < cursor) a = cursor;
+    if (b <= a) continue;
+    if (a > cursor) emit(cursor, a, -1);
+    emit(a, b, slot);
+    cursor = b;
+  }
+  if (cursor < T) emit(cursor, T, -1);
+  *gcount = ng;
+  *rcount = nr;
+}
+
+// 32 x 32 shared-memory tile transpose of fp32 matrices, one matrix per blockIdx.z.
+__global__ void k_transpose_slots(const TransposeTab tab) {
+  __shared__ float tile[32][33];
+  const int z = blockIdx.z;
+  const int64_t rows = tab.rows[z], cols = tab.cols[z];
+  const int64_t c0 = (int64_t)blockIdx.x * 32, r0 = (int64_t)blockIdx.y * 32;
+  if (r0 >= rows || c0 >= cols) return;
+  const float* src = tab.src[z];
+  float* dst = tab.dst[z];
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    const int64_t r = r0 + i, c = c0 + threadIdx.x;
+    if (r < rows && c < cols) tile[i][threadIdx.x] = src[r * cols + c];
+  }
+  __syncthreads();
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    const int64_t c = c0 + i, r = r0 + threadIdx.x;
+    if (r < rows && c < cols) dst[c * rows + r] = tile[threadIdx.x][i];
+  }
+}
+
+template <typename T>
+__global__ void k_transpose_w(const T* __restrict__ src, T* __restrict__ dst, int64_t rows,
+                              int64_t cols) {
+  __shared__ T tile[32][33];
+  const int64_t c0 = (int64_t)blockIdx.x * 32, r0 = (int64_t)blockIdx.y * 32;
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    const int64_t r = r0 + i, c = c0 + threadIdx.x;
+    if (r < rows && c < cols) tile[i][threadIdx.x] = src[r * cols + c];
+  }
+  __syncthreads();
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    const int64_t c = c0 + i, r = r0 + threadIdx.x;
+    if (r < rows && c < cols) dst[c * rows + r] = tile[threadIdx.x][i];
+  }
+}
+
+// out_slot += sum over the slot's items, in item order, of the per-item partials.
+// part[item] is [M][ldp]; element (m, j), j < rank_slot, goes to out_slot[m * rank + j]
+// (transposed == 0, dB layout [out, r]) or out_slot[j * M + m] (transposed == 1, dA [r, in]).
+__global__ void k_reduce_parts(const float* __restrict__ part, const TokenItem* __restrict__ items,
+                               const int32_t* __restrict__ n_items, int64_t M, int64_t ldp,
+                               int transposed, const ReduceTab tab) {
+  const int slot = blockIdx.y;
+  const int32_t r = tab.rank[slot];
+  float* out = tab.out[slot];
+  const int64_t total = M * ldp;
+  const int32_t ni = *n_items;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t m = e / ldp;
+    const int32_t j = (int32_t)(e - m * ldp);
+    if (j >= r) continue;
+    float acc = 0.f;
+    bool any = false;
+    for (int32_t it = 0; it < ni; ++it) {
+      if (items[it].slot != slot) continue;
+      acc += part[(int64_t)it * total + e];
+      any = true;
+    }
+    if (!any) continue;
+    const int64_t o = transposed ? ((int64_t)j * M + m) : (m * r + j);
+    out[o] += acc;
+  }
+}
+
+__global__ void k_dropout_mask(const DropParams dp, int64_t T, int64_t in_dim, uint8_t* mask) {
+  const int64_t n = T * in_dim;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = e / in_dim, i = e - t * in_dim;
+    mask[e] = (!dp.enabled || drop_keep(dp, t, i)) ? 1 : 0;
+  }
+}
+
+__global__ void k_ratio(const float* __restrict__ num, const float* __restrict__ den, int64_t n,
+                        float* __restrict__ out) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) out[i] = num[i] / den[i];
+}
+
+// Slot of every token by the same segment walk as k_make_items: one CTA, segments in order,
+// the CTA's threads fill each covered range.
+__global__ void k_token_slots(int64_t T, int32_t n_seg, const int32_t* __restrict__ seg_start,
+                              const int32_t* __restrict__ seg_slot, int32_t n_slots,
+                              int32_t* __restrict__ token_slot) {
+  int64_t cursor = 0;
+  for (int32_t k = 0; k < n_seg; ++k) {
+    int64_t a = max((int64_t)0, min((int64_t)seg_start[k], T));
+    int64_t b = max((int64_t)0, min((int64_t)seg_start[k + 1], T));
+    int32_t slot = seg_slot[k];
+    if (slot < 0 || slot >= n_slots) slot = -1;
+    if (a < cursor) a = cursor;
+    if (b <= a) continue;
+    for (int64_t t = cursor + threadIdx.x; t < a; t += blockDim.x) token_slot[t] = -1;
+    for (int64_t t = a + threadIdx.x; t < b; t += blockDim.x) token_slot[t] = slot;
+    cursor = b;
+  }
+  for (int64_t t = cursor + threadIdx.x; t < T; t += blockDim.x) token_slot[t] = -1;
+}
+
+}  // namespace
+
+cudaError_t launch_make_items(int64_t T, int32_t n_seg, const int32_t* seg_start,
+                              const int32_t* seg_slot, int32_t n_slots, TokenItem* gitems,
+                              int32_t* gcount, int32_t gmax, TokenItem* ritems, int32_t* rcount,
+                              int32_t rmax, cudaStream_t st) {
+  { prof_begin(0, st); k_make_items<<<1, 32, 0, st>>>(T, n_seg, seg_start, seg_slot, n_slots, gitems, gcount, gmax,
+                                 ritems, rcount, rmax); }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_slots(const TransposeTab& t, int n, int64_t max_rows, int64_t max_cols,
+                                   cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  dim3 grid((unsigned)((max_cols + 31) / 32), (unsigned)((max_rows + 31) / 32), (unsigned)n);
+  { prof_begin(0, st); k_transpose_slots<<<grid, dim3(32, 8), 0, st>>>(t); }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_weight(int dtype, const void* W, void* Wt, int64_t rows, int64_t cols,
+                                    cudaStream_t st) {
+  dim3 grid((unsigned)((cols + 31) / 32), (unsigned)((rows + 31) / 32));
+  if (dtype == LORA_F32)
+    { prof_begin(0, st); k_transpose_w<float><<<grid, dim3(32, 8), 0, st>>>((const float*)W, (float*)Wt, rows, cols); }
+  else
+    { prof_begin(0, st); k_transpose_w<__nv_bfloat16><<<grid, dim3(32, 8), 0, st>>>((const __nv_bfloat16*)W,
+                                                                (__nv_bfloat16*)Wt, rows, cols); }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reduce_parts(const float* part, const TokenItem* items, const int32_t* n_items,
+                                int max_items, int64_t M, int64_t ldp, int transposed,
+                                const ReduceTab& tab, int n_slots, cudaStream_t st) {
+  (void)max_items;
+  const int64_t total = M * ldp;
+  const int threads = 256;
+  int64_t blocks = (total + threads - 1) / threads;
+  if (blocks > 4096) blocks = 4096;
+  dim3 grid((unsigned)blocks, (unsigned)n_slots);
+  { prof_begin(0, st); k_reduce_parts<<<grid, threads, 0, st>>>(part, items, n_items, M, ldp, transposed, tab); }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dropout_mask(const DropParams& dp, int64_t T, int64_t in_dim, uint8_t* mask,
+                                cudaStream_t st) {
+  const int64_t n = T * in_dim;
+  if (n == 0) return cudaSuccess;
+  int64_t blocks = (n + 255) / 256;
+  if (blocks > 8192) blocks = 8192;
+  { prof_begin(0, st); k_dropout_mask<<<(unsigned)blocks, 256, 0, st>>>(dp, T, in_dim, mask); }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ratio(const float* num, const float* den, int64_t n, float* out, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  { prof_begin(0, st); k_ratio<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(num, den, n, out); }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_token_slots(int64_t T, int32_t n_seg, const int32_t* seg_start,
+                               const int32_t* seg_slot, int32_t n_slots, int32_t* token_slot,
+                               cudaStream_t st) {
+  { prof_begin(0, st); k_token_slots<<<1, 256, 0, st>>>(T, n_seg, seg_start, seg_slot, n_slots, token_slot); }
+  return cudaGetLastError();
+}
+
+}  // namespace lora

@@ -1,0 +1,226 @@
+// Two-pass global-norm clip and the fused clip + A-only decoupled AdamW update over flat fp32
+// arenas ("4.3. Training Guide", Gradient clipping: pass 1 accumulates the squared norm in double
+// and rejects non-finite values before any mutation, pass 2 applies one combined normalisation x
+// clipping factor; Optimizer: decay on A only from the pre-update value with the scheduled lr,
+// LoRA+ ratio on B's lr, moments see the gradient without decay).
+#include "lora_kernels.h"
+
+namespace lora {
+
+namespace {
+
+// a^2 added exactly into the float-float pair (hi, lo): the square is split error-free with an
+// FMA (TwoProduct) and added with Knuth's TwoSum. The *_rn intrinsics keep the compiler from
+// fusing or reassociating these steps.
+__device__ __forceinline__ void ff_add_square(float a, float& hi, float& lo) {
+  const float p = __fmul_rn(a, a);
+  const float e = fmaf(a, a, -p);
+  const float s = __fadd_rn(hi, p);
+  const float bp = __fsub_rn(s, hi);
+  const float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bp)), __fsub_rn(p, bp));
+  hi = s;
+  lo = __fadd_rn(lo, __fadd_rn(err, e));
+}
+
+// One element of pass 1. |a| > 2^60 (and +-Inf) goes to a double accumulator so that no finite
+// square overflows; NaN propagates through hi. The block sum is non-finite iff an element is.
+__device__ __forceinline__ void sq_accum(float a, float& hi, float& lo, double& big) {
+  if (fabsf(a) > 0x1p60f) {
+    const double d = (double)a;
+    big = fma(d, d, big);
+  } else {
+    ff_add_square(a, hi, lo);
+  }
+}
+
+__device__ __forceinline__ double block_sum_double(double v, double* sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_down_sync(0xffffffffu, v, off);
+  __syncthreads();
+  if (lane == 0) sh[warp] = v;
+  __syncthreads();
+  double r = 0.0;
+  if (threadIdx.x == 0)
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) r += sh[w];
+  return r;  // valid in thread 0
+}
+
+__device__ __forceinline__ int find_group(const GroupTab& g, int b) {
+  int lo = 0, hi = g.n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (g.block_begin[mid] <= b) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+__global__ void __launch_bounds__(kPrepThreads) k_grad_prepare(const float* __restrict__ grads,
+                                                               const GroupTab gt,
+                                                               double* __restrict__ scale_norm,
+                                                               int32_t* __restrict__ status,
+                                                               double* part, uint32_t* counter) {
+  __shared__ double sh[kPrepThreads / 32];
+  __shared__ bool am_last;
+  const int b = blockIdx.x;
+  const int g = find_group(gt, b);
+  const int64_t begin = (int64_t)(b - gt.block_begin[g]) * kPrepElemsPerBlock;
+  const int64_t n = min((int64_t)kPrepElemsPerBlock, gt.count[g] - begin);
+  const float* p = grads + gt.offset[g] + begin;
+  float hi = 0.f, lo = 0.f;
+  double big = 0.0;
+  const int64_t nv = n >> 2;
+#pragma unroll 4
+  for (int64_t v = threadIdx.x; v < nv; v += kPrepThreads) {
+    const float4 x = __ldcs(reinterpret_cast<const float4*>(p) + v);
+    sq_accum(x.x, hi, lo, big);
+    sq_accum(x.y, hi, lo, big);
+    sq_accum(x.z, hi, lo, big);
+    sq_accum(x.w, hi, lo, big);
+  }
+  for (int64_t e = (nv << 2) + threadIdx.x; e < n; e += kPrepThreads) sq_accum(p[e], hi, lo, big);
+  const double mine = ((double)hi + (double)lo) + big;
+  const double tot = block_sum_double(mine, sh);
+  if (threadIdx.x == 0) {
+    part[b] = tot;
+    __threadfence();
+    const uint32_t done = atomicAdd(counter, 1u);
+    am_last = (done == gridDim.x - 1);
+  }
+  __syncthreads();
+  if (!am_last) return;
+  __threadfence();
+  // last block: per group, fixed-order reduction of that group's block partials
+  for (int gg = 0; gg < gt.n; ++gg) {
+    const int b0 = gt.block_begin[gg], b1 = gt.block_begin[gg + 1];
+    double acc = 0.0;
+    for (int k = b0 + threadIdx.x; k < b1; k += kPrepThreads) acc += __ldcg(part + k);
+    const double S = block_sum_double(acc, sh);
+    if (threadIdx.x == 0) {
+      if (!isfinite(S)) {
+        status[gg] = LORA_ERR_NONFINITE;
+        scale_norm[2 * gg] = 0.0;
+        scale_norm[2 * gg + 1] = S;
+      } else {
+        const double gamma = gt.gamma[gg];
+        const double norm = sqrt(S) * gamma;
+        const double mx = (double)gt.max_norm[gg];
+        const double c = (mx > 0.0 && norm > mx) ? gamma * (mx / norm) : gamma;
+        status[gg] = LORA_OK;
+        scale_norm[2 * gg] = c;
+        scale_norm[2 * gg + 1] = norm;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void adam_elem(float& p, float& g, float& m, float& v, int kind,
+                                          float c, float lr, float b1, float b2, float eps,
+                                          float wd, float rho, float inv_bc1, float inv_bc2) {
+  const float gh = g * c;
+  m = fmaf(b1, m, (1.f - b1) * gh);
+  v = fmaf(b2, v, (1.f - b2) * gh * gh);
+  const float u = (m * inv_bc1) / (sqrtf(v * inv_bc2) + eps);
+  if (kind == 0)
+    p = p - lr * u - lr * wd * p;
+  else if (kind == 1)
+    p = p - (lr * rho) * u;
+  else
+    p = p - lr * u;
+}
+
+__global__ void __launch_bounds__(kAdamThreads) k_adamw(float* __restrict__ P, float* __restrict__ G,
+                                                        float* __restrict__ Mo, float* __restrict__ V,
+                                                        const GroupTab gt, const lora_adamw_hp hp,
+                                                        const double* __restrict__ scale_norm,
+                                                        const int32_t* __restrict__ status,
+                                                        int zero_grads) {
+  const int b = blockIdx.x;
+  const int g = find_group(gt, b);
+  if (status[g] != LORA_OK) return;
+  const float c = (float)scale_norm[2 * g];
+  const float lr = gt.lr[g];
+  const float inv_bc1 = 1.f / gt.bc1[g], inv_bc2 = 1.f / gt.bc2[g];
+  const int64_t begin = (int64_t)(b - gt.block_begin[g]) * kAdamElemsPerBlock;
+  const int64_t n = min((int64_t)kAdamElemsPerBlock, gt.count[g] - begin);
+  const int64_t base = gt.offset[g] + begin;
+  const int64_t na = gt.n_a[g], nab = gt.n_a[g] + gt.n_b[g];
+  const int64_t nv = n >> 2;
+  for (int64_t q = threadIdx.x; q < nv; q += kAdamThreads) {
+    const int64_t e = base + (q << 2);
+    float4 p = *reinterpret_cast<float4*>(P + e);
+    float4 gr = *reinterpret_cast<float4*>(G + e);
+    float4 m = *reinterpret_cast<float4*>(Mo + e);
+    float4 v = *reinterpret_cast<float4*>(V + e);
+    float* pp = &p.x; float* gg = &gr.x; float* mm = &m.x; float* vv = &v.x;
+    const int64_t li = begin + (q << 2);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int64_t l = li + j;
+      const int kind = (l < na) ? 0 : ((l < nab) ? 1 : 2);
+      adam_elem(pp[j], gg[j], mm[j], vv[j], kind, c, lr, hp.beta1, hp.beta2, hp.eps,
+                hp.weight_decay, hp.plus_ratio, inv_bc1, inv_bc2);
+    }
+    *reinterpret_cast<float4*>(P + e) = p;
+    *reinterpret_cast<float4*>(Mo + e) = m;
+    *reinterpret_cast<float4*>(V + e) = v;
+    if (zero_grads) *reinterpret_cast<float4*>(G + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  for (int64_t l = begin + (nv << 2) + threadIdx.x; l < begin + n; l += kAdamThreads) {
+    const int64_t e = gt.offset[g] + l;
+    const int kind = (l < na) ? 0 : ((l < nab) ? 1 : 2);
+    float p = P[e], gr = G[e], m = Mo[e], v = V[e];
+    adam_elem(p, gr, m, v, kind, c, lr, hp.beta1, hp.beta2, hp.eps, hp.weight_decay,
+              hp.plus_ratio, inv_bc1, inv_bc2);
+    P[e] = p; Mo[e] = m; V[e] = v;
+    if (zero_grads) G[e] = 0.f;
+  }
+}
+
+int set_blocks(GroupTab& g, int64_t per_block) {
+  int total = 0;
+  for (int i = 0; i < g.n; ++i) {
+    g.block_begin[i] = total;
+    total += (int)((g.count[i] + per_block - 1) / per_block);
+  }
+  g.block_begin[g.n] = total;
+  return total;
+}
+
+}  // namespace
+
+int prepare_blocks(const GroupTab& g) {
+  GroupTab t = g;
+  return set_blocks(t, kPrepElemsPerBlock);
+}
+
+cudaError_t launch_grad_prepare(const float* grads, const GroupTab& g_in, double* d_scale_norm,
+                                int32_t* d_status, double* part, uint32_t* counter, cudaStream_t st) {
+  GroupTab g = g_in;
+  int blocks = set_blocks(g, kPrepElemsPerBlock);
+  cudaError_t e = cudaMemsetAsync(counter, 0, sizeof(uint32_t), st);
+  if (e != cudaSuccess) return e;
+  if (blocks == 0) {
+    // every group is empty: one block writes the zero-norm results
+    blocks = 1;
+    g.block_begin[g.n] = 1;
+    for (int i = 0; i < g.n; ++i) g.block_begin[i] = 0;
+  }
+  prof_begin(LORA_PROF_PREPARE, st);
+  k_grad_prepare<<<blocks, kPrepThreads, 0, st>>>(grads, g, d_scale_norm, d_status, part, counter);
+  prof_end(LORA_PROF_PREPARE, st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_adamw(float* p, float* g, float* m, float* v, const GroupTab& gt_in,
+                         const lora_adamw_hp& hp, const double* d_scale_norm,
+                         const int32_t* d_status, int zero_grads, cudaStream_t st) {
+  GroupTab gt = gt_in;
+  const int blocks = set_blocks(gt, kAdamElemsPerBlock);
+  if (blocks == 0) return cudaSuccess;
+  prof_begin(LORA_PROF_ADAMW, st);
+  k_adamw<<<blocks, kAdamThreads, 0, st>>>(p, g, m, v, gt, hp, d_scale_norm, d_status, zero_grads);
+  prof_end(LORA_PROF_ADAMW, st);
+  return cudaGetLastError();
+}
+
+}  // namespace lora

@@ -1,0 +1,334 @@
+"""Host orchestration of one optimizer step through the C ABI.
+
+This module allocates device buffers with torch (flat fp32 arenas for parameters, gradients and
+Adam moments; per-stream workspaces) and sequences the library calls: per adapted linear a
+forward and a backward over all accumulation chunks, then one grad-prepare and one AdamW launch
+over the arena. It computes nothing itself: every number of the step comes from the library's
+kernels.
+
+Arena layout (one per adapter set): [A of every linear | B of every linear | DoRA magnitudes],
+so a single lora_group describes the global clip ("4.3. Training Guide", Gradient clipping:
+clipped globally by L2 norm) and the AdamW kinds. Multi-LoRA uses one group per slot
+("Multi-LoRA Training Example (fully-async)", Design: per-slot state, step counts and clipping).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+from typing import Dict, List, Optional, Sequence, Tuple
+
+import torch
+
+from . import binding as L
+
+_DT = {"f32": L.LORA_F32, "bf16": L.LORA_BF16}
+
+
+def _ws(nbytes: int, device) -> torch.Tensor:
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+@dataclass
+class Linear:
+    """One adapted linear with its activations (device tensors)."""
+    layer: int
+    proj_id: int
+    X: torch.Tensor          # [T, in]
+    W: torch.Tensor          # [out, in]
+    dY: torch.Tensor         # [T, out]
+    Wt: Optional[torch.Tensor] = None   # [in, out], filled by prepare_weights
+    Y: Optional[torch.Tensor] = None
+    dX: Optional[torch.Tensor] = None
+    H: Optional[torch.Tensor] = None
+    # views into the arenas
+    A: Optional[torch.Tensor] = None
+    B: Optional[torch.Tensor] = None
+    gA: Optional[torch.Tensor] = None
+    gB: Optional[torch.Tensor] = None
+    mag: Optional[torch.Tensor] = None
+    gmag: Optional[torch.Tensor] = None
+    norm: Optional[torch.Tensor] = None
+
+    @property
+    def in_dim(self) -> int:
+        return self.W.shape[1]
+
+    @property
+    def out_dim(self) -> int:
+        return self.W.shape[0]
+
+
+class Arena:
+    """Flat fp32 parameter / gradient / moment arenas with named views."""
+
+    def __init__(self, n: int, device):
+        self.n = n
+        self.params = torch.zeros(n, dtype=torch.float32, device=device)
+        self.grads = torch.zeros(n, dtype=torch.float32, device=device)
+        self.m = torch.zeros(n, dtype=torch.float32, device=device)
+        self.v = torch.zeros(n, dtype=torch.float32, device=device)
+
+    def view(self, which: str, offset: int, shape) -> torch.Tensor:
+        numel = 1
+        for s in shape:
+            numel *= s
+        return getattr(self, which)[offset:offset + numel].view(*shape)
+
+
+class LoraStep:
+    """One optimizer step over a set of independent adapted linears sharing rank/scale/dtype."""
+
+    def __init__(self, linears: Sequence[Linear], *, rank: int, scale: float, dtype: str,
+                 tokens: int, chunks: int, dropout_p: float = 0.0, seed: int = 0,
+                 dora: bool = False, max_norm: float = 1.0, hp: Optional[L.lora_adamw_hp] = None,
+                 n_streams: int = 1, device="cuda"):
+        self.linears = list(linears)
+        self.rank, self.scale, self.dtype = rank, scale, _DT[dtype]
+        self.T, self.chunks = tokens, chunks
+        self.dropout_p, self.seed, self.dora = dropout_p, seed, dora
+        self.max_norm = max_norm
+        self.hp = hp if hp is not None else L.make_hp()
+        self.device = torch.device(device)
+        # arena: [A ... | B ... | MAG ...]
+        na = sum(rank * l.in_dim for l in self.linears)
+        nb = sum(l.out_dim * rank for l in self.linears)
+        nm = sum(l.out_dim for l in self.linears) if dora else 0
+        self.n_a, self.n_b, self.n_mag = na, nb, nm
+        self.arena = Arena(na + nb + nm, self.device)
+        oa, ob, om = 0, na, na + nb
+        for l in self.linears:
+            l.A = self.arena.view("params", oa, (rank, l.in_dim))
+            l.gA = self.arena.view("grads", oa, (rank, l.in_dim))
+            oa += rank * l.in_dim
+            l.B = self.arena.view("params", ob, (l.out_dim, rank))
+            l.gB = self.arena.view("grads", ob, (l.out_dim, rank))
+            ob += l.out_dim * rank
+            if dora:
+                l.mag = self.arena.view("params", om, (l.out_dim,))
+                l.gmag = self.arena.view("grads", om, (l.out_dim,))
+                om += l.out_dim
+                l.norm = torch.empty(l.out_dim, dtype=torch.float32, device=self.device)
+            act = l.X.dtype
+            if l.Y is None:
+                l.Y = torch.empty((self.T, l.out_dim), dtype=act, device=self.device)
+            if l.dX is None:
+                l.dX = torch.empty((self.T, l.in_dim), dtype=act, device=self.device)
+            if l.H is None:
+                l.H = torch.empty((self.T, rank), dtype=torch.float32, device=self.device)
+        self.n_streams = max(1, n_streams)
+        self.streams = [torch.cuda.Stream(device=self.device) for _ in range(self.n_streams)] \
+            if self.n_streams > 1 else []
+        ws_need = max(L.lora_workspace_size(self.desc(l), self.T) for l in self.linears)
+        if ws_need == 0:
+            raise L.LoraError(L.LORA_ERR_INVALID, "lora_workspace_size")
+        self.ws = [_ws(ws_need, self.device) for _ in range(self.n_streams)]
+        self.scale_norm = torch.zeros(2, dtype=torch.float64, device=self.device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
+        self._groups_cache = None
+
+    # ------------------------------------------------------------------------------------------
+    def desc(self, l: Linear) -> L.lora_desc:
+        return L.make_desc(l.in_dim, l.out_dim, self.rank, self.scale, self.dtype, self.dropout_p,
+                           self.seed, l.layer, l.proj_id, self.dora)
+
+    def prepare_weights(self, stream=None):
+        for l in self.linears:
+            if l.Wt is None:
+                l.Wt = torch.empty((l.in_dim, l.out_dim), dtype=l.W.dtype, device=self.device)
+            L.lora_prepare_weight(self.desc(l), l.W, l.Wt, stream)
+
+    def groups(self, lr: float, step: int):
+        return L.make_groups([dict(offset=0, n_a=self.n_a, n_b=self.n_b, n_mag=self.n_mag,
+                                   grad_scale=1.0 / self.T, max_norm=self.max_norm, lr=lr,
+                                   step=step)])
+
+    def prepare_ws(self) -> torch.Tensor:
+        g = self.groups(0.0, 0)
+        if not hasattr(self, "_prep_ws"):
+            self._prep_ws = _ws(L.lora_grad_prepare_workspace_size(g), self.device)
+        return self._prep_ws
+
+    # ------------------------------------------------------------------------------------------
+    def forward_backward(self, opt_step: int, per_chunk_calls: bool = False):
+        """Enqueue forward + backward of every linear over all chunks (gradients accumulate)."""
+        main = torch.cuda.current_stream(self.device)
+        if self.streams:
+            ev = torch.cuda.Event()
+            ev.record(main)
+            for s in self.streams:
+                s.wait_event(ev)
+        ct = self.T // self.chunks
+        for i, l in enumerate(self.linears):
+            st = self.streams[i % self.n_streams] if self.streams else main
+            ws = self.ws[i % self.n_streams]
+            d = self.desc(l)
+            if self.dora:
+                L.lora_dora_norm(d, l.W, l.A, l.B, l.norm, st)
+            if per_chunk_calls:
+                spans = [(c, c * ct, ct) for c in range(self.chunks)]
+            else:
+                spans = [(0, 0, self.T)]
+            for (ordinal, t0, n) in spans:
+                ctx = L.make_ctx(opt_step, ordinal, ct)
+                sl = slice(t0, t0 + n)
+                X, dY, Y, dX, H = l.X[sl], l.dY[sl], l.Y[sl], l.dX[sl], l.H[sl]
+                L.lora_forward(d, ctx, n, X, l.W, l.A, l.B, l.mag, l.norm, Y, H, ws, stream=st)
+                L.lora_backward(d, ctx, n, X, l.Wt, l.A, l.B, dY, H, l.mag, l.norm, Y, dX, l.gA,
+                                l.gB, l.gmag, ws, stream=st)
+        if self.streams:
+            for s in self.streams:
+                ev = torch.cuda.Event()
+                ev.record(s)
+                main.wait_event(ev)
+
+    def optimizer_step(self, lr: float, step: int, zero_grads: bool = True):
+        g = self.groups(lr, step)
+        ws = self.prepare_ws()
+        L.lora_grad_prepare(self.arena.grads, g, self.scale_norm, self.status, ws)
+        L.lora_adamw_step(self.arena.params, self.arena.grads, self.arena.m, self.arena.v, g,
+                          self.hp, self.scale_norm, self.status, zero_grads)
+
+    def run(self, opt_step: int, lr: float, per_chunk_calls: bool = False, zero_grads: bool = True):
+        self.forward_backward(opt_step, per_chunk_calls)
+        self.optimizer_step(lr, opt_step, zero_grads)
+
+
+# ----------------------------------------------------------------------------------------------
+@dataclass
+class MultiLinear:
+    proj_id: int
+    X: torch.Tensor
+    W: torch.Tensor
+    dY: torch.Tensor
+    Wt: Optional[torch.Tensor] = None
+    Y: Optional[torch.Tensor] = None
+    dX: Optional[torch.Tensor] = None
+    H: Optional[torch.Tensor] = None
+    A: List[torch.Tensor] = field(default_factory=list)    # per slot, views into the arena
+    B: List[torch.Tensor] = field(default_factory=list)
+    gA: List[torch.Tensor] = field(default_factory=list)
+    gB: List[torch.Tensor] = field(default_factory=list)
+
+    @property
+    def in_dim(self) -> int:
+        return self.W.shape[1]
+
+    @property
+    def out_dim(self) -> int:
+        return self.W.shape[0]
+
+
+class MultiLoraStep:
+    """Slot-keyed multi-LoRA over a shared frozen base: every linear has one adapter per slot;
+    one arena group per slot = [A of the slot over all linears | B of the slot]."""
+
+    def __init__(self, linears: Sequence[MultiLinear], *, slot_ranks: Sequence[int],
+                 slot_scales: Sequence[float], dtype: str, tokens: int, seg_start: torch.Tensor,
+                 seg_slot: torch.Tensor, dropout_p: float = 0.0, seed: int = 0,
+                 max_norm: float = 1.0, hp: Optional[L.lora_adamw_hp] = None, n_streams: int = 1,
+                 device="cuda"):
+        self.linears = list(linears)
+        self.ranks, self.scales = list(slot_ranks), list(slot_scales)
+        self.n_slots = len(self.ranks)
+        self.rmax = max(self.ranks)
+        self.dtype = _DT[dtype]
+        self.T = tokens
+        self.seg_start, self.seg_slot = seg_start, seg_slot
+        self.n_seg = int(seg_slot.numel())
+        self.dropout_p, self.seed = dropout_p, seed
+        self.max_norm = max_norm
+        self.hp = hp if hp is not None else L.make_hp()
+        self.device = torch.device(device)
+        self.slot_off, self.slot_na, self.slot_nb = [], [], []
+        off = 0
+        for r in self.ranks:
+            na = sum(r * l.in_dim for l in self.linears)
+            nb = sum(l.out_dim * r for l in self.linears)
+            self.slot_off.append(off)
+            self.slot_na.append(na)
+            self.slot_nb.append(nb)
+            off += na + nb
+        self.arena = Arena(off, self.device)
+        for s, r in enumerate(self.ranks):
+            oa, ob = self.slot_off[s], self.slot_off[s] + self.slot_na[s]
+            for l in self.linears:
+                l.A.append(self.arena.view("params", oa, (r, l.in_dim)))
+                l.gA.append(self.arena.view("grads", oa, (r, l.in_dim)))
+                oa += r * l.in_dim
+                l.B.append(self.arena.view("params", ob, (l.out_dim, r)))
+                l.gB.append(self.arena.view("grads", ob, (l.out_dim, r)))
+                ob += l.out_dim * r
+        for l in self.linears:
+            act = l.X.dtype
+            if l.Y is None:
+                l.Y = torch.empty((self.T, l.out_dim), dtype=act, device=self.device)
+            if l.dX is None:
+                l.dX = torch.empty((self.T, l.in_dim), dtype=act, device=self.device)
+            if l.H is None:
+                l.H = torch.empty((self.T, self.rmax), dtype=torch.float32, device=self.device)
+        self.n_streams = max(1, n_streams)
+        self.streams = [torch.cuda.Stream(device=self.device) for _ in range(self.n_streams)] \
+            if self.n_streams > 1 else []
+        need = max(L.multi_lora_workspace_size(self.desc(l), self.T, self.n_seg, self.slots(l))
+                   for l in self.linears)
+        if need == 0:
+            raise L.LoraError(L.LORA_ERR_INVALID, "multi_lora_workspace_size")
+        self.ws = [_ws(need, self.device) for _ in range(self.n_streams)]
+        self.scale_norm = torch.zeros(2 * self.n_slots, dtype=torch.float64, device=self.device)
+        self.status = torch.zeros(self.n_slots, dtype=torch.int32, device=self.device)
+
+    def desc(self, l: MultiLinear) -> L.lora_desc:
+        return L.make_desc(l.in_dim, l.out_dim, self.rmax, 0.0, self.dtype, self.dropout_p,
+                           self.seed, 0, l.proj_id, False)
+
+    def slots(self, l: MultiLinear):
+        return L.make_slots([dict(A=l.A[s], B=l.B[s], dA=l.gA[s], dB=l.gB[s], rank=self.ranks[s],
+                                  scale=self.scales[s]) for s in range(self.n_slots)])
+
+    def prepare_weights(self, stream=None):
+        for l in self.linears:
+            if l.Wt is None:
+                l.Wt = torch.empty((l.in_dim, l.out_dim), dtype=l.W.dtype, device=self.device)
+            L.lora_prepare_weight(self.desc(l), l.W, l.Wt, stream)
+
+    def forward_backward(self, opt_step: int = 0):
+        main = torch.cuda.current_stream(self.device)
+        if self.streams:
+            ev = torch.cuda.Event()
+            ev.record(main)
+            for s in self.streams:
+                s.wait_event(ev)
+        for i, l in enumerate(self.linears):
+            st = self.streams[i % self.n_streams] if self.streams else main
+            ws = self.ws[i % self.n_streams]
+            d = self.desc(l)
+            ctx = L.make_ctx(opt_step, 0, 0)
+            sl = self.slots(l)
+            L.multi_lora_forward(d, ctx, self.T, l.X, l.W, self.n_seg, self.seg_start,
+                                 self.seg_slot, sl, l.Y, l.H, ws, stream=st)
+            L.multi_lora_backward(d, ctx, self.T, l.X, l.Wt, self.n_seg, self.seg_start,
+                                  self.seg_slot, sl, l.dY, l.H, l.dX, ws, stream=st)
+        if self.streams:
+            for s in self.streams:
+                ev = torch.cuda.Event()
+                ev.record(s)
+                main.wait_event(ev)
+
+    def groups(self, ready: Sequence[int], gbs: Sequence[int], lrs: Sequence[float],
+               steps: Sequence[int]):
+        return L.make_groups([dict(offset=self.slot_off[s], n_a=self.slot_na[s],
+                                   n_b=self.slot_nb[s], grad_scale=1.0 / gbs[s],
+                                   max_norm=self.max_norm, lr=lrs[s], step=steps[s])
+                              for s in ready])
+
+    def optimizer_step(self, ready: Sequence[int], gbs, lrs, steps, zero_grads: bool = True):
+        """Prepare + AdamW for the slots whose adapter batch is full (one group each); group i of
+        the call reports in scale_norm[2i:2i+2] and status[i]."""
+        if not ready:
+            return
+        g = self.groups(ready, gbs, lrs, steps)
+        if not hasattr(self, "_prep_ws"):
+            full = self.groups(range(self.n_slots), gbs, lrs, steps)
+            self._prep_ws = _ws(L.lora_grad_prepare_workspace_size(full), self.device)
+        L.lora_grad_prepare(self.arena.grads, g, self.scale_norm, self.status, self._prep_ws)
+        L.lora_adamw_step(self.arena.params, self.arena.grads, self.arena.m, self.arena.v, g,
+                          self.hp, self.scale_norm, self.status, zero_grads)

@@ -1,0 +1,257 @@
+/*
+ * lora_gb300.h -- C ABI for one training step of a LoRA-adapted linear layer on GB300 (sm_103a).
+ *
+ * The step (for each adapted linear with frozen W [out, in], adapter A [r, in], B [out, r]):
+ *   forward   Y  = X W^T + s' (Xd A^T) B^T,  Xd = M * X, s' = s / (1 - p)
+ *             ("8. LoRA Fundamentals", How it works: W_eff = W + s B A, s = alpha/r or alpha/sqrt(r))
+ *   DoRA      Y  = (m / n) * (X W^T + s' (Xd A^T) B^T),  n_o = ||W_o + s (B A)_o||, n detached
+ *             ("8. LoRA Fundamentals", How it works: canonical DoRA)
+ *   backward  dY' = dY (or dY * m/n), G = dY' B, dX = dY' W + s' (G A) * M,
+ *             dA += s' G^T Xd, dB += s' dY'^T (Xd A^T), dm += sum_t dY * Y / m
+ *             ("Backward Bug Hunts and Vulkan Tiled GEMM", Bug #1 and Bug #2: the activation
+ *             gradient through the frozen weight and the out_prod LoRA-B gradient)
+ *   prepare   S = sum g^2 (double); non-finite -> reject; c = gamma * min(1, max_norm / norm)
+ *             ("4.3. Training Guide", Gradient accumulation and Gradient clipping)
+ *   AdamW     A-only decoupled decay from the pre-update value with the scheduled lr; LoRA+ ratio
+ *             on B's lr ("4.3. Training Guide", Optimizer and Schedules)
+ *   multi     token segments routed to per-slot adapters, per-slot scale/clip/Adam
+ *             ("Multi-LoRA Training Example (fully-async)", Design)
+ *
+ * Conventions for every call:
+ *   - All tensor pointers are DEVICE pointers owned by the caller, row-major, densely packed.
+ *     Descriptor structs, group tables and slot tables are HOST pointers read during the call.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream). Every call only
+ *     enqueues work on that stream and returns; nothing synchronises unless documented.
+ *   - Argument errors are found on the host before any launch and return a nonzero status with
+ *     nothing enqueued. A launch error returns LORA_ERR_CUDA.
+ *   - The library allocates no device memory. Scratch comes from a caller workspace whose size
+ *     the matching *_workspace_size call gives; a smaller workspace returns LORA_ERR_WORKSPACE.
+ *   - Calls are not thread-safe on one workspace; two calls in flight need two workspaces.
+ *   - Activations X, dY, Y, dX and the frozen W share one dtype (LORA_F32 or LORA_BF16).
+ *     A, B, their gradients, the Adam moments, H and the DoRA vectors are always fp32.
+ *   - Shapes: 1 <= rank <= LORA_MAX_RANK and rank % 4 == 0; in and out multiples of 8;
+ *     all pointers 16-byte aligned (LORA_ERR_ALIGN otherwise).
+ */
+#ifndef LORA_GB300_H
+#define LORA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ---------------------------------------------------------------------------*/
+#define LORA_OK 0
+#define LORA_ERR_INVALID 1      /* null pointer, negative size, bad rank, bad enum */
+#define LORA_ERR_ALIGN 2        /* pointer or row stride not 16-byte aligned */
+#define LORA_ERR_UNSUPPORTED 3  /* valid request this build does not serve (dtype, rank, sizes) */
+#define LORA_ERR_WORKSPACE 4    /* workspace too small */
+#define LORA_ERR_CUDA 5         /* a CUDA launch or runtime call failed */
+#define LORA_ERR_NONFINITE 6    /* device status: a gradient element is NaN or +-Inf */
+
+/* ---- enums ----------------------------------------------------------------------------------*/
+#define LORA_F32 0
+#define LORA_BF16 1
+
+#define LORA_SCHED_CONSTANT 0
+#define LORA_SCHED_WARMUP_COSINE 1
+
+#define LORA_MAX_RANK 64
+#define LORA_MAX_SLOTS 32
+#define LORA_MAX_GROUPS 64
+#define LORA_MAX_CHUNKS_PER_CALL 64
+
+/* One adapted linear. W is [out_dim, in_dim] (nn.Linear layout). */
+typedef struct lora_desc {
+  int64_t in_dim;
+  int64_t out_dim;
+  int32_t rank;        /* r; for multi-LoRA calls: the largest slot rank (H row stride) */
+  float scale;         /* s = lora_scale(alpha, rank, rslora); ignored by multi-LoRA calls */
+  int32_t dtype;       /* LORA_F32 | LORA_BF16 for X, W, dY, Y, dX */
+  float dropout_p;     /* 0 <= p < 1; applies to the adapter branch input only */
+  uint64_t seed;       /* dropout seed */
+  uint32_t layer_id;   /* dropout key fields */
+  uint32_t proj_id;    /* < 65536 */
+  int32_t dora;        /* 1: DoRA row-magnitude mode (single-adapter calls only) */
+} lora_desc;
+
+/* Where the call's tokens sit in the optimizer step (dropout key fields). Token t of a call
+ * belongs to accumulation chunk accum_ordinal + t / chunk_tokens at position t % chunk_tokens;
+ * chunk_tokens == 0 means all T tokens are one chunk. At most LORA_MAX_CHUNKS_PER_CALL chunks
+ * per call, and accum_ordinal + chunks <= 65536. */
+typedef struct lora_ctx {
+  uint64_t opt_step;
+  uint32_t accum_ordinal;
+  int64_t chunk_tokens;
+} lora_ctx;
+
+/* One slot of the multi-LoRA page table ("Multi-LoRA Training Example", Design: slot-keyed
+ * adapter page table with per-slot rank/alpha). All pointers device, fp32. */
+typedef struct lora_slot {
+  const float* A;   /* [rank, in_dim] */
+  const float* B;   /* [out_dim, rank] */
+  float* dA;        /* [rank, in_dim], accumulated (+=) by multi_lora_backward */
+  float* dB;        /* [out_dim, rank], accumulated (+=) */
+  int32_t rank;     /* 1..desc.rank, multiple of 4 */
+  float scale;      /* s_k = lora_scale(alpha_k, rank_k, rslora) */
+} lora_slot;
+
+/* A group of adapter parameters stored contiguously in the flat fp32 arenas (params, grads,
+ * m, v share one layout): [n_a elements of kind A | n_b of kind B | n_mag DoRA magnitudes]
+ * starting at `offset`. One group = one clip norm and one Adam clock: the whole model for a
+ * single adapter set (global clip), or one slot for multi-LoRA. */
+typedef struct lora_group {
+  int64_t offset;
+  int64_t n_a;
+  int64_t n_b;
+  int64_t n_mag;
+  double grad_scale;   /* gamma: 1 / prediction tokens, or 1 / adapter_global_batch_size */
+  float max_norm;      /* 0 disables clipping (normalisation by gamma still applies) */
+  float lr;            /* scheduled learning rate of this update (lora_lr_at) */
+  int64_t step;        /* completed updates of this group before this one (bias correction) */
+} lora_group;
+
+typedef struct lora_adamw_hp {
+  float beta1;         /* 0.9 */
+  float beta2;         /* 0.999 */
+  float eps;           /* 1e-8, added outside the square root */
+  float weight_decay;  /* applied to kind A only */
+  float plus_ratio;    /* LoRA+: B's lr = lr * plus_ratio */
+} lora_adamw_hp;
+
+/* ---- host helpers ---------------------------------------------------------------------------*/
+/* Static string for a status code. */
+const char* lora_status_string(int status);
+
+/* s = alpha / rank, or alpha / sqrt(rank) when rslora != 0 ("8. LoRA Fundamentals", How it
+ * works). Returns 0 for rank <= 0. */
+float lora_scale(float alpha, int32_t rank, int32_t rslora);
+
+/* Learning rate at optimizer-update index `step` ("4.3. Training Guide", Schedules): constant,
+ * or linear warmup base*(step+1)/warmup then cosine from base to min_lr over total - warmup
+ * updates (progress clamped to 1). Returns NaN for an unknown kind. */
+double lora_lr_at(int32_t kind, double base, uint64_t step, uint64_t warmup, uint64_t total,
+                  double min_lr);
+
+/* Workspace bytes for lora_forward / lora_backward / lora_dora_norm on T tokens. */
+size_t lora_workspace_size(const lora_desc* d, int64_t T);
+
+/* ---- frozen-weight preparation (once per frozen W, not per step) ----------------------------*/
+/* W_t = W^T ([in_dim, out_dim]): the layout the dX product reads, kept resident beside W so
+ * that both frozen products stream K-contiguous operands. */
+int lora_prepare_weight(const lora_desc* d, const void* W, void* W_t, void* stream);
+
+/* DoRA row norm n_o = || W_o + s (B A)_o ||_2 for the current A, B (fp32 [out_dim]); call once
+ * per optimizer step before the first forward ("8. LoRA Fundamentals", How it works, and its
+ * norm-refresh event). */
+int lora_dora_norm(const lora_desc* d, const void* W, const float* A, const float* B,
+                   float* norm_out, void* stream);
+
+/* ---- forward / backward (one adapted linear, T tokens) --------------------------------------*/
+/* Y [T, out] = X W^T + Hs B^T, then * (dora_m / dora_n) per column in DoRA mode.
+ * H_save [T, rank] fp32 receives Hs = s' (Xd A^T) (the scaled shrink), which lora_backward
+ * reads. dora_m, dora_n: [out] fp32, required iff desc.dora. */
+int lora_forward(const lora_desc* d, const lora_ctx* c, int64_t T, const void* X, const void* W,
+                 const float* A, const float* B, const float* dora_m, const float* dora_n,
+                 void* Y, float* H_save, void* ws, size_t ws_bytes, void* stream);
+
+/* dX [T, in] = dY' W + (Gs A) * M with Gs = s' dY' B (written, may be NULL to skip dX);
+ * dA [r, in] += Gs^T Xd; dB [out, r] += dY'^T H_save; dm [out] += sum_t dY * Y_save / m (DoRA).
+ * W_t from lora_prepare_weight. Y_save (the forward's Y) and dm are required iff desc.dora.
+ * Accumulation over chunks is the caller's sequence of calls (or one call with chunk_tokens);
+ * the token sums inside one call are reduced in a fixed order, so reruns are bitwise equal. */
+int lora_backward(const lora_desc* d, const lora_ctx* c, int64_t T, const void* X,
+                  const void* W_t, const float* A, const float* B, const void* dY,
+                  const float* H_save, const float* dora_m, const float* dora_n,
+                  const void* Y_save, void* dX, float* dA, float* dB, float* dm, void* ws,
+                  size_t ws_bytes, void* stream);
+
+/* ---- grad prepare and AdamW over flat fp32 arenas -------------------------------------------*/
+/* Workspace bytes for lora_grad_prepare over these groups. */
+size_t lora_grad_prepare_workspace_size(int32_t n_groups, const lora_group* groups);
+
+/* Pass 1 of the two-pass clip for each group: S_g = sum of squares of grads[offset, offset+n)
+ * accumulated in double (per-thread exact float-float partials combined in double), then
+ *   status[g] = LORA_ERR_NONFINITE if any element is NaN or +-Inf, else LORA_OK;
+ *   scale_norm[2g]   = c = gamma * max_norm / norm if max_norm > 0 and norm > max_norm, else gamma
+ *   scale_norm[2g+1] = norm = gamma * sqrt(S_g)
+ * d_scale_norm [2 * n_groups] double and d_status [n_groups] int32 are device outputs.
+ * 1 <= n_groups <= LORA_MAX_GROUPS. Groups must not overlap. */
+int lora_grad_prepare(const float* grads, int32_t n_groups, const lora_group* groups,
+                      double* d_scale_norm, int32_t* d_status, void* ws, size_t ws_bytes,
+                      void* stream);
+
+/* Pass 2 fused with the AdamW update, for every group whose device status is LORA_OK (groups
+ * with another status are left untouched: params, moments and grads):
+ *   g_hat = c g; m = b1 m + (1-b1) g_hat; v = b2 v + (1-b2) g_hat^2; k = step + 1;
+ *   u = (m / (1 - b1^k)) / (sqrt(v / (1 - b2^k)) + eps)
+ *   A:   p -= lr u + lr wd p      B: p -= lr plus_ratio u      MAG: p -= lr u
+ * zero_grads != 0 also clears the group's gradients after reading them. The caller advances
+ * each group's step (and re-evaluates lr) only for groups whose status was LORA_OK. */
+int lora_adamw_step(float* params, float* grads, float* m, float* v, int32_t n_groups,
+                    const lora_group* groups, const lora_adamw_hp* hp, const double* d_scale_norm,
+                    const int32_t* d_status, int32_t zero_grads, void* stream);
+
+/* ---- slot-keyed multi-LoRA ------------------------------------------------------------------*/
+/* Segments: segment k covers tokens [seg_start[k], seg_start[k+1]) (device int32 [n_seg + 1],
+ * non-decreasing, within [0, T]) and uses slot seg_slot[k] (device int32 [n_seg]). Tokens in no
+ * segment, or in a segment whose slot id is outside [0, n_slots), get no adapter (frozen output
+ * only). `slots` is a host array of n_slots entries (1 <= n_slots <= LORA_MAX_SLOTS); desc.rank
+ * is the largest slot rank and the row stride of H_save. desc.dora must be 0. */
+size_t multi_lora_workspace_size(const lora_desc* d, int64_t T, int32_t n_seg, int32_t n_slots,
+                                 const lora_slot* slots);
+
+int multi_lora_forward(const lora_desc* d, const lora_ctx* c, int64_t T, const void* X,
+                       const void* W, int32_t n_seg, const int32_t* d_seg_start,
+                       const int32_t* d_seg_slot, int32_t n_slots, const lora_slot* slots,
+                       void* Y, float* H_save, void* ws, size_t ws_bytes, void* stream);
+
+/* dX may be NULL. Each slot's dA/dB accumulate that slot's tokens with weight 1; per-slot
+ * 1/adapter_global_batch_size, clip and Adam are lora_grad_prepare / lora_adamw_step with one
+ * group per ready slot. */
+int multi_lora_backward(const lora_desc* d, const lora_ctx* c, int64_t T, const void* X,
+                        const void* W_t, int32_t n_seg, const int32_t* d_seg_start,
+                        const int32_t* d_seg_slot, int32_t n_slots, const lora_slot* slots,
+                        const void* dY, const float* H_save, void* dX, void* ws,
+                        size_t ws_bytes, void* stream);
+
+/* ---- test hooks (not part of the timed path) ------------------------------------------------*/
+/* Keep mask M [T, in_dim] as uint8 (1 = kept), exactly as the kernels regenerate it. */
+int lora_dropout_mask(const lora_desc* d, const lora_ctx* c, int64_t T, uint8_t* d_mask,
+                      void* stream);
+
+/* Slot of every token (int32 [T], -1 = no adapter) under the segment rules above. */
+int multi_lora_token_slots(int64_t T, int32_t n_seg, const int32_t* d_seg_start,
+                           const int32_t* d_seg_slot, int32_t n_slots, int32_t* d_token_slot,
+                           void* stream);
+
+/* ---- instrumentation (benchmark and tests; not part of the method) -------------------------*/
+/* Kernel classes for lora_profile_arm. */
+#define LORA_PROF_NONE 0
+#define LORA_PROF_FROZEN_FWD 1   /* frozen forward product with the fused up-projection */
+#define LORA_PROF_FROZEN_DX 2    /* frozen dX product with the fused LoRA dX term */
+#define LORA_PROF_SHRINK 3       /* Hs = s' Xd A^T */
+#define LORA_PROF_G 4            /* Gs = s' dY' B */
+#define LORA_PROF_RED_DB 5       /* dB token-reduction partials */
+#define LORA_PROF_RED_DA 6       /* dA token-reduction partials */
+#define LORA_PROF_PREPARE 7      /* grad-prepare pass 1 */
+#define LORA_PROF_ADAMW 8        /* fused clip + AdamW */
+
+/* Arm event brackets: the next n launches of `kernel_class` record start_events[i] before and
+ * stop_events[i] after launch i on the launching stream (cudaEvent_t handles, caller-owned).
+ * Re-arming replaces the previous set; n == 0 disarms. Under stream capture the records become
+ * graph nodes and fire on every replay. Not thread-safe with concurrent arming. */
+int lora_profile_arm(int32_t kernel_class, void* const* start_events, void* const* stop_events,
+                     int32_t n);
+/* How many armed brackets have been used so far. */
+int32_t lora_profile_used(void);
+/* Kernel launches enqueued by this library since it was loaded (all classes). */
+uint64_t lora_launch_counter(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LORA_GB300_H */

@@ -449,3 +449,12 @@ def run_single_step(problems: Dict[object, dict], state: Dict[object, AdapterSta
             ns.mag, ns.mM, ns.vM = adamw_update(st.mag, gM, st.mM, st.vM, KIND_MAG, prep.scale, hp)
         new_state[key] = ns
     return StepResult(prep, grads, new_state, outputs)
+
+
+def lora_adapter_grads(X, A, B, dY, s: float, keep=None, q: float = 1.0):
+    """dA and dB alone (no frozen product needed): dA = s q (dY B)^T Xd, dB = s q dY^T (Xd A^T).
+    Same definitions as lora_backward, for cases where the frozen products are too large."""
+    X, A, B, dY = _f64(X), _f64(A), _f64(B), _f64(dY)
+    Xd = X if keep is None else keep * X
+    G = dY @ B
+    return (s * q) * (G.T @ Xd), (s * q) * (dY.T @ (Xd @ A.T))

@@ -1,0 +1,341 @@
+"""CUDA path vs the CPU oracle, element by element on the same seeded inputs.
+
+Every case runs through the C ABI (via the ctypes binding and the step orchestration). Integer
+work (dropout masks, token routing) must be bit-exact; floating point within the per-tensor
+max-relative-error bars of the north-star specification: 1e-5 for fp32 frozen-W paths, 2e-2 on
+outputs and gradients and 1e-2 on the post-step A/B for bf16 frozen-W paths.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import lora_inputs as LI
+from oracle import lora_oracle as O
+from tests.helpers import (TOL_BF16, TOL_BF16_STEP, TOL_F32, build_single, lr_for, rel_err, to64)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from bwd_adapter_adamw_gb300 import binding
+    return binding
+
+
+def _tols(cfg):
+    return (TOL_F32, TOL_F32) if cfg.dtype == "f32" else (TOL_BF16, TOL_BF16_STEP)
+
+
+# ------------------------------------------------------------------------------------ integer work
+@pytest.mark.parametrize("p,seed,step,ordinal,layer,proj,T,in_dim,ct", [
+    (0.1, 1234, 25, 0, 0, 0, 64, 1536, 0),
+    (0.5, 7, 3, 2, 31, 6, 100, 72, 25),
+    (0.9, 2**63 + 5, 2**40, 65000, 2**31, 65535, 33, 8, 11),
+    (0.0, 1, 1, 1, 1, 1, 9, 16, 0),
+])
+def test_dropout_mask_bit_exact(L, p, seed, step, ordinal, layer, proj, T, in_dim, ct):
+    d = L.make_desc(in_dim, 8, 4, 1.0, L.LORA_BF16, p, seed, layer, proj)
+    c = L.make_ctx(step, ordinal, ct)
+    mask = torch.empty((T, in_dim), dtype=torch.uint8, device="cuda")
+    L.lora_dropout_mask(d, c, T, mask)
+    want = O.dropout_keep(p, seed, step, ordinal, layer, proj, T, in_dim, ct)
+    got = mask.cpu().numpy().astype(np.float64)
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("T,starts,slots,n_slots", [
+    (16384, None, None, 8),
+    (100, [0, 10, 10, 40, 90], [3, 1, 0, 2], 4),
+    (50, [5, 20, 15, 45, 60], [0, 1, 9, -1], 2),   # gaps, overlap, out-of-range and tail
+    (7, [0, 7], [0], 1),
+])
+def test_token_slots_bit_exact(L, T, starts, slots, n_slots):
+    if starts is None:
+        r = LI.make_routing(LI.CONFIGS["c5"], T)
+        starts, slots = r.seg_start.tolist(), r.seg_slot.tolist()
+    ss = torch.tensor(starts, dtype=torch.int32, device="cuda")
+    sl = torch.tensor(slots, dtype=torch.int32, device="cuda")
+    out = torch.full((T,), 123, dtype=torch.int32, device="cuda")
+    L.multi_lora_token_slots(T, len(slots), ss, sl, n_slots, out)
+    want = O.token_slots(T, starts, slots, n_slots)
+    assert np.array_equal(out.cpu().numpy(), want)
+
+
+# ------------------------------------------------------------------------- single-adapter steps
+def _check_step(cfg, step, problems, state, s, hp_o, per_chunk):
+    step.run(cfg.opt_step, hp_o.lr, per_chunk_calls=per_chunk, zero_grads=False)
+    torch.cuda.synchronize()
+    ref = O.run_single_step(problems, state, s=s, chunks=cfg.chunks, p=cfg.dropout_p,
+                            seed=cfg.dropout_seed, opt_step=cfg.opt_step, max_norm=cfg.max_norm,
+                            hp=hp_o, dora=cfg.dora)
+    tol, tol_step = _tols(cfg)
+    q = O.dropout_q(cfg.dropout_p) if cfg.dropout_p > 0 else 1.0
+    errs = {}
+    for lin in step.linears:
+        key = (lin.layer, lin.proj_id)
+        outs = ref.outputs[key]
+        Y = np.concatenate([o[0] for o in outs])
+        dX = np.concatenate([o[1] for o in outs])
+        H = np.concatenate([o[2] for o in outs])
+        gA, gB, gM = ref.grads[key]
+        errs[(key, "Y")] = rel_err(lin.Y, Y)
+        errs[(key, "dX")] = rel_err(lin.dX, dX)
+        errs[(key, "H")] = rel_err(lin.H, s * q * H)
+        errs[(key, "dA")] = rel_err(lin.gA, gA)
+        errs[(key, "dB")] = rel_err(lin.gB, gB)
+        if cfg.dora:
+            errs[(key, "dm")] = rel_err(lin.gmag, gM)
+    for k, e in errs.items():
+        assert e <= tol, (k, e)
+    assert int(step.status.item()) == O.STATUS_OK
+    sn = step.scale_norm.cpu().numpy()
+    assert abs(sn[0] - ref.prepared.scale) <= 1e-5 * abs(ref.prepared.scale)
+    assert abs(sn[1] - ref.prepared.norm) <= 1e-5 * abs(ref.prepared.norm)
+    for lin in step.linears:
+        ns = ref.new_state[(lin.layer, lin.proj_id)]
+        assert rel_err(lin.A, ns.A) <= tol_step, ("A", lin.layer, lin.proj_id)
+        assert rel_err(lin.B, ns.B) <= tol_step, ("B", lin.layer, lin.proj_id)
+        if cfg.dora:
+            assert rel_err(lin.mag, ns.mag) <= tol_step
+    na, nb = step.n_a, step.n_b
+    mA = np.concatenate([ref.new_state[(l.layer, l.proj_id)].mA.ravel() for l in step.linears])
+    vB = np.concatenate([ref.new_state[(l.layer, l.proj_id)].vB.ravel() for l in step.linears])
+    assert rel_err(step.arena.m[:na], mA) <= tol_step
+    assert rel_err(step.arena.v[na:na + nb], vB) <= tol_step
+    return ref, errs
+
+
+SINGLE_CASES = {
+    "c1": ("c1", [0], [0], None, {}),
+    "c1_ragged_f32": ("c1", [0], [0], 37, dict(rank=12, chunks=1, dropout_p=0.3, dropout_seed=5,
+                                               projs=(LI.Proj("lin", 72, 40, "x"),))),
+    "ragged_bf16": ("c3", [0], [0], 203, dict(rank=4, chunks=1, projs=(LI.Proj("lin", 136, 264, "x"),),
+                                              opt_step=3)),
+    "c3": ("c3", [0], [0], None, {}),
+    "c2_two_layers": ("c2", [0, 21], [0, 1], None, {}),
+    "c4_small": ("c4", [0], [1, 6], 512, {}),
+    "c4dora_small": ("c4dora", [3], [2, 4], 256, dict(chunks=2)),
+}
+
+
+@pytest.mark.parametrize("name", list(SINGLE_CASES))
+@pytest.mark.parametrize("per_chunk", [False, True])
+def test_single_step_parity(L, name, per_chunk):
+    base, layers, projs, T, ov = SINGLE_CASES[name]
+    cfg = LI.with_overrides(LI.CONFIGS[base], **ov) if ov else LI.CONFIGS[base]
+    if per_chunk and cfg.chunks == 1:
+        pytest.skip("one chunk")
+    step, problems, state, s, hp_o = build_single(cfg, layers, projs, tokens=T)
+    _check_step(cfg, step, problems, state, s, hp_o, per_chunk)
+
+
+def test_c2_two_consecutive_steps_from_zero_B(L):
+    """TinyLlama-shaped config: B = 0 at step 0 (so dA = 0 and A only decays), then the second step
+    from the post-step state, both against the oracle."""
+    cfg = LI.CONFIGS["c2"]
+    step, problems, state, s, hp_o = build_single(cfg, [5], [0, 1])
+    ref, errs = _check_step(cfg, step, problems, state, s, hp_o, False)
+    for lin in step.linears:
+        assert float(lin.gA.abs().max()) == 0.0
+    # second step: zero the GPU gradients, advance the clock on both sides
+    step.arena.grads.zero_()
+    cfg2 = LI.with_overrides(cfg, opt_step=1)
+    hp2 = O.AdamHP(lr=lr_for(cfg2), beta1=cfg.beta1, beta2=cfg.beta2, eps=cfg.eps, wd=cfg.wd,
+                   plus_ratio=cfg.plus_ratio, step=1)
+    _check_step(cfg2, step, problems, ref.new_state, s, hp2, False)
+
+
+def test_nonfinite_gradient_rejects_the_step(L):
+    cfg = LI.CONFIGS["c1"]
+    step, problems, state, s, hp_o = build_single(cfg, [0], [0])
+    step.linears[0].dY[3, 7] = float("nan")
+    before = [t.clone() for t in (step.arena.params, step.arena.m, step.arena.v)]
+    step.run(0, hp_o.lr, zero_grads=True)
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == L.LORA_ERR_NONFINITE
+    for a, b in zip(before, (step.arena.params, step.arena.m, step.arena.v)):
+        assert torch.equal(a, b)
+    # gradients are left in place for inspection
+    assert not torch.isfinite(step.arena.grads).all()
+
+
+def test_inf_gradient_rejects_and_huge_finite_does_not(L):
+    from bwd_adapter_adamw_gb300.step import Arena
+    g = torch.zeros(1000, device="cuda")
+    groups = L.make_groups([dict(offset=0, n_a=500, n_b=500, grad_scale=1.0, max_norm=1.0)])
+    ws = torch.empty(L.lora_grad_prepare_workspace_size(groups), dtype=torch.uint8, device="cuda")
+    sn = torch.zeros(2, dtype=torch.float64, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    g[17] = float("inf")
+    L.lora_grad_prepare(g, groups, sn, st, ws)
+    assert int(st.item()) == L.LORA_ERR_NONFINITE
+    g[17] = 3e30   # square overflows fp32 but not double
+    L.lora_grad_prepare(g, groups, sn, st, ws)
+    torch.cuda.synchronize()
+    assert int(st.item()) == L.LORA_OK
+    ref = O.grad_prepare([g.cpu().numpy()], 1.0, 1.0)
+    assert abs(sn[1].item() - ref.norm) <= 1e-12 * ref.norm
+
+
+def test_rerun_is_bitwise_identical(L):
+    cfg = LI.with_overrides(LI.CONFIGS["c3"], tokens=1024)
+    outs = []
+    for _ in range(2):
+        step, problems, state, s, hp_o = build_single(cfg, [0], [0])
+        step.run(cfg.opt_step, hp_o.lr, zero_grads=False)
+        torch.cuda.synchronize()
+        lin = step.linears[0]
+        outs.append([t.clone() for t in (lin.Y, lin.dX, lin.H, step.arena.grads, step.arena.params,
+                                         step.arena.m, step.arena.v)])
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
+
+
+def test_zero_adapter_is_a_noop_and_dA_is_zero(L):
+    cfg = LI.with_overrides(LI.CONFIGS["c3"], tokens=512, b_zero=True, dropout_p=0.0)
+    step, problems, state, s, hp_o = build_single(cfg, [0], [0])
+    step.forward_backward(0)
+    torch.cuda.synchronize()
+    lin = step.linears[0]
+    assert float(lin.gA.abs().max()) == 0.0
+    pr = problems[(0, 0)]
+    ref = to64(pr["X"]) @ to64(pr["W"]).T
+    assert rel_err(lin.Y, ref) <= TOL_BF16
+
+
+def test_multi_stream_matches_single_stream(L):
+    cfg = LI.with_overrides(LI.CONFIGS["c4"], tokens=256, chunks=2)
+    res = []
+    for ns in (1, 3):
+        step, *_ = build_single(cfg, [0, 1], [0, 3], n_streams=ns)
+        step.run(0, 1e-4, zero_grads=False)
+        torch.cuda.synchronize()
+        res.append((step.arena.params.clone(), step.arena.grads.clone(),
+                    torch.cat([l.Y.float().flatten() for l in step.linears])))
+    for a, b in zip(*res):
+        assert torch.equal(a, b)
+
+
+# --------------------------------------------------------------------------------- multi-LoRA
+def _build_multi(cfg, proj_idx, T, device="cuda"):
+    from bwd_adapter_adamw_gb300 import binding as L
+    from bwd_adapter_adamw_gb300.step import MultiLinear, MultiLoraStep
+    r = LI.make_routing(cfg, T)
+    ranks = r.slot_rank
+    scales = [O.lora_scale(a, rk, cfg.rslora) for a, rk in zip(r.slot_alpha, ranks)]
+    lins, host = [], {}
+    for pi in proj_idx:
+        pr = cfg.projs[pi]
+        X = LI.make_x(cfg, 0, pr, tokens=T)
+        W = LI.make_w(cfg, 0, pr)
+        dY = LI.make_dy(cfg, 0, pr, tokens=T)
+        lins.append(MultiLinear(pi, X.to(device), W.to(device), dY.to(device)))
+        slots = [(LI.make_a(cfg, 0, pr, rank=rk, tag=f"slot{k}"),
+                  LI.make_b(cfg, 0, pr, rank=rk, tag=f"slot{k}")) for k, rk in enumerate(ranks)]
+        host[pi] = dict(X=X, W=W, dY=dY, slots=slots)
+    hp = L.make_hp(cfg.beta1, cfg.beta2, cfg.eps, cfg.wd, cfg.plus_ratio)
+    step = MultiLoraStep(lins, slot_ranks=ranks, slot_scales=scales, dtype=cfg.dtype, tokens=T,
+                         seg_start=torch.tensor(r.seg_start, device=device),
+                         seg_slot=torch.tensor(r.seg_slot, device=device),
+                         dropout_p=cfg.dropout_p, seed=cfg.dropout_seed, max_norm=cfg.max_norm,
+                         hp=hp, device=device)
+    for lin in step.linears:
+        for k, (A, B) in enumerate(host[lin.proj_id]["slots"]):
+            lin.A[k].copy_(A)
+            lin.B[k].copy_(B)
+    step.prepare_weights()
+    torch.cuda.synchronize()
+    return step, host, r, scales
+
+
+@pytest.mark.parametrize("T,proj_idx,p", [(1500, [0, 3, 6], 0.0), (700, [1], 0.25)])
+def test_multi_lora_parity(L, T, proj_idx, p):
+    cfg = LI.with_overrides(LI.CONFIGS["c5"], dropout_p=p, dropout_seed=99)
+    step, host, r, scales = _build_multi(cfg, proj_idx, T)
+    step.forward_backward(0)
+    torch.cuda.synchronize()
+    tok = O.token_slots(T, r.seg_start, r.seg_slot, len(r.slot_rank))
+    q = O.dropout_q(p) if p > 0 else 1.0
+    grads = {}
+    for lin in step.linears:
+        h = host[lin.proj_id]
+        keep = O.dropout_keep(p, cfg.dropout_seed, 0, 0, 0, lin.proj_id, T, lin.in_dim) if p > 0 else None
+        slots = [O.SlotTensors(A, B, sc) for (A, B), sc in zip(h["slots"], scales)]
+        Y, H = O.multi_lora_forward(h["X"], h["W"], slots, tok, keep, q)
+        dX, dA, dB = O.multi_lora_backward_vectorised(h["X"], h["W"], h["dY"], slots, tok, keep, q)
+        assert rel_err(lin.Y, Y) <= TOL_BF16
+        Hs = H.copy()
+        for t in range(T):
+            if tok[t] >= 0:
+                Hs[t] *= scales[tok[t]] * q
+        assert rel_err(lin.H, Hs) <= TOL_BF16
+        assert rel_err(lin.dX, dX) <= TOL_BF16
+        for k in range(len(slots)):
+            if np.any(tok == k):
+                assert rel_err(lin.gA[k], dA[k]) <= TOL_BF16, ("dA", k)
+                assert rel_err(lin.gB[k], dB[k]) <= TOL_BF16, ("dB", k)
+            else:
+                assert float(lin.gA[k].abs().max()) == 0.0
+        grads[lin.proj_id] = (dA, dB)
+    # per-slot prepare + Adam for the slots whose adapter batch is full
+    ready = [k for k in range(len(r.slot_rank)) if LI.slot_ready(r, k)]
+    lrs = [cfg.lr] * len(r.slot_rank)
+    before = step.arena.params.clone()
+    step.optimizer_step(ready, r.slot_gbs, lrs, r.slot_step, zero_grads=False)
+    torch.cuda.synchronize()
+    st = step.status.cpu().numpy()
+    for i, k in enumerate(ready):
+        assert st[i] == O.STATUS_OK
+        glist = []
+        for lin in step.linears:
+            glist += [grads[lin.proj_id][0][k], grads[lin.proj_id][1][k]]
+        prep = O.grad_prepare([g.astype(np.float32) for g in glist], 1.0 / r.slot_gbs[k], cfg.max_norm)
+        hp = O.AdamHP(lr=cfg.lr, beta1=cfg.beta1, beta2=cfg.beta2, eps=cfg.eps, wd=cfg.wd,
+                      plus_ratio=cfg.plus_ratio, step=r.slot_step[k])
+        for lin in step.linears:
+            A0, B0 = host[lin.proj_id]["slots"][k]
+            z = np.zeros
+            A1, _, _ = O.adamw_update(A0, grads[lin.proj_id][0][k].astype(np.float32),
+                                      z(A0.shape), z(A0.shape), O.KIND_A, prep.scale, hp)
+            B1, _, _ = O.adamw_update(B0, grads[lin.proj_id][1][k].astype(np.float32),
+                                      z(B0.shape), z(B0.shape), O.KIND_B, prep.scale, hp)
+            assert rel_err(lin.A[k], A1) <= TOL_BF16_STEP
+            assert rel_err(lin.B[k], B1) <= TOL_BF16_STEP
+    not_ready = [k for k in range(len(r.slot_rank)) if k not in ready]
+    for k in not_ready:
+        o, n = step.slot_off[k], step.slot_na[k] + step.slot_nb[k]
+        assert torch.equal(step.arena.params[o:o + n], before[o:o + n])
+
+
+def test_multi_single_slot_equals_single_lora(L):
+    """One slot holding one full-T segment gives the single-adapter result (same kernels, same
+    reduction order), so the two paths agree bitwise."""
+    from bwd_adapter_adamw_gb300.step import MultiLinear, MultiLoraStep
+    cfg = LI.with_overrides(LI.CONFIGS["c3"], tokens=640, dropout_p=0.0)
+    step, problems, state, s, hp_o = build_single(cfg, [0], [0])
+    step.forward_backward(0)
+    lin = step.linears[0]
+    ml = MultiLinear(0, lin.X, lin.W, lin.dY, Wt=lin.Wt)
+    ms = MultiLoraStep([ml], slot_ranks=[cfg.rank], slot_scales=[s], dtype="bf16", tokens=640,
+                       seg_start=torch.tensor([0, 640], dtype=torch.int32, device="cuda"),
+                       seg_slot=torch.tensor([0], dtype=torch.int32, device="cuda"))
+    ml.A[0].copy_(lin.A)
+    ml.B[0].copy_(lin.B)
+    ms.forward_backward(0)
+    torch.cuda.synchronize()
+    assert torch.equal(ml.Y, lin.Y)
+    assert torch.equal(ml.dX, lin.dX)
+    assert torch.equal(ml.gA[0], lin.gA)
+    assert torch.equal(ml.gB[0], lin.gB)
+
+
+# ------------------------------------------------------------------- schedule through the ABI
+def test_lr_schedule_and_scale_match_oracle(L):
+    for k in (0, 5, 9, 10, 25, 55, 99, 100, 250):
+        assert L.lora_lr_at(1, 1e-4, k, 10, 100, 1e-6) == pytest.approx(
+            O.lr_at("cosine", 1e-4, k, 10, 100, 1e-6), rel=1e-15)
+    assert L.lora_scale(128, 64, True) == O.lora_scale(128, 64, True)
