@@ -320,6 +320,9 @@ def run_ours(args):
     n_prof = (layers if not cfg.multi else 1) * len(cfg.projs)
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(n_prof)]
     stops = [torch.cuda.Event(enable_timing=True) for _ in range(n_prof)]
+    for e in starts + stops:   # torch creates the CUDA event on first record
+        e.record()
+    torch.cuda.synchronize()
     L.lora_profile_arm(prof_class, starts, stops)
     graph = None
     if not args.no_graph:

@@ -61,8 +61,8 @@ class lora_group(C.Structure):
 
 
 class lora_adamw_hp(C.Structure):
-    _fields_ = [("beta1", C.c_float), ("beta2", C.c_float), ("eps", C.c_float),
-                ("weight_decay", C.c_float), ("plus_ratio", C.c_float)]
+    _fields_ = [("beta1", C.c_double), ("beta2", C.c_double), ("eps", C.c_double),
+                ("weight_decay", C.c_double), ("plus_ratio", C.c_double)]
 
 
 def _load() -> C.CDLL:
@@ -96,6 +96,7 @@ def _load() -> C.CDLL:
         "lora_profile_arm": (C.c_int, [I32, C.POINTER(C.c_void_p), C.POINTER(C.c_void_p), I32]),
         "lora_profile_used": (I32, []),
         "lora_launch_counter": (U64, []),
+        "lora_last_cuda_error": (C.c_char_p, []),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -110,7 +111,7 @@ EXPORTED = ("lora_status_string", "lora_scale", "lora_lr_at", "lora_workspace_si
             "lora_grad_prepare_workspace_size", "lora_grad_prepare", "lora_adamw_step",
             "multi_lora_workspace_size", "multi_lora_forward", "multi_lora_backward",
             "lora_dropout_mask", "multi_lora_token_slots", "lora_profile_arm",
-            "lora_profile_used", "lora_launch_counter")
+            "lora_profile_used", "lora_launch_counter", "lora_last_cuda_error")
 
 LORA_PROF_NONE = 0
 LORA_PROF_FROZEN_FWD = 1
@@ -146,6 +147,8 @@ def _stream(stream) -> Optional[int]:
 
 
 def _check(status: int, where: str) -> int:
+    if status == LORA_ERR_CUDA:
+        raise LoraError(status, f"{where} [{_lib.lora_last_cuda_error().decode()}]")
     if status != LORA_OK:
         raise LoraError(status, where)
     return status
@@ -288,6 +291,9 @@ def lora_profile_arm(kernel_class: int, start_events: Sequence, stop_events: Seq
     """Bracket the next len(start_events) launches of one kernel class with torch.cuda.Event
     pairs (recorded on the launching stream)."""
     n = len(start_events)
+    if any(not e.cuda_event for e in list(start_events) + list(stop_events)):
+        raise ValueError("lora_profile_arm: record each event once first (torch creates the "
+                         "CUDA event lazily)")
     starts = (C.c_void_p * max(n, 1))(*[e.cuda_event for e in start_events])
     stops = (C.c_void_p * max(n, 1))(*[e.cuda_event for e in stop_events])
     return _check(_lib.lora_profile_arm(kernel_class, starts, stops, n), "lora_profile_arm")

@@ -27,12 +27,22 @@ struct Carve {
 
 inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? LORA_OK : LORA_ERR_CUDA; }
+thread_local cudaError_t t_last_error = cudaSuccess;
 
-#define LORA_TRY(expr)                         \
-  do {                                         \
-    cudaError_t _e = (expr);                   \
-    if (_e != cudaSuccess) return LORA_ERR_CUDA; \
+// Errors left behind by other code in this thread (cudaGetLastError reports the most recent
+// error of any runtime call) are cleared before our launches, so that a LORA_ERR_CUDA is ours.
+inline void clear_stale() { (void)cudaGetLastError(); }
+
+inline int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return LORA_OK;
+  t_last_error = e;
+  return LORA_ERR_CUDA;
+}
+
+#define LORA_TRY(expr)                                 \
+  do {                                                 \
+    cudaError_t _e = (expr);                           \
+    if (_e != cudaSuccess) return cuda_status(_e);     \
   } while (0)
 
 int64_t max_gemm_items(int64_t T, int32_t n_seg) {
@@ -178,6 +188,7 @@ int run_forward(const lora_desc* d, const DropParams& dp, int64_t T, const void*
                 const float* ratio_src_m, const float* ratio_src_n, void* Y, float* H, void* ws,
                 cudaStream_t st) {
   Layout L = carve(d, T, n_seg, s.rank_sum, false, ws);
+  clear_stale();
   LORA_TRY(launch_make_items(T, n_seg, seg_start, seg_slot, s.n, L.gitems, L.gcount, (int32_t)L.gmax,
                              L.ritems, L.rcount, (int32_t)L.rmax, st));
   const float q = dropout_q(d);
@@ -225,6 +236,7 @@ int run_backward(const lora_desc* d, const DropParams& dp, int64_t T, const void
                  const void* dY, const float* H, const float* dora_m, const float* dora_n,
                  const void* Y_save, void* dX, float* dm, void* ws, cudaStream_t st) {
   Layout L = carve(d, T, n_seg, s.rank_sum, true, ws);
+  clear_stale();
   LORA_TRY(launch_make_items(T, n_seg, seg_start, seg_slot, s.n, L.gitems, L.gcount, (int32_t)L.gmax,
                              L.ritems, L.rcount, (int32_t)L.rmax, st));
   const float q = dropout_q(d);
@@ -317,6 +329,8 @@ int run_backward(const lora_desc* d, const DropParams& dp, int64_t T, const void
 
 extern "C" {
 
+const char* lora_last_cuda_error(void) { return cudaGetErrorString(t_last_error); }
+
 const char* lora_status_string(int status) {
   switch (status) {
     case LORA_OK: return "ok";
@@ -364,6 +378,7 @@ int lora_prepare_weight(const lora_desc* d, const void* W, void* W_t, void* stre
   if (rc) return rc;
   if (!W || !W_t) return LORA_ERR_INVALID;
   if (!al16(W) || !al16(W_t)) return LORA_ERR_ALIGN;
+  clear_stale();
   return cuda_status(launch_transpose_weight(d->dtype, W, W_t, d->out_dim, d->in_dim,
                                              (cudaStream_t)stream));
 }
@@ -374,6 +389,7 @@ int lora_dora_norm(const lora_desc* d, const void* W, const float* A, const floa
   if (rc) return rc;
   if (!W || !A || !B || !norm_out) return LORA_ERR_INVALID;
   if (!al16(W) || !al16(A) || !al16(B) || !al16(norm_out)) return LORA_ERR_ALIGN;
+  clear_stale();
   return cuda_status(launch_dora_norm(d->dtype, W, A, B, d->scale, d->out_dim, d->in_dim, d->rank,
                                       norm_out, (cudaStream_t)stream));
 }
@@ -531,6 +547,7 @@ int lora_grad_prepare(const float* grads, int32_t n_groups, const lora_group* gr
   Carve c(ws);
   double* part = c.take<double>((size_t)(blocks > 0 ? blocks : 1));
   uint32_t* counter = c.take<uint32_t>(4);
+  clear_stale();
   return cuda_status(launch_grad_prepare(grads, g, d_scale_norm, d_status, part, counter,
                                          (cudaStream_t)stream));
 }
@@ -539,15 +556,24 @@ int lora_adamw_step(float* params, float* grads, float* m, float* v, int32_t n_g
                     const lora_group* groups, const lora_adamw_hp* hp, const double* d_scale_norm,
                     const int32_t* d_status, int32_t zero_grads, void* stream) {
   if (!hp) return LORA_ERR_INVALID;
-  if (!(hp->beta1 >= 0.f && hp->beta1 < 1.f && hp->beta2 >= 0.f && hp->beta2 < 1.f &&
-        hp->eps > 0.f && std::isfinite(hp->weight_decay) && std::isfinite(hp->plus_ratio)))
+  if (!(hp->beta1 >= 0.0 && hp->beta1 < 1.0 && hp->beta2 >= 0.0 && hp->beta2 < 1.0 &&
+        hp->eps > 0.0 && std::isfinite(hp->weight_decay) && std::isfinite(hp->plus_ratio)))
     return LORA_ERR_INVALID;
   GroupTab g;
   int rc = build_groups(n_groups, groups, g, hp);
   if (rc) return rc;
   if (!params || !grads || !m || !v || !d_scale_norm || !d_status) return LORA_ERR_INVALID;
   if (!al16(params) || !al16(grads) || !al16(m) || !al16(v)) return LORA_ERR_ALIGN;
-  return cuda_status(launch_adamw(params, grads, m, v, g, *hp, d_scale_norm, d_status, zero_grads,
+  AdamK k;
+  k.b1 = (float)hp->beta1;
+  k.omb1 = (float)(1.0 - hp->beta1);
+  k.b2 = (float)hp->beta2;
+  k.omb2 = (float)(1.0 - hp->beta2);
+  k.eps = (float)hp->eps;
+  k.wd = (float)hp->weight_decay;
+  k.rho = (float)hp->plus_ratio;
+  clear_stale();
+  return cuda_status(launch_adamw(params, grads, m, v, g, k, d_scale_norm, d_status, zero_grads,
                                   (cudaStream_t)stream));
 }
 
@@ -558,6 +584,7 @@ int lora_dropout_mask(const lora_desc* d, const lora_ctx* c, int64_t T, uint8_t*
   DropParams dp;
   if ((rc = build_drop(d, c, T, dp))) return rc;
   if (!d_mask) return LORA_ERR_INVALID;
+  clear_stale();
   return cuda_status(launch_dropout_mask(dp, T, d->in_dim, d_mask, (cudaStream_t)stream));
 }
 
@@ -569,6 +596,7 @@ int multi_lora_token_slots(int64_t T, int32_t n_seg, const int32_t* d_seg_start,
   if (n_slots > LORA_MAX_SLOTS) return LORA_ERR_UNSUPPORTED;
   if (T >= (int64_t(1) << 31) - kRedTileT) return LORA_ERR_UNSUPPORTED;
   if (T == 0) return LORA_OK;
+  clear_stale();
   return cuda_status(launch_token_slots(T, n_seg, d_seg_start, d_seg_slot, n_slots, d_token_slot,
                                         (cudaStream_t)stream));
 }

@@ -138,11 +138,34 @@ struct MLoad {
   }
 };
 
-template <int BN>
-__device__ __forceinline__ void mma_tile(float (&acc)[8][BN / 16], const float (*sa)[BM + PAD],
+// Accumulator of one thread's 8 x TN outputs. COMP: every 16-wide K-tile is summed into fresh
+// registers and the tile sums are added with Knuth's TwoSum, carrying the rounding error in
+// `comp`, so that the long reductions of the skinny products (K = in, out or a token range)
+// lose no more than one tile's worth of fp32 rounding.
+template <int TN, bool COMP>
+struct Acc {
+  float v[8][TN];
+  float c[8][TN];
+  __device__ __forceinline__ void zero() {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int j = 0; j < TN; ++j) v[i][j] = 0.f, c[i][j] = 0.f;
+  }
+  __device__ __forceinline__ float get(int i, int j) const { return COMP ? v[i][j] + c[i][j] : v[i][j]; }
+  __device__ __forceinline__ void scale(int i, int j, float s) { v[i][j] *= s; c[i][j] *= s; }
+};
+
+template <int BN, bool COMP>
+__device__ __forceinline__ void mma_tile(Acc<BN / 16, COMP>& acc, const float (*sa)[BM + PAD],
                                          const float (*sb)[BN + PAD]) {
   constexpr int TN = BN / 16;
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  float t[8][TN];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < TN; ++j) t[i][j] = COMP ? 0.f : acc.v[i][j];
 #pragma unroll
   for (int kk = 0; kk < BK; ++kk) {
     float a[8], b[TN];
@@ -154,13 +177,27 @@ __device__ __forceinline__ void mma_tile(float (&acc)[8][BN / 16], const float (
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
-      for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+      for (int j = 0; j < TN; ++j) t[i][j] = fmaf(a[i], b[j], t[i][j]);
   }
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < TN; ++j) {
+      if (COMP) {
+        const float s = __fadd_rn(acc.v[i][j], t[i][j]);
+        const float bp = __fsub_rn(s, acc.v[i][j]);
+        const float err = __fadd_rn(__fsub_rn(acc.v[i][j], __fsub_rn(s, bp)), __fsub_rn(t[i][j], bp));
+        acc.v[i][j] = s;
+        acc.c[i][j] = __fadd_rn(acc.c[i][j], err);
+      } else {
+        acc.v[i][j] = t[i][j];
+      }
+    }
 }
 
 // Double-buffered main loop over K-major operands (rows along M for A, along N for B).
-template <typename TA, typename TB, int BN>
-__device__ void loop_kk(float (&acc)[8][BN / 16], Smem<BN>& sm, const OpRef& a, int64_t m0,
+template <typename TA, typename TB, int BN, bool COMP>
+__device__ void loop_kk(Acc<BN / 16, COMP>& acc, Smem<BN>& sm, const OpRef& a, int64_t m0,
                         const OpRef& b, int64_t n0, int64_t K, const DropParams& dp) {
   const int ntiles = (int)((K + BK - 1) / BK);
   if (ntiles <= 0) return;
@@ -177,7 +214,7 @@ __device__ void loop_kk(float (&acc)[8][BN / 16], Smem<BN>& sm, const OpRef& a, 
       la.load(a, m0, (int64_t)(t + 1) * BK, dp);
       lb.load(b, n0, (int64_t)(t + 1) * BK, dp);
     }
-    mma_tile<BN>(acc, sm.a[cur], sm.b[cur]);
+    mma_tile<BN, COMP>(acc, sm.a[cur], sm.b[cur]);
     if (t + 1 < ntiles) {
       la.store(sm.a[cur ^ 1]);
       lb.store(sm.b[cur ^ 1]);
@@ -187,8 +224,8 @@ __device__ void loop_kk(float (&acc)[8][BN / 16], Smem<BN>& sm, const OpRef& a, 
 }
 
 // Double-buffered main loop over M-major operands: K = tokens [t0, t1).
-template <typename TA, typename TB, int BN>
-__device__ void loop_mm(float (&acc)[8][BN / 16], Smem<BN>& sm, const OpRef& a, int64_t m0,
+template <typename TA, typename TB, int BN, bool COMP>
+__device__ void loop_mm(Acc<BN / 16, COMP>& acc, Smem<BN>& sm, const OpRef& a, int64_t m0,
                         const OpRef& b, int64_t n0, int64_t t0, int64_t t1, const DropParams& dp) {
   const int ntiles = (int)((t1 - t0 + BK - 1) / BK);
   if (ntiles <= 0) return;
@@ -205,7 +242,7 @@ __device__ void loop_mm(float (&acc)[8][BN / 16], Smem<BN>& sm, const OpRef& a, 
       la.load(a, m0, t0 + (int64_t)(t + 1) * BK, dp);
       lb.load(b, n0, t0 + (int64_t)(t + 1) * BK, dp);
     }
-    mma_tile<BN>(acc, sm.a[cur], sm.b[cur]);
+    mma_tile<BN, COMP>(acc, sm.a[cur], sm.b[cur]);
     if (t + 1 < ntiles) {
       la.store(sm.a[cur ^ 1]);
       lb.store(sm.b[cur ^ 1]);
@@ -226,17 +263,15 @@ __global__ void __launch_bounds__(256) k_tok_gemm(const TokGemmArgs args) {
   const int64_t m0 = it.t0;
   const int64_t n0 = (int64_t)blockIdx.x * BN;
   constexpr int TN = BN / 16;
-  float acc[8][TN];
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-#pragma unroll
-    for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
+  constexpr bool COMP = (BN == 64);
+  Acc<TN, COMP> acc;
+  acc.zero();
 
   // LoRA phase: sum_j P[t, j] Q_slot[n, j] over the slot's rank (the up-projection as extra K-steps)
   if (args.lora_phase && slot >= 0) {
     OpRef p{args.lp, args.ldlp, m0, it.t1, args.lq.rank[slot], nullptr, 0, 1};
     OpRef q{args.lq.p[slot], args.lq.ld[slot], 0, args.n_rows, args.lq.rank[slot], nullptr, 0, 0};
-    loop_kk<float, float, BN>(acc, sm, p, m0, q, n0, args.lq.rank[slot], args.drop);
+    loop_kk<float, float, BN, COMP>(acc, sm, p, m0, q, n0, args.lq.rank[slot], args.drop);
     if (args.mask_after_lora) {
       const int tx = threadIdx.x & 15;
 #pragma unroll
@@ -245,7 +280,7 @@ __global__ void __launch_bounds__(256) k_tok_gemm(const TokGemmArgs args) {
 #pragma unroll
         for (int j = 0; j < TN; ++j) {
           const int64_t n = n0 + ((j < 4) ? (tx * 4 + j) : (64 + tx * 4 + j - 4));
-          if (m < it.t1 && n < args.n_rows && !drop_keep(args.drop, m, n)) acc[i][j] = 0.f;
+          if (m < it.t1 && n < args.n_rows && !drop_keep(args.drop, m, n)) acc.scale(i, j, 0.f);
         }
       }
     }
@@ -262,7 +297,7 @@ __global__ void __launch_bounds__(256) k_tok_gemm(const TokGemmArgs args) {
     } else {
       b = OpRef{args.b, args.ldb, 0, args.n_rows, args.K, nullptr, 0, 0};
     }
-    if (!(args.b_per_slot && slot < 0)) loop_kk<TA, TB, BN>(acc, sm, a, m0, b, n0, args.K, args.drop);
+    if (!(args.b_per_slot && slot < 0)) loop_kk<TA, TB, BN, COMP>(acc, sm, a, m0, b, n0, args.K, args.drop);
   }
 
   // epilogue
@@ -281,7 +316,7 @@ __global__ void __launch_bounds__(256) k_tok_gemm(const TokGemmArgs args) {
       float v[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        v[e] = acc[i][g * 4 + e] * alpha;
+        v[e] = acc.get(i, g * 4 + e) * alpha;
         if (args.n_colscale) v[e] *= __ldg(args.n_colscale + n + e);
       }
       store4(out + m * args.ldo + n, v);
@@ -300,14 +335,11 @@ __global__ void __launch_bounds__(256) k_red_gemm(const RedGemmArgs args) {
   const int64_t m0 = (int64_t)blockIdx.y * BM;
   const int64_t n0 = (int64_t)blockIdx.x * BN;
   const int32_t nrank = args.rank[it.slot];
-  float acc[8][4];
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+  Acc<4, true> acc;
+  acc.zero();
   OpRef a{args.a, args.lda, it.t0, it.t1, args.M, args.a_colscale, args.a_mask, 1};
   OpRef b{args.b, args.ldb, it.t0, it.t1, nrank, nullptr, 0, 1};
-  loop_mm<TA, float, BN>(acc, sm, a, m0, b, n0, it.t0, it.t1, args.drop);
+  loop_mm<TA, float, BN, true>(acc, sm, a, m0, b, n0, it.t0, it.t1, args.drop);
   float* part = args.part + (int64_t)item * args.M * args.ldp;
   const int tx = threadIdx.x & 15;
 #pragma unroll
@@ -315,7 +347,7 @@ __global__ void __launch_bounds__(256) k_red_gemm(const RedGemmArgs args) {
     const int64_t m = m0 + row_of(i);
     const int64_t n = n0 + tx * 4;
     if (m >= args.M || n >= args.ldp) continue;
-    float v[4] = {acc[i][0], acc[i][1], acc[i][2], acc[i][3]};
+    float v[4] = {acc.get(i, 0), acc.get(i, 1), acc.get(i, 2), acc.get(i, 3)};
     store4(part + m * args.ldp + n, v);
   }
 }

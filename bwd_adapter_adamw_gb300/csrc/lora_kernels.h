@@ -132,8 +132,11 @@ constexpr int kAdamElemsPerBlock = kAdamThreads * 16;
 int prepare_blocks(const GroupTab& g);  // CTAs (and double partials) of one prepare launch
 cudaError_t launch_grad_prepare(const float* grads, const GroupTab& g, double* d_scale_norm,
                                 int32_t* d_status, double* part, uint32_t* counter, cudaStream_t st);
+struct AdamK {
+  float b1, omb1, b2, omb2, eps, wd, rho;   // 1 - beta formed in double on the host
+};
 cudaError_t launch_adamw(float* p, float* g, float* m, float* v, const GroupTab& gt,
-                         const lora_adamw_hp& hp, const double* d_scale_norm,
-                         const int32_t* d_status, int zero_grads, cudaStream_t st);
+                         const AdamK& hp, const double* d_scale_norm, const int32_t* d_status,
+                         int zero_grads, cudaStream_t st);
 
 }  // namespace lora

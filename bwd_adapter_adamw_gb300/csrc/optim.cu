@@ -113,24 +113,24 @@ __global__ void __launch_bounds__(kPrepThreads) k_grad_prepare(const float* __re
   }
 }
 
-__device__ __forceinline__ void adam_elem(float& p, float& g, float& m, float& v, int kind,
-                                          float c, float lr, float b1, float b2, float eps,
-                                          float wd, float rho, float inv_bc1, float inv_bc2) {
+__device__ __forceinline__ void adam_elem(float& p, float g, float& m, float& v, int kind,
+                                          float c, float lr, const AdamK& k, float inv_bc1,
+                                          float inv_bc2) {
   const float gh = g * c;
-  m = fmaf(b1, m, (1.f - b1) * gh);
-  v = fmaf(b2, v, (1.f - b2) * gh * gh);
-  const float u = (m * inv_bc1) / (sqrtf(v * inv_bc2) + eps);
+  m = fmaf(k.b1, m, k.omb1 * gh);
+  v = fmaf(k.b2, v, k.omb2 * gh * gh);
+  const float u = (m * inv_bc1) / (sqrtf(v * inv_bc2) + k.eps);
   if (kind == 0)
-    p = p - lr * u - lr * wd * p;
+    p = p - lr * u - lr * k.wd * p;
   else if (kind == 1)
-    p = p - (lr * rho) * u;
+    p = p - (lr * k.rho) * u;
   else
     p = p - lr * u;
 }
 
 __global__ void __launch_bounds__(kAdamThreads) k_adamw(float* __restrict__ P, float* __restrict__ G,
                                                         float* __restrict__ Mo, float* __restrict__ V,
-                                                        const GroupTab gt, const lora_adamw_hp hp,
+                                                        const GroupTab gt, const AdamK hp,
                                                         const double* __restrict__ scale_norm,
                                                         const int32_t* __restrict__ status,
                                                         int zero_grads) {
@@ -157,8 +157,7 @@ __global__ void __launch_bounds__(kAdamThreads) k_adamw(float* __restrict__ P, f
     for (int j = 0; j < 4; ++j) {
       const int64_t l = li + j;
       const int kind = (l < na) ? 0 : ((l < nab) ? 1 : 2);
-      adam_elem(pp[j], gg[j], mm[j], vv[j], kind, c, lr, hp.beta1, hp.beta2, hp.eps,
-                hp.weight_decay, hp.plus_ratio, inv_bc1, inv_bc2);
+      adam_elem(pp[j], gg[j], mm[j], vv[j], kind, c, lr, hp, inv_bc1, inv_bc2);
     }
     *reinterpret_cast<float4*>(P + e) = p;
     *reinterpret_cast<float4*>(Mo + e) = m;
@@ -169,8 +168,7 @@ __global__ void __launch_bounds__(kAdamThreads) k_adamw(float* __restrict__ P, f
     const int64_t e = gt.offset[g] + l;
     const int kind = (l < na) ? 0 : ((l < nab) ? 1 : 2);
     float p = P[e], gr = G[e], m = Mo[e], v = V[e];
-    adam_elem(p, gr, m, v, kind, c, lr, hp.beta1, hp.beta2, hp.eps, hp.weight_decay,
-              hp.plus_ratio, inv_bc1, inv_bc2);
+    adam_elem(p, gr, m, v, kind, c, lr, hp, inv_bc1, inv_bc2);
     P[e] = p; Mo[e] = m; V[e] = v;
     if (zero_grads) G[e] = 0.f;
   }
@@ -212,8 +210,8 @@ cudaError_t launch_grad_prepare(const float* grads, const GroupTab& g_in, double
 }
 
 cudaError_t launch_adamw(float* p, float* g, float* m, float* v, const GroupTab& gt_in,
-                         const lora_adamw_hp& hp, const double* d_scale_norm,
-                         const int32_t* d_status, int zero_grads, cudaStream_t st) {
+                         const AdamK& hp, const double* d_scale_norm, const int32_t* d_status,
+                         int zero_grads, cudaStream_t st) {
   GroupTab gt = gt_in;
   const int blocks = set_blocks(gt, kAdamElemsPerBlock);
   if (blocks == 0) return cudaSuccess;

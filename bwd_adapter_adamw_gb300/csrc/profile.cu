@@ -1,6 +1,6 @@
 // Launch instrumentation: a launch counter and optional CUDA-event brackets around the launches
 // of one kernel class (used by the benchmark to time its dominant kernel on the launching stream,
-// including inside captured CUDA graphs, where each record becomes an event-record node).
+// including inside captured CUDA graphs, where each record becomes an external event node).
 #include <atomic>
 #include <mutex>
 #include <vector>
@@ -15,20 +15,30 @@ std::mutex g_mu;
 int g_kind = 0;
 std::vector<cudaEvent_t> g_starts, g_stops;
 size_t g_used = 0;
+
+// Under stream capture a plain record only orders streams inside the capture; the external flag
+// makes it an event-record node that fires (and timestamps) on every replay.
+void record(cudaEvent_t e, cudaStream_t st) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(e, st, cudaEventRecordExternal);
+  else
+    cudaEventRecord(e, st);
+}
 }  // namespace
 
 void prof_begin(int kind, cudaStream_t st) {
   g_launches.fetch_add(1, std::memory_order_relaxed);
   if (kind == 0) return;
   std::lock_guard<std::mutex> lk(g_mu);
-  if (g_kind == kind && g_used < g_starts.size()) cudaEventRecord(g_starts[g_used], st);
+  if (g_kind == kind && g_used < g_starts.size()) record(g_starts[g_used], st);
 }
 
 void prof_end(int kind, cudaStream_t st) {
   if (kind == 0) return;
   std::lock_guard<std::mutex> lk(g_mu);
   if (g_kind == kind && g_used < g_stops.size()) {
-    cudaEventRecord(g_stops[g_used], st);
+    record(g_stops[g_used], st);
     ++g_used;
   }
 }
@@ -41,6 +51,8 @@ int lora_profile_arm(int32_t kernel_class, void* const* start_events, void* cons
                      int32_t n) {
   if (kernel_class < 0 || n < 0 || (n > 0 && (!start_events || !stop_events)))
     return LORA_ERR_INVALID;
+  for (int i = 0; i < n; ++i)
+    if (!start_events[i] || !stop_events[i]) return LORA_ERR_INVALID;
   std::lock_guard<std::mutex> lk(lora::g_mu);
   lora::g_kind = kernel_class;
   lora::g_starts.assign(n, nullptr);

@@ -113,12 +113,14 @@ typedef struct lora_group {
   int64_t step;        /* completed updates of this group before this one (bias correction) */
 } lora_group;
 
+/* Doubles so that 1 - beta is formed on the host before rounding (0.999f would shift 1 - beta2
+ * by 1.3e-5 relative). The kernels compute in fp32. */
 typedef struct lora_adamw_hp {
-  float beta1;         /* 0.9 */
-  float beta2;         /* 0.999 */
-  float eps;           /* 1e-8, added outside the square root */
-  float weight_decay;  /* applied to kind A only */
-  float plus_ratio;    /* LoRA+: B's lr = lr * plus_ratio */
+  double beta1;         /* 0.9 */
+  double beta2;         /* 0.999 */
+  double eps;           /* 1e-8, added outside the square root */
+  double weight_decay;  /* applied to kind A only */
+  double plus_ratio;    /* LoRA+: B's lr = lr * plus_ratio */
 } lora_adamw_hp;
 
 /* ---- host helpers ---------------------------------------------------------------------------*/
@@ -249,6 +251,9 @@ int lora_profile_arm(int32_t kernel_class, void* const* start_events, void* cons
 int32_t lora_profile_used(void);
 /* Kernel launches enqueued by this library since it was loaded (all classes). */
 uint64_t lora_launch_counter(void);
+/* Text of the last CUDA error an entry point of this library reported as LORA_ERR_CUDA in the
+ * calling thread ("no error" if none). */
+const char* lora_last_cuda_error(void);
 
 #ifdef __cplusplus
 }
