@@ -123,13 +123,20 @@ def check_post_step(x_gpu, p0, m0, v0, g_ref, g_bound, kind: int, c: float, hp, 
     the band, which must stay below max_clause_frac of the tensor."""
     x = to64(x_gpu) if hasattr(x_gpu, "detach") else np.asarray(x_gpu, np.float64)
     g = np.asarray(g_ref, np.float64)
+    m0 = np.asarray(m0, np.float64)
     bound = np.asarray(g_bound, np.float64) + 1e-6 * np.abs(g)
     r = O.adamw_update(p0, g, m0, v0, kind, c, hp)[0].astype(np.float64)
-    lo = O.adamw_update(p0, g - bound, m0, v0, kind, c, hp)[0].astype(np.float64)
-    hi = O.adamw_update(p0, g + bound, m0, v0, kind, c, hp)[0].astype(np.float64)
+    # corners: the gradient within its bound, and the first moment within the fp32 rounding of
+    # m = b1 m0 + (1 - b1) c g (which can cancel to ~0, where u = m_hat / sqrt(v_hat) is steep)
+    dm = 4 * U32 * (np.abs(m0) + (1 - hp.beta1) / hp.beta1 * np.abs(c * g))
+    lo, hi = r.copy(), r.copy()
+    for gg in (g - bound, g, g + bound):
+        for mm in (m0 - dm, m0, m0 + dm):
+            y = O.adamw_update(p0, gg, mm, v0, kind, c, hp)[0].astype(np.float64)
+            lo, hi = np.minimum(lo, y), np.maximum(hi, y)
     slack = tol * max(float(np.max(np.abs(r))), 1e-30)
     plain = np.abs(x - r) <= slack
-    band = (x >= np.minimum(np.minimum(lo, hi), r) - slack) & (x <= np.maximum(np.maximum(lo, hi), r) + slack)
+    band = (x >= lo - slack) & (x <= hi + slack)
     ok = plain | band
     if exclude is not None:
         # elements whose previous update already needed the band carry that (bounded) difference
