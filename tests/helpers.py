@@ -129,8 +129,12 @@ def check_post_step(x_gpu, p0, m0, v0, g_ref, g_bound, kind: int, c: float, hp, 
     # corners: the gradient within its bound, and the first moment within the fp32 rounding of
     # m = b1 m0 + (1 - b1) c g (which can cancel to ~0, where u = m_hat / sqrt(v_hat) is steep)
     dm = 4 * U32 * (np.abs(m0) + (1 - hp.beta1) / hp.beta1 * np.abs(c * g))
+    # u(g) is not monotonic (it saturates towards a constant for large |g_hat|), so the interval is
+    # sampled densely, linearly and log-spaced around g, rather than at its ends only
+    ts = np.concatenate([np.linspace(-1.0, 1.0, 41), np.logspace(-9, 0, 28), -np.logspace(-9, 0, 28)])
     lo, hi = r.copy(), r.copy()
-    for gg in (g - bound, g, g + bound):
+    for t in ts:
+        gg = g + t * bound
         for mm in (m0 - dm, m0, m0 + dm):
             y = O.adamw_update(p0, gg, mm, v0, kind, c, hp)[0].astype(np.float64)
             lo, hi = np.minimum(lo, y), np.maximum(hi, y)
@@ -143,7 +147,14 @@ def check_post_step(x_gpu, p0, m0, v0, g_ref, g_bound, kind: int, c: float, hp, 
         # in their state; they are left out here and counted by the caller
         ok = ok | exclude
         plain = plain | exclude
-    assert ok.all(), (int((~ok).sum()), float(np.max(np.abs(x - r))) / max(slack / tol, 1e-30))
+    if not ok.all():
+        bad = np.argwhere(~ok)
+        i = tuple(bad[np.argmax(np.abs((x - r)[~ok]))])
+        detail = dict(index=i, x=x[i], r=r[i], lo=lo[i], hi=hi[i], g=g[i], bound=bound[i],
+                      m0=m0[i], v0=np.asarray(v0, np.float64)[i], p0=np.asarray(p0, np.float64)[i],
+                      c=c, slack=slack)
+        raise AssertionError((int((~ok).sum()), float(np.max(np.abs(x - r))) / max(slack / tol, 1e-30),
+                              detail))
     n_clause = int((~plain).sum())
     assert n_clause <= max(2, int(max_clause_frac * x.size)), n_clause
     return n_clause, ~(np.abs(x - r) <= slack)
