@@ -84,6 +84,7 @@ def _load() -> C.CDLL:
         "lora_backward": (C.c_int, [DP, CP, I64, P, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P]),
         "lora_grad_prepare_workspace_size": (SZ, [I32, C.POINTER(lora_group)]),
         "lora_grad_prepare": (C.c_int, [P, I32, C.POINTER(lora_group), P, P, P, SZ, P]),
+        "lora_grad_prepare_noalloc": (C.c_int, [P, I32, C.POINTER(lora_group), P, P, P]),
         "lora_adamw_step": (C.c_int, [P, P, P, P, I32, C.POINTER(lora_group),
                                       C.POINTER(lora_adamw_hp), P, P, I32, P]),
         "multi_lora_workspace_size": (SZ, [DP, I64, I32, I32, C.POINTER(lora_slot)]),
@@ -108,7 +109,8 @@ def _load() -> C.CDLL:
 _lib = _load()
 EXPORTED = ("lora_status_string", "lora_scale", "lora_lr_at", "lora_workspace_size",
             "lora_prepare_weight", "lora_dora_norm", "lora_forward", "lora_backward",
-            "lora_grad_prepare_workspace_size", "lora_grad_prepare", "lora_adamw_step",
+            "lora_grad_prepare_workspace_size", "lora_grad_prepare", "lora_grad_prepare_noalloc",
+            "lora_adamw_step",
             "multi_lora_workspace_size", "multi_lora_forward", "multi_lora_backward",
             "lora_dropout_mask", "multi_lora_token_slots", "lora_profile_arm",
             "lora_profile_used", "lora_launch_counter", "lora_last_cuda_error")
@@ -229,6 +231,14 @@ def lora_grad_prepare(grads, groups, d_scale_norm, d_status, ws, ws_bytes=None, 
     st = _lib.lora_grad_prepare(_ptr(grads), len(groups), groups, _ptr(d_scale_norm),
                                 _ptr(d_status), _ptr(ws), nbytes, _stream(stream))
     return _check(st, "lora_grad_prepare") if check else st
+
+
+def lora_grad_prepare_noalloc(grads, groups, d_scale_norm, d_status, stream=None, check=True):
+    """lora_grad_prepare without a workspace, for callers that cannot allocate device memory (its
+    scratch is a fixed device array inside the library; calls must not overlap on the GPU)."""
+    st = _lib.lora_grad_prepare_noalloc(_ptr(grads), len(groups), groups, _ptr(d_scale_norm),
+                                        _ptr(d_status), _stream(stream))
+    return _check(st, "lora_grad_prepare_noalloc") if check else st
 
 
 def make_hp(beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01, plus_ratio=1.0) -> lora_adamw_hp:

@@ -552,6 +552,21 @@ int lora_grad_prepare(const float* grads, int32_t n_groups, const lora_group* gr
                                          (cudaStream_t)stream));
 }
 
+int lora_grad_prepare_noalloc(const float* grads, int32_t n_groups, const lora_group* groups,
+                              double* d_scale_norm, int32_t* d_status, void* stream) {
+  GroupTab g;
+  int rc = build_groups(n_groups, groups, g, nullptr);
+  if (rc) return rc;
+  if (!grads || !d_scale_norm || !d_status) return LORA_ERR_INVALID;
+  if (!al16(grads) || (reinterpret_cast<uintptr_t>(d_scale_norm) & 7u) ||
+      (reinterpret_cast<uintptr_t>(d_status) & 3u))
+    return LORA_ERR_ALIGN;
+  if (prepare_blocks(g) > kNoallocMaxPartials) return LORA_ERR_UNSUPPORTED;
+  clear_stale();
+  return cuda_status(launch_grad_prepare_noalloc(grads, g, d_scale_norm, d_status,
+                                                 (cudaStream_t)stream));
+}
+
 int lora_adamw_step(float* params, float* grads, float* m, float* v, int32_t n_groups,
                     const lora_group* groups, const lora_adamw_hp* hp, const double* d_scale_norm,
                     const int32_t* d_status, int32_t zero_grads, void* stream) {

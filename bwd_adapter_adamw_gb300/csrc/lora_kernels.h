@@ -135,6 +135,10 @@ cudaError_t launch_grad_prepare(const float* grads, const GroupTab& g, double* d
 struct AdamK {
   float b1, omb1, b2, omb2, eps, wd, rho;   // 1 - beta formed in double on the host
 };
+// Allocation-free prepare: at most kNoallocMaxPartials CTAs (partials) in total.
+constexpr int kNoallocMaxPartials = 16384;
+cudaError_t launch_grad_prepare_noalloc(const float* grads, const GroupTab& g,
+                                        double* d_scale_norm, int32_t* d_status, cudaStream_t st);
 cudaError_t launch_adamw(float* p, float* g, float* m, float* v, const GroupTab& gt,
                          const AdamK& hp, const double* d_scale_norm, const int32_t* d_status,
                          int zero_grads, cudaStream_t st);

@@ -3,6 +3,8 @@
 // and rejects non-finite values before any mutation, pass 2 applies one combined normalisation x
 // clipping factor; Optimizer: decay on A only from the pre-update value with the scheduled lr,
 // LoRA+ ratio on B's lr, moments see the gradient without decay).
+#include <mutex>
+
 #include "lora_kernels.h"
 
 namespace lora {
@@ -219,6 +221,51 @@ cudaError_t launch_adamw(float* p, float* g, float* m, float* v, const GroupTab&
   k_adamw<<<blocks, kAdamThreads, 0, st>>>(p, g, m, v, gt, hp, d_scale_norm, d_status, zero_grads);
   prof_end(LORA_PROF_ADAMW, st);
   return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------------------------
+// Allocation-free variant of the prepare launch: its scratch (the per-block double partials and
+// the last-block counter) lives in this file-scope device array instead of a caller workspace.
+// Every GPU that loads the library holds the array until exit; all calls share it, so calls
+// that overlap on the GPU race, and the counter is cleared by every call.
+// ------------------------------------------------------------------------------------------
+namespace {
+constexpr size_t kNoallocCounterOffset = sizeof(double) * kNoallocMaxPartials;
+constexpr size_t kNoallocBytes = kNoallocCounterOffset + 256;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocBytes];
+
+std::mutex g_noalloc_mu;
+constexpr int kMaxDevices = 64;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Host code cannot use &g_noalloc_scratch as a device address (it names a host-side stand-in);
+// the device address is looked up once per device, with that device current.
+cudaError_t noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return cudaSuccess;
+}
+}  // namespace
+
+cudaError_t launch_grad_prepare_noalloc(const float* grads, const GroupTab& g,
+                                        double* d_scale_norm, int32_t* d_status,
+                                        cudaStream_t st) {
+  void* base = nullptr;
+  cudaError_t e = noalloc_scratch(&base);
+  if (e != cudaSuccess) return e;
+  double* part = reinterpret_cast<double*>(base);
+  uint32_t* counter = reinterpret_cast<uint32_t*>(static_cast<char*>(base) + kNoallocCounterOffset);
+  return launch_grad_prepare(grads, g, d_scale_norm, d_status, part, counter, st);
 }
 
 }  // namespace lora

@@ -185,6 +185,27 @@ int lora_grad_prepare(const float* grads, int32_t n_groups, const lora_group* gr
                       double* d_scale_norm, int32_t* d_status, void* ws, size_t ws_bytes,
                       void* stream);
 
+/* Allocation-free lora_grad_prepare (the paper has no counterpart; this is a deployment aid).
+ * For callers that cannot allocate device memory and so cannot supply a workspace: code that
+ * runs under another framework's allocator which owns the whole device pool, code that must not
+ * allocate after initialisation (allocation can stall or fail mid-training), and code that
+ * enqueues work while some other component is capturing a CUDA graph, where a cudaMalloc would
+ * break or poison the capture. Same arguments and results as lora_grad_prepare, minus the
+ * workspace: the scratch is a fixed file-scope device array of LORA_NOALLOC_PREPARE_PARTIALS
+ * doubles plus a counter (about 128 KB), which every GPU that loads the library holds until
+ * process exit. The call allocates nothing (no cudaMalloc, cudaFree or allocating library call).
+ *   - Size limit: sum over groups of ceil(elements / 16384) must be at most
+ *     LORA_NOALLOC_PREPARE_PARTIALS (one group: at most 268,435,456 elements); larger requests
+ *     return LORA_ERR_UNSUPPORTED with nothing enqueued.
+ *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
+ *     that device current; make that first call before any stream capture on that device.
+ *   - All calls share the one array: calls that overlap on the GPU (other streams, other host
+ *     threads) race and give wrong results; order them on one stream. The array keeps the last
+ *     call's contents; each call clears the counter it needs before use. */
+#define LORA_NOALLOC_PREPARE_PARTIALS 16384
+int lora_grad_prepare_noalloc(const float* grads, int32_t n_groups, const lora_group* groups,
+                              double* d_scale_norm, int32_t* d_status, void* stream);
+
 /* Pass 2 fused with the AdamW update, for every group whose device status is LORA_OK (groups
  * with another status are left untouched: params, moments and grads):
  *   g_hat = c g; m = b1 m + (1-b1) g_hat; v = b2 v + (1-b2) g_hat^2; k = step + 1;
