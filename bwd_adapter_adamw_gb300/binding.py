@@ -98,6 +98,7 @@ def _load() -> C.CDLL:
         "lora_profile_used": (I32, []),
         "lora_launch_counter": (U64, []),
         "lora_last_cuda_error": (C.c_char_p, []),
+        "lora_device_error": (C.c_int, [C.POINTER(C.c_uint32), I32]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -113,7 +114,8 @@ EXPORTED = ("lora_status_string", "lora_scale", "lora_lr_at", "lora_workspace_si
             "lora_adamw_step",
             "multi_lora_workspace_size", "multi_lora_forward", "multi_lora_backward",
             "lora_dropout_mask", "multi_lora_token_slots", "lora_profile_arm",
-            "lora_profile_used", "lora_launch_counter", "lora_last_cuda_error")
+            "lora_profile_used", "lora_launch_counter", "lora_last_cuda_error",
+            "lora_device_error")
 
 LORA_PROF_NONE = 0
 LORA_PROF_FROZEN_FWD = 1
@@ -315,3 +317,10 @@ def lora_profile_used() -> int:
 
 def lora_launch_counter() -> int:
     return _lib.lora_launch_counter()
+
+
+def lora_device_error(reset: bool = False) -> int:
+    """Device error bits of the tensor-core products (0 = none); synchronous."""
+    v = C.c_uint32(0)
+    _check(_lib.lora_device_error(C.byref(v), 1 if reset else 0), "lora_device_error")
+    return v.value

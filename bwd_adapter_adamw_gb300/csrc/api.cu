@@ -154,6 +154,7 @@ struct Layout {
   float* Bt;           // per slot [r_s, out]
   float* partB;        // [rmax_items][out][rank]
   float* partA;        // [rmax_items][in][rank]
+  uint16_t* dYs;       // [T, out] bf16 dY * (m / n) for the DoRA tensor-core dX product
   size_t bytes;
 };
 
@@ -173,6 +174,7 @@ Layout carve(const lora_desc* d, int64_t T, int32_t n_seg, int64_t rank_sum, boo
     L.Bt = c.take<float>((size_t)rank_sum * d->out_dim);
     L.partB = c.take<float>((size_t)L.rmax * d->out_dim * d->rank);
     L.partA = c.take<float>((size_t)L.rmax * d->in_dim * d->rank);
+    if (d->dora && d->dtype == LORA_BF16) L.dYs = c.take<uint16_t>((size_t)T * d->out_dim);
   }
   L.bytes = c.off + kWsAlign;
   return L;
@@ -226,7 +228,17 @@ int run_forward(const lora_desc* d, const DropParams& dp, int64_t T, const void*
     a.n_colscale = ratio;
     a.out = Y; a.ldo = d->out_dim; a.n_out = d->out_dim;
     a.drop = dp;
-    LORA_TRY(launch_tok_gemm(d->dtype, d->dtype, d->dtype, 128, a, (int)L.gmax, st, LORA_PROF_FROZEN_FWD));
+    if (d->dtype == LORA_BF16) {
+      TcGemmArgs t{};
+      t.a = X; t.T = T; t.b = W; t.n_rows = d->out_dim; t.K = d->in_dim;
+      t.p = H; t.ldp = d->rank; t.n_slots = s.n;
+      for (int k = 0; k < s.n; ++k) { t.q[k] = s.B[k]; t.q_rank[k] = s.rank[k]; }
+      t.n_colscale = ratio; t.out = Y; t.ldo = d->out_dim;
+      t.items = L.gitems; t.n_items = L.gcount; t.max_items = (int)L.gmax; t.drop = dp;
+      LORA_TRY(launch_tc_gemm(t, st, LORA_PROF_FROZEN_FWD));
+    } else {
+      LORA_TRY(launch_tok_gemm(d->dtype, d->dtype, d->dtype, 128, a, (int)L.gmax, st, LORA_PROF_FROZEN_FWD));
+    }
   }
   return LORA_OK;
 }
@@ -289,7 +301,22 @@ int run_backward(const lora_desc* d, const DropParams& dp, int64_t T, const void
     a.alpha = 1.f;
     a.out = dX; a.ldo = d->in_dim; a.n_out = d->in_dim;
     a.drop = dp;
-    LORA_TRY(launch_tok_gemm(d->dtype, d->dtype, d->dtype, 128, a, (int)L.gmax, st, LORA_PROF_FROZEN_DX));
+    if (d->dtype == LORA_BF16) {
+      const void* dYp = dY;
+      if (ratio) {   // DoRA: dY' = dY * (m / n) along K, materialised once in bf16
+        LORA_TRY(launch_colscale_bf16(dY, ratio, T, d->out_dim, L.dYs, st));
+        dYp = L.dYs;
+      }
+      TcGemmArgs t{};
+      t.a = dYp; t.T = T; t.b = Wt; t.n_rows = d->in_dim; t.K = d->out_dim;
+      t.p = L.Gs; t.ldp = d->rank; t.n_slots = s.n;
+      for (int k = 0; k < s.n; ++k) { t.q[k] = At[k]; t.q_rank[k] = s.rank[k]; }
+      t.lora_separate = dp.enabled; t.out = dX; t.ldo = d->in_dim;
+      t.items = L.gitems; t.n_items = L.gcount; t.max_items = (int)L.gmax; t.drop = dp;
+      LORA_TRY(launch_tc_gemm(t, st, LORA_PROF_FROZEN_DX));
+    } else {
+      LORA_TRY(launch_tok_gemm(d->dtype, d->dtype, d->dtype, 128, a, (int)L.gmax, st, LORA_PROF_FROZEN_DX));
+    }
   }
   ReduceTab rt{};
   for (int k = 0; k < s.n; ++k) rt.rank[k] = s.rank[k];
@@ -330,6 +357,11 @@ int run_backward(const lora_desc* d, const DropParams& dp, int64_t T, const void
 extern "C" {
 
 const char* lora_last_cuda_error(void) { return cudaGetErrorString(t_last_error); }
+
+int lora_device_error(uint32_t* flags, int32_t reset) {
+  if (!flags) return LORA_ERR_INVALID;
+  return cuda_status(read_tc_error(flags, reset != 0));
+}
 
 const char* lora_status_string(int status) {
   switch (status) {

@@ -69,7 +69,33 @@ cudaError_t launch_tok_gemm(int dtype_a, int dtype_b, int dtype_out, int bn, con
 cudaError_t launch_red_gemm(int dtype_a, const RedGemmArgs& a, int max_items, cudaStream_t st,
                             int prof_kind);
 
+// ---- gemm_tc.cu: tcgen05 frozen products (bf16 activations) ----
+struct TcGemmArgs {
+  const void* a;             // [T, K] bf16, K-contiguous
+  int64_t T;
+  const void* b;             // [n_rows, K] bf16, K-contiguous
+  int64_t n_rows;
+  int64_t K;
+  const float* p;            // LoRA term P [T, ldp] fp32 (nullptr: no LoRA term)
+  int64_t ldp;
+  const float* q[LORA_MAX_SLOTS];   // Q_slot [n_rows, q_rank] fp32
+  int32_t q_rank[LORA_MAX_SLOTS];
+  int32_t n_slots;
+  int32_t lora_separate;     // LoRA term in its own accumulator, masked by dropout at (t, n)
+  DropParams drop;
+  const float* n_colscale;   // per output column scale (DoRA m / n), nullable
+  void* out;                 // [T, ldo] bf16
+  int64_t ldo;
+  const TokenItem* items;
+  const int32_t* n_items;
+  int max_items;
+};
+cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st, int prof_kind);
+cudaError_t read_tc_error(uint32_t* out, bool reset);
+
 // ---- lowrank.cu ----
+cudaError_t launch_colscale_bf16(const void* src, const float* scale, int64_t rows, int64_t cols,
+                                 void* dst, cudaStream_t st);
 cudaError_t launch_make_items(int64_t T, int32_t n_seg, const int32_t* seg_start,
                               const int32_t* seg_slot, int32_t n_slots, TokenItem* gitems,
                               int32_t* gcount, int32_t gmax, TokenItem* ritems, int32_t* rcount,

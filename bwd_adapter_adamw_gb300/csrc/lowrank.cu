@@ -118,6 +118,30 @@ __global__ void k_dropout_mask(const DropParams dp, int64_t T, int64_t in_dim, u
   }
 }
 
+// dst[t, o] = bf16(src[t, o] * scale[o]): the DoRA dY' operand of the tensor-core dX product,
+// whose column scale runs along K and so cannot be applied in the epilogue.
+__global__ void k_colscale_bf16(const __nv_bfloat16* __restrict__ src, const float* __restrict__ scale,
+                                int64_t rows, int64_t cols, __nv_bfloat16* __restrict__ dst) {
+  const int64_t n8 = rows * cols / 8;
+  for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < n8;
+       v += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t e = v * 8;
+    const int64_t c = e % cols;
+    float x[8];
+    load16(src + e, x);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) x[j] *= __ldg(scale + c + j);
+    uint4 u;
+    uint32_t* w = &u.x;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      __nv_bfloat162 h = __floats2bfloat162_rn(x[2 * j], x[2 * j + 1]);
+      w[j] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    *reinterpret_cast<uint4*>(dst + e) = u;
+  }
+}
+
 __global__ void k_ratio(const float* __restrict__ num, const float* __restrict__ den, int64_t n,
                         float* __restrict__ out) {
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -194,6 +218,18 @@ cudaError_t launch_dropout_mask(const DropParams& dp, int64_t T, int64_t in_dim,
   int64_t blocks = (n + 255) / 256;
   if (blocks > 8192) blocks = 8192;
   { prof_begin(0, st); k_dropout_mask<<<(unsigned)blocks, 256, 0, st>>>(dp, T, in_dim, mask); }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_colscale_bf16(const void* src, const float* scale, int64_t rows, int64_t cols,
+                                 void* dst, cudaStream_t st) {
+  const int64_t n8 = rows * cols / 8;
+  if (n8 <= 0) return cudaSuccess;
+  int64_t blocks = (n8 + 255) / 256;
+  if (blocks > 16384) blocks = 16384;
+  prof_begin(0, st);
+  k_colscale_bf16<<<(unsigned)blocks, 256, 0, st>>>((const __nv_bfloat16*)src, scale, rows, cols,
+                                                    (__nv_bfloat16*)dst);
   return cudaGetLastError();
 }
 

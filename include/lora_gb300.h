@@ -275,6 +275,11 @@ uint64_t lora_launch_counter(void);
 /* Text of the last CUDA error an entry point of this library reported as LORA_ERR_CUDA in the
  * calling thread ("no error" if none). */
 const char* lora_last_cuda_error(void);
+/* Error bits raised on the device by the tensor-core products when a pipeline wait ran out of
+ * its bound (bit 0 loads, bit 1 MMA, bit 2 epilogue): the kernel then skipped its remaining
+ * work, released its tensor memory and returned, so the output is invalid. Synchronous (reads
+ * a device word of the current device); reset != 0 clears it. */
+int lora_device_error(uint32_t* flags, int32_t reset);
 
 #ifdef __cplusplus
 }

@@ -427,3 +427,8 @@ def test_lr_schedule_and_scale_match_oracle(L):
         assert L.lora_lr_at(1, 1e-4, k, 10, 100, 1e-6) == pytest.approx(
             O.lr_at("cosine", 1e-4, k, 10, 100, 1e-6), rel=1e-15)
     assert L.lora_scale(128, 64, True) == O.lora_scale(128, 64, True)
+
+
+def test_zz_no_device_pipeline_errors(L):
+    """No tensor-core pipeline wait ran out of its bound in any test of this module."""
+    assert L.lora_device_error(reset=True) == 0
