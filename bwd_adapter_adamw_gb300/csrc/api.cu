@@ -144,44 +144,297 @@ void single_slot(const lora_desc* d, const float* A, const float* B, float* dA, 
   s.rank_sum = d->rank;
 }
 
+// ---- tensor-core path shape choices (bf16 activations) ---------------------------------------
+constexpr int kMaxRowSplits = 8;
+
+int np_for(int rmax) {           // MMA N covering hi + lo rows of the largest slot
+  const int n = 2 * rmax;
+  return n <= 16 ? 16 : n <= 32 ? 32 : n <= 64 ? 64 : 128;
+}
+
+// K splits of the skinny token-row products so that about two CTAs per SM stream the input.
+int row_splits(int64_t T, int32_t n_seg, int64_t K) {
+  const int64_t items = max_gemm_items(T, n_seg);
+  int64_t s = (296 + items - 1) / items;
+  const int64_t nk = (K + 63) / 64;
+  if (s > nk / 2) s = nk / 2;
+  if (s > kMaxRowSplits) s = kMaxRowSplits;
+  return s < 1 ? 1 : (int)s;
+}
+
+// 64-token blocks per reduction work item: enough items for ~2 CTAs per SM over the N tiles,
+// but at least 8 blocks so that the per-item partials stay small next to the streamed input.
+int red_span_blocks(int64_t T, int64_t N) {
+  const int64_t tiles = (N + 255) / 256;
+  int64_t blocks = ((T * tiles) / 296 + 63) / 64;
+  if (blocks < 8) blocks = 8;
+  if (blocks > 64) blocks = 64;
+  return (int)blocks;
+}
+
+int64_t red_items_bound(int64_t T, int32_t n_seg, int n_slots, int span) {
+  const int64_t ns = n_seg < 1 ? 1 : n_seg;
+  const int64_t nb = (T + 63) / 64;
+  return ns + 1 + n_slots + (nb + ns + span - 1) / span;
+}
+
 struct Layout {
   TokenItem* gitems; int32_t* gcount;
-  TokenItem* ritems; int32_t* rcount;
+  TokenItem* ritems; int32_t* rcount;   // SIMT token reductions (fp32 path)
   int64_t gmax, rmax;
   float* ratio;        // [out] DoRA m / n
   float* Gs;           // [T, rmax]
   float* At;           // per slot [in, r_s]
-  float* Bt;           // per slot [r_s, out]
-  float* partB;        // [rmax_items][out][rank]
-  float* partA;        // [rmax_items][in][rank]
-  uint16_t* dYs;       // [T, out] bf16 dY * (m / n) for the DoRA tensor-core dX product
+  float* Bt;           // per slot [r_s, out] (fp32 path)
+  float* partB;        // [rmax_items][out][rank] (fp32 path)
+  float* partA;        // [rmax_items][in][rank] (fp32 path)
+  uint16_t* dYs;       // [T, out] bf16 dY * (m / n) for the DoRA tensor-core products
+  // tensor-core path
+  uint16_t* Xd;        // [T, in] bf16 masked input (dropout)
+  uint16_t* Sa;        // per slot [2 r, in] bf16 split of A
+  uint16_t* Sb;        // per slot [2 r, out] bf16 split of B^T
+  float* rows_part;    // [splits][T][NP]
+  int64_t ldt;         // padded token stride of the transposed splits
+  uint16_t* HsT;       // per slot [2 r, ldt] bf16
+  uint16_t* GsT;       // per slot [2 r, ldt] bf16
+  TokenItem* items_db; int32_t* count_db; int64_t max_db; int span_db;
+  TokenItem* items_da; int32_t* count_da; int64_t max_da; int span_da;
+  float* red_part;     // [items][2 rmax][N]
   size_t bytes;
 };
 
-Layout carve(const lora_desc* d, int64_t T, int32_t n_seg, int64_t rank_sum, bool backward, void* ws) {
+Layout carve(const lora_desc* d, int64_t T, int32_t n_seg, int n_slots, int64_t rank_sum,
+             bool backward, void* ws) {
   Layout L{};
   Carve c(ws);
+  const bool tc = d->dtype == LORA_BF16;
   L.gmax = max_gemm_items(T, n_seg);
   L.rmax = max_red_items(T, n_seg);
   L.gitems = c.take<TokenItem>((size_t)L.gmax);
   L.gcount = c.take<int32_t>(4);
-  L.ritems = c.take<TokenItem>((size_t)L.rmax);
-  L.rcount = c.take<int32_t>(4);
   L.ratio = c.take<float>((size_t)d->out_dim);
+  if (tc) {
+    const int np = np_for(d->rank);
+    if (d->dropout_p > 0.f) L.Xd = c.take<uint16_t>((size_t)T * d->in_dim);
+    L.Sa = c.take<uint16_t>((size_t)2 * rank_sum * d->in_dim);
+    L.rows_part = c.take<float>((size_t)kMaxRowSplits * T * np);
+  }
   if (backward) {
     L.Gs = c.take<float>((size_t)T * d->rank);
     L.At = c.take<float>((size_t)rank_sum * d->in_dim);
-    L.Bt = c.take<float>((size_t)rank_sum * d->out_dim);
-    L.partB = c.take<float>((size_t)L.rmax * d->out_dim * d->rank);
-    L.partA = c.take<float>((size_t)L.rmax * d->in_dim * d->rank);
-    if (d->dora && d->dtype == LORA_BF16) L.dYs = c.take<uint16_t>((size_t)T * d->out_dim);
+    if (d->dora && tc) L.dYs = c.take<uint16_t>((size_t)T * d->out_dim);
+    if (tc) {
+      L.Sb = c.take<uint16_t>((size_t)2 * rank_sum * d->out_dim);
+      L.ldt = (T + 7) / 8 * 8;
+      L.HsT = c.take<uint16_t>((size_t)2 * rank_sum * L.ldt);
+      L.GsT = c.take<uint16_t>((size_t)2 * rank_sum * L.ldt);
+      L.span_db = red_span_blocks(T, d->out_dim);
+      L.span_da = red_span_blocks(T, d->in_dim);
+      L.max_db = red_items_bound(T, n_seg, n_slots, L.span_db);
+      L.max_da = red_items_bound(T, n_seg, n_slots, L.span_da);
+      L.items_db = c.take<TokenItem>((size_t)L.max_db);
+      L.count_db = c.take<int32_t>(4);
+      L.items_da = c.take<TokenItem>((size_t)L.max_da);
+      L.count_da = c.take<int32_t>(4);
+      const int64_t a = L.max_db * d->out_dim, b = L.max_da * d->in_dim;
+      L.red_part = c.take<float>((size_t)(a > b ? a : b) * 2 * d->rank);
+    } else {
+      L.ritems = c.take<TokenItem>((size_t)L.rmax);
+      L.rcount = c.take<int32_t>(4);
+      L.Bt = c.take<float>((size_t)rank_sum * d->out_dim);
+      L.partB = c.take<float>((size_t)L.rmax * d->out_dim * d->rank);
+      L.partA = c.take<float>((size_t)L.rmax * d->in_dim * d->rank);
+    }
+  } else if (!tc) {
+    L.ritems = c.take<TokenItem>((size_t)L.rmax);
+    L.rcount = c.take<int32_t>(4);
   }
   L.bytes = c.off + kWsAlign;
   return L;
 }
 
-size_t ws_size(const lora_desc* d, int64_t T, int32_t n_seg, int64_t rank_sum) {
-  return carve(d, T, n_seg, rank_sum, true, nullptr).bytes;
+size_t ws_size(const lora_desc* d, int64_t T, int32_t n_seg, int n_slots, int64_t rank_sum) {
+  return carve(d, T, n_seg, n_slots, rank_sum, true, nullptr).bytes;
+}
+
+SlotInfo slot_info(const Slots& s, float q) {
+  SlotInfo si{};
+  int32_t region = 0;
+  for (int k = 0; k < s.n; ++k) {
+    si.rank[k] = s.rank[k];
+    si.alpha[k] = s.scale[k] * q;
+    si.region[k] = region;
+    region += 2 * s.rank[k];
+  }
+  return si;
+}
+
+// shrink on tensor cores: Hs[t, j] = s_k q (Xd[t, :] . A_k[j, :]) via the hi/lo split of A_k
+int tc_shrink(const lora_desc* d, const DropParams& dp, int64_t T, const void* X, int32_t n_seg,
+              const Slots& s, const Layout& L, float* H, cudaStream_t st) {
+  const float q = dropout_q(d);
+  const void* Xin = X;
+  if (dp.enabled) {
+    LORA_TRY(launch_mask_bf16(X, T, d->in_dim, dp, L.Xd, st));
+    Xin = L.Xd;
+  }
+  SplitTab sp{};
+  sp.K = d->in_dim;
+  TcRowsArgs r{};
+  int64_t off = 0;
+  for (int k = 0; k < s.n; ++k) {
+    sp.src[k] = s.A[k];
+    sp.dst[k] = L.Sa + off;
+    sp.rank[k] = s.rank[k];
+    r.s[k] = L.Sa + off;
+    r.rank[k] = s.rank[k];
+    off += 2 * (int64_t)s.rank[k] * d->in_dim;
+  }
+  LORA_TRY(launch_split(sp, s.n, st));
+  r.a = Xin; r.T = T; r.K = d->in_dim; r.n_slots = s.n;
+  r.NP = np_for(d->rank);
+  r.splits = row_splits(T, n_seg, d->in_dim);
+  r.part = L.rows_part;
+  r.si = slot_info(s, q);
+  r.out = H; r.ldo = d->rank;
+  r.items = L.gitems; r.n_items = L.gcount; r.max_items = (int)L.gmax;
+  LORA_TRY(launch_tc_rows(r, st, LORA_PROF_SHRINK));
+  return LORA_OK;
+}
+
+// forward, bf16 activations: shrink and frozen product on tensor cores
+int run_forward_tc(const lora_desc* d, const DropParams& dp, int64_t T, const void* X,
+                   const void* W, int32_t n_seg, const int32_t* seg_start, const int32_t* seg_slot,
+                   const Slots& s, const float* ratio_src_m, const float* ratio_src_n, void* Y,
+                   float* H, void* ws, cudaStream_t st) {
+  Layout L = carve(d, T, n_seg, s.n, s.rank_sum, false, ws);
+  clear_stale();
+  LORA_TRY(launch_make_items(T, n_seg, seg_start, seg_slot, s.n, L.gitems, L.gcount,
+                             (int32_t)L.gmax, nullptr, nullptr, 0, st));
+  const float* ratio = nullptr;
+  if (ratio_src_m) {
+    LORA_TRY(launch_ratio(ratio_src_m, ratio_src_n, d->out_dim, L.ratio, st));
+    ratio = L.ratio;
+  }
+  int rc = tc_shrink(d, dp, T, X, n_seg, s, L, H, st);
+  if (rc) return rc;
+  TcGemmArgs t{};
+  t.a = X; t.T = T; t.b = W; t.n_rows = d->out_dim; t.K = d->in_dim;
+  t.p = H; t.ldp = d->rank; t.n_slots = s.n;
+  for (int k = 0; k < s.n; ++k) { t.q[k] = s.B[k]; t.q_rank[k] = s.rank[k]; }
+  t.n_colscale = ratio; t.out = Y; t.ldo = d->out_dim;
+  t.items = L.gitems; t.n_items = L.gcount; t.max_items = (int)L.gmax; t.drop = dp;
+  LORA_TRY(launch_tc_gemm(t, st, LORA_PROF_FROZEN_FWD));
+  return LORA_OK;
+}
+
+// backward, bf16 activations: G, dX, dB and dA on tensor cores
+int run_backward_tc(const lora_desc* d, const DropParams& dp, int64_t T, const void* X,
+                    const void* Wt, int32_t n_seg, const int32_t* seg_start,
+                    const int32_t* seg_slot, const Slots& s, const void* dY, const float* H,
+                    const float* dora_m, const float* dora_n, const void* Y_save, void* dX,
+                    float* dm, void* ws, cudaStream_t st) {
+  Layout L = carve(d, T, n_seg, s.n, s.rank_sum, true, ws);
+  clear_stale();
+  LORA_TRY(launch_make_items(T, n_seg, seg_start, seg_slot, s.n, L.gitems, L.gcount,
+                             (int32_t)L.gmax, nullptr, nullptr, 0, st));
+  LORA_TRY(launch_make_red_items_tc(T, n_seg, seg_start, seg_slot, s.n, L.span_db, L.items_db,
+                                    L.count_db, (int32_t)L.max_db, st));
+  LORA_TRY(launch_make_red_items_tc(T, n_seg, seg_start, seg_slot, s.n, L.span_da, L.items_da,
+                                    L.count_da, (int32_t)L.max_da, st));
+  const float q = dropout_q(d);
+  const SlotInfo si = slot_info(s, q);
+  // A^T (fp32) for the LoRA K-steps of dX; hi/lo split of B^T for G
+  float* At[LORA_MAX_SLOTS];
+  {
+    TransposeTab ta{};
+    SplitTab sp{};
+    sp.K = d->out_dim;
+    sp.transposed = 1;
+    int64_t oa = 0, ob = 0;
+    for (int k = 0; k < s.n; ++k) {
+      At[k] = L.At + oa; oa += (int64_t)s.rank[k] * d->in_dim;
+      ta.src[k] = s.A[k]; ta.dst[k] = At[k]; ta.rows[k] = s.rank[k]; ta.cols[k] = d->in_dim;
+      sp.src[k] = s.B[k]; sp.dst[k] = L.Sb + ob; sp.rank[k] = s.rank[k];
+      ob += 2 * (int64_t)s.rank[k] * d->out_dim;
+    }
+    LORA_TRY(launch_transpose_slots(ta, s.n, d->rank, d->in_dim, st));
+    LORA_TRY(launch_split(sp, s.n, st));
+  }
+  const void* dYp = dY;
+  if (dora_m) {   // DoRA: dY' = dY * (m / n), materialised once in bf16 for every product
+    LORA_TRY(launch_ratio(dora_m, dora_n, d->out_dim, L.ratio, st));
+    LORA_TRY(launch_colscale_bf16(dY, L.ratio, T, d->out_dim, L.dYs, st));
+    dYp = L.dYs;
+  }
+  const void* Xin = X;
+  if (dp.enabled) {
+    LORA_TRY(launch_mask_bf16(X, T, d->in_dim, dp, L.Xd, st));
+    Xin = L.Xd;
+  }
+  // Gs[t, j] = s_k q (dY'[t, :] . B_k[:, j])
+  {
+    TcRowsArgs r{};
+    int64_t ob = 0;
+    for (int k = 0; k < s.n; ++k) {
+      r.s[k] = L.Sb + ob;
+      r.rank[k] = s.rank[k];
+      ob += 2 * (int64_t)s.rank[k] * d->out_dim;
+    }
+    r.a = dYp; r.T = T; r.K = d->out_dim; r.n_slots = s.n;
+    r.NP = np_for(d->rank);
+    r.splits = row_splits(T, n_seg, d->out_dim);
+    r.part = L.rows_part;
+    r.si = si;
+    r.out = L.Gs; r.ldo = d->rank;
+    r.items = L.gitems; r.n_items = L.gcount; r.max_items = (int)L.gmax;
+    LORA_TRY(launch_tc_rows(r, st, LORA_PROF_G));
+  }
+  // dX = dY' W + (Gs A_k) * M
+  if (dX) {
+    TcGemmArgs t{};
+    t.a = dYp; t.T = T; t.b = Wt; t.n_rows = d->in_dim; t.K = d->out_dim;
+    t.p = L.Gs; t.ldp = d->rank; t.n_slots = s.n;
+    for (int k = 0; k < s.n; ++k) { t.q[k] = At[k]; t.q_rank[k] = s.rank[k]; }
+    t.lora_separate = dp.enabled; t.out = dX; t.ldo = d->in_dim;
+    t.items = L.gitems; t.n_items = L.gcount; t.max_items = (int)L.gmax; t.drop = dp;
+    LORA_TRY(launch_tc_gemm(t, st, LORA_PROF_FROZEN_DX));
+  }
+  const size_t split_bytes = (size_t)2 * s.rank_sum * L.ldt * sizeof(uint16_t);
+  ReduceTab rt{};
+  for (int k = 0; k < s.n; ++k) rt.rank[k] = s.rank[k];
+  // dB_k += dY'^T Hs over the slot's tokens (as dB^T rows of the transposed Hs split)
+  {
+    LORA_TRY(launch_split_rows_t(H, d->rank, L.ldt, L.gitems, L.gcount, (int)L.gmax, si, L.HsT,
+                                 split_bytes, st));
+    TcRedArgs a{};
+    for (int k = 0; k < s.n; ++k) {
+      a.st[k] = L.HsT + (int64_t)si.region[k] * L.ldt;
+      a.rank[k] = s.rank[k];
+      rt.out[k] = s.dB[k];
+    }
+    a.n_slots = s.n; a.max_rank = d->rank; a.T = T; a.ldt = L.ldt;
+    a.b = dYp; a.N = d->out_dim; a.part = L.red_part; a.tab = rt; a.transposed = 1;
+    a.items = L.items_db; a.n_items = L.count_db; a.max_items = (int)L.max_db;
+    LORA_TRY(launch_tc_red(a, st, LORA_PROF_RED_DB));
+  }
+  // dA_k += Gs^T Xd over the slot's tokens
+  {
+    LORA_TRY(launch_split_rows_t(L.Gs, d->rank, L.ldt, L.gitems, L.gcount, (int)L.gmax, si,
+                                 L.GsT, split_bytes, st));
+    TcRedArgs a{};
+    for (int k = 0; k < s.n; ++k) {
+      a.st[k] = L.GsT + (int64_t)si.region[k] * L.ldt;
+      a.rank[k] = s.rank[k];
+      rt.out[k] = s.dA[k];
+    }
+    a.n_slots = s.n; a.max_rank = d->rank; a.T = T; a.ldt = L.ldt;
+    a.b = Xin; a.N = d->in_dim; a.part = L.red_part; a.tab = rt; a.transposed = 0;
+    a.items = L.items_da; a.n_items = L.count_da; a.max_items = (int)L.max_da;
+    LORA_TRY(launch_tc_red(a, st, LORA_PROF_RED_DA));
+  }
+  if (dm) LORA_TRY(launch_dora_dm(d->dtype, dY, Y_save, dora_m, T, d->out_dim, dm, st));
+  return LORA_OK;
 }
 
 // forward: shrink then the frozen product with the up-projection as extra K-steps
@@ -189,7 +442,10 @@ int run_forward(const lora_desc* d, const DropParams& dp, int64_t T, const void*
                 int32_t n_seg, const int32_t* seg_start, const int32_t* seg_slot, const Slots& s,
                 const float* ratio_src_m, const float* ratio_src_n, void* Y, float* H, void* ws,
                 cudaStream_t st) {
-  Layout L = carve(d, T, n_seg, s.rank_sum, false, ws);
+  if (d->dtype == LORA_BF16)
+    return run_forward_tc(d, dp, T, X, W, n_seg, seg_start, seg_slot, s, ratio_src_m,
+                          ratio_src_n, Y, H, ws, st);
+  Layout L = carve(d, T, n_seg, s.n, s.rank_sum, false, ws);
   clear_stale();
   LORA_TRY(launch_make_items(T, n_seg, seg_start, seg_slot, s.n, L.gitems, L.gcount, (int32_t)L.gmax,
                              L.ritems, L.rcount, (int32_t)L.rmax, st));
@@ -228,17 +484,7 @@ int run_forward(const lora_desc* d, const DropParams& dp, int64_t T, const void*
     a.n_colscale = ratio;
     a.out = Y; a.ldo = d->out_dim; a.n_out = d->out_dim;
     a.drop = dp;
-    if (d->dtype == LORA_BF16) {
-      TcGemmArgs t{};
-      t.a = X; t.T = T; t.b = W; t.n_rows = d->out_dim; t.K = d->in_dim;
-      t.p = H; t.ldp = d->rank; t.n_slots = s.n;
-      for (int k = 0; k < s.n; ++k) { t.q[k] = s.B[k]; t.q_rank[k] = s.rank[k]; }
-      t.n_colscale = ratio; t.out = Y; t.ldo = d->out_dim;
-      t.items = L.gitems; t.n_items = L.gcount; t.max_items = (int)L.gmax; t.drop = dp;
-      LORA_TRY(launch_tc_gemm(t, st, LORA_PROF_FROZEN_FWD));
-    } else {
-      LORA_TRY(launch_tok_gemm(d->dtype, d->dtype, d->dtype, 128, a, (int)L.gmax, st, LORA_PROF_FROZEN_FWD));
-    }
+    LORA_TRY(launch_tok_gemm(d->dtype, d->dtype, d->dtype, 128, a, (int)L.gmax, st, LORA_PROF_FROZEN_FWD));
   }
   return LORA_OK;
 }
@@ -247,7 +493,10 @@ int run_backward(const lora_desc* d, const DropParams& dp, int64_t T, const void
                  int32_t n_seg, const int32_t* seg_start, const int32_t* seg_slot, const Slots& s,
                  const void* dY, const float* H, const float* dora_m, const float* dora_n,
                  const void* Y_save, void* dX, float* dm, void* ws, cudaStream_t st) {
-  Layout L = carve(d, T, n_seg, s.rank_sum, true, ws);
+  if (d->dtype == LORA_BF16)
+    return run_backward_tc(d, dp, T, X, Wt, n_seg, seg_start, seg_slot, s, dY, H, dora_m, dora_n,
+                           Y_save, dX, dm, ws, st);
+  Layout L = carve(d, T, n_seg, s.n, s.rank_sum, true, ws);
   clear_stale();
   LORA_TRY(launch_make_items(T, n_seg, seg_start, seg_slot, s.n, L.gitems, L.gcount, (int32_t)L.gmax,
                              L.ritems, L.rcount, (int32_t)L.rmax, st));
@@ -301,22 +550,7 @@ int run_backward(const lora_desc* d, const DropParams& dp, int64_t T, const void
     a.alpha = 1.f;
     a.out = dX; a.ldo = d->in_dim; a.n_out = d->in_dim;
     a.drop = dp;
-    if (d->dtype == LORA_BF16) {
-      const void* dYp = dY;
-      if (ratio) {   // DoRA: dY' = dY * (m / n) along K, materialised once in bf16
-        LORA_TRY(launch_colscale_bf16(dY, ratio, T, d->out_dim, L.dYs, st));
-        dYp = L.dYs;
-      }
-      TcGemmArgs t{};
-      t.a = dYp; t.T = T; t.b = Wt; t.n_rows = d->in_dim; t.K = d->out_dim;
-      t.p = L.Gs; t.ldp = d->rank; t.n_slots = s.n;
-      for (int k = 0; k < s.n; ++k) { t.q[k] = At[k]; t.q_rank[k] = s.rank[k]; }
-      t.lora_separate = dp.enabled; t.out = dX; t.ldo = d->in_dim;
-      t.items = L.gitems; t.n_items = L.gcount; t.max_items = (int)L.gmax; t.drop = dp;
-      LORA_TRY(launch_tc_gemm(t, st, LORA_PROF_FROZEN_DX));
-    } else {
-      LORA_TRY(launch_tok_gemm(d->dtype, d->dtype, d->dtype, 128, a, (int)L.gmax, st, LORA_PROF_FROZEN_DX));
-    }
+    LORA_TRY(launch_tok_gemm(d->dtype, d->dtype, d->dtype, 128, a, (int)L.gmax, st, LORA_PROF_FROZEN_DX));
   }
   ReduceTab rt{};
   for (int k = 0; k < s.n; ++k) rt.rank[k] = s.rank[k];
@@ -394,7 +628,7 @@ double lora_lr_at(int32_t kind, double base, uint64_t step, uint64_t warmup, uin
 
 size_t lora_workspace_size(const lora_desc* d, int64_t T) {
   if (check_desc(d, T, false) != LORA_OK) return 0;
-  return ws_size(d, T, -1, d->rank);
+  return ws_size(d, T, -1, 1, d->rank);
 }
 
 size_t multi_lora_workspace_size(const lora_desc* d, int64_t T, int32_t n_seg, int32_t n_slots,
@@ -402,7 +636,7 @@ size_t multi_lora_workspace_size(const lora_desc* d, int64_t T, int32_t n_seg, i
   if (check_desc(d, T, true) != LORA_OK || n_seg < 0) return 0;
   Slots s;
   if (slots_from_table(d, n_slots, slots, false, s) != LORA_OK) return 0;
-  return ws_size(d, T, n_seg, s.rank_sum);
+  return ws_size(d, T, n_seg, s.n, s.rank_sum);
 }
 
 int lora_prepare_weight(const lora_desc* d, const void* W, void* W_t, void* stream) {
@@ -438,7 +672,7 @@ int lora_forward(const lora_desc* d, const lora_ctx* c, int64_t T, const void* X
   if (!al16(X) || !al16(W) || !al16(A) || !al16(B) || !al16(Y) || !al16(H_save) || !al16(ws))
     return LORA_ERR_ALIGN;
   if (d->dora && (!al16(dora_m) || !al16(dora_n))) return LORA_ERR_ALIGN;
-  if (ws_bytes < ws_size(d, T, -1, d->rank)) return LORA_ERR_WORKSPACE;
+  if (ws_bytes < ws_size(d, T, -1, 1, d->rank)) return LORA_ERR_WORKSPACE;
   if (T == 0) return LORA_OK;
   Slots s;
   single_slot(d, A, B, nullptr, nullptr, s);
@@ -462,7 +696,7 @@ int lora_backward(const lora_desc* d, const lora_ctx* c, int64_t T, const void* 
     return LORA_ERR_ALIGN;
   if (d->dora && (!al16(dora_m) || !al16(dora_n) || !al16(Y_save) || !al16(dm)))
     return LORA_ERR_ALIGN;
-  if (ws_bytes < ws_size(d, T, -1, d->rank)) return LORA_ERR_WORKSPACE;
+  if (ws_bytes < ws_size(d, T, -1, 1, d->rank)) return LORA_ERR_WORKSPACE;
   if (T == 0) return LORA_OK;
   Slots s;
   single_slot(d, A, B, dA, dB, s);
@@ -484,7 +718,7 @@ int multi_lora_forward(const lora_desc* d, const lora_ctx* c, int64_t T, const v
   if (n_seg < 0 || (n_seg > 0 && (!d_seg_start || !d_seg_slot))) return LORA_ERR_INVALID;
   if (!X || !W || !Y || !H_save || !ws) return LORA_ERR_INVALID;
   if (!al16(X) || !al16(W) || !al16(Y) || !al16(H_save) || !al16(ws)) return LORA_ERR_ALIGN;
-  if (ws_bytes < ws_size(d, T, n_seg, s.rank_sum)) return LORA_ERR_WORKSPACE;
+  if (ws_bytes < ws_size(d, T, n_seg, s.n, s.rank_sum)) return LORA_ERR_WORKSPACE;
   if (T == 0) return LORA_OK;
   return run_forward(d, dp, T, X, W, n_seg, n_seg ? d_seg_start : nullptr,
                      n_seg ? d_seg_slot : nullptr, s, nullptr, nullptr, Y, H_save, ws,
@@ -506,7 +740,7 @@ int multi_lora_backward(const lora_desc* d, const lora_ctx* c, int64_t T, const 
   if (!X || !W_t || !dY || !H_save || !ws) return LORA_ERR_INVALID;
   if (!al16(X) || !al16(W_t) || !al16(dY) || !al16(H_save) || !al16(ws) || (dX && !al16(dX)))
     return LORA_ERR_ALIGN;
-  if (ws_bytes < ws_size(d, T, n_seg, s.rank_sum)) return LORA_ERR_WORKSPACE;
+  if (ws_bytes < ws_size(d, T, n_seg, s.n, s.rank_sum)) return LORA_ERR_WORKSPACE;
   if (T == 0) return LORA_OK;
   return run_backward(d, dp, T, X, W_t, n_seg, n_seg ? d_seg_start : nullptr,
                       n_seg ? d_seg_slot : nullptr, s, dY, H_save, nullptr, nullptr, nullptr, dX,

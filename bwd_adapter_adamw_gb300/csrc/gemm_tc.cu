@@ -21,11 +21,31 @@
 #include <cstring>
 #include <mutex>
 
-#include "lora_kernels.h"
+#include "tc_ptx.cuh"
 
 namespace lora {
+namespace tc {
+namespace {
+__device__ uint32_t g_tc_error = 0;
+std::mutex g_err_mu;
+uint32_t* g_err_ptr[64] = {};
+}  // namespace
+
+uint32_t* error_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(g_err_mu);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_tc_error) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<uint32_t*>(p);
+  }
+  return g_err_ptr[dev];
+}
+}  // namespace tc
 
 namespace {
+using namespace tc;
 
 constexpr int kBM = 128;
 constexpr int kBN = 256;
@@ -35,9 +55,8 @@ constexpr int kBBytes = kBN * 128;   // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kThreads = 192;
 constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*barriers*/ + 1024 /*alignment*/;
-constexpr unsigned long long kWaitCycles = 1ull << 33;   // ~4 s at 2 GHz
-
-__device__ uint32_t g_tc_error = 0;   // bit 0: producer, 1: MMA, 2: epilogue wait timed out
+constexpr uint32_t kIdescBF16 = tc::idesc(tc::kFmtBF16, kBM, kBN);
+constexpr uint32_t kIdescTF32 = tc::idesc(tc::kFmtTF32, kBM, kBN);
 
 struct TcParams {
   CUtensorMap ta;                       // A [rows, K] bf16, box {64, 128}
@@ -46,6 +65,7 @@ struct TcParams {
   CUtensorMap tq[LORA_MAX_SLOTS];       // Q_slot [N, r] fp32, box {32, 256}
   const TokenItem* items;
   const int32_t* n_items;
+  uint32_t* err;
   int32_t nk_main;
   int32_t has_lora;
   int32_t lora_separate;
@@ -56,141 +76,6 @@ struct TcParams {
   int64_t n_out;
   DropParams drop;
 };
-
-// ---- PTX wrappers -------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-               "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}\n"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Bounded wait: false (and an error bit) if the phase has not completed within kWaitCycles.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t err_bit) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > kWaitCycles) {
-      atomicOr(&g_tc_error, err_bit);
-      return false;
-    }
-  }
-  return true;
-}
-
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
-                                            int32_t c0, int32_t c1) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
-      : "memory");
-}
-
-__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                   smem_u32(slot)),
-               "r"(ncols));
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
-}
-
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols));
-}
-
-__device__ __forceinline__ void fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// K-major operand tile in 128-byte swizzled rows: 8-row groups 1024 bytes apart (SBO), leading
-// offset unused for swizzled K-major, descriptor version 1, swizzle mode 2 (128B).
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
-  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
-         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-
-// Instruction descriptor: fp32 accumulate (bits 4-5 = 1), A/B formats (bits 7-9, 10-12),
-// K-major both, N >> 3 at bit 17, M >> 4 at bit 24.
-constexpr uint32_t idesc(uint32_t fmt) {
-  return (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(kBN >> 3) << 17) |
-         ((uint32_t)(kBM >> 4) << 24);
-}
-constexpr uint32_t kIdescBF16 = idesc(1);   // kind::f16 with bf16 operands
-constexpr uint32_t kIdescTF32 = idesc(2);   // kind::tf32
-
-__device__ __forceinline__ void umma_bf16(uint32_t d, uint64_t a, uint64_t b, uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d),
-      "l"(a), "l"(b), "r"(kIdescBF16), "r"(acc));
-}
-
-__device__ __forceinline__ void umma_tf32(uint32_t d, uint64_t a, uint64_t b, uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d),
-      "l"(a), "l"(b), "r"(kIdescTF32), "r"(acc));
-}
-
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          smem_u32(bar))
-      : "memory");
-}
-
-// 32 consecutive fp32 columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
-      "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
-      "%30, %31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-__device__ __forceinline__ void store8(__nv_bfloat16* p, const float* v) {
-  uint4 u;
-  __nv_bfloat162 h0 = __floats2bfloat162_rn(v[0], v[1]);
-  __nv_bfloat162 h1 = __floats2bfloat162_rn(v[2], v[3]);
-  __nv_bfloat162 h2 = __floats2bfloat162_rn(v[4], v[5]);
-  __nv_bfloat162 h3 = __floats2bfloat162_rn(v[6], v[7]);
-  u.x = *reinterpret_cast<uint32_t*>(&h0);
-  u.y = *reinterpret_cast<uint32_t*>(&h1);
-  u.z = *reinterpret_cast<uint32_t*>(&h2);
-  u.w = *reinterpret_cast<uint32_t*>(&h3);
-  *reinterpret_cast<uint4*>(p) = u;
-}
 
 // ---- the kernel ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__ TcParams p) {
@@ -237,7 +122,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
       for (int kb = 0; kb < nk; ++kb) {
         const int s = kb % kStages;
         const uint32_t ph = (uint32_t)(kb / kStages) & 1u;
-        if (kb >= kStages && !mbar_wait(&empty_bar[s], ph ^ 1u, 1u)) break;
+        if (kb >= kStages && !mbar_wait(&empty_bar[s], ph ^ 1u, 1u, p.err)) break;
         uint8_t* sa = tiles + s * kStageBytes;
         uint8_t* sb = sa + kABytes;
         mbar_expect_tx(&full_bar[s], kStageBytes);
@@ -253,7 +138,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
       }
       // drain: every issued load must have landed before the CTA may exit
       for (int kb = (issued > kStages ? issued - kStages : 0); kb < issued; ++kb)
-        if (!mbar_wait(&full_bar[kb % kStages], (uint32_t)(kb / kStages) & 1u, 1u)) break;
+        if (!mbar_wait(&full_bar[kb % kStages], (uint32_t)(kb / kStages) & 1u, 1u, p.err)) break;
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -261,7 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
       for (int kb = 0; kb < nk && ok; ++kb) {
         const int s = kb % kStages;
         const uint32_t ph = (uint32_t)(kb / kStages) & 1u;
-        if (!mbar_wait(&full_bar[s], ph, 2u)) { ok = false; break; }
+        if (!mbar_wait(&full_bar[s], ph, 2u, p.err)) { ok = false; break; }
         fence_after();
         const uint32_t sa = smem_u32(tiles + s * kStageBytes);
         const uint32_t sb = sa + kABytes;
@@ -269,12 +154,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
         if (kb < p.nk_main) {
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            umma_bf16(tmem, da + 2 * k, db + 2 * k, (kb > 0 || k > 0) ? 1u : 0u);
+            umma_f16(tmem, da + 2 * k, db + 2 * k, kIdescBF16, (kb > 0 || k > 0) ? 1u : 0u);
         } else {
           const uint32_t d = sep ? tmem + 256u : tmem;
           const bool first = sep && kb == p.nk_main;
 #pragma unroll
-          for (int k = 0; k < 4; ++k) umma_tf32(d, da + 2 * k, db + 2 * k, (first && k == 0) ? 0u : 1u);
+          for (int k = 0; k < 4; ++k) umma_tf32(d, da + 2 * k, db + 2 * k, kIdescTF32, (first && k == 0) ? 0u : 1u);
         }
         umma_commit(&empty_bar[s]);
       }
@@ -287,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
     const int64_t m = (int64_t)m0 + row;
     const bool row_ok = m < it.t1;
     // warp-uniform decision: the TMEM loads below are .sync.aligned
-    const bool ready = __all_sync(0xffffffffu, mbar_wait(acc_bar, 0u, 4u));
+    const bool ready = __all_sync(0xffffffffu, mbar_wait(acc_bar, 0u, 4u, p.err));
     if (ready) {
       fence_after();
       __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
@@ -340,7 +225,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-bool make_map(CUtensorMap* map, const void* ptr, CUtensorMapDataType dt, int elem, uint64_t inner,
+}  // namespace
+
+namespace tc {
+bool make_map_2d(CUtensorMap* map, const void* ptr, CUtensorMapDataType dt, int elem, uint64_t inner,
               uint64_t outer, uint64_t row_elems, uint32_t box_inner, uint32_t box_outer) {
   auto fn = encode_fn();
   if (!fn) return false;
@@ -353,29 +241,31 @@ bool make_map(CUtensorMap* map, const void* ptr, CUtensorMapDataType dt, int ele
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-}  // namespace
+}  // namespace tc
 
 cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st, int prof_kind) {
   static TcParams prm;   // large: filled per call on the host, copied into the launch
   static std::mutex mu;
   std::lock_guard<std::mutex> lk(mu);
   std::memset(&prm, 0, sizeof(prm));
-  if (!make_map(&prm.ta, a.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.K, a.T, a.K, 64, kBM) ||
-      !make_map(&prm.tb, a.b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.K, a.n_rows, a.K, 64, kBN))
+  if (!tc::make_map_2d(&prm.ta, a.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.K, a.T, a.K, 64, kBM) ||
+      !tc::make_map_2d(&prm.tb, a.b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.K, a.n_rows, a.K, 64, kBN))
     return cudaErrorInvalidValue;
   prm.has_lora = a.p != nullptr;
   if (a.p) {
-    if (!make_map(&prm.tp, a.p, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.ldp, a.T, a.ldp, 32, kBM))
+    if (!tc::make_map_2d(&prm.tp, a.p, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.ldp, a.T, a.ldp, 32, kBM))
       return cudaErrorInvalidValue;
     for (int k = 0; k < a.n_slots; ++k) {
       prm.q_rank[k] = a.q_rank[k];
-      if (!make_map(&prm.tq[k], a.q[k], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.q_rank[k], a.n_rows,
+      if (!tc::make_map_2d(&prm.tq[k], a.q[k], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.q_rank[k], a.n_rows,
                     a.q_rank[k], 32, kBN))
         return cudaErrorInvalidValue;
     }
   }
   prm.items = a.items;
   prm.n_items = a.n_items;
+  prm.err = tc::error_word();
+  if (!prm.err) return cudaErrorInvalidDevice;
   prm.nk_main = (int32_t)((a.K + 63) / 64);
   prm.lora_separate = a.lora_separate;
   prm.n_colscale = a.n_colscale;
@@ -399,10 +289,10 @@ cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st, int prof_kind) 
 }
 
 cudaError_t read_tc_error(uint32_t* out, bool reset) {
-  cudaError_t e = cudaMemcpyFromSymbol(out, g_tc_error, sizeof(uint32_t));
+  cudaError_t e = cudaMemcpyFromSymbol(out, tc::g_tc_error, sizeof(uint32_t));
   if (e != cudaSuccess || !reset) return e;
   const uint32_t zero = 0;
-  return cudaMemcpyToSymbol(g_tc_error, &zero, sizeof(uint32_t));
+  return cudaMemcpyToSymbol(tc::g_tc_error, &zero, sizeof(uint32_t));
 }
 
 }  // namespace lora

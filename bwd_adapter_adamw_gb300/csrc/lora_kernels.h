@@ -93,6 +93,71 @@ struct TcGemmArgs {
 cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st, int prof_kind);
 cudaError_t read_tc_error(uint32_t* out, bool reset);
 
+// out_slot[j, i] (+)= sum over items of `slot` of part[item][...]; see lowrank.cu
+struct ReduceTab {
+  float* out[LORA_MAX_SLOTS];
+  int32_t rank[LORA_MAX_SLOTS];
+};
+
+// ---- lowrank_tc.cu: tensor-core low-rank products (bf16 activations) ----
+struct SlotInfo {
+  int32_t rank[LORA_MAX_SLOTS];
+  float alpha[LORA_MAX_SLOTS];
+  int32_t region[LORA_MAX_SLOTS];   // first row of the slot in a per-slot [sum 2 r, ldt] buffer
+};
+struct TcRowsArgs {                 // out[t, j] = alpha * (A[t, :] . (S_hi[j] + S_lo[j]))
+  const void* a;                    // [T, K] bf16
+  int64_t T;
+  int64_t K;
+  const uint16_t* s[LORA_MAX_SLOTS];   // per slot [2 r, K] bf16 split (hi rows, lo rows)
+  int32_t rank[LORA_MAX_SLOTS];
+  int32_t n_slots;
+  int32_t NP;                       // MMA N: 16, 32, 64 or 128 (>= 2 * max rank)
+  int32_t splits;                   // K splits
+  float* part;                      // [splits][T][NP] scratch
+  SlotInfo si;
+  float* out;                       // [T, ldo] fp32
+  int64_t ldo;
+  const TokenItem* items;
+  const int32_t* n_items;
+  int max_items;
+};
+struct TcRedArgs {                  // dst_slot += (ST_hi + ST_lo)[., t] x B[t, .] over the slot's tokens
+  const uint16_t* st[LORA_MAX_SLOTS];  // per slot [2 r, ldt] bf16 transposed split
+  int32_t rank[LORA_MAX_SLOTS];
+  int32_t n_slots;
+  int32_t max_rank;
+  int64_t T;
+  int64_t ldt;
+  const void* b;                    // [T, N] bf16 (dY' or Xd)
+  int64_t N;
+  float* part;                      // [items][128][N] scratch
+  ReduceTab tab;
+  int32_t transposed;               // 1: dst is [N, r] (dB); 0: dst is [r, N] (dA)
+  const TokenItem* items;           // 64-token aligned runs (launch_make_red_items_tc)
+  const int32_t* n_items;
+  int max_items;
+};
+struct SplitTab {
+  const float* src[LORA_MAX_SLOTS];
+  uint16_t* dst[LORA_MAX_SLOTS];
+  int32_t rank[LORA_MAX_SLOTS];
+  int64_t K;
+  int32_t transposed;               // src is [K, r] instead of [r, K]
+};
+cudaError_t launch_tc_rows(const TcRowsArgs& a, cudaStream_t st, int prof_kind);
+cudaError_t launch_tc_red(const TcRedArgs& a, cudaStream_t st, int prof_kind);
+cudaError_t launch_split(const SplitTab& t, int n, cudaStream_t st);
+cudaError_t launch_split_rows_t(const float* src, int64_t lds, int64_t ldt, const TokenItem* items,
+                                const int32_t* n_items, int max_items, const SlotInfo& si,
+                                uint16_t* dst, size_t dst_bytes, cudaStream_t st);
+cudaError_t launch_make_red_items_tc(int64_t T, int32_t n_seg, const int32_t* seg_start,
+                                     const int32_t* seg_slot, int32_t n_slots, int32_t span_blocks,
+                                     TokenItem* items, int32_t* count, int32_t max_items,
+                                     cudaStream_t st);
+cudaError_t launch_mask_bf16(const void* X, int64_t T, int64_t in_dim, const DropParams& dp,
+                             void* Xd, cudaStream_t st);
+
 // ---- lowrank.cu ----
 cudaError_t launch_colscale_bf16(const void* src, const float* scale, int64_t rows, int64_t cols,
                                  void* dst, cudaStream_t st);
@@ -112,11 +177,6 @@ cudaError_t launch_transpose_slots(const TransposeTab& t, int n, int64_t max_row
 cudaError_t launch_transpose_weight(int dtype, const void* W, void* Wt, int64_t rows, int64_t cols,
                                     cudaStream_t st);
 
-// out_slot[j, i] (+)= sum over items of `slot` of part[item][...]; see lowrank.cu
-struct ReduceTab {
-  float* out[LORA_MAX_SLOTS];
-  int32_t rank[LORA_MAX_SLOTS];
-};
 cudaError_t launch_reduce_parts(const float* part, const TokenItem* items, const int32_t* n_items,
                                 int max_items, int64_t M, int64_t ldp, int transposed,
                                 const ReduceTab& tab, int n_slots, cudaStream_t st);

@@ -20,7 +20,7 @@ __global__ void k_make_items(int64_t T, int32_t n_seg, const int32_t* __restrict
   auto emit = [&](int64_t a, int64_t b, int32_t slot) {
     for (int64_t t = a; t < b; t += kGemmTileT)
       if (ng < gmax) gitems[ng++] = TokenItem{(int32_t)t, (int32_t)min(b, t + kGemmTileT), slot, 0};
-    if (slot >= 0)
+    if (slot >= 0 && ritems)
       for (int64_t t = a; t < b; t += kRedTileT)
         if (nr < rmax) ritems[nr++] = TokenItem{(int32_t)t, (int32_t)min(b, t + kRedTileT), slot, 0};
   };
@@ -41,7 +41,7 @@ __global__ void k_make_items(int64_t T, int32_t n_seg, const int32_t* __restrict
   }
   if (cursor < T) emit(cursor, T, -1);
   *gcount = ng;
-  *rcount = nr;
+  if (rcount) *rcount = nr;
 }
 
 // 32 x 32 shared-memory tile transpose of fp32 matrices, one matrix per blockIdx.z.

@@ -1,0 +1,580 @@
+// Tensor-core low-rank products for bf16 activations (sm_103a): the shrink Hs = s' Xd A^T, the
+// G = s' dY' B product and the token reductions dA += Gs^T Xd, dB += dY'^T Hs
+// ("8. LoRA Fundamentals", How it works; "Backward Bug Hunts and Vulkan Tiled GEMM", Bug #1 and
+// Bug #2: the adapter gradients as out_prod-style token reductions).
+//
+// The fp32 operand of each product (A, B^T, Hs or Gs) is split into bf16 hi + lo parts
+// (x = hi + lo + O(2^-16 |x|)); both parts are multiplied against the exact bf16 activations, so
+// the products keep fp32-level accuracy while running on kind::f16 tensor cores.
+//
+//  k_tc_rows: part[z][t][j] = sum_{k in split z} A[t, k] S_slot[j, k]   (shrink, G)
+//             M = 128 tokens of one work item, N = NP >= 2 r (hi rows then lo rows), K-major.
+//  k_tc_red:  part[item][m][n] = sum_{t in item} ST_slot[m, t] Bmn[t, n]   (dA, dB^T)
+//             M = 128 (2 r rows of the slot's transposed split), N = 256 columns of dY or X
+//             (MN-major tiles), K = the item's tokens in 64-token blocks.
+// Partials are combined in a fixed order by the finish kernels, so reruns are bitwise equal.
+#include <cstring>
+#include <mutex>
+
+#include "tc_ptx.cuh"
+
+namespace lora {
+
+namespace {
+using namespace tc;
+
+constexpr int kThreads = 192;
+constexpr int kBM = 128;
+
+__device__ __forceinline__ uint16_t bf16_bits(float x) {
+  __nv_bfloat16 h = __float2bfloat16_rn(x);
+  return *reinterpret_cast<uint16_t*>(&h);
+}
+__device__ __forceinline__ float bf16_val(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+
+// ---------------------------------------------------------------------------------------------
+// k_tc_rows
+// ---------------------------------------------------------------------------------------------
+struct RowsParams {
+  CUtensorMap ta;                    // A [T, K] bf16, box {64, 128}
+  CUtensorMap ts[LORA_MAX_SLOTS];    // S_slot [2 r, K] bf16, box {64, NP}
+  const TokenItem* items;
+  const int32_t* n_items;
+  uint32_t* err;
+  int32_t nk;                        // K blocks in total
+  int32_t nk_per_split;
+  float* part;                       // [splits][T][NP]
+  int64_t T;
+};
+
+template <int NP>
+struct RowsCfg {
+  static constexpr int kBBytes = NP * 128;
+  static constexpr int kStageBytes = 16384 + kBBytes;
+  static constexpr int kStages = (NP <= 32) ? 8 : 6;
+  static constexpr int kSmem = kStages * kStageBytes + 1024 + 1024;
+  static constexpr uint32_t kCols = NP < 32 ? 32u : (uint32_t)NP;
+  static constexpr uint32_t kIdesc = idesc(kFmtBF16, kBM, NP);
+};
+
+template <int NP>
+__global__ void __launch_bounds__(kThreads, 1) k_tc_rows(const __grid_constant__ RowsParams p) {
+  using C = RowsCfg<NP>;
+  extern __shared__ uint8_t smem_raw[];
+  const int item = blockIdx.x;
+  if (item >= *p.n_items) return;
+  const TokenItem it = p.items[item];
+  const int z = blockIdx.y;
+  const int kb0 = z * p.nk_per_split;
+  const int kb1 = min(p.nk, kb0 + p.nk_per_split);
+  float* part = p.part + (int64_t)z * p.T * NP;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (it.slot < 0 || kb0 >= kb1) {
+    // no adapter for these tokens (or an empty split): the partial rows are zero
+    for (int r = threadIdx.x; r < it.t1 - it.t0; r += kThreads) {
+      float4* dst = reinterpret_cast<float4*>(part + (int64_t)(it.t0 + r) * NP);
+      for (int j = 0; j < NP / 4; ++j) dst[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    return;
+  }
+  const int nk = kb1 - kb0;
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(base + C::kStages * C::kStageBytes);
+  uint64_t* empty_bar = full_bar + C::kStages;
+  uint64_t* acc_bar = empty_bar + C::kStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_bar + 1);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    mbar_init(acc_bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, C::kCols);
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int issued = 0;
+      for (int i = 0; i < nk; ++i) {
+        const int s = i % C::kStages;
+        const uint32_t ph = (uint32_t)(i / C::kStages) & 1u;
+        if (i >= C::kStages && !mbar_wait(&empty_bar[s], ph ^ 1u, 1u, p.err)) break;
+        uint8_t* sa = base + s * C::kStageBytes;
+        mbar_expect_tx(&full_bar[s], C::kStageBytes);
+        tma_load_2d(sa, &p.ta, &full_bar[s], (kb0 + i) * 64, it.t0);
+        tma_load_2d(sa + 16384, &p.ts[it.slot], &full_bar[s], (kb0 + i) * 64, 0);
+        issued = i + 1;
+      }
+      for (int i = (issued > C::kStages ? issued - C::kStages : 0); i < issued; ++i)
+        if (!mbar_wait(&full_bar[i % C::kStages], (uint32_t)(i / C::kStages) & 1u, 1u, p.err)) break;
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      for (int i = 0; i < nk; ++i) {
+        const int s = i % C::kStages;
+        if (!mbar_wait(&full_bar[s], (uint32_t)(i / C::kStages) & 1u, 2u, p.err)) break;
+        fence_after();
+        const uint32_t sa = smem_u32(base + s * C::kStageBytes);
+        const uint64_t da = smem_desc_sw128(sa), db = smem_desc_sw128(sa + 16384);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          umma_f16(tmem, da + 2 * k, db + 2 * k, C::kIdesc, (i > 0 || k > 0) ? 1u : 0u);
+        umma_commit(&empty_bar[s]);
+      }
+      umma_commit(acc_bar);
+    }
+  } else {
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    const int64_t t = (int64_t)it.t0 + row;
+    const bool ready = __all_sync(0xffffffffu, mbar_wait(acc_bar, 0u, 4u, p.err));
+    if (ready) {
+      fence_after();
+#pragma unroll
+      for (int c = 0; c < NP / 16; ++c) {
+        float v[16];
+        tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * 16), v);
+        if (t < it.t1) {
+          float4* dst = reinterpret_cast<float4*>(part + t * NP + c * 16);
+#pragma unroll
+          for (int g = 0; g < 4; ++g) dst[g] = make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+        }
+      }
+    }
+    fence_before();
+  }
+  __syncthreads();
+  if (warp == 1) {
+    fence_after();
+    tmem_dealloc(tmem, C::kCols);
+  }
+}
+
+// out[t, j] = alpha_slot * sum_z (part[z][t][j] + part[z][t][r + j]) for j < r, 0 for r <= j < ldo.
+__global__ void k_rows_finish(const float* __restrict__ part, int32_t splits, int64_t T, int32_t NP,
+                              const TokenItem* __restrict__ items, const int32_t* __restrict__ n_items,
+                              const SlotInfo si, float* __restrict__ out, int64_t ldo) {
+  const int item = blockIdx.x;
+  if (item >= *n_items) return;
+  const TokenItem it = items[item];
+  const int32_t r = it.slot >= 0 ? si.rank[it.slot] : 0;
+  const float alpha = it.slot >= 0 ? si.alpha[it.slot] : 0.f;
+  const int64_t n = (int64_t)(it.t1 - it.t0) * ldo;
+  for (int64_t e = threadIdx.x; e < n; e += blockDim.x) {
+    const int64_t t = it.t0 + e / ldo;
+    const int j = (int)(e % ldo);
+    float v = 0.f;
+    if (j < r) {
+      for (int z = 0; z < splits; ++z) {
+        const float* pr = part + ((int64_t)z * T + t) * NP;
+        v += pr[j] + pr[r + j];
+      }
+      v *= alpha;
+    }
+    out[t * ldo + j] = v;
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// k_tc_red
+// ---------------------------------------------------------------------------------------------
+struct RedParams {
+  CUtensorMap tst[LORA_MAX_SLOTS];   // ST_slot [2 r, T] bf16 (tokens contiguous), box {64, 128}
+  CUtensorMap tb;                    // B [T, N] bf16, box {64 (n), 64 (t)}
+  const TokenItem* items;
+  const int32_t* n_items;
+  uint32_t* err;
+  int32_t rows2[LORA_MAX_SLOTS];     // 2 r per slot
+  int32_t rstride;                   // partial rows per item (2 * max rank)
+  float* part;                       // [items][rstride][N]
+  int64_t N;
+};
+
+constexpr int kRedBN = 256;
+constexpr int kRedStageBytes = 16384 + 32768;
+constexpr int kRedStages = 4;
+constexpr int kRedSmem = kRedStages * kRedStageBytes + 1024 + 1024;
+constexpr uint32_t kRedIdesc = idesc(kFmtBF16, kBM, kRedBN, false, true);
+
+__global__ void __launch_bounds__(kThreads, 1) k_tc_red(const __grid_constant__ RedParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const int item = blockIdx.y;
+  if (item >= *p.n_items) return;
+  const TokenItem it = p.items[item];
+  if (it.slot < 0) return;
+  const int32_t n0 = blockIdx.x * kRedBN;
+  const int32_t tb0 = it.t0 & ~63;                  // 64-token blocks covering [t0, t1)
+  const int nk = (it.t1 - tb0 + 63) / 64;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(base + kRedStages * kRedStageBytes);
+  uint64_t* empty_bar = full_bar + kRedStages;
+  uint64_t* acc_bar = empty_bar + kRedStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_bar + 1);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kRedStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    mbar_init(acc_bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, 256u);
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int issued = 0;
+      for (int i = 0; i < nk; ++i) {
+        const int s = i % kRedStages;
+        const uint32_t ph = (uint32_t)(i / kRedStages) & 1u;
+        if (i >= kRedStages && !mbar_wait(&empty_bar[s], ph ^ 1u, 1u, p.err)) break;
+        uint8_t* sa = base + s * kRedStageBytes;
+        mbar_expect_tx(&full_bar[s], kRedStageBytes);
+        const int32_t t = tb0 + i * 64;
+        tma_load_2d(sa, &p.tst[it.slot], &full_bar[s], t, 0);
+#pragma unroll
+        for (int b = 0; b < 4; ++b) tma_load_2d(sa + 16384 + b * 8192, &p.tb, &full_bar[s], n0 + 64 * b, t);
+        issued = i + 1;
+      }
+      for (int i = (issued > kRedStages ? issued - kRedStages : 0); i < issued; ++i)
+        if (!mbar_wait(&full_bar[i % kRedStages], (uint32_t)(i / kRedStages) & 1u, 1u, p.err)) break;
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      for (int i = 0; i < nk; ++i) {
+        const int s = i % kRedStages;
+        if (!mbar_wait(&full_bar[s], (uint32_t)(i / kRedStages) & 1u, 2u, p.err)) break;
+        fence_after();
+        const uint32_t sa = smem_u32(base + s * kRedStageBytes);
+        const uint64_t da = smem_desc_sw128(sa);
+        const uint64_t db = smem_desc_sw128_mn(sa + 16384, 8192);
+        // K step of 16 tokens: +32 bytes in the K-major A rows, +2 KB (two 8-row atoms) in B
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          umma_f16(tmem, da + 2 * k, db + 128 * k, kRedIdesc, (i > 0 || k > 0) ? 1u : 0u);
+        umma_commit(&empty_bar[s]);
+      }
+      umma_commit(acc_bar);
+    }
+  } else {
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    const bool row_ok = row < p.rows2[it.slot];
+    float* part = p.part + ((int64_t)item * p.rstride + row) * p.N;
+    const bool ready = __all_sync(0xffffffffu, mbar_wait(acc_bar, 0u, 4u, p.err));
+    if (ready) {
+      fence_after();
+      for (int c = 0; c < kRedBN / 32; ++c) {
+        float v[32];
+        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * 32), v);
+        const int64_t nb = (int64_t)n0 + c * 32;
+        if (row_ok) {
+#pragma unroll
+          for (int g = 0; g < 8; ++g)
+            if (nb + 4 * g + 4 <= p.N)
+              *reinterpret_cast<float4*>(part + nb + 4 * g) =
+                  make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+        }
+      }
+    }
+    fence_before();
+  }
+  __syncthreads();
+  if (warp == 1) {
+    fence_after();
+    tmem_dealloc(tmem, 256u);
+  }
+}
+
+// dst_slot += sum over the slot's items (in item order) of hi + lo partial rows:
+// transposed == 0: dst[j * N + n] (dA [r, N]); transposed == 1: dst[n * r + j] (dB [N, r]).
+__global__ void k_red_finish(const float* __restrict__ part, const TokenItem* __restrict__ items,
+                             const int32_t* __restrict__ n_items, int64_t N, int32_t rstride,
+                             int transposed, const ReduceTab tab) {
+  const int slot = blockIdx.y;
+  const int32_t r = tab.rank[slot];
+  float* dst = tab.out[slot];
+  const int32_t ni = *n_items;
+  const int64_t total = (int64_t)r * N;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t j = e / N, n = e - j * N;
+    float acc = 0.f;
+    bool any = false;
+    for (int32_t i = 0; i < ni; ++i) {
+      if (items[i].slot != slot) continue;
+      const float* pr = part + (int64_t)i * rstride * N;
+      acc += pr[j * N + n] + pr[(j + r) * N + n];
+      any = true;
+    }
+    if (!any) continue;
+    if (transposed)
+      dst[n * r + j] += acc;
+    else
+      dst[j * N + n] += acc;
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// split helpers
+// ---------------------------------------------------------------------------------------------
+// dst [2 r, K] bf16: rows j < r = hi(src[j, :]), rows r + j = lo(src[j, :]); src [r, K] fp32.
+// transposed: src is [K, r] and row j of dst takes column j of src.
+__global__ void k_split(const SplitTab tab) {
+  const int z = blockIdx.z;
+  const int32_t r = tab.rank[z];
+  const int64_t K = tab.K;
+  const float* src = tab.src[z];
+  uint16_t* dst = tab.dst[z];
+  const int64_t n = (int64_t)r * K;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    int64_t j, k;
+    if (tab.transposed) {   // walk src row-major for coalesced reads
+      k = e / r;
+      j = e - k * r;
+    } else {
+      j = e / K;
+      k = e - j * K;
+    }
+    const float x = tab.transposed ? src[k * r + j] : src[j * K + k];
+    const uint16_t hb = bf16_bits(x);
+    dst[j * K + k] = hb;
+    dst[(r + j) * K + k] = bf16_bits(x - bf16_val(hb));
+  }
+}
+
+// Transposed split of H / G rows per slot region: for token t of an item with slot s and j < r_s,
+// dst[region_s + j][t] = hi(src[t, j]), dst[region_s + r_s + j][t] = lo(src[t, j]).
+__global__ void k_split_rows_t(const float* __restrict__ src, int64_t lds, int64_t ldt,
+                               const TokenItem* __restrict__ items, const int32_t* __restrict__ n_items,
+                               const SlotInfo si, uint16_t* __restrict__ dst) {
+  const int item = blockIdx.x;
+  if (item >= *n_items) return;
+  const TokenItem it = items[item];
+  if (it.slot < 0) return;
+  const int32_t r = si.rank[it.slot];
+  uint16_t* d = dst + (int64_t)si.region[it.slot] * ldt;
+  const int n = it.t1 - it.t0;
+  for (int j = 0; j < r; ++j)
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+      const int64_t t = it.t0 + i;
+      const float x = src[t * lds + j];
+      const uint16_t hb = bf16_bits(x);
+      d[(int64_t)j * ldt + t] = hb;
+      d[(int64_t)(r + j) * ldt + t] = bf16_bits(x - bf16_val(hb));
+    }
+}
+
+// Reduction work items: for every slot, the absolute 64-token blocks that hold any of its tokens
+// (segment walk as in the token items), merged into runs and cut into spans of at most
+// span_blocks blocks. A block shared by two slots is listed for both; each slot's transposed
+// operand is zero at the other slot's tokens, so every token counts exactly once.
+__global__ void k_make_red_items_tc(int64_t T, int32_t n_seg, const int32_t* __restrict__ seg_start,
+                                    const int32_t* __restrict__ seg_slot, int32_t n_slots,
+                                    int32_t span_blocks, TokenItem* items, int32_t* count,
+                                    int32_t max_items) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  int32_t n = 0;
+  auto emit_run = [&](int64_t b0, int64_t b1, int32_t slot) {
+    for (int64_t b = b0; b < b1; b += span_blocks)
+      if (n < max_items)
+        items[n++] = TokenItem{(int32_t)(b * 64), (int32_t)(min(b1, b + span_blocks) * 64), slot, 0};
+  };
+  const int32_t nsegs = seg_start ? n_seg : (n_seg < 0 ? 1 : 0);
+  for (int32_t s = 0; s < n_slots; ++s) {
+    int64_t cursor = 0, rb = -1, re = -1;
+    for (int32_t k = 0; k < nsegs; ++k) {
+      int64_t a = seg_start ? (int64_t)seg_start[k] : 0;
+      int64_t b = seg_start ? (int64_t)seg_start[k + 1] : T;
+      int32_t slot = seg_slot ? seg_slot[k] : 0;
+      if (slot < 0 || slot >= n_slots) slot = -1;
+      a = max((int64_t)0, min(a, T));
+      b = max((int64_t)0, min(b, T));
+      if (a < cursor) a = cursor;
+      if (b <= a) continue;
+      cursor = b;
+      if (slot != s) continue;
+      const int64_t ba = a / 64, bb = (b + 63) / 64;
+      if (re >= 0 && ba <= re) {
+        re = max(re, bb);
+      } else {
+        if (re >= 0) emit_run(rb, re, s);
+        rb = ba;
+        re = bb;
+      }
+    }
+    if (re >= 0) emit_run(rb, re, s);
+  }
+  *count = n;
+}
+
+// Xd = bf16(M * X): the masked operand of the shrink and of dA when dropout is on.
+__global__ void k_mask_bf16(const __nv_bfloat16* __restrict__ X, int64_t T, int64_t in_dim,
+                            const DropParams dp, __nv_bfloat16* __restrict__ Xd) {
+  const int64_t n = T * in_dim;
+  const __nv_bfloat16 zero = __float2bfloat16_rn(0.f);
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = e / in_dim, i = e - t * in_dim;
+    Xd[e] = drop_keep(dp, t, i) ? X[e] : zero;
+  }
+}
+
+template <typename K>
+cudaError_t set_smem(K kernel, int bytes) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------------------------
+cudaError_t launch_tc_rows(const TcRowsArgs& a, cudaStream_t st, int prof_kind) {
+  static RowsParams prm;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lk(mu);
+  std::memset(&prm, 0, sizeof(prm));
+  const int NP = a.NP;
+  if (!tc::make_map_2d(&prm.ta, a.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.K, a.T, a.K, 64, kBM))
+    return cudaErrorInvalidValue;
+  for (int k = 0; k < a.n_slots; ++k)
+    if (!tc::make_map_2d(&prm.ts[k], a.s[k], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.K,
+                         2 * (uint64_t)a.rank[k], a.K, 64, (uint32_t)NP))
+      return cudaErrorInvalidValue;
+  prm.items = a.items;
+  prm.n_items = a.n_items;
+  prm.err = tc::error_word();
+  if (!prm.err) return cudaErrorInvalidDevice;
+  prm.nk = (int32_t)((a.K + 63) / 64);
+  prm.nk_per_split = (prm.nk + a.splits - 1) / a.splits;
+  prm.part = a.part;
+  prm.T = a.T;
+  dim3 grid((unsigned)a.max_items, (unsigned)a.splits);
+  cudaError_t e = cudaSuccess;
+  prof_begin(prof_kind, st);
+  switch (NP) {
+#define LORA_ROWS_CASE(NPV)                                                        \
+  case NPV: {                                                                      \
+    static bool attr = false;                                                      \
+    if (!attr) {                                                                   \
+      e = set_smem(k_tc_rows<NPV>, RowsCfg<NPV>::kSmem);                           \
+      if (e != cudaSuccess) return e;                                              \
+      attr = true;                                                                 \
+    }                                                                              \
+    k_tc_rows<NPV><<<grid, kThreads, RowsCfg<NPV>::kSmem, st>>>(prm);              \
+    break;                                                                         \
+  }
+    LORA_ROWS_CASE(16)
+    LORA_ROWS_CASE(32)
+    LORA_ROWS_CASE(64)
+    LORA_ROWS_CASE(128)
+#undef LORA_ROWS_CASE
+    default:
+      return cudaErrorInvalidValue;
+  }
+  prof_end(prof_kind, st);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  prof_begin(0, st);
+  k_rows_finish<<<(unsigned)a.max_items, 256, 0, st>>>(a.part, a.splits, a.T, NP, a.items,
+                                                        a.n_items, a.si, a.out, a.ldo);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tc_red(const TcRedArgs& a, cudaStream_t st, int prof_kind) {
+  static RedParams prm;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lk(mu);
+  std::memset(&prm, 0, sizeof(prm));
+  for (int k = 0; k < a.n_slots; ++k) {
+    if (!tc::make_map_2d(&prm.tst[k], a.st[k], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T,
+                         2 * (uint64_t)a.rank[k], a.ldt, 64, kBM))
+      return cudaErrorInvalidValue;
+    prm.rows2[k] = 2 * a.rank[k];
+  }
+  if (!tc::make_map_2d(&prm.tb, a.b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.N, a.T, a.N, 64, 64))
+    return cudaErrorInvalidValue;
+  prm.items = a.items;
+  prm.n_items = a.n_items;
+  prm.err = tc::error_word();
+  if (!prm.err) return cudaErrorInvalidDevice;
+  prm.part = a.part;
+  prm.N = a.N;
+  prm.rstride = 2 * a.max_rank;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = set_smem(k_tc_red, kRedSmem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  dim3 grid((unsigned)((a.N + kRedBN - 1) / kRedBN), (unsigned)a.max_items);
+  prof_begin(prof_kind, st);
+  k_tc_red<<<grid, kThreads, kRedSmem, st>>>(prm);
+  prof_end(prof_kind, st);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  int64_t total = (int64_t)a.max_rank * a.N;
+  int64_t blocks = (total + 255) / 256;
+  if (blocks > 8192) blocks = 8192;
+  prof_begin(0, st);
+  k_red_finish<<<dim3((unsigned)blocks, (unsigned)a.n_slots), 256, 0, st>>>(
+      a.part, a.items, a.n_items, a.N, 2 * a.max_rank, a.transposed, a.tab);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_split(const SplitTab& t, int n, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  int64_t most = 0;
+  for (int k = 0; k < n; ++k) most = (int64_t)t.rank[k] * t.K > most ? (int64_t)t.rank[k] * t.K : most;
+  int64_t blocks = (most + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  prof_begin(0, st);
+  k_split<<<dim3((unsigned)blocks, 1, (unsigned)n), 256, 0, st>>>(t);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_split_rows_t(const float* src, int64_t lds, int64_t ldt, const TokenItem* items,
+                                const int32_t* n_items, int max_items, const SlotInfo& si,
+                                uint16_t* dst, size_t dst_bytes, cudaStream_t st) {
+  if (max_items <= 0) return cudaSuccess;
+  cudaError_t e = cudaMemsetAsync(dst, 0, dst_bytes, st);
+  if (e != cudaSuccess) return e;
+  prof_begin(0, st);
+  k_split_rows_t<<<(unsigned)max_items, 128, 0, st>>>(src, lds, ldt, items, n_items, si, dst);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_make_red_items_tc(int64_t T, int32_t n_seg, const int32_t* seg_start,
+                                     const int32_t* seg_slot, int32_t n_slots, int32_t span_blocks,
+                                     TokenItem* items, int32_t* count, int32_t max_items,
+                                     cudaStream_t st) {
+  prof_begin(0, st);
+  k_make_red_items_tc<<<1, 32, 0, st>>>(T, n_seg, seg_start, seg_slot, n_slots, span_blocks,
+                                        items, count, max_items);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mask_bf16(const void* X, int64_t T, int64_t in_dim, const DropParams& dp,
+                             void* Xd, cudaStream_t st) {
+  const int64_t n = T * in_dim;
+  if (n <= 0) return cudaSuccess;
+  int64_t blocks = (n + 255) / 256;
+  if (blocks > 16384) blocks = 16384;
+  prof_begin(0, st);
+  k_mask_bf16<<<(unsigned)blocks, 256, 0, st>>>((const __nv_bfloat16*)X, T, in_dim, dp,
+                                                (__nv_bfloat16*)Xd);
+  return cudaGetLastError();
+}
+
+}  // namespace lora

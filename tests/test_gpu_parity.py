@@ -97,8 +97,10 @@ def _check_step(cfg, step, problems, state, s, hp_o, per_chunk, exclude=None):
     errs = dict(errs)
     assert int(step.status.item()) == O.STATUS_OK
     sn = step.scale_norm.cpu().numpy()
-    assert abs(sn[0] - ref.prepared.scale) <= 1e-5 * abs(ref.prepared.scale)
-    assert abs(sn[1] - ref.prepared.norm) <= 1e-5 * abs(ref.prepared.norm)
+    # the norm inherits the gradients' error: fp32 paths ~1e-7; bf16 DoRA reads a bf16 dY*(m/n)
+    tol_norm = 1e-5 if cfg.dtype == "f32" else 1e-3
+    assert abs(sn[0] - ref.prepared.scale) <= tol_norm * abs(ref.prepared.scale)
+    assert abs(sn[1] - ref.prepared.norm) <= tol_norm * abs(ref.prepared.norm)
     # post-step A and B: plain per-tensor bar, with the Adam-conditioning band near g_hat ~ 0
     ct = step.T // cfg.chunks
     n_clause = 0
