@@ -401,10 +401,13 @@ def run_ours(args):
             else cnt["dx_flops_per_launch"]
         avg_kern = statistics.mean(kern_ms) if kern_ms else None
         if cfg.dtype == "f32":
-            peak = 152 * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
-            bound, punit = "alu", "TFLOP/s"
-            note = ("fp32 FMA peak derived: 152 SMs x 128 FP32 lanes x 2 flop x max SM clock "
-                    f"{peaks.get('sm_max_mhz', 2070.0):.0f} MHz")
+            # 3xTF32 on tensor cores: three tf32 products per fp32 product; tf32 dense rate is
+            # the measured bf16 rate x the nominal tf32 : bf16 ratio (1.1 : 2.25)
+            tf32 = peaks["bf16_tflops"] * 1.1 / 2.25
+            peak = tf32 / 3.0
+            bound, punit = "tensor", "TFLOP/s"
+            note = (f"3xTF32 effective: measured bf16 {peaks['bf16_tflops']:.0f} x 1.1/2.25 "
+                    f"= {tf32:.0f} tf32 TF/s, / 3 products ({peak_src})")
         else:
             peak = peaks["bf16_tflops"]
             bound, punit = "tensor", "TFLOP/s"

@@ -457,34 +457,25 @@ int run_forward(const lora_desc* d, const DropParams& dp, int64_t T, const void*
   }
   // shrink: Hs[t, j] = s_k q sum_i M[t,i] X[t,i] A_k[j,i]   (columns j >= r_k written as 0)
   {
-    TokGemmArgs a{};
-    a.items = L.gitems; a.n_items = L.gcount;
-    a.a = X; a.lda = d->in_dim; a.K = d->in_dim; a.a_mask = dp.enabled;
-    a.b_per_slot = 1;
+    RowDotArgs a{};
+    a.a = X; a.lda = d->in_dim; a.K = d->in_dim; a.lds = d->in_dim;
     for (int k = 0; k < s.n; ++k) {
-      a.bslot.p[k] = s.A[k]; a.bslot.ld[k] = d->in_dim; a.bslot.rank[k] = s.rank[k];
-      a.bslot.alpha[k] = s.scale[k] * q;
+      a.s[k] = s.A[k]; a.rank[k] = s.rank[k]; a.alpha[k] = s.scale[k] * q;
     }
-    a.alpha_per_slot = 1;
-    a.out = H; a.ldo = d->rank; a.n_out = d->rank;
-    a.drop = dp;
-    LORA_TRY(launch_tok_gemm(d->dtype, LORA_F32, LORA_F32, 64, a, (int)L.gmax, st, LORA_PROF_SHRINK));
+    a.max_rank = d->rank; a.mask = dp.enabled; a.drop = dp;
+    a.out = H; a.ldo = d->rank;
+    a.items = L.gitems; a.n_items = L.gcount;
+    LORA_TRY(launch_rowdot(d->dtype, a, (int)L.gmax, st, LORA_PROF_SHRINK));
   }
-  // frozen product + Hs B_k^T, times m/n per column in DoRA mode
+  // frozen product + Hs B_k^T, times m/n per column in DoRA mode (3xTF32 tensor cores)
   {
-    TokGemmArgs a{};
-    a.items = L.gitems; a.n_items = L.gcount;
-    a.a = X; a.lda = d->in_dim; a.K = d->in_dim;
-    a.b = W; a.ldb = d->in_dim; a.n_rows = d->out_dim;
-    a.lora_phase = 1; a.lp = H; a.ldlp = d->rank;
-    for (int k = 0; k < s.n; ++k) {
-      a.lq.p[k] = s.B[k]; a.lq.ld[k] = s.rank[k]; a.lq.rank[k] = s.rank[k];
-    }
-    a.alpha = 1.f;
-    a.n_colscale = ratio;
-    a.out = Y; a.ldo = d->out_dim; a.n_out = d->out_dim;
-    a.drop = dp;
-    LORA_TRY(launch_tok_gemm(d->dtype, d->dtype, d->dtype, 128, a, (int)L.gmax, st, LORA_PROF_FROZEN_FWD));
+    TcGemmArgs t{};
+    t.a = X; t.T = T; t.b = W; t.n_rows = d->out_dim; t.K = d->in_dim;
+    t.p = H; t.ldp = d->rank; t.n_slots = s.n;
+    for (int k = 0; k < s.n; ++k) { t.q[k] = s.B[k]; t.q_rank[k] = s.rank[k]; }
+    t.n_colscale = ratio; t.out = Y; t.ldo = d->out_dim;
+    t.items = L.gitems; t.n_items = L.gcount; t.max_items = (int)L.gmax; t.drop = dp;
+    LORA_TRY(launch_tc_gemm_f32(t, st, LORA_PROF_FROZEN_FWD));
   }
   return LORA_OK;
 }
@@ -523,61 +514,52 @@ int run_backward(const lora_desc* d, const DropParams& dp, int64_t T, const void
   }
   // Gs[t, j] = s_k q sum_o dY'[t, o] B_k[o, j]
   {
-    TokGemmArgs a{};
-    a.items = L.gitems; a.n_items = L.gcount;
-    a.a = dY; a.lda = d->out_dim; a.K = d->out_dim; a.a_colscale = ratio;
-    a.b_per_slot = 1;
+    RowDotArgs a{};
+    a.a = dY; a.lda = d->out_dim; a.K = d->out_dim; a.lds = d->out_dim;
     for (int k = 0; k < s.n; ++k) {
-      a.bslot.p[k] = Bt[k]; a.bslot.ld[k] = d->out_dim; a.bslot.rank[k] = s.rank[k];
-      a.bslot.alpha[k] = s.scale[k] * q;
+      a.s[k] = Bt[k]; a.rank[k] = s.rank[k]; a.alpha[k] = s.scale[k] * q;
     }
-    a.alpha_per_slot = 1;
-    a.out = L.Gs; a.ldo = d->rank; a.n_out = d->rank;
-    a.drop = dp;
-    LORA_TRY(launch_tok_gemm(d->dtype, LORA_F32, LORA_F32, 64, a, (int)L.gmax, st, LORA_PROF_G));
+    a.max_rank = d->rank; a.colscale = ratio; a.drop = dp;
+    a.out = L.Gs; a.ldo = d->rank;
+    a.items = L.gitems; a.n_items = L.gcount;
+    LORA_TRY(launch_rowdot(d->dtype, a, (int)L.gmax, st, LORA_PROF_G));
   }
   // dX = dY' W + (Gs A_k) * M
   if (dX) {
-    TokGemmArgs a{};
-    a.items = L.gitems; a.n_items = L.gcount;
-    a.a = dY; a.lda = d->out_dim; a.K = d->out_dim; a.a_colscale = ratio;
-    a.b = Wt; a.ldb = d->out_dim; a.n_rows = d->in_dim;
-    a.lora_phase = 1; a.lp = L.Gs; a.ldlp = d->rank;
-    for (int k = 0; k < s.n; ++k) {
-      a.lq.p[k] = At[k]; a.lq.ld[k] = s.rank[k]; a.lq.rank[k] = s.rank[k];
-    }
-    a.mask_after_lora = dp.enabled;
-    a.alpha = 1.f;
-    a.out = dX; a.ldo = d->in_dim; a.n_out = d->in_dim;
-    a.drop = dp;
-    LORA_TRY(launch_tok_gemm(d->dtype, d->dtype, d->dtype, 128, a, (int)L.gmax, st, LORA_PROF_FROZEN_DX));
+    TcGemmArgs t{};
+    t.a = dY; t.T = T; t.b = Wt; t.n_rows = d->in_dim; t.K = d->out_dim;
+    t.p = L.Gs; t.ldp = d->rank; t.n_slots = s.n;
+    for (int k = 0; k < s.n; ++k) { t.q[k] = At[k]; t.q_rank[k] = s.rank[k]; }
+    t.lora_separate = dp.enabled; t.a_colscale = ratio; t.out = dX; t.ldo = d->in_dim;
+    t.items = L.gitems; t.n_items = L.gcount; t.max_items = (int)L.gmax; t.drop = dp;
+    LORA_TRY(launch_tc_gemm_f32(t, st, LORA_PROF_FROZEN_DX));
   }
   ReduceTab rt{};
   for (int k = 0; k < s.n; ++k) rt.rank[k] = s.rank[k];
   // dB_k += sum_t dY'[t, o] Hs[t, j]
   {
-    RedGemmArgs a{};
-    a.items = L.ritems; a.n_items = L.rcount;
-    a.a = dY; a.lda = d->out_dim; a.M = d->out_dim; a.a_colscale = ratio;
-    a.b = H; a.ldb = d->rank;
+    ColRedArgs a{};
+    a.p = H; a.ldp = d->rank;
+    a.b = dY; a.ldb = d->out_dim; a.N = d->out_dim; a.colscale = ratio;
     for (int k = 0; k < s.n; ++k) a.rank[k] = s.rank[k];
-    a.part = L.partB; a.ldp = d->rank;
-    a.drop = dp;
-    LORA_TRY(launch_red_gemm(d->dtype, a, (int)L.rmax, st, LORA_PROF_RED_DB));
+    a.max_rank = d->rank; a.drop = dp;
+    a.part = L.partB; a.ldpart = d->rank;
+    a.items = L.ritems; a.n_items = L.rcount;
+    LORA_TRY(launch_colred(d->dtype, a, (int)L.rmax, st, LORA_PROF_RED_DB));
     for (int k = 0; k < s.n; ++k) rt.out[k] = s.dB[k];
     LORA_TRY(launch_reduce_parts(L.partB, L.ritems, L.rcount, (int)L.rmax, d->out_dim, d->rank, 0,
                                  rt, s.n, st));
   }
   // dA_k += sum_t Gs[t, j] M[t, i] X[t, i]   (computed as dA^T partials)
   {
-    RedGemmArgs a{};
-    a.items = L.ritems; a.n_items = L.rcount;
-    a.a = X; a.lda = d->in_dim; a.M = d->in_dim; a.a_mask = dp.enabled;
-    a.b = L.Gs; a.ldb = d->rank;
+    ColRedArgs a{};
+    a.p = L.Gs; a.ldp = d->rank;
+    a.b = X; a.ldb = d->in_dim; a.N = d->in_dim; a.mask = dp.enabled;
     for (int k = 0; k < s.n; ++k) a.rank[k] = s.rank[k];
-    a.part = L.partA; a.ldp = d->rank;
-    a.drop = dp;
-    LORA_TRY(launch_red_gemm(d->dtype, a, (int)L.rmax, st, LORA_PROF_RED_DA));
+    a.max_rank = d->rank; a.drop = dp;
+    a.part = L.partA; a.ldpart = d->rank;
+    a.items = L.ritems; a.n_items = L.rcount;
+    LORA_TRY(launch_colred(d->dtype, a, (int)L.rmax, st, LORA_PROF_RED_DA));
     for (int k = 0; k < s.n; ++k) rt.out[k] = s.dA[k];
     LORA_TRY(launch_reduce_parts(L.partA, L.ritems, L.rcount, (int)L.rmax, d->in_dim, d->rank, 1,
                                  rt, s.n, st));

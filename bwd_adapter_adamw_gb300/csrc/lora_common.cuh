@@ -10,7 +10,7 @@
 namespace lora {
 
 constexpr int kGemmTileT = 128;   // token rows per forward/dX/shrink/G work item
-constexpr int kRedTileT = 512;    // tokens per split of the token reductions (dA, dB)
+constexpr int kRedTileT = 128;    // tokens per split of the CUDA-core token reductions (dA, dB)
 
 // ------------------------------------------------------------------------------------------
 // Stateless dropout hash ("4.3. Training Guide", Dropout: masks come from a stateless index

@@ -9,66 +9,6 @@ namespace lora {
 void prof_begin(int kind, cudaStream_t st);
 void prof_end(int kind, cudaStream_t st);
 
-// Per-slot operand table (fp32 adapters or their transposes).
-struct SlotTab {
-  const float* p[LORA_MAX_SLOTS];
-  int64_t ld[LORA_MAX_SLOTS];
-  int32_t rank[LORA_MAX_SLOTS];
-  float alpha[LORA_MAX_SLOTS];
-};
-
-struct TokGemmArgs {
-  const TokenItem* items;
-  const int32_t* n_items;
-  // main phase, A side: tokens x K, K-contiguous
-  const void* a;
-  int64_t lda;
-  int64_t K;
-  const float* a_colscale;   // multiply A[t, k] by a_colscale[k] (DoRA dY')
-  int32_t a_mask;            // zero A[t, k] where the dropout mask drops (t, k)
-  // main phase, B side: n_rows x K, K-contiguous; fixed or per slot
-  const void* b;
-  int64_t ldb;
-  int64_t n_rows;
-  int32_t b_per_slot;
-  SlotTab bslot;
-  // LoRA phase (extra K-steps): P [T, rank_slot] (row stride ldlp) times Q_slot [n_rows, rank_slot]
-  int32_t lora_phase;
-  const float* lp;
-  int64_t ldlp;
-  SlotTab lq;
-  int32_t mask_after_lora;   // multiply the LoRA phase result by the dropout mask at (t, n)
-  // epilogue
-  float alpha;
-  int32_t alpha_per_slot;    // alpha = bslot.alpha[slot]
-  const float* n_colscale;   // multiply column n by n_colscale[n] (DoRA m / n)
-  void* out;
-  int64_t ldo;
-  int64_t n_out;             // columns written
-  DropParams drop;
-};
-
-struct RedGemmArgs {
-  const TokenItem* items;
-  const int32_t* n_items;
-  const void* a;             // [T, lda], column m (M extent)
-  int64_t lda;
-  int64_t M;
-  const float* a_colscale;
-  int32_t a_mask;
-  const float* b;            // [T, ldb] fp32, column j < rank[slot]
-  int64_t ldb;
-  int32_t rank[LORA_MAX_SLOTS];
-  float* part;               // [items][M][ldp]
-  int64_t ldp;
-  DropParams drop;
-};
-
-cudaError_t launch_tok_gemm(int dtype_a, int dtype_b, int dtype_out, int bn, const TokGemmArgs& a,
-                            int max_items, cudaStream_t st, int prof_kind);
-cudaError_t launch_red_gemm(int dtype_a, const RedGemmArgs& a, int max_items, cudaStream_t st,
-                            int prof_kind);
-
 // ---- gemm_tc.cu: tcgen05 frozen products (bf16 activations) ----
 struct TcGemmArgs {
   const void* a;             // [T, K] bf16, K-contiguous
@@ -83,14 +23,17 @@ struct TcGemmArgs {
   int32_t n_slots;
   int32_t lora_separate;     // LoRA term in its own accumulator, masked by dropout at (t, n)
   DropParams drop;
+  const float* a_colscale;   // fp32 kernel only: A[t, k] * a_colscale[k] (DoRA dY'), nullable
   const float* n_colscale;   // per output column scale (DoRA m / n), nullable
-  void* out;                 // [T, ldo] bf16
+  void* out;                 // [T, ldo] in the activation dtype
   int64_t ldo;
   const TokenItem* items;
   const int32_t* n_items;
   int max_items;
 };
 cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st, int prof_kind);
+// gemm_tc_f32.cu: the same products for fp32 activations, 3xTF32 with an in-shared-memory split
+cudaError_t launch_tc_gemm_f32(const TcGemmArgs& a, cudaStream_t st, int prof_kind);
 cudaError_t read_tc_error(uint32_t* out, bool reset);
 
 // out_slot[j, i] (+)= sum over items of `slot` of part[item][...]; see lowrank.cu
@@ -157,6 +100,45 @@ cudaError_t launch_make_red_items_tc(int64_t T, int32_t n_seg, const int32_t* se
                                      cudaStream_t st);
 cudaError_t launch_mask_bf16(const void* X, int64_t T, int64_t in_dim, const DropParams& dp,
                              void* Xd, cudaStream_t st);
+
+// ---- lowrank_simt.cu: streaming CUDA-core low-rank products (fp32 activations) ----
+struct RowDotArgs {                 // out[t, j] = alpha_slot * sum_k A'[t, k] S_slot[j, k]
+  const void* a;                    // [T, lda]
+  int64_t lda;
+  int64_t K;
+  const float* s[LORA_MAX_SLOTS];   // per slot [rank, lds] fp32
+  int64_t lds;
+  int32_t rank[LORA_MAX_SLOTS];
+  float alpha[LORA_MAX_SLOTS];
+  int32_t max_rank;
+  const float* colscale;            // A'[t, k] = A[t, k] * colscale[k] (nullable)
+  int32_t mask;                     // A'[t, k] = 0 where the dropout mask drops (t, k)
+  DropParams drop;
+  float* out;                       // [T, ldo]
+  int32_t ldo;
+  const TokenItem* items;           // <= 128-token items
+  const int32_t* n_items;
+};
+struct ColRedArgs {                 // part[item][n][j] = sum_{t in item} P[t, j] B'[t, n]
+  const float* p;                   // [T, ldp] fp32
+  int64_t ldp;
+  const void* b;                    // [T, ldb]
+  int64_t ldb;
+  int64_t N;
+  int32_t rank[LORA_MAX_SLOTS];
+  int32_t max_rank;
+  const float* colscale;            // B'[t, n] = B[t, n] * colscale[n] (nullable)
+  int32_t mask;                     // B'[t, n] = 0 where the dropout mask drops (t, n)
+  DropParams drop;
+  float* part;                      // [items][N][ldpart]
+  int32_t ldpart;
+  const TokenItem* items;
+  const int32_t* n_items;
+};
+cudaError_t launch_rowdot(int dtype, const RowDotArgs& a, int max_items, cudaStream_t st,
+                          int prof_kind);
+cudaError_t launch_colred(int dtype, const ColRedArgs& a, int max_items, cudaStream_t st,
+                          int prof_kind);
 
 // ---- lowrank.cu ----
 cudaError_t launch_colscale_bf16(const void* src, const float* scale, int64_t rows, int64_t cols,

@@ -1,0 +1,241 @@
+// Streaming CUDA-core low-rank products for fp32 activations (and small ranks): at rank r the
+// products do ~r/2 flops per streamed byte of X or dY, so for the ranks of fp32 workloads they
+// are bound by HBM, not by the FMA units, and run at exact rank width here.
+//
+//  k_rowdot:  out[t, j] = alpha_slot * sum_k A'[t, k] S_slot[j, k]   (shrink with S = A,
+//             G with S = B^T); one warp per token, lanes stride over K with 16-byte loads, the
+//             slot's S staged in shared memory one K-chunk at a time, warp-shuffle reduction.
+//  k_colred:  part[item][n][j] = sum_{t in item} P[t, j] B'[t, n]   (dB with P = Hs, B' = dY';
+//             dA^T with P = Gs, B' = Xd); every thread owns CPT adjacent columns, the item's P
+//             rows are staged in shared memory, one partial per work item, reduced in order.
+// ("Backward Bug Hunts and Vulkan Tiled GEMM", The fix: a 16x16 shared-memory tiled GEMM --
+// operand reuse through shared memory; here the reused operand is the small adapter side.)
+#include "lora_kernels.h"
+
+namespace lora {
+
+namespace {
+
+constexpr int kRowWarps = 8;
+constexpr int kRowSmemFloats = 12288;              // 48 KB of S per K-chunk
+
+// tokens per warp: 4 for small ranks (amortises the shared S reads), 1 for large ranks
+template <int R> struct RowTpw { static constexpr int v = R <= 16 ? 4 : 1; };
+
+template <typename TA, int R>
+__global__ void __launch_bounds__(256) k_rowdot(const RowDotArgs a) {
+  constexpr int kTokPerWarp = RowTpw<R>::v;
+  constexpr int kRowTok = kRowWarps * kTokPerWarp;   // tokens per CTA (within one work item)
+  __shared__ __align__(16) float sS[kRowSmemFloats];
+  const int item = blockIdx.x;
+  if (item >= *a.n_items) return;
+  const TokenItem it = a.items[item];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t tbase = (int64_t)it.t0 + (int64_t)blockIdx.y * kRowTok + warp * kTokPerWarp;
+  if ((int64_t)it.t0 + (int64_t)blockIdx.y * kRowTok >= it.t1) return;
+  const int slot = it.slot;
+  const int32_t r = slot >= 0 ? a.rank[slot] : 0;
+  const float* S = slot >= 0 ? a.s[slot] : nullptr;
+  const int64_t K = a.K;
+  // chunk width: columns of S held in shared memory (a multiple of 128 = 32 lanes x 4)
+  int64_t chunk = (kRowSmemFloats / R) / 128 * 128;
+  if (chunk > K) chunk = (K + 127) / 128 * 128;
+  float acc[kTokPerWarp][R];
+#pragma unroll
+  for (int u = 0; u < kTokPerWarp; ++u)
+#pragma unroll
+    for (int j = 0; j < R; ++j) acc[u][j] = 0.f;
+  for (int64_t k0 = 0; k0 < K && r > 0; k0 += chunk) {
+    const int64_t kn = min(chunk, K - k0);
+    __syncthreads();
+    for (int64_t e = threadIdx.x; e < (int64_t)R * chunk; e += 256) {
+      const int j = (int)(e / chunk);
+      const int64_t k = e - (int64_t)j * chunk;
+      sS[e] = (j < r && k < kn) ? __ldg(S + (int64_t)j * a.lds + k0 + k) : 0.f;
+    }
+    __syncthreads();
+    for (int64_t k = lane * 4; k < kn; k += 128) {
+      float s4[R][4];
+#pragma unroll
+      for (int j = 0; j < R; ++j) {
+        const float4 v = *reinterpret_cast<const float4*>(&sS[(int64_t)j * chunk + k]);
+        s4[j][0] = v.x; s4[j][1] = v.y; s4[j][2] = v.z; s4[j][3] = v.w;
+      }
+#pragma unroll
+      for (int u = 0; u < kTokPerWarp; ++u) {
+        const int64_t t = tbase + u;
+        if (t >= it.t1) continue;
+        float x[8];
+        const TA* src = reinterpret_cast<const TA*>(a.a) + t * a.lda + k0 + k;
+        if (Vec<TA>::N == 4) {
+          load16(reinterpret_cast<const float*>(src), x);
+        } else {
+          // bf16: 4 elements = 8 bytes
+          const uint2 w = __ldg(reinterpret_cast<const uint2*>(src));
+          x[0] = __uint_as_float(w.x << 16); x[1] = __uint_as_float(w.x & 0xFFFF0000u);
+          x[2] = __uint_as_float(w.y << 16); x[3] = __uint_as_float(w.y & 0xFFFF0000u);
+        }
+        if (a.colscale) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) x[e] *= __ldg(a.colscale + k0 + k + e);
+        }
+        if (a.mask) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (!drop_keep(a.drop, t, k0 + k + e)) x[e] = 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < R; ++j)
+          acc[u][j] = fmaf(x[0], s4[j][0], fmaf(x[1], s4[j][1], fmaf(x[2], s4[j][2], fmaf(x[3], s4[j][3], acc[u][j]))));
+      }
+    }
+  }
+  const float alpha = slot >= 0 ? a.alpha[slot] : 0.f;
+#pragma unroll
+  for (int u = 0; u < kTokPerWarp; ++u) {
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+      float v = acc[u][j];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+      acc[u][j] = v;
+    }
+    const int64_t t = tbase + u;
+    if (t < it.t1) {
+      // lane j writes column j (columns r..ldo-1 are zero)
+      for (int j = lane; j < a.ldo; j += 32) {
+        float v = 0.f;
+#pragma unroll
+        for (int jj = 0; jj < R; ++jj)
+          if (jj == j) v = acc[u][jj];
+        a.out[t * a.ldo + j] = (j < r) ? v * alpha : 0.f;
+      }
+    }
+  }
+}
+
+constexpr int kColThreads = 256;
+constexpr int kColTokChunk = 64;
+
+template <typename TB, int R, int CPT>
+__global__ void __launch_bounds__(kColThreads) k_colred(const ColRedArgs a) {
+  __shared__ __align__(16) float sP[kColTokChunk * R];
+  const int item = blockIdx.y;
+  if (item >= *a.n_items) return;
+  const TokenItem it = a.items[item];
+  if (it.slot < 0) return;
+  const int32_t r = a.rank[it.slot];
+  const int64_t n0 = ((int64_t)blockIdx.x * kColThreads + threadIdx.x) * CPT;
+  float acc[CPT][R];
+#pragma unroll
+  for (int c = 0; c < CPT; ++c)
+#pragma unroll
+    for (int j = 0; j < R; ++j) acc[c][j] = 0.f;
+  for (int64_t t0 = it.t0; t0 < it.t1; t0 += kColTokChunk) {
+    const int nt = (int)min((int64_t)kColTokChunk, (int64_t)it.t1 - t0);
+    __syncthreads();
+    for (int e = threadIdx.x; e < kColTokChunk * R; e += kColThreads) {
+      const int tt = e / R, j = e - tt * R;
+      sP[e] = (tt < nt && j < r) ? a.p[(t0 + tt) * a.ldp + j] : 0.f;
+    }
+    __syncthreads();
+    if (n0 < a.N) {
+      for (int tt = 0; tt < nt; ++tt) {
+        const int64_t t = t0 + tt;
+        float b[CPT];
+        const TB* src = reinterpret_cast<const TB*>(a.b) + t * a.ldb + n0;
+        if (CPT == 4 && Vec<TB>::N == 4) {
+          load16(reinterpret_cast<const float*>(src), b);
+        } else {
+#pragma unroll
+          for (int c = 0; c < CPT; ++c) b[c] = to_f(src[c]);
+        }
+        if (a.colscale) {
+#pragma unroll
+          for (int c = 0; c < CPT; ++c) b[c] *= __ldg(a.colscale + n0 + c);
+        }
+        if (a.mask) {
+#pragma unroll
+          for (int c = 0; c < CPT; ++c)
+            if (!drop_keep(a.drop, t, n0 + c)) b[c] = 0.f;
+        }
+        float pv[R];
+#pragma unroll
+        for (int j = 0; j < R; j += 4) {
+          const float4 v = *reinterpret_cast<const float4*>(&sP[tt * R + j]);
+          pv[j] = v.x; pv[j + 1] = v.y; pv[j + 2] = v.z; pv[j + 3] = v.w;
+        }
+#pragma unroll
+        for (int c = 0; c < CPT; ++c)
+#pragma unroll
+          for (int j = 0; j < R; ++j) acc[c][j] = fmaf(pv[j], b[c], acc[c][j]);
+      }
+    }
+  }
+  if (n0 >= a.N) return;
+  float* part = a.part + (int64_t)item * a.N * a.ldpart;
+#pragma unroll
+  for (int c = 0; c < CPT; ++c) {
+    float* dst = part + (n0 + c) * a.ldpart;
+#pragma unroll
+    for (int j = 0; j < R; ++j)
+      if (j < a.ldpart) dst[j] = acc[c][j];
+  }
+}
+
+template <typename TA, int R>
+void rowdot_launch(const RowDotArgs& a, int max_items, cudaStream_t st) {
+  constexpr int tok = kRowWarps * RowTpw<R>::v;
+  dim3 grid((unsigned)max_items, (unsigned)((kGemmTileT + tok - 1) / tok));
+  k_rowdot<TA, R><<<grid, 256, 0, st>>>(a);
+}
+
+template <typename TA>
+cudaError_t rowdot_for_rank(const RowDotArgs& a, int max_items, cudaStream_t st) {
+  const int rm = a.max_rank;
+  if (rm <= 4) rowdot_launch<TA, 4>(a, max_items, st);
+  else if (rm <= 8) rowdot_launch<TA, 8>(a, max_items, st);
+  else if (rm <= 16) rowdot_launch<TA, 16>(a, max_items, st);
+  else if (rm <= 32) rowdot_launch<TA, 32>(a, max_items, st);
+  else rowdot_launch<TA, 64>(a, max_items, st);
+  return cudaGetLastError();
+}
+
+template <typename TB>
+cudaError_t colred_for_rank(const ColRedArgs& a, int max_items, cudaStream_t st) {
+  const int rm = a.max_rank;
+  auto grid = [&](int cpt) {
+    return dim3((unsigned)((a.N + (int64_t)kColThreads * cpt - 1) / ((int64_t)kColThreads * cpt)),
+                (unsigned)max_items);
+  };
+  if (rm <= 4) k_colred<TB, 4, 1><<<grid(1), kColThreads, 0, st>>>(a);
+  else if (rm <= 8) k_colred<TB, 8, 1><<<grid(1), kColThreads, 0, st>>>(a);
+  else if (rm <= 16) k_colred<TB, 16, 1><<<grid(1), kColThreads, 0, st>>>(a);
+  else if (rm <= 32) k_colred<TB, 32, 1><<<grid(1), kColThreads, 0, st>>>(a);
+  else k_colred<TB, 64, 1><<<grid(1), kColThreads, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_rowdot(int dtype, const RowDotArgs& a, int max_items, cudaStream_t st,
+                          int prof_kind) {
+  if (max_items <= 0) return cudaSuccess;
+  prof_begin(prof_kind, st);
+  cudaError_t e = dtype == LORA_F32 ? rowdot_for_rank<float>(a, max_items, st)
+                                    : rowdot_for_rank<__nv_bfloat16>(a, max_items, st);
+  prof_end(prof_kind, st);
+  return e;
+}
+
+cudaError_t launch_colred(int dtype, const ColRedArgs& a, int max_items, cudaStream_t st,
+                          int prof_kind) {
+  if (max_items <= 0) return cudaSuccess;
+  prof_begin(prof_kind, st);
+  cudaError_t e = dtype == LORA_F32 ? colred_for_rank<float>(a, max_items, st)
+                                    : colred_for_rank<__nv_bfloat16>(a, max_items, st);
+  prof_end(prof_kind, st);
+  return e;
+}
+
+}  // namespace lora
