@@ -189,6 +189,7 @@ struct Layout {
   float* partB;        // [rmax_items][out][rank] (fp32 path)
   float* partA;        // [rmax_items][in][rank] (fp32 path)
   uint16_t* dYs;       // [T, out] bf16 dY * (m / n) for the DoRA tensor-core products
+  float* rd_part;      // [K chunks][T][16] partials of the CUDA-core shrink / G (fp32 path)
   // tensor-core path
   uint16_t* Xd;        // [T, in] bf16 masked input (dropout)
   uint16_t* Sa;        // per slot [2 r, in] bf16 split of A
@@ -242,12 +243,16 @@ Layout carve(const lora_desc* d, int64_t T, int32_t n_seg, int n_slots, int64_t 
       L.ritems = c.take<TokenItem>((size_t)L.rmax);
       L.rcount = c.take<int32_t>(4);
       L.Bt = c.take<float>((size_t)rank_sum * d->out_dim);
-      L.partB = c.take<float>((size_t)L.rmax * d->out_dim * d->rank);
-      L.partA = c.take<float>((size_t)L.rmax * d->in_dim * d->rank);
+      L.partB = c.take<float>((size_t)L.rmax * kRedSub * d->out_dim * d->rank);
+      L.partA = c.take<float>((size_t)L.rmax * kRedSub * d->in_dim * d->rank);
     }
   } else if (!tc) {
     L.ritems = c.take<TokenItem>((size_t)L.rmax);
     L.rcount = c.take<int32_t>(4);
+  }
+  if (!tc) {
+    const int64_t kmax = d->in_dim > d->out_dim ? d->in_dim : d->out_dim;
+    L.rd_part = c.take<float>((size_t)((kmax + kRowChunk - 1) / kRowChunk) * T * kRowPartCols);
   }
   L.bytes = c.off + kWsAlign;
   return L;
@@ -465,6 +470,7 @@ int run_forward(const lora_desc* d, const DropParams& dp, int64_t T, const void*
     a.max_rank = d->rank; a.mask = dp.enabled; a.drop = dp;
     a.out = H; a.ldo = d->rank;
     a.items = L.gitems; a.n_items = L.gcount;
+    a.T = T; a.part = L.rd_part;
     LORA_TRY(launch_rowdot(d->dtype, a, (int)L.gmax, st, LORA_PROF_SHRINK));
   }
   // frozen product + Hs B_k^T, times m/n per column in DoRA mode (3xTF32 tensor cores)
@@ -522,6 +528,7 @@ int run_backward(const lora_desc* d, const DropParams& dp, int64_t T, const void
     a.max_rank = d->rank; a.colscale = ratio; a.drop = dp;
     a.out = L.Gs; a.ldo = d->rank;
     a.items = L.gitems; a.n_items = L.gcount;
+    a.T = T; a.part = L.rd_part;
     LORA_TRY(launch_rowdot(d->dtype, a, (int)L.gmax, st, LORA_PROF_G));
   }
   // dX = dY' W + (Gs A_k) * M
@@ -543,11 +550,11 @@ int run_backward(const lora_desc* d, const DropParams& dp, int64_t T, const void
     a.b = dY; a.ldb = d->out_dim; a.N = d->out_dim; a.colscale = ratio;
     for (int k = 0; k < s.n; ++k) a.rank[k] = s.rank[k];
     a.max_rank = d->rank; a.drop = dp;
-    a.part = L.partB; a.ldpart = d->rank;
+    a.part = L.partB; a.ldpart = d->rank; a.sub_groups = kRedSub;
     a.items = L.ritems; a.n_items = L.rcount;
     LORA_TRY(launch_colred(d->dtype, a, (int)L.rmax, st, LORA_PROF_RED_DB));
     for (int k = 0; k < s.n; ++k) rt.out[k] = s.dB[k];
-    LORA_TRY(launch_reduce_parts(L.partB, L.ritems, L.rcount, (int)L.rmax, d->out_dim, d->rank, 0,
+    LORA_TRY(launch_reduce_parts(L.partB, L.ritems, L.rcount, (int)L.rmax, kRedSub, d->out_dim, d->rank, 0,
                                  rt, s.n, st));
   }
   // dA_k += sum_t Gs[t, j] M[t, i] X[t, i]   (computed as dA^T partials)
@@ -557,11 +564,11 @@ int run_backward(const lora_desc* d, const DropParams& dp, int64_t T, const void
     a.b = X; a.ldb = d->in_dim; a.N = d->in_dim; a.mask = dp.enabled;
     for (int k = 0; k < s.n; ++k) a.rank[k] = s.rank[k];
     a.max_rank = d->rank; a.drop = dp;
-    a.part = L.partA; a.ldpart = d->rank;
+    a.part = L.partA; a.ldpart = d->rank; a.sub_groups = kRedSub;
     a.items = L.ritems; a.n_items = L.rcount;
     LORA_TRY(launch_colred(d->dtype, a, (int)L.rmax, st, LORA_PROF_RED_DA));
     for (int k = 0; k < s.n; ++k) rt.out[k] = s.dA[k];
-    LORA_TRY(launch_reduce_parts(L.partA, L.ritems, L.rcount, (int)L.rmax, d->in_dim, d->rank, 1,
+    LORA_TRY(launch_reduce_parts(L.partA, L.ritems, L.rcount, (int)L.rmax, kRedSub, d->in_dim, d->rank, 1,
                                  rt, s.n, st));
   }
   if (dm) LORA_TRY(launch_dora_dm(d->dtype, dY, Y_save, dora_m, T, d->out_dim, dm, st));

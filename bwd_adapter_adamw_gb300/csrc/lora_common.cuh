@@ -11,6 +11,9 @@ namespace lora {
 
 constexpr int kGemmTileT = 128;   // token rows per forward/dX/shrink/G work item
 constexpr int kRedTileT = 128;    // tokens per split of the CUDA-core token reductions (dA, dB)
+constexpr int kRedSub = 4;        // token groups (separate partials) per reduction item
+constexpr int kRowPartCols = 16;  // partial row width of the CUDA-core shrink / G (ranks <= 16)
+constexpr int kRowChunk = 1024;   // K columns per partial of the CUDA-core shrink / G
 
 // ------------------------------------------------------------------------------------------
 // Stateless dropout hash ("4.3. Training Guide", Dropout: masks come from a stateless index

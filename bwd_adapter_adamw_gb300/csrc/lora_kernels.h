@@ -118,6 +118,8 @@ struct RowDotArgs {                 // out[t, j] = alpha_slot * sum_k A'[t, k] S
   int32_t ldo;
   const TokenItem* items;           // <= 128-token items
   const int32_t* n_items;
+  int64_t T;
+  float* part;                      // K-chunk partials [ceil(K / 1024)][T][16] (ranks <= 16)
 };
 struct ColRedArgs {                 // part[item][n][j] = sum_{t in item} P[t, j] B'[t, n]
   const float* p;                   // [T, ldp] fp32
@@ -130,8 +132,9 @@ struct ColRedArgs {                 // part[item][n][j] = sum_{t in item} P[t, j
   const float* colscale;            // B'[t, n] = B[t, n] * colscale[n] (nullable)
   int32_t mask;                     // B'[t, n] = 0 where the dropout mask drops (t, n)
   DropParams drop;
-  float* part;                      // [items][N][ldpart]
+  float* part;                      // [items * sub_groups][N][ldpart]
   int32_t ldpart;
+  int32_t sub_groups;               // token groups per item (partials per item)
   const TokenItem* items;
   const int32_t* n_items;
 };
@@ -160,7 +163,7 @@ cudaError_t launch_transpose_weight(int dtype, const void* W, void* Wt, int64_t 
                                     cudaStream_t st);
 
 cudaError_t launch_reduce_parts(const float* part, const TokenItem* items, const int32_t* n_items,
-                                int max_items, int64_t M, int64_t ldp, int transposed,
+                                int max_items, int32_t sub, int64_t M, int64_t ldp, int transposed,
                                 const ReduceTab& tab, int n_slots, cudaStream_t st);
 
 cudaError_t launch_dropout_mask(const DropParams& dp, int64_t T, int64_t in_dim, uint8_t* mask,

@@ -81,11 +81,12 @@ __global__ void k_transpose_w(const T* __restrict__ src, T* __restrict__ dst, in
 }
 
 // out_slot += sum over the slot's items, in item order, of the per-item partials.
-// part[item] is [M][ldp]; element (m, j), j < rank_slot, goes to out_slot[m * rank + j]
+// part[item * sub + g] is [M][ldp] (sub partials per item); element (m, j), j < rank_slot, goes to
+// out_slot[m * rank + j]
 // (transposed == 0, dB layout [out, r]) or out_slot[j * M + m] (transposed == 1, dA [r, in]).
 __global__ void k_reduce_parts(const float* __restrict__ part, const TokenItem* __restrict__ items,
-                               const int32_t* __restrict__ n_items, int64_t M, int64_t ldp,
-                               int transposed, const ReduceTab tab) {
+                               const int32_t* __restrict__ n_items, int32_t sub, int64_t M,
+                               int64_t ldp, int transposed, const ReduceTab tab) {
   const int slot = blockIdx.y;
   const int32_t r = tab.rank[slot];
   float* out = tab.out[slot];
@@ -100,7 +101,7 @@ __global__ void k_reduce_parts(const float* __restrict__ part, const TokenItem* 
     bool any = false;
     for (int32_t it = 0; it < ni; ++it) {
       if (items[it].slot != slot) continue;
-      acc += part[(int64_t)it * total + e];
+      for (int32_t g = 0; g < sub; ++g) acc += part[((int64_t)it * sub + g) * total + e];
       any = true;
     }
     if (!any) continue;
@@ -199,7 +200,7 @@ cudaError_t launch_transpose_weight(int dtype, const void* W, void* Wt, int64_t 
 }
 
 cudaError_t launch_reduce_parts(const float* part, const TokenItem* items, const int32_t* n_items,
-                                int max_items, int64_t M, int64_t ldp, int transposed,
+                                int max_items, int32_t sub, int64_t M, int64_t ldp, int transposed,
                                 const ReduceTab& tab, int n_slots, cudaStream_t st) {
   (void)max_items;
   const int64_t total = M * ldp;
@@ -207,7 +208,7 @@ cudaError_t launch_reduce_parts(const float* part, const TokenItem* items, const
   int64_t blocks = (total + threads - 1) / threads;
   if (blocks > 4096) blocks = 4096;
   dim3 grid((unsigned)blocks, (unsigned)n_slots);
-  { prof_begin(0, st); k_reduce_parts<<<grid, threads, 0, st>>>(part, items, n_items, M, ldp, transposed, tab); }
+  { prof_begin(0, st); k_reduce_parts<<<grid, threads, 0, st>>>(part, items, n_items, sub, M, ldp, transposed, tab); }
   return cudaGetLastError();
 }
 

@@ -190,6 +190,194 @@ void rowdot_launch(const RowDotArgs& a, int max_items, cudaStream_t st) {
   k_rowdot<TA, R><<<grid, 256, 0, st>>>(a);
 }
 
+// ---------------------------------------------------------------------------------------------
+// Wide variants for ranks <= 16: many small CTAs and all loads of a thread in flight at once.
+// ---------------------------------------------------------------------------------------------
+constexpr int kRdTok = 8;       // tokens per CTA
+constexpr int kRdCols = 1024;   // K columns per CTA (256 threads x 4)
+
+// Sum each of V values over the 32 lanes by recursive halving: afterwards lane L holds the totals
+// of the original indices [L * V / 32, (L + 1) * V / 32) in v[0 .. V / 32).
+template <int V>
+__device__ __forceinline__ void warp_halving_sum(float (&v)[V], const int lane) {
+#pragma unroll
+  for (int off = 16, n = V; off >= 1; off >>= 1, n >>= 1) {
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) {
+      const float send = upper ? v[i] : v[i + n / 2];
+      const float keep = upper ? v[i + n / 2] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+    }
+  }
+}
+
+// part[kc][t][j] = sum over the CTA's K-chunk kc of A'[t, k] S_slot[j, k]
+template <typename TA, int R>
+__global__ void __launch_bounds__(256) k_rowdot_wide(const RowDotArgs a, float* __restrict__ part) {
+  constexpr int V = kRdTok * R;
+  __shared__ float red[8][V];
+  const int item = blockIdx.x / (kGemmTileT / kRdTok);
+  const int grp = blockIdx.x % (kGemmTileT / kRdTok);
+  if (item >= *a.n_items) return;
+  const TokenItem it = a.items[item];
+  const int64_t tg = (int64_t)it.t0 + (int64_t)grp * kRdTok;
+  if (tg >= it.t1) return;
+  const int kc = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int slot = it.slot;
+  const int32_t r = slot >= 0 ? a.rank[slot] : 0;
+  const int64_t k = (int64_t)kc * kRdCols + threadIdx.x * 4;
+  const bool kok = k < a.K && r > 0;
+  float sv[R][4];
+#pragma unroll
+  for (int j = 0; j < R; ++j) {
+    if (kok && j < r) {
+      const float4 q = __ldg(reinterpret_cast<const float4*>(a.s[slot] + (int64_t)j * a.lds + k));
+      sv[j][0] = q.x; sv[j][1] = q.y; sv[j][2] = q.z; sv[j][3] = q.w;
+    } else {
+      sv[j][0] = sv[j][1] = sv[j][2] = sv[j][3] = 0.f;
+    }
+  }
+  float x[kRdTok][4];
+#pragma unroll
+  for (int u = 0; u < kRdTok; ++u) {
+    const int64_t t = tg + u;
+    if (kok && t < it.t1) {
+      const TA* src = reinterpret_cast<const TA*>(a.a) + t * a.lda + k;
+      if (Vec<TA>::N == 4) {
+        load16(reinterpret_cast<const float*>(src), x[u]);
+      } else {
+        const uint2 w = __ldg(reinterpret_cast<const uint2*>(src));
+        x[u][0] = __uint_as_float(w.x << 16); x[u][1] = __uint_as_float(w.x & 0xFFFF0000u);
+        x[u][2] = __uint_as_float(w.y << 16); x[u][3] = __uint_as_float(w.y & 0xFFFF0000u);
+      }
+    } else {
+      x[u][0] = x[u][1] = x[u][2] = x[u][3] = 0.f;
+    }
+  }
+  if (kok && a.colscale) {
+    const float4 c4 = __ldg(reinterpret_cast<const float4*>(a.colscale + k));
+#pragma unroll
+    for (int u = 0; u < kRdTok; ++u) { x[u][0] *= c4.x; x[u][1] *= c4.y; x[u][2] *= c4.z; x[u][3] *= c4.w; }
+  }
+  if (kok && a.mask) {
+#pragma unroll
+    for (int u = 0; u < kRdTok; ++u)
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (tg + u < it.t1 && !drop_keep(a.drop, tg + u, k + e)) x[u][e] = 0.f;
+  }
+  float v[V];
+#pragma unroll
+  for (int u = 0; u < kRdTok; ++u)
+#pragma unroll
+    for (int j = 0; j < R; ++j)
+      v[u * R + j] = fmaf(x[u][0], sv[j][0], fmaf(x[u][1], sv[j][1], fmaf(x[u][2], sv[j][2], x[u][3] * sv[j][3])));
+  warp_halving_sum<V>(v, lane);
+#pragma unroll
+  for (int i = 0; i < V / 32; ++i) red[warp][lane * (V / 32) + i] = v[i];
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < V; idx += 256) {
+    float acc = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) acc += red[w][idx];
+    const int u = idx / R, j = idx - u * R;
+    const int64_t t = tg + u;
+    if (t < it.t1) part[((int64_t)kc * a.T + t) * R + j] = acc;
+  }
+}
+
+// out[t, j] = alpha_slot * sum_kc part[kc][t][j] for j < r_slot, 0 for r_slot <= j < ldo
+template <int R>
+__global__ void k_rowdot_finish(const RowDotArgs a, const float* __restrict__ part, int nkc) {
+  const int item = blockIdx.x;
+  if (item >= *a.n_items) return;
+  const TokenItem it = a.items[item];
+  const int32_t r = it.slot >= 0 ? a.rank[it.slot] : 0;
+  const float alpha = it.slot >= 0 ? a.alpha[it.slot] : 0.f;
+  const int64_t n = (int64_t)(it.t1 - it.t0) * a.ldo;
+  for (int64_t e = threadIdx.x; e < n; e += blockDim.x) {
+    const int64_t t = it.t0 + e / a.ldo;
+    const int j = (int)(e % a.ldo);
+    float v = 0.f;
+    if (j < r)
+      for (int kc = 0; kc < nkc; ++kc) v += part[((int64_t)kc * a.T + t) * R + j];
+    a.out[t * a.ldo + j] = (j < r) ? v * alpha : 0.f;
+  }
+}
+
+constexpr int kCrTok = 32;      // tokens per CTA
+constexpr int kCrCols = 512;    // columns per CTA (256 threads x 2)
+
+// part[g][n][j] = sum over the 32 tokens of token group g (within one work item) of P[t, j] B'[t, n]
+template <typename TB, int R>
+__global__ void __launch_bounds__(256) k_colred_wide(const ColRedArgs a) {
+  __shared__ __align__(16) float sP[kCrTok * R];
+  const int item = blockIdx.y / (kRedTileT / kCrTok);
+  const int sub = blockIdx.y % (kRedTileT / kCrTok);
+  if (item >= *a.n_items) return;
+  const TokenItem it = a.items[item];
+  const int64_t t0 = (int64_t)it.t0 + (int64_t)sub * kCrTok;
+  const int64_t n0 = (int64_t)blockIdx.x * kCrCols + threadIdx.x * 2;
+  float* dst = a.part + (int64_t)blockIdx.y * a.N * a.ldpart;
+  if (it.slot < 0) return;
+  const int32_t r = a.rank[it.slot];
+  const int nt = (int)max((int64_t)0, min((int64_t)kCrTok, (int64_t)it.t1 - t0));
+  for (int e = threadIdx.x; e < kCrTok * R; e += 256) {
+    const int tt = e / R, j = e - tt * R;
+    sP[e] = (tt < nt && j < r) ? a.p[(t0 + tt) * a.ldp + j] : 0.f;
+  }
+  __syncthreads();
+  if (n0 >= a.N) return;
+  float acc[2][R];
+#pragma unroll
+  for (int c = 0; c < 2; ++c)
+#pragma unroll
+    for (int j = 0; j < R; ++j) acc[c][j] = 0.f;
+  float cs0 = 1.f, cs1 = 1.f;
+  if (a.colscale) { cs0 = __ldg(a.colscale + n0); cs1 = __ldg(a.colscale + n0 + 1); }
+#pragma unroll 1
+  for (int tb = 0; tb < kCrTok; tb += 8) {
+    float b[8][2];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int tt = tb + u;
+      if (tt < nt) {
+        const TB* src = reinterpret_cast<const TB*>(a.b) + (t0 + tt) * a.ldb + n0;
+        b[u][0] = to_f(src[0]);
+        b[u][1] = to_f(src[1]);
+      } else {
+        b[u][0] = b[u][1] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int tt = tb + u;
+      float b0 = b[u][0] * cs0, b1 = b[u][1] * cs1;
+      if (a.mask && tt < nt) {
+        if (!drop_keep(a.drop, t0 + tt, n0)) b0 = 0.f;
+        if (!drop_keep(a.drop, t0 + tt, n0 + 1)) b1 = 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < R; j += 4) {
+        const float4 pv = *reinterpret_cast<const float4*>(&sP[tt * R + j]);
+        acc[0][j] = fmaf(pv.x, b0, acc[0][j]); acc[1][j] = fmaf(pv.x, b1, acc[1][j]);
+        acc[0][j + 1] = fmaf(pv.y, b0, acc[0][j + 1]); acc[1][j + 1] = fmaf(pv.y, b1, acc[1][j + 1]);
+        acc[0][j + 2] = fmaf(pv.z, b0, acc[0][j + 2]); acc[1][j + 2] = fmaf(pv.z, b1, acc[1][j + 2]);
+        acc[0][j + 3] = fmaf(pv.w, b0, acc[0][j + 3]); acc[1][j + 3] = fmaf(pv.w, b1, acc[1][j + 3]);
+      }
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    float* d = dst + (n0 + c) * a.ldpart;
+#pragma unroll
+    for (int j = 0; j < R; ++j)
+      if (j < a.ldpart) d[j] = acc[c][j];
+  }
+}
+
 template <typename TA>
 cudaError_t rowdot_for_rank(const RowDotArgs& a, int max_items, cudaStream_t st) {
   const int rm = a.max_rank;
@@ -218,9 +406,34 @@ cudaError_t colred_for_rank(const ColRedArgs& a, int max_items, cudaStream_t st)
 
 }  // namespace
 
+template <typename TA, int R>
+cudaError_t rowdot_wide(const RowDotArgs& a, int max_items, cudaStream_t st, int prof_kind) {
+  const int nkc = (int)((a.K + kRdCols - 1) / kRdCols);
+  dim3 grid((unsigned)(max_items * (kGemmTileT / kRdTok)), (unsigned)nkc);
+  prof_begin(prof_kind, st);
+  k_rowdot_wide<TA, R><<<grid, 256, 0, st>>>(a, a.part);
+  prof_end(prof_kind, st);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  prof_begin(0, st);
+  k_rowdot_finish<R><<<(unsigned)max_items, 256, 0, st>>>(a, a.part, nkc);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_rowdot(int dtype, const RowDotArgs& a, int max_items, cudaStream_t st,
                           int prof_kind) {
   if (max_items <= 0) return cudaSuccess;
+  if (a.part && a.max_rank <= 16 && (a.K % 4) == 0) {
+    const bool f = dtype == LORA_F32;
+    if (a.max_rank <= 4)
+      return f ? rowdot_wide<float, 4>(a, max_items, st, prof_kind)
+               : rowdot_wide<__nv_bfloat16, 4>(a, max_items, st, prof_kind);
+    if (a.max_rank <= 8)
+      return f ? rowdot_wide<float, 8>(a, max_items, st, prof_kind)
+               : rowdot_wide<__nv_bfloat16, 8>(a, max_items, st, prof_kind);
+    return f ? rowdot_wide<float, 16>(a, max_items, st, prof_kind)
+             : rowdot_wide<__nv_bfloat16, 16>(a, max_items, st, prof_kind);
+  }
   prof_begin(prof_kind, st);
   cudaError_t e = dtype == LORA_F32 ? rowdot_for_rank<float>(a, max_items, st)
                                     : rowdot_for_rank<__nv_bfloat16>(a, max_items, st);
@@ -231,6 +444,21 @@ cudaError_t launch_rowdot(int dtype, const RowDotArgs& a, int max_items, cudaStr
 cudaError_t launch_colred(int dtype, const ColRedArgs& a, int max_items, cudaStream_t st,
                           int prof_kind) {
   if (max_items <= 0) return cudaSuccess;
+  if (a.max_rank <= 16 && a.sub_groups == kRedTileT / kCrTok) {
+    dim3 grid((unsigned)((a.N + kCrCols - 1) / kCrCols), (unsigned)(max_items * a.sub_groups));
+    prof_begin(prof_kind, st);
+    if (dtype == LORA_F32) {
+      if (a.max_rank <= 4) k_colred_wide<float, 4><<<grid, 256, 0, st>>>(a);
+      else if (a.max_rank <= 8) k_colred_wide<float, 8><<<grid, 256, 0, st>>>(a);
+      else k_colred_wide<float, 16><<<grid, 256, 0, st>>>(a);
+    } else {
+      if (a.max_rank <= 4) k_colred_wide<__nv_bfloat16, 4><<<grid, 256, 0, st>>>(a);
+      else if (a.max_rank <= 8) k_colred_wide<__nv_bfloat16, 8><<<grid, 256, 0, st>>>(a);
+      else k_colred_wide<__nv_bfloat16, 16><<<grid, 256, 0, st>>>(a);
+    }
+    prof_end(prof_kind, st);
+    return cudaGetLastError();
+  }
   prof_begin(prof_kind, st);
   cudaError_t e = dtype == LORA_F32 ? colred_for_rank<float>(a, max_items, st)
                                     : colred_for_rank<__nv_bfloat16>(a, max_items, st);
