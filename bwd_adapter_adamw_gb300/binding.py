@@ -78,9 +78,10 @@ def _load() -> C.CDLL:
         "lora_scale": (F, [F, I32, I32]),
         "lora_lr_at": (D, [I32, D, U64, U64, U64, D]),
         "lora_workspace_size": (SZ, [DP, I64]),
+        "lora_prepared_weight_size": (SZ, [DP]),
         "lora_prepare_weight": (C.c_int, [DP, P, P, P]),
         "lora_dora_norm": (C.c_int, [DP, P, P, P, P, P]),
-        "lora_forward": (C.c_int, [DP, CP, I64, P, P, P, P, P, P, P, P, P, SZ, P]),
+        "lora_forward": (C.c_int, [DP, CP, I64, P, P, P, P, P, P, P, P, P, P, SZ, P]),
         "lora_backward": (C.c_int, [DP, CP, I64, P, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P]),
         "lora_grad_prepare_workspace_size": (SZ, [I32, C.POINTER(lora_group)]),
         "lora_grad_prepare": (C.c_int, [P, I32, C.POINTER(lora_group), P, P, P, SZ, P]),
@@ -88,8 +89,8 @@ def _load() -> C.CDLL:
         "lora_adamw_step": (C.c_int, [P, P, P, P, I32, C.POINTER(lora_group),
                                       C.POINTER(lora_adamw_hp), P, P, I32, P]),
         "multi_lora_workspace_size": (SZ, [DP, I64, I32, I32, C.POINTER(lora_slot)]),
-        "multi_lora_forward": (C.c_int, [DP, CP, I64, P, P, I32, P, P, I32, C.POINTER(lora_slot),
-                                         P, P, P, SZ, P]),
+        "multi_lora_forward": (C.c_int, [DP, CP, I64, P, P, P, I32, P, P, I32,
+                                         C.POINTER(lora_slot), P, P, P, SZ, P]),
         "multi_lora_backward": (C.c_int, [DP, CP, I64, P, P, I32, P, P, I32,
                                           C.POINTER(lora_slot), P, P, P, P, SZ, P]),
         "lora_dropout_mask": (C.c_int, [DP, CP, I64, P, P]),
@@ -109,7 +110,7 @@ def _load() -> C.CDLL:
 
 _lib = _load()
 EXPORTED = ("lora_status_string", "lora_scale", "lora_lr_at", "lora_workspace_size",
-            "lora_prepare_weight", "lora_dora_norm", "lora_forward", "lora_backward",
+            "lora_prepared_weight_size", "lora_prepare_weight", "lora_dora_norm", "lora_forward", "lora_backward",
             "lora_grad_prepare_workspace_size", "lora_grad_prepare", "lora_grad_prepare_noalloc",
             "lora_adamw_step",
             "multi_lora_workspace_size", "multi_lora_forward", "multi_lora_backward",
@@ -184,8 +185,12 @@ def lora_workspace_size(d: lora_desc, T: int) -> int:
     return _lib.lora_workspace_size(C.byref(d), T)
 
 
-def lora_prepare_weight(d: lora_desc, W, W_t, stream=None):
-    return _check(_lib.lora_prepare_weight(C.byref(d), _ptr(W), _ptr(W_t), _stream(stream)),
+def lora_prepared_weight_size(d: lora_desc) -> int:
+    return _lib.lora_prepared_weight_size(C.byref(d))
+
+
+def lora_prepare_weight(d: lora_desc, W, W_prep, stream=None):
+    return _check(_lib.lora_prepare_weight(C.byref(d), _ptr(W), _ptr(W_prep), _stream(stream)),
                   "lora_prepare_weight")
 
 
@@ -194,21 +199,21 @@ def lora_dora_norm(d: lora_desc, W, A, B, norm_out, stream=None):
                                       _stream(stream)), "lora_dora_norm")
 
 
-def lora_forward(d: lora_desc, c: Optional[lora_ctx], T: int, X, W, A, B, dora_m, dora_n, Y,
-                 H_save, ws, ws_bytes: Optional[int] = None, stream=None, check=True):
+def lora_forward(d: lora_desc, c: Optional[lora_ctx], T: int, X, W, W_prep, A, B, dora_m, dora_n,
+                 Y, H_save, ws, ws_bytes: Optional[int] = None, stream=None, check=True):
     nbytes = ws_bytes if ws_bytes is not None else ws.numel() * ws.element_size()
     st = _lib.lora_forward(C.byref(d), C.byref(c) if c is not None else None, T, _ptr(X), _ptr(W),
-                           _ptr(A), _ptr(B), _ptr(dora_m), _ptr(dora_n), _ptr(Y), _ptr(H_save),
+                           _ptr(W_prep), _ptr(A), _ptr(B), _ptr(dora_m), _ptr(dora_n), _ptr(Y), _ptr(H_save),
                            _ptr(ws), nbytes, _stream(stream))
     return _check(st, "lora_forward") if check else st
 
 
-def lora_backward(d: lora_desc, c: Optional[lora_ctx], T: int, X, W_t, A, B, dY, H_save, dora_m,
+def lora_backward(d: lora_desc, c: Optional[lora_ctx], T: int, X, W_prep, A, B, dY, H_save, dora_m,
                   dora_n, Y_save, dX, dA, dB, dm, ws, ws_bytes: Optional[int] = None, stream=None,
                   check=True):
     nbytes = ws_bytes if ws_bytes is not None else ws.numel() * ws.element_size()
     st = _lib.lora_backward(C.byref(d), C.byref(c) if c is not None else None, T, _ptr(X),
-                            _ptr(W_t), _ptr(A), _ptr(B), _ptr(dY), _ptr(H_save), _ptr(dora_m),
+                            _ptr(W_prep), _ptr(A), _ptr(B), _ptr(dY), _ptr(H_save), _ptr(dora_m),
                             _ptr(dora_n), _ptr(Y_save), _ptr(dX), _ptr(dA), _ptr(dB), _ptr(dm),
                             _ptr(ws), nbytes, _stream(stream))
     return _check(st, "lora_backward") if check else st
@@ -267,20 +272,20 @@ def multi_lora_workspace_size(d: lora_desc, T: int, n_seg: int, slots) -> int:
     return _lib.multi_lora_workspace_size(C.byref(d), T, n_seg, len(slots), slots)
 
 
-def multi_lora_forward(d, c, T, X, W, n_seg, seg_start, seg_slot, slots, Y, H_save, ws,
+def multi_lora_forward(d, c, T, X, W, W_prep, n_seg, seg_start, seg_slot, slots, Y, H_save, ws,
                        ws_bytes=None, stream=None, check=True):
     nbytes = ws_bytes if ws_bytes is not None else ws.numel() * ws.element_size()
     st = _lib.multi_lora_forward(C.byref(d), C.byref(c) if c is not None else None, T, _ptr(X),
-                                 _ptr(W), n_seg, _ptr(seg_start), _ptr(seg_slot), len(slots),
+                                 _ptr(W), _ptr(W_prep), n_seg, _ptr(seg_start), _ptr(seg_slot), len(slots),
                                  slots, _ptr(Y), _ptr(H_save), _ptr(ws), nbytes, _stream(stream))
     return _check(st, "multi_lora_forward") if check else st
 
 
-def multi_lora_backward(d, c, T, X, W_t, n_seg, seg_start, seg_slot, slots, dY, H_save, dX, ws,
+def multi_lora_backward(d, c, T, X, W_prep, n_seg, seg_start, seg_slot, slots, dY, H_save, dX, ws,
                         ws_bytes=None, stream=None, check=True):
     nbytes = ws_bytes if ws_bytes is not None else ws.numel() * ws.element_size()
     st = _lib.multi_lora_backward(C.byref(d), C.byref(c) if c is not None else None, T, _ptr(X),
-                                  _ptr(W_t), n_seg, _ptr(seg_start), _ptr(seg_slot), len(slots),
+                                  _ptr(W_prep), n_seg, _ptr(seg_start), _ptr(seg_slot), len(slots),
                                   slots, _ptr(dY), _ptr(H_save), _ptr(dX), _ptr(ws), nbytes,
                                   _stream(stream))
     return _check(st, "multi_lora_backward") if check else st

@@ -190,6 +190,9 @@ struct Layout {
   float* partA;        // [rmax_items][in][rank] (fp32 path)
   uint16_t* dYs;       // [T, out] bf16 dY * (m / n) for the DoRA tensor-core products
   float* rd_part;      // [K chunks][T][16] partials of the CUDA-core shrink / G (fp32 path)
+  float* Ah;           // [T, K] tf32 split of X (forward) or dY' (backward): hi ... (fp32 path)
+  float* Al;           // ... and lo
+
   // tensor-core path
   uint16_t* Xd;        // [T, in] bf16 masked input (dropout)
   uint16_t* Sa;        // per slot [2 r, in] bf16 split of A
@@ -253,6 +256,8 @@ Layout carve(const lora_desc* d, int64_t T, int32_t n_seg, int n_slots, int64_t 
   if (!tc) {
     const int64_t kmax = d->in_dim > d->out_dim ? d->in_dim : d->out_dim;
     L.rd_part = c.take<float>((size_t)((kmax + kRowChunk - 1) / kRowChunk) * T * kRowPartCols);
+    L.Ah = c.take<float>((size_t)T * kmax);
+    L.Al = c.take<float>((size_t)T * kmax);
   }
   L.bytes = c.off + kWsAlign;
   return L;
@@ -444,7 +449,7 @@ int run_backward_tc(const lora_desc* d, const DropParams& dp, int64_t T, const v
 
 // forward: shrink then the frozen product with the up-projection as extra K-steps
 int run_forward(const lora_desc* d, const DropParams& dp, int64_t T, const void* X, const void* W,
-                int32_t n_seg, const int32_t* seg_start, const int32_t* seg_slot, const Slots& s,
+                const void* Wprep, int32_t n_seg, const int32_t* seg_start, const int32_t* seg_slot, const Slots& s,
                 const float* ratio_src_m, const float* ratio_src_n, void* Y, float* H, void* ws,
                 cudaStream_t st) {
   if (d->dtype == LORA_BF16)
@@ -471,12 +476,17 @@ int run_forward(const lora_desc* d, const DropParams& dp, int64_t T, const void*
     a.out = H; a.ldo = d->rank;
     a.items = L.gitems; a.n_items = L.gcount;
     a.T = T; a.part = L.rd_part;
+    a.split_hi = L.Ah; a.split_lo = L.Al;
     LORA_TRY(launch_rowdot(d->dtype, a, (int)L.gmax, st, LORA_PROF_SHRINK));
   }
-  // frozen product + Hs B_k^T, times m/n per column in DoRA mode (3xTF32 tensor cores)
+  // frozen product + Hs B_k^T, times m/n per column in DoRA mode (3xTF32 tensor cores); the
+  // prepared weight holds [W_hi | W_lo | W^T_hi | W^T_lo]
   {
+    const int64_t n = d->out_dim * d->in_dim;
     TcGemmArgs t{};
-    t.a = X; t.T = T; t.b = W; t.n_rows = d->out_dim; t.K = d->in_dim;
+    t.a = L.Ah; t.a_lo = L.Al; t.T = T;
+    t.b = Wprep; t.b_lo = static_cast<const float*>(Wprep) + n;
+    t.n_rows = d->out_dim; t.K = d->in_dim;
     t.p = H; t.ldp = d->rank; t.n_slots = s.n;
     for (int k = 0; k < s.n; ++k) { t.q[k] = s.B[k]; t.q_rank[k] = s.rank[k]; }
     t.n_colscale = ratio; t.out = Y; t.ldo = d->out_dim;
@@ -529,15 +539,19 @@ int run_backward(const lora_desc* d, const DropParams& dp, int64_t T, const void
     a.out = L.Gs; a.ldo = d->rank;
     a.items = L.gitems; a.n_items = L.gcount;
     a.T = T; a.part = L.rd_part;
+    if (dX) { a.split_hi = L.Ah; a.split_lo = L.Al; }
     LORA_TRY(launch_rowdot(d->dtype, a, (int)L.gmax, st, LORA_PROF_G));
   }
-  // dX = dY' W + (Gs A_k) * M
+  // dX = dY' W + (Gs A_k) * M, from the split of dY' and of W^T
   if (dX) {
+    const int64_t n = d->out_dim * d->in_dim;
     TcGemmArgs t{};
-    t.a = dY; t.T = T; t.b = Wt; t.n_rows = d->in_dim; t.K = d->out_dim;
+    t.a = L.Ah; t.a_lo = L.Al; t.T = T;
+    t.b = static_cast<const float*>(Wt) + 2 * n; t.b_lo = static_cast<const float*>(Wt) + 3 * n;
+    t.n_rows = d->in_dim; t.K = d->out_dim;
     t.p = L.Gs; t.ldp = d->rank; t.n_slots = s.n;
     for (int k = 0; k < s.n; ++k) { t.q[k] = At[k]; t.q_rank[k] = s.rank[k]; }
-    t.lora_separate = dp.enabled; t.a_colscale = ratio; t.out = dX; t.ldo = d->in_dim;
+    t.lora_separate = dp.enabled; t.out = dX; t.ldo = d->in_dim;
     t.items = L.gitems; t.n_items = L.gcount; t.max_items = (int)L.gmax; t.drop = dp;
     LORA_TRY(launch_tc_gemm_f32(t, st, LORA_PROF_FROZEN_DX));
   }
@@ -628,14 +642,20 @@ size_t multi_lora_workspace_size(const lora_desc* d, int64_t T, int32_t n_seg, i
   return ws_size(d, T, n_seg, s.n, s.rank_sum);
 }
 
-int lora_prepare_weight(const lora_desc* d, const void* W, void* W_t, void* stream) {
+size_t lora_prepared_weight_size(const lora_desc* d) {
+  if (check_desc(d, 0, false) != LORA_OK) return 0;
+  const size_t n = (size_t)d->out_dim * (size_t)d->in_dim;
+  return d->dtype == LORA_F32 ? 16 * n : 2 * n;
+}
+
+int lora_prepare_weight(const lora_desc* d, const void* W, void* W_prep, void* stream) {
   int rc = check_desc(d, 0, false);
   if (rc) return rc;
-  if (!W || !W_t) return LORA_ERR_INVALID;
-  if (!al16(W) || !al16(W_t)) return LORA_ERR_ALIGN;
+  if (!W || !W_prep) return LORA_ERR_INVALID;
+  if (!al16(W) || !al16(W_prep)) return LORA_ERR_ALIGN;
   clear_stale();
-  return cuda_status(launch_transpose_weight(d->dtype, W, W_t, d->out_dim, d->in_dim,
-                                             (cudaStream_t)stream));
+  return cuda_status(launch_prepare_weight(d->dtype, W, W_prep, d->out_dim, d->in_dim,
+                                           (cudaStream_t)stream));
 }
 
 int lora_dora_norm(const lora_desc* d, const void* W, const float* A, const float* B,
@@ -650,27 +670,29 @@ int lora_dora_norm(const lora_desc* d, const void* W, const float* A, const floa
 }
 
 int lora_forward(const lora_desc* d, const lora_ctx* c, int64_t T, const void* X, const void* W,
-                 const float* A, const float* B, const float* dora_m, const float* dora_n,
-                 void* Y, float* H_save, void* ws, size_t ws_bytes, void* stream) {
+                 const void* W_prep, const float* A, const float* B, const float* dora_m,
+                 const float* dora_n, void* Y, float* H_save, void* ws, size_t ws_bytes,
+                 void* stream) {
   int rc = check_desc(d, T, false);
   if (rc) return rc;
   DropParams dp;
   if ((rc = build_drop(d, c, T, dp))) return rc;
-  if (!X || !W || !A || !B || !Y || !H_save || !ws) return LORA_ERR_INVALID;
+  if (!X || !W || !W_prep || !A || !B || !Y || !H_save || !ws) return LORA_ERR_INVALID;
   if (d->dora && (!dora_m || !dora_n)) return LORA_ERR_INVALID;
-  if (!al16(X) || !al16(W) || !al16(A) || !al16(B) || !al16(Y) || !al16(H_save) || !al16(ws))
+  if (!al16(X) || !al16(W) || !al16(W_prep) || !al16(A) || !al16(B) || !al16(Y) ||
+      !al16(H_save) || !al16(ws))
     return LORA_ERR_ALIGN;
   if (d->dora && (!al16(dora_m) || !al16(dora_n))) return LORA_ERR_ALIGN;
   if (ws_bytes < ws_size(d, T, -1, 1, d->rank)) return LORA_ERR_WORKSPACE;
   if (T == 0) return LORA_OK;
   Slots s;
   single_slot(d, A, B, nullptr, nullptr, s);
-  return run_forward(d, dp, T, X, W, -1, nullptr, nullptr, s, d->dora ? dora_m : nullptr,
+  return run_forward(d, dp, T, X, W, W_prep, -1, nullptr, nullptr, s, d->dora ? dora_m : nullptr,
                      d->dora ? dora_n : nullptr, Y, H_save, ws, (cudaStream_t)stream);
 }
 
 int lora_backward(const lora_desc* d, const lora_ctx* c, int64_t T, const void* X,
-                  const void* W_t, const float* A, const float* B, const void* dY,
+                  const void* W_prep, const float* A, const float* B, const void* dY,
                   const float* H_save, const float* dora_m, const float* dora_n,
                   const void* Y_save, void* dX, float* dA, float* dB, float* dm, void* ws,
                   size_t ws_bytes, void* stream) {
@@ -678,9 +700,9 @@ int lora_backward(const lora_desc* d, const lora_ctx* c, int64_t T, const void* 
   if (rc) return rc;
   DropParams dp;
   if ((rc = build_drop(d, c, T, dp))) return rc;
-  if (!X || !W_t || !A || !B || !dY || !H_save || !dA || !dB || !ws) return LORA_ERR_INVALID;
+  if (!X || !W_prep || !A || !B || !dY || !H_save || !dA || !dB || !ws) return LORA_ERR_INVALID;
   if (d->dora && (!dora_m || !dora_n || !Y_save || !dm)) return LORA_ERR_INVALID;
-  if (!al16(X) || !al16(W_t) || !al16(A) || !al16(B) || !al16(dY) || !al16(H_save) || !al16(dA) ||
+  if (!al16(X) || !al16(W_prep) || !al16(A) || !al16(B) || !al16(dY) || !al16(H_save) || !al16(dA) ||
       !al16(dB) || !al16(ws) || (dX && !al16(dX)))
     return LORA_ERR_ALIGN;
   if (d->dora && (!al16(dora_m) || !al16(dora_n) || !al16(Y_save) || !al16(dm)))
@@ -689,15 +711,15 @@ int lora_backward(const lora_desc* d, const lora_ctx* c, int64_t T, const void* 
   if (T == 0) return LORA_OK;
   Slots s;
   single_slot(d, A, B, dA, dB, s);
-  return run_backward(d, dp, T, X, W_t, -1, nullptr, nullptr, s, dY, H_save,
+  return run_backward(d, dp, T, X, W_prep, -1, nullptr, nullptr, s, dY, H_save,
                       d->dora ? dora_m : nullptr, d->dora ? dora_n : nullptr, Y_save, dX,
                       d->dora ? dm : nullptr, ws, (cudaStream_t)stream);
 }
 
 int multi_lora_forward(const lora_desc* d, const lora_ctx* c, int64_t T, const void* X,
-                       const void* W, int32_t n_seg, const int32_t* d_seg_start,
-                       const int32_t* d_seg_slot, int32_t n_slots, const lora_slot* slots,
-                       void* Y, float* H_save, void* ws, size_t ws_bytes, void* stream) {
+                       const void* W, const void* W_prep, int32_t n_seg,
+                       const int32_t* d_seg_start, const int32_t* d_seg_slot, int32_t n_slots,
+                       const lora_slot* slots, void* Y, float* H_save, void* ws, size_t ws_bytes, void* stream) {
   int rc = check_desc(d, T, true);
   if (rc) return rc;
   DropParams dp;
@@ -705,17 +727,18 @@ int multi_lora_forward(const lora_desc* d, const lora_ctx* c, int64_t T, const v
   Slots s;
   if ((rc = slots_from_table(d, n_slots, slots, false, s))) return rc;
   if (n_seg < 0 || (n_seg > 0 && (!d_seg_start || !d_seg_slot))) return LORA_ERR_INVALID;
-  if (!X || !W || !Y || !H_save || !ws) return LORA_ERR_INVALID;
-  if (!al16(X) || !al16(W) || !al16(Y) || !al16(H_save) || !al16(ws)) return LORA_ERR_ALIGN;
+  if (!X || !W || !W_prep || !Y || !H_save || !ws) return LORA_ERR_INVALID;
+  if (!al16(X) || !al16(W) || !al16(W_prep) || !al16(Y) || !al16(H_save) || !al16(ws))
+    return LORA_ERR_ALIGN;
   if (ws_bytes < ws_size(d, T, n_seg, s.n, s.rank_sum)) return LORA_ERR_WORKSPACE;
   if (T == 0) return LORA_OK;
-  return run_forward(d, dp, T, X, W, n_seg, n_seg ? d_seg_start : nullptr,
+  return run_forward(d, dp, T, X, W, W_prep, n_seg, n_seg ? d_seg_start : nullptr,
                      n_seg ? d_seg_slot : nullptr, s, nullptr, nullptr, Y, H_save, ws,
                      (cudaStream_t)stream);
 }
 
 int multi_lora_backward(const lora_desc* d, const lora_ctx* c, int64_t T, const void* X,
-                        const void* W_t, int32_t n_seg, const int32_t* d_seg_start,
+                        const void* W_prep, int32_t n_seg, const int32_t* d_seg_start,
                         const int32_t* d_seg_slot, int32_t n_slots, const lora_slot* slots,
                         const void* dY, const float* H_save, void* dX, void* ws,
                         size_t ws_bytes, void* stream) {
@@ -726,12 +749,12 @@ int multi_lora_backward(const lora_desc* d, const lora_ctx* c, int64_t T, const 
   Slots s;
   if ((rc = slots_from_table(d, n_slots, slots, true, s))) return rc;
   if (n_seg < 0 || (n_seg > 0 && (!d_seg_start || !d_seg_slot))) return LORA_ERR_INVALID;
-  if (!X || !W_t || !dY || !H_save || !ws) return LORA_ERR_INVALID;
-  if (!al16(X) || !al16(W_t) || !al16(dY) || !al16(H_save) || !al16(ws) || (dX && !al16(dX)))
+  if (!X || !W_prep || !dY || !H_save || !ws) return LORA_ERR_INVALID;
+  if (!al16(X) || !al16(W_prep) || !al16(dY) || !al16(H_save) || !al16(ws) || (dX && !al16(dX)))
     return LORA_ERR_ALIGN;
   if (ws_bytes < ws_size(d, T, n_seg, s.n, s.rank_sum)) return LORA_ERR_WORKSPACE;
   if (T == 0) return LORA_OK;
-  return run_backward(d, dp, T, X, W_t, n_seg, n_seg ? d_seg_start : nullptr,
+  return run_backward(d, dp, T, X, W_prep, n_seg, n_seg ? d_seg_start : nullptr,
                       n_seg ? d_seg_slot : nullptr, s, dY, H_save, nullptr, nullptr, nullptr, dX,
                       nullptr, ws, (cudaStream_t)stream);
 }

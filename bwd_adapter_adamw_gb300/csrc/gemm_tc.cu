@@ -236,8 +236,12 @@ bool make_map_2d(CUtensorMap* map, const void* ptr, CUtensorMapDataType dt, int 
   cuuint64_t strides[1] = {row_elems * (uint64_t)elem};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
+  // the box row decides the swizzle: 128-byte rows -> 128B, 64-byte rows -> 64B
+  const uint32_t row_bytes = box_inner * (uint32_t)elem;
+  if (row_bytes != 128 && row_bytes != 64) return false;
+  const CUtensorMapSwizzle swz = row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   return fn(map, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

@@ -11,9 +11,11 @@ void prof_end(int kind, cudaStream_t st);
 
 // ---- gemm_tc.cu: tcgen05 frozen products (bf16 activations) ----
 struct TcGemmArgs {
-  const void* a;             // [T, K] bf16, K-contiguous
+  const void* a;             // [T, K] K-contiguous: bf16, or the tf32-rounded hi part (fp32 kernel)
+  const void* a_lo;          // fp32 kernel: [T, K] remainders a - hi
   int64_t T;
-  const void* b;             // [n_rows, K] bf16, K-contiguous
+  const void* b;             // [n_rows, K] K-contiguous: bf16, or the hi part (fp32 kernel)
+  const void* b_lo;          // fp32 kernel: [n_rows, K] remainders
   int64_t n_rows;
   int64_t K;
   const float* p;            // LoRA term P [T, ldp] fp32 (nullptr: no LoRA term)
@@ -23,7 +25,6 @@ struct TcGemmArgs {
   int32_t n_slots;
   int32_t lora_separate;     // LoRA term in its own accumulator, masked by dropout at (t, n)
   DropParams drop;
-  const float* a_colscale;   // fp32 kernel only: A[t, k] * a_colscale[k] (DoRA dY'), nullable
   const float* n_colscale;   // per output column scale (DoRA m / n), nullable
   void* out;                 // [T, ldo] in the activation dtype
   int64_t ldo;
@@ -32,7 +33,7 @@ struct TcGemmArgs {
   int max_items;
 };
 cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st, int prof_kind);
-// gemm_tc_f32.cu: the same products for fp32 activations, 3xTF32 with an in-shared-memory split
+// gemm_tc_f32.cu: the same products for fp32 activations, 3xTF32 on operands split beforehand
 cudaError_t launch_tc_gemm_f32(const TcGemmArgs& a, cudaStream_t st, int prof_kind);
 cudaError_t read_tc_error(uint32_t* out, bool reset);
 
@@ -120,6 +121,8 @@ struct RowDotArgs {                 // out[t, j] = alpha_slot * sum_k A'[t, k] S
   const int32_t* n_items;
   int64_t T;
   float* part;                      // K-chunk partials [ceil(K / 1024)][T][16] (ranks <= 16)
+  float* split_hi;                  // fp32, nullable: A' (colscaled, unmasked) rounded to tf32 ...
+  float* split_lo;                  // ... and A' - hi, both [T, K]: the 3xTF32 product's operands
 };
 struct ColRedArgs {                 // part[item][n][j] = sum_{t in item} P[t, j] B'[t, n]
   const float* p;                   // [T, ldp] fp32
@@ -159,8 +162,9 @@ struct TransposeTab {
 };
 cudaError_t launch_transpose_slots(const TransposeTab& t, int n, int64_t max_rows, int64_t max_cols,
                                    cudaStream_t st);
-cudaError_t launch_transpose_weight(int dtype, const void* W, void* Wt, int64_t rows, int64_t cols,
-                                    cudaStream_t st);
+// prepared copy of a frozen W [rows, cols]: bf16 W^T, or fp32 [W_hi | W_lo | W^T_hi | W^T_lo]
+cudaError_t launch_prepare_weight(int dtype, const void* W, void* Wt, int64_t rows, int64_t cols,
+                                  cudaStream_t st);
 
 cudaError_t launch_reduce_parts(const float* part, const TokenItem* items, const int32_t* n_items,
                                 int max_items, int32_t sub, int64_t M, int64_t ldp, int transposed,

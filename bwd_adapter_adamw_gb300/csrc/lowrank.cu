@@ -80,6 +80,34 @@ __global__ void k_transpose_w(const T* __restrict__ src, T* __restrict__ dst, in
   }
 }
 
+// fp32 prepared weight: W [rows, cols] -> [W_hi | W_lo | W^T_hi | W^T_lo] (tf32 split, above)
+__global__ void k_prepare_w_f32(const float* __restrict__ src, float* __restrict__ dst, int64_t rows,
+                                int64_t cols) {
+  __shared__ float tile[32][33];
+  const int64_t n = rows * cols;
+  const int64_t c0 = (int64_t)blockIdx.x * 32, r0 = (int64_t)blockIdx.y * 32;
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    const int64_t r = r0 + i, c = c0 + threadIdx.x;
+    if (r < rows && c < cols) {
+      const float x = src[r * cols + c];
+      const float h = tf32_hi(x);
+      dst[r * cols + c] = h;
+      dst[n + r * cols + c] = x - h;
+      tile[i][threadIdx.x] = x;
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    const int64_t c = c0 + i, r = r0 + threadIdx.x;
+    if (r < rows && c < cols) {
+      const float x = tile[threadIdx.x][i];
+      const float h = tf32_hi(x);
+      dst[2 * n + c * rows + r] = h;
+      dst[3 * n + c * rows + r] = x - h;
+    }
+  }
+}
+
 // out_slot += sum over the slot's items, in item order, of the per-item partials.
 // part[item * sub + g] is [M][ldp] (sub partials per item); element (m, j), j < rank_slot, goes to
 // out_slot[m * rank + j]
@@ -188,11 +216,11 @@ cudaError_t launch_transpose_slots(const TransposeTab& t, int n, int64_t max_row
   return cudaGetLastError();
 }
 
-cudaError_t launch_transpose_weight(int dtype, const void* W, void* Wt, int64_t rows, int64_t cols,
-                                    cudaStream_t st) {
+cudaError_t launch_prepare_weight(int dtype, const void* W, void* Wt, int64_t rows, int64_t cols,
+                                  cudaStream_t st) {
   dim3 grid((unsigned)((cols + 31) / 32), (unsigned)((rows + 31) / 32));
   if (dtype == LORA_F32)
-    { prof_begin(0, st); k_transpose_w<float><<<grid, dim3(32, 8), 0, st>>>((const float*)W, (float*)Wt, rows, cols); }
+    { prof_begin(0, st); k_prepare_w_f32<<<grid, dim3(32, 8), 0, st>>>((const float*)W, (float*)Wt, rows, cols); }
   else
     { prof_begin(0, st); k_transpose_w<__nv_bfloat16><<<grid, dim3(32, 8), 0, st>>>((const __nv_bfloat16*)W,
                                                                 (__nv_bfloat16*)Wt, rows, cols); }

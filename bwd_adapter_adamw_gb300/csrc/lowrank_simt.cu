@@ -5,6 +5,8 @@
 //  k_rowdot:  out[t, j] = alpha_slot * sum_k A'[t, k] S_slot[j, k]   (shrink with S = A,
 //             G with S = B^T); one warp per token, lanes stride over K with 16-byte loads, the
 //             slot's S staged in shared memory one K-chunk at a time, warp-shuffle reduction.
+//             Since it reads every A'[t, k] anyway, it also writes the tf32 hi / lo split of A'
+//             that the 3xTF32 frozen product consumes (X in the forward, dY' in the backward).
 //  k_colred:  part[item][n][j] = sum_{t in item} P[t, j] B'[t, n]   (dB with P = Hs, B' = dY';
 //             dA^T with P = Gs, B' = Xd); every thread owns CPT adjacent columns, the item's P
 //             rows are staged in shared memory, one partial per work item, reduced in order.
@@ -15,6 +17,22 @@
 namespace lora {
 
 namespace {
+
+// hi / lo of A'[t, k .. k + 3] for the tokens t = t0 + u < t1 (the 3xTF32 frozen product's operand)
+template <int U>
+__device__ __forceinline__ void write_split(const RowDotArgs& a, const float (&x)[U][4], int64_t t0,
+                                            int64_t t1, int64_t k) {
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    if (t0 + u >= t1) continue;
+    const int64_t o = (t0 + u) * a.K + k;
+    float4 h, l;
+    h.x = tf32_hi(x[u][0]); h.y = tf32_hi(x[u][1]); h.z = tf32_hi(x[u][2]); h.w = tf32_hi(x[u][3]);
+    l.x = x[u][0] - h.x; l.y = x[u][1] - h.y; l.z = x[u][2] - h.z; l.w = x[u][3] - h.w;
+    *reinterpret_cast<float4*>(a.split_hi + o) = h;
+    *reinterpret_cast<float4*>(a.split_lo + o) = l;
+  }
+}
 
 constexpr int kRowWarps = 8;
 constexpr int kRowSmemFloats = 12288;              // 48 KB of S per K-chunk
@@ -45,7 +63,8 @@ __global__ void __launch_bounds__(256) k_rowdot(const RowDotArgs a) {
   for (int u = 0; u < kTokPerWarp; ++u)
 #pragma unroll
     for (int j = 0; j < R; ++j) acc[u][j] = 0.f;
-  for (int64_t k0 = 0; k0 < K && r > 0; k0 += chunk) {
+  const bool split = Vec<TA>::N == 4 && a.split_hi != nullptr;
+  for (int64_t k0 = 0; k0 < K && (r > 0 || split); k0 += chunk) {
     const int64_t kn = min(chunk, K - k0);
     __syncthreads();
     for (int64_t e = threadIdx.x; e < (int64_t)R * chunk; e += 256) {
@@ -78,6 +97,10 @@ __global__ void __launch_bounds__(256) k_rowdot(const RowDotArgs a) {
         if (a.colscale) {
 #pragma unroll
           for (int e = 0; e < 4; ++e) x[e] *= __ldg(a.colscale + k0 + k + e);
+        }
+        if (split) {
+          const float xs[1][4] = {{x[0], x[1], x[2], x[3]}};
+          write_split<1>(a, xs, t, it.t1, k0 + k);
         }
         if (a.mask) {
 #pragma unroll
@@ -228,7 +251,8 @@ __global__ void __launch_bounds__(256) k_rowdot_wide(const RowDotArgs a, float* 
   const int slot = it.slot;
   const int32_t r = slot >= 0 ? a.rank[slot] : 0;
   const int64_t k = (int64_t)kc * kRdCols + threadIdx.x * 4;
-  const bool kok = k < a.K && r > 0;
+  const bool kin = k < a.K;
+  const bool kok = kin && r > 0;
   float sv[R][4];
 #pragma unroll
   for (int j = 0; j < R; ++j) {
@@ -243,7 +267,7 @@ __global__ void __launch_bounds__(256) k_rowdot_wide(const RowDotArgs a, float* 
 #pragma unroll
   for (int u = 0; u < kRdTok; ++u) {
     const int64_t t = tg + u;
-    if (kok && t < it.t1) {
+    if (kin && t < it.t1) {
       const TA* src = reinterpret_cast<const TA*>(a.a) + t * a.lda + k;
       if (Vec<TA>::N == 4) {
         load16(reinterpret_cast<const float*>(src), x[u]);
@@ -256,11 +280,12 @@ __global__ void __launch_bounds__(256) k_rowdot_wide(const RowDotArgs a, float* 
       x[u][0] = x[u][1] = x[u][2] = x[u][3] = 0.f;
     }
   }
-  if (kok && a.colscale) {
+  if (kin && a.colscale) {
     const float4 c4 = __ldg(reinterpret_cast<const float4*>(a.colscale + k));
 #pragma unroll
     for (int u = 0; u < kRdTok; ++u) { x[u][0] *= c4.x; x[u][1] *= c4.y; x[u][2] *= c4.z; x[u][3] *= c4.w; }
   }
+  if (Vec<TA>::N == 4 && kin && a.split_hi) write_split(a, x, tg, it.t1, k);
   if (kok && a.mask) {
 #pragma unroll
     for (int u = 0; u < kRdTok; ++u)

@@ -90,6 +90,13 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
          ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
+// K-major operand tile in 64-byte swizzled rows: 8-row groups 512 bytes apart (SBO), swizzle mode
+// 4 (64B).
+__device__ __forceinline__ uint64_t smem_desc_sw64(uint32_t saddr) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(512 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)4 << 61);
+}
+
 // MN-major operand tile in the 128-byte swizzle: each K row holds 64 contiguous 16-bit MN
 // elements (128 bytes), 8 K rows form a 1024-byte atom (SBO = 1024 between K groups), and
 // successive 64-element MN blocks sit lbo_bytes apart (LBO).
@@ -178,7 +185,8 @@ __device__ __forceinline__ void store8(__nv_bfloat16* p, const float* v) {
 }
 
 
-// Shared helpers for host-side tensor maps (gemm_tc.cu).
+// Shared helpers for host-side tensor maps (gemm_tc.cu). The box row (box_inner * elem bytes) must
+// be 128 or 64 bytes and selects the matching swizzle.
 bool make_map_2d(CUtensorMap* map, const void* ptr, CUtensorMapDataType dt, int elem, uint64_t inner,
                  uint64_t outer, uint64_t row_elems, uint32_t box_inner, uint32_t box_outer);
 

@@ -35,7 +35,7 @@ class Linear:
     X: torch.Tensor          # [T, in]
     W: torch.Tensor          # [out, in]
     dY: torch.Tensor         # [T, out]
-    Wt: Optional[torch.Tensor] = None   # [in, out], filled by prepare_weights
+    Wp: Optional[torch.Tensor] = None   # prepared copy of W (bytes), filled by prepare_weights
     Y: Optional[torch.Tensor] = None
     dX: Optional[torch.Tensor] = None
     H: Optional[torch.Tensor] = None
@@ -132,9 +132,10 @@ class LoraStep:
 
     def prepare_weights(self, stream=None):
         for l in self.linears:
-            if l.Wt is None:
-                l.Wt = torch.empty((l.in_dim, l.out_dim), dtype=l.W.dtype, device=self.device)
-            L.lora_prepare_weight(self.desc(l), l.W, l.Wt, stream)
+            if l.Wp is None:
+                l.Wp = torch.empty(L.lora_prepared_weight_size(self.desc(l)), dtype=torch.uint8,
+                                   device=self.device)
+            L.lora_prepare_weight(self.desc(l), l.W, l.Wp, stream)
 
     def groups(self, lr: float, step: int):
         return L.make_groups([dict(offset=0, n_a=self.n_a, n_b=self.n_b, n_mag=self.n_mag,
@@ -171,8 +172,8 @@ class LoraStep:
                 ctx = L.make_ctx(opt_step, ordinal, ct)
                 sl = slice(t0, t0 + n)
                 X, dY, Y, dX, H = l.X[sl], l.dY[sl], l.Y[sl], l.dX[sl], l.H[sl]
-                L.lora_forward(d, ctx, n, X, l.W, l.A, l.B, l.mag, l.norm, Y, H, ws, stream=st)
-                L.lora_backward(d, ctx, n, X, l.Wt, l.A, l.B, dY, H, l.mag, l.norm, Y, dX, l.gA,
+                L.lora_forward(d, ctx, n, X, l.W, l.Wp, l.A, l.B, l.mag, l.norm, Y, H, ws, stream=st)
+                L.lora_backward(d, ctx, n, X, l.Wp, l.A, l.B, dY, H, l.mag, l.norm, Y, dX, l.gA,
                                 l.gB, l.gmag, ws, stream=st)
         if self.streams:
             for s in self.streams:
@@ -199,7 +200,7 @@ class MultiLinear:
     X: torch.Tensor
     W: torch.Tensor
     dY: torch.Tensor
-    Wt: Optional[torch.Tensor] = None
+    Wp: Optional[torch.Tensor] = None
     Y: Optional[torch.Tensor] = None
     dX: Optional[torch.Tensor] = None
     H: Optional[torch.Tensor] = None
@@ -286,9 +287,10 @@ class MultiLoraStep:
 
     def prepare_weights(self, stream=None):
         for l in self.linears:
-            if l.Wt is None:
-                l.Wt = torch.empty((l.in_dim, l.out_dim), dtype=l.W.dtype, device=self.device)
-            L.lora_prepare_weight(self.desc(l), l.W, l.Wt, stream)
+            if l.Wp is None:
+                l.Wp = torch.empty(L.lora_prepared_weight_size(self.desc(l)), dtype=torch.uint8,
+                                   device=self.device)
+            L.lora_prepare_weight(self.desc(l), l.W, l.Wp, stream)
 
     def forward_backward(self, opt_step: int = 0):
         main = torch.cuda.current_stream(self.device)
@@ -303,9 +305,9 @@ class MultiLoraStep:
             d = self.desc(l)
             ctx = L.make_ctx(opt_step, 0, 0)
             sl = self.slots(l)
-            L.multi_lora_forward(d, ctx, self.T, l.X, l.W, self.n_seg, self.seg_start,
+            L.multi_lora_forward(d, ctx, self.T, l.X, l.W, l.Wp, self.n_seg, self.seg_start,
                                  self.seg_slot, sl, l.Y, l.H, ws, stream=st)
-            L.multi_lora_backward(d, ctx, self.T, l.X, l.Wt, self.n_seg, self.seg_start,
+            L.multi_lora_backward(d, ctx, self.T, l.X, l.Wp, self.n_seg, self.seg_start,
                                   self.seg_slot, sl, l.dY, l.H, l.dX, ws, stream=st)
         if self.streams:
             for s in self.streams:

@@ -141,9 +141,19 @@ double lora_lr_at(int32_t kind, double base, uint64_t step, uint64_t warmup, uin
 size_t lora_workspace_size(const lora_desc* d, int64_t T);
 
 /* ---- frozen-weight preparation (once per frozen W, not per step) ----------------------------*/
-/* W_t = W^T ([in_dim, out_dim]): the layout the dX product reads, kept resident beside W so
- * that both frozen products stream K-contiguous operands. */
-int lora_prepare_weight(const lora_desc* d, const void* W, void* W_t, void* stream);
+/* Bytes of the prepared copy of W that lora_prepare_weight writes (W is frozen, so this is made
+ * once and kept resident beside W):
+ *   bf16: W^T [in_dim, out_dim] bf16, the K-contiguous operand of the dX product
+ *         (2 * in_dim * out_dim bytes);
+ *   fp32: the tf32 split of W and of W^T for the 3xTF32 tensor-core products, four fp32 arrays
+ *         [W_hi | W_lo | W^T_hi | W^T_lo], each element x stored as x_hi = x rounded to tf32
+ *         (nearest, ties away from zero) and x_lo = x - x_hi (16 * in_dim * out_dim bytes).
+ * Returns 0 for an invalid descriptor. */
+size_t lora_prepared_weight_size(const lora_desc* d);
+
+/* Writes the prepared copy (above) of W [out_dim, in_dim] into W_prep (16-byte aligned, at least
+ * lora_prepared_weight_size bytes). */
+int lora_prepare_weight(const lora_desc* d, const void* W, void* W_prep, void* stream);
 
 /* DoRA row norm n_o = || W_o + s (B A)_o ||_2 for the current A, B (fp32 [out_dim]); call once
  * per optimizer step before the first forward ("8. LoRA Fundamentals", How it works, and its
@@ -153,19 +163,22 @@ int lora_dora_norm(const lora_desc* d, const void* W, const float* A, const floa
 
 /* ---- forward / backward (one adapted linear, T tokens) --------------------------------------*/
 /* Y [T, out] = X W^T + Hs B^T, then * (dora_m / dora_n) per column in DoRA mode.
+ * W is the frozen weight and W_prep its prepared copy (lora_prepare_weight); both are required
+ * (the bf16 product reads W, the fp32 product reads W_prep).
  * H_save [T, rank] fp32 receives Hs = s' (Xd A^T) (the scaled shrink), which lora_backward
  * reads. dora_m, dora_n: [out] fp32, required iff desc.dora. */
 int lora_forward(const lora_desc* d, const lora_ctx* c, int64_t T, const void* X, const void* W,
-                 const float* A, const float* B, const float* dora_m, const float* dora_n,
-                 void* Y, float* H_save, void* ws, size_t ws_bytes, void* stream);
+                 const void* W_prep, const float* A, const float* B, const float* dora_m,
+                 const float* dora_n, void* Y, float* H_save, void* ws, size_t ws_bytes,
+                 void* stream);
 
 /* dX [T, in] = dY' W + (Gs A) * M with Gs = s' dY' B (written, may be NULL to skip dX);
  * dA [r, in] += Gs^T Xd; dB [out, r] += dY'^T H_save; dm [out] += sum_t dY * Y_save / m (DoRA).
- * W_t from lora_prepare_weight. Y_save (the forward's Y) and dm are required iff desc.dora.
+ * W_prep from lora_prepare_weight. Y_save (the forward's Y) and dm are required iff desc.dora.
  * Accumulation over chunks is the caller's sequence of calls (or one call with chunk_tokens);
  * the token sums inside one call are reduced in a fixed order, so reruns are bitwise equal. */
 int lora_backward(const lora_desc* d, const lora_ctx* c, int64_t T, const void* X,
-                  const void* W_t, const float* A, const float* B, const void* dY,
+                  const void* W_prep, const float* A, const float* B, const void* dY,
                   const float* H_save, const float* dora_m, const float* dora_n,
                   const void* Y_save, void* dX, float* dA, float* dB, float* dm, void* ws,
                   size_t ws_bytes, void* stream);
@@ -227,15 +240,15 @@ size_t multi_lora_workspace_size(const lora_desc* d, int64_t T, int32_t n_seg, i
                                  const lora_slot* slots);
 
 int multi_lora_forward(const lora_desc* d, const lora_ctx* c, int64_t T, const void* X,
-                       const void* W, int32_t n_seg, const int32_t* d_seg_start,
-                       const int32_t* d_seg_slot, int32_t n_slots, const lora_slot* slots,
-                       void* Y, float* H_save, void* ws, size_t ws_bytes, void* stream);
+                       const void* W, const void* W_prep, int32_t n_seg,
+                       const int32_t* d_seg_start, const int32_t* d_seg_slot, int32_t n_slots,
+                       const lora_slot* slots, void* Y, float* H_save, void* ws, size_t ws_bytes, void* stream);
 
 /* dX may be NULL. Each slot's dA/dB accumulate that slot's tokens with weight 1; per-slot
  * 1/adapter_global_batch_size, clip and Adam are lora_grad_prepare / lora_adamw_step with one
  * group per ready slot. */
 int multi_lora_backward(const lora_desc* d, const lora_ctx* c, int64_t T, const void* X,
-                        const void* W_t, int32_t n_seg, const int32_t* d_seg_start,
+                        const void* W_prep, int32_t n_seg, const int32_t* d_seg_start,
                         const int32_t* d_seg_slot, int32_t n_slots, const lora_slot* slots,
                         const void* dY, const float* H_save, void* dX, void* ws,
                         size_t ws_bytes, void* stream);

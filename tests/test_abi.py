@@ -56,9 +56,9 @@ FAKE = 1 << 20   # an aligned non-null address; never dereferenced (validation f
 
 
 def _fwd(L, d, T=16, ws_bytes=1 << 30, **kw):
-    args = dict(X=FAKE, W=FAKE, A=FAKE, B=FAKE, dm=None, dn=None, Y=FAKE, H=FAKE, ws=FAKE)
+    args = dict(X=FAKE, W=FAKE, Wp=FAKE, A=FAKE, B=FAKE, dm=None, dn=None, Y=FAKE, H=FAKE, ws=FAKE)
     args.update(kw)
-    return L.lora_forward(d, None, T, args["X"], args["W"], args["A"], args["B"], args["dm"],
+    return L.lora_forward(d, None, T, args["X"], args["W"], args["Wp"], args["A"], args["B"], args["dm"],
                           args["dn"], args["Y"], args["H"], args["ws"], ws_bytes, stream=0,
                           check=False)
 
@@ -74,19 +74,27 @@ def test_forward_argument_errors(L):
     assert _fwd(L, L.make_desc(64, 64, 4, 2.0, L.LORA_F32, proj_id=70000)) == L.LORA_ERR_INVALID
     assert _fwd(L, ok, T=-1) == L.LORA_ERR_INVALID
     assert _fwd(L, ok, X=None) == L.LORA_ERR_INVALID
+    assert _fwd(L, ok, Wp=None) == L.LORA_ERR_INVALID
+    assert _fwd(L, ok, Wp=FAKE + 8) == L.LORA_ERR_ALIGN
     assert _fwd(L, ok, Y=FAKE + 4) == L.LORA_ERR_ALIGN
     assert _fwd(L, ok, ws_bytes=16) == L.LORA_ERR_WORKSPACE
     dora = L.make_desc(64, 64, 4, 2.0, L.LORA_F32, dora=True)
     assert _fwd(L, dora) == L.LORA_ERR_INVALID          # magnitudes missing
     # more chunks in one call than the key table holds
     c = L.make_ctx(0, 0, 1)
-    st = L.lora_forward(ok, c, 65, FAKE, FAKE, FAKE, FAKE, None, None, FAKE, FAKE, FAKE, 1 << 30,
-                        stream=0, check=False)
+    st = L.lora_forward(ok, c, 65, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, FAKE, FAKE, FAKE,
+                        1 << 30, stream=0, check=False)
     assert st == L.LORA_ERR_UNSUPPORTED
     c = L.make_ctx(0, 65535, 8)
-    st = L.lora_forward(ok, c, 16, FAKE, FAKE, FAKE, FAKE, None, None, FAKE, FAKE, FAKE, 1 << 30,
-                        stream=0, check=False)
+    st = L.lora_forward(ok, c, 16, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, FAKE, FAKE, FAKE,
+                        1 << 30, stream=0, check=False)
     assert st == L.LORA_ERR_INVALID
+
+
+def test_prepared_weight_size(L):
+    assert L.lora_prepared_weight_size(L.make_desc(2048, 256, 8, 2.0, L.LORA_F32)) == 16 * 2048 * 256
+    assert L.lora_prepared_weight_size(L.make_desc(1536, 4096, 16, 2.0, L.LORA_BF16)) == 2 * 1536 * 4096
+    assert L.lora_prepared_weight_size(L.make_desc(1536, 4096, 0, 2.0, L.LORA_BF16)) == 0
 
 
 def test_workspace_sizes(L):
@@ -105,10 +113,10 @@ def test_multi_argument_errors(L):
     bad = L.make_slots([dict(A=FAKE, B=FAKE, dA=FAKE, dB=FAKE, rank=72, scale=1.0)])
     assert L.multi_lora_workspace_size(d, 1024, 5, bad) == 0
     st = L.multi_lora_forward(L.make_desc(2560, 4096, 64, 0.0, L.LORA_BF16, dora=True), None, 16,
-                              FAKE, FAKE, 1, FAKE, FAKE, slots, FAKE, FAKE, FAKE, 1 << 30,
+                              FAKE, FAKE, FAKE, 1, FAKE, FAKE, slots, FAKE, FAKE, FAKE, 1 << 30,
                               stream=0, check=False)
     assert st == L.LORA_ERR_UNSUPPORTED
-    st = L.multi_lora_forward(d, None, 16, FAKE, FAKE, 1, None, FAKE, slots, FAKE, FAKE, FAKE,
+    st = L.multi_lora_forward(d, None, 16, FAKE, FAKE, FAKE, 1, None, FAKE, slots, FAKE, FAKE, FAKE,
                               1 << 30, stream=0, check=False)
     assert st == L.LORA_ERR_INVALID
     st = L.multi_lora_backward(d, None, 16, FAKE, FAKE, 1, FAKE, FAKE, slots, FAKE, FAKE, None, FAKE,

@@ -409,7 +409,7 @@ def test_multi_single_slot_equals_single_lora(L):
     step, problems, state, s, hp_o = build_single(cfg, [0], [0])
     step.forward_backward(0)
     lin = step.linears[0]
-    ml = MultiLinear(0, lin.X, lin.W, lin.dY, Wt=lin.Wt)
+    ml = MultiLinear(0, lin.X, lin.W, lin.dY, Wp=lin.Wp)
     ms = MultiLoraStep([ml], slot_ranks=[cfg.rank], slot_scales=[s], dtype="bf16", tokens=640,
                        seg_start=torch.tensor([0, 640], dtype=torch.int32, device="cuda"),
                        seg_slot=torch.tensor([0], dtype=torch.int32, device="cuda"))
