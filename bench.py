@@ -36,7 +36,8 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--config", default="c2", choices=sorted(LI.CONFIGS))
     p.add_argument("--layers", type=int, default=0, help="override the layer count (0 = config's)")
-    p.add_argument("--streams", type=int, default=1)
+    p.add_argument("--streams", type=int, default=4,
+                   help="CUDA streams over the independent adapted linears of the step")
     p.add_argument("--no-graph", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--prof-class", type=int, default=0, help="kernel class to time (0 = auto)")

@@ -457,8 +457,14 @@ int run_forward(const lora_desc* d, const DropParams& dp, int64_t T, const void*
                           ratio_src_n, Y, H, ws, st);
   Layout L = carve(d, T, n_seg, s.n, s.rank_sum, false, ws);
   clear_stale();
-  LORA_TRY(launch_make_items(T, n_seg, seg_start, seg_slot, s.n, L.gitems, L.gcount, (int32_t)L.gmax,
-                             L.ritems, L.rcount, (int32_t)L.rmax, st));
+  // single adapter, rank <= 16: uniform token tiles computed in the kernels, single-pass shrink
+  const bool fused = n_seg < 0 && d->rank <= 16;
+  const TokenItem* items = fused ? nullptr : L.gitems;
+  const int32_t* n_items = fused ? nullptr : L.gcount;
+  const int max_items = fused ? (int)((T + kGemmTileT - 1) / kGemmTileT) : (int)L.gmax;
+  if (!fused)
+    LORA_TRY(launch_make_items(T, n_seg, seg_start, seg_slot, s.n, L.gitems, L.gcount,
+                               (int32_t)L.gmax, L.ritems, L.rcount, (int32_t)L.rmax, st));
   const float q = dropout_q(d);
   const float* ratio = nullptr;
   if (ratio_src_m) {
@@ -474,10 +480,10 @@ int run_forward(const lora_desc* d, const DropParams& dp, int64_t T, const void*
     }
     a.max_rank = d->rank; a.mask = dp.enabled; a.drop = dp;
     a.out = H; a.ldo = d->rank;
-    a.items = L.gitems; a.n_items = L.gcount;
+    a.items = items; a.n_items = n_items; a.single_pass = fused;
     a.T = T; a.part = L.rd_part;
     a.split_hi = L.Ah; a.split_lo = L.Al;
-    LORA_TRY(launch_rowdot(d->dtype, a, (int)L.gmax, st, LORA_PROF_SHRINK));
+    LORA_TRY(launch_rowdot(d->dtype, a, max_items, st, LORA_PROF_SHRINK));
   }
   // frozen product + Hs B_k^T, times m/n per column in DoRA mode (3xTF32 tensor cores); the
   // prepared weight holds [W_hi | W_lo | W^T_hi | W^T_lo]
@@ -490,7 +496,7 @@ int run_forward(const lora_desc* d, const DropParams& dp, int64_t T, const void*
     t.p = H; t.ldp = d->rank; t.n_slots = s.n;
     for (int k = 0; k < s.n; ++k) { t.q[k] = s.B[k]; t.q_rank[k] = s.rank[k]; }
     t.n_colscale = ratio; t.out = Y; t.ldo = d->out_dim;
-    t.items = L.gitems; t.n_items = L.gcount; t.max_items = (int)L.gmax; t.drop = dp;
+    t.items = items; t.n_items = n_items; t.max_items = max_items; t.drop = dp;
     LORA_TRY(launch_tc_gemm_f32(t, st, LORA_PROF_FROZEN_FWD));
   }
   return LORA_OK;
@@ -505,13 +511,23 @@ int run_backward(const lora_desc* d, const DropParams& dp, int64_t T, const void
                            Y_save, dX, dm, ws, st);
   Layout L = carve(d, T, n_seg, s.n, s.rank_sum, true, ws);
   clear_stale();
-  LORA_TRY(launch_make_items(T, n_seg, seg_start, seg_slot, s.n, L.gitems, L.gcount, (int32_t)L.gmax,
-                             L.ritems, L.rcount, (int32_t)L.rmax, st));
+  // single adapter, rank <= 16: uniform token tiles, single-pass G that also writes A^T, and
+  // token reductions that finish inside their thread-block clusters (4 launches)
+  const bool fused = n_seg < 0 && d->rank <= 16;
+  const TokenItem* items = fused ? nullptr : L.gitems;
+  const int32_t* n_items = fused ? nullptr : L.gcount;
+  const int max_items = fused ? (int)((T + kGemmTileT - 1) / kGemmTileT) : (int)L.gmax;
+  if (!fused)
+    LORA_TRY(launch_make_items(T, n_seg, seg_start, seg_slot, s.n, L.gitems, L.gcount,
+                               (int32_t)L.gmax, L.ritems, L.rcount, (int32_t)L.rmax, st));
   const float q = dropout_q(d);
   // transposed adapters: At_k = A_k^T [in, r_k], Bt_k = B_k^T [r_k, out]
   float* At[LORA_MAX_SLOTS];
   float* Bt[LORA_MAX_SLOTS];
-  {
+  if (fused) {
+    At[0] = L.At;                  // written by the G pass below
+    Bt[0] = nullptr;               // G reads B in place
+  } else {
     TransposeTab ta{}, tb{};
     int64_t oa = 0, ob = 0;
     for (int k = 0; k < s.n; ++k) {
@@ -537,10 +553,15 @@ int run_backward(const lora_desc* d, const DropParams& dp, int64_t T, const void
     }
     a.max_rank = d->rank; a.colscale = ratio; a.drop = dp;
     a.out = L.Gs; a.ldo = d->rank;
-    a.items = L.gitems; a.n_items = L.gcount;
+    a.items = items; a.n_items = n_items;
     a.T = T; a.part = L.rd_part;
     if (dX) { a.split_hi = L.Ah; a.split_lo = L.Al; }
-    LORA_TRY(launch_rowdot(d->dtype, a, (int)L.gmax, st, LORA_PROF_G));
+    if (fused) {
+      a.single_pass = 1;
+      a.s[0] = s.B[0]; a.lds = d->rank; a.s_rows_k = 1;
+      a.t_src = s.A[0]; a.t_dst = At[0]; a.t_rows = d->rank; a.t_cols = d->in_dim;
+    }
+    LORA_TRY(launch_rowdot(d->dtype, a, max_items, st, LORA_PROF_G));
   }
   // dX = dY' W + (Gs A_k) * M, from the split of dY' and of W^T
   if (dX) {
@@ -552,7 +573,7 @@ int run_backward(const lora_desc* d, const DropParams& dp, int64_t T, const void
     t.p = L.Gs; t.ldp = d->rank; t.n_slots = s.n;
     for (int k = 0; k < s.n; ++k) { t.q[k] = At[k]; t.q_rank[k] = s.rank[k]; }
     t.lora_separate = dp.enabled; t.out = dX; t.ldo = d->in_dim;
-    t.items = L.gitems; t.n_items = L.gcount; t.max_items = (int)L.gmax; t.drop = dp;
+    t.items = items; t.n_items = n_items; t.max_items = max_items; t.drop = dp;
     LORA_TRY(launch_tc_gemm_f32(t, st, LORA_PROF_FROZEN_DX));
   }
   ReduceTab rt{};
@@ -566,10 +587,15 @@ int run_backward(const lora_desc* d, const DropParams& dp, int64_t T, const void
     a.max_rank = d->rank; a.drop = dp;
     a.part = L.partB; a.ldpart = d->rank; a.sub_groups = kRedSub;
     a.items = L.ritems; a.n_items = L.rcount;
-    LORA_TRY(launch_colred(d->dtype, a, (int)L.rmax, st, LORA_PROF_RED_DB));
-    for (int k = 0; k < s.n; ++k) rt.out[k] = s.dB[k];
-    LORA_TRY(launch_reduce_parts(L.partB, L.ritems, L.rcount, (int)L.rmax, kRedSub, d->out_dim, d->rank, 0,
-                                 rt, s.n, st));
+    if (fused) {
+      a.T = T; a.out = s.dB[0]; a.out_transposed = 0;
+      LORA_TRY(launch_colred(d->dtype, a, 0, st, LORA_PROF_RED_DB));
+    } else {
+      LORA_TRY(launch_colred(d->dtype, a, (int)L.rmax, st, LORA_PROF_RED_DB));
+      for (int k = 0; k < s.n; ++k) rt.out[k] = s.dB[k];
+      LORA_TRY(launch_reduce_parts(L.partB, L.ritems, L.rcount, (int)L.rmax, kRedSub, d->out_dim,
+                                   d->rank, 0, rt, s.n, st));
+    }
   }
   // dA_k += sum_t Gs[t, j] M[t, i] X[t, i]   (computed as dA^T partials)
   {
@@ -580,10 +606,15 @@ int run_backward(const lora_desc* d, const DropParams& dp, int64_t T, const void
     a.max_rank = d->rank; a.drop = dp;
     a.part = L.partA; a.ldpart = d->rank; a.sub_groups = kRedSub;
     a.items = L.ritems; a.n_items = L.rcount;
-    LORA_TRY(launch_colred(d->dtype, a, (int)L.rmax, st, LORA_PROF_RED_DA));
-    for (int k = 0; k < s.n; ++k) rt.out[k] = s.dA[k];
-    LORA_TRY(launch_reduce_parts(L.partA, L.ritems, L.rcount, (int)L.rmax, kRedSub, d->in_dim, d->rank, 1,
-                                 rt, s.n, st));
+    if (fused) {
+      a.T = T; a.out = s.dA[0]; a.out_transposed = 1;
+      LORA_TRY(launch_colred(d->dtype, a, 0, st, LORA_PROF_RED_DA));
+    } else {
+      LORA_TRY(launch_colred(d->dtype, a, (int)L.rmax, st, LORA_PROF_RED_DA));
+      for (int k = 0; k < s.n; ++k) rt.out[k] = s.dA[k];
+      LORA_TRY(launch_reduce_parts(L.partA, L.ritems, L.rcount, (int)L.rmax, kRedSub, d->in_dim,
+                                   d->rank, 1, rt, s.n, st));
+    }
   }
   if (dm) LORA_TRY(launch_dora_dm(d->dtype, dY, Y_save, dora_m, T, d->out_dim, dm, st));
   return LORA_OK;

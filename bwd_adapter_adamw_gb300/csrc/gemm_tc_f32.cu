@@ -55,8 +55,9 @@ struct F32Params {
   CUtensorMap tbh, tbl;               // B hi / lo [N, K] fp32, box {32, 128}
   CUtensorMap tp;                     // P [T, ldp] fp32, box {32, 128}
   CUtensorMap tq[LORA_MAX_SLOTS];     // Q_slot [N, r] fp32, box {32, 128}
-  const TokenItem* items;
+  const TokenItem* items;             // null: uniform 128-token tiles, slot 0
   const int32_t* n_items;
+  int64_t T;
   uint32_t* err;
   int32_t nk_main;
   int32_t has_lora;
@@ -84,9 +85,8 @@ __device__ __forceinline__ void split_tile(uint8_t* t, int ct) {
 
 __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm_f32(const __grid_constant__ F32Params p) {
   extern __shared__ uint8_t smem_raw[];
-  const int item = blockIdx.y;
-  if (item >= *p.n_items) return;
-  const TokenItem it = p.items[item];
+  TokenItem it;
+  if (!get_item(p.items, p.n_items, blockIdx.y, p.T, it)) return;
   const int slot = it.slot;
   const int32_t m0 = it.t0;
   const int32_t n0 = blockIdx.x * kBN;
@@ -273,6 +273,7 @@ cudaError_t launch_tc_gemm_f32(const TcGemmArgs& a, cudaStream_t st, int prof_ki
   }
   prm.items = a.items;
   prm.n_items = a.n_items;
+  prm.T = a.T;
   prm.err = tc::error_word();
   if (!prm.err) return cudaErrorInvalidDevice;
   prm.nk_main = (int32_t)((a.K + kBK - 1) / kBK);

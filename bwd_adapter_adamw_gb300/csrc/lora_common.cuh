@@ -97,4 +97,22 @@ struct TokenItem {
   int32_t t0, t1, slot, pad;
 };
 
+// Work item idx of a call: from the item table, or, when the table is null (a single-adapter
+// call), the uniform kGemmTileT-token tiles of [0, T) with slot 0. False past the last item.
+__device__ __forceinline__ bool get_item(const TokenItem* items, const int32_t* n_items, int idx,
+                                         int64_t T, TokenItem& it) {
+  if (items) {
+    if (idx >= *n_items) return false;
+    it = items[idx];
+    return true;
+  }
+  const int64_t t0 = (int64_t)idx * kGemmTileT;
+  if (t0 >= T) return false;
+  it.t0 = (int32_t)t0;
+  it.t1 = (int32_t)(T < t0 + kGemmTileT ? T : t0 + kGemmTileT);
+  it.slot = 0;
+  it.pad = 0;
+  return true;
+}
+
 }  // namespace lora

@@ -28,7 +28,7 @@ struct TcGemmArgs {
   const float* n_colscale;   // per output column scale (DoRA m / n), nullable
   void* out;                 // [T, ldo] in the activation dtype
   int64_t ldo;
-  const TokenItem* items;
+  const TokenItem* items;     // null: uniform 128-token tiles of a single-adapter call
   const int32_t* n_items;
   int max_items;
 };
@@ -117,10 +117,17 @@ struct RowDotArgs {                 // out[t, j] = alpha_slot * sum_k A'[t, k] S
   DropParams drop;
   float* out;                       // [T, ldo]
   int32_t ldo;
-  const TokenItem* items;           // <= 128-token items
+  const TokenItem* items;           // <= 128-token items (null: uniform tiles, slot 0)
   const int32_t* n_items;
   int64_t T;
   float* part;                      // K-chunk partials [ceil(K / 1024)][T][16] (ranks <= 16)
+  int32_t single_pass;              // ranks <= 16: whole K per CTA, no partials
+  int32_t s_rows_k;                 // S_slot stored as [K, lds] (element (j, k) at k lds + j)
+  // side task done by the kernel's CTAs before the product (saves a launch): write the transpose
+  // t_dst [t_cols, t_rows] of t_src [t_rows, t_cols]
+  const float* t_src;
+  float* t_dst;
+  int64_t t_rows, t_cols;
   float* split_hi;                  // fp32, nullable: A' (colscaled, unmasked) rounded to tf32 ...
   float* split_lo;                  // ... and A' - hi, both [T, K]: the 3xTF32 product's operands
 };
@@ -140,7 +147,15 @@ struct ColRedArgs {                 // part[item][n][j] = sum_{t in item} P[t, j
   int32_t sub_groups;               // token groups per item (partials per item)
   const TokenItem* items;
   const int32_t* n_items;
+  // single-adapter fused form (out != null, ranks <= 16): kColGroups token groups of all T tokens,
+  // one cluster per 64-column block, whose fixed-order sum is added into out ([N, ldpart], or
+  // [ldpart, N] when out_transposed)
+  int64_t T;
+  float* out;
+  int32_t out_transposed;
 };
+constexpr int kColGroups = 8;
+constexpr int kColBlock = 64;
 cudaError_t launch_rowdot(int dtype, const RowDotArgs& a, int max_items, cudaStream_t st,
                           int prof_kind);
 cudaError_t launch_colred(int dtype, const ColRedArgs& a, int max_items, cudaStream_t st,

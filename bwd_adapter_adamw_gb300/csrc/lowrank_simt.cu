@@ -46,8 +46,8 @@ __global__ void __launch_bounds__(256) k_rowdot(const RowDotArgs a) {
   constexpr int kRowTok = kRowWarps * kTokPerWarp;   // tokens per CTA (within one work item)
   __shared__ __align__(16) float sS[kRowSmemFloats];
   const int item = blockIdx.x;
-  if (item >= *a.n_items) return;
-  const TokenItem it = a.items[item];
+  TokenItem it;
+  if (!get_item(a.items, a.n_items, item, a.T, it)) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t tbase = (int64_t)it.t0 + (int64_t)blockIdx.y * kRowTok + warp * kTokPerWarp;
   if ((int64_t)it.t0 + (int64_t)blockIdx.y * kRowTok >= it.t1) return;
@@ -70,7 +70,8 @@ __global__ void __launch_bounds__(256) k_rowdot(const RowDotArgs a) {
     for (int64_t e = threadIdx.x; e < (int64_t)R * chunk; e += 256) {
       const int j = (int)(e / chunk);
       const int64_t k = e - (int64_t)j * chunk;
-      sS[e] = (j < r && k < kn) ? __ldg(S + (int64_t)j * a.lds + k0 + k) : 0.f;
+      sS[e] = (j < r && k < kn) ? __ldg(S + (a.s_rows_k ? (k0 + k) * a.lds + j : (int64_t)j * a.lds + k0 + k))
+                                : 0.f;
     }
     __syncthreads();
     for (int64_t k = lane * 4; k < kn; k += 128) {
@@ -144,8 +145,8 @@ template <typename TB, int R, int CPT>
 __global__ void __launch_bounds__(kColThreads) k_colred(const ColRedArgs a) {
   __shared__ __align__(16) float sP[kColTokChunk * R];
   const int item = blockIdx.y;
-  if (item >= *a.n_items) return;
-  const TokenItem it = a.items[item];
+  TokenItem it;
+  if (!get_item(a.items, a.n_items, item, a.T, it)) return;
   if (it.slot < 0) return;
   const int32_t r = a.rank[it.slot];
   const int64_t n0 = ((int64_t)blockIdx.x * kColThreads + threadIdx.x) * CPT;
@@ -242,8 +243,8 @@ __global__ void __launch_bounds__(256) k_rowdot_wide(const RowDotArgs a, float* 
   __shared__ float red[8][V];
   const int item = blockIdx.x / (kGemmTileT / kRdTok);
   const int grp = blockIdx.x % (kGemmTileT / kRdTok);
-  if (item >= *a.n_items) return;
-  const TokenItem it = a.items[item];
+  TokenItem it;
+  if (!get_item(a.items, a.n_items, item, a.T, it)) return;
   const int64_t tg = (int64_t)it.t0 + (int64_t)grp * kRdTok;
   if (tg >= it.t1) return;
   const int kc = blockIdx.y;
@@ -317,8 +318,8 @@ __global__ void __launch_bounds__(256) k_rowdot_wide(const RowDotArgs a, float* 
 template <int R>
 __global__ void k_rowdot_finish(const RowDotArgs a, const float* __restrict__ part, int nkc) {
   const int item = blockIdx.x;
-  if (item >= *a.n_items) return;
-  const TokenItem it = a.items[item];
+  TokenItem it;
+  if (!get_item(a.items, a.n_items, item, a.T, it)) return;
   const int32_t r = it.slot >= 0 ? a.rank[it.slot] : 0;
   const float alpha = it.slot >= 0 ? a.alpha[it.slot] : 0.f;
   const int64_t n = (int64_t)(it.t1 - it.t0) * a.ldo;
@@ -341,8 +342,8 @@ __global__ void __launch_bounds__(256) k_colred_wide(const ColRedArgs a) {
   __shared__ __align__(16) float sP[kCrTok * R];
   const int item = blockIdx.y / (kRedTileT / kCrTok);
   const int sub = blockIdx.y % (kRedTileT / kCrTok);
-  if (item >= *a.n_items) return;
-  const TokenItem it = a.items[item];
+  TokenItem it;
+  if (!get_item(a.items, a.n_items, item, a.T, it)) return;
   const int64_t t0 = (int64_t)it.t0 + (int64_t)sub * kCrTok;
   const int64_t n0 = (int64_t)blockIdx.x * kCrCols + threadIdx.x * 2;
   float* dst = a.part + (int64_t)blockIdx.y * a.N * a.ldpart;
@@ -403,6 +404,244 @@ __global__ void __launch_bounds__(256) k_colred_wide(const ColRedArgs a) {
   }
 }
 
+// ---------------------------------------------------------------------------------------------
+// Single-pass forms for single-adapter calls (ranks <= 16): no partial buffers, no second launch.
+// ---------------------------------------------------------------------------------------------
+
+// two consecutive elements (8- or 4-byte aligned) as floats
+__device__ __forceinline__ void load2(const float* p, float* out) {
+  const float2 v = __ldg(reinterpret_cast<const float2*>(p));
+  out[0] = v.x; out[1] = v.y;
+}
+__device__ __forceinline__ void load2(const __nv_bfloat16* p, float* out) {
+  const uint32_t w = __ldg(reinterpret_cast<const unsigned int*>(p));
+  out[0] = __uint_as_float(w << 16); out[1] = __uint_as_float(w & 0xFFFF0000u);
+}
+
+// Side tasks of a row-dot launch, spread over all its threads (see RowDotArgs).
+__device__ __forceinline__ void rowdot_side_tasks(const RowDotArgs& a) {
+  const int64_t gt = ((int64_t)blockIdx.y * gridDim.x + blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t gs = (int64_t)gridDim.x * gridDim.y * blockDim.x;
+  if (a.t_src) {
+    const int64_t n = a.t_rows * a.t_cols;
+    for (int64_t e = gt; e < n; e += gs) {
+      const int64_t r = e / a.t_cols, c = e - r * a.t_cols;
+      a.t_dst[c * a.t_rows + r] = __ldg(a.t_src + e);
+    }
+  }
+}
+
+// S[j, k .. k + 3] (zero for j >= r) and A'[t, k .. k + 3] for the TOK tokens from tg (zero past t1)
+template <typename TA, int R, int TOK>
+__device__ __forceinline__ void rowdot_load(const RowDotArgs& a, const float* S, int32_t r, int64_t tg,
+                                            int64_t t1, int64_t k, float (&sv)[R][4], float (&x)[TOK][4]) {
+  if (a.s_rows_k) {
+    // S[j, k + e] = S_store[(k + e) lds + j]: rank-contiguous rows of B
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+#pragma unroll
+      for (int j4 = 0; j4 < R / 4; ++j4) {
+        float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (4 * j4 < r) q = __ldg(reinterpret_cast<const float4*>(S + (k + e) * a.lds + 4 * j4));
+        sv[4 * j4][e] = q.x; sv[4 * j4 + 1][e] = q.y; sv[4 * j4 + 2][e] = q.z; sv[4 * j4 + 3][e] = q.w;
+      }
+  } else {
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+      float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (j < r) q = __ldg(reinterpret_cast<const float4*>(S + (int64_t)j * a.lds + k));
+      sv[j][0] = q.x; sv[j][1] = q.y; sv[j][2] = q.z; sv[j][3] = q.w;
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < TOK; ++u) {
+    const int64_t t = tg + u;
+    if (t < t1) {
+      const TA* src = reinterpret_cast<const TA*>(a.a) + t * a.lda + k;
+      if (Vec<TA>::N == 4) {
+        load16(reinterpret_cast<const float*>(src), x[u]);
+      } else {
+        const uint2 w = __ldg(reinterpret_cast<const uint2*>(src));
+        x[u][0] = __uint_as_float(w.x << 16); x[u][1] = __uint_as_float(w.x & 0xFFFF0000u);
+        x[u][2] = __uint_as_float(w.y << 16); x[u][3] = __uint_as_float(w.y & 0xFFFF0000u);
+      }
+    } else {
+      x[u][0] = x[u][1] = x[u][2] = x[u][3] = 0.f;
+    }
+  }
+}
+
+// out[t, j] = alpha * sum_k A'[t, k] S[j, k] for TOK tokens per CTA over the whole K (256 threads
+// x 4 columns per pass, per-thread sums kept across passes), then one warp / CTA reduction.
+template <typename TA, int R, int TOK>
+__global__ void __launch_bounds__(256) k_rowdot_full(const RowDotArgs a) {
+  constexpr int V = TOK * R;
+  static_assert(V % 32 == 0, "per-thread values must fill the warp reduction");
+  __shared__ float red[8][V];
+  rowdot_side_tasks(a);
+  const int item = blockIdx.x / (kGemmTileT / TOK);
+  const int grp = blockIdx.x % (kGemmTileT / TOK);
+  TokenItem it;
+  if (!get_item(a.items, a.n_items, item, a.T, it)) return;
+  const int64_t tg = (int64_t)it.t0 + (int64_t)grp * TOK;
+  if (tg >= it.t1) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int slot = it.slot;
+  const int32_t r = slot >= 0 ? a.rank[slot] : 0;
+  const float* S = slot >= 0 ? a.s[slot] : nullptr;
+  float v[V];
+#pragma unroll
+  for (int i = 0; i < V; ++i) v[i] = 0.f;
+  for (int64_t k = (int64_t)threadIdx.x * 4; k < a.K; k += 1024) {
+    float sv[R][4], x[TOK][4];
+    rowdot_load<TA, R, TOK>(a, S, r, tg, it.t1, k, sv, x);
+    if (a.colscale) {
+      const float4 c4 = __ldg(reinterpret_cast<const float4*>(a.colscale + k));
+#pragma unroll
+      for (int u = 0; u < TOK; ++u) { x[u][0] *= c4.x; x[u][1] *= c4.y; x[u][2] *= c4.z; x[u][3] *= c4.w; }
+    }
+    if (Vec<TA>::N == 4 && a.split_hi) write_split(a, x, tg, it.t1, k);
+    if (a.mask) {
+#pragma unroll
+      for (int u = 0; u < TOK; ++u)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (tg + u < it.t1 && !drop_keep(a.drop, tg + u, k + e)) x[u][e] = 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < TOK; ++u)
+#pragma unroll
+      for (int j = 0; j < R; ++j)
+        v[u * R + j] = fmaf(x[u][0], sv[j][0], fmaf(x[u][1], sv[j][1],
+                            fmaf(x[u][2], sv[j][2], fmaf(x[u][3], sv[j][3], v[u * R + j]))));
+  }
+  warp_halving_sum<V>(v, lane);
+#pragma unroll
+  for (int i = 0; i < V / 32; ++i) red[warp][lane * (V / 32) + i] = v[i];
+  __syncthreads();
+  const float alpha = slot >= 0 ? a.alpha[slot] : 0.f;
+  for (int idx = threadIdx.x; idx < V; idx += 256) {
+    const int u = idx / R, j = idx - u * R;
+    const int64_t t = tg + u;
+    if (t >= it.t1 || j >= a.ldo) continue;
+    float acc = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) acc += red[w][idx];
+    a.out[t * a.ldo + j] = j < r ? acc * alpha : 0.f;
+  }
+}
+
+// Thread-block cluster helpers (distributed shared memory).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// value of float `local` (a shared-memory address in this CTA's layout) in cluster CTA `rank`
+__device__ __forceinline__ float ld_peer(const float* local, uint32_t rank) {
+  uint32_t a = (uint32_t)__cvta_generic_to_shared(local), remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(a), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  return v;
+}
+
+// Fused token reduction of a single-adapter call (ColRedArgs, fused form). The kColGroups CTAs of
+// one 64-column block form a cluster; CTA g sums P[t, j] B'[t, n] over token group g (2 columns
+// per lane; the 8 warps take every 8th token of a 128-token chunk, P rows staged in shared
+// memory) and reduces its warps in warp order. Then every CTA of the cluster adds, for 8 of the
+// block's columns, the groups' sums in group order (read from the peers' shared memory) into
+// out, so reruns are bitwise equal and no partials leave the chip.
+template <typename TB, int R>
+__global__ void __launch_bounds__(256) k_colred_fused(const ColRedArgs a) {
+  constexpr int kChunk = 128;   // tokens staged per pass (16 per warp, all loads in flight)
+  constexpr int U = kChunk / 8;
+  __shared__ __align__(16) float sP[kChunk * R];
+  __shared__ float red[8][kColBlock * R];
+  __shared__ float mine[kColBlock * R];   // this group's sums, [col][j]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t N = a.N;
+  const int64_t nb = (int64_t)blockIdx.x * kColBlock;
+  const int64_t n0 = nb + 2 * lane;
+  const bool nok = n0 < N;
+  const int g = blockIdx.y;   // == rank in the cluster (cluster dims 1 x kColGroups)
+  const int64_t tg = (a.T + kColGroups - 1) / kColGroups;
+  const int64_t t_begin = (int64_t)g * tg;
+  const int64_t t_end = min(a.T, t_begin + tg);
+  const int32_t r = a.rank[0];
+  float cs0 = 1.f, cs1 = 1.f;
+  if (a.colscale && nok) { cs0 = __ldg(a.colscale + n0); cs1 = __ldg(a.colscale + n0 + 1); }
+  float acc[2][R];
+#pragma unroll
+  for (int c = 0; c < 2; ++c)
+#pragma unroll
+    for (int j = 0; j < R; ++j) acc[c][j] = 0.f;
+  for (int64_t c0 = t_begin; c0 < t_end; c0 += kChunk) {
+    const int nt = (int)min((int64_t)kChunk, t_end - c0);
+    // B' loads first, so that they are in flight while P is staged
+    float b[U][2];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int tt = warp + 8 * u;
+      b[u][0] = b[u][1] = 0.f;
+      if (nok && tt < nt) load2(reinterpret_cast<const TB*>(a.b) + (c0 + tt) * a.ldb + n0, b[u]);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < kChunk * R; e += 256) {
+      const int tt = e / R, j = e - tt * R;
+      sP[e] = (tt < nt && j < r) ? __ldg(a.p + (c0 + tt) * a.ldp + j) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int tt = warp + 8 * u;
+      b[u][0] *= cs0;
+      b[u][1] *= cs1;
+      if (a.mask && nok && tt < nt) {
+        if (!drop_keep(a.drop, c0 + tt, n0)) b[u][0] = 0.f;
+        if (!drop_keep(a.drop, c0 + tt, n0 + 1)) b[u][1] = 0.f;
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const float* pr = sP + (warp + 8 * u) * R;   // zero rows past the chunk's tokens
+#pragma unroll
+      for (int j = 0; j < R; j += 4) {
+        const float4 pv = *reinterpret_cast<const float4*>(pr + j);
+        acc[0][j] = fmaf(pv.x, b[u][0], acc[0][j]); acc[1][j] = fmaf(pv.x, b[u][1], acc[1][j]);
+        acc[0][j + 1] = fmaf(pv.y, b[u][0], acc[0][j + 1]); acc[1][j + 1] = fmaf(pv.y, b[u][1], acc[1][j + 1]);
+        acc[0][j + 2] = fmaf(pv.z, b[u][0], acc[0][j + 2]); acc[1][j + 2] = fmaf(pv.z, b[u][1], acc[1][j + 2]);
+        acc[0][j + 3] = fmaf(pv.w, b[u][0], acc[0][j + 3]); acc[1][j + 3] = fmaf(pv.w, b[u][1], acc[1][j + 3]);
+      }
+    }
+  }
+  // reduce the 8 warps in warp order: red[w][j][col] (column-minor, conflict-free)
+#pragma unroll
+  for (int c = 0; c < 2; ++c)
+#pragma unroll
+    for (int j = 0; j < R; ++j) red[warp][j * kColBlock + 2 * lane + c] = acc[c][j];
+  __syncthreads();
+  for (int e = threadIdx.x; e < kColBlock * R; e += 256) {
+    float sum = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) sum += red[w][e];
+    mine[e] = sum;
+  }
+  cluster_sync();
+  // this CTA's share of the block: columns [g * 8, g * 8 + 8), all j; groups summed in order
+  constexpr int kShare = kColBlock / kColGroups;
+  for (int e = threadIdx.x; e < kShare * R; e += 256) {
+    const int jj = e / kShare, cc = e - jj * kShare;
+    const int col = g * kShare + cc;
+    const int64_t n = nb + col;
+    if (n < N && jj < r) {
+      float sum = 0.f;
+      for (int gg = 0; gg < kColGroups; ++gg) sum += ld_peer(&mine[jj * kColBlock + col], (uint32_t)gg);
+      float* o = a.out_transposed ? a.out + (int64_t)jj * N + n : a.out + n * a.ldpart + jj;
+      *o += sum;
+    }
+  }
+  cluster_sync();   // peers' shared memory stays alive until every CTA has read it
+}
+
 template <typename TA>
 cudaError_t rowdot_for_rank(const RowDotArgs& a, int max_items, cudaStream_t st) {
   const int rm = a.max_rank;
@@ -445,9 +684,30 @@ cudaError_t rowdot_wide(const RowDotArgs& a, int max_items, cudaStream_t st, int
   return cudaGetLastError();
 }
 
+template <typename TA, int R, int TOK>
+cudaError_t rowdot_full(const RowDotArgs& a, int max_items, cudaStream_t st, int prof_kind) {
+  prof_begin(prof_kind, st);
+  k_rowdot_full<TA, R, TOK><<<(unsigned)(max_items * (kGemmTileT / TOK)), 256, 0, st>>>(a);
+  prof_end(prof_kind, st);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_rowdot(int dtype, const RowDotArgs& a, int max_items, cudaStream_t st,
                           int prof_kind) {
   if (max_items <= 0) return cudaSuccess;
+  const bool side = a.t_src != nullptr;
+  if (a.single_pass && a.max_rank <= 16) {
+    const bool f = dtype == LORA_F32;
+    if (a.max_rank <= 4)
+      return f ? rowdot_full<float, 4, 8>(a, max_items, st, prof_kind)
+               : rowdot_full<__nv_bfloat16, 4, 8>(a, max_items, st, prof_kind);
+    if (a.max_rank <= 8)
+      return f ? rowdot_full<float, 8, 4>(a, max_items, st, prof_kind)
+               : rowdot_full<__nv_bfloat16, 8, 4>(a, max_items, st, prof_kind);
+    return f ? rowdot_full<float, 16, 2>(a, max_items, st, prof_kind)
+             : rowdot_full<__nv_bfloat16, 16, 2>(a, max_items, st, prof_kind);
+  }
+  if (side || a.s_rows_k) return cudaErrorInvalidValue;   // only the single-pass form has these
   if (a.part && a.max_rank <= 16 && (a.K % 4) == 0) {
     const bool f = dtype == LORA_F32;
     if (a.max_rank <= 4)
@@ -468,6 +728,34 @@ cudaError_t launch_rowdot(int dtype, const RowDotArgs& a, int max_items, cudaStr
 
 cudaError_t launch_colred(int dtype, const ColRedArgs& a, int max_items, cudaStream_t st,
                           int prof_kind) {
+  if (a.out) {
+    if (a.T <= 0) return cudaSuccess;
+    if (a.max_rank > 16) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)((a.N + kColBlock - 1) / kColBlock), (unsigned)kColGroups);
+    cfg.blockDim = dim3(256);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = kColGroups;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e;
+    prof_begin(prof_kind, st);
+    if (dtype == LORA_F32) {
+      if (a.max_rank <= 4) e = cudaLaunchKernelEx(&cfg, k_colred_fused<float, 4>, a);
+      else if (a.max_rank <= 8) e = cudaLaunchKernelEx(&cfg, k_colred_fused<float, 8>, a);
+      else e = cudaLaunchKernelEx(&cfg, k_colred_fused<float, 16>, a);
+    } else {
+      if (a.max_rank <= 4) e = cudaLaunchKernelEx(&cfg, k_colred_fused<__nv_bfloat16, 4>, a);
+      else if (a.max_rank <= 8) e = cudaLaunchKernelEx(&cfg, k_colred_fused<__nv_bfloat16, 8>, a);
+      else e = cudaLaunchKernelEx(&cfg, k_colred_fused<__nv_bfloat16, 16>, a);
+    }
+    prof_end(prof_kind, st);
+    return e != cudaSuccess ? e : cudaGetLastError();
+  }
   if (max_items <= 0) return cudaSuccess;
   if (a.max_rank <= 16 && a.sub_groups == kRedTileT / kCrTok) {
     dim3 grid((unsigned)((a.N + kCrCols - 1) / kCrCols), (unsigned)(max_items * a.sub_groups));
