@@ -10,6 +10,7 @@ Prints ONE JSON line (rank 0). `--impl reference` times the CPU oracle instead.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import math
 import os
@@ -49,6 +50,22 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def max_over_ranks(values, world, device="cpu"):
+    """Element-wise maximum of per-rank timings over all ranks (every rank gets the result)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def whole_job_rate(world, steps, tokens, ms):
+    """Tokens per second of the whole job: every rank processes `tokens` per step (weak scaling),
+    and the job takes the slowest rank's time."""
+    return world * steps * tokens / (ms / 1e3)
+
+
 # --------------------------------------------------------------------------------- algorithmic counts
 def counts(cfg: LI.LoraConfig, layers: int):
     """Per-step algorithmic flops/bytes (stated in the design doc): frozen = 2 T in out per product,
@@ -63,6 +80,32 @@ def counts(cfg: LI.LoraConfig, layers: int):
                 dx_flops_per_launch=dx / (len(cfg.projs) * layers),
                 fwd_flops=fwd, dx_flops=dx, lowrank_flops=lowrank, params=params,
                 opt_bytes=32 * params, act_bytes=a)
+
+
+# DRAM bytes per launch of the dominant kernel class (dram__bytes_read.sum + dram__bytes_write.sum,
+# one ncu capture, caches flushed by ncu), averaged over the class's launch shapes, keyed by
+# (workload, kernel class); valid only while the kernel source still hashes to the recorded
+# value. Command and table: profiles/launch_list_c2_tinyllama_f32.md.
+NCU_TRAFFIC = {
+    ("c2", 1): {"source": "gemm_tc_f32.cu", "sha256_16": "1b1fa9f6ae8235a9",
+                "bytes": (50.50e6 + 21.09e6) / 2,
+                "note": "wq fwd 50.50 MB, wv fwd 21.09 MB read, ~0 written (outputs stay in L2)"},
+}
+
+
+def traffic_for(cfg_name, prof_class):
+    ent = NCU_TRAFFIC.get((cfg_name, prof_class))
+    if ent is None:
+        return None, "no ncu capture for this workload"
+    path = os.path.join(ROOT, "bwd_adapter_adamw_gb300", "csrc", ent["source"])
+    try:
+        with open(path, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    except OSError:
+        return None, "kernel source not found"
+    if sha != ent["sha256_16"]:
+        return None, "kernel changed since the ncu capture"
+    return ent["bytes"], ent["note"]
 
 
 def load_peaks():
@@ -387,13 +430,10 @@ def run_ours(args):
     e2e_ms = e0.elapsed_time(e1)
     clk = clocks.stop()
 
-    t = torch.tensor([ms, e2e_ms], dtype=torch.float64, device=device)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms, e2e_ms = float(t[0]), float(t[1])
+    ms, e2e_ms = max_over_ranks([ms, e2e_ms], world, device)
     tokens = cfg.tokens
-    value = world * K * tokens / (ms / 1e3)
-    e2e_value = world * Ke * tokens / (e2e_ms / 1e3)
+    value = whole_job_rate(world, K, tokens, ms)
+    e2e_value = whole_job_rate(world, Ke, tokens, e2e_ms)
 
     if rank == 0:
         peaks, peak_src = load_peaks()
@@ -414,6 +454,7 @@ def run_ours(args):
             bound, punit = "tensor", "TFLOP/s"
             note = f"dense bf16 cuBLAS burst, {peak_src}"
         achieved = per_launch / (avg_kern / 1e3) / 1e12 if avg_kern else None
+        traffic, traffic_note = traffic_for(cfg.name, prof_class)
         cpu = None
         if not args.no_cpu_baseline and world == 1:
             cpu = cpu_baseline(cfg, layers)
@@ -428,7 +469,8 @@ def run_ours(args):
                        if cfg.name != "c1" else "inputs fit in L2",
                        "cuda_graph": graph is not None, "streams": args.streams},
             "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": punit,
-                         "frac": (achieved / peak) if achieved else None, "traffic": None,
+                         "frac": (achieved / peak) if achieved else None, "traffic": traffic,
+                         "traffic_note": traffic_note,
                          "kernel": {1: "frozen forward GEMM", 2: "frozen dX GEMM"}.get(
                              prof_class, f"class {prof_class}"),
                          "launches_timed": len(kern_ms), "avg_launch_ms": avg_kern,
