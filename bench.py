@@ -68,7 +68,7 @@ def whole_job_rate(world, steps, tokens, ms):
 
 # --------------------------------------------------------------------------------- algorithmic counts
 def counts(cfg: LI.LoraConfig, layers: int):
-    """Per-step algorithmic flops/bytes (stated in the design doc): frozen = 2 T in out per product,
+    """Per-step algorithmic flops/bytes: frozen = 2 T in out per product,
     fused LoRA terms = 2 T r out (forward) / 2 T r in (dX); optimizer = 32 B/param."""
     T, r = cfg.tokens, cfg.rank
     a = 4 if cfg.dtype == "f32" else 2
@@ -85,7 +85,8 @@ def counts(cfg: LI.LoraConfig, layers: int):
 # DRAM bytes per launch of the dominant kernel class (dram__bytes_read.sum + dram__bytes_write.sum,
 # one ncu capture, caches flushed by ncu), averaged over the class's launch shapes, keyed by
 # (workload, kernel class); valid only while the kernel source still hashes to the recorded
-# value. Command and table: profiles/launch_list_c2_tinyllama_f32.md.
+# value. Captured with `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum` on
+# `python bench.py --layers 1 --steps 2 --warmup 3 --no-cpu-baseline --streams 1`.
 NCU_TRAFFIC = {
     ("c2", 1): {"source": "gemm_tc_f32.cu", "sha256_16": "1b1fa9f6ae8235a9",
                 "bytes": (50.50e6 + 21.09e6) / 2,

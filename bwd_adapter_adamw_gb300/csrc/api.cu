@@ -578,6 +578,9 @@ int run_backward(const lora_desc* d, const DropParams& dp, int64_t T, const void
   }
   ReduceTab rt{};
   for (int k = 0; k < s.n; ++k) rt.rank[k] = s.rank[k];
+  // item-based reductions: ranks <= 16 stream 4 token groups per item (4 partials per item), larger
+  // ranks one partial per item
+  const int32_t sub = d->rank <= 16 ? kRedSub : 1;
   // dB_k += sum_t dY'[t, o] Hs[t, j]
   {
     ColRedArgs a{};
@@ -585,7 +588,7 @@ int run_backward(const lora_desc* d, const DropParams& dp, int64_t T, const void
     a.b = dY; a.ldb = d->out_dim; a.N = d->out_dim; a.colscale = ratio;
     for (int k = 0; k < s.n; ++k) a.rank[k] = s.rank[k];
     a.max_rank = d->rank; a.drop = dp;
-    a.part = L.partB; a.ldpart = d->rank; a.sub_groups = kRedSub;
+    a.part = L.partB; a.ldpart = d->rank; a.sub_groups = sub;
     a.items = L.ritems; a.n_items = L.rcount;
     if (fused) {
       a.T = T; a.out = s.dB[0]; a.out_transposed = 0;
@@ -593,7 +596,7 @@ int run_backward(const lora_desc* d, const DropParams& dp, int64_t T, const void
     } else {
       LORA_TRY(launch_colred(d->dtype, a, (int)L.rmax, st, LORA_PROF_RED_DB));
       for (int k = 0; k < s.n; ++k) rt.out[k] = s.dB[k];
-      LORA_TRY(launch_reduce_parts(L.partB, L.ritems, L.rcount, (int)L.rmax, kRedSub, d->out_dim,
+      LORA_TRY(launch_reduce_parts(L.partB, L.ritems, L.rcount, (int)L.rmax, sub, d->out_dim,
                                    d->rank, 0, rt, s.n, st));
     }
   }
@@ -604,7 +607,7 @@ int run_backward(const lora_desc* d, const DropParams& dp, int64_t T, const void
     a.b = X; a.ldb = d->in_dim; a.N = d->in_dim; a.mask = dp.enabled;
     for (int k = 0; k < s.n; ++k) a.rank[k] = s.rank[k];
     a.max_rank = d->rank; a.drop = dp;
-    a.part = L.partA; a.ldpart = d->rank; a.sub_groups = kRedSub;
+    a.part = L.partA; a.ldpart = d->rank; a.sub_groups = sub;
     a.items = L.ritems; a.n_items = L.rcount;
     if (fused) {
       a.T = T; a.out = s.dA[0]; a.out_transposed = 1;
@@ -612,7 +615,7 @@ int run_backward(const lora_desc* d, const DropParams& dp, int64_t T, const void
     } else {
       LORA_TRY(launch_colred(d->dtype, a, (int)L.rmax, st, LORA_PROF_RED_DA));
       for (int k = 0; k < s.n; ++k) rt.out[k] = s.dA[k];
-      LORA_TRY(launch_reduce_parts(L.partA, L.ritems, L.rcount, (int)L.rmax, kRedSub, d->in_dim,
+      LORA_TRY(launch_reduce_parts(L.partA, L.ritems, L.rcount, (int)L.rmax, sub, d->in_dim,
                                    d->rank, 1, rt, s.n, st));
     }
   }

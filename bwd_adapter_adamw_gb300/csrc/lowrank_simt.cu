@@ -757,7 +757,10 @@ cudaError_t launch_colred(int dtype, const ColRedArgs& a, int max_items, cudaStr
     return e != cudaSuccess ? e : cudaGetLastError();
   }
   if (max_items <= 0) return cudaSuccess;
-  if (a.max_rank <= 16 && a.sub_groups == kRedTileT / kCrTok) {
+  // the partial layout must match what the caller reduces: kRedTileT / kCrTok partials per item
+  // from the wide kernel (ranks <= 16), one per item otherwise
+  if (a.sub_groups != (a.max_rank <= 16 ? kRedTileT / kCrTok : 1)) return cudaErrorInvalidValue;
+  if (a.max_rank <= 16) {
     dim3 grid((unsigned)((a.N + kCrCols - 1) / kCrCols), (unsigned)(max_items * a.sub_groups));
     prof_begin(prof_kind, st);
     if (dtype == LORA_F32) {

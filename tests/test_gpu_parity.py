@@ -2,7 +2,7 @@
 
 Every case runs through the C ABI (via the ctypes binding and the step orchestration). Integer
 work (dropout masks, token routing) must be bit-exact; floating point within the per-tensor
-max-relative-error bars of the north-star specification: 1e-5 for fp32 frozen-W paths, 2e-2 on
+max-relative-error bars: 1e-5 for fp32 frozen-W paths, 2e-2 on
 outputs and gradients and 1e-2 on the post-step A/B for bf16 frozen-W paths.
 """
 import json
@@ -342,32 +342,35 @@ def _build_multi(cfg, proj_idx, T, device="cuda"):
     return step, host, r, scales
 
 
-@pytest.mark.parametrize("T,proj_idx,p", [(1500, [0, 3, 6], 0.0), (700, [1], 0.25)])
-def test_multi_lora_parity(L, T, proj_idx, p):
-    cfg = LI.with_overrides(LI.CONFIGS["c5"], dropout_p=p, dropout_seed=99)
+@pytest.mark.parametrize("T,proj_idx,p,dtype", [(1500, [0, 3, 6], 0.0, "bf16"), (700, [1], 0.25, "bf16"),
+                                                (600, [0], 0.0, "f32"), (333, [1], 0.25, "f32")])
+def test_multi_lora_parity(L, T, proj_idx, p, dtype):
+    cfg = LI.with_overrides(LI.CONFIGS["c5"], dropout_p=p, dropout_seed=99, dtype=dtype)
+    tol, tol_step = (TOL_F32, TOL_F32) if dtype == "f32" else (TOL_BF16, TOL_BF16_STEP)
     step, host, r, scales = _build_multi(cfg, proj_idx, T)
     step.forward_backward(0)
     torch.cuda.synchronize()
     tok = O.token_slots(T, r.seg_start, r.seg_slot, len(r.slot_rank))
     q = O.dropout_q(p) if p > 0 else 1.0
-    grads = {}
+    grads, kept = {}, {}
     for lin in step.linears:
         h = host[lin.proj_id]
         keep = O.dropout_keep(p, cfg.dropout_seed, 0, 0, 0, lin.proj_id, T, lin.in_dim) if p > 0 else None
+        kept[lin.proj_id] = keep
         slots = [O.SlotTensors(A, B, sc) for (A, B), sc in zip(h["slots"], scales)]
         Y, H = O.multi_lora_forward(h["X"], h["W"], slots, tok, keep, q)
         dX, dA, dB = O.multi_lora_backward_vectorised(h["X"], h["W"], h["dY"], slots, tok, keep, q)
-        assert rel_err(lin.Y, Y) <= TOL_BF16
+        assert rel_err(lin.Y, Y) <= tol
         Hs = H.copy()
         for t in range(T):
             if tok[t] >= 0:
                 Hs[t] *= scales[tok[t]] * q
-        assert rel_err(lin.H, Hs) <= TOL_BF16
-        assert rel_err(lin.dX, dX) <= TOL_BF16
+        assert rel_err(lin.H, Hs) <= tol
+        assert rel_err(lin.dX, dX) <= tol
         for k in range(len(slots)):
             if np.any(tok == k):
-                assert rel_err(lin.gA[k], dA[k]) <= TOL_BF16, ("dA", k)
-                assert rel_err(lin.gB[k], dB[k]) <= TOL_BF16, ("dB", k)
+                assert rel_err(lin.gA[k], dA[k]) <= tol, ("dA", k)
+                assert rel_err(lin.gB[k], dB[k]) <= tol, ("dB", k)
             else:
                 assert float(lin.gA[k].abs().max()) == 0.0
         grads[lin.proj_id] = (dA, dB)
@@ -386,15 +389,23 @@ def test_multi_lora_parity(L, T, proj_idx, p):
         prep = O.grad_prepare([g.astype(np.float32) for g in glist], 1.0 / r.slot_gbs[k], cfg.max_norm)
         hp = O.AdamHP(lr=cfg.lr, beta1=cfg.beta1, beta2=cfg.beta2, eps=cfg.eps, wd=cfg.wd,
                       plus_ratio=cfg.plus_ratio, step=r.slot_step[k])
+        sel = np.nonzero(tok == k)[0]
         for lin in step.linears:
-            A0, B0 = host[lin.proj_id]["slots"][k]
+            h = host[lin.proj_id]
+            A0, B0 = h["slots"][k]
             z = np.zeros
-            A1, _, _ = O.adamw_update(A0, grads[lin.proj_id][0][k].astype(np.float32),
-                                      z(A0.shape), z(A0.shape), O.KIND_A, prep.scale, hp)
-            B1, _, _ = O.adamw_update(B0, grads[lin.proj_id][1][k].astype(np.float32),
-                                      z(B0.shape), z(B0.shape), O.KIND_B, prep.scale, hp)
-            assert rel_err(lin.A[k], A1) <= TOL_BF16_STEP
-            assert rel_err(lin.B[k], B1) <= TOL_BF16_STEP
+            keep = kept[lin.proj_id]
+            # the Adam-conditioning band near g_hat ~ 0, from the slot's fp32 gradient bounds
+            ch = dict(X=h["X"][torch.from_numpy(sel)], dY=h["dY"][torch.from_numpy(sel)])
+            bA, bB = grad_bounds(ch, A0, B0, scales[k], None if keep is None else keep[sel], q)
+            nA, _ = check_post_step(lin.A[k], A0, z(A0.shape), z(A0.shape),
+                                    grads[lin.proj_id][0][k].astype(np.float32), bA, O.KIND_A,
+                                    prep.scale, hp, tol_step)
+            nB, _ = check_post_step(lin.B[k], B0, z(B0.shape), z(B0.shape),
+                                    grads[lin.proj_id][1][k].astype(np.float32), bB, O.KIND_B,
+                                    prep.scale, hp, tol_step)
+            if dtype != "f32":
+                assert nA + nB == 0
     not_ready = [k for k in range(len(r.slot_rank)) if k not in ready]
     for k in not_ready:
         o, n = step.slot_off[k], step.slot_na[k] + step.slot_nb[k]
