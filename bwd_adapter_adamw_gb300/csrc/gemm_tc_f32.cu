@@ -3,23 +3,30 @@
 //   out[t, n] = ( sum_k A[t, k] B[n, k] + [mask(t, n)] * sum_j P[t, j] Q_slot[n, j] ) * colscale[n]
 //
 // with every fp32 operand x split into x_hi = tf32(x) (round to nearest) and x_lo = x - x_hi, and
-// each product formed as A_hi B_hi + A_hi B_lo + A_lo B_hi with tcgen05.mma kind::tf32 into fp32
-// TMEM accumulators. The dropped A_lo B_lo term and the tf32 reading of x_lo are both O(2^-22)
-// relative, so the result stays at fp32-level accuracy. (Same roles as the bf16 kernel: frozen
-// forward X W^T + Hs B^T, frozen dX dY' W + (Gs A) * M; "8. LoRA Fundamentals", How it works;
-// "Backward Bug Hunts and Vulkan Tiled GEMM", Bug #1.)
+// each product formed as A_hi B_hi + A_hi B_lo + A_lo B_hi with tcgen05.mma kind::tf32. The
+// dropped A_lo B_lo term and the tf32 reading of x_lo are both O(2^-22) relative, so the result
+// stays at fp32-level accuracy. (Same roles as the bf16 kernel: frozen forward X W^T + Hs B^T,
+// frozen dX dY' W + (Gs A) * M; "8. LoRA Fundamentals", How it works; "Backward Bug Hunts and
+// Vulkan Tiled GEMM", Bug #1.)
 //
 // The frozen operands arrive already split in HBM: B (W or W^T) by the weight preparation, once,
 // and A (X or dY') by the streaming shrink / G kernel, which reads A anyway. So the main K-loop
 // is a plain TMA -> MMA pipeline of four tiles per stage (A_hi, A_lo, B_hi, B_lo). Only the
 // short LoRA K-blocks (P = Hs or Gs, Q = B or A^T, at most two 32-wide blocks) land raw and are
-// split in shared memory by four converter warps.
+// split in shared memory by two converter warps.
 //
-// The tensor core's fp32 accumulation loses a little at every MMA, so the K-blocks are spread
-// round-robin over up to four TMEM accumulators (three when the masked LoRA term needs its own)
-// and summed in the epilogue with ordinary round-to-nearest fp32 adds.
+// Per K-step two MMAs: A_hi x [B_hi; B_lo] as one N = 256 instruction (the stage holds B_hi and
+// B_lo back to back), whose first 128 columns take A_hi B_hi and last 128 A_hi B_lo, then
+// A_lo x B_hi (N = 128) into the first 128 columns. N = 256 MMAs run about 1.3x faster per flop
+// than N = 128 ones.
 //
-// CTA (320 threads): warp 0 TMA, warp 1 TMEM + MMA issue, warps 2..5 epilogue, warps 6..9 LoRA
+// The tensor core's fp32 accumulation loses a little at every MMA, so no accumulation chain is
+// allowed to grow with K: two 256-column TMEM regions take turns, each holding the partial sum of
+// 8 K-blocks (a period), and while one fills, the epilogue warps drain the other into fp32
+// registers with ordinary round-to-nearest adds. The LoRA K-blocks form a period of their own,
+// masked element-wise when the LoRA term is dropout-masked.
+//
+// CTA (384 threads): warp 0 TMA, warp 1 TMEM + MMA issue, warps 2..9 epilogue, warps 10..11 LoRA
 // split. Tile 128 x 128; K-block 32 fp32 = one 128-byte swizzled row; three stages of four tiles.
 // (Seven stages of 16-wide K-blocks in the 64-byte swizzle measured slower: the TMA engine moves
 // 64-byte rows at a lower byte rate than 128-byte rows.)
@@ -39,8 +46,11 @@ constexpr int kBK = 32;                        // fp32 K per K-block: one 128-by
 constexpr int kStages = 3;
 constexpr int kTile = 128 * kBK * 4;           // 128 rows x 128 bytes
 constexpr int kStageBytes = 4 * kTile;         // A, A_lo, B, B_lo
-constexpr int kThreads = 320;
-constexpr int kConvThreads = 128;
+constexpr int kEpiWarps = 8;     // two per TMEM lane quarter, 64 columns each
+constexpr int kEpiThreads = 32 * kEpiWarps;
+constexpr int kConvThreads = 64;
+// TMA, MMA, epilogue, LoRA split: 12 warps, 3 per SM sub-partition, so up to 168 registers each
+constexpr int kThreads = 64 + kEpiThreads + kConvThreads;
 constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 1024;
 constexpr int kMaxLoraKb = (LORA_MAX_RANK + kBK - 1) / kBK;   // LoRA K-blocks per tile
 static_assert(kSmemBytes <= 232448, "dynamic shared memory per CTA");
@@ -48,7 +58,9 @@ static_assert(kSmemBytes <= 232448, "dynamic shared memory per CTA");
 __device__ __forceinline__ uint64_t kdesc(uint32_t saddr) {
   return kBK == 32 ? smem_desc_sw128(saddr) : smem_desc_sw64(saddr);
 }
-constexpr uint32_t kIdesc = idesc(kFmtTF32, kBM, kBN);
+constexpr uint32_t kIdesc = idesc(kFmtTF32, kBM, kBN);            // lo x B_hi into the big half
+constexpr uint32_t kIdesc2 = idesc(kFmtTF32, kBM, 2 * kBN);       // hi x [B_hi; B_lo]
+constexpr int kPeriod = 8;   // K-blocks accumulated in one TMEM region before it is drained
 
 struct F32Params {
   CUtensorMap tah, tal;               // A hi / lo [T, K] fp32, box {32, 128}
@@ -93,10 +105,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm_f32(const __grid_consta
   const int nk_lora = (p.has_lora && slot >= 0) ? (p.q_rank[slot] + kBK - 1) / kBK : 0;
   const int nk = p.nk_main + nk_lora;
   const bool sep = p.lora_separate && nk_lora > 0;
-  const uint32_t ncols = 512u;
-  const int nacc = p.lora_separate ? 3 : 4;                  // main-product accumulators
-  const int nused = p.nk_main < nacc ? p.nk_main : nacc;     // accumulators actually written
-  const uint32_t lora_col = 384u;                            // separate LoRA accumulator
+  const uint32_t ncols = 512u;   // two regions of 256 columns: [hi x B_hi (+ lo x B_hi) | hi x B_lo]
+  // accumulation periods: kPeriod main K-blocks each, then the LoRA K-blocks as a period of their
+  // own (masked element-wise in the epilogue when the LoRA term is dropout-masked)
+  const int n_main_periods = (p.nk_main + kPeriod - 1) / kPeriod;
+  const int n_periods = n_main_periods + (nk_lora > 0 ? 1 : 0);
 
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   // full_bar / empty_bar: the stage ring of the main K-blocks. The LoRA K-blocks use the same
@@ -106,8 +119,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm_f32(const __grid_consta
   uint64_t* empty_bar = full_bar + kStages;
   uint64_t* lora_full = empty_bar + kStages;
   uint64_t* lora_conv = lora_full + kMaxLoraKb;
-  uint64_t* acc_bar = lora_conv + kMaxLoraKb;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_bar + 1);
+  uint64_t* acc_full = lora_conv + kMaxLoraKb;   // [2]: a region's period is complete
+  uint64_t* acc_empty = acc_full + 2;           // [2]: the epilogue has drained the region
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -119,7 +133,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm_f32(const __grid_consta
       mbar_init(&lora_full[j], 1);
       mbar_init(&lora_conv[j], kConvThreads);
     }
-    mbar_init(acc_bar, 1);
+    for (int r = 0; r < 2; ++r) {
+      mbar_init(&acc_full[r], 1);
+      mbar_init(&acc_empty[r], kEpiThreads);
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
@@ -161,32 +178,43 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm_f32(const __grid_consta
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      for (int kb = 0; kb < nk; ++kb) {
+      // Per K-step: hi x [B_hi; B_lo] as one N = 256 MMA (big half: hi x B_hi, small half:
+      // hi x B_lo), then lo x B_hi into the big half. Regions alternate per period; a region is
+      // reused only after the epilogue has drained it.
+      int per = -1;
+      uint32_t d = tmem;
+      bool ok = true;
+      for (int kb = 0; kb < nk && ok; ++kb) {
         const int s = kb % kStages;
         const bool lora = kb >= p.nk_main;
+        const bool start = lora ? kb == p.nk_main : (kb % kPeriod) == 0;
+        if (start) {
+          if (per >= 0) umma_commit(&acc_full[per & 1]);
+          ++per;
+          const int use = per >> 1;
+          if (use >= 1 && !mbar_wait(&acc_empty[per & 1], (uint32_t)(use - 1) & 1u, 2u, p.err)) break;
+          fence_after();
+          d = tmem + 256u * (uint32_t)(per & 1);
+        }
         // main K-blocks are consumed as landed; LoRA K-blocks once the converter has split them
-        const bool ok = lora ? mbar_wait(&lora_conv[kb - p.nk_main], 0u, 2u, p.err)
-                             : mbar_wait(&full_bar[s], (uint32_t)(kb / kStages) & 1u, 2u, p.err);
+        ok = lora ? mbar_wait(&lora_conv[kb - p.nk_main], 0u, 2u, p.err)
+                  : mbar_wait(&full_bar[s], (uint32_t)(kb / kStages) & 1u, 2u, p.err);
         if (!ok) break;
         fence_after();
         const uint32_t sa = smem_u32(base + s * kStageBytes);
-        const uint64_t ah = kdesc(sa), al = kdesc(sa + kTile);
-        const uint64_t bh = kdesc(sa + 2 * kTile), bl = kdesc(sa + 3 * kTile);
-        const uint32_t d = lora ? (sep ? tmem + lora_col : tmem) : tmem + 128u * (uint32_t)(kb % nacc);
-        const bool first = lora ? (sep && kb == p.nk_main) : (kb < nacc);
+        const uint64_t ah = kdesc(sa), al = kdesc(sa + kTile), bh = kdesc(sa + 2 * kTile);
 #pragma unroll
         for (int k = 0; k < kBK / 8; ++k) {
-          umma_tf32(d, al + 2 * k, bh + 2 * k, kIdesc, (first && k == 0) ? 0u : 1u);
-          umma_tf32(d, ah + 2 * k, bl + 2 * k, kIdesc, 1u);
-          umma_tf32(d, ah + 2 * k, bh + 2 * k, kIdesc, 1u);
+          umma_tf32(d, ah + 2 * k, bh + 2 * k, kIdesc2, (start && k == 0) ? 0u : 1u);
+          umma_tf32(d, al + 2 * k, bh + 2 * k, kIdesc, 1u);
         }
         umma_commit(&empty_bar[s]);
       }
-      umma_commit(acc_bar);
+      if (per >= 0) umma_commit(&acc_full[per & 1]);
     }
-  } else if (warp >= 6) {
+  } else if (warp >= 2 + kEpiWarps) {
     // LoRA K-blocks: split the landed P and Q tiles (x -> tf32(x) in place, x - tf32(x) one tile on)
-    const int ct = threadIdx.x - 192;
+    const int ct = threadIdx.x - (64 + kEpiThreads);
     for (int kb = p.nk_main; kb < nk; ++kb) {
       const int s = kb % kStages;
       if (!mbar_wait(&lora_full[kb - p.nk_main], 0u, 8u, p.err)) break;
@@ -198,33 +226,57 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm_f32(const __grid_consta
       asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&lora_conv[kb - p.nk_main])) : "memory");
     }
   } else {
-    // epilogue warps 2..5: TMEM lanes 32 * (warp % 4)
+    // epilogue warps 2..9: TMEM lanes 32 * (warp % 4), columns [64 half, 64 half + 64); each
+    // thread keeps its row's 64 sums in registers and adds every drained period into them
+    // (round-to-nearest fp32 adds)
+    constexpr int kCols = kBN / 2;
     const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int row = q * 32 + lane;
     const int64_t m = (int64_t)m0 + row;
     const bool row_ok = m < it.t1;
-    const bool ready = __all_sync(0xffffffffu, mbar_wait(acc_bar, 0u, 4u, p.err));
-    if (ready) {
+    const int c0 = half * kCols;
+    const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0;
+    float run[kCols];
+#pragma unroll
+    for (int j = 0; j < kCols; ++j) run[j] = 0.f;
+    bool ready = true;
+    for (int per = 0; per < n_periods && ready; ++per) {
+      const int r = per & 1;
+      ready = __all_sync(0xffffffffu, mbar_wait(&acc_full[r], (uint32_t)(per >> 1) & 1u, 4u, p.err));
+      if (!ready) break;
       fence_after();
-      for (int c = 0; c < kBN / 32; ++c) {
-        float v[32];
-        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * 32), v);
-        for (int a = 1; a < nused; ++a) {
-          float u[32];
-          tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + 128u * (uint32_t)a + (uint32_t)(c * 32), u);
+      const bool masked = sep && per == n_periods - 1;
+      const uint32_t reg = lane_base + 256u * (uint32_t)r;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] += u[j];
-        }
-        if (sep) {
-          float w[32];
-          tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + lora_col + (uint32_t)(c * 32), w);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int64_t n = (int64_t)n0 + c * 32 + j;
-            if (row_ok && n < p.n_out && drop_keep(p.drop, m, n)) v[j] += w[j];
+      for (int h = 0; h < kCols / 16; ++h) {
+        uint32_t big[16], small[16];
+        tmem_ld16_nw(reg + (uint32_t)(h * 16), big);
+        tmem_ld16_nw(reg + 128u + (uint32_t)(h * 16), small);
+        tmem_wait_ld();
+        if (masked) {
+          // dropout-masked LoRA term: keep bits first (a rolled loop: the hash is register-heavy)
+          uint32_t keep = 0u;
+#pragma unroll 1
+          for (int j = 0; j < 16; ++j) {
+            const int64_t n = (int64_t)n0 + c0 + h * 16 + j;
+            if (row_ok && n < p.n_out && drop_keep(p.drop, m, n)) keep |= 1u << j;
           }
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (!((keep >> j) & 1u)) big[j] = small[j] = 0u;
         }
-        const int64_t nb = (int64_t)n0 + c * 32;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) run[h * 16 + j] += __uint_as_float(big[j]) + __uint_as_float(small[j]);
+      }
+      fence_before();
+      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&acc_empty[r])) : "memory");
+    }
+    if (ready) {
+#pragma unroll
+      for (int c = 0; c < kCols / 32; ++c) {
+        const int64_t nb = (int64_t)n0 + c0 + c * 32;
+        float* v = run + c * 32;
         if (p.n_colscale) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] *= (nb + j < p.n_out) ? __ldg(p.n_colscale + nb + j) : 0.f;
