@@ -873,7 +873,7 @@ int lora_grad_prepare_noalloc(const float* grads, int32_t n_groups, const lora_g
   if (!al16(grads) || (reinterpret_cast<uintptr_t>(d_scale_norm) & 7u) ||
       (reinterpret_cast<uintptr_t>(d_status) & 3u))
     return LORA_ERR_ALIGN;
-  if (prepare_blocks(g) > kNoallocMaxPartials) return LORA_ERR_UNSUPPORTED;
+  if (prepare_blocks(g, kPrepElemsPerBlock) > kNoallocMaxPartials) return LORA_ERR_UNSUPPORTED;
   clear_stale();
   return cuda_status(launch_grad_prepare_noalloc(grads, g, d_scale_norm, d_status,
                                                  (cudaStream_t)stream));

@@ -61,17 +61,36 @@ __device__ __forceinline__ uint64_t kdesc(uint32_t saddr) {
 constexpr uint32_t kIdesc = idesc(kFmtTF32, kBM, kBN);            // lo x B_hi into the big half
 constexpr uint32_t kIdesc2 = idesc(kFmtTF32, kBM, 2 * kBN);       // hi x [B_hi; B_lo]
 constexpr int kPeriod = 8;   // K-blocks accumulated in one TMEM region before it is drained
+constexpr int kPartLd = kBN + 4;   // row stride (floats) of a split-K partial tile in shared memory
+constexpr int kMaxSplits = 8;      // portable cluster size
+static_assert(kBM * kPartLd * 4 <= kStages * kStageBytes, "partial tile fits the stage buffers");
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// float4 at `local` (this CTA's shared-memory layout) in cluster CTA `rank`
+__device__ __forceinline__ float4 ld_peer4(const float* local, uint32_t rank) {
+  uint32_t a = (uint32_t)__cvta_generic_to_shared(local), remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(a), "r"(rank));
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(remote) : "memory");
+  return v;
+}
 
 struct F32Params {
   CUtensorMap tah, tal;               // A hi / lo [T, K] fp32, box {32, 128}
   CUtensorMap tbh, tbl;               // B hi / lo [N, K] fp32, box {32, 128}
   CUtensorMap tp;                     // P [T, ldp] fp32, box {32, 128}
   CUtensorMap tq[LORA_MAX_SLOTS];     // Q_slot [N, r] fp32, box {32, 128}
+  CUtensorMap to;                     // out [T, ldo] fp32, box {32, 32} (the epilogue's stores)
   const TokenItem* items;             // null: uniform 128-token tiles, slot 0
   const int32_t* n_items;
   int64_t T;
   uint32_t* err;
   int32_t nk_main;
+  int32_t splits;                     // CTAs of one cluster splitting the main K-blocks (1..8)
+  int32_t kb_per_split;
   int32_t has_lora;
   int32_t lora_separate;
   int32_t q_rank[LORA_MAX_SLOTS];
@@ -102,13 +121,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm_f32(const __grid_consta
   const int slot = it.slot;
   const int32_t m0 = it.t0;
   const int32_t n0 = blockIdx.x * kBN;
-  const int nk_lora = (p.has_lora && slot >= 0) ? (p.q_rank[slot] + kBK - 1) / kBK : 0;
-  const int nk = p.nk_main + nk_lora;
+  // this CTA's main K-blocks (split z of the cluster) and, for split 0, the LoRA K-blocks; local
+  // index i runs over [0, nml) main blocks then [nml, nk) LoRA blocks
+  const int z = blockIdx.z;
+  const int kb_lo = z * p.kb_per_split;
+  const int nml = max(0, min(p.nk_main, kb_lo + p.kb_per_split) - kb_lo);
+  const int nk_lora = (p.has_lora && slot >= 0 && z == 0) ? (p.q_rank[slot] + kBK - 1) / kBK : 0;
+  const int nk = nml + nk_lora;
   const bool sep = p.lora_separate && nk_lora > 0;
   const uint32_t ncols = 512u;   // two regions of 256 columns: [hi x B_hi (+ lo x B_hi) | hi x B_lo]
   // accumulation periods: kPeriod main K-blocks each, then the LoRA K-blocks as a period of their
   // own (masked element-wise in the epilogue when the LoRA term is dropout-masked)
-  const int n_main_periods = (p.nk_main + kPeriod - 1) / kPeriod;
+  const int n_main_periods = (nml + kPeriod - 1) / kPeriod;
   const int n_periods = n_main_periods + (nk_lora > 0 ? 1 : 0);
 
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -154,14 +178,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm_f32(const __grid_consta
         const uint32_t ph = (uint32_t)(kb / kStages) & 1u;
         if (kb >= kStages && !mbar_wait(&empty_bar[s], ph ^ 1u, 1u, p.err)) break;
         uint8_t* st = base + s * kStageBytes;
-        if (kb < p.nk_main) {
+        if (kb < nml) {
+          const int x = (kb_lo + kb) * kBK;
           mbar_expect_tx(&full_bar[s], 4 * kTile);
-          tma_load_2d(st, &p.tah, &full_bar[s], kb * kBK, m0);
-          tma_load_2d(st + kTile, &p.tal, &full_bar[s], kb * kBK, m0);
-          tma_load_2d(st + 2 * kTile, &p.tbh, &full_bar[s], kb * kBK, n0);
-          tma_load_2d(st + 3 * kTile, &p.tbl, &full_bar[s], kb * kBK, n0);
+          tma_load_2d(st, &p.tah, &full_bar[s], x, m0);
+          tma_load_2d(st + kTile, &p.tal, &full_bar[s], x, m0);
+          tma_load_2d(st + 2 * kTile, &p.tbh, &full_bar[s], x, n0);
+          tma_load_2d(st + 3 * kTile, &p.tbl, &full_bar[s], x, n0);
         } else {
-          const int j = kb - p.nk_main;
+          const int j = kb - nml;
           mbar_expect_tx(&lora_full[j], 2 * kTile);
           tma_load_2d(st, &p.tp, &lora_full[j], j * kBK, m0);
           tma_load_2d(st + 2 * kTile, &p.tq[slot], &lora_full[j], j * kBK, n0);
@@ -170,9 +195,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm_f32(const __grid_consta
       }
       // copies still in flight complete before the CTA can exit
       for (int kb = (issued > kStages ? issued - kStages : 0); kb < issued; ++kb) {
-        const bool ok = kb < p.nk_main
+        const bool ok = kb < nml
                             ? mbar_wait(&full_bar[kb % kStages], (uint32_t)(kb / kStages) & 1u, 1u, p.err)
-                            : mbar_wait(&lora_full[kb - p.nk_main], 0u, 1u, p.err);
+                            : mbar_wait(&lora_full[kb - nml], 0u, 1u, p.err);
         if (!ok) break;
       }
     }
@@ -186,8 +211,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm_f32(const __grid_consta
       bool ok = true;
       for (int kb = 0; kb < nk && ok; ++kb) {
         const int s = kb % kStages;
-        const bool lora = kb >= p.nk_main;
-        const bool start = lora ? kb == p.nk_main : (kb % kPeriod) == 0;
+        const bool lora = kb >= nml;
+        const bool start = lora ? kb == nml : (kb % kPeriod) == 0;
         if (start) {
           if (per >= 0) umma_commit(&acc_full[per & 1]);
           ++per;
@@ -197,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm_f32(const __grid_consta
           d = tmem + 256u * (uint32_t)(per & 1);
         }
         // main K-blocks are consumed as landed; LoRA K-blocks once the converter has split them
-        ok = lora ? mbar_wait(&lora_conv[kb - p.nk_main], 0u, 2u, p.err)
+        ok = lora ? mbar_wait(&lora_conv[kb - nml], 0u, 2u, p.err)
                   : mbar_wait(&full_bar[s], (uint32_t)(kb / kStages) & 1u, 2u, p.err);
         if (!ok) break;
         fence_after();
@@ -215,15 +240,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm_f32(const __grid_consta
   } else if (warp >= 2 + kEpiWarps) {
     // LoRA K-blocks: split the landed P and Q tiles (x -> tf32(x) in place, x - tf32(x) one tile on)
     const int ct = threadIdx.x - (64 + kEpiThreads);
-    for (int kb = p.nk_main; kb < nk; ++kb) {
+    for (int kb = nml; kb < nk; ++kb) {
       const int s = kb % kStages;
-      if (!mbar_wait(&lora_full[kb - p.nk_main], 0u, 8u, p.err)) break;
+      if (!mbar_wait(&lora_full[kb - nml], 0u, 8u, p.err)) break;
       uint8_t* st = base + s * kStageBytes;
       split_tile(st, ct);
       split_tile(st + 2 * kTile, ct);
       // generic-proxy writes must be visible to the tensor core's async proxy
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&lora_conv[kb - p.nk_main])) : "memory");
+      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&lora_conv[kb - nml])) : "memory");
     }
   } else {
     // epilogue warps 2..9: TMEM lanes 32 * (warp % 4), columns [64 half, 64 half + 64); each
@@ -272,7 +297,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm_f32(const __grid_consta
       fence_before();
       asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&acc_empty[r])) : "memory");
     }
-    if (ready) {
+    if (ready && p.splits > 1) {
+      // split K: this CTA's partial tile goes to shared memory (row stride kPartLd floats, so
+      // that the float4 row writes of a quarter warp hit distinct banks); the cluster sums the
+      // splits below
+      float* part = reinterpret_cast<float*>(base) + (size_t)row * kPartLd + c0;
+#pragma unroll
+      for (int g = 0; g < kCols / 4; ++g)
+        *reinterpret_cast<float4*>(part + 4 * g) =
+            make_float4(run[4 * g], run[4 * g + 1], run[4 * g + 2], run[4 * g + 3]);
+    } else if (ready) {
+      // Whole tiles (and the last tile of the call, which the tensor bounds clip) leave through
+      // bulk tensor stores of 32 x 32 boxes staged in the now idle stage buffers, 128-byte
+      // swizzled so that the row-per-thread writes hit distinct banks. A partial item of a
+      // multi-adapter call stores row by row: the rows past it belong to other CTAs.
+      const bool tile_store = (it.t1 - it.t0 == kBM) || ((int64_t)it.t1 == p.T);
+      uint8_t* box0 = base + (size_t)(warp - 2) * (kCols / 32) * 4096;
 #pragma unroll
       for (int c = 0; c < kCols / 32; ++c) {
         const int64_t nb = (int64_t)n0 + c0 + c * 32;
@@ -281,7 +321,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm_f32(const __grid_consta
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] *= (nb + j < p.n_out) ? __ldg(p.n_colscale + nb + j) : 0.f;
         }
-        if (row_ok) {
+        if (tile_store) {
+          uint8_t* box = box0 + c * 4096 + lane * 128;
+#pragma unroll
+          for (int g = 0; g < 8; ++g)
+            *reinterpret_cast<float4*>(box + ((g ^ (lane & 7)) << 4)) =
+                make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+        } else if (row_ok) {
 #pragma unroll
           for (int g = 0; g < 8; ++g)
             if (nb + 4 * g + 4 <= p.n_out)
@@ -289,10 +335,47 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm_f32(const __grid_consta
                   make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
         }
       }
+      if (tile_store) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+#pragma unroll
+          for (int c = 0; c < kCols / 32; ++c)
+            tma_store_2d(&p.to, box0 + c * 4096, n0 + c0 + c * 32, m0 + q * 32);
+          tma_store_commit_and_wait_read();
+        }
+        __syncwarp();
+      }
     }
     fence_before();
   }
   __syncthreads();
+  if (p.splits > 1) {
+    // CTA z of the cluster adds rows [z R, z R + R) of the tile over all splits, in split order
+    // (reruns are bitwise equal), from the peers' shared memory, and stores them coalesced
+    cluster_sync();
+    const int rows = kBM / p.splits;
+    const float* part = reinterpret_cast<const float*>(base);
+    for (int e = threadIdx.x; e < rows * (kBN / 4); e += kThreads) {
+      const int rr = z * rows + e / (kBN / 4);
+      const int cc = 4 * (e % (kBN / 4));
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int zz = 0; zz < p.splits; ++zz) {
+        const float4 v = ld_peer4(part + (size_t)rr * kPartLd + cc, (uint32_t)zz);
+        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+      }
+      const int64_t m = (int64_t)m0 + rr;
+      const int64_t n = (int64_t)n0 + cc;
+      if (m < it.t1 && n < p.n_out) {
+        if (p.n_colscale) {
+          acc.x *= __ldg(p.n_colscale + n); acc.y *= __ldg(p.n_colscale + n + 1);
+          acc.z *= __ldg(p.n_colscale + n + 2); acc.w *= __ldg(p.n_colscale + n + 3);
+        }
+        *reinterpret_cast<float4*>(p.out + m * p.ldo + n) = acc;
+      }
+    }
+    cluster_sync();   // peers' shared memory stays alive until every CTA has read it
+  }
   if (warp == 1) {
     fence_after();
     tmem_dealloc(tmem, ncols);
@@ -326,9 +409,20 @@ cudaError_t launch_tc_gemm_f32(const TcGemmArgs& a, cudaStream_t st, int prof_ki
   prm.items = a.items;
   prm.n_items = a.n_items;
   prm.T = a.T;
+  if (!tc::make_map_2d(&prm.to, a.out, F32, 4, a.n_rows, a.T, a.ldo, 32, 32))
+    return cudaErrorInvalidValue;
   prm.err = tc::error_word();
   if (!prm.err) return cudaErrorInvalidDevice;
   prm.nk_main = (int32_t)((a.K + kBK - 1) / kBK);
+  // Split the K-blocks over a cluster when the tile grid alone would leave most SMs idle (few
+  // output tiles, long K): up to 8 splits, at least 4 K-blocks each, and at most ~80 CTAs in
+  // all. (Measured at T 1024, K 2048, N 256: 35 us unsplit, 14 us as 4 splits over 64 CTAs,
+  // 21 us as 8 splits over 128 CTAs, whose 8-SM clusters no longer fit the GPCs in one wave.)
+  const int64_t tiles = ((a.n_rows + kBN - 1) / kBN) * (int64_t)(a.max_items > 0 ? a.max_items : 1);
+  int splits = 1;
+  while (splits < kMaxSplits && tiles * splits * 2 <= 80 && prm.nk_main >= 4 * splits * 2) splits *= 2;
+  prm.kb_per_split = (prm.nk_main + splits - 1) / splits;
+  prm.splits = (prm.nk_main + prm.kb_per_split - 1) / prm.kb_per_split;
   prm.lora_separate = a.lora_separate;
   prm.n_colscale = a.n_colscale;
   prm.out = reinterpret_cast<float*>(a.out);
@@ -343,11 +437,28 @@ cudaError_t launch_tc_gemm_f32(const TcGemmArgs& a, cudaStream_t st, int prof_ki
     attr = true;
   }
   if (a.max_items <= 0) return cudaSuccess;
-  dim3 grid((unsigned)((a.n_rows + kBN - 1) / kBN), (unsigned)a.max_items);
+  dim3 grid((unsigned)((a.n_rows + kBN - 1) / kBN), (unsigned)a.max_items, (unsigned)prm.splits);
   prof_begin(prof_kind, st);
-  k_tc_gemm_f32<<<grid, kThreads, kSmemBytes, st>>>(prm);
+  cudaError_t e = cudaSuccess;
+  if (prm.splits > 1) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = (unsigned)prm.splits;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, k_tc_gemm_f32, prm);
+  } else {
+    k_tc_gemm_f32<<<grid, kThreads, kSmemBytes, st>>>(prm);
+  }
   prof_end(prof_kind, st);
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace lora

@@ -214,14 +214,17 @@ struct GroupTab {
   float bc2[LORA_MAX_GROUPS];   // 1 - beta2^k
 };
 constexpr int kPrepThreads = 256;
-constexpr int kPrepElemsPerBlock = kPrepThreads * 64;
+constexpr int kPrepElemsWs = kPrepThreads * 16;         // per CTA, workspace form (more CTAs)
+constexpr int kPrepElemsPerBlock = kPrepThreads * 64;   // per CTA, allocation-free form
 constexpr int kAdamThreads = 256;
 constexpr int kAdamElemsPerBlock = kAdamThreads * 16;
 
 // workspace: [blocks] double partials, [blocks] int flags, 1 int counter
-int prepare_blocks(const GroupTab& g);  // CTAs (and double partials) of one prepare launch
+// CTAs (and double partials) of one prepare launch
+int prepare_blocks(const GroupTab& g, int64_t per_block = kPrepElemsWs);
 cudaError_t launch_grad_prepare(const float* grads, const GroupTab& g, double* d_scale_norm,
-                                int32_t* d_status, double* part, uint32_t* counter, cudaStream_t st);
+                                int32_t* d_status, double* part, uint32_t* counter, cudaStream_t st,
+                                int64_t per_block = kPrepElemsWs);
 struct AdamK {
   float b1, omb1, b2, omb2, eps, wd, rho;   // 1 - beta formed in double on the host
 };

@@ -60,13 +60,14 @@ __global__ void __launch_bounds__(kPrepThreads) k_grad_prepare(const float* __re
                                                                const GroupTab gt,
                                                                double* __restrict__ scale_norm,
                                                                int32_t* __restrict__ status,
-                                                               double* part, uint32_t* counter) {
+                                                               double* part, uint32_t* counter,
+                                                               int64_t per_block) {
   __shared__ double sh[kPrepThreads / 32];
   __shared__ bool am_last;
   const int b = blockIdx.x;
   const int g = find_group(gt, b);
-  const int64_t begin = (int64_t)(b - gt.block_begin[g]) * kPrepElemsPerBlock;
-  const int64_t n = min((int64_t)kPrepElemsPerBlock, gt.count[g] - begin);
+  const int64_t begin = (int64_t)(b - gt.block_begin[g]) * per_block;
+  const int64_t n = min(per_block, gt.count[g] - begin);
   const float* p = grads + gt.offset[g] + begin;
   float hi = 0.f, lo = 0.f;
   double big = 0.0;
@@ -188,15 +189,16 @@ int set_blocks(GroupTab& g, int64_t per_block) {
 
 }  // namespace
 
-int prepare_blocks(const GroupTab& g) {
+int prepare_blocks(const GroupTab& g, int64_t per_block) {
   GroupTab t = g;
-  return set_blocks(t, kPrepElemsPerBlock);
+  return set_blocks(t, per_block);
 }
 
 cudaError_t launch_grad_prepare(const float* grads, const GroupTab& g_in, double* d_scale_norm,
-                                int32_t* d_status, double* part, uint32_t* counter, cudaStream_t st) {
+                                int32_t* d_status, double* part, uint32_t* counter, cudaStream_t st,
+                                int64_t per_block) {
   GroupTab g = g_in;
-  int blocks = set_blocks(g, kPrepElemsPerBlock);
+  int blocks = set_blocks(g, per_block);
   cudaError_t e = cudaMemsetAsync(counter, 0, sizeof(uint32_t), st);
   if (e != cudaSuccess) return e;
   if (blocks == 0) {
@@ -206,7 +208,8 @@ cudaError_t launch_grad_prepare(const float* grads, const GroupTab& g_in, double
     for (int i = 0; i < g.n; ++i) g.block_begin[i] = 0;
   }
   prof_begin(LORA_PROF_PREPARE, st);
-  k_grad_prepare<<<blocks, kPrepThreads, 0, st>>>(grads, g, d_scale_norm, d_status, part, counter);
+  k_grad_prepare<<<blocks, kPrepThreads, 0, st>>>(grads, g, d_scale_norm, d_status, part, counter,
+                                                  per_block);
   prof_end(LORA_PROF_PREPARE, st);
   return cudaGetLastError();
 }
@@ -265,7 +268,8 @@ cudaError_t launch_grad_prepare_noalloc(const float* grads, const GroupTab& g,
   if (e != cudaSuccess) return e;
   double* part = reinterpret_cast<double*>(base);
   uint32_t* counter = reinterpret_cast<uint32_t*>(static_cast<char*>(base) + kNoallocCounterOffset);
-  return launch_grad_prepare(grads, g, d_scale_norm, d_status, part, counter, st);
+  return launch_grad_prepare(grads, g, d_scale_norm, d_status, part, counter, st,
+                             kPrepElemsPerBlock);
 }
 
 }  // namespace lora
