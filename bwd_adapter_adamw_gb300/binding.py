@@ -80,7 +80,8 @@ def _load() -> C.CDLL:
         "lora_workspace_size": (SZ, [DP, I64]),
         "lora_prepared_weight_size": (SZ, [DP]),
         "lora_prepare_weight": (C.c_int, [DP, P, P, P]),
-        "lora_dora_norm": (C.c_int, [DP, P, P, P, P, P]),
+        "lora_dora_norm_workspace_size": (SZ, [DP]),
+        "lora_dora_norm": (C.c_int, [DP, P, P, P, P, P, SZ, P]),
         "lora_forward": (C.c_int, [DP, CP, I64, P, P, P, P, P, P, P, P, P, P, SZ, P]),
         "lora_backward": (C.c_int, [DP, CP, I64, P, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P]),
         "lora_grad_prepare_workspace_size": (SZ, [I32, C.POINTER(lora_group)]),
@@ -110,7 +111,8 @@ def _load() -> C.CDLL:
 
 _lib = _load()
 EXPORTED = ("lora_status_string", "lora_scale", "lora_lr_at", "lora_workspace_size",
-            "lora_prepared_weight_size", "lora_prepare_weight", "lora_dora_norm", "lora_forward", "lora_backward",
+            "lora_prepared_weight_size", "lora_prepare_weight", "lora_dora_norm_workspace_size",
+            "lora_dora_norm", "lora_forward", "lora_backward",
             "lora_grad_prepare_workspace_size", "lora_grad_prepare", "lora_grad_prepare_noalloc",
             "lora_adamw_step",
             "multi_lora_workspace_size", "multi_lora_forward", "multi_lora_backward",
@@ -194,9 +196,15 @@ def lora_prepare_weight(d: lora_desc, W, W_prep, stream=None):
                   "lora_prepare_weight")
 
 
-def lora_dora_norm(d: lora_desc, W, A, B, norm_out, stream=None):
+def lora_dora_norm_workspace_size(d: lora_desc) -> int:
+    return _lib.lora_dora_norm_workspace_size(C.byref(d))
+
+
+def lora_dora_norm(d: lora_desc, W, A, B, norm_out, ws, ws_bytes: Optional[int] = None,
+                   stream=None):
+    nbytes = ws_bytes if ws_bytes is not None else ws.numel() * ws.element_size()
     return _check(_lib.lora_dora_norm(C.byref(d), _ptr(W), _ptr(A), _ptr(B), _ptr(norm_out),
-                                      _stream(stream)), "lora_dora_norm")
+                                      _ptr(ws), nbytes, _stream(stream)), "lora_dora_norm")
 
 
 def lora_forward(d: lora_desc, c: Optional[lora_ctx], T: int, X, W, W_prep, A, B, dora_m, dora_n,

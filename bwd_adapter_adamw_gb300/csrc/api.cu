@@ -623,6 +623,55 @@ int run_backward(const lora_desc* d, const DropParams& dp, int64_t T, const void
   return LORA_OK;
 }
 
+// DoRA row norm for bf16 W on tensor cores: H = W A^T by the shrink kernel over W's rows (the hi /
+// lo bf16 split of A), then ||W_o||^2 + 2 s H_o . B_o + s^2 B_o (A A^T) B_o^T per row.
+struct NormLayout {
+  uint16_t* Sa;        // [2 r, in] bf16 split of A
+  float* part;         // [splits][out][NP]
+  float* H;            // [out, r]
+  float* C;            // [r, r]
+  size_t bytes;
+};
+
+NormLayout dora_norm_carve(const lora_desc* d, void* ws) {
+  NormLayout L{};
+  Carve c(ws);
+  if (d->dtype == LORA_BF16) {
+    L.Sa = c.take<uint16_t>((size_t)2 * d->rank * d->in_dim);
+    L.part = c.take<float>((size_t)kMaxRowSplits * d->out_dim * np_for(d->rank));
+    L.H = c.take<float>((size_t)d->out_dim * d->rank);
+    L.C = c.take<float>((size_t)d->rank * d->rank);
+  }
+  L.bytes = c.off + kWsAlign;
+  return L;
+}
+
+cudaError_t run_dora_norm_tc(const lora_desc* d, const void* W, const float* A, const float* B,
+                             float* norm_out, void* ws, cudaStream_t st) {
+  NormLayout L = dora_norm_carve(d, ws);
+  SplitTab sp{};
+  sp.K = d->in_dim;
+  sp.src[0] = A;
+  sp.dst[0] = L.Sa;
+  sp.rank[0] = d->rank;
+  cudaError_t e = launch_split(sp, 1, st);
+  if (e != cudaSuccess) return e;
+  TcRowsArgs r{};
+  r.a = W; r.T = d->out_dim; r.K = d->in_dim; r.n_slots = 1;
+  r.s[0] = L.Sa; r.rank[0] = d->rank;
+  r.NP = np_for(d->rank);
+  r.splits = row_splits(d->out_dim, -1, d->in_dim);
+  r.part = L.part;
+  r.si.rank[0] = d->rank; r.si.alpha[0] = 1.f; r.si.region[0] = 0;
+  r.out = L.H; r.ldo = d->rank;
+  r.items = nullptr; r.n_items = nullptr;   // uniform 128-row tiles of W
+  r.max_items = (int)((d->out_dim + kGemmTileT - 1) / kGemmTileT);
+  e = launch_tc_rows(r, st, 0);
+  if (e != cudaSuccess) return e;
+  return launch_dora_gram_combine(W, L.H, A, B, d->scale, d->out_dim, d->in_dim, d->rank, L.C,
+                                  norm_out, st);
+}
+
 }  // namespace
 
 extern "C" {
@@ -692,15 +741,24 @@ int lora_prepare_weight(const lora_desc* d, const void* W, void* W_prep, void* s
                                            (cudaStream_t)stream));
 }
 
+size_t lora_dora_norm_workspace_size(const lora_desc* d) {
+  if (check_desc(d, 0, false) != LORA_OK) return 0;
+  return dora_norm_carve(d, nullptr).bytes;
+}
+
 int lora_dora_norm(const lora_desc* d, const void* W, const float* A, const float* B,
-                   float* norm_out, void* stream) {
+                   float* norm_out, void* ws, size_t ws_bytes, void* stream) {
   int rc = check_desc(d, 0, false);
   if (rc) return rc;
-  if (!W || !A || !B || !norm_out) return LORA_ERR_INVALID;
-  if (!al16(W) || !al16(A) || !al16(B) || !al16(norm_out)) return LORA_ERR_ALIGN;
+  if (!W || !A || !B || !norm_out || !ws) return LORA_ERR_INVALID;
+  if (!al16(W) || !al16(A) || !al16(B) || !al16(norm_out) || !al16(ws)) return LORA_ERR_ALIGN;
+  if (ws_bytes < dora_norm_carve(d, nullptr).bytes) return LORA_ERR_WORKSPACE;
   clear_stale();
-  return cuda_status(launch_dora_norm(d->dtype, W, A, B, d->scale, d->out_dim, d->in_dim, d->rank,
-                                      norm_out, (cudaStream_t)stream));
+  cudaStream_t st = (cudaStream_t)stream;
+  if (d->dtype == LORA_F32)
+    return cuda_status(launch_dora_norm(d->dtype, W, A, B, d->scale, d->out_dim, d->in_dim,
+                                        d->rank, norm_out, st));
+  return cuda_status(run_dora_norm_tc(d, W, A, B, norm_out, ws, st));
 }
 
 int lora_forward(const lora_desc* d, const lora_ctx* c, int64_t T, const void* X, const void* W,

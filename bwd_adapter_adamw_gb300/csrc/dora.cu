@@ -56,16 +56,159 @@ __global__ void __launch_bounds__(256) k_dora_norm(const T* __restrict__ W, cons
   }
 }
 
-// dm_o += (sum_t dY[t, o] * Y[t, o]) / m_o  (= sum_t dY * Z / n with Y = (m / n) Z).
-template <typename T>
-__global__ void k_dora_dm(const T* __restrict__ dY, const T* __restrict__ Y,
-                          const float* __restrict__ mag, int64_t Tn, int64_t out_dim,
-                          float* __restrict__ dm) {
-  const int64_t o = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+// ---------------------------------------------------------------------------------------------
+// Row norm from the expanded identity (bf16 W): with H = W A^T [out, r] (tensor cores, the
+// shrink kernel applied to W's rows) and the Gram matrix C = A A^T [r, r],
+//   ||W_o + s (B A)_o||^2 = ||W_o||^2 + 2 s sum_j H[o, j] B[o, j] + s^2 B_o C B_o^T.
+// ---------------------------------------------------------------------------------------------
+
+// C[j, k] for k in [8 blockIdx.y, 8 blockIdx.y + 8): 256 threads stride over the input columns.
+__global__ void __launch_bounds__(256) k_dora_gram(const float* __restrict__ A, int64_t in_dim,
+                                                   int32_t rank, float* __restrict__ C) {
+  __shared__ float red[8][8];
+  const int j = blockIdx.x, k0 = blockIdx.y * 8;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int64_t i = threadIdx.x; i < in_dim; i += 256) {
+    const float a = __ldg(A + (int64_t)j * in_dim + i);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+      if (k0 + kk < rank) acc[kk] = fmaf(a, __ldg(A + (int64_t)(k0 + kk) * in_dim + i), acc[kk]);
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    float v = acc[kk];
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    if (lane == 0) red[warp][kk] = v;
+  }
+  __syncthreads();
+  if (threadIdx.x < 8 && k0 + threadIdx.x < rank) {
+    float v = 0.f;
+    for (int w = 0; w < 8; ++w) v += red[w][threadIdx.x];
+    C[j * rank + k0 + threadIdx.x] = v;
+  }
+}
+
+// One warp per output row: ||W_o||^2 from 16-byte loads of the row, the H.B and B C B^T terms
+// with C in shared memory (lane j of the warp takes ranks j and j + 32).
+__global__ void __launch_bounds__(256) k_dora_combine(const __nv_bfloat16* __restrict__ W,
+                                                      const float* __restrict__ H,
+                                                      const float* __restrict__ B,
+                                                      const float* __restrict__ C, float s,
+                                                      int64_t out_dim, int64_t in_dim, int32_t rank,
+                                                      float* __restrict__ norm_out) {
+  __shared__ float sC[LORA_MAX_RANK * LORA_MAX_RANK];
+  for (int e = threadIdx.x; e < rank * rank; e += 256) sC[e] = C[e];
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t o = (int64_t)blockIdx.x * 8 + warp;
   if (o >= out_dim) return;
-  float acc = 0.f;
-  for (int64_t t = 0; t < Tn; ++t) acc = fmaf(to_f(dY[t * out_dim + o]), to_f(Y[t * out_dim + o]), acc);
-  dm[o] += acc / mag[o];
+  const __nv_bfloat16* w = W + o * in_dim;
+  float wsq = 0.f;
+  for (int64_t i = (int64_t)lane * 8; i < in_dim; i += 256) {
+    float x[8];
+    load16(w + i, x);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) wsq = fmaf(x[e], x[e], wsq);
+  }
+  float hb = 0.f, bcb = 0.f;
+  for (int j = lane; j < rank; j += 32) {
+    const float bj = B[o * rank + j];
+    hb = fmaf(H[o * rank + j], bj, hb);
+    float cb = 0.f;
+    for (int k = 0; k < rank; ++k) cb = fmaf(sC[j * rank + k], B[o * rank + k], cb);
+    bcb = fmaf(bj, cb, bcb);
+  }
+  for (int off = 16; off > 0; off >>= 1) {
+    wsq += __shfl_xor_sync(0xffffffffu, wsq, off);
+    hb += __shfl_xor_sync(0xffffffffu, hb, off);
+    bcb += __shfl_xor_sync(0xffffffffu, bcb, off);
+  }
+  if (lane == 0) {
+    const double n2 = (double)wsq + 2.0 * (double)s * hb + (double)s * (double)s * bcb;
+    norm_out[o] = (float)sqrt(n2 > 0.0 ? n2 : 0.0);
+  }
+}
+
+__device__ __forceinline__ void dm_cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ float dm_ld_peer(const float* local, uint32_t rank) {
+  uint32_t a = (uint32_t)__cvta_generic_to_shared(local), remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(a), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  return v;
+}
+
+constexpr int kDmGroups = 8;   // token groups = CTAs of one cluster
+constexpr int kDmU = 8;        // tokens per warp in flight
+
+// dm_o += (sum_t dY[t, o] * Y[t, o]) / m_o  (= sum_t dY * Z / n with Y = (m / n) Z).
+// A cluster of kDmGroups CTAs covers a block of 32 * VEC columns (VEC = 16 bytes of elements per
+// lane); CTA g sums its token group (8 warps taking every 8th token, kDmU loads in flight per
+// warp), reduces its warps in warp order, and then each CTA adds, for its share of the block's
+// columns, the groups' sums in group order (from the peers' shared memory) into dm.
+template <typename T>
+__global__ void __launch_bounds__(256) k_dora_dm(const T* __restrict__ dY, const T* __restrict__ Y,
+                                                 const float* __restrict__ mag, int64_t Tn,
+                                                 int64_t out_dim, float* __restrict__ dm) {
+  constexpr int V = Vec<T>::N;
+  constexpr int kCols = 32 * V;
+  __shared__ float red[8][kCols];
+  __shared__ float mine[kCols];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t nb = (int64_t)blockIdx.x * kCols;
+  const int64_t n0 = nb + (int64_t)lane * V;
+  const bool nok = n0 < out_dim;   // out_dim is a multiple of 8, so a lane's columns are all in
+  const int g = blockIdx.y;
+  const int64_t tg = (Tn + kDmGroups - 1) / kDmGroups;
+  const int64_t t_begin = (int64_t)g * tg;
+  const int64_t t_end = min(Tn, t_begin + tg);
+  float acc[V];
+#pragma unroll
+  for (int e = 0; e < V; ++e) acc[e] = 0.f;
+  if (nok) {
+    for (int64_t t = t_begin + warp; t < t_end; t += 8 * kDmU) {
+      float a[kDmU][V], b[kDmU][V];
+#pragma unroll
+      for (int u = 0; u < kDmU; ++u) {
+        const int64_t tt = t + 8 * u;
+        if (tt < t_end) {
+          load16(dY + tt * out_dim + n0, a[u]);
+          load16(Y + tt * out_dim + n0, b[u]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < V; ++e) a[u][e] = b[u][e] = 0.f;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kDmU; ++u)
+#pragma unroll
+        for (int e = 0; e < V; ++e) acc[e] = fmaf(a[u][e], b[u][e], acc[e]);
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < V; ++e) red[warp][lane * V + e] = acc[e];
+  __syncthreads();
+  for (int c = threadIdx.x; c < kCols; c += 256) {
+    float sum = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) sum += red[w][c];
+    mine[c] = sum;
+  }
+  dm_cluster_sync();
+  constexpr int kShare = kCols / kDmGroups;
+  for (int cc = threadIdx.x; cc < kShare; cc += 256) {
+    const int c = g * kShare + cc;
+    const int64_t o = nb + c;
+    if (o < out_dim) {
+      float sum = 0.f;
+      for (int gg = 0; gg < kDmGroups; ++gg) sum += dm_ld_peer(&mine[c], (uint32_t)gg);
+      dm[o] += sum / mag[o];
+    }
+  }
+  dm_cluster_sync();   // peers' shared memory stays alive until every CTA has read it
 }
 
 }  // namespace
@@ -82,15 +225,42 @@ cudaError_t launch_dora_norm(int dtype, const void* W, const float* A, const flo
   return cudaGetLastError();
 }
 
+cudaError_t launch_dora_gram_combine(const void* W, const float* H, const float* A, const float* B,
+                                     float s, int64_t out_dim, int64_t in_dim, int32_t rank,
+                                     float* C, float* norm_out, cudaStream_t st) {
+  prof_begin(0, st);
+  k_dora_gram<<<dim3((unsigned)rank, (unsigned)((rank + 7) / 8)), 256, 0, st>>>(A, in_dim, rank, C);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  prof_begin(0, st);
+  k_dora_combine<<<(unsigned)((out_dim + 7) / 8), 256, 0, st>>>(
+      (const __nv_bfloat16*)W, H, B, C, s, out_dim, in_dim, rank, norm_out);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_dora_dm(int dtype, const void* dY, const void* Y, const float* mag, int64_t T,
                            int64_t out_dim, float* dm, cudaStream_t st) {
-  const unsigned blocks = (unsigned)((out_dim + 127) / 128);
-  if (dtype == LORA_F32)
-    { prof_begin(0, st); k_dora_dm<float><<<blocks, 128, 0, st>>>((const float*)dY, (const float*)Y, mag, T, out_dim, dm); }
-  else
-    { prof_begin(0, st); k_dora_dm<__nv_bfloat16><<<blocks, 128, 0, st>>>((const __nv_bfloat16*)dY,
-                                                     (const __nv_bfloat16*)Y, mag, T, out_dim, dm); }
-  return cudaGetLastError();
+  if (T <= 0) return cudaSuccess;
+  const int cols = dtype == LORA_F32 ? 32 * Vec<float>::N : 32 * Vec<__nv_bfloat16>::N;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)((out_dim + cols - 1) / cols), (unsigned)kDmGroups);
+  cfg.blockDim = dim3(256);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = kDmGroups;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  prof_begin(0, st);
+  cudaError_t e = dtype == LORA_F32
+                      ? cudaLaunchKernelEx(&cfg, k_dora_dm<float>, (const float*)dY, (const float*)Y,
+                                           mag, T, out_dim, dm)
+                      : cudaLaunchKernelEx(&cfg, k_dora_dm<__nv_bfloat16>,
+                                           (const __nv_bfloat16*)dY, (const __nv_bfloat16*)Y, mag, T,
+                                           out_dim, dm);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace lora

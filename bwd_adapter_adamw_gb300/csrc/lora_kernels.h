@@ -196,6 +196,10 @@ cudaError_t launch_token_slots(int64_t T, int32_t n_seg, const int32_t* seg_star
 cudaError_t launch_dora_norm(int dtype, const void* W, const float* A, const float* B, float s,
                              int64_t out_dim, int64_t in_dim, int32_t rank, float* norm_out,
                              cudaStream_t st);
+// bf16 W: the Gram matrix C = A A^T [r, r] and the row norms from H = W A^T [out, r]
+cudaError_t launch_dora_gram_combine(const void* W, const float* H, const float* A, const float* B,
+                                     float s, int64_t out_dim, int64_t in_dim, int32_t rank,
+                                     float* C, float* norm_out, cudaStream_t st);
 cudaError_t launch_dora_dm(int dtype, const void* dY, const void* Y, const float* mag, int64_t T,
                            int64_t out_dim, float* dm, cudaStream_t st);
 

@@ -61,9 +61,8 @@ template <int NP>
 __global__ void __launch_bounds__(kThreads, 1) k_tc_rows(const __grid_constant__ RowsParams p) {
   using C = RowsCfg<NP>;
   extern __shared__ uint8_t smem_raw[];
-  const int item = blockIdx.x;
-  if (item >= *p.n_items) return;
-  const TokenItem it = p.items[item];
+  TokenItem it;
+  if (!get_item(p.items, p.n_items, blockIdx.x, p.T, it)) return;
   const int z = blockIdx.y;
   const int kb0 = z * p.nk_per_split;
   const int kb1 = min(p.nk, kb0 + p.nk_per_split);
@@ -160,9 +159,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_rows(const __grid_constant__
 __global__ void k_rows_finish(const float* __restrict__ part, int32_t splits, int64_t T, int32_t NP,
                               const TokenItem* __restrict__ items, const int32_t* __restrict__ n_items,
                               const SlotInfo si, float* __restrict__ out, int64_t ldo) {
-  const int item = blockIdx.x;
-  if (item >= *n_items) return;
-  const TokenItem it = items[item];
+  TokenItem it;
+  if (!get_item(items, n_items, blockIdx.x, T, it)) return;
   const int32_t r = it.slot >= 0 ? si.rank[it.slot] : 0;
   const float alpha = it.slot >= 0 ? si.alpha[it.slot] : 0.f;
   const int64_t n = (int64_t)(it.t1 - it.t0) * ldo;

@@ -118,6 +118,9 @@ class LoraStep:
         self.streams = [torch.cuda.Stream(device=self.device) for _ in range(self.n_streams)] \
             if self.n_streams > 1 else []
         ws_need = max(L.lora_workspace_size(self.desc(l), self.T) for l in self.linears)
+        if self.dora:   # the norm refresh shares the stream's workspace
+            ws_need = max(ws_need, max(L.lora_dora_norm_workspace_size(self.desc(l))
+                                       for l in self.linears))
         if ws_need == 0:
             raise L.LoraError(L.LORA_ERR_INVALID, "lora_workspace_size")
         self.ws = [_ws(ws_need, self.device) for _ in range(self.n_streams)]
@@ -163,7 +166,7 @@ class LoraStep:
             ws = self.ws[i % self.n_streams]
             d = self.desc(l)
             if self.dora:
-                L.lora_dora_norm(d, l.W, l.A, l.B, l.norm, st)
+                L.lora_dora_norm(d, l.W, l.A, l.B, l.norm, ws, stream=st)
             if per_chunk_calls:
                 spans = [(c, c * ct, ct) for c in range(self.chunks)]
             else:

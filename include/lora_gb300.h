@@ -137,7 +137,7 @@ float lora_scale(float alpha, int32_t rank, int32_t rslora);
 double lora_lr_at(int32_t kind, double base, uint64_t step, uint64_t warmup, uint64_t total,
                   double min_lr);
 
-/* Workspace bytes for lora_forward / lora_backward / lora_dora_norm on T tokens. */
+/* Workspace bytes for lora_forward / lora_backward on T tokens. */
 size_t lora_workspace_size(const lora_desc* d, int64_t T);
 
 /* ---- frozen-weight preparation (once per frozen W, not per step) ----------------------------*/
@@ -157,9 +157,12 @@ int lora_prepare_weight(const lora_desc* d, const void* W, void* W_prep, void* s
 
 /* DoRA row norm n_o = || W_o + s (B A)_o ||_2 for the current A, B (fp32 [out_dim]); call once
  * per optimizer step before the first forward ("8. LoRA Fundamentals", How it works, and its
- * norm-refresh event). */
+ * norm-refresh event). For bf16 W it is evaluated on tensor cores from the expanded form
+ * ||W_o||^2 + 2 s (W A^T)_o . B_o + s^2 B_o (A A^T) B_o^T (the same quantity); scratch comes from
+ * ws (at least lora_dora_norm_workspace_size bytes, 16-byte aligned). */
+size_t lora_dora_norm_workspace_size(const lora_desc* d);
 int lora_dora_norm(const lora_desc* d, const void* W, const float* A, const float* B,
-                   float* norm_out, void* stream);
+                   float* norm_out, void* ws, size_t ws_bytes, void* stream);
 
 /* ---- forward / backward (one adapted linear, T tokens) --------------------------------------*/
 /* Y [T, out] = X W^T + Hs B^T, then * (dora_m / dora_n) per column in DoRA mode.
