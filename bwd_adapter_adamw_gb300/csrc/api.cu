@@ -279,6 +279,17 @@ SlotInfo slot_info(const Slots& s, float q) {
   return si;
 }
 
+// A single-adapter call (no segments) runs on uniform work items that the kernels compute from
+// the index: 128-token tiles and span-token reduction runs, all of slot 0. No item tables.
+void use_uniform_items(Layout& L, int64_t T) {
+  L.gitems = nullptr; L.gcount = nullptr;
+  L.gmax = (T + kGemmTileT - 1) / kGemmTileT;
+  L.items_db = nullptr; L.count_db = nullptr;
+  L.max_db = (T + (int64_t)L.span_db * 64 - 1) / ((int64_t)L.span_db * 64);
+  L.items_da = nullptr; L.count_da = nullptr;
+  L.max_da = (T + (int64_t)L.span_da * 64 - 1) / ((int64_t)L.span_da * 64);
+}
+
 // shrink on tensor cores: Hs[t, j] = s_k q (Xd[t, :] . A_k[j, :]) via the hi/lo split of A_k
 int tc_shrink(const lora_desc* d, const DropParams& dp, int64_t T, const void* X, int32_t n_seg,
               const Slots& s, const Layout& L, float* H, cudaStream_t st) {
@@ -319,8 +330,11 @@ int run_forward_tc(const lora_desc* d, const DropParams& dp, int64_t T, const vo
                    float* H, void* ws, cudaStream_t st) {
   Layout L = carve(d, T, n_seg, s.n, s.rank_sum, false, ws);
   clear_stale();
-  LORA_TRY(launch_make_items(T, n_seg, seg_start, seg_slot, s.n, L.gitems, L.gcount,
-                             (int32_t)L.gmax, nullptr, nullptr, 0, st));
+  if (n_seg < 0)
+    use_uniform_items(L, T);
+  else
+    LORA_TRY(launch_make_items(T, n_seg, seg_start, seg_slot, s.n, L.gitems, L.gcount,
+                               (int32_t)L.gmax, nullptr, nullptr, 0, st));
   const float* ratio = nullptr;
   if (ratio_src_m) {
     LORA_TRY(launch_ratio(ratio_src_m, ratio_src_n, d->out_dim, L.ratio, st));
@@ -346,12 +360,16 @@ int run_backward_tc(const lora_desc* d, const DropParams& dp, int64_t T, const v
                     float* dm, void* ws, cudaStream_t st) {
   Layout L = carve(d, T, n_seg, s.n, s.rank_sum, true, ws);
   clear_stale();
-  LORA_TRY(launch_make_items(T, n_seg, seg_start, seg_slot, s.n, L.gitems, L.gcount,
-                             (int32_t)L.gmax, nullptr, nullptr, 0, st));
-  LORA_TRY(launch_make_red_items_tc(T, n_seg, seg_start, seg_slot, s.n, L.span_db, L.items_db,
-                                    L.count_db, (int32_t)L.max_db, st));
-  LORA_TRY(launch_make_red_items_tc(T, n_seg, seg_start, seg_slot, s.n, L.span_da, L.items_da,
-                                    L.count_da, (int32_t)L.max_da, st));
+  if (n_seg < 0) {
+    use_uniform_items(L, T);
+  } else {
+    LORA_TRY(launch_make_items(T, n_seg, seg_start, seg_slot, s.n, L.gitems, L.gcount,
+                               (int32_t)L.gmax, nullptr, nullptr, 0, st));
+    LORA_TRY(launch_make_red_items_tc(T, n_seg, seg_start, seg_slot, s.n, L.span_db, L.items_db,
+                                      L.count_db, (int32_t)L.max_db, st));
+    LORA_TRY(launch_make_red_items_tc(T, n_seg, seg_start, seg_slot, s.n, L.span_da, L.items_da,
+                                      L.count_da, (int32_t)L.max_da, st));
+  }
   const float q = dropout_q(d);
   const SlotInfo si = slot_info(s, q);
   // A^T (fp32) for the LoRA K-steps of dX; hi/lo split of B^T for G
@@ -416,7 +434,7 @@ int run_backward_tc(const lora_desc* d, const DropParams& dp, int64_t T, const v
   // dB_k += dY'^T Hs over the slot's tokens (as dB^T rows of the transposed Hs split)
   {
     LORA_TRY(launch_split_rows_t(H, d->rank, L.ldt, L.gitems, L.gcount, (int)L.gmax, si, L.HsT,
-                                 split_bytes, st));
+                                 split_bytes, T, st));
     TcRedArgs a{};
     for (int k = 0; k < s.n; ++k) {
       a.st[k] = L.HsT + (int64_t)si.region[k] * L.ldt;
@@ -426,12 +444,13 @@ int run_backward_tc(const lora_desc* d, const DropParams& dp, int64_t T, const v
     a.n_slots = s.n; a.max_rank = d->rank; a.T = T; a.ldt = L.ldt;
     a.b = dYp; a.N = d->out_dim; a.part = L.red_part; a.tab = rt; a.transposed = 1;
     a.items = L.items_db; a.n_items = L.count_db; a.max_items = (int)L.max_db;
+    a.span_tokens = (int64_t)L.span_db * 64;
     LORA_TRY(launch_tc_red(a, st, LORA_PROF_RED_DB));
   }
   // dA_k += Gs^T Xd over the slot's tokens
   {
     LORA_TRY(launch_split_rows_t(L.Gs, d->rank, L.ldt, L.gitems, L.gcount, (int)L.gmax, si,
-                                 L.GsT, split_bytes, st));
+                                 L.GsT, split_bytes, T, st));
     TcRedArgs a{};
     for (int k = 0; k < s.n; ++k) {
       a.st[k] = L.GsT + (int64_t)si.region[k] * L.ldt;
@@ -441,6 +460,7 @@ int run_backward_tc(const lora_desc* d, const DropParams& dp, int64_t T, const v
     a.n_slots = s.n; a.max_rank = d->rank; a.T = T; a.ldt = L.ldt;
     a.b = Xin; a.N = d->in_dim; a.part = L.red_part; a.tab = rt; a.transposed = 0;
     a.items = L.items_da; a.n_items = L.count_da; a.max_items = (int)L.max_da;
+    a.span_tokens = (int64_t)L.span_da * 64;
     LORA_TRY(launch_tc_red(a, st, LORA_PROF_RED_DA));
   }
   if (dm) LORA_TRY(launch_dora_dm(d->dtype, dY, Y_save, dora_m, T, d->out_dim, dm, st));

@@ -63,8 +63,9 @@ struct TcParams {
   CUtensorMap tb;                       // B [N, K] bf16, box {64, 256}
   CUtensorMap tp;                       // P [T, ldp] fp32, box {32, 128}
   CUtensorMap tq[LORA_MAX_SLOTS];       // Q_slot [N, r] fp32, box {32, 256}
-  const TokenItem* items;
+  const TokenItem* items;               // null: uniform 128-token tiles, slot 0
   const int32_t* n_items;
+  int64_t T;
   uint32_t* err;
   int32_t nk_main;
   int32_t has_lora;
@@ -80,9 +81,8 @@ struct TcParams {
 // ---- the kernel ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__ TcParams p) {
   extern __shared__ uint8_t smem_raw[];
-  const int item = blockIdx.y;
-  if (item >= *p.n_items) return;
-  const TokenItem it = p.items[item];
+  TokenItem it;
+  if (!get_item(p.items, p.n_items, blockIdx.y, p.T, it)) return;
   const int slot = it.slot;
   const int32_t m0 = it.t0;
   const int32_t n0 = blockIdx.x * kBN;
@@ -268,6 +268,7 @@ cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st, int prof_kind) 
   }
   prm.items = a.items;
   prm.n_items = a.n_items;
+  prm.T = a.T;
   prm.err = tc::error_word();
   if (!prm.err) return cudaErrorInvalidDevice;
   prm.nk_main = (int32_t)((a.K + 63) / 64);

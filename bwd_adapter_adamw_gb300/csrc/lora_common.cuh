@@ -115,4 +115,22 @@ __device__ __forceinline__ bool get_item(const TokenItem* items, const int32_t* 
   return true;
 }
 
+// Token-reduction work item idx: from the table, or (null table, single-adapter call) the uniform
+// runs of span tokens covering [0, T), slot 0.
+__device__ __forceinline__ bool get_span_item(const TokenItem* items, const int32_t* n_items, int idx,
+                                              int64_t T, int64_t span, TokenItem& it) {
+  if (items) {
+    if (idx >= *n_items) return false;
+    it = items[idx];
+    return true;
+  }
+  const int64_t t0 = (int64_t)idx * span;
+  if (t0 >= T) return false;
+  it.t0 = (int32_t)t0;
+  it.t1 = (int32_t)(T < t0 + span ? T : t0 + span);
+  it.slot = 0;
+  it.pad = 0;
+  return true;
+}
+
 }  // namespace lora

@@ -81,6 +81,7 @@ struct TcRedArgs {                  // dst_slot += (ST_hi + ST_lo)[., t] x B[t, 
   const TokenItem* items;           // 64-token aligned runs (launch_make_red_items_tc)
   const int32_t* n_items;
   int max_items;
+  int64_t span_tokens;              // tokens per uniform item when items is null (single adapter)
 };
 struct SplitTab {
   const float* src[LORA_MAX_SLOTS];
@@ -94,7 +95,7 @@ cudaError_t launch_tc_red(const TcRedArgs& a, cudaStream_t st, int prof_kind);
 cudaError_t launch_split(const SplitTab& t, int n, cudaStream_t st);
 cudaError_t launch_split_rows_t(const float* src, int64_t lds, int64_t ldt, const TokenItem* items,
                                 const int32_t* n_items, int max_items, const SlotInfo& si,
-                                uint16_t* dst, size_t dst_bytes, cudaStream_t st);
+                                uint16_t* dst, size_t dst_bytes, int64_t T, cudaStream_t st);
 cudaError_t launch_make_red_items_tc(int64_t T, int32_t n_seg, const int32_t* seg_start,
                                      const int32_t* seg_slot, int32_t n_slots, int32_t span_blocks,
                                      TokenItem* items, int32_t* count, int32_t max_items,

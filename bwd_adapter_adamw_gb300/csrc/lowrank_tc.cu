@@ -156,16 +156,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_rows(const __grid_constant__
 }
 
 // out[t, j] = alpha_slot * sum_z (part[z][t][j] + part[z][t][r + j]) for j < r, 0 for r <= j < ldo.
+// CTA (item, blockIdx.y) covers kFinishTok tokens of the item.
+constexpr int kFinishTok = 8;
 __global__ void k_rows_finish(const float* __restrict__ part, int32_t splits, int64_t T, int32_t NP,
                               const TokenItem* __restrict__ items, const int32_t* __restrict__ n_items,
                               const SlotInfo si, float* __restrict__ out, int64_t ldo) {
   TokenItem it;
   if (!get_item(items, n_items, blockIdx.x, T, it)) return;
+  const int64_t tb = (int64_t)it.t0 + (int64_t)blockIdx.y * kFinishTok;
+  if (tb >= it.t1) return;
   const int32_t r = it.slot >= 0 ? si.rank[it.slot] : 0;
   const float alpha = it.slot >= 0 ? si.alpha[it.slot] : 0.f;
-  const int64_t n = (int64_t)(it.t1 - it.t0) * ldo;
+  const int64_t n = min((int64_t)kFinishTok, (int64_t)it.t1 - tb) * ldo;
   for (int64_t e = threadIdx.x; e < n; e += blockDim.x) {
-    const int64_t t = it.t0 + e / ldo;
+    const int64_t t = tb + e / ldo;
     const int j = (int)(e % ldo);
     float v = 0.f;
     if (j < r) {
@@ -192,6 +196,8 @@ struct RedParams {
   int32_t rstride;                   // partial rows per item (2 * max rank)
   float* part;                       // [items][rstride][N]
   int64_t N;
+  int64_t T;
+  int64_t span;                      // tokens per uniform item (null item table)
 };
 
 constexpr int kRedBN = 256;
@@ -203,8 +209,8 @@ constexpr uint32_t kRedIdesc = idesc(kFmtBF16, kBM, kRedBN, false, true);
 __global__ void __launch_bounds__(kThreads, 1) k_tc_red(const __grid_constant__ RedParams p) {
   extern __shared__ uint8_t smem_raw[];
   const int item = blockIdx.y;
-  if (item >= *p.n_items) return;
-  const TokenItem it = p.items[item];
+  TokenItem it;
+  if (!get_span_item(p.items, p.n_items, item, p.T, p.span, it)) return;
   if (it.slot < 0) return;
   const int32_t n0 = blockIdx.x * kRedBN;
   const int32_t tb0 = it.t0 & ~63;                  // 64-token blocks covering [t0, t1)
@@ -297,26 +303,59 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_red(const __grid_constant__ 
 
 // dst_slot += sum over the slot's items (in item order) of hi + lo partial rows:
 // transposed == 0: dst[j * N + n] (dA [r, N]); transposed == 1: dst[n * r + j] (dB [N, r]).
+constexpr int kRedFinishMaxItems = 1024;   // items of one slot held in shared memory per pass
 __global__ void k_red_finish(const float* __restrict__ part, const TokenItem* __restrict__ items,
                              const int32_t* __restrict__ n_items, int64_t N, int32_t rstride,
-                             int transposed, const ReduceTab tab) {
+                             int transposed, const ReduceTab tab, int64_t T, int64_t span) {
+  __shared__ int32_t mine[kRedFinishMaxItems];
+  __shared__ int32_t n_mine;
   const int slot = blockIdx.y;
   const int32_t r = tab.rank[slot];
   float* dst = tab.out[slot];
-  const int32_t ni = *n_items;
+  const int32_t ni = items ? *n_items : (int32_t)((T + span - 1) / span);
   const int64_t total = (int64_t)r * N;
+  // this slot's items, in item order (the summation order); a null table is the uniform runs of
+  // a single-adapter call, all of slot 0
+  if (threadIdx.x == 0) {
+    int32_t c = 0;
+    for (int32_t i = 0; i < ni; ++i)
+      if (items ? items[i].slot == slot : slot == 0) {
+        if (c < kRedFinishMaxItems) mine[c] = i;
+        ++c;
+      }
+    n_mine = c;
+  }
+  __syncthreads();
+  const int32_t nm = n_mine;
+  if (nm == 0) return;
   for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
        e += (int64_t)gridDim.x * blockDim.x) {
     const int64_t j = e / N, n = e - j * N;
     float acc = 0.f;
-    bool any = false;
-    for (int32_t i = 0; i < ni; ++i) {
-      if (items[i].slot != slot) continue;
-      const float* pr = part + (int64_t)i * rstride * N;
-      acc += pr[j * N + n] + pr[(j + r) * N + n];
-      any = true;
+    if (nm <= kRedFinishMaxItems) {
+      int32_t k = 0;
+      for (; k + 4 <= nm; k += 4) {   // four items' loads in flight, added in item order
+        float v[8];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float* pr = part + (int64_t)mine[k + u] * rstride * N;
+          v[2 * u] = pr[j * N + n];
+          v[2 * u + 1] = pr[(j + r) * N + n];
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) acc += v[2 * u] + v[2 * u + 1];
+      }
+      for (; k < nm; ++k) {
+        const float* pr = part + (int64_t)mine[k] * rstride * N;
+        acc += pr[j * N + n] + pr[(j + r) * N + n];
+      }
+    } else {   // more items than the list holds: scan the table, same order
+      for (int32_t i = 0; i < ni; ++i) {
+        if (items ? items[i].slot != slot : slot != 0) continue;
+        const float* pr = part + (int64_t)i * rstride * N;
+        acc += pr[j * N + n] + pr[(j + r) * N + n];
+      }
     }
-    if (!any) continue;
     if (transposed)
       dst[n * r + j] += acc;
     else
@@ -357,10 +396,9 @@ __global__ void k_split(const SplitTab tab) {
 // dst[region_s + j][t] = hi(src[t, j]), dst[region_s + r_s + j][t] = lo(src[t, j]).
 __global__ void k_split_rows_t(const float* __restrict__ src, int64_t lds, int64_t ldt,
                                const TokenItem* __restrict__ items, const int32_t* __restrict__ n_items,
-                               const SlotInfo si, uint16_t* __restrict__ dst) {
-  const int item = blockIdx.x;
-  if (item >= *n_items) return;
-  const TokenItem it = items[item];
+                               const SlotInfo si, uint16_t* __restrict__ dst, int64_t T) {
+  TokenItem it;
+  if (!get_item(items, n_items, blockIdx.x, T, it)) return;
   if (it.slot < 0) return;
   const int32_t r = si.rank[it.slot];
   uint16_t* d = dst + (int64_t)si.region[it.slot] * ldt;
@@ -485,8 +523,8 @@ cudaError_t launch_tc_rows(const TcRowsArgs& a, cudaStream_t st, int prof_kind) 
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   prof_begin(0, st);
-  k_rows_finish<<<(unsigned)a.max_items, 256, 0, st>>>(a.part, a.splits, a.T, NP, a.items,
-                                                        a.n_items, a.si, a.out, a.ldo);
+  k_rows_finish<<<dim3((unsigned)a.max_items, (unsigned)(kBM / kFinishTok)), 256, 0, st>>>(
+      a.part, a.splits, a.T, NP, a.items, a.n_items, a.si, a.out, a.ldo);
   return cudaGetLastError();
 }
 
@@ -509,6 +547,8 @@ cudaError_t launch_tc_red(const TcRedArgs& a, cudaStream_t st, int prof_kind) {
   if (!prm.err) return cudaErrorInvalidDevice;
   prm.part = a.part;
   prm.N = a.N;
+  prm.T = a.T;
+  prm.span = a.span_tokens;
   prm.rstride = 2 * a.max_rank;
   static bool attr = false;
   if (!attr) {
@@ -527,7 +567,7 @@ cudaError_t launch_tc_red(const TcRedArgs& a, cudaStream_t st, int prof_kind) {
   if (blocks > 8192) blocks = 8192;
   prof_begin(0, st);
   k_red_finish<<<dim3((unsigned)blocks, (unsigned)a.n_slots), 256, 0, st>>>(
-      a.part, a.items, a.n_items, a.N, 2 * a.max_rank, a.transposed, a.tab);
+      a.part, a.items, a.n_items, a.N, 2 * a.max_rank, a.transposed, a.tab, a.T, a.span_tokens);
   return cudaGetLastError();
 }
 
@@ -544,12 +584,16 @@ cudaError_t launch_split(const SplitTab& t, int n, cudaStream_t st) {
 
 cudaError_t launch_split_rows_t(const float* src, int64_t lds, int64_t ldt, const TokenItem* items,
                                 const int32_t* n_items, int max_items, const SlotInfo& si,
-                                uint16_t* dst, size_t dst_bytes, cudaStream_t st) {
+                                uint16_t* dst, size_t dst_bytes, int64_t T, cudaStream_t st) {
   if (max_items <= 0) return cudaSuccess;
-  cudaError_t e = cudaMemsetAsync(dst, 0, dst_bytes, st);
-  if (e != cudaSuccess) return e;
+  // With an item table, tokens of other slots must read as zero in each slot's rows. A null table
+  // (single adapter) writes every token of the one slot, and the tensor maps stop at T.
+  if (items) {
+    cudaError_t e = cudaMemsetAsync(dst, 0, dst_bytes, st);
+    if (e != cudaSuccess) return e;
+  }
   prof_begin(0, st);
-  k_split_rows_t<<<(unsigned)max_items, 128, 0, st>>>(src, lds, ldt, items, n_items, si, dst);
+  k_split_rows_t<<<(unsigned)max_items, 128, 0, st>>>(src, lds, ldt, items, n_items, si, dst, T);
   return cudaGetLastError();
 }
 
