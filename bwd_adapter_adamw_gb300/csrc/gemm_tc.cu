@@ -54,6 +54,12 @@ constexpr int kABytes = kBM * 128;   // 16 KB: 128 rows x 128 bytes
 constexpr int kBBytes = kBN * 128;   // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kThreads = 192;
+constexpr int kEpiThreads = 128;
+// Items per tile group (rasterization for L2 reuse): 16 when W spans more than 16 N tiles; with
+// fewer, the N tile runs fastest (group of 1), so that the CTAs of one wave read all of W
+// together. Measured at T 8192 (us): N 4096 / K 4096: 152 (N fastest), 152 (8), 162 (16);
+// N 14336 / K 4096: 688, 585, 550; N 4096 / K 14336: 542, 566, 557.
+constexpr int kGroupWide = 16;
 constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*barriers*/ + 1024 /*alignment*/;
 constexpr uint32_t kIdescBF16 = tc::idesc(tc::kFmtBF16, kBM, kBN);
 constexpr uint32_t kIdescTF32 = tc::idesc(tc::kFmtTF32, kBM, kBN);
@@ -66,6 +72,10 @@ struct TcParams {
   const TokenItem* items;               // null: uniform 128-token tiles, slot 0
   const int32_t* n_items;
   int64_t T;
+  int32_t n_tiles;                      // N tiles per item
+  int32_t max_items;                    // item slots
+  int32_t group_m;                      // items per tile group
+  int32_t total_tiles;                  // n_tiles x item slots
   uint32_t* err;
   int32_t nk_main;
   int32_t has_lora;
@@ -79,34 +89,48 @@ struct TcParams {
 };
 
 // ---- the kernel ---------------------------------------------------------------------------
+// Persistent: CTA b takes tiles b, b + gridDim.x, ... Tiles are ordered in groups of group_m items:
+// within a group the item index runs fastest, then the N tile, so that for a wide W one wave of
+// CTAs touches group_m items of A and about 152 / group_m N-tiles of W, which both stay in L2
+// (with the N tile fastest, every few items would stream all of a wide W from HBM again). The
+// stage ring runs on across tiles, and two
+// 256-column TMEM accumulators alternate between tiles, so that the epilogue of one tile drains
+// and stores while the MMAs of the next run. With a dropout-masked LoRA term the second 256
+// columns hold that term instead, and tiles take turns on one accumulator.
+__device__ __forceinline__ bool decode_tile(const TcParams& p, int t, TokenItem& it, int32_t& n0) {
+  const int per_group = p.group_m * p.n_tiles;
+  const int group = t / per_group;
+  const int first = group * p.group_m;
+  const int gsize = min(p.group_m, p.max_items - first);
+  const int idx = t - group * per_group;
+  n0 = (idx / gsize) * kBN;
+  return get_item(p.items, p.n_items, first + idx % gsize, p.T, it);
+}
+
 __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__ TcParams p) {
   extern __shared__ uint8_t smem_raw[];
-  TokenItem it;
-  if (!get_item(p.items, p.n_items, blockIdx.y, p.T, it)) return;
-  const int slot = it.slot;
-  const int32_t m0 = it.t0;
-  const int32_t n0 = blockIdx.x * kBN;
-  const int nk_lora = (p.has_lora && slot >= 0) ? (p.q_rank[slot] + 31) / 32 : 0;
-  const int nk = p.nk_main + nk_lora;
-  const bool sep = p.lora_separate && nk_lora > 0;
-
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* tiles = base;
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(base + kStages * kStageBytes);
   uint64_t* empty_bar = full_bar + kStages;
-  uint64_t* acc_bar = empty_bar + kStages;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_bar + 1);
+  uint64_t* acc_full = empty_bar + kStages;   // [2]: a tile's accumulation is complete
+  uint64_t* acc_empty = acc_full + 2;         // [2]: the epilogue has drained the accumulator
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t ncols = p.lora_separate ? 512u : 256u;
+  const uint32_t ncols = 512u;
+  const int nbuf = p.lora_separate ? 1 : 2;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
-    mbar_init(acc_bar, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], kEpiThreads);
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
@@ -118,88 +142,124 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
 
   if (warp == 0) {
     if (lane == 0) {
-      int issued = 0;
-      for (int kb = 0; kb < nk; ++kb) {
-        const int s = kb % kStages;
-        const uint32_t ph = (uint32_t)(kb / kStages) & 1u;
-        if (kb >= kStages && !mbar_wait(&empty_bar[s], ph ^ 1u, 1u, p.err)) break;
-        uint8_t* sa = tiles + s * kStageBytes;
-        uint8_t* sb = sa + kABytes;
-        mbar_expect_tx(&full_bar[s], kStageBytes);
-        if (kb < p.nk_main) {
-          tma_load_2d(sa, &p.ta, &full_bar[s], kb * 64, m0);
-          tma_load_2d(sb, &p.tb, &full_bar[s], kb * 64, n0);
-        } else {
-          const int j = kb - p.nk_main;
-          tma_load_2d(sa, &p.tp, &full_bar[s], j * 32, m0);
-          tma_load_2d(sb, &p.tq[slot], &full_bar[s], j * 32, n0);
+      int g = 0;   // stage uses so far (across tiles)
+      bool ok = true;
+      for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
+        TokenItem it;
+        int32_t n0;
+        if (!decode_tile(p, t, it, n0)) continue;
+        const int slot = it.slot;
+        const int nk = p.nk_main + ((p.has_lora && slot >= 0) ? (p.q_rank[slot] + 31) / 32 : 0);
+        for (int kb = 0; kb < nk; ++kb, ++g) {
+          const int s = g % kStages;
+          const uint32_t ph = (uint32_t)(g / kStages) & 1u;
+          if (g >= kStages && !mbar_wait(&empty_bar[s], ph ^ 1u, 1u, p.err)) { ok = false; break; }
+          uint8_t* sa = tiles + s * kStageBytes;
+          uint8_t* sb = sa + kABytes;
+          mbar_expect_tx(&full_bar[s], kStageBytes);
+          if (kb < p.nk_main) {
+            tma_load_2d(sa, &p.ta, &full_bar[s], kb * 64, it.t0);
+            tma_load_2d(sb, &p.tb, &full_bar[s], kb * 64, n0);
+          } else {
+            const int j = kb - p.nk_main;
+            tma_load_2d(sa, &p.tp, &full_bar[s], j * 32, it.t0);
+            tma_load_2d(sb, &p.tq[slot], &full_bar[s], j * 32, n0);
+          }
         }
-        issued = kb + 1;
       }
       // drain: every issued load must have landed before the CTA may exit
-      for (int kb = (issued > kStages ? issued - kStages : 0); kb < issued; ++kb)
-        if (!mbar_wait(&full_bar[kb % kStages], (uint32_t)(kb / kStages) & 1u, 1u, p.err)) break;
+      for (int gg = (g > kStages ? g - kStages : 0); gg < g; ++gg)
+        if (!mbar_wait(&full_bar[gg % kStages], (uint32_t)(gg / kStages) & 1u, 1u, p.err)) break;
     }
   } else if (warp == 1) {
     if (lane == 0) {
+      int g = 0, j = 0;
       bool ok = true;
-      for (int kb = 0; kb < nk && ok; ++kb) {
-        const int s = kb % kStages;
-        const uint32_t ph = (uint32_t)(kb / kStages) & 1u;
-        if (!mbar_wait(&full_bar[s], ph, 2u, p.err)) { ok = false; break; }
+      for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
+        TokenItem it;
+        int32_t n0;
+        if (!decode_tile(p, t, it, n0)) continue;
+        const int slot = it.slot;
+        const int nk_lora = (p.has_lora && slot >= 0) ? (p.q_rank[slot] + 31) / 32 : 0;
+        const int nk = p.nk_main + nk_lora;
+        const bool sep = p.lora_separate && nk_lora > 0;
+        const int b = j % nbuf, use = j / nbuf;
+        if (use >= 1 && !mbar_wait(&acc_empty[b], (uint32_t)(use - 1) & 1u, 2u, p.err)) break;
         fence_after();
-        const uint32_t sa = smem_u32(tiles + s * kStageBytes);
-        const uint32_t sb = sa + kABytes;
-        const uint64_t da = smem_desc_sw128(sa), db = smem_desc_sw128(sb);
-        if (kb < p.nk_main) {
+        const uint32_t dm = tmem + 256u * (uint32_t)b;
+        for (int kb = 0; kb < nk; ++kb, ++g) {
+          const int s = g % kStages;
+          const uint32_t ph = (uint32_t)(g / kStages) & 1u;
+          if (!mbar_wait(&full_bar[s], ph, 2u, p.err)) { ok = false; break; }
+          fence_after();
+          const uint32_t sa = smem_u32(tiles + s * kStageBytes);
+          const uint32_t sb = sa + kABytes;
+          const uint64_t da = smem_desc_sw128(sa), db = smem_desc_sw128(sb);
+          if (kb < p.nk_main) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            umma_f16(tmem, da + 2 * k, db + 2 * k, kIdescBF16, (kb > 0 || k > 0) ? 1u : 0u);
-        } else {
-          const uint32_t d = sep ? tmem + 256u : tmem;
-          const bool first = sep && kb == p.nk_main;
+            for (int k = 0; k < 4; ++k)
+              umma_f16(dm, da + 2 * k, db + 2 * k, kIdescBF16, (kb > 0 || k > 0) ? 1u : 0u);
+          } else {
+            const uint32_t d = sep ? tmem + 256u : dm;
+            const bool first = sep && kb == p.nk_main;
 #pragma unroll
-          for (int k = 0; k < 4; ++k) umma_tf32(d, da + 2 * k, db + 2 * k, kIdescTF32, (first && k == 0) ? 0u : 1u);
+            for (int k = 0; k < 4; ++k)
+              umma_tf32(d, da + 2 * k, db + 2 * k, kIdescTF32, (first && k == 0) ? 0u : 1u);
+          }
+          umma_commit(&empty_bar[s]);
         }
-        umma_commit(&empty_bar[s]);
+        if (!ok) break;
+        umma_commit(&acc_full[b]);
+        ++j;
       }
-      umma_commit(acc_bar);
     }
   } else {
     // epilogue: warp w drains TMEM lanes 32*(w % 4) .. +31 (one output row per thread)
     const int q = warp & 3;
     const int row = q * 32 + lane;
-    const int64_t m = (int64_t)m0 + row;
-    const bool row_ok = m < it.t1;
-    // warp-uniform decision: the TMEM loads below are .sync.aligned
-    const bool ready = __all_sync(0xffffffffu, mbar_wait(acc_bar, 0u, 4u, p.err));
-    if (ready) {
+    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+    int j = 0;
+    for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+      TokenItem it;
+      int32_t n0;
+      if (!decode_tile(p, t, it, n0)) continue;
+      const int slot = it.slot;
+      const bool sep = p.lora_separate && p.has_lora && slot >= 0 && p.q_rank[slot] > 0;
+      const int b = j % nbuf, use = j / nbuf;
+      const int64_t m = (int64_t)it.t0 + row;
+      const bool row_ok = m < it.t1;
+      // warp-uniform decision: the TMEM loads below are .sync.aligned
+      const bool ready = __all_sync(0xffffffffu, mbar_wait(&acc_full[b], (uint32_t)use & 1u, 4u, p.err));
+      if (!ready) break;
       fence_after();
-      __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+      const uint32_t acc = tmem + ((uint32_t)(q * 32) << 16) + 256u * (uint32_t)b;
       for (int c = 0; c < kBN / 32; ++c) {
         float v[32];
-        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * 32), v);
+        tmem_ld32(acc + (uint32_t)(c * 32), v);
         if (sep) {
           float w[32];
           tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + 256u + (uint32_t)(c * 32), w);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int64_t n = (int64_t)n0 + c * 32 + j;
-            if (row_ok && n < p.n_out && drop_keep(p.drop, m, n)) v[j] += w[j];
+          for (int jj = 0; jj < 32; ++jj) {
+            const int64_t n = (int64_t)n0 + c * 32 + jj;
+            if (row_ok && n < p.n_out && drop_keep(p.drop, m, n)) v[jj] += w[jj];
           }
         }
         const int64_t nb = (int64_t)n0 + c * 32;
         if (p.n_colscale) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            v[j] *= (nb + j < p.n_out) ? __ldg(p.n_colscale + nb + j) : 0.f;
+          for (int jj = 0; jj < 32; ++jj)
+            v[jj] *= (nb + jj < p.n_out) ? __ldg(p.n_colscale + nb + jj) : 0.f;
         }
         if (row_ok) {
 #pragma unroll
-          for (int g = 0; g < 4; ++g)
-            if (nb + g * 8 + 8 <= p.n_out) store8(out + m * p.ldo + nb + g * 8, v + g * 8);
+          for (int gq = 0; gq < 4; ++gq)
+            if (nb + gq * 8 + 8 <= p.n_out) store8(out + m * p.ldo + nb + gq * 8, v + gq * 8);
         }
       }
+      fence_before();
+      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&acc_empty[b])) : "memory");
+      ++j;
     }
     fence_before();
   }
@@ -228,6 +288,18 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }  // namespace
 
 namespace tc {
+int sm_count() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (!cached[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
 bool make_map_2d(CUtensorMap* map, const void* ptr, CUtensorMapDataType dt, int elem, uint64_t inner,
               uint64_t outer, uint64_t row_elems, uint32_t box_inner, uint32_t box_outer) {
   auto fn = encode_fn();
@@ -285,8 +357,16 @@ cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st, int prof_kind) 
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  dim3 grid((unsigned)((a.n_rows + kBN - 1) / kBN), (unsigned)a.max_items);
   if (a.max_items <= 0) return cudaSuccess;
+  prm.n_tiles = (int32_t)((a.n_rows + kBN - 1) / kBN);
+  prm.max_items = a.max_items;
+  prm.group_m = prm.n_tiles > 16 ? kGroupWide : 1;
+  const int64_t total = (int64_t)prm.n_tiles * a.max_items;
+  if (total > INT32_MAX) return cudaErrorInvalidValue;
+  prm.total_tiles = (int32_t)total;
+  const int sms = tc::sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  const unsigned grid = (unsigned)(total < sms ? total : sms);   // one persistent CTA per SM
   prof_begin(prof_kind, st);
   k_tc_gemm<<<grid, kThreads, kSmemBytes, st>>>(prm);
   prof_end(prof_kind, st);

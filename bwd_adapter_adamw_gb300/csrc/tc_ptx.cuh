@@ -214,6 +214,9 @@ __device__ __forceinline__ void store8(__nv_bfloat16* p, const float* v) {
 }
 
 
+// Streaming multiprocessors of the current device (cached per device; 0 on error).
+int sm_count();
+
 // Shared helpers for host-side tensor maps (gemm_tc.cu). The box row (box_inner * elem bytes) must
 // be 128 or 64 bytes and selects the matching swizzle.
 bool make_map_2d(CUtensorMap* map, const void* ptr, CUtensorMapDataType dt, int elem, uint64_t inner,
