@@ -115,6 +115,26 @@ __device__ __forceinline__ bool get_item(const TokenItem* items, const int32_t* 
   return true;
 }
 
+// Segment table staged in shared memory by a block (at most kSegSmem segments; larger tables are
+// read from global memory): start[k], end[k] = start[k + 1], slot[k].
+constexpr int kSegSmem = 2048;
+struct SegView {
+  const int32_t* start;   // [n + 1]
+  const int32_t* slot;    // [n]
+  int32_t n;
+};
+__device__ __forceinline__ SegView stage_segments(int32_t n_seg, const int32_t* seg_start,
+                                                  const int32_t* seg_slot, int32_t* s_start,
+                                                  int32_t* s_slot) {
+  if (!seg_start || n_seg > kSegSmem) return SegView{seg_start, seg_slot, seg_start ? n_seg : 0};
+  for (int k = threadIdx.x; k <= n_seg; k += blockDim.x) {
+    s_start[k] = seg_start[k];
+    if (k < n_seg) s_slot[k] = seg_slot[k];
+  }
+  __syncthreads();
+  return SegView{s_start, s_slot, n_seg};
+}
+
 // Token-reduction work item idx: from the table, or (null table, single-adapter call) the uniform
 // runs of span tokens covering [0, T), slot 0.
 __device__ __forceinline__ bool get_span_item(const TokenItem* items, const int32_t* n_items, int idx,

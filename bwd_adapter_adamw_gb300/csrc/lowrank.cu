@@ -14,6 +14,8 @@ __global__ void k_make_items(int64_t T, int32_t n_seg, const int32_t* __restrict
                              const int32_t* __restrict__ seg_slot, int32_t n_slots,
                              TokenItem* gitems, int32_t* gcount, int32_t gmax, TokenItem* ritems,
                              int32_t* rcount, int32_t rmax) {
+  __shared__ int32_t s_start[kSegSmem + 1], s_slot[kSegSmem];
+  const SegView sv = stage_segments(n_seg, seg_start, seg_slot, s_start, s_slot);
   if (threadIdx.x != 0 || blockIdx.x != 0) return;
   int32_t ng = 0, nr = 0;
   int64_t cursor = 0;
@@ -27,9 +29,9 @@ __global__ void k_make_items(int64_t T, int32_t n_seg, const int32_t* __restrict
   // n_seg < 0: one implicit segment [0, T) with slot 0 (single-adapter calls)
   const int32_t nsegs = seg_start ? n_seg : (n_seg < 0 ? 1 : 0);
   for (int32_t k = 0; k < nsegs; ++k) {
-    int64_t a = seg_start ? (int64_t)seg_start[k] : 0;
-    int64_t b = seg_start ? (int64_t)seg_start[k + 1] : T;
-    int32_t slot = seg_slot ? seg_slot[k] : 0;
+    int64_t a = seg_start ? (int64_t)sv.start[k] : 0;
+    int64_t b = seg_start ? (int64_t)sv.start[k + 1] : T;
+    int32_t slot = seg_slot ? sv.slot[k] : 0;
     if (slot < 0 || slot >= n_slots) slot = -1;
     a = max((int64_t)0, min(a, T));
     b = max((int64_t)0, min(b, T));
@@ -203,7 +205,7 @@ cudaError_t launch_make_items(int64_t T, int32_t n_seg, const int32_t* seg_start
                               const int32_t* seg_slot, int32_t n_slots, TokenItem* gitems,
                               int32_t* gcount, int32_t gmax, TokenItem* ritems, int32_t* rcount,
                               int32_t rmax, cudaStream_t st) {
-  { prof_begin(0, st); k_make_items<<<1, 32, 0, st>>>(T, n_seg, seg_start, seg_slot, n_slots, gitems, gcount, gmax,
+  { prof_begin(0, st); k_make_items<<<1, 128, 0, st>>>(T, n_seg, seg_start, seg_slot, n_slots, gitems, gcount, gmax,
                                  ritems, rcount, rmax); }
   return cudaGetLastError();
 }

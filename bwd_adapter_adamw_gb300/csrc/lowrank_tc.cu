@@ -421,20 +421,28 @@ __global__ void k_make_red_items_tc(int64_t T, int32_t n_seg, const int32_t* __r
                                     const int32_t* __restrict__ seg_slot, int32_t n_slots,
                                     int32_t span_blocks, TokenItem* items, int32_t* count,
                                     int32_t max_items) {
-  if (threadIdx.x != 0 || blockIdx.x != 0) return;
-  int32_t n = 0;
-  auto emit_run = [&](int64_t b0, int64_t b1, int32_t slot) {
-    for (int64_t b = b0; b < b1; b += span_blocks)
-      if (n < max_items)
-        items[n++] = TokenItem{(int32_t)(b * 64), (int32_t)(min(b1, b + span_blocks) * 64), slot, 0};
-  };
+  // The segment table is staged in shared memory; thread s walks it for slot s (counting its
+  // items, then writing them after the lower slots' items), so the table is the same as a walk
+  // slot by slot.
+  __shared__ int32_t s_start[kSegSmem + 1], s_slot[kSegSmem];
+  __shared__ int32_t s_count[LORA_MAX_SLOTS + 1];
+  const SegView sv = stage_segments(n_seg, seg_start, seg_slot, s_start, s_slot);
   const int32_t nsegs = seg_start ? n_seg : (n_seg < 0 ? 1 : 0);
-  for (int32_t s = 0; s < n_slots; ++s) {
+  const int s = threadIdx.x;
+  auto walk = [&](bool write, int32_t base) {
+    int32_t n = 0;
+    auto emit_run = [&](int64_t b0, int64_t b1) {
+      for (int64_t b = b0; b < b1; b += span_blocks) {
+        if (write && base + n < max_items)
+          items[base + n] = TokenItem{(int32_t)(b * 64), (int32_t)(min(b1, b + span_blocks) * 64), s, 0};
+        ++n;
+      }
+    };
     int64_t cursor = 0, rb = -1, re = -1;
     for (int32_t k = 0; k < nsegs; ++k) {
-      int64_t a = seg_start ? (int64_t)seg_start[k] : 0;
-      int64_t b = seg_start ? (int64_t)seg_start[k + 1] : T;
-      int32_t slot = seg_slot ? seg_slot[k] : 0;
+      int64_t a = seg_start ? (int64_t)sv.start[k] : 0;
+      int64_t b = seg_start ? (int64_t)sv.start[k + 1] : T;
+      int32_t slot = seg_slot ? sv.slot[k] : 0;
       if (slot < 0 || slot >= n_slots) slot = -1;
       a = max((int64_t)0, min(a, T));
       b = max((int64_t)0, min(b, T));
@@ -446,14 +454,23 @@ __global__ void k_make_red_items_tc(int64_t T, int32_t n_seg, const int32_t* __r
       if (re >= 0 && ba <= re) {
         re = max(re, bb);
       } else {
-        if (re >= 0) emit_run(rb, re, s);
+        if (re >= 0) emit_run(rb, re);
         rb = ba;
         re = bb;
       }
     }
-    if (re >= 0) emit_run(rb, re, s);
+    if (re >= 0) emit_run(rb, re);
+    return n;
+  };
+  if (s < n_slots) s_count[s + 1] = walk(false, 0);
+  __syncthreads();
+  if (s == 0) {
+    s_count[0] = 0;
+    for (int k = 1; k <= n_slots; ++k) s_count[k] += s_count[k - 1];
+    *count = min(s_count[n_slots], max_items);
   }
-  *count = n;
+  __syncthreads();
+  if (s < n_slots) walk(true, s_count[s]);
 }
 
 // Xd = bf16(M * X): the masked operand of the shrink and of dA when dropout is on.
@@ -602,8 +619,8 @@ cudaError_t launch_make_red_items_tc(int64_t T, int32_t n_seg, const int32_t* se
                                      TokenItem* items, int32_t* count, int32_t max_items,
                                      cudaStream_t st) {
   prof_begin(0, st);
-  k_make_red_items_tc<<<1, 32, 0, st>>>(T, n_seg, seg_start, seg_slot, n_slots, span_blocks,
-                                        items, count, max_items);
+  k_make_red_items_tc<<<1, 128, 0, st>>>(T, n_seg, seg_start, seg_slot, n_slots, span_blocks,
+                                         items, count, max_items);
   return cudaGetLastError();
 }
 
