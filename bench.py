@@ -432,6 +432,33 @@ def run_ours(args):
     e2e_ms = e0.elapsed_time(e1)
     clk = clocks.stop()
 
+    # the same kernel class once more with every linear on one stream (a second capture after
+    # the timed region): the kernel's own duration, without the sharing of the multi-stream step
+    kern_serial = []
+    if graph is not None and getattr(step, "n_streams", 1) > 1:
+        step.active_streams = 1
+        s_starts = [torch.cuda.Event(enable_timing=True) for _ in range(n_prof)]
+        s_stops = [torch.cuda.Event(enable_timing=True) for _ in range(n_prof)]
+        for e in s_starts + s_stops:
+            e.record()
+        torch.cuda.synchronize()
+        L.lora_profile_arm(prof_class, s_starts, s_stops)
+        g1 = torch.cuda.CUDAGraph()
+        s1 = torch.cuda.Stream(device=device)
+        s1.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s1):
+            with torch.cuda.graph(g1, stream=s1):
+                run()
+        torch.cuda.current_stream().wait_stream(s1)
+        used1 = L.lora_profile_used()
+        L.lora_profile_arm(0, [], [])
+        for _ in range(2):
+            g1.replay()
+        torch.cuda.synchronize()
+        kern_serial = [a.elapsed_time(b) for a, b in zip(s_starts[:used1], s_stops[:used1])]
+        step.active_streams = step.n_streams
+        del g1
+
     ms, e2e_ms = max_over_ranks([ms, e2e_ms], world, device)
     tokens = cfg.tokens
     value = whole_job_rate(world, K, tokens, ms)
@@ -456,6 +483,8 @@ def run_ours(args):
             bound, punit = "tensor", "TFLOP/s"
             note = f"dense bf16 cuBLAS burst, {peak_src}"
         achieved = per_launch / (avg_kern / 1e3) / 1e12 if avg_kern else None
+        avg_serial = statistics.mean(kern_serial) if kern_serial else None
+        achieved_serial = per_launch / (avg_serial / 1e3) / 1e12 if avg_serial else None
         traffic, traffic_note = traffic_for(cfg.name, prof_class)
         cpu = None
         if not args.no_cpu_baseline and world == 1:
@@ -477,6 +506,11 @@ def run_ours(args):
                              prof_class, f"class {prof_class}"),
                          "launches_timed": len(kern_ms), "avg_launch_ms": avg_kern,
                          "peak_source": note},
+            "roofline_serial": None if achieved_serial is None else {
+                "achieved": achieved_serial, "peak": peak, "unit": punit,
+                "frac": achieved_serial / peak, "avg_launch_ms": avg_serial,
+                "launches_timed": len(kern_serial),
+                "note": "same kernel class, same step captured with every linear on one stream"},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},

@@ -27,6 +27,28 @@ def _ws(nbytes: int, device) -> torch.Tensor:
     return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
 
 
+def _streams_in_use(step):
+    """(k, streams): the first k = min(active_streams, n_streams) side streams, or none for k = 1
+    (everything on the caller's current stream)."""
+    k = max(1, min(step.active_streams, step.n_streams))
+    return k, (step.streams[:k] if (step.streams and k > 1) else [])
+
+
+def _fork(main, use):
+    if use:
+        ev = torch.cuda.Event()
+        ev.record(main)
+        for s in use:
+            s.wait_event(ev)
+
+
+def _join(main, use):
+    for s in use:
+        ev = torch.cuda.Event()
+        ev.record(s)
+        main.wait_event(ev)
+
+
 @dataclass
 class Linear:
     """One adapted linear with its activations (device tensors)."""
@@ -117,6 +139,7 @@ class LoraStep:
         self.n_streams = max(1, n_streams)
         self.streams = [torch.cuda.Stream(device=self.device) for _ in range(self.n_streams)] \
             if self.n_streams > 1 else []
+        self.active_streams = self.n_streams   # streams used by the next enqueue (<= n_streams)
         ws_need = max(L.lora_workspace_size(self.desc(l), self.T) for l in self.linears)
         if self.dora:   # the norm refresh shares the stream's workspace
             ws_need = max(ws_need, max(L.lora_dora_norm_workspace_size(self.desc(l))
@@ -155,15 +178,12 @@ class LoraStep:
     def forward_backward(self, opt_step: int, per_chunk_calls: bool = False):
         """Enqueue forward + backward of every linear over all chunks (gradients accumulate)."""
         main = torch.cuda.current_stream(self.device)
-        if self.streams:
-            ev = torch.cuda.Event()
-            ev.record(main)
-            for s in self.streams:
-                s.wait_event(ev)
+        k, use = _streams_in_use(self)
+        _fork(main, use)
         ct = self.T // self.chunks
         for i, l in enumerate(self.linears):
-            st = self.streams[i % self.n_streams] if self.streams else main
-            ws = self.ws[i % self.n_streams]
+            st = use[i % k] if use else main
+            ws = self.ws[i % k]
             d = self.desc(l)
             if self.dora:
                 L.lora_dora_norm(d, l.W, l.A, l.B, l.norm, ws, stream=st)
@@ -178,11 +198,7 @@ class LoraStep:
                 L.lora_forward(d, ctx, n, X, l.W, l.Wp, l.A, l.B, l.mag, l.norm, Y, H, ws, stream=st)
                 L.lora_backward(d, ctx, n, X, l.Wp, l.A, l.B, dY, H, l.mag, l.norm, Y, dX, l.gA,
                                 l.gB, l.gmag, ws, stream=st)
-        if self.streams:
-            for s in self.streams:
-                ev = torch.cuda.Event()
-                ev.record(s)
-                main.wait_event(ev)
+        _join(main, use)
 
     def optimizer_step(self, lr: float, step: int, zero_grads: bool = True):
         g = self.groups(lr, step)
@@ -272,6 +288,7 @@ class MultiLoraStep:
         self.n_streams = max(1, n_streams)
         self.streams = [torch.cuda.Stream(device=self.device) for _ in range(self.n_streams)] \
             if self.n_streams > 1 else []
+        self.active_streams = self.n_streams   # streams used by the next enqueue (<= n_streams)
         need = max(L.multi_lora_workspace_size(self.desc(l), self.T, self.n_seg, self.slots(l))
                    for l in self.linears)
         if need == 0:
@@ -297,14 +314,11 @@ class MultiLoraStep:
 
     def forward_backward(self, opt_step: int = 0):
         main = torch.cuda.current_stream(self.device)
-        if self.streams:
-            ev = torch.cuda.Event()
-            ev.record(main)
-            for s in self.streams:
-                s.wait_event(ev)
+        k, use = _streams_in_use(self)
+        _fork(main, use)
         for i, l in enumerate(self.linears):
-            st = self.streams[i % self.n_streams] if self.streams else main
-            ws = self.ws[i % self.n_streams]
+            st = use[i % k] if use else main
+            ws = self.ws[i % k]
             d = self.desc(l)
             ctx = L.make_ctx(opt_step, 0, 0)
             sl = self.slots(l)
@@ -312,11 +326,7 @@ class MultiLoraStep:
                                  self.seg_slot, sl, l.Y, l.H, ws, stream=st)
             L.multi_lora_backward(d, ctx, self.T, l.X, l.Wp, self.n_seg, self.seg_start,
                                   self.seg_slot, sl, l.dY, l.H, l.dX, ws, stream=st)
-        if self.streams:
-            for s in self.streams:
-                ev = torch.cuda.Event()
-                ev.record(s)
-                main.wait_event(ev)
+        _join(main, use)
 
     def groups(self, ready: Sequence[int], gbs: Sequence[int], lrs: Sequence[float],
                steps: Sequence[int]):
