@@ -82,6 +82,39 @@ def counts(cfg: LI.LoraConfig, layers: int):
                 opt_bytes=32 * params, act_bytes=a)
 
 
+def memory_counts(cfg: LI.LoraConfig, layers: int):
+    """Algorithmic HBM bytes per step of the memory-bound kernel classes (each array the class
+    must touch, once): shrink reads X and A and writes Hs (and, on the fp32 path, the tf32 split
+    of X); G reads dY' and B and writes Gs (and the split of dY'); the dB / dA reductions read dY'
+    or X and Hs or Gs and update dB / dA; grad-prepare reads 4 B and AdamW moves 32 B per
+    parameter (p, g, m, v read; p, m, v written; g cleared)."""
+    T = cfg.tokens
+    a = 4 if cfg.dtype == "f32" else 2
+    split = 8 if cfg.dtype == "f32" else 0
+    if cfg.multi:
+        ranks = list(LI.make_routing(cfg).slot_rank)
+        r_all, layers = sum(ranks), 1
+        r_row = max(ranks)
+    else:
+        r_all = r_row = cfg.rank
+    out = {"shrink": 0, "G": 0, "redB": 0, "redA": 0}
+    for p in cfg.projs:
+        i, o = p.in_dim, p.out_dim
+        out["shrink"] += T * i * a + r_all * i * 4 + T * r_row * 4 + split * T * i
+        out["G"] += T * o * a + r_all * o * 4 + T * r_row * 4 + split * T * o
+        out["redB"] += T * o * a + T * r_row * 4 + 2 * r_all * o * 4
+        out["redA"] += T * i * a + T * r_row * 4 + 2 * r_all * i * 4
+    out = {k: v * layers for k, v in out.items()}
+    r_step = r_all
+    if cfg.multi:   # only the slots whose adapter batch is full take a step
+        rt = LI.make_routing(cfg)
+        r_step = sum(rk for k, rk in enumerate(rt.slot_rank) if LI.slot_ready(rt, k))
+    params = sum(r_step * (p.in_dim + p.out_dim) for p in cfg.projs) * layers
+    out["prepare"] = 4 * params
+    out["adamw"] = 32 * params
+    return out
+
+
 # DRAM bytes per launch of the dominant kernel class (dram__bytes_read.sum + dram__bytes_write.sum,
 # one ncu capture, caches flushed by ncu), averaged over the class's launch shapes, keyed by
 # (workload, kernel class); valid only while the kernel source still hashes to the recorded
@@ -432,17 +465,16 @@ def run_ours(args):
     e2e_ms = e0.elapsed_time(e1)
     clk = clocks.stop()
 
-    # the same kernel class once more with every linear on one stream (a second capture after
-    # the timed region): the kernel's own duration, without the sharing of the multi-stream step
-    kern_serial = []
-    if graph is not None and getattr(step, "n_streams", 1) > 1:
+    # the kernel classes once more with every linear on one stream (a capture per class after
+    # the timed region): the kernels' own durations, without the sharing of the multi-stream step
+    def serial_times(cls, n_max):
         step.active_streams = 1
-        s_starts = [torch.cuda.Event(enable_timing=True) for _ in range(n_prof)]
-        s_stops = [torch.cuda.Event(enable_timing=True) for _ in range(n_prof)]
+        s_starts = [torch.cuda.Event(enable_timing=True) for _ in range(n_max)]
+        s_stops = [torch.cuda.Event(enable_timing=True) for _ in range(n_max)]
         for e in s_starts + s_stops:
             e.record()
         torch.cuda.synchronize()
-        L.lora_profile_arm(prof_class, s_starts, s_stops)
+        L.lora_profile_arm(cls, s_starts, s_stops)
         g1 = torch.cuda.CUDAGraph()
         s1 = torch.cuda.Stream(device=device)
         s1.wait_stream(torch.cuda.current_stream())
@@ -455,9 +487,18 @@ def run_ours(args):
         for _ in range(2):
             g1.replay()
         torch.cuda.synchronize()
-        kern_serial = [a.elapsed_time(b) for a, b in zip(s_starts[:used1], s_stops[:used1])]
         step.active_streams = step.n_streams
         del g1
+        return [a.elapsed_time(b) for a, b in zip(s_starts[:used1], s_stops[:used1])]
+
+    kern_serial, mem_times = [], {}
+    if graph is not None:
+        if getattr(step, "n_streams", 1) > 1:
+            kern_serial = serial_times(prof_class, n_prof)
+        for name, cls in (("shrink", L.LORA_PROF_SHRINK), ("G", L.LORA_PROF_G),
+                          ("redB", L.LORA_PROF_RED_DB), ("redA", L.LORA_PROF_RED_DA),
+                          ("prepare", L.LORA_PROF_PREPARE), ("adamw", L.LORA_PROF_ADAMW)):
+            mem_times[name] = serial_times(cls, max(n_prof, 8))
 
     ms, e2e_ms = max_over_ranks([ms, e2e_ms], world, device)
     tokens = cfg.tokens
@@ -484,6 +525,14 @@ def run_ours(args):
             note = f"dense bf16 cuBLAS burst, {peak_src}"
         achieved = per_launch / (avg_kern / 1e3) / 1e12 if avg_kern else None
         avg_serial = statistics.mean(kern_serial) if kern_serial else None
+        mem = memory_counts(cfg, layers if not cfg.multi else 1)
+        memory_bound = {}
+        for name, ts in mem_times.items():
+            if ts:
+                gbs = mem[name] / (sum(ts) / 1e3) / 1e9
+                memory_bound[name] = {"achieved_gbs": gbs, "frac": gbs / peaks["hbm_gbs"],
+                                      "launches": len(ts), "ms_total": sum(ts),
+                                      "bytes_per_step": mem[name]}
         achieved_serial = per_launch / (avg_serial / 1e3) / 1e12 if avg_serial else None
         traffic, traffic_note = traffic_for(cfg.name, prof_class)
         cpu = None
@@ -511,6 +560,9 @@ def run_ours(args):
                 "frac": achieved_serial / peak, "avg_launch_ms": avg_serial,
                 "launches_timed": len(kern_serial),
                 "note": "same kernel class, same step captured with every linear on one stream"},
+            "memory_bound": {"peak_gbs": peaks["hbm_gbs"], "kernels": memory_bound,
+                             "note": "algorithmic bytes per step / summed launch times, "
+                                     "single-stream capture"} if memory_bound else None,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},

@@ -536,12 +536,12 @@ cudaError_t launch_tc_rows(const TcRowsArgs& a, cudaStream_t st, int prof_kind) 
     default:
       return cudaErrorInvalidValue;
   }
-  prof_end(prof_kind, st);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   prof_begin(0, st);
   k_rows_finish<<<dim3((unsigned)a.max_items, (unsigned)(kBM / kFinishTok)), 256, 0, st>>>(
       a.part, a.splits, a.T, NP, a.items, a.n_items, a.si, a.out, a.ldo);
+  prof_end(prof_kind, st);   // the class's time spans the product and its split-K finish
   return cudaGetLastError();
 }
 
@@ -576,7 +576,6 @@ cudaError_t launch_tc_red(const TcRedArgs& a, cudaStream_t st, int prof_kind) {
   dim3 grid((unsigned)((a.N + kRedBN - 1) / kRedBN), (unsigned)a.max_items);
   prof_begin(prof_kind, st);
   k_tc_red<<<grid, kThreads, kRedSmem, st>>>(prm);
-  prof_end(prof_kind, st);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   int64_t total = (int64_t)a.max_rank * a.N;
@@ -585,6 +584,7 @@ cudaError_t launch_tc_red(const TcRedArgs& a, cudaStream_t st, int prof_kind) {
   prof_begin(0, st);
   k_red_finish<<<dim3((unsigned)blocks, (unsigned)a.n_slots), 256, 0, st>>>(
       a.part, a.items, a.n_items, a.N, 2 * a.max_rank, a.transposed, a.tab, a.T, a.span_tokens);
+  prof_end(prof_kind, st);   // the class's time spans the product and its item reduction
   return cudaGetLastError();
 }
 
