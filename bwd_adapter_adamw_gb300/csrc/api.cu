@@ -152,22 +152,29 @@ int np_for(int rmax) {           // MMA N covering hi + lo rows of the largest s
   return n <= 16 ? 16 : n <= 32 ? 32 : n <= 64 ? 64 : 128;
 }
 
-// K splits of the skinny token-row products so that about two CTAs per SM stream the input.
+// Resident CTAs of the skinny tensor-core products: two per SM on the 152-SM part. A shape choice
+// only (any count is correct); it is a constant so that workspace sizes do not depend on the device.
+constexpr int64_t kLowRankSlots = 2 * 152;
+
+// K splits of the skinny token-row products: as many as keep every CTA resident in one wave.
 int row_splits(int64_t T, int32_t n_seg, int64_t K) {
   const int64_t items = max_gemm_items(T, n_seg);
-  int64_t s = (296 + items - 1) / items;
+  int64_t s = kLowRankSlots / items;
   const int64_t nk = (K + 63) / 64;
   if (s > nk / 2) s = nk / 2;
   if (s > kMaxRowSplits) s = kMaxRowSplits;
   return s < 1 ? 1 : (int)s;
 }
 
-// 64-token blocks per reduction work item: enough items for ~2 CTAs per SM over the N tiles,
-// but at least 8 blocks so that the per-item partials stay small next to the streamed input.
+// 64-token blocks per reduction work item: as few items as fill the resident CTA slots over the
+// N tiles, but at least 4 blocks so that the per-item partial ([r, 256] fp32 per tile) stays small
+// next to the streamed input (256 tokens x 256 columns bf16 per tile).
 int red_span_blocks(int64_t T, int64_t N) {
   const int64_t tiles = (N + 255) / 256;
-  int64_t blocks = ((T * tiles) / 296 + 63) / 64;
-  if (blocks < 8) blocks = 8;
+  int64_t items = kLowRankSlots / tiles;
+  if (items < 1) items = 1;
+  int64_t blocks = ((T + 63) / 64 + items - 1) / items;
+  if (blocks < 4) blocks = 4;
   if (blocks > 64) blocks = 64;
   return (int)blocks;
 }
@@ -197,13 +204,13 @@ struct Layout {
   uint16_t* Xd;        // [T, in] bf16 masked input (dropout)
   uint16_t* Sa;        // per slot [2 r, in] bf16 split of A
   uint16_t* Sb;        // per slot [2 r, out] bf16 split of B^T
-  float* rows_part;    // [splits][T][NP]
+  float* rows_part;    // [splits][T][rmax]
   int64_t ldt;         // padded token stride of the transposed splits
   uint16_t* HsT;       // per slot [2 r, ldt] bf16
   uint16_t* GsT;       // per slot [2 r, ldt] bf16
   TokenItem* items_db; int32_t* count_db; int64_t max_db; int span_db;
   TokenItem* items_da; int32_t* count_da; int64_t max_da; int span_da;
-  float* red_part;     // [items][2 rmax][N]
+  float* red_part;     // [items][rmax][N]
   size_t bytes;
 };
 
@@ -218,10 +225,9 @@ Layout carve(const lora_desc* d, int64_t T, int32_t n_seg, int n_slots, int64_t 
   L.gcount = c.take<int32_t>(4);
   L.ratio = c.take<float>((size_t)d->out_dim);
   if (tc) {
-    const int np = np_for(d->rank);
     if (d->dropout_p > 0.f) L.Xd = c.take<uint16_t>((size_t)T * d->in_dim);
     L.Sa = c.take<uint16_t>((size_t)2 * rank_sum * d->in_dim);
-    L.rows_part = c.take<float>((size_t)kMaxRowSplits * T * np);
+    L.rows_part = c.take<float>((size_t)kMaxRowSplits * T * d->rank);
   }
   if (backward) {
     L.Gs = c.take<float>((size_t)T * d->rank);
@@ -241,7 +247,7 @@ Layout carve(const lora_desc* d, int64_t T, int32_t n_seg, int n_slots, int64_t 
       L.items_da = c.take<TokenItem>((size_t)L.max_da);
       L.count_da = c.take<int32_t>(4);
       const int64_t a = L.max_db * d->out_dim, b = L.max_da * d->in_dim;
-      L.red_part = c.take<float>((size_t)(a > b ? a : b) * 2 * d->rank);
+      L.red_part = c.take<float>((size_t)(a > b ? a : b) * d->rank);
     } else {
       L.ritems = c.take<TokenItem>((size_t)L.rmax);
       L.rcount = c.take<int32_t>(4);
@@ -415,6 +421,7 @@ int run_backward_tc(const lora_desc* d, const DropParams& dp, int64_t T, const v
     r.part = L.rows_part;
     r.si = si;
     r.out = L.Gs; r.ldo = d->rank;
+    r.outT = L.GsT; r.ldt = L.ldt; r.outT_bytes = (size_t)2 * s.rank_sum * L.ldt * sizeof(uint16_t);
     r.items = L.gitems; r.n_items = L.gcount; r.max_items = (int)L.gmax;
     LORA_TRY(launch_tc_rows(r, st, LORA_PROF_G));
   }
@@ -447,10 +454,8 @@ int run_backward_tc(const lora_desc* d, const DropParams& dp, int64_t T, const v
     a.span_tokens = (int64_t)L.span_db * 64;
     LORA_TRY(launch_tc_red(a, st, LORA_PROF_RED_DB));
   }
-  // dA_k += Gs^T Xd over the slot's tokens
+  // dA_k += Gs^T Xd over the slot's tokens (GsT was written by the G product's finish)
   {
-    LORA_TRY(launch_split_rows_t(L.Gs, d->rank, L.ldt, L.gitems, L.gcount, (int)L.gmax, si,
-                                 L.GsT, split_bytes, T, st));
     TcRedArgs a{};
     for (int k = 0; k < s.n; ++k) {
       a.st[k] = L.GsT + (int64_t)si.region[k] * L.ldt;
@@ -647,7 +652,7 @@ int run_backward(const lora_desc* d, const DropParams& dp, int64_t T, const void
 // lo bf16 split of A), then ||W_o||^2 + 2 s H_o . B_o + s^2 B_o (A A^T) B_o^T per row.
 struct NormLayout {
   uint16_t* Sa;        // [2 r, in] bf16 split of A
-  float* part;         // [splits][out][NP]
+  float* part;         // [splits][out][r]
   float* H;            // [out, r]
   float* C;            // [r, r]
   size_t bytes;
@@ -658,7 +663,7 @@ NormLayout dora_norm_carve(const lora_desc* d, void* ws) {
   Carve c(ws);
   if (d->dtype == LORA_BF16) {
     L.Sa = c.take<uint16_t>((size_t)2 * d->rank * d->in_dim);
-    L.part = c.take<float>((size_t)kMaxRowSplits * d->out_dim * np_for(d->rank));
+    L.part = c.take<float>((size_t)kMaxRowSplits * d->out_dim * d->rank);
     L.H = c.take<float>((size_t)d->out_dim * d->rank);
     L.C = c.take<float>((size_t)d->rank * d->rank);
   }

@@ -58,10 +58,13 @@ struct TcRowsArgs {                 // out[t, j] = alpha * (A[t, :] . (S_hi[j] +
   int32_t n_slots;
   int32_t NP;                       // MMA N: 16, 32, 64 or 128 (>= 2 * max rank)
   int32_t splits;                   // K splits
-  float* part;                      // [splits][T][NP] scratch
+  float* part;                      // [splits][T][ldo] scratch
   SlotInfo si;
-  float* out;                       // [T, ldo] fp32
+  float* out;                       // [T, ldo] fp32 (ldo = largest rank)
   int64_t ldo;
+  uint16_t* outT;                   // optional per slot [2 r, ldt] bf16 transposed split of out
+  int64_t ldt;
+  size_t outT_bytes;                // zeroed first when an item table routes several slots
   const TokenItem* items;
   const int32_t* n_items;
   int max_items;
@@ -75,7 +78,7 @@ struct TcRedArgs {                  // dst_slot += (ST_hi + ST_lo)[., t] x B[t, 
   int64_t ldt;
   const void* b;                    // [T, N] bf16 (dY' or Xd)
   int64_t N;
-  float* part;                      // [items][128][N] scratch
+  float* part;                      // [items][max_rank][N] scratch
   ReduceTab tab;
   int32_t transposed;               // 1: dst is [N, r] (dB); 0: dst is [r, N] (dA)
   const TokenItem* items;           // 64-token aligned runs (launch_make_red_items_tc)

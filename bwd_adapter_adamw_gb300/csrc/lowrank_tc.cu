@@ -7,11 +7,14 @@
 // (x = hi + lo + O(2^-16 |x|)); both parts are multiplied against the exact bf16 activations, so
 // the products keep fp32-level accuracy while running on kind::f16 tensor cores.
 //
-//  k_tc_rows: part[z][t][j] = sum_{k in split z} A[t, k] S_slot[j, k]   (shrink, G)
-//             M = 128 tokens of one work item, N = NP >= 2 r (hi rows then lo rows), K-major.
-//  k_tc_red:  part[item][m][n] = sum_{t in item} ST_slot[m, t] Bmn[t, n]   (dA, dB^T)
-//             M = 128 (2 r rows of the slot's transposed split), N = 256 columns of dY or X
-//             (MN-major tiles), K = the item's tokens in 64-token blocks.
+//  k_tc_rows: part[z][t][j] = sum_{k in split z} A[t, k] (S_slot[j, k] + S_slot[r + j, k])
+//             (shrink, G). M = 128 tokens of one work item, N = NP >= 2 r (hi rows then lo
+//             rows), K-major; the epilogue adds the hi and lo columns.
+//  k_tc_red:  part[item][j][n] = sum_{t in item} (ST_slot[j, t] + ST_slot[r + j, t]) Bmn[t, n]
+//             (dA, dB^T). M = 128 (2 r rows of the slot's transposed split), N = 256 columns of
+//             dY or X (MN-major tiles), K = the item's tokens in 64-token blocks; the epilogue adds
+//             the hi and lo rows.
+// Both run two CTAs per SM so that one CTA's prologue and epilogue overlap the other's stream.
 // Partials are combined in a fixed order by the finish kernels, so reruns are bitwise equal.
 #include <cstring>
 #include <mutex>
@@ -41,9 +44,11 @@ struct RowsParams {
   const TokenItem* items;
   const int32_t* n_items;
   uint32_t* err;
+  int32_t rank[LORA_MAX_SLOTS];
   int32_t nk;                        // K blocks in total
   int32_t nk_per_split;
-  float* part;                       // [splits][T][NP]
+  int32_t ldp;                       // partial row stride (largest rank)
+  float* part;                       // [splits][T][ldp]
   int64_t T;
 };
 
@@ -51,14 +56,18 @@ template <int NP>
 struct RowsCfg {
   static constexpr int kBBytes = NP * 128;
   static constexpr int kStageBytes = 16384 + kBBytes;
-  static constexpr int kStages = (NP <= 32) ? 8 : 6;
+  // about 100 KB of stages, so that two CTAs fit one SM
+  static constexpr int kStages = (100 * 1024 / kStageBytes) < 8 ? (100 * 1024 / kStageBytes) : 8;
   static constexpr int kSmem = kStages * kStageBytes + 1024 + 1024;
+  static constexpr int kLdb = NP + 4;   // staging row stride of the epilogue (floats)
+  static_assert(kStages >= 2, "pipeline depth");
+  static_assert(kBM * kLdb * 4 <= kStages * kStageBytes, "epilogue staging fits the stages");
   static constexpr uint32_t kCols = NP < 32 ? 32u : (uint32_t)NP;
   static constexpr uint32_t kIdesc = idesc(kFmtBF16, kBM, NP);
 };
 
 template <int NP>
-__global__ void __launch_bounds__(kThreads, 1) k_tc_rows(const __grid_constant__ RowsParams p) {
+__global__ void __launch_bounds__(kThreads, 2) k_tc_rows(const __grid_constant__ RowsParams p) {
   using C = RowsCfg<NP>;
   extern __shared__ uint8_t smem_raw[];
   TokenItem it;
@@ -66,14 +75,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_rows(const __grid_constant__
   const int z = blockIdx.y;
   const int kb0 = z * p.nk_per_split;
   const int kb1 = min(p.nk, kb0 + p.nk_per_split);
-  float* part = p.part + (int64_t)z * p.T * NP;
+  float* part = p.part + (int64_t)z * p.T * p.ldp;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (it.slot < 0 || kb0 >= kb1) {
     // no adapter for these tokens (or an empty split): the partial rows are zero
-    for (int r = threadIdx.x; r < it.t1 - it.t0; r += kThreads) {
-      float4* dst = reinterpret_cast<float4*>(part + (int64_t)(it.t0 + r) * NP);
-      for (int j = 0; j < NP / 4; ++j) dst[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
+    float4* dst = reinterpret_cast<float4*>(part + (int64_t)it.t0 * p.ldp);
+    const int n4 = (it.t1 - it.t0) * (p.ldp / 4);
+    for (int e = threadIdx.x; e < n4; e += kThreads) dst[e] = make_float4(0.f, 0.f, 0.f, 0.f);
     return;
   }
   const int nk = kb1 - kb0;
@@ -129,9 +137,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_rows(const __grid_constant__
       umma_commit(acc_bar);
     }
   } else {
+    // epilogue: the accumulator rows go through shared memory (the stages are idle once acc_bar
+    // has fired), then hi + lo columns are added and the item's [n, ldp] partial block, which is
+    // contiguous in memory, is written with coalesced float4 stores
     const int q = warp & 3;
     const int row = q * 32 + lane;
-    const int64_t t = (int64_t)it.t0 + row;
+    float* buf = reinterpret_cast<float*>(base);
     const bool ready = __all_sync(0xffffffffu, mbar_wait(acc_bar, 0u, 4u, p.err));
     if (ready) {
       fence_after();
@@ -139,14 +150,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_rows(const __grid_constant__
       for (int c = 0; c < NP / 16; ++c) {
         float v[16];
         tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * 16), v);
-        if (t < it.t1) {
-          float4* dst = reinterpret_cast<float4*>(part + t * NP + c * 16);
+        float4* dst = reinterpret_cast<float4*>(buf + row * C::kLdb + c * 16);
 #pragma unroll
-          for (int g = 0; g < 4; ++g) dst[g] = make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
-        }
+        for (int g = 0; g < 4; ++g) dst[g] = make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
       }
     }
     fence_before();
+    asm volatile("bar.sync 1, 128;" ::: "memory");   // the four epilogue warps
+    if (ready) {
+      const int r = p.rank[it.slot];
+      const int r4 = r / 4, l4 = p.ldp / 4;
+      const int n4 = (it.t1 - it.t0) * l4;
+      float4* dst = reinterpret_cast<float4*>(part + (int64_t)it.t0 * p.ldp);
+      for (int e = threadIdx.x - 64; e < n4; e += 128) {
+        const int i = e / l4, c = e - i * l4;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (c < r4) {
+          const float4 h = *reinterpret_cast<const float4*>(buf + i * C::kLdb + 4 * c);
+          const float4 l = *reinterpret_cast<const float4*>(buf + i * C::kLdb + r + 4 * c);
+          v = make_float4(h.x + l.x, h.y + l.y, h.z + l.z, h.w + l.w);
+        }
+        dst[e] = v;
+      }
+    }
   }
   __syncthreads();
   if (warp == 1) {
@@ -155,31 +181,52 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_rows(const __grid_constant__
   }
 }
 
-// out[t, j] = alpha_slot * sum_z (part[z][t][j] + part[z][t][r + j]) for j < r, 0 for r <= j < ldo.
+// out[t, j] = alpha_slot * sum_z part[z][t][j] for j < r, 0 for r <= j < ldo. With outT, also the
+// transposed bf16 split that the token reductions take as their K-major operand:
+// outT[region_slot + j][t] = hi(out[t, j]), outT[region_slot + r + j][t] = lo(out[t, j]).
 // CTA (item, blockIdx.y) covers kFinishTok tokens of the item.
-constexpr int kFinishTok = 8;
-__global__ void k_rows_finish(const float* __restrict__ part, int32_t splits, int64_t T, int32_t NP,
-                              const TokenItem* __restrict__ items, const int32_t* __restrict__ n_items,
-                              const SlotInfo si, float* __restrict__ out, int64_t ldo) {
+constexpr int kFinishTok = 32;
+constexpr int kMaxSplitsRows = 8;   // K splits of the rows kernel (the launcher rejects more)
+__global__ void __launch_bounds__(256) k_rows_finish(
+    const float* __restrict__ part, int32_t splits, int64_t T, int32_t ldp,
+    const TokenItem* __restrict__ items, const int32_t* __restrict__ n_items, const SlotInfo si,
+    float* __restrict__ out, int64_t ldo, uint16_t* __restrict__ outT, int64_t ldt) {
+  __shared__ float tile[kFinishTok][LORA_MAX_RANK + 1];
   TokenItem it;
   if (!get_item(items, n_items, blockIdx.x, T, it)) return;
   const int64_t tb = (int64_t)it.t0 + (int64_t)blockIdx.y * kFinishTok;
   if (tb >= it.t1) return;
   const int32_t r = it.slot >= 0 ? si.rank[it.slot] : 0;
   const float alpha = it.slot >= 0 ? si.alpha[it.slot] : 0.f;
-  const int64_t n = min((int64_t)kFinishTok, (int64_t)it.t1 - tb) * ldo;
-  for (int64_t e = threadIdx.x; e < n; e += blockDim.x) {
-    const int64_t t = tb + e / ldo;
-    const int j = (int)(e % ldo);
+  const int ld = (int)ldo;
+  const int nt = (int)min((int64_t)kFinishTok, (int64_t)it.t1 - tb);
+  for (int e = threadIdx.x; e < nt * ld; e += blockDim.x) {
+    const int i = e / ld, j = e - i * ld;
+    const int64_t t = tb + i;
     float v = 0.f;
     if (j < r) {
-      for (int z = 0; z < splits; ++z) {
-        const float* pr = part + ((int64_t)z * T + t) * NP;
-        v += pr[j] + pr[r + j];
-      }
+      // every split's partial loaded first (independent loads in flight), then added in order
+      float pz[kMaxSplitsRows];
+#pragma unroll
+      for (int z = 0; z < kMaxSplitsRows; ++z)
+        pz[z] = z < splits ? part[((int64_t)z * T + t) * ldp + j] : 0.f;
+#pragma unroll
+      for (int z = 0; z < kMaxSplitsRows; ++z)
+        if (z < splits) v += pz[z];
       v *= alpha;
+      tile[i][j] = v;
     }
     out[t * ldo + j] = v;
+  }
+  if (!outT || it.slot < 0) return;   // uniform over the CTA
+  __syncthreads();
+  uint16_t* d = outT + (int64_t)si.region[it.slot] * ldt + tb;
+  for (int e = threadIdx.x; e < nt * r; e += blockDim.x) {
+    const int j = e / nt, i = e - j * nt;
+    const float x = tile[i][j];
+    const uint16_t hb = bf16_bits(x);
+    d[(int64_t)j * ldt + i] = hb;
+    d[(int64_t)(r + j) * ldt + i] = bf16_bits(x - bf16_val(hb));
   }
 }
 
@@ -192,8 +239,8 @@ struct RedParams {
   const TokenItem* items;
   const int32_t* n_items;
   uint32_t* err;
-  int32_t rows2[LORA_MAX_SLOTS];     // 2 r per slot
-  int32_t rstride;                   // partial rows per item (2 * max rank)
+  int32_t rank[LORA_MAX_SLOTS];
+  int32_t rstride;                   // partial rows per item (largest rank)
   float* part;                       // [items][rstride][N]
   int64_t N;
   int64_t T;
@@ -202,11 +249,14 @@ struct RedParams {
 
 constexpr int kRedBN = 256;
 constexpr int kRedStageBytes = 16384 + 32768;
-constexpr int kRedStages = 4;
+constexpr int kRedStages = 2;       // about 100 KB of stages, so that two CTAs fit one SM
 constexpr int kRedSmem = kRedStages * kRedStageBytes + 1024 + 1024;
+constexpr int kRedHalf = kRedBN / 2;   // epilogue columns staged per pass
+constexpr int kRedLdb = kRedHalf + 4;
+static_assert(kBM * kRedLdb * 4 <= kRedStages * kRedStageBytes, "epilogue staging fits the stages");
 constexpr uint32_t kRedIdesc = idesc(kFmtBF16, kBM, kRedBN, false, true);
 
-__global__ void __launch_bounds__(kThreads, 1) k_tc_red(const __grid_constant__ RedParams p) {
+__global__ void __launch_bounds__(kThreads, 2) k_tc_red(const __grid_constant__ RedParams p) {
   extern __shared__ uint8_t smem_raw[];
   const int item = blockIdx.y;
   TokenItem it;
@@ -272,25 +322,42 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_red(const __grid_constant__ 
       umma_commit(acc_bar);
     }
   } else {
+    // epilogue, in two passes of 128 columns: the accumulator rows go through shared memory (the
+    // stages are idle once acc_bar has fired), then row j (hi) and row r + j (lo) are added and
+    // written along n with coalesced float4 stores
     const int q = warp & 3;
     const int row = q * 32 + lane;
-    const bool row_ok = row < p.rows2[it.slot];
-    float* part = p.part + ((int64_t)item * p.rstride + row) * p.N;
+    const int r = p.rank[it.slot];
+    float* buf = reinterpret_cast<float*>(base);
+    float* part = p.part + (int64_t)item * p.rstride * p.N;
     const bool ready = __all_sync(0xffffffffu, mbar_wait(acc_bar, 0u, 4u, p.err));
-    if (ready) {
-      fence_after();
-      for (int c = 0; c < kRedBN / 32; ++c) {
-        float v[32];
-        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * 32), v);
-        const int64_t nb = (int64_t)n0 + c * 32;
-        if (row_ok) {
+    if (ready) fence_after();
+    for (int h = 0; h < kRedBN / kRedHalf; ++h) {
+      if (ready) {
 #pragma unroll
-          for (int g = 0; g < 8; ++g)
-            if (nb + 4 * g + 4 <= p.N)
-              *reinterpret_cast<float4*>(part + nb + 4 * g) =
-                  make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+        for (int c = 0; c < kRedHalf / 32; ++c) {
+          float v[32];
+          tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * kRedHalf + c * 32), v);
+          float4* dst = reinterpret_cast<float4*>(buf + row * kRedLdb + c * 32);
+#pragma unroll
+          for (int g = 0; g < 8; ++g) dst[g] = make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
         }
       }
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (ready) {
+        constexpr int kC4 = kRedHalf / 4;
+        for (int e = threadIdx.x - 64; e < r * kC4; e += 128) {
+          const int j = e / kC4, c = e - j * kC4;
+          const int64_t nb = (int64_t)n0 + h * kRedHalf + 4 * c;
+          if (nb + 4 <= p.N) {
+            const float4 hi = *reinterpret_cast<const float4*>(buf + j * kRedLdb + 4 * c);
+            const float4 lo = *reinterpret_cast<const float4*>(buf + (r + j) * kRedLdb + 4 * c);
+            *reinterpret_cast<float4*>(part + (int64_t)j * p.N + nb) =
+                make_float4(hi.x + lo.x, hi.y + lo.y, hi.z + lo.z, hi.w + lo.w);
+          }
+        }
+      }
+      asm volatile("bar.sync 1, 128;" ::: "memory");   // the staging rows are reused next pass
     }
     fence_before();
   }
@@ -301,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_red(const __grid_constant__ 
   }
 }
 
-// dst_slot += sum over the slot's items (in item order) of hi + lo partial rows:
+// dst_slot += sum over the slot's items (in item order) of their partial rows:
 // transposed == 0: dst[j * N + n] (dA [r, N]); transposed == 1: dst[n * r + j] (dB [N, r]).
 constexpr int kRedFinishMaxItems = 1024;   // items of one slot held in shared memory per pass
 __global__ void k_red_finish(const float* __restrict__ part, const TokenItem* __restrict__ items,
@@ -328,32 +395,31 @@ __global__ void k_red_finish(const float* __restrict__ part, const TokenItem* __
   __syncthreads();
   const int32_t nm = n_mine;
   if (nm == 0) return;
-  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
-       e += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t j = e / N, n = e - j * N;
+  const int Ni = (int)N;   // N < 2^24 and r <= 64, so the element index fits 32 bits
+  for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < (int)total; e += gridDim.x * blockDim.x) {
+    const int64_t j = e / Ni, n = e - j * Ni;
     float acc = 0.f;
     if (nm <= kRedFinishMaxItems) {
       int32_t k = 0;
       for (; k + 4 <= nm; k += 4) {   // four items' loads in flight, added in item order
-        float v[8];
+        float v[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const float* pr = part + (int64_t)mine[k + u] * rstride * N;
-          v[2 * u] = pr[j * N + n];
-          v[2 * u + 1] = pr[(j + r) * N + n];
+          v[u] = pr[j * N + n];
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) acc += v[2 * u] + v[2 * u + 1];
+        for (int u = 0; u < 4; ++u) acc += v[u];
       }
       for (; k < nm; ++k) {
         const float* pr = part + (int64_t)mine[k] * rstride * N;
-        acc += pr[j * N + n] + pr[(j + r) * N + n];
+        acc += pr[j * N + n];
       }
     } else {   // more items than the list holds: scan the table, same order
       for (int32_t i = 0; i < ni; ++i) {
         if (items ? items[i].slot != slot : slot != 0) continue;
         const float* pr = part + (int64_t)i * rstride * N;
-        acc += pr[j * N + n] + pr[(j + r) * N + n];
+        acc += pr[j * N + n];
       }
     }
     if (transposed)
@@ -394,23 +460,33 @@ __global__ void k_split(const SplitTab tab) {
 
 // Transposed split of H / G rows per slot region: for token t of an item with slot s and j < r_s,
 // dst[region_s + j][t] = hi(src[t, j]), dst[region_s + r_s + j][t] = lo(src[t, j]).
-__global__ void k_split_rows_t(const float* __restrict__ src, int64_t lds, int64_t ldt,
-                               const TokenItem* __restrict__ items, const int32_t* __restrict__ n_items,
-                               const SlotInfo si, uint16_t* __restrict__ dst, int64_t T) {
+__global__ void __launch_bounds__(256) k_split_rows_t(const float* __restrict__ src, int64_t lds,
+                                                      int64_t ldt, const TokenItem* __restrict__ items,
+                                                      const int32_t* __restrict__ n_items,
+                                                      const SlotInfo si, uint16_t* __restrict__ dst,
+                                                      int64_t T) {
+  // the item's [n, r] block of src staged through shared memory: read along rows, written along
+  // tokens, so that both sides are coalesced
+  __shared__ float tile[kBM][LORA_MAX_RANK + 1];
   TokenItem it;
   if (!get_item(items, n_items, blockIdx.x, T, it)) return;
   if (it.slot < 0) return;
   const int32_t r = si.rank[it.slot];
   uint16_t* d = dst + (int64_t)si.region[it.slot] * ldt;
   const int n = it.t1 - it.t0;
-  for (int j = 0; j < r; ++j)
-    for (int i = threadIdx.x; i < n; i += blockDim.x) {
-      const int64_t t = it.t0 + i;
-      const float x = src[t * lds + j];
-      const uint16_t hb = bf16_bits(x);
-      d[(int64_t)j * ldt + t] = hb;
-      d[(int64_t)(r + j) * ldt + t] = bf16_bits(x - bf16_val(hb));
-    }
+  for (int e = threadIdx.x; e < n * r; e += blockDim.x) {
+    const int i = e / r, j = e - i * r;
+    tile[i][j] = src[(int64_t)(it.t0 + i) * lds + j];
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < n * r; e += blockDim.x) {
+    const int j = e / n, i = e - j * n;
+    const float x = tile[i][j];
+    const uint16_t hb = bf16_bits(x);
+    const int64_t t = it.t0 + i;
+    d[(int64_t)j * ldt + t] = hb;
+    d[(int64_t)(r + j) * ldt + t] = bf16_bits(x - bf16_val(hb));
+  }
 }
 
 // Reduction work items: for every slot, the absolute 64-token blocks that hold any of its tokens
@@ -505,12 +581,19 @@ cudaError_t launch_tc_rows(const TcRowsArgs& a, cudaStream_t st, int prof_kind) 
     if (!tc::make_map_2d(&prm.ts[k], a.s[k], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.K,
                          2 * (uint64_t)a.rank[k], a.K, 64, (uint32_t)NP))
       return cudaErrorInvalidValue;
+  for (int k = 0; k < a.n_slots; ++k) {
+    if (2 * a.rank[k] > NP || a.rank[k] > a.ldo || a.rank[k] % 4) return cudaErrorInvalidValue;
+    prm.rank[k] = a.rank[k];
+  }
+  if (a.splits < 1 || a.splits > kMaxSplitsRows || a.ldo % 4 || a.ldo > LORA_MAX_RANK)
+    return cudaErrorInvalidValue;
   prm.items = a.items;
   prm.n_items = a.n_items;
   prm.err = tc::error_word();
   if (!prm.err) return cudaErrorInvalidDevice;
   prm.nk = (int32_t)((a.K + 63) / 64);
   prm.nk_per_split = (prm.nk + a.splits - 1) / a.splits;
+  prm.ldp = (int32_t)a.ldo;
   prm.part = a.part;
   prm.T = a.T;
   dim3 grid((unsigned)a.max_items, (unsigned)a.splits);
@@ -538,9 +621,13 @@ cudaError_t launch_tc_rows(const TcRowsArgs& a, cudaStream_t st, int prof_kind) 
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  if (a.outT && a.items) {   // tokens of other slots read as zero in each slot's rows
+    e = cudaMemsetAsync(a.outT, 0, a.outT_bytes, st);
+    if (e != cudaSuccess) return e;
+  }
   prof_begin(0, st);
   k_rows_finish<<<dim3((unsigned)a.max_items, (unsigned)(kBM / kFinishTok)), 256, 0, st>>>(
-      a.part, a.splits, a.T, NP, a.items, a.n_items, a.si, a.out, a.ldo);
+      a.part, a.splits, a.T, (int32_t)a.ldo, a.items, a.n_items, a.si, a.out, a.ldo, a.outT, a.ldt);
   prof_end(prof_kind, st);   // the class's time spans the product and its split-K finish
   return cudaGetLastError();
 }
@@ -554,7 +641,7 @@ cudaError_t launch_tc_red(const TcRedArgs& a, cudaStream_t st, int prof_kind) {
     if (!tc::make_map_2d(&prm.tst[k], a.st[k], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T,
                          2 * (uint64_t)a.rank[k], a.ldt, 64, kBM))
       return cudaErrorInvalidValue;
-    prm.rows2[k] = 2 * a.rank[k];
+    prm.rank[k] = a.rank[k];
   }
   if (!tc::make_map_2d(&prm.tb, a.b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.N, a.T, a.N, 64, 64))
     return cudaErrorInvalidValue;
@@ -566,7 +653,7 @@ cudaError_t launch_tc_red(const TcRedArgs& a, cudaStream_t st, int prof_kind) {
   prm.N = a.N;
   prm.T = a.T;
   prm.span = a.span_tokens;
-  prm.rstride = 2 * a.max_rank;
+  prm.rstride = a.max_rank;
   static bool attr = false;
   if (!attr) {
     cudaError_t e = set_smem(k_tc_red, kRedSmem);
@@ -583,7 +670,7 @@ cudaError_t launch_tc_red(const TcRedArgs& a, cudaStream_t st, int prof_kind) {
   if (blocks > 8192) blocks = 8192;
   prof_begin(0, st);
   k_red_finish<<<dim3((unsigned)blocks, (unsigned)a.n_slots), 256, 0, st>>>(
-      a.part, a.items, a.n_items, a.N, 2 * a.max_rank, a.transposed, a.tab, a.T, a.span_tokens);
+      a.part, a.items, a.n_items, a.N, a.max_rank, a.transposed, a.tab, a.T, a.span_tokens);
   prof_end(prof_kind, st);   // the class's time spans the product and its item reduction
   return cudaGetLastError();
 }
@@ -610,7 +697,7 @@ cudaError_t launch_split_rows_t(const float* src, int64_t lds, int64_t ldt, cons
     if (e != cudaSuccess) return e;
   }
   prof_begin(0, st);
-  k_split_rows_t<<<(unsigned)max_items, 128, 0, st>>>(src, lds, ldt, items, n_items, si, dst, T);
+  k_split_rows_t<<<(unsigned)max_items, 256, 0, st>>>(src, lds, ldt, items, n_items, si, dst, T);
   return cudaGetLastError();
 }
 
