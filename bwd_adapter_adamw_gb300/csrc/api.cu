@@ -243,9 +243,9 @@ Layout carve(const lora_desc* d, int64_t T, int32_t n_seg, int n_slots, int64_t 
       L.max_db = red_items_bound(T, n_seg, n_slots, L.span_db);
       L.max_da = red_items_bound(T, n_seg, n_slots, L.span_da);
       L.items_db = c.take<TokenItem>((size_t)L.max_db);
-      L.count_db = c.take<int32_t>(4);
+      L.count_db = c.take<int32_t>(LORA_MAX_SLOTS + 8);   // total, then per-slot item ranges
       L.items_da = c.take<TokenItem>((size_t)L.max_da);
-      L.count_da = c.take<int32_t>(4);
+      L.count_da = c.take<int32_t>(LORA_MAX_SLOTS + 8);
       const int64_t a = L.max_db * d->out_dim, b = L.max_da * d->in_dim;
       L.red_part = c.take<float>((size_t)(a > b ? a : b) * d->rank);
     } else {

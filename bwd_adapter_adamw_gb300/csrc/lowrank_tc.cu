@@ -181,47 +181,69 @@ __global__ void __launch_bounds__(kThreads, 2) k_tc_rows(const __grid_constant__
   }
 }
 
-// out[t, j] = alpha_slot * sum_z part[z][t][j] for j < r, 0 for r <= j < ldo. With outT, also the
-// transposed bf16 split that the token reductions take as their K-major operand:
+// out[t, j] = alpha_slot * sum_z part[z][t][j] for j < r, 0 for r <= j < ldp (alpha_slot = 1
+// when use_alpha is 0; out may be null). With outT, also the transposed bf16 split that the token
+// reductions take as their K-major operand:
 // outT[region_slot + j][t] = hi(out[t, j]), outT[region_slot + r + j][t] = lo(out[t, j]).
-// CTA (item, blockIdx.y) covers kFinishTok tokens of the item.
+// CTA (item, blockIdx.y) covers kFinishTok tokens of the item; every thread issues all of its
+// loads (kFinishVec float4 groups x the splits) before the first add.
 constexpr int kFinishTok = 32;
+constexpr int kFinishThreads = 256;
+constexpr int kFinishVec = kFinishTok * LORA_MAX_RANK / 4 / kFinishThreads;
 constexpr int kMaxSplitsRows = 8;   // K splits of the rows kernel (the launcher rejects more)
-__global__ void __launch_bounds__(256) k_rows_finish(
-    const float* __restrict__ part, int32_t splits, int64_t T, int32_t ldp,
+__global__ void __launch_bounds__(kFinishThreads) k_rows_finish(
+    const float* __restrict__ part, int32_t splits, int64_t T, int32_t ldp, int use_alpha,
     const TokenItem* __restrict__ items, const int32_t* __restrict__ n_items, const SlotInfo si,
-    float* __restrict__ out, int64_t ldo, uint16_t* __restrict__ outT, int64_t ldt) {
+    float* __restrict__ out, uint16_t* __restrict__ outT, int64_t ldt) {
   __shared__ float tile[kFinishTok][LORA_MAX_RANK + 1];
   TokenItem it;
   if (!get_item(items, n_items, blockIdx.x, T, it)) return;
   const int64_t tb = (int64_t)it.t0 + (int64_t)blockIdx.y * kFinishTok;
   if (tb >= it.t1) return;
   const int32_t r = it.slot >= 0 ? si.rank[it.slot] : 0;
-  const float alpha = it.slot >= 0 ? si.alpha[it.slot] : 0.f;
-  const int ld = (int)ldo;
+  const float alpha = !use_alpha ? 1.f : it.slot >= 0 ? si.alpha[it.slot] : 0.f;
   const int nt = (int)min((int64_t)kFinishTok, (int64_t)it.t1 - tb);
-  for (int e = threadIdx.x; e < nt * ld; e += blockDim.x) {
-    const int i = e / ld, j = e - i * ld;
-    const int64_t t = tb + i;
-    float v = 0.f;
-    if (j < r) {
-      // every split's partial loaded first (independent loads in flight), then added in order
-      float pz[kMaxSplitsRows];
+  const int c4n = ldp / 4;
+  const int n4 = nt * c4n;
+  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 pz[kFinishVec][kMaxSplitsRows];
+#pragma unroll
+  for (int u = 0; u < kFinishVec; ++u) {
+    const int q = threadIdx.x + u * kFinishThreads;
+    const int i = q / c4n, c = q - i * c4n;
+    const bool live = q < n4 && 4 * c < r;
+    const float4* src = reinterpret_cast<const float4*>(part + (tb + i) * ldp) + c;
+#pragma unroll
+    for (int z = 0; z < kMaxSplitsRows; ++z)
+      pz[u][z] = (live && z < splits) ? src[(int64_t)z * T * c4n] : zero;
+  }
+#pragma unroll
+  for (int u = 0; u < kFinishVec; ++u) {
+    const int q = threadIdx.x + u * kFinishThreads;
+    if (q >= n4) continue;
+    const int i = q / c4n, c = q - i * c4n;
+    float4 v = zero;
+    if (4 * c < r) {
 #pragma unroll
       for (int z = 0; z < kMaxSplitsRows; ++z)
-        pz[z] = z < splits ? part[((int64_t)z * T + t) * ldp + j] : 0.f;
-#pragma unroll
-      for (int z = 0; z < kMaxSplitsRows; ++z)
-        if (z < splits) v += pz[z];
-      v *= alpha;
-      tile[i][j] = v;
+        if (z < splits) {
+          v.x += pz[u][z].x;
+          v.y += pz[u][z].y;
+          v.z += pz[u][z].z;
+          v.w += pz[u][z].w;
+        }
+      v = make_float4(v.x * alpha, v.y * alpha, v.z * alpha, v.w * alpha);
+      tile[i][4 * c] = v.x;
+      tile[i][4 * c + 1] = v.y;
+      tile[i][4 * c + 2] = v.z;
+      tile[i][4 * c + 3] = v.w;
     }
-    out[t * ldo + j] = v;
+    if (out) reinterpret_cast<float4*>(out + (tb + i) * ldp)[c] = v;
   }
   if (!outT || it.slot < 0) return;   // uniform over the CTA
   __syncthreads();
   uint16_t* d = outT + (int64_t)si.region[it.slot] * ldt + tb;
-  for (int e = threadIdx.x; e < nt * r; e += blockDim.x) {
+  for (int e = threadIdx.x; e < nt * r; e += kFinishThreads) {
     const int j = e / nt, i = e - j * nt;
     const float x = tile[i][j];
     const uint16_t hb = bf16_bits(x);
@@ -370,62 +392,93 @@ __global__ void __launch_bounds__(kThreads, 2) k_tc_red(const __grid_constant__ 
 
 // dst_slot += sum over the slot's items (in item order) of their partial rows:
 // transposed == 0: dst[j * N + n] (dA [r, N]); transposed == 1: dst[n * r + j] (dB [N, r]).
-constexpr int kRedFinishMaxItems = 1024;   // items of one slot held in shared memory per pass
-__global__ void k_red_finish(const float* __restrict__ part, const TokenItem* __restrict__ items,
-                             const int32_t* __restrict__ n_items, int64_t N, int32_t rstride,
-                             int transposed, const ReduceTab tab, int64_t T, int64_t span) {
-  __shared__ int32_t mine[kRedFinishMaxItems];
-  __shared__ int32_t n_mine;
+// The slot's items are contiguous in the table, from counts[1 + slot] to counts[2 + slot] (a null
+// table is the uniform runs of a single-adapter call, all of slot 0). CTA (blockIdx.x, slot)
+// covers kRedFinCols columns; each thread holds kRedFinVec float4 groups and loads four items'
+// partials before adding them.
+constexpr int kRedFinCols = 32;
+constexpr int kRedFinC4 = kRedFinCols / 4;
+constexpr int kRedFinVec = LORA_MAX_RANK * kRedFinC4 / kFinishThreads;
+__global__ void __launch_bounds__(kFinishThreads) k_red_finish(
+    const float* __restrict__ part, const TokenItem* __restrict__ items,
+    const int32_t* __restrict__ counts, int64_t N, int32_t rstride, int transposed,
+    const ReduceTab tab, int64_t T, int64_t span) {
+  __shared__ float tile[kRedFinCols][LORA_MAX_RANK + 1];
   const int slot = blockIdx.y;
   const int32_t r = tab.rank[slot];
   float* dst = tab.out[slot];
-  const int32_t ni = items ? *n_items : (int32_t)((T + span - 1) / span);
-  const int64_t total = (int64_t)r * N;
-  // this slot's items, in item order (the summation order); a null table is the uniform runs of
-  // a single-adapter call, all of slot 0
-  if (threadIdx.x == 0) {
-    int32_t c = 0;
-    for (int32_t i = 0; i < ni; ++i)
-      if (items ? items[i].slot == slot : slot == 0) {
-        if (c < kRedFinishMaxItems) mine[c] = i;
-        ++c;
-      }
-    n_mine = c;
+  int32_t i0 = 0, i1 = 0;
+  if (items) {
+    i0 = counts[1 + slot];
+    i1 = counts[2 + slot];
+  } else if (slot == 0) {
+    i1 = (int32_t)((T + span - 1) / span);
+  }
+  if (i1 <= i0) return;
+  const int64_t n0 = (int64_t)blockIdx.x * kRedFinCols;
+  const int nc = (int)min((int64_t)kRedFinCols, N - n0);
+  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 acc[kRedFinVec];
+  int64_t off[kRedFinVec];
+  bool live[kRedFinVec];
+#pragma unroll
+  for (int u = 0; u < kRedFinVec; ++u) {
+    const int q = threadIdx.x + u * kFinishThreads;
+    const int j = q / kRedFinC4, c = q - j * kRedFinC4;
+    live[u] = j < r && 4 * c < nc;
+    off[u] = (int64_t)j * N + n0 + 4 * c;
+    acc[u] = zero;
+  }
+  const int64_t istride = (int64_t)rstride * N;
+  for (int32_t i = i0; i < i1; i += 4) {
+    float4 v[4][kRedFinVec];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+#pragma unroll
+      for (int u = 0; u < kRedFinVec; ++u)
+        v[k][u] = (live[u] && i + k < i1)
+                      ? *reinterpret_cast<const float4*>(part + (int64_t)(i + k) * istride + off[u])
+                      : zero;
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+#pragma unroll
+      for (int u = 0; u < kRedFinVec; ++u)
+        if (i + k < i1) {
+          acc[u].x += v[k][u].x;
+          acc[u].y += v[k][u].y;
+          acc[u].z += v[k][u].z;
+          acc[u].w += v[k][u].w;
+        }
+  }
+  if (!transposed) {
+#pragma unroll
+    for (int u = 0; u < kRedFinVec; ++u) {
+      if (!live[u]) continue;
+      float4* p = reinterpret_cast<float4*>(dst + off[u]);
+      float4 d = *p;
+      d.x += acc[u].x;
+      d.y += acc[u].y;
+      d.z += acc[u].z;
+      d.w += acc[u].w;
+      *p = d;
+    }
+    return;
+  }
+  // dB [N, r]: through shared memory so that the row-major writes are coalesced
+#pragma unroll
+  for (int u = 0; u < kRedFinVec; ++u) {
+    if (!live[u]) continue;
+    const int q = threadIdx.x + u * kFinishThreads;
+    const int j = q / kRedFinC4, c = q - j * kRedFinC4;
+    tile[4 * c][j] = acc[u].x;
+    tile[4 * c + 1][j] = acc[u].y;
+    tile[4 * c + 2][j] = acc[u].z;
+    tile[4 * c + 3][j] = acc[u].w;
   }
   __syncthreads();
-  const int32_t nm = n_mine;
-  if (nm == 0) return;
-  const int Ni = (int)N;   // N < 2^24 and r <= 64, so the element index fits 32 bits
-  for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < (int)total; e += gridDim.x * blockDim.x) {
-    const int64_t j = e / Ni, n = e - j * Ni;
-    float acc = 0.f;
-    if (nm <= kRedFinishMaxItems) {
-      int32_t k = 0;
-      for (; k + 4 <= nm; k += 4) {   // four items' loads in flight, added in item order
-        float v[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const float* pr = part + (int64_t)mine[k + u] * rstride * N;
-          v[u] = pr[j * N + n];
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) acc += v[u];
-      }
-      for (; k < nm; ++k) {
-        const float* pr = part + (int64_t)mine[k] * rstride * N;
-        acc += pr[j * N + n];
-      }
-    } else {   // more items than the list holds: scan the table, same order
-      for (int32_t i = 0; i < ni; ++i) {
-        if (items ? items[i].slot != slot : slot != 0) continue;
-        const float* pr = part + (int64_t)i * rstride * N;
-        acc += pr[j * N + n];
-      }
-    }
-    if (transposed)
-      dst[n * r + j] += acc;
-    else
-      dst[j * N + n] += acc;
+  for (int e = threadIdx.x; e < nc * r; e += kFinishThreads) {
+    const int n = e / r, j = e - n * r;
+    dst[(n0 + n) * r + j] += tile[n][j];
   }
 }
 
@@ -455,37 +508,6 @@ __global__ void k_split(const SplitTab tab) {
     const uint16_t hb = bf16_bits(x);
     dst[j * K + k] = hb;
     dst[(r + j) * K + k] = bf16_bits(x - bf16_val(hb));
-  }
-}
-
-// Transposed split of H / G rows per slot region: for token t of an item with slot s and j < r_s,
-// dst[region_s + j][t] = hi(src[t, j]), dst[region_s + r_s + j][t] = lo(src[t, j]).
-__global__ void __launch_bounds__(256) k_split_rows_t(const float* __restrict__ src, int64_t lds,
-                                                      int64_t ldt, const TokenItem* __restrict__ items,
-                                                      const int32_t* __restrict__ n_items,
-                                                      const SlotInfo si, uint16_t* __restrict__ dst,
-                                                      int64_t T) {
-  // the item's [n, r] block of src staged through shared memory: read along rows, written along
-  // tokens, so that both sides are coalesced
-  __shared__ float tile[kBM][LORA_MAX_RANK + 1];
-  TokenItem it;
-  if (!get_item(items, n_items, blockIdx.x, T, it)) return;
-  if (it.slot < 0) return;
-  const int32_t r = si.rank[it.slot];
-  uint16_t* d = dst + (int64_t)si.region[it.slot] * ldt;
-  const int n = it.t1 - it.t0;
-  for (int e = threadIdx.x; e < n * r; e += blockDim.x) {
-    const int i = e / r, j = e - i * r;
-    tile[i][j] = src[(int64_t)(it.t0 + i) * lds + j];
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e < n * r; e += blockDim.x) {
-    const int j = e / n, i = e - j * n;
-    const float x = tile[i][j];
-    const uint16_t hb = bf16_bits(x);
-    const int64_t t = it.t0 + i;
-    d[(int64_t)j * ldt + t] = hb;
-    d[(int64_t)(r + j) * ldt + t] = bf16_bits(x - bf16_val(hb));
   }
 }
 
@@ -544,6 +566,7 @@ __global__ void k_make_red_items_tc(int64_t T, int32_t n_seg, const int32_t* __r
     s_count[0] = 0;
     for (int k = 1; k <= n_slots; ++k) s_count[k] += s_count[k - 1];
     *count = min(s_count[n_slots], max_items);
+    for (int k = 0; k <= n_slots; ++k) count[1 + k] = min(s_count[k], max_items);   // slot ranges
   }
   __syncthreads();
   if (s < n_slots) walk(true, s_count[s]);
@@ -626,8 +649,8 @@ cudaError_t launch_tc_rows(const TcRowsArgs& a, cudaStream_t st, int prof_kind) 
     if (e != cudaSuccess) return e;
   }
   prof_begin(0, st);
-  k_rows_finish<<<dim3((unsigned)a.max_items, (unsigned)(kBM / kFinishTok)), 256, 0, st>>>(
-      a.part, a.splits, a.T, (int32_t)a.ldo, a.items, a.n_items, a.si, a.out, a.ldo, a.outT, a.ldt);
+  k_rows_finish<<<dim3((unsigned)a.max_items, (unsigned)(kBM / kFinishTok)), kFinishThreads, 0, st>>>(
+      a.part, a.splits, a.T, (int32_t)a.ldo, 1, a.items, a.n_items, a.si, a.out, a.outT, a.ldt);
   prof_end(prof_kind, st);   // the class's time spans the product and its split-K finish
   return cudaGetLastError();
 }
@@ -665,11 +688,9 @@ cudaError_t launch_tc_red(const TcRedArgs& a, cudaStream_t st, int prof_kind) {
   k_tc_red<<<grid, kThreads, kRedSmem, st>>>(prm);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  int64_t total = (int64_t)a.max_rank * a.N;
-  int64_t blocks = (total + 255) / 256;
-  if (blocks > 8192) blocks = 8192;
+  const int64_t blocks = (a.N + kRedFinCols - 1) / kRedFinCols;
   prof_begin(0, st);
-  k_red_finish<<<dim3((unsigned)blocks, (unsigned)a.n_slots), 256, 0, st>>>(
+  k_red_finish<<<dim3((unsigned)blocks, (unsigned)a.n_slots), kFinishThreads, 0, st>>>(
       a.part, a.items, a.n_items, a.N, a.max_rank, a.transposed, a.tab, a.T, a.span_tokens);
   prof_end(prof_kind, st);   // the class's time spans the product and its item reduction
   return cudaGetLastError();
@@ -696,8 +717,10 @@ cudaError_t launch_split_rows_t(const float* src, int64_t lds, int64_t ldt, cons
     cudaError_t e = cudaMemsetAsync(dst, 0, dst_bytes, st);
     if (e != cudaSuccess) return e;
   }
+  if (lds % 4 || lds > LORA_MAX_RANK) return cudaErrorInvalidValue;
   prof_begin(0, st);
-  k_split_rows_t<<<(unsigned)max_items, 256, 0, st>>>(src, lds, ldt, items, n_items, si, dst, T);
+  k_rows_finish<<<dim3((unsigned)max_items, (unsigned)(kBM / kFinishTok)), kFinishThreads, 0, st>>>(
+      src, 1, T, (int32_t)lds, 0, items, n_items, si, nullptr, dst, ldt);
   return cudaGetLastError();
 }
 
