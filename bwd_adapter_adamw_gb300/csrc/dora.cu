@@ -14,6 +14,7 @@ __global__ void __launch_bounds__(256) k_dora_norm(const T* __restrict__ W, cons
                                                    const float* __restrict__ B, float s,
                                                    int64_t out_dim, int64_t in_dim, int32_t rank,
                                                    float* __restrict__ norm_out) {
+  grid_dep_sync();
   constexpr int R = 4;
   __shared__ float sb[R][LORA_MAX_RANK];
   __shared__ double red[R][8];
@@ -65,6 +66,7 @@ __global__ void __launch_bounds__(256) k_dora_norm(const T* __restrict__ W, cons
 // C[j, k] for k in [8 blockIdx.y, 8 blockIdx.y + 8): 256 threads stride over the input columns.
 __global__ void __launch_bounds__(256) k_dora_gram(const float* __restrict__ A, int64_t in_dim,
                                                    int32_t rank, float* __restrict__ C) {
+  grid_dep_sync();
   __shared__ float red[8][8];
   const int j = blockIdx.x, k0 = blockIdx.y * 8;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -97,6 +99,7 @@ __global__ void __launch_bounds__(256) k_dora_combine(const __nv_bfloat16* __res
                                                       const float* __restrict__ C, float s,
                                                       int64_t out_dim, int64_t in_dim, int32_t rank,
                                                       float* __restrict__ norm_out) {
+  grid_dep_sync();
   __shared__ float sC[LORA_MAX_RANK * LORA_MAX_RANK];
   for (int e = threadIdx.x; e < rank * rank; e += 256) sC[e] = C[e];
   __syncthreads();
@@ -153,6 +156,7 @@ template <typename T>
 __global__ void __launch_bounds__(256) k_dora_dm(const T* __restrict__ dY, const T* __restrict__ Y,
                                                  const float* __restrict__ mag, int64_t Tn,
                                                  int64_t out_dim, float* __restrict__ dm) {
+  grid_dep_sync();
   constexpr int V = Vec<T>::N;
   constexpr int kCols = 32 * V;
   __shared__ float red[8][kCols];
@@ -218,9 +222,9 @@ cudaError_t launch_dora_norm(int dtype, const void* W, const float* A, const flo
                              cudaStream_t st) {
   const unsigned blocks = (unsigned)((out_dim + 3) / 4);
   if (dtype == LORA_F32)
-    { prof_begin(0, st); k_dora_norm<float><<<blocks, 256, 0, st>>>((const float*)W, A, B, s, out_dim, in_dim, rank, norm_out); }
+    { prof_begin(0, st); launch_kernel(k_dora_norm<float>, blocks, 256, 0, st, (const float*)W, A, B, s, out_dim, in_dim, rank, norm_out); }
   else
-    { prof_begin(0, st); k_dora_norm<__nv_bfloat16><<<blocks, 256, 0, st>>>((const __nv_bfloat16*)W, A, B, s, out_dim,
+    { prof_begin(0, st); launch_kernel(k_dora_norm<__nv_bfloat16>, blocks, 256, 0, st, (const __nv_bfloat16*)W, A, B, s, out_dim,
                                                        in_dim, rank, norm_out); }
   return cudaGetLastError();
 }
@@ -229,11 +233,11 @@ cudaError_t launch_dora_gram_combine(const void* W, const float* H, const float*
                                      float s, int64_t out_dim, int64_t in_dim, int32_t rank,
                                      float* C, float* norm_out, cudaStream_t st) {
   prof_begin(0, st);
-  k_dora_gram<<<dim3((unsigned)rank, (unsigned)((rank + 7) / 8)), 256, 0, st>>>(A, in_dim, rank, C);
+  launch_kernel(k_dora_gram, dim3((unsigned)rank, (unsigned)((rank + 7) / 8)), 256, 0, st, A, in_dim, rank, C);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   prof_begin(0, st);
-  k_dora_combine<<<(unsigned)((out_dim + 7) / 8), 256, 0, st>>>(
+  launch_kernel(k_dora_combine, (unsigned)((out_dim + 7) / 8), 256, 0, st, 
       (const __nv_bfloat16*)W, H, B, C, s, out_dim, in_dim, rank, norm_out);
   return cudaGetLastError();
 }
@@ -246,13 +250,13 @@ cudaError_t launch_dora_dm(int dtype, const void* dY, const void* Y, const float
   cfg.gridDim = dim3((unsigned)((out_dim + cols - 1) / cols), (unsigned)kDmGroups);
   cfg.blockDim = dim3(256);
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 1;
   attr[0].val.clusterDim.y = kDmGroups;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = add_pdl_attr(attr, 1);
   prof_begin(0, st);
   cudaError_t e = dtype == LORA_F32
                       ? cudaLaunchKernelEx(&cfg, k_dora_dm<float>, (const float*)dY, (const float*)Y,

@@ -48,11 +48,7 @@ namespace {
 using namespace tc;
 
 constexpr int kBM = 128;
-constexpr int kBN = 256;
-constexpr int kStages = 4;
 constexpr int kABytes = kBM * 128;   // 16 KB: 128 rows x 128 bytes
-constexpr int kBBytes = kBN * 128;   // 32 KB
-constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
 // Items per tile group (rasterization for L2 reuse): 16 when W spans more than 16 N tiles; with
@@ -60,15 +56,27 @@ constexpr int kEpiThreads = 128;
 // together. Measured at T 8192 (us): N 4096 / K 4096: 152 (N fastest), 152 (8), 162 (16);
 // N 14336 / K 4096: 688, 585, 550; N 4096 / K 14336: 542, 566, 557.
 constexpr int kGroupWide = 16;
-constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*barriers*/ + 1024 /*alignment*/;
-constexpr uint32_t kIdescBF16 = tc::idesc(tc::kFmtBF16, kBM, kBN);
-constexpr uint32_t kIdescTF32 = tc::idesc(tc::kFmtTF32, kBM, kBN);
+
+// Tile 128 x BN. BN = 256 is the fastest MMA shape per flop; 224 and 192 (the same kernel with
+// narrower B tiles and accumulators) let the host trade a little MMA rate for fewer idle SMs in
+// the last round of tiles.
+template <int BN>
+struct GemmCfg {
+  static_assert(BN % 32 == 0 && BN >= 128 && BN <= 256, "tile width");
+  static constexpr int kBBytes = BN * 128;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = (200 * 1024 / kStageBytes) < 6 ? (200 * 1024 / kStageBytes) : 6;
+  static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*barriers*/ + 1024 /*alignment*/;
+  static constexpr uint32_t kIdescBF16 = tc::idesc(tc::kFmtBF16, kBM, BN);
+  static constexpr uint32_t kIdescTF32 = tc::idesc(tc::kFmtTF32, kBM, BN);
+  static_assert(kStageBytes % 1024 == 0, "stage alignment of the 128-byte swizzle");
+};
 
 struct TcParams {
   CUtensorMap ta;                       // A [rows, K] bf16, box {64, 128}
-  CUtensorMap tb;                       // B [N, K] bf16, box {64, 256}
+  CUtensorMap tb;                       // B [N, K] bf16, box {64, BN}
   CUtensorMap tp;                       // P [T, ldp] fp32, box {32, 128}
-  CUtensorMap tq[LORA_MAX_SLOTS];       // Q_slot [N, r] fp32, box {32, 256}
+  CUtensorMap tq[LORA_MAX_SLOTS];       // Q_slot [N, r] fp32, box {32, BN}
   const TokenItem* items;               // null: uniform 128-token tiles, slot 0
   const int32_t* n_items;
   int64_t T;
@@ -97,17 +105,23 @@ struct TcParams {
 // 256-column TMEM accumulators alternate between tiles, so that the epilogue of one tile drains
 // and stores while the MMAs of the next run. With a dropout-masked LoRA term the second 256
 // columns hold that term instead, and tiles take turns on one accumulator.
+template <int BN>
 __device__ __forceinline__ bool decode_tile(const TcParams& p, int t, TokenItem& it, int32_t& n0) {
   const int per_group = p.group_m * p.n_tiles;
   const int group = t / per_group;
   const int first = group * p.group_m;
   const int gsize = min(p.group_m, p.max_items - first);
   const int idx = t - group * per_group;
-  n0 = (idx / gsize) * kBN;
+  n0 = (idx / gsize) * BN;
   return get_item(p.items, p.n_items, first + idx % gsize, p.T, it);
 }
 
+template <int BN>
 __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__ TcParams p) {
+  grid_dep_sync();
+  using C = GemmCfg<BN>;
+  constexpr int kStages = C::kStages;
+  constexpr int kStageBytes = C::kStageBytes;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* tiles = base;
@@ -147,7 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
       for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
         TokenItem it;
         int32_t n0;
-        if (!decode_tile(p, t, it, n0)) continue;
+        if (!decode_tile<BN>(p, t, it, n0)) continue;
         const int slot = it.slot;
         const int nk = p.nk_main + ((p.has_lora && slot >= 0) ? (p.q_rank[slot] + 31) / 32 : 0);
         for (int kb = 0; kb < nk; ++kb, ++g) {
@@ -178,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
       for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
         TokenItem it;
         int32_t n0;
-        if (!decode_tile(p, t, it, n0)) continue;
+        if (!decode_tile<BN>(p, t, it, n0)) continue;
         const int slot = it.slot;
         const int nk_lora = (p.has_lora && slot >= 0) ? (p.q_rank[slot] + 31) / 32 : 0;
         const int nk = p.nk_main + nk_lora;
@@ -198,13 +212,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
           if (kb < p.nk_main) {
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-              umma_f16(dm, da + 2 * k, db + 2 * k, kIdescBF16, (kb > 0 || k > 0) ? 1u : 0u);
+              umma_f16(dm, da + 2 * k, db + 2 * k, C::kIdescBF16, (kb > 0 || k > 0) ? 1u : 0u);
           } else {
             const uint32_t d = sep ? tmem + 256u : dm;
             const bool first = sep && kb == p.nk_main;
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-              umma_tf32(d, da + 2 * k, db + 2 * k, kIdescTF32, (first && k == 0) ? 0u : 1u);
+              umma_tf32(d, da + 2 * k, db + 2 * k, C::kIdescTF32, (first && k == 0) ? 0u : 1u);
           }
           umma_commit(&empty_bar[s]);
         }
@@ -222,28 +236,42 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
     for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
       TokenItem it;
       int32_t n0;
-      if (!decode_tile(p, t, it, n0)) continue;
+      if (!decode_tile<BN>(p, t, it, n0)) continue;
       const int slot = it.slot;
       const bool sep = p.lora_separate && p.has_lora && slot >= 0 && p.q_rank[slot] > 0;
       const int b = j % nbuf, use = j / nbuf;
       const int64_t m = (int64_t)it.t0 + row;
       const bool row_ok = m < it.t1;
+      // dropout keep bits of this row's BN columns, evaluated while the tile's MMAs still run
+      uint32_t keep[BN / 32];
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) keep[c] = 0u;
+      if (sep && row_ok) {
+        const DropRow drow = drop_row(p.drop, m);
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) {
+#pragma unroll 4
+          for (int jj = 0; jj < 32; ++jj) {
+            const int64_t n = (int64_t)n0 + c * 32 + jj;
+            if (n < p.n_out && drop_keep_at(drow, p.drop.tau, n)) keep[c] |= 1u << jj;
+          }
+        }
+      }
       // warp-uniform decision: the TMEM loads below are .sync.aligned
       const bool ready = __all_sync(0xffffffffu, mbar_wait(&acc_full[b], (uint32_t)use & 1u, 4u, p.err));
       if (!ready) break;
       fence_after();
       const uint32_t acc = tmem + ((uint32_t)(q * 32) << 16) + 256u * (uint32_t)b;
-      for (int c = 0; c < kBN / 32; ++c) {
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) {
         float v[32];
         tmem_ld32(acc + (uint32_t)(c * 32), v);
         if (sep) {
           float w[32];
           tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + 256u + (uint32_t)(c * 32), w);
 #pragma unroll
-          for (int jj = 0; jj < 32; ++jj) {
-            const int64_t n = (int64_t)n0 + c * 32 + jj;
-            if (row_ok && n < p.n_out && drop_keep(p.drop, m, n)) v[jj] += w[jj];
-          }
+          for (int jj = 0; jj < 32; ++jj)
+            if ((keep[c] >> jj) & 1u) v[jj] += w[jj];
         }
         const int64_t nb = (int64_t)n0 + c * 32;
         if (p.n_colscale) {
@@ -319,13 +347,49 @@ bool make_map_2d(CUtensorMap* map, const void* ptr, CUtensorMapDataType dt, int 
 
 }  // namespace tc
 
+namespace {
+template <int BN>
+cudaError_t launch_gemm_bn(unsigned grid, cudaStream_t st, const TcParams& prm) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(k_tc_gemm<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         GemmCfg<BN>::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  return launch_kernel(k_tc_gemm<BN>, grid, kThreads, GemmCfg<BN>::kSmemBytes, st, prm);
+}
+
+// Tile width: the fewest tile-columns of MMA work per SM, rounds x BN x (relative cost of a
+// column at that width), over the persistent CTAs' rounds of tiles.
+int pick_tile_n(int64_t n_rows, int64_t items, int sms) {
+  static const int kWidths[] = {256, 224, 192};
+  static const double kColumnCost[] = {1.0, 1.10, 1.17};   // measured per-column MMA time
+  int best = 256;
+  double best_cost = 1e300;
+  for (int i = 0; i < 3; ++i) {
+    const int64_t tiles = items * ((n_rows + kWidths[i] - 1) / kWidths[i]);
+    const int64_t rounds = (tiles + sms - 1) / sms;
+    const double cost = (double)rounds * kWidths[i] * kColumnCost[i];
+    if (cost < best_cost * 0.999) {
+      best_cost = cost;
+      best = kWidths[i];
+    }
+  }
+  return best;
+}
+}  // namespace
+
 cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st, int prof_kind) {
   static TcParams prm;   // large: filled per call on the host, copied into the launch
   static std::mutex mu;
   std::lock_guard<std::mutex> lk(mu);
   std::memset(&prm, 0, sizeof(prm));
+  const int sms = tc::sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  const int bn = pick_tile_n(a.n_rows, a.max_items, sms);
   if (!tc::make_map_2d(&prm.ta, a.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.K, a.T, a.K, 64, kBM) ||
-      !tc::make_map_2d(&prm.tb, a.b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.K, a.n_rows, a.K, 64, kBN))
+      !tc::make_map_2d(&prm.tb, a.b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.K, a.n_rows, a.K, 64, bn))
     return cudaErrorInvalidValue;
   prm.has_lora = a.p != nullptr;
   if (a.p) {
@@ -334,7 +398,7 @@ cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st, int prof_kind) 
     for (int k = 0; k < a.n_slots; ++k) {
       prm.q_rank[k] = a.q_rank[k];
       if (!tc::make_map_2d(&prm.tq[k], a.q[k], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.q_rank[k], a.n_rows,
-                    a.q_rank[k], 32, kBN))
+                    a.q_rank[k], 32, bn))
         return cudaErrorInvalidValue;
     }
   }
@@ -350,25 +414,22 @@ cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st, int prof_kind) 
   prm.ldo = a.ldo;
   prm.n_out = a.n_rows;
   prm.drop = a.drop;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k_tc_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
   if (a.max_items <= 0) return cudaSuccess;
-  prm.n_tiles = (int32_t)((a.n_rows + kBN - 1) / kBN);
+  prm.n_tiles = (int32_t)((a.n_rows + bn - 1) / bn);
   prm.max_items = a.max_items;
   prm.group_m = prm.n_tiles > 16 ? kGroupWide : 1;
   const int64_t total = (int64_t)prm.n_tiles * a.max_items;
   if (total > INT32_MAX) return cudaErrorInvalidValue;
   prm.total_tiles = (int32_t)total;
-  const int sms = tc::sm_count();
-  if (sms <= 0) return cudaErrorInvalidDevice;
   const unsigned grid = (unsigned)(total < sms ? total : sms);   // one persistent CTA per SM
   prof_begin(prof_kind, st);
-  k_tc_gemm<<<grid, kThreads, kSmemBytes, st>>>(prm);
+  cudaError_t e = cudaErrorInvalidValue;
+  switch (bn) {
+    case 256: e = launch_gemm_bn<256>(grid, st, prm); break;
+    case 224: e = launch_gemm_bn<224>(grid, st, prm); break;
+    case 192: e = launch_gemm_bn<192>(grid, st, prm); break;
+  }
+  if (e != cudaSuccess) return e;
   prof_end(prof_kind, st);
   return cudaGetLastError();
 }

@@ -115,6 +115,7 @@ __device__ __forceinline__ void split_tile(uint8_t* t, int ct) {
 }
 
 __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm_f32(const __grid_constant__ F32Params p) {
+  grid_dep_sync();
   extern __shared__ uint8_t smem_raw[];
   TokenItem it;
   if (!get_item(p.items, p.n_items, blockIdx.y, p.T, it)) return;
@@ -272,6 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm_f32(const __grid_consta
       if (!ready) break;
       fence_after();
       const bool masked = sep && per == n_periods - 1;
+      const DropRow drow = masked ? drop_row(p.drop, m) : DropRow{0, 0};
       const uint32_t reg = lane_base + 256u * (uint32_t)r;
 #pragma unroll
       for (int h = 0; h < kCols / 16; ++h) {
@@ -285,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm_f32(const __grid_consta
 #pragma unroll 1
           for (int j = 0; j < 16; ++j) {
             const int64_t n = (int64_t)n0 + c0 + h * 16 + j;
-            if (row_ok && n < p.n_out && drop_keep(p.drop, m, n)) keep |= 1u << j;
+            if (row_ok && n < p.n_out && drop_keep_at(drow, p.drop.tau, n)) keep |= 1u << j;
           }
 #pragma unroll
           for (int j = 0; j < 16; ++j)
@@ -446,16 +448,16 @@ cudaError_t launch_tc_gemm_f32(const TcGemmArgs& a, cudaStream_t st, int prof_ki
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 1;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = (unsigned)prm.splits;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = add_pdl_attr(attr, 1);
     e = cudaLaunchKernelEx(&cfg, k_tc_gemm_f32, prm);
   } else {
-    k_tc_gemm_f32<<<grid, kThreads, kSmemBytes, st>>>(prm);
+    launch_kernel(k_tc_gemm_f32, grid, kThreads, kSmemBytes, st, prm);
   }
   prof_end(prof_kind, st);
   return e != cudaSuccess ? e : cudaGetLastError();

@@ -9,6 +9,17 @@
 
 namespace lora {
 
+// Programmatic dependent launch. Every kernel of the library starts with grid_dep_sync(): it waits
+// until the kernels before it in the stream have completed and their writes are visible
+// (griddepcontrol.wait), then lets the next kernel in the stream begin its launch
+// (griddepcontrol.launch_dependents). Launched with the programmatic stream serialization
+// attribute (launch_kernel), a kernel's launch and CTA dispatch overlap the tail of the kernel
+// before it; launched without it, the wait returns at once.
+__device__ __forceinline__ void grid_dep_sync() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 constexpr int kGemmTileT = 128;   // token rows per forward/dX/shrink/G work item
 constexpr int kRedTileT = 128;    // tokens per split of the CUDA-core token reductions (dA, dB)
 constexpr int kRedSub = 4;        // token groups (separate partials) per reduction item
@@ -43,6 +54,21 @@ __device__ __forceinline__ bool drop_keep(const DropParams& d, int64_t t, int64_
   const int64_t pos = t - c * d.chunk_tokens;
   const uint64_t h = mix64(d.keys[c] ^ (uint64_t)(pos * d.in_dim + i));
   return (uint32_t)(h >> 32) >= d.tau;
+}
+
+// The per-token part of the keep decision (the chunk's key and the token's element index base), for
+// loops over the columns of one token: drop_keep_at(drop_row(d, t), d.tau, i) == drop_keep(d, t, i).
+struct DropRow {
+  uint64_t key;
+  uint64_t base;
+};
+__device__ __forceinline__ DropRow drop_row(const DropParams& d, int64_t t) {
+  const int64_t c = t / d.chunk_tokens;
+  const int64_t pos = t - c * d.chunk_tokens;
+  return DropRow{d.keys[c], (uint64_t)(pos * d.in_dim)};
+}
+__device__ __forceinline__ bool drop_keep_at(const DropRow& r, uint32_t tau, int64_t i) {
+  return (uint32_t)(mix64(r.key ^ (r.base + (uint64_t)i)) >> 32) >= tau;
 }
 
 // ------------------------------------------------------------------------------------------

@@ -5,6 +5,34 @@
 
 namespace lora {
 
+// profile.cu: programmatic dependent launch switch (on unless LORA_PDL=0 is in the environment).
+bool pdl_enabled();
+
+// Appends the programmatic stream serialization attribute to attr[0 .. n) when it is enabled and
+// returns the new count. Every kernel begins with grid_dep_sync(), which makes this safe.
+inline unsigned add_pdl_attr(cudaLaunchAttribute* attr, unsigned n) {
+  if (!pdl_enabled()) return n;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  return n + 1;
+}
+
+// Kernel launch on a stream with programmatic dependent launch. Errors are also left for
+// cudaGetLastError, like a <<<>>> launch.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  cfg.attrs = attr;
+  cfg.numAttrs = add_pdl_attr(attr, 0);
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // profile.cu: launch counter and optional event brackets per kernel class (LORA_PROF_*).
 void prof_begin(int kind, cudaStream_t st);
 void prof_end(int kind, cudaStream_t st);

@@ -14,6 +14,7 @@ __global__ void k_make_items(int64_t T, int32_t n_seg, const int32_t* __restrict
                              const int32_t* __restrict__ seg_slot, int32_t n_slots,
                              TokenItem* gitems, int32_t* gcount, int32_t gmax, TokenItem* ritems,
                              int32_t* rcount, int32_t rmax) {
+  grid_dep_sync();
   __shared__ int32_t s_start[kSegSmem + 1], s_slot[kSegSmem];
   const SegView sv = stage_segments(n_seg, seg_start, seg_slot, s_start, s_slot);
   if (threadIdx.x != 0 || blockIdx.x != 0) return;
@@ -48,6 +49,7 @@ __global__ void k_make_items(int64_t T, int32_t n_seg, const int32_t* __restrict
 
 // 32 x 32 shared-memory tile transpose of fp32 matrices, one matrix per blockIdx.z.
 __global__ void k_transpose_slots(const TransposeTab tab) {
+  grid_dep_sync();
   __shared__ float tile[32][33];
   const int z = blockIdx.z;
   const int64_t rows = tab.rows[z], cols = tab.cols[z];
@@ -69,6 +71,7 @@ __global__ void k_transpose_slots(const TransposeTab tab) {
 template <typename T>
 __global__ void k_transpose_w(const T* __restrict__ src, T* __restrict__ dst, int64_t rows,
                               int64_t cols) {
+  grid_dep_sync();
   __shared__ T tile[32][33];
   const int64_t c0 = (int64_t)blockIdx.x * 32, r0 = (int64_t)blockIdx.y * 32;
   for (int i = threadIdx.y; i < 32; i += 8) {
@@ -85,6 +88,7 @@ __global__ void k_transpose_w(const T* __restrict__ src, T* __restrict__ dst, in
 // fp32 prepared weight: W [rows, cols] -> [W_hi | W_lo | W^T_hi | W^T_lo] (tf32 split, above)
 __global__ void k_prepare_w_f32(const float* __restrict__ src, float* __restrict__ dst, int64_t rows,
                                 int64_t cols) {
+  grid_dep_sync();
   __shared__ float tile[32][33];
   const int64_t n = rows * cols;
   const int64_t c0 = (int64_t)blockIdx.x * 32, r0 = (int64_t)blockIdx.y * 32;
@@ -117,6 +121,7 @@ __global__ void k_prepare_w_f32(const float* __restrict__ src, float* __restrict
 __global__ void k_reduce_parts(const float* __restrict__ part, const TokenItem* __restrict__ items,
                                const int32_t* __restrict__ n_items, int32_t sub, int64_t M,
                                int64_t ldp, int transposed, const ReduceTab tab) {
+  grid_dep_sync();
   const int slot = blockIdx.y;
   const int32_t r = tab.rank[slot];
   float* out = tab.out[slot];
@@ -141,6 +146,7 @@ __global__ void k_reduce_parts(const float* __restrict__ part, const TokenItem* 
 }
 
 __global__ void k_dropout_mask(const DropParams dp, int64_t T, int64_t in_dim, uint8_t* mask) {
+  grid_dep_sync();
   const int64_t n = T * in_dim;
   for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
        e += (int64_t)gridDim.x * blockDim.x) {
@@ -153,6 +159,7 @@ __global__ void k_dropout_mask(const DropParams dp, int64_t T, int64_t in_dim, u
 // whose column scale runs along K and so cannot be applied in the epilogue.
 __global__ void k_colscale_bf16(const __nv_bfloat16* __restrict__ src, const float* __restrict__ scale,
                                 int64_t rows, int64_t cols, __nv_bfloat16* __restrict__ dst) {
+  grid_dep_sync();
   const int64_t n8 = rows * cols / 8;
   for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < n8;
        v += (int64_t)gridDim.x * blockDim.x) {
@@ -175,6 +182,7 @@ __global__ void k_colscale_bf16(const __nv_bfloat16* __restrict__ src, const flo
 
 __global__ void k_ratio(const float* __restrict__ num, const float* __restrict__ den, int64_t n,
                         float* __restrict__ out) {
+  grid_dep_sync();
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i < n) out[i] = num[i] / den[i];
 }
@@ -184,6 +192,7 @@ __global__ void k_ratio(const float* __restrict__ num, const float* __restrict__
 __global__ void k_token_slots(int64_t T, int32_t n_seg, const int32_t* __restrict__ seg_start,
                               const int32_t* __restrict__ seg_slot, int32_t n_slots,
                               int32_t* __restrict__ token_slot) {
+  grid_dep_sync();
   int64_t cursor = 0;
   for (int32_t k = 0; k < n_seg; ++k) {
     int64_t a = max((int64_t)0, min((int64_t)seg_start[k], T));
@@ -205,7 +214,7 @@ cudaError_t launch_make_items(int64_t T, int32_t n_seg, const int32_t* seg_start
                               const int32_t* seg_slot, int32_t n_slots, TokenItem* gitems,
                               int32_t* gcount, int32_t gmax, TokenItem* ritems, int32_t* rcount,
                               int32_t rmax, cudaStream_t st) {
-  { prof_begin(0, st); k_make_items<<<1, 128, 0, st>>>(T, n_seg, seg_start, seg_slot, n_slots, gitems, gcount, gmax,
+  { prof_begin(0, st); launch_kernel(k_make_items, 1, 128, 0, st, T, n_seg, seg_start, seg_slot, n_slots, gitems, gcount, gmax,
                                  ritems, rcount, rmax); }
   return cudaGetLastError();
 }
@@ -214,7 +223,7 @@ cudaError_t launch_transpose_slots(const TransposeTab& t, int n, int64_t max_row
                                    cudaStream_t st) {
   if (n <= 0) return cudaSuccess;
   dim3 grid((unsigned)((max_cols + 31) / 32), (unsigned)((max_rows + 31) / 32), (unsigned)n);
-  { prof_begin(0, st); k_transpose_slots<<<grid, dim3(32, 8), 0, st>>>(t); }
+  { prof_begin(0, st); launch_kernel(k_transpose_slots, grid, dim3(32, 8), 0, st, t); }
   return cudaGetLastError();
 }
 
@@ -222,9 +231,9 @@ cudaError_t launch_prepare_weight(int dtype, const void* W, void* Wt, int64_t ro
                                   cudaStream_t st) {
   dim3 grid((unsigned)((cols + 31) / 32), (unsigned)((rows + 31) / 32));
   if (dtype == LORA_F32)
-    { prof_begin(0, st); k_prepare_w_f32<<<grid, dim3(32, 8), 0, st>>>((const float*)W, (float*)Wt, rows, cols); }
+    { prof_begin(0, st); launch_kernel(k_prepare_w_f32, grid, dim3(32, 8), 0, st, (const float*)W, (float*)Wt, rows, cols); }
   else
-    { prof_begin(0, st); k_transpose_w<__nv_bfloat16><<<grid, dim3(32, 8), 0, st>>>((const __nv_bfloat16*)W,
+    { prof_begin(0, st); launch_kernel(k_transpose_w<__nv_bfloat16>, grid, dim3(32, 8), 0, st, (const __nv_bfloat16*)W,
                                                                 (__nv_bfloat16*)Wt, rows, cols); }
   return cudaGetLastError();
 }
@@ -238,7 +247,7 @@ cudaError_t launch_reduce_parts(const float* part, const TokenItem* items, const
   int64_t blocks = (total + threads - 1) / threads;
   if (blocks > 4096) blocks = 4096;
   dim3 grid((unsigned)blocks, (unsigned)n_slots);
-  { prof_begin(0, st); k_reduce_parts<<<grid, threads, 0, st>>>(part, items, n_items, sub, M, ldp, transposed, tab); }
+  { prof_begin(0, st); launch_kernel(k_reduce_parts, grid, threads, 0, st, part, items, n_items, sub, M, ldp, transposed, tab); }
   return cudaGetLastError();
 }
 
@@ -248,7 +257,7 @@ cudaError_t launch_dropout_mask(const DropParams& dp, int64_t T, int64_t in_dim,
   if (n == 0) return cudaSuccess;
   int64_t blocks = (n + 255) / 256;
   if (blocks > 8192) blocks = 8192;
-  { prof_begin(0, st); k_dropout_mask<<<(unsigned)blocks, 256, 0, st>>>(dp, T, in_dim, mask); }
+  { prof_begin(0, st); launch_kernel(k_dropout_mask, (unsigned)blocks, 256, 0, st, dp, T, in_dim, mask); }
   return cudaGetLastError();
 }
 
@@ -259,21 +268,21 @@ cudaError_t launch_colscale_bf16(const void* src, const float* scale, int64_t ro
   int64_t blocks = (n8 + 255) / 256;
   if (blocks > 16384) blocks = 16384;
   prof_begin(0, st);
-  k_colscale_bf16<<<(unsigned)blocks, 256, 0, st>>>((const __nv_bfloat16*)src, scale, rows, cols,
+  launch_kernel(k_colscale_bf16, (unsigned)blocks, 256, 0, st, (const __nv_bfloat16*)src, scale, rows, cols,
                                                     (__nv_bfloat16*)dst);
   return cudaGetLastError();
 }
 
 cudaError_t launch_ratio(const float* num, const float* den, int64_t n, float* out, cudaStream_t st) {
   if (n <= 0) return cudaSuccess;
-  { prof_begin(0, st); k_ratio<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(num, den, n, out); }
+  { prof_begin(0, st); launch_kernel(k_ratio, (unsigned)((n + 255) / 256), 256, 0, st, num, den, n, out); }
   return cudaGetLastError();
 }
 
 cudaError_t launch_token_slots(int64_t T, int32_t n_seg, const int32_t* seg_start,
                                const int32_t* seg_slot, int32_t n_slots, int32_t* token_slot,
                                cudaStream_t st) {
-  { prof_begin(0, st); k_token_slots<<<1, 256, 0, st>>>(T, n_seg, seg_start, seg_slot, n_slots, token_slot); }
+  { prof_begin(0, st); launch_kernel(k_token_slots, 1, 256, 0, st, T, n_seg, seg_start, seg_slot, n_slots, token_slot); }
   return cudaGetLastError();
 }
 

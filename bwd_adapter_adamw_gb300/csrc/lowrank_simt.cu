@@ -42,6 +42,7 @@ template <int R> struct RowTpw { static constexpr int v = R <= 16 ? 4 : 1; };
 
 template <typename TA, int R>
 __global__ void __launch_bounds__(256) k_rowdot(const RowDotArgs a) {
+  grid_dep_sync();
   constexpr int kTokPerWarp = RowTpw<R>::v;
   constexpr int kRowTok = kRowWarps * kTokPerWarp;   // tokens per CTA (within one work item)
   __shared__ __align__(16) float sS[kRowSmemFloats];
@@ -143,6 +144,7 @@ constexpr int kColTokChunk = 64;
 
 template <typename TB, int R, int CPT>
 __global__ void __launch_bounds__(kColThreads) k_colred(const ColRedArgs a) {
+  grid_dep_sync();
   __shared__ __align__(16) float sP[kColTokChunk * R];
   const int item = blockIdx.y;
   TokenItem it;
@@ -211,7 +213,7 @@ template <typename TA, int R>
 void rowdot_launch(const RowDotArgs& a, int max_items, cudaStream_t st) {
   constexpr int tok = kRowWarps * RowTpw<R>::v;
   dim3 grid((unsigned)max_items, (unsigned)((kGemmTileT + tok - 1) / tok));
-  k_rowdot<TA, R><<<grid, 256, 0, st>>>(a);
+  launch_kernel(k_rowdot<TA, R>, grid, 256, 0, st, a);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -239,6 +241,7 @@ __device__ __forceinline__ void warp_halving_sum(float (&v)[V], const int lane) 
 // part[kc][t][j] = sum over the CTA's K-chunk kc of A'[t, k] S_slot[j, k]
 template <typename TA, int R>
 __global__ void __launch_bounds__(256) k_rowdot_wide(const RowDotArgs a, float* __restrict__ part) {
+  grid_dep_sync();
   constexpr int V = kRdTok * R;
   __shared__ float red[8][V];
   const int item = blockIdx.x / (kGemmTileT / kRdTok);
@@ -317,6 +320,7 @@ __global__ void __launch_bounds__(256) k_rowdot_wide(const RowDotArgs a, float* 
 // out[t, j] = alpha_slot * sum_kc part[kc][t][j] for j < r_slot, 0 for r_slot <= j < ldo
 template <int R>
 __global__ void k_rowdot_finish(const RowDotArgs a, const float* __restrict__ part, int nkc) {
+  grid_dep_sync();
   const int item = blockIdx.x;
   TokenItem it;
   if (!get_item(a.items, a.n_items, item, a.T, it)) return;
@@ -339,6 +343,7 @@ constexpr int kCrCols = 512;    // columns per CTA (256 threads x 2)
 // part[g][n][j] = sum over the 32 tokens of token group g (within one work item) of P[t, j] B'[t, n]
 template <typename TB, int R>
 __global__ void __launch_bounds__(256) k_colred_wide(const ColRedArgs a) {
+  grid_dep_sync();
   __shared__ __align__(16) float sP[kCrTok * R];
   const int item = blockIdx.y / (kRedTileT / kCrTok);
   const int sub = blockIdx.y % (kRedTileT / kCrTok);
@@ -475,6 +480,7 @@ __device__ __forceinline__ void rowdot_load(const RowDotArgs& a, const float* S,
 // x 4 columns per pass, per-thread sums kept across passes), then one warp / CTA reduction.
 template <typename TA, int R, int TOK>
 __global__ void __launch_bounds__(256) k_rowdot_full(const RowDotArgs a) {
+  grid_dep_sync();
   constexpr int V = TOK * R;
   static_assert(V % 32 == 0, "per-thread values must fill the warp reduction");
   __shared__ float red[8][V];
@@ -552,6 +558,7 @@ __device__ __forceinline__ float ld_peer(const float* local, uint32_t rank) {
 // out, so reruns are bitwise equal and no partials leave the chip.
 template <typename TB, int R>
 __global__ void __launch_bounds__(256) k_colred_fused(const ColRedArgs a) {
+  grid_dep_sync();
   constexpr int kChunk = 128;   // tokens staged per pass (16 per warp, all loads in flight)
   constexpr int U = kChunk / 8;
   __shared__ __align__(16) float sP[kChunk * R];
@@ -660,11 +667,11 @@ cudaError_t colred_for_rank(const ColRedArgs& a, int max_items, cudaStream_t st)
     return dim3((unsigned)((a.N + (int64_t)kColThreads * cpt - 1) / ((int64_t)kColThreads * cpt)),
                 (unsigned)max_items);
   };
-  if (rm <= 4) k_colred<TB, 4, 1><<<grid(1), kColThreads, 0, st>>>(a);
-  else if (rm <= 8) k_colred<TB, 8, 1><<<grid(1), kColThreads, 0, st>>>(a);
-  else if (rm <= 16) k_colred<TB, 16, 1><<<grid(1), kColThreads, 0, st>>>(a);
-  else if (rm <= 32) k_colred<TB, 32, 1><<<grid(1), kColThreads, 0, st>>>(a);
-  else k_colred<TB, 64, 1><<<grid(1), kColThreads, 0, st>>>(a);
+  if (rm <= 4) launch_kernel(k_colred<TB, 4, 1>, grid(1), kColThreads, 0, st, a);
+  else if (rm <= 8) launch_kernel(k_colred<TB, 8, 1>, grid(1), kColThreads, 0, st, a);
+  else if (rm <= 16) launch_kernel(k_colred<TB, 16, 1>, grid(1), kColThreads, 0, st, a);
+  else if (rm <= 32) launch_kernel(k_colred<TB, 32, 1>, grid(1), kColThreads, 0, st, a);
+  else launch_kernel(k_colred<TB, 64, 1>, grid(1), kColThreads, 0, st, a);
   return cudaGetLastError();
 }
 
@@ -675,19 +682,19 @@ cudaError_t rowdot_wide(const RowDotArgs& a, int max_items, cudaStream_t st, int
   const int nkc = (int)((a.K + kRdCols - 1) / kRdCols);
   dim3 grid((unsigned)(max_items * (kGemmTileT / kRdTok)), (unsigned)nkc);
   prof_begin(prof_kind, st);
-  k_rowdot_wide<TA, R><<<grid, 256, 0, st>>>(a, a.part);
+  launch_kernel(k_rowdot_wide<TA, R>, grid, 256, 0, st, a, a.part);
   prof_end(prof_kind, st);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   prof_begin(0, st);
-  k_rowdot_finish<R><<<(unsigned)max_items, 256, 0, st>>>(a, a.part, nkc);
+  launch_kernel(k_rowdot_finish<R>, (unsigned)max_items, 256, 0, st, a, a.part, nkc);
   return cudaGetLastError();
 }
 
 template <typename TA, int R, int TOK>
 cudaError_t rowdot_full(const RowDotArgs& a, int max_items, cudaStream_t st, int prof_kind) {
   prof_begin(prof_kind, st);
-  k_rowdot_full<TA, R, TOK><<<(unsigned)(max_items * (kGemmTileT / TOK)), 256, 0, st>>>(a);
+  launch_kernel(k_rowdot_full<TA, R, TOK>, (unsigned)(max_items * (kGemmTileT / TOK)), 256, 0, st, a);
   prof_end(prof_kind, st);
   return cudaGetLastError();
 }
@@ -735,13 +742,13 @@ cudaError_t launch_colred(int dtype, const ColRedArgs& a, int max_items, cudaStr
     cfg.gridDim = dim3((unsigned)((a.N + kColBlock - 1) / kColBlock), (unsigned)kColGroups);
     cfg.blockDim = dim3(256);
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 1;
     attr[0].val.clusterDim.y = kColGroups;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = add_pdl_attr(attr, 1);
     cudaError_t e;
     prof_begin(prof_kind, st);
     if (dtype == LORA_F32) {
@@ -764,13 +771,13 @@ cudaError_t launch_colred(int dtype, const ColRedArgs& a, int max_items, cudaStr
     dim3 grid((unsigned)((a.N + kCrCols - 1) / kCrCols), (unsigned)(max_items * a.sub_groups));
     prof_begin(prof_kind, st);
     if (dtype == LORA_F32) {
-      if (a.max_rank <= 4) k_colred_wide<float, 4><<<grid, 256, 0, st>>>(a);
-      else if (a.max_rank <= 8) k_colred_wide<float, 8><<<grid, 256, 0, st>>>(a);
-      else k_colred_wide<float, 16><<<grid, 256, 0, st>>>(a);
+      if (a.max_rank <= 4) launch_kernel(k_colred_wide<float, 4>, grid, 256, 0, st, a);
+      else if (a.max_rank <= 8) launch_kernel(k_colred_wide<float, 8>, grid, 256, 0, st, a);
+      else launch_kernel(k_colred_wide<float, 16>, grid, 256, 0, st, a);
     } else {
-      if (a.max_rank <= 4) k_colred_wide<__nv_bfloat16, 4><<<grid, 256, 0, st>>>(a);
-      else if (a.max_rank <= 8) k_colred_wide<__nv_bfloat16, 8><<<grid, 256, 0, st>>>(a);
-      else k_colred_wide<__nv_bfloat16, 16><<<grid, 256, 0, st>>>(a);
+      if (a.max_rank <= 4) launch_kernel(k_colred_wide<__nv_bfloat16, 4>, grid, 256, 0, st, a);
+      else if (a.max_rank <= 8) launch_kernel(k_colred_wide<__nv_bfloat16, 8>, grid, 256, 0, st, a);
+      else launch_kernel(k_colred_wide<__nv_bfloat16, 16>, grid, 256, 0, st, a);
     }
     prof_end(prof_kind, st);
     return cudaGetLastError();

@@ -68,6 +68,7 @@ struct RowsCfg {
 
 template <int NP>
 __global__ void __launch_bounds__(kThreads, 2) k_tc_rows(const __grid_constant__ RowsParams p) {
+  grid_dep_sync();
   using C = RowsCfg<NP>;
   extern __shared__ uint8_t smem_raw[];
   TokenItem it;
@@ -195,6 +196,7 @@ __global__ void __launch_bounds__(kFinishThreads) k_rows_finish(
     const float* __restrict__ part, int32_t splits, int64_t T, int32_t ldp, int use_alpha,
     const TokenItem* __restrict__ items, const int32_t* __restrict__ n_items, const SlotInfo si,
     float* __restrict__ out, uint16_t* __restrict__ outT, int64_t ldt) {
+  grid_dep_sync();
   __shared__ float tile[kFinishTok][LORA_MAX_RANK + 1];
   TokenItem it;
   if (!get_item(items, n_items, blockIdx.x, T, it)) return;
@@ -279,6 +281,7 @@ static_assert(kBM * kRedLdb * 4 <= kRedStages * kRedStageBytes, "epilogue stagin
 constexpr uint32_t kRedIdesc = idesc(kFmtBF16, kBM, kRedBN, false, true);
 
 __global__ void __launch_bounds__(kThreads, 2) k_tc_red(const __grid_constant__ RedParams p) {
+  grid_dep_sync();
   extern __shared__ uint8_t smem_raw[];
   const int item = blockIdx.y;
   TokenItem it;
@@ -403,6 +406,7 @@ __global__ void __launch_bounds__(kFinishThreads) k_red_finish(
     const float* __restrict__ part, const TokenItem* __restrict__ items,
     const int32_t* __restrict__ counts, int64_t N, int32_t rstride, int transposed,
     const ReduceTab tab, int64_t T, int64_t span) {
+  grid_dep_sync();
   __shared__ float tile[kRedFinCols][LORA_MAX_RANK + 1];
   const int slot = blockIdx.y;
   const int32_t r = tab.rank[slot];
@@ -488,6 +492,7 @@ __global__ void __launch_bounds__(kFinishThreads) k_red_finish(
 // dst [2 r, K] bf16: rows j < r = hi(src[j, :]), rows r + j = lo(src[j, :]); src [r, K] fp32.
 // transposed: src is [K, r] and row j of dst takes column j of src.
 __global__ void k_split(const SplitTab tab) {
+  grid_dep_sync();
   const int z = blockIdx.z;
   const int32_t r = tab.rank[z];
   const int64_t K = tab.K;
@@ -519,6 +524,7 @@ __global__ void k_make_red_items_tc(int64_t T, int32_t n_seg, const int32_t* __r
                                     const int32_t* __restrict__ seg_slot, int32_t n_slots,
                                     int32_t span_blocks, TokenItem* items, int32_t* count,
                                     int32_t max_items) {
+  grid_dep_sync();
   // The segment table is staged in shared memory; thread s walks it for slot s (counting its
   // items, then writing them after the lower slots' items), so the table is the same as a walk
   // slot by slot.
@@ -572,15 +578,22 @@ __global__ void k_make_red_items_tc(int64_t T, int32_t n_seg, const int32_t* __r
   if (s < n_slots) walk(true, s_count[s]);
 }
 
-// Xd = bf16(M * X): the masked operand of the shrink and of dA when dropout is on.
-__global__ void k_mask_bf16(const __nv_bfloat16* __restrict__ X, int64_t T, int64_t in_dim,
-                            const DropParams dp, __nv_bfloat16* __restrict__ Xd) {
-  const int64_t n = T * in_dim;
-  const __nv_bfloat16 zero = __float2bfloat16_rn(0.f);
-  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
-       e += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t t = e / in_dim, i = e - t * in_dim;
-    Xd[e] = drop_keep(dp, t, i) ? X[e] : zero;
+// Xd = bf16(M * X): the masked operand of the shrink and of dA when dropout is on. Rows run over
+// blockIdx.y (grid-stride); a thread masks 8 consecutive columns (one 16-byte load and store).
+__global__ void __launch_bounds__(256) k_mask_bf16(const __nv_bfloat16* __restrict__ X, int64_t T,
+                                                   int64_t in_dim, const DropParams dp,
+                                                   __nv_bfloat16* __restrict__ Xd) {
+  grid_dep_sync();
+  const int64_t i0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 8;
+  if (i0 >= in_dim) return;
+  for (int64_t t = blockIdx.y; t < T; t += gridDim.y) {
+    const DropRow dr = drop_row(dp, t);
+    uint4 v = *reinterpret_cast<const uint4*>(X + t * in_dim + i0);
+    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      if (!drop_keep_at(dr, dp.tau, i0 + e)) w[e / 2] &= (e & 1) ? 0x0000FFFFu : 0xFFFF0000u;
+    *reinterpret_cast<uint4*>(Xd + t * in_dim + i0) = make_uint4(w[0], w[1], w[2], w[3]);
   }
 }
 
@@ -631,7 +644,7 @@ cudaError_t launch_tc_rows(const TcRowsArgs& a, cudaStream_t st, int prof_kind) 
       if (e != cudaSuccess) return e;                                              \
       attr = true;                                                                 \
     }                                                                              \
-    k_tc_rows<NPV><<<grid, kThreads, RowsCfg<NPV>::kSmem, st>>>(prm);              \
+    launch_kernel(k_tc_rows<NPV>, grid, kThreads, RowsCfg<NPV>::kSmem, st, prm);              \
     break;                                                                         \
   }
     LORA_ROWS_CASE(16)
@@ -649,7 +662,7 @@ cudaError_t launch_tc_rows(const TcRowsArgs& a, cudaStream_t st, int prof_kind) 
     if (e != cudaSuccess) return e;
   }
   prof_begin(0, st);
-  k_rows_finish<<<dim3((unsigned)a.max_items, (unsigned)(kBM / kFinishTok)), kFinishThreads, 0, st>>>(
+  launch_kernel(k_rows_finish, dim3((unsigned)a.max_items, (unsigned)(kBM / kFinishTok)), kFinishThreads, 0, st, 
       a.part, a.splits, a.T, (int32_t)a.ldo, 1, a.items, a.n_items, a.si, a.out, a.outT, a.ldt);
   prof_end(prof_kind, st);   // the class's time spans the product and its split-K finish
   return cudaGetLastError();
@@ -685,12 +698,12 @@ cudaError_t launch_tc_red(const TcRedArgs& a, cudaStream_t st, int prof_kind) {
   }
   dim3 grid((unsigned)((a.N + kRedBN - 1) / kRedBN), (unsigned)a.max_items);
   prof_begin(prof_kind, st);
-  k_tc_red<<<grid, kThreads, kRedSmem, st>>>(prm);
+  launch_kernel(k_tc_red, grid, kThreads, kRedSmem, st, prm);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t blocks = (a.N + kRedFinCols - 1) / kRedFinCols;
   prof_begin(0, st);
-  k_red_finish<<<dim3((unsigned)blocks, (unsigned)a.n_slots), kFinishThreads, 0, st>>>(
+  launch_kernel(k_red_finish, dim3((unsigned)blocks, (unsigned)a.n_slots), kFinishThreads, 0, st, 
       a.part, a.items, a.n_items, a.N, a.max_rank, a.transposed, a.tab, a.T, a.span_tokens);
   prof_end(prof_kind, st);   // the class's time spans the product and its item reduction
   return cudaGetLastError();
@@ -703,7 +716,7 @@ cudaError_t launch_split(const SplitTab& t, int n, cudaStream_t st) {
   int64_t blocks = (most + 255) / 256;
   if (blocks > 4096) blocks = 4096;
   prof_begin(0, st);
-  k_split<<<dim3((unsigned)blocks, 1, (unsigned)n), 256, 0, st>>>(t);
+  launch_kernel(k_split, dim3((unsigned)blocks, 1, (unsigned)n), 256, 0, st, t);
   return cudaGetLastError();
 }
 
@@ -719,7 +732,7 @@ cudaError_t launch_split_rows_t(const float* src, int64_t lds, int64_t ldt, cons
   }
   if (lds % 4 || lds > LORA_MAX_RANK) return cudaErrorInvalidValue;
   prof_begin(0, st);
-  k_rows_finish<<<dim3((unsigned)max_items, (unsigned)(kBM / kFinishTok)), kFinishThreads, 0, st>>>(
+  launch_kernel(k_rows_finish, dim3((unsigned)max_items, (unsigned)(kBM / kFinishTok)), kFinishThreads, 0, st, 
       src, 1, T, (int32_t)lds, 0, items, n_items, si, nullptr, dst, ldt);
   return cudaGetLastError();
 }
@@ -729,20 +742,20 @@ cudaError_t launch_make_red_items_tc(int64_t T, int32_t n_seg, const int32_t* se
                                      TokenItem* items, int32_t* count, int32_t max_items,
                                      cudaStream_t st) {
   prof_begin(0, st);
-  k_make_red_items_tc<<<1, 128, 0, st>>>(T, n_seg, seg_start, seg_slot, n_slots, span_blocks,
+  launch_kernel(k_make_red_items_tc, 1, 128, 0, st, T, n_seg, seg_start, seg_slot, n_slots, span_blocks,
                                          items, count, max_items);
   return cudaGetLastError();
 }
 
 cudaError_t launch_mask_bf16(const void* X, int64_t T, int64_t in_dim, const DropParams& dp,
                              void* Xd, cudaStream_t st) {
-  const int64_t n = T * in_dim;
-  if (n <= 0) return cudaSuccess;
-  int64_t blocks = (n + 255) / 256;
-  if (blocks > 16384) blocks = 16384;
+  if (T <= 0 || in_dim <= 0) return cudaSuccess;
+  if (in_dim % 8) return cudaErrorInvalidValue;
+  const unsigned gx = (unsigned)((in_dim / 8 + 255) / 256);
+  const unsigned gy = (unsigned)(T < 8192 ? T : 8192);
   prof_begin(0, st);
-  k_mask_bf16<<<(unsigned)blocks, 256, 0, st>>>((const __nv_bfloat16*)X, T, in_dim, dp,
-                                                (__nv_bfloat16*)Xd);
+  launch_kernel(k_mask_bf16, dim3(gx, gy), 256, 0, st, (const __nv_bfloat16*)X, T, in_dim, dp,
+                (__nv_bfloat16*)Xd);
   return cudaGetLastError();
 }
 

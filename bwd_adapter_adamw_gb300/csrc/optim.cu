@@ -62,6 +62,7 @@ __global__ void __launch_bounds__(kPrepThreads) k_grad_prepare(const float* __re
                                                                int32_t* __restrict__ status,
                                                                double* part, uint32_t* counter,
                                                                int64_t per_block) {
+  grid_dep_sync();
   __shared__ double sh[kPrepThreads / 32];
   __shared__ bool am_last;
   const int b = blockIdx.x;
@@ -137,6 +138,7 @@ __global__ void __launch_bounds__(kAdamThreads) k_adamw(float* __restrict__ P, f
                                                         const double* __restrict__ scale_norm,
                                                         const int32_t* __restrict__ status,
                                                         int zero_grads) {
+  grid_dep_sync();
   const int b = blockIdx.x;
   const int g = find_group(gt, b);
   if (status[g] != LORA_OK) return;
@@ -208,7 +210,7 @@ cudaError_t launch_grad_prepare(const float* grads, const GroupTab& g_in, double
     for (int i = 0; i < g.n; ++i) g.block_begin[i] = 0;
   }
   prof_begin(LORA_PROF_PREPARE, st);
-  k_grad_prepare<<<blocks, kPrepThreads, 0, st>>>(grads, g, d_scale_norm, d_status, part, counter,
+  launch_kernel(k_grad_prepare, blocks, kPrepThreads, 0, st, grads, g, d_scale_norm, d_status, part, counter,
                                                   per_block);
   prof_end(LORA_PROF_PREPARE, st);
   return cudaGetLastError();
@@ -221,7 +223,7 @@ cudaError_t launch_adamw(float* p, float* g, float* m, float* v, const GroupTab&
   const int blocks = set_blocks(gt, kAdamElemsPerBlock);
   if (blocks == 0) return cudaSuccess;
   prof_begin(LORA_PROF_ADAMW, st);
-  k_adamw<<<blocks, kAdamThreads, 0, st>>>(p, g, m, v, gt, hp, d_scale_norm, d_status, zero_grads);
+  launch_kernel(k_adamw, blocks, kAdamThreads, 0, st, p, g, m, v, gt, hp, d_scale_norm, d_status, zero_grads);
   prof_end(LORA_PROF_ADAMW, st);
   return cudaGetLastError();
 }

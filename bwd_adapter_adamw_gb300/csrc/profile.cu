@@ -2,6 +2,7 @@
 // of one kernel class (used by the benchmark to time its dominant kernel on the launching stream,
 // including inside captured CUDA graphs, where each record becomes an external event node).
 #include <atomic>
+#include <cstdlib>
 #include <mutex>
 #include <vector>
 
@@ -26,6 +27,14 @@ void record(cudaEvent_t e, cudaStream_t st) {
     cudaEventRecord(e, st);
 }
 }  // namespace
+
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("LORA_PDL");
+    return !(v && v[0] == '0');
+  }();
+  return on;
+}
 
 void prof_begin(int kind, cudaStream_t st) {
   g_launches.fetch_add(1, std::memory_order_relaxed);
