@@ -351,6 +351,15 @@ def run_reference(args):
     return 0
 
 
+def step_stats(per_step):
+    """Median, 10th and 90th percentile of the timed steps' durations (ms), this rank's clock."""
+    xs = sorted(per_step)
+    if not xs:
+        return None
+    q = statistics.quantiles(xs, n=10, method="inclusive") if len(xs) > 1 else [xs[0]] * 9
+    return {"median": statistics.median(xs), "p10": q[0], "p90": q[8], "n": len(xs)}
+
+
 def workload_name(cfg, layers):
     projs = "+".join(f"{p.name}:{p.in_dim}->{p.out_dim}" for p in cfg.projs)
     extra = []
@@ -433,14 +442,17 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
+    step_ev = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ev0.record(stream)
-    for _ in range(K):
+    for i in range(K):
         replay()
+        step_ev[i].record(stream)   # per-step boundaries for the median / p10 / p90
     ev1.record(stream)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     ms = ev0.elapsed_time(ev1)
+    per_step = [(ev0 if i == 0 else step_ev[i - 1]).elapsed_time(step_ev[i]) for i in range(K)]
     # dominant-kernel durations from the last replay
     kern_ms = [a.elapsed_time(b) for a, b in zip(starts[:used], stops[:used])] if used else []
     # end-to-end through host buffers: H2D of the step's inputs, the step, D2H of the result
@@ -534,6 +546,13 @@ def run_ours(args):
                                       "launches": len(ts), "ms_total": sum(ts),
                                       "bytes_per_step": mem[name]}
         achieved_serial = per_launch / (avg_serial / 1e3) / 1e12 if avg_serial else None
+        # step-level bound: every frozen product at the tensor peak plus every memory-bound
+        # class's algorithmic bytes at the HBM peak, against the measured step
+        t_tensor = (cnt["fwd_flops"] + cnt["dx_flops"]) / (peak * 1e12) * 1e3
+        t_hbm = sum(mem.values()) / (peaks["hbm_gbs"] * 1e9) * 1e3
+        step_roofline = {"t_bound_ms": t_tensor + t_hbm, "t_tensor_ms": t_tensor,
+                         "t_hbm_ms": t_hbm, "t_measured_ms": ms / K,
+                         "frac": (t_tensor + t_hbm) / (ms / K)}
         traffic, traffic_note = traffic_for(cfg.name, prof_class)
         cpu = None
         if not args.no_cpu_baseline and world == 1:
@@ -541,6 +560,8 @@ def run_ours(args):
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms / K, "higher_is_better": True,
+            "step_ms": step_stats(per_step),
+            "step_roofline": step_roofline,
             "scaling": "weak", "vs_baseline": None,
             "dtype": "f32" if cfg.dtype == "f32" else "bf16", "data": "synthetic",
             "config": {"workload": workload_name(cfg, layers), "tokens_per_step": tokens,

@@ -938,13 +938,19 @@ int lora_grad_prepare(const float* grads, int32_t n_groups, const lora_group* gr
       (reinterpret_cast<uintptr_t>(d_status) & 3u))
     return LORA_ERR_ALIGN;
   if (ws_bytes < lora_grad_prepare_workspace_size(n_groups, groups)) return LORA_ERR_WORKSPACE;
-  const int blocks = prepare_blocks(g);
+  const int blocks = prepare_blocks(g);   // the workspace holds this many partials (the most)
   Carve c(ws);
   double* part = c.take<double>((size_t)(blocks > 0 ? blocks : 1));
   uint32_t* counter = c.take<uint32_t>(4);
+  // elements per CTA: enough CTAs for about eight per SM over the whole arena, each streaming a
+  // long run (a multiple of the workspace form's run, so the partials still fit)
+  int64_t total = 0;
+  for (int i = 0; i < g.n; ++i) total += g.count[i];
+  int64_t per = (total / kPrepTargetBlocks + kPrepElemsWs - 1) / kPrepElemsWs * kPrepElemsWs;
+  if (per < kPrepElemsWs) per = kPrepElemsWs;
   clear_stale();
   return cuda_status(launch_grad_prepare(grads, g, d_scale_norm, d_status, part, counter,
-                                         (cudaStream_t)stream));
+                                         (cudaStream_t)stream, per));
 }
 
 int lora_grad_prepare_noalloc(const float* grads, int32_t n_groups, const lora_group* groups,

@@ -254,6 +254,7 @@ struct GroupTab {
 constexpr int kPrepThreads = 256;
 constexpr int kPrepElemsWs = kPrepThreads * 16;         // per CTA, workspace form (more CTAs)
 constexpr int kPrepElemsPerBlock = kPrepThreads * 64;   // per CTA, allocation-free form
+constexpr int64_t kPrepTargetBlocks = 8 * 152;          // CTAs of the workspace form, large arenas
 constexpr int kAdamThreads = 256;
 constexpr int kAdamElemsPerBlock = kAdamThreads * 16;
 

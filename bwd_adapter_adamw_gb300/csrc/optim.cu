@@ -97,6 +97,7 @@ __global__ void __launch_bounds__(kPrepThreads) k_grad_prepare(const float* __re
   for (int gg = 0; gg < gt.n; ++gg) {
     const int b0 = gt.block_begin[gg], b1 = gt.block_begin[gg + 1];
     double acc = 0.0;
+#pragma unroll 4
     for (int k = b0 + threadIdx.x; k < b1; k += kPrepThreads) acc += __ldcg(part + k);
     const double S = block_sum_double(acc, sh);
     if (threadIdx.x == 0) {
