@@ -121,9 +121,9 @@ def memory_counts(cfg: LI.LoraConfig, layers: int):
 # value. Captured with `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum` on
 # `python bench.py --layers 1 --steps 2 --warmup 3 --no-cpu-baseline --streams 1`.
 NCU_TRAFFIC = {
-    ("c2", 1): {"source": "gemm_tc_f32.cu", "sha256_16": "a711ea7e9c97d349",
-                "bytes": (50.49e6 + 21.07e6) / 2,
-                "note": "wq fwd 50.49 MB, wv fwd (4-way split K) 21.07 MB read, ~0 written "
+    ("c2", 1): {"source": "gemm_tc_f32.cu", "sha256_16": "deb64ff3168e75dd",
+                "bytes": (50.48e6 + 21.06e6) / 2,
+                "note": "wq fwd 50.48 MB, wv fwd (4-way split K) 21.06 MB read, ~0 written "
                         "(outputs stay in L2)"},
 }
 
