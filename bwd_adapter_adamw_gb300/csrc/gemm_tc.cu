@@ -65,8 +65,10 @@ struct GemmCfg {
   static_assert(BN % 32 == 0 && BN >= 128 && BN <= 256, "tile width");
   static constexpr int kBBytes = BN * 128;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kStages = (200 * 1024 / kStageBytes) < 6 ? (200 * 1024 / kStageBytes) : 6;
+  // as many stages as fit 225 KB of shared memory (4 at BN 256, 5 at 224 and 192)
+  static constexpr int kStages = (225 * 1024 / kStageBytes) < 6 ? (225 * 1024 / kStageBytes) : 6;
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*barriers*/ + 1024 /*alignment*/;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
   static constexpr uint32_t kIdescBF16 = tc::idesc(tc::kFmtBF16, kBM, BN);
   static constexpr uint32_t kIdescTF32 = tc::idesc(tc::kFmtTF32, kBM, BN);
   static_assert(kStageBytes % 1024 == 0, "stage alignment of the 128-byte swizzle");

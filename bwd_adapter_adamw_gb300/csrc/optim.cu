@@ -56,7 +56,7 @@ __device__ __forceinline__ int find_group(const GroupTab& g, int b) {
   return lo;
 }
 
-__global__ void __launch_bounds__(kPrepThreads) k_grad_prepare(const float* __restrict__ grads,
+__global__ void __launch_bounds__(kPrepThreads, 8) k_grad_prepare(const float* __restrict__ grads,
                                                                const GroupTab gt,
                                                                double* __restrict__ scale_norm,
                                                                int32_t* __restrict__ status,
