@@ -89,6 +89,9 @@ def _load() -> C.CDLL:
         "lora_grad_prepare_noalloc": (C.c_int, [P, I32, C.POINTER(lora_group), P, P, P]),
         "lora_adamw_step": (C.c_int, [P, P, P, P, I32, C.POINTER(lora_group),
                                       C.POINTER(lora_adamw_hp), P, P, I32, P]),
+        "lora_snapshot": (C.c_int, [P, P, I32, C.POINTER(lora_group), P]),
+        "lora_restore": (C.c_int, [P, P, P, P, P, I32, C.POINTER(lora_group), I32, P]),
+        "lora_retire": (C.c_int, [P, P, P, P, I32, C.POINTER(lora_group), I32, P]),
         "multi_lora_workspace_size": (SZ, [DP, I64, I32, I32, C.POINTER(lora_slot)]),
         "multi_lora_forward": (C.c_int, [DP, CP, I64, P, P, P, I32, P, P, I32,
                                          C.POINTER(lora_slot), P, P, P, SZ, P]),
@@ -114,7 +117,7 @@ EXPORTED = ("lora_status_string", "lora_scale", "lora_lr_at", "lora_workspace_si
             "lora_prepared_weight_size", "lora_prepare_weight", "lora_dora_norm_workspace_size",
             "lora_dora_norm", "lora_forward", "lora_backward",
             "lora_grad_prepare_workspace_size", "lora_grad_prepare", "lora_grad_prepare_noalloc",
-            "lora_adamw_step",
+            "lora_adamw_step", "lora_snapshot", "lora_restore", "lora_retire",
             "multi_lora_workspace_size", "multi_lora_forward", "multi_lora_backward",
             "lora_dropout_mask", "multi_lora_token_slots", "lora_profile_arm",
             "lora_profile_used", "lora_launch_counter", "lora_last_cuda_error",
@@ -266,6 +269,28 @@ def lora_adamw_step(params, grads, m, v, groups, hp: lora_adamw_hp, d_scale_norm
                               C.byref(hp), _ptr(d_scale_norm), _ptr(d_status),
                               1 if zero_grads else 0, _stream(stream))
     return _check(st, "lora_adamw_step") if check else st
+
+
+def lora_snapshot(params, snap, groups, stream=None, check=True):
+    """snap = params over the groups' ranges (best-weights snapshot)."""
+    st = _lib.lora_snapshot(_ptr(params), _ptr(snap), len(groups), groups, _stream(stream))
+    return _check(st, "lora_snapshot") if check else st
+
+
+def lora_restore(params, snap, grads, m, v, groups, zero_grads=False, stream=None, check=True):
+    """params = snap and m = v = 0 (optimizer reset) over the groups' ranges; grads = 0 too when
+    zero_grads. The caller restarts the groups' step counts."""
+    st = _lib.lora_restore(_ptr(params), _ptr(snap), _ptr(grads), _ptr(m), _ptr(v), len(groups),
+                           groups, 1 if zero_grads else 0, _stream(stream))
+    return _check(st, "lora_restore") if check else st
+
+
+def lora_retire(params, grads, m, v, groups, clear_params=False, stream=None, check=True):
+    """grads = m = v = 0 over the groups' ranges (retired slots); params = 0 too when
+    clear_params."""
+    st = _lib.lora_retire(_ptr(params), _ptr(grads), _ptr(m), _ptr(v), len(groups), groups,
+                          1 if clear_params else 0, _stream(stream))
+    return _check(st, "lora_retire") if check else st
 
 
 def make_slots(slots: Sequence[dict]):

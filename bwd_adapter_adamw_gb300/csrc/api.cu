@@ -993,6 +993,46 @@ int lora_adamw_step(float* params, float* grads, float* m, float* v, int32_t n_g
                                   (cudaStream_t)stream));
 }
 
+int lora_snapshot(const float* params, float* snap, int32_t n_groups, const lora_group* groups,
+                  void* stream) {
+  GroupTab g;
+  int rc = build_groups(n_groups, groups, g, nullptr);
+  if (rc) return rc;
+  if (!params || !snap) return LORA_ERR_INVALID;
+  if (!al16(params) || !al16(snap)) return LORA_ERR_ALIGN;
+  clear_stale();
+  return cuda_status(launch_group_maint(snap, params, nullptr, nullptr, nullptr, g, kMaintCopy,
+                                        (cudaStream_t)stream));
+}
+
+int lora_restore(float* params, const float* snap, float* grads, float* m, float* v,
+                 int32_t n_groups, const lora_group* groups, int32_t zero_grads, void* stream) {
+  GroupTab g;
+  int rc = build_groups(n_groups, groups, g, nullptr);
+  if (rc) return rc;
+  if (!params || !snap || !m || !v || (zero_grads && !grads)) return LORA_ERR_INVALID;
+  if (!al16(params) || !al16(snap) || !al16(m) || !al16(v) || (zero_grads && !al16(grads)))
+    return LORA_ERR_ALIGN;
+  clear_stale();
+  const int flags = kMaintCopy | kMaintZeroMV | (zero_grads ? kMaintZeroG : 0);
+  return cuda_status(launch_group_maint(params, snap, grads, m, v, g, flags,
+                                        (cudaStream_t)stream));
+}
+
+int lora_retire(float* params, float* grads, float* m, float* v, int32_t n_groups,
+                const lora_group* groups, int32_t clear_params, void* stream) {
+  GroupTab g;
+  int rc = build_groups(n_groups, groups, g, nullptr);
+  if (rc) return rc;
+  if (!grads || !m || !v || (clear_params && !params)) return LORA_ERR_INVALID;
+  if (!al16(grads) || !al16(m) || !al16(v) || (clear_params && !al16(params)))
+    return LORA_ERR_ALIGN;
+  clear_stale();
+  const int flags = kMaintZeroG | kMaintZeroMV | (clear_params ? kMaintZeroDst : 0);
+  return cuda_status(launch_group_maint(params, nullptr, grads, m, v, g, flags,
+                                        (cudaStream_t)stream));
+}
+
 int lora_dropout_mask(const lora_desc* d, const lora_ctx* c, int64_t T, uint8_t* d_mask,
                       void* stream) {
   int rc = check_desc(d, T, false);

@@ -255,6 +255,13 @@ constexpr int kPrepThreads = 256;
 constexpr int kPrepElemsWs = kPrepThreads * 16;         // per CTA, workspace form (more CTAs)
 constexpr int kPrepElemsPerBlock = kPrepThreads * 64;   // per CTA, allocation-free form
 constexpr int64_t kPrepTargetBlocks = 8 * 152;          // CTAs of the workspace form, large arenas
+// adapter-state maintenance (launch_group_maint flags)
+constexpr int kMaintCopy = 1;     // dst = src
+constexpr int kMaintZeroDst = 2;  // dst = 0
+constexpr int kMaintZeroG = 4;    // grads = 0
+constexpr int kMaintZeroMV = 8;   // Adam moments = 0
+cudaError_t launch_group_maint(float* dst, const float* src, float* g, float* m, float* v,
+                               const GroupTab& gt, int flags, cudaStream_t st);
 constexpr int kAdamThreads = 256;
 constexpr int kAdamElemsPerBlock = kAdamThreads * 16;
 

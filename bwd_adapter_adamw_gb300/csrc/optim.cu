@@ -180,6 +180,43 @@ __global__ void __launch_bounds__(kAdamThreads) k_adamw(float* __restrict__ P, f
   }
 }
 
+// Adapter-state maintenance over the groups' ranges (snapshot, restore with optimizer reset,
+// slot retirement): dst = src when kMaintCopy, dst = 0 when kMaintZeroDst, G = 0 when kMaintZeroG,
+// M = V = 0 when kMaintZeroMV. One CTA per kAdamElemsPerBlock elements of a group.
+__global__ void __launch_bounds__(kAdamThreads) k_group_maint(float* __restrict__ dst,
+                                                              const float* __restrict__ src,
+                                                              float* __restrict__ G,
+                                                              float* __restrict__ M,
+                                                              float* __restrict__ V,
+                                                              const GroupTab gt, int flags) {
+  grid_dep_sync();
+  const int b = blockIdx.x;
+  const int g = find_group(gt, b);
+  const int64_t begin = (int64_t)(b - gt.block_begin[g]) * kAdamElemsPerBlock;
+  const int64_t n = min((int64_t)kAdamElemsPerBlock, gt.count[g] - begin);
+  const int64_t base = gt.offset[g] + begin;
+  const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int64_t nv = n >> 2;
+  for (int64_t q = threadIdx.x; q < nv; q += kAdamThreads) {
+    const int64_t e = base + (q << 2);
+    if (flags & kMaintCopy)
+      *reinterpret_cast<float4*>(dst + e) = *reinterpret_cast<const float4*>(src + e);
+    else if (flags & kMaintZeroDst)
+      *reinterpret_cast<float4*>(dst + e) = z4;
+    if (flags & kMaintZeroG) *reinterpret_cast<float4*>(G + e) = z4;
+    if (flags & kMaintZeroMV) {
+      *reinterpret_cast<float4*>(M + e) = z4;
+      *reinterpret_cast<float4*>(V + e) = z4;
+    }
+  }
+  for (int64_t e = base + (nv << 2) + threadIdx.x; e < base + n; e += kAdamThreads) {
+    if (flags & kMaintCopy) dst[e] = src[e];
+    else if (flags & kMaintZeroDst) dst[e] = 0.f;
+    if (flags & kMaintZeroG) G[e] = 0.f;
+    if (flags & kMaintZeroMV) { M[e] = 0.f; V[e] = 0.f; }
+  }
+}
+
 int set_blocks(GroupTab& g, int64_t per_block) {
   int total = 0;
   for (int i = 0; i < g.n; ++i) {
@@ -214,6 +251,16 @@ cudaError_t launch_grad_prepare(const float* grads, const GroupTab& g_in, double
   launch_kernel(k_grad_prepare, blocks, kPrepThreads, 0, st, grads, g, d_scale_norm, d_status, part, counter,
                                                   per_block);
   prof_end(LORA_PROF_PREPARE, st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_group_maint(float* dst, const float* src, float* g, float* m, float* v,
+                               const GroupTab& gt_in, int flags, cudaStream_t st) {
+  GroupTab gt = gt_in;
+  const int blocks = set_blocks(gt, kAdamElemsPerBlock);
+  if (blocks == 0) return cudaSuccess;
+  prof_begin(0, st);
+  launch_kernel(k_group_maint, blocks, kAdamThreads, 0, st, dst, src, g, m, v, gt, flags);
   return cudaGetLastError();
 }
 

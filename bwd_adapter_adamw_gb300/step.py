@@ -211,6 +211,19 @@ class LoraStep:
         self.forward_backward(opt_step, per_chunk_calls)
         self.optimizer_step(lr, opt_step, zero_grads)
 
+    def snapshot(self, snap: Optional[torch.Tensor] = None) -> torch.Tensor:
+        """Device copy of every adapter's parameters (the best-weights snapshot)."""
+        if snap is None:
+            snap = torch.empty_like(self.arena.params)
+        L.lora_snapshot(self.arena.params, snap, self.groups(0.0, 0))
+        return snap
+
+    def restore(self, snap: torch.Tensor, zero_grads: bool = True):
+        """Restore a snapshot and reset the optimizer (moments zeroed); the caller's next update
+        passes step 0 again."""
+        L.lora_restore(self.arena.params, snap, self.arena.grads, self.arena.m, self.arena.v,
+                       self.groups(0.0, 0), zero_grads)
+
 
 # ----------------------------------------------------------------------------------------------
 @dataclass
@@ -334,6 +347,17 @@ class MultiLoraStep:
                                    n_b=self.slot_nb[s], grad_scale=1.0 / gbs[s],
                                    max_norm=self.max_norm, lr=lrs[s], step=steps[s])
                               for s in ready])
+
+    def retire(self, slots: Sequence[int], clear_params: bool = True):
+        """Retire finished adapter slots: their gradients (the partial accumulation), moments and,
+        with clear_params, weights are zeroed. The caller resets the slots' accumulated sample
+        counts and update counts."""
+        if not slots:
+            return
+        g = L.make_groups([dict(offset=self.slot_off[s], n_a=self.slot_na[s],
+                                n_b=self.slot_nb[s], grad_scale=1.0) for s in slots])
+        L.lora_retire(self.arena.params, self.arena.grads, self.arena.m, self.arena.v, g,
+                      clear_params)
 
     def optimizer_step(self, ready: Sequence[int], gbs, lrs, steps, zero_grads: bool = True):
         """Prepare + AdamW for the slots whose adapter batch is full (one group each); group i of

@@ -233,6 +233,30 @@ int lora_adamw_step(float* params, float* grads, float* m, float* v, int32_t n_g
                     const lora_group* groups, const lora_adamw_hp* hp, const double* d_scale_norm,
                     const int32_t* d_status, int32_t zero_grads, void* stream);
 
+/* ---- adapter-state maintenance --------------------------------------------------------------*/
+/* Snapshot, restore and retirement of adapter state over the groups' ranges
+ * [offset, offset + n_a + n_b + n_mag) of the flat fp32 arenas ("4.3. Training Guide",
+ * Validation early stopping: the best A/B are snapshotted, restored on exit, and the optimizer
+ * is reset after the restore; "Multi-LoRA Training Example", a finished adapter is retired:
+ * its slot cleared, its optimizer state and retained gradients zeroed, its partially
+ * accumulated gradients discarded). All arrays are device fp32 with the arenas' layout and
+ * 16-byte aligned; only the groups' ranges are read or written. Asynchronous on `stream`;
+ * groups are checked as for lora_grad_prepare (LORA_ERR_INVALID / LORA_ERR_ALIGN before any
+ * launch), a launch failure gives LORA_ERR_CUDA.
+ *
+ * lora_snapshot: snap = params.
+ * lora_restore:  params = snap, m = v = 0, and grads = 0 when zero_grads != 0. The caller
+ *                restarts each group's update count (lora_group.step = 0 on its next
+ *                lora_adamw_step), which completes the optimizer reset.
+ * lora_retire:   grads = m = v = 0, and params = 0 when clear_params != 0. The caller resets
+ *                the slots' accumulated sample counts and update counts on the host. */
+int lora_snapshot(const float* params, float* snap, int32_t n_groups, const lora_group* groups,
+                  void* stream);
+int lora_restore(float* params, const float* snap, float* grads, float* m, float* v,
+                 int32_t n_groups, const lora_group* groups, int32_t zero_grads, void* stream);
+int lora_retire(float* params, float* grads, float* m, float* v, int32_t n_groups,
+                const lora_group* groups, int32_t clear_params, void* stream);
+
 /* ---- slot-keyed multi-LoRA ------------------------------------------------------------------*/
 /* Segments: segment k covers tokens [seg_start[k], seg_start[k+1]) (device int32 [n_seg + 1],
  * non-decreasing, within [0, T]) and uses slot seg_slot[k] (device int32 [n_seg]). Tokens in no

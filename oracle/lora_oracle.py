@@ -15,7 +15,9 @@ Everything is numpy float64. Each function restates one step of the method as th
     the LoRA gradients dA = B^T-side product and dB = out_prod of grad and the shrink activations.
   * "Multi-LoRA Training Example (fully-async)", section "Design (decoupled per-adapter
     optimizers)": per-slot accumulation with weight 1, 1/adapter_global_batch_size at step time,
-    per-slot Adam state, step count and clipping.
+    per-slot Adam state, step count and clipping; and the retirement of a finished adapter.
+  * "4.3. Training Guide", section "Validation early stopping": snapshot and restore of the best
+    A/B with an optimizer reset.
 
 Where the pages leave a step open the oracle takes one reading and the CUDA path implements the
 same reading independently (no shared code):
@@ -277,6 +279,55 @@ def adamw_update(p, g, m, v, kind: int, c: float, hp: AdamHP):
     else:
         raise ValueError(kind)
     return p1.astype(np.float32), m1.astype(np.float32), v1.astype(np.float32)
+
+
+# ----------------------------------------------------------------------------------------------
+# adapter-state maintenance  ("4.3. Training Guide" / Validation early stopping: the best A/B
+# are snapshotted and restored, and the optimizer is reset after the restore; "Multi-LoRA
+# Training Example (fully-async)": a finished adapter is retired, its slot cleared, its optimizer
+# state and retained gradients zeroed and its partial accumulation discarded)
+# ----------------------------------------------------------------------------------------------
+def group_ranges(groups: Sequence[Tuple[int, int]]):
+    """(offset, count) pairs -> the flat index ranges they cover."""
+    return [range(off, off + cnt) for off, cnt in groups]
+
+
+def snapshot(params, snap, groups: Sequence[Tuple[int, int]]) -> np.ndarray:
+    """Returns snap with snap[i] = params[i] for every index i in a group; other entries kept."""
+    out = np.array(snap, dtype=np.float32, copy=True)
+    for r in group_ranges(groups):
+        for i in r:
+            out[i] = params[i]
+    return out
+
+
+def restore(params, snap, grads, m, v, groups: Sequence[Tuple[int, int]], zero_grads: bool):
+    """Returns (params, grads, m, v) with, inside the groups: params = snap, m = v = 0 (the
+    optimizer reset; the caller also restarts the update count) and grads = 0 when zero_grads.
+    Entries outside the groups are kept."""
+    p, g, mm, vv = (np.array(a, dtype=np.float32, copy=True) for a in (params, grads, m, v))
+    for r in group_ranges(groups):
+        for i in r:
+            p[i] = snap[i]
+            mm[i] = 0.0
+            vv[i] = 0.0
+            if zero_grads:
+                g[i] = 0.0
+    return p, g, mm, vv
+
+
+def retire(params, grads, m, v, groups: Sequence[Tuple[int, int]], clear_params: bool):
+    """Returns (params, grads, m, v) with, inside the groups: grads = m = v = 0 and params = 0
+    when clear_params. Entries outside the groups are kept."""
+    p, g, mm, vv = (np.array(a, dtype=np.float32, copy=True) for a in (params, grads, m, v))
+    for r in group_ranges(groups):
+        for i in r:
+            g[i] = 0.0
+            mm[i] = 0.0
+            vv[i] = 0.0
+            if clear_params:
+                p[i] = 0.0
+    return p, g, mm, vv
 
 
 # ----------------------------------------------------------------------------------------------

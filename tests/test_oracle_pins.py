@@ -445,3 +445,62 @@ def test_multi_slot_gradient_equals_that_slot_training_alone():
                               O.lora_backward(X[ts == 1], W, slots[1].A, slots[1].B, dY[ts == 1], 2.0).dB],
                              1.0 / gbs, 1.0)
     assert p_multi.scale == pytest.approx(p_alone.scale, rel=1e-12)
+
+
+# ---- adapter-state maintenance ("4.3. Training Guide", Validation early stopping; "Multi-LoRA
+# Training Example (fully-async)", adapter retirement) ----
+def _arenas(n=64, seed=7):
+    rng = np.random.default_rng(seed)
+    return [rng.standard_normal(n).astype(np.float32) for _ in range(4)]
+
+
+def test_restore_returns_the_snapshot_and_a_fresh_optimizer():
+    # snapshot, two updates that move params and moments, restore: params are the snapshot bit for
+    # bit inside the groups, moments are zero there, everything outside the groups is untouched
+    p, g, m, v = _arenas()
+    v = np.abs(v)                          # a second moment is non-negative
+    groups = [(4, 20), (32, 13)]
+    snap = O.snapshot(p, np.full_like(p, np.nan), groups)
+    hp = O.AdamHP(lr=0.05, wd=0.01)
+    p1, m1, v1 = p.copy(), m.copy(), v.copy()
+    for k in range(2):
+        hp.step = k
+        p1, m1, v1 = O.adamw_update(p1, g, m1, v1, O.KIND_A, 1.0, hp)
+    pr, gr, mr, vr = O.restore(p1, snap, g, m1, v1, groups, zero_grads=True)
+    inside = np.zeros(p.size, bool)
+    for off, cnt in groups:
+        inside[off:off + cnt] = True
+    assert np.array_equal(pr[inside], p[inside])
+    assert not np.any(mr[inside]) and not np.any(vr[inside]) and not np.any(gr[inside])
+    assert np.array_equal(pr[~inside], p1[~inside])
+    assert np.array_equal(mr[~inside], m1[~inside]) and np.array_equal(gr[~inside], g[~inside])
+    assert np.all(np.isnan(snap[~inside]))
+
+
+def test_step_after_restore_is_the_normalised_sign_step_from_the_snapshot():
+    # after the reset the next update (update count restarted at 0) is Adam's first step from
+    # zero moments, whatever the moments were before: p_snap - lr * g / (|g| + eps) for B
+    p, g, m, v = _arenas(seed=11)
+    v = np.abs(v) + 1.0                   # stale moments that would change the update
+    groups = [(0, 64)]
+    snap = O.snapshot(p, np.zeros_like(p), groups)
+    pr, _, mr, vr = O.restore(p + 1.0, snap, g, m, v, groups, zero_grads=False)
+    p1, _, _ = O.adamw_update(pr, g, mr, vr, O.KIND_B, 1.0, O.AdamHP(lr=0.1, wd=0.0, step=0))
+    g64 = g.astype(np.float64)
+    want = p.astype(np.float64) - 0.1 * g64 / (np.abs(g64) + 1e-8)
+    np.testing.assert_allclose(p1, want.astype(np.float32), rtol=1e-6, atol=1e-7)
+
+
+def test_retire_clears_only_the_retired_slot():
+    p, g, m, v = _arenas(seed=3)
+    slots = [(0, 16), (16, 24), (40, 24)]
+    pr, gr, mr, vr = O.retire(p, g, m, v, [slots[1]], clear_params=True)
+    for (off, cnt), retired in zip(slots, (False, True, False)):
+        sl = slice(off, off + cnt)
+        if retired:
+            assert not np.any(pr[sl]) and not np.any(gr[sl]) and not np.any(mr[sl]) and not np.any(vr[sl])
+        else:
+            for a, b in ((pr, p), (gr, g), (mr, m), (vr, v)):
+                assert np.array_equal(a[sl], b[sl])
+    pk, _, _, _ = O.retire(p, g, m, v, [slots[1]], clear_params=False)
+    assert np.array_equal(pk, p)
