@@ -502,6 +502,57 @@ def run_single_step(problems: Dict[object, dict], state: Dict[object, AdapterSta
     return StepResult(prep, grads, new_state, outputs)
 
 
+@dataclass
+class ChainResult:
+    Y: np.ndarray                      # [T, d_L] output of the last layer
+    dX: np.ndarray                     # [T, d_0] gradient of the first layer's input
+    grads: List[Tuple[np.ndarray, np.ndarray]]   # per layer fp32 sums (dA, dB)
+
+
+def chained_forward_backward(X0, Ws: Sequence, As: Sequence, Bs: Sequence, dY_top, s: float,
+                             chunks: int, *, round_act=None, p: float = 0.0, seed: int = 0,
+                             opt_step: int = 0, layer_ids: Optional[Sequence[int]] = None,
+                             proj: int = 0) -> ChainResult:
+    """A stack of adapted linears in which layer l's output is layer l + 1's input ("4.3.
+    Training Guide", Truncated BPTT: the backward window is one chunk of tokens, and Gradient
+    accumulation: raw sums over the chunks in order). Per chunk: the forward runs through every
+    layer, then the backward runs through them in reverse, layer l's output gradient being layer
+    l + 1's input gradient. Activations handed from one layer to the next pass through round_act
+    (the activation dtype: identity for fp32, round to bf16 for bf16 activations), as they do
+    when stored between layers. Gradient sums accumulate in fp32 as in run_single_step."""
+    rnd = round_act if round_act is not None else (lambda a: a)
+    X0, dY_top = _f64(X0), _f64(dY_top)
+    T = X0.shape[0]
+    ct = T // chunks
+    nl = len(Ws)
+    ids = list(layer_ids) if layer_ids is not None else list(range(nl))
+    q = dropout_q(p) if p > 0 else 1.0
+    grads = [(np.zeros(np.shape(As[l]), np.float32), np.zeros(np.shape(Bs[l]), np.float32))
+             for l in range(nl)]
+    Y_out = np.zeros((T, np.shape(Ws[-1])[0]))
+    dX_in = np.zeros((T, np.shape(Ws[0])[1]))
+    for c in range(chunks):
+        rows = slice(c * ct, (c + 1) * ct)
+        xs, keeps = [], []
+        x = X0[rows]
+        for l in range(nl):
+            keep = dropout_keep(p, seed, opt_step, c, ids[l], proj, ct, np.shape(Ws[l])[1]) \
+                if p > 0 else None
+            xs.append(x)
+            keeps.append(keep)
+            x = rnd(lora_forward(x, Ws[l], As[l], Bs[l], s, keep, q).Y)
+        Y_out[rows] = x
+        g = dY_top[rows]
+        for l in reversed(range(nl)):
+            b = lora_backward(xs[l], Ws[l], As[l], Bs[l], g, s, keeps[l], q)
+            gA, gB = grads[l]
+            grads[l] = ((gA.astype(np.float64) + b.dA).astype(np.float32),
+                        (gB.astype(np.float64) + b.dB).astype(np.float32))
+            g = rnd(b.dX)
+        dX_in[rows] = g
+    return ChainResult(Y_out, dX_in, grads)
+
+
 def lora_adapter_grads(X, A, B, dY, s: float, keep=None, q: float = 1.0):
     """dA and dB alone (no frozen product needed): dA = s q (dY B)^T Xd, dB = s q dY^T (Xd A^T).
     Same definitions as lora_backward, for cases where the frozen products are too large."""

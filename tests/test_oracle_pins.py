@@ -504,3 +504,73 @@ def test_retire_clears_only_the_retired_slot():
                 assert np.array_equal(a[sl], b[sl])
     pk, _, _, _ = O.retire(p, g, m, v, [slots[1]], clear_params=False)
     assert np.array_equal(pk, p)
+
+
+# ---- chained layers ("4.3. Training Guide", Truncated BPTT, Gradient accumulation) ----
+def _chain(seed=5, dims=(6, 5, 7), r=2, T=4, zero_b=False):
+    rng = np.random.default_rng(seed)
+    Ws = [rng.standard_normal((dims[l + 1], dims[l])) / math.sqrt(dims[l]) for l in range(len(dims) - 1)]
+    As = [rng.standard_normal((r, dims[l])) for l in range(len(dims) - 1)]
+    Bs = [np.zeros((dims[l + 1], r)) if zero_b else 0.3 * rng.standard_normal((dims[l + 1], r))
+          for l in range(len(dims) - 1)]
+    X0 = rng.standard_normal((T, dims[0]))
+    dY = rng.standard_normal((T, dims[-1]))
+    return Ws, As, Bs, X0, dY
+
+
+def test_chain_equals_product_of_merged_weights():
+    Ws, As, Bs, X0, dY = _chain()
+    s = 1.5
+    res = O.chained_forward_backward(X0, Ws, As, Bs, dY, s, chunks=2)
+    M = [W + s * B @ A for W, A, B in zip(Ws, As, Bs)]
+    want_Y = X0 @ M[0].T @ M[1].T
+    want_dX = dY @ M[1] @ M[0]
+    np.testing.assert_allclose(res.Y, want_Y, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(res.dX, want_dX, rtol=1e-12, atol=1e-12)
+
+
+def test_chain_with_zero_adapters_gives_zero_dA_and_frozen_products():
+    Ws, As, Bs, X0, dY = _chain(zero_b=True)
+    res = O.chained_forward_backward(X0, Ws, As, Bs, dY, 2.0, chunks=1)
+    for gA, _ in res.grads:
+        assert not np.any(gA)
+    np.testing.assert_allclose(res.Y, X0 @ Ws[0].T @ Ws[1].T, rtol=1e-12, atol=1e-12)
+
+
+def test_chain_gradients_match_central_finite_differences():
+    Ws, As, Bs, X0, dY = _chain(seed=9)
+    s = 0.7
+    res = O.chained_forward_backward(X0, Ws, As, Bs, dY, s, chunks=2)
+
+    def loss(As_, Bs_):
+        Y = X0
+        for W, A, B in zip(Ws, As_, Bs_):
+            Y = Y @ (W + s * B @ A).T
+        return float(np.sum(Y * dY))
+
+    h = 1e-5
+    for l in range(2):
+        for name, idx in (("A", (1, 3)), ("B", (2, 0))):
+            Ap = [a.copy() for a in As]
+            Am = [a.copy() for a in As]
+            Bp = [b.copy() for b in Bs]
+            Bm = [b.copy() for b in Bs]
+            if name == "A":
+                Ap[l][idx] += h
+                Am[l][idx] -= h
+            else:
+                Bp[l][idx] += h
+                Bm[l][idx] -= h
+            fd = (loss(Ap, Bp) - loss(Am, Bm)) / (2 * h)
+            got = res.grads[l][0 if name == "A" else 1][idx]
+            assert abs(got - fd) <= 1e-5 * max(1.0, abs(fd))
+
+
+def test_chain_chunking_changes_only_the_summation_order():
+    Ws, As, Bs, X0, dY = _chain(seed=13, T=8)
+    one = O.chained_forward_backward(X0, Ws, As, Bs, dY, 1.0, chunks=1)
+    four = O.chained_forward_backward(X0, Ws, As, Bs, dY, 1.0, chunks=4)
+    np.testing.assert_allclose(one.Y, four.Y, rtol=1e-13, atol=1e-13)
+    for (a1, b1), (a4, b4) in zip(one.grads, four.grads):
+        np.testing.assert_allclose(a1, a4, rtol=1e-6, atol=1e-6)
+        np.testing.assert_allclose(b1, b4, rtol=1e-6, atol=1e-6)
