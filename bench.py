@@ -39,6 +39,9 @@ def parse():
     p.add_argument("--layers", type=int, default=0, help="override the layer count (0 = config's)")
     p.add_argument("--streams", type=int, default=4,
                    help="CUDA streams over the independent adapted linears of the step")
+    p.add_argument("--chain", action="store_true",
+                   help="stack the config's first square projection over its layers, each "
+                        "layer's output feeding the next (one stream)")
     p.add_argument("--no-graph", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--prof-class", type=int, default=0, help="kernel class to time (0 = auto)")
@@ -242,6 +245,44 @@ def make_single(cfg, layers, streams, device):
     return step, run, inputs, [step.scale_norm, step.status]
 
 
+def chain_config(cfg):
+    """The chained workload of a config: its first square projection stacked over the config's
+    layers (layer l's output is layer l + 1's input), one accumulation chunk per backward
+    window."""
+    sq = [pr for pr in cfg.projs if pr.in_dim == pr.out_dim]
+    if not sq or cfg.multi or cfg.dora:
+        raise SystemExit(f"--chain needs a single-adapter config with a square projection "
+                         f"({cfg.name} has none)")
+    return LI.with_overrides(cfg, projs=(sq[0],))
+
+
+def make_chain(cfg, layers, device):
+    from bwd_adapter_adamw_gb300 import binding as L
+    from bwd_adapter_adamw_gb300.step import ChainStep
+    pr = cfg.projs[0]
+    X0 = LI.make_x(cfg, 0, pr, device=device)
+    dY = LI.make_dy(cfg, layers - 1, pr, device=device)
+    Ws = [LI.make_w(cfg, l, pr, device=device) for l in range(layers)]
+    hp = L.make_hp(cfg.beta1, cfg.beta2, cfg.eps, cfg.wd, cfg.plus_ratio)
+    step = ChainStep(Ws, X0, dY, rank=cfg.rank, scale=_scale(cfg, L), dtype=cfg.dtype,
+                     chunks=cfg.chunks, dropout_p=cfg.dropout_p, seed=cfg.dropout_seed,
+                     max_norm=cfg.max_norm, hp=hp, device=device)
+    for lin in step.linears:
+        lin.A.copy_(LI.make_a(cfg, lin.layer, pr, device=device))
+        lin.B.copy_(LI.make_b(cfg, lin.layer, pr, device=device))
+    m, v = LI.make_adam_state(cfg, step.arena.n, "all", device=device)
+    step.arena.m.copy_(m)
+    step.arena.v.copy_(v)
+    step.prepare_weights()
+    lr = L.lora_lr_at(1 if cfg.sched == "cosine" else 0, cfg.lr, cfg.opt_step, cfg.warmup,
+                      cfg.total, cfg.min_lr)
+
+    def run():
+        step.run(cfg.opt_step, lr)
+
+    return step, run, [X0, dY], [step.scale_norm, step.status]
+
+
 def make_multi(cfg, streams, device):
     import torch
     from bwd_adapter_adamw_gb300 import binding as L
@@ -330,6 +371,8 @@ def run_reference(args):
     if rank != 0:
         return 0
     cfg = LI.CONFIGS[args.config]
+    if args.chain:
+        cfg = chain_config(cfg)   # same per-layer arithmetic; the chain only orders the layers
     layers = args.layers or cfg.layers
     budget = 240.0 / max(1, args.steps + args.warmup)
     vals = []
@@ -342,7 +385,8 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * cfg.tokens / value,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "impl": "reference",
-            "config": {"workload": workload_name(cfg, layers), "tokens_per_step": cfg.tokens},
+            "config": {"workload": workload_name(cfg, layers, args.chain),
+                       "tokens_per_step": cfg.tokens},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": vals[0]["cores"],
                              "kind": "oracle", "sample": vals[0]["sample"]},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -360,7 +404,7 @@ def step_stats(per_step):
     return {"median": statistics.median(xs), "p10": q[0], "p90": q[8], "n": len(xs)}
 
 
-def workload_name(cfg, layers):
+def workload_name(cfg, layers, chained=False):
     projs = "+".join(f"{p.name}:{p.in_dim}->{p.out_dim}" for p in cfg.projs)
     extra = []
     if cfg.multi:
@@ -371,6 +415,8 @@ def workload_name(cfg, layers):
         extra.append("DoRA")
     if cfg.dropout_p:
         extra.append(f"dropout {cfg.dropout_p}")
+    if chained:
+        extra.append("chained: layer l's output is layer l+1's input")
     return (f"{cfg.name}: {layers} layers x [{projs}], {cfg.dtype} frozen W, "
             f"{', '.join(extra)}, T={cfg.tokens} in {cfg.chunks} chunks")
 
@@ -388,7 +434,10 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=device)
     cfg = LI.CONFIGS[args.config]
     layers = args.layers or cfg.layers
-    if cfg.multi:
+    if args.chain:
+        cfg = chain_config(cfg)
+        step, run, inputs, results = make_chain(cfg, layers, device)
+    elif cfg.multi:
         step, run, inputs, results = make_multi(cfg, args.streams, device)
     else:
         step, run, inputs, results = make_single(cfg, layers, args.streams, device)
@@ -522,6 +571,8 @@ def run_ours(args):
         cnt = counts(cfg, layers if not cfg.multi else 1)
         per_launch = cnt["fwd_flops_per_launch"] if prof_class == L.LORA_PROF_FROZEN_FWD \
             else cnt["dx_flops_per_launch"]
+        if args.chain:   # the chained step launches each product once per chunk
+            per_launch /= cfg.chunks
         avg_kern = statistics.mean(kern_ms) if kern_ms else None
         if cfg.dtype == "f32":
             # 3xTF32 on tensor cores: three tf32 products per fp32 product; tf32 dense rate is
@@ -564,11 +615,13 @@ def run_ours(args):
             "step_roofline": step_roofline,
             "scaling": "weak", "vs_baseline": None,
             "dtype": "f32" if cfg.dtype == "f32" else "bf16", "data": "synthetic",
-            "config": {"workload": workload_name(cfg, layers), "tokens_per_step": tokens,
+            "config": {"workload": workload_name(cfg, layers, args.chain),
+                       "tokens_per_step": tokens,
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                        "l2": "inputs larger than L2 (frozen W alone exceeds 129 MB)"
                        if cfg.name != "c1" else "inputs fit in L2",
-                       "cuda_graph": graph is not None, "streams": args.streams},
+                       "cuda_graph": graph is not None,
+                       "streams": 1 if args.chain else args.streams},
             "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": punit,
                          "frac": (achieved / peak) if achieved else None, "traffic": traffic,
                          "traffic_note": traffic_note,

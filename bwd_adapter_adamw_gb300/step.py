@@ -225,6 +225,51 @@ class LoraStep:
                        self.groups(0.0, 0), zero_grads)
 
 
+class ChainStep(LoraStep):
+    """One optimizer step over a stack of adapted linears in which layer l's output is layer
+    l + 1's input ("4.3. Training Guide", Truncated BPTT: the backward window is one chunk of
+    tokens; Gradient accumulation: raw sums over the chunks in order). Each chunk runs forward
+    through every layer and then backward through them in reverse, layer l's output gradient
+    being layer l + 1's input gradient, all on one stream (each launch depends on the one
+    before). The layers share the adapter rank, scale and dtype; W_l is [d_{l+1}, d_l]."""
+
+    def __init__(self, Ws: Sequence[torch.Tensor], X0: torch.Tensor, dY_top: torch.Tensor, *,
+                 layer_ids: Optional[Sequence[int]] = None, proj_id: int = 0, **kw):
+        if kw.get("dora"):
+            raise ValueError("the chained step has no DoRA mode")
+        T, act, dev = X0.shape[0], X0.dtype, X0.device
+        for l in range(1, len(Ws)):
+            if Ws[l].shape[1] != Ws[l - 1].shape[0]:
+                raise ValueError("layer widths do not chain")
+        ids = list(layer_ids) if layer_ids is not None else list(range(len(Ws)))
+        lins = [Linear(ids[l], proj_id, None, W, None) for l, W in enumerate(Ws)]
+        for lin in lins:
+            lin.Y = torch.empty((T, lin.out_dim), dtype=act, device=dev)
+            lin.dX = torch.empty((T, lin.in_dim), dtype=act, device=dev)
+        for l, lin in enumerate(lins):
+            lin.X = X0 if l == 0 else lins[l - 1].Y          # the previous layer's output
+            lin.dY = dY_top if l == len(lins) - 1 else lins[l + 1].dX
+        kw["n_streams"] = 1
+        super().__init__(lins, tokens=T, **kw)
+
+    def forward_backward(self, opt_step: int, per_chunk_calls: bool = True):
+        """Enqueue the chunked forward / reverse backward of the whole stack (gradients
+        accumulate into the arena)."""
+        st = torch.cuda.current_stream(self.device)
+        ws = self.ws[0]
+        ct = self.T // self.chunks
+        for c in range(self.chunks):
+            ctx = L.make_ctx(opt_step, c, ct)
+            sl = slice(c * ct, (c + 1) * ct)
+            for l in self.linears:
+                L.lora_forward(self.desc(l), ctx, ct, l.X[sl], l.W, l.Wp, l.A, l.B, None, None,
+                               l.Y[sl], l.H[sl], ws, stream=st)
+            for l in reversed(self.linears):
+                L.lora_backward(self.desc(l), ctx, ct, l.X[sl], l.Wp, l.A, l.B, l.dY[sl],
+                                l.H[sl], None, None, None, l.dX[sl], l.gA, l.gB, None, ws,
+                                stream=st)
+
+
 # ----------------------------------------------------------------------------------------------
 @dataclass
 class MultiLinear:
