@@ -218,6 +218,100 @@ def lora_backward(X, W, A, B, dY, s: float, keep=None, q: float = 1.0, mag=None,
 
 
 # ----------------------------------------------------------------------------------------------
+# FP8 frozen base ("LoRA Training and Serving" / Quantized rollout: an FP8 base under a bf16-
+# trained adapter; "Backward Bug Hunts" and "4.3. Training Guide" / Quick start: quantized frozen
+# weights under the LoRA backward)
+# ----------------------------------------------------------------------------------------------
+# E4M3 (OCP 8-bit float): sign, 4 exponent bits (bias 7), 3 mantissa bits, no infinities, NaN =
+# S.1111.111, largest finite 448 = 1.75 * 2^8, smallest normal 2^-6, subnormals m * 2^-9.
+E4M3_MAX = 448.0
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """uint8 codes -> float64 values (NaN for S.1111.111)."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = c & 0x7
+    val = np.where(e == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.power(2.0, e - 7))
+    val = np.where((e == 15) & (m == 7), np.nan, val)
+    return sign * val
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """float32 values -> uint8 codes: round to nearest, ties to even, finite values beyond the
+    largest code saturate to +-448, NaN -> 0x7F with the sign bit of x."""
+    x = np.asarray(x, dtype=np.float32)
+    out = np.zeros(x.shape, dtype=np.uint8)
+    flat, of = x.reshape(-1), out.reshape(-1)
+    for i, v in enumerate(flat.astype(np.float64)):
+        sign = 0x80 if math.copysign(1.0, v) < 0 else 0
+        if math.isnan(v):
+            of[i] = sign | 0x7F
+            continue
+        a = abs(v)
+        if a >= E4M3_MAX:
+            of[i] = sign | 0x7E
+            continue
+        if a < 2.0 ** -6:                  # subnormal grid: spacing 2^-9 (q = 8 is 2^-6)
+            q = round(a / 2.0 ** -9)       # Python round: ties to even
+            of[i] = sign | q
+            continue
+        e = math.floor(math.log2(a))
+        while 2.0 ** e > a:                # guard the log against rounding
+            e -= 1
+        while 2.0 ** (e + 1) <= a:
+            e += 1
+        q = round(a / 2.0 ** (e - 3))      # 8 .. 16 steps of 2^(e-3)
+        if q == 16:
+            e, q = e + 1, 8
+        code = ((e + 7) << 3) | (q - 8)
+        of[i] = sign | min(code, 0x7E)     # 464 and above round past 448: saturate
+    return out
+
+
+def quantize_rows_e4m3(M):
+    """Per-row scaled E4M3 codes of an fp32 (or bf16-valued) matrix: s_r = amax_r / 448 in fp32
+    (1 when that is not positive), codes = e4m3(M[r, :] / s_r) with the division in fp32.
+    Returns (codes uint8 [R, K], scales float32 [R])."""
+    M = np.asarray(M, dtype=np.float32)
+    amax = np.max(np.abs(M), axis=1) if M.shape[1] else np.zeros(M.shape[0], np.float32)
+    sc = (amax / np.float32(E4M3_MAX)).astype(np.float32)
+    sc = np.where(sc > 0, sc, np.float32(1.0)).astype(np.float32)
+    q = (M / sc[:, None]).astype(np.float32)
+    return e4m3_encode(q), sc
+
+
+def fp8_product(Xc, sx, Wc, sw) -> np.ndarray:
+    """diag(sx) (dec(Xc) dec(Wc)^T) diag(sw): the frozen product on E4M3 operands with per-row
+    scales of X's rows and W's rows (the contraction runs over the columns of both)."""
+    return (_f64(sx)[:, None] * (e4m3_decode(Xc) @ e4m3_decode(Wc).T)) * _f64(sw)[None, :]
+
+
+def lora_forward_fp8(X, W, A, B, s: float, keep=None, q: float = 1.0) -> Forward:
+    """Y = fp8 frozen product of (X, W) + s q (Xd A^T) B^T: the frozen term runs on the per-row
+    E4M3 quantisations of X (per token) and W (per output row); the adapter branch reads the
+    bf16 X unchanged."""
+    Xc, sx = quantize_rows_e4m3(X)
+    Wc, sw = quantize_rows_e4m3(W)
+    X64, A, B = _f64(X), _f64(A), _f64(B)
+    Xd = X64 if keep is None else keep * X64
+    H = Xd @ A.T
+    Y = fp8_product(Xc, sx, Wc, sw) + (s * q) * (H @ B.T)
+    return Forward(Y, H, Y)
+
+
+def lora_dx_fp8(dY, W, A, G, s: float, keep=None, q: float = 1.0) -> np.ndarray:
+    """dX = fp8 product of (dY, W^T) + s q (G A) * M: the frozen term runs on the per-token
+    E4M3 quantisation of dY and the per-row quantisation of W^T (one scale per input column
+    of W); G = dY B is taken in full precision as in lora_backward."""
+    Dc, sd = quantize_rows_e4m3(dY)
+    Wtc, swt = quantize_rows_e4m3(np.asarray(W, np.float32).T)
+    M = 1.0 if keep is None else keep
+    return fp8_product(Dc, sd, Wtc, swt) + (s * q) * (_f64(G) @ _f64(A)) * M
+
+
+# ----------------------------------------------------------------------------------------------
 # grad prepare and optimizer  ("4.3. Training Guide" / Gradient clipping, Optimizer)
 # ----------------------------------------------------------------------------------------------
 @dataclass

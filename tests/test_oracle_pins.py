@@ -574,3 +574,83 @@ def test_chain_chunking_changes_only_the_summation_order():
     for (a1, b1), (a4, b4) in zip(one.grads, four.grads):
         np.testing.assert_allclose(a1, a4, rtol=1e-6, atol=1e-6)
         np.testing.assert_allclose(b1, b4, rtol=1e-6, atol=1e-6)
+
+
+# ---- FP8 E4M3 frozen base ----
+def test_e4m3_reference_values():
+    # OCP 8-bit float E4M3: 448 largest finite, 2^-6 smallest normal, 2^-9 smallest subnormal,
+    # 1.0 = 0x38, S.1111.111 is NaN (no infinities)
+    dec = O.e4m3_decode(np.array([0x7E, 0xFE, 0x38, 0x08, 0x01, 0x00, 0x80, 0x77, 0x3C],
+                                 np.uint8))
+    np.testing.assert_array_equal(dec, [448.0, -448.0, 1.0, 2.0 ** -6, 2.0 ** -9, 0.0, -0.0,
+                                        240.0, 1.5])
+    assert np.isnan(O.e4m3_decode(np.array([0x7F, 0xFF], np.uint8))).all()
+
+
+def test_e4m3_round_trip_and_monotone():
+    codes = np.arange(256, dtype=np.uint8)
+    vals = O.e4m3_decode(codes)
+    fin = ~np.isnan(vals)
+    assert np.array_equal(O.e4m3_encode(vals[fin].astype(np.float32)), codes[fin])
+    xs = np.linspace(0.0, 500.0, 20001).astype(np.float32)
+    dec = O.e4m3_decode(O.e4m3_encode(xs))
+    assert np.all(np.diff(dec) >= 0)
+
+
+def test_e4m3_ties_to_even_and_saturation():
+    x = np.array([1.0625, 1.1875, 2.0 ** -10, 3 * 2.0 ** -11, 463.9, 464.0, 1e6, -1e6, -0.0],
+                 np.float32)
+    np.testing.assert_array_equal(O.e4m3_encode(x), [0x38, 0x3A, 0x00, 0x01, 0x7E, 0x7E, 0x7E,
+                                                     0xFE, 0x80])
+
+
+def test_e4m3_relative_error_bound():
+    # three mantissa bits: round-to-nearest error <= 2^-4 of the value in the normal range
+    rng = np.random.default_rng(0)
+    x = np.exp(rng.uniform(np.log(2.0 ** -6), np.log(448.0), 5000)).astype(np.float32)
+    err = np.abs(O.e4m3_decode(O.e4m3_encode(x)) - x) / x
+    assert err.max() <= 2.0 ** -4 + 1e-12
+
+
+def test_quantize_rows_maps_each_row_max_to_448():
+    rng = np.random.default_rng(1)
+    M = (rng.standard_normal((16, 40)) * np.exp(rng.uniform(-5, 5, (16, 1)))).astype(np.float32)
+    M[3] = 0.0
+    codes, sc = O.quantize_rows_e4m3(M)
+    assert sc[3] == 1.0 and not np.any(codes[3] & 0x7F)
+    for r in range(16):
+        if r == 3:
+            continue
+        assert np.max(np.abs(O.e4m3_decode(codes[r]))) == 448.0
+        assert sc[r] == np.float32(np.max(np.abs(M[r])) / np.float32(448.0))
+
+
+def test_fp8_product_brute_force_and_error_bound():
+    rng = np.random.default_rng(2)
+    X = rng.standard_normal((3, 20)).astype(np.float32)
+    W = rng.standard_normal((4, 20)).astype(np.float32)
+    Xc, sx = O.quantize_rows_e4m3(X)
+    Wc, sw = O.quantize_rows_e4m3(W)
+    got = O.fp8_product(Xc, sx, Wc, sw)
+    for t in range(3):
+        for n in range(4):
+            acc = 0.0
+            for k in range(20):
+                acc += O.e4m3_decode([Xc[t, k]])[0] * O.e4m3_decode([Wc[n, k]])[0]
+            assert abs(got[t, n] - float(sx[t]) * acc * float(sw[n])) <= 1e-12 * max(1.0, abs(acc))
+    # each operand is within 2^-4 (relative) of its value, or within half a subnormal step
+    bound = (np.abs(X) @ np.abs(W).T) * (2 * 2.0 ** -4 + 2.0 ** -8) \
+        + 2.0 ** -10 * (sx[:, None] * (np.abs(W).sum(1))[None, :] + (np.abs(X).sum(1))[:, None] * sw[None, :])
+    assert np.all(np.abs(got - X.astype(np.float64) @ W.T.astype(np.float64)) <= bound)
+
+
+def test_fp8_forward_with_zero_adapter_is_the_fp8_product():
+    rng = np.random.default_rng(3)
+    X = rng.standard_normal((5, 16)).astype(np.float32)
+    W = rng.standard_normal((6, 16)).astype(np.float32)
+    A = rng.standard_normal((4, 16)).astype(np.float32)
+    B = np.zeros((6, 4), np.float32)
+    f = O.lora_forward_fp8(X, W, A, B, 2.0)
+    Xc, sx = O.quantize_rows_e4m3(X)
+    Wc, sw = O.quantize_rows_e4m3(W)
+    np.testing.assert_array_equal(f.Y, O.fp8_product(Xc, sx, Wc, sw))
