@@ -582,6 +582,12 @@ def run_ours(args):
             bound, punit = "tensor", "TFLOP/s"
             note = (f"3xTF32 effective: measured bf16 {peaks['bf16_tflops']:.0f} x 1.1/2.25 "
                     f"= {tf32:.0f} tf32 TF/s, / 3 products ({peak_src})")
+        elif cfg.dtype == "bf16fp8":
+            # E4M3 products: the measured bf16 rate x the nominal fp8 : bf16 ratio (4.5 : 2.25)
+            peak = peaks["bf16_tflops"] * 4.5 / 2.25
+            bound, punit = "tensor", "TFLOP/s"
+            note = (f"fp8 effective: measured bf16 {peaks['bf16_tflops']:.0f} x 4.5/2.25 "
+                    f"({peak_src})")
         else:
             peak = peaks["bf16_tflops"]
             bound, punit = "tensor", "TFLOP/s"
@@ -614,7 +620,8 @@ def run_ours(args):
             "step_ms": step_stats(per_step),
             "step_roofline": step_roofline,
             "scaling": "weak", "vs_baseline": None,
-            "dtype": "f32" if cfg.dtype == "f32" else "bf16", "data": "synthetic",
+            "dtype": {"f32": "f32", "bf16": "bf16"}.get(cfg.dtype, "e4m3 frozen, bf16 adapter"),
+            "data": "synthetic",
             "config": {"workload": workload_name(cfg, layers, args.chain),
                        "tokens_per_step": tokens,
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",

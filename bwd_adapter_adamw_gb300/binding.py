@@ -24,6 +24,7 @@ LORA_ERR_NONFINITE = 6
 
 LORA_F32 = 0
 LORA_BF16 = 1
+LORA_BF16_FP8 = 2
 LORA_SCHED_CONSTANT = 0
 LORA_SCHED_WARMUP_COSINE = 1
 LORA_MAX_RANK = 64
@@ -98,6 +99,7 @@ def _load() -> C.CDLL:
         "multi_lora_backward": (C.c_int, [DP, CP, I64, P, P, I32, P, P, I32,
                                           C.POINTER(lora_slot), P, P, P, P, SZ, P]),
         "lora_dropout_mask": (C.c_int, [DP, CP, I64, P, P]),
+        "lora_quantize_e4m3": (C.c_int, [P, I64, I64, P, P, P]),
         "multi_lora_token_slots": (C.c_int, [I64, I32, P, P, I32, P, P]),
         "lora_profile_arm": (C.c_int, [I32, C.POINTER(C.c_void_p), C.POINTER(C.c_void_p), I32]),
         "lora_profile_used": (I32, []),
@@ -119,7 +121,7 @@ EXPORTED = ("lora_status_string", "lora_scale", "lora_lr_at", "lora_workspace_si
             "lora_grad_prepare_workspace_size", "lora_grad_prepare", "lora_grad_prepare_noalloc",
             "lora_adamw_step", "lora_snapshot", "lora_restore", "lora_retire",
             "multi_lora_workspace_size", "multi_lora_forward", "multi_lora_backward",
-            "lora_dropout_mask", "multi_lora_token_slots", "lora_profile_arm",
+            "lora_dropout_mask", "lora_quantize_e4m3", "multi_lora_token_slots", "lora_profile_arm",
             "lora_profile_used", "lora_launch_counter", "lora_last_cuda_error",
             "lora_device_error")
 
@@ -291,6 +293,13 @@ def lora_retire(params, grads, m, v, groups, clear_params=False, stream=None, ch
     st = _lib.lora_retire(_ptr(params), _ptr(grads), _ptr(m), _ptr(v), len(groups), groups,
                           1 if clear_params else 0, _stream(stream))
     return _check(st, "lora_retire") if check else st
+
+
+def lora_quantize_e4m3(src, codes, scales, stream=None, check=True):
+    """Test hook: per-row E4M3 codes and scales of a bf16 [rows, K] matrix."""
+    rows, K = src.shape
+    st = _lib.lora_quantize_e4m3(_ptr(src), rows, K, _ptr(codes), _ptr(scales), _stream(stream))
+    return _check(st, "lora_quantize_e4m3") if check else st
 
 
 def make_slots(slots: Sequence[dict]):

@@ -58,7 +58,8 @@ int64_t max_red_items(int64_t T, int32_t n_seg) {
 int check_desc(const lora_desc* d, int64_t T, bool multi) {
   if (!d || T < 0) return LORA_ERR_INVALID;
   if (d->in_dim <= 0 || d->out_dim <= 0) return LORA_ERR_INVALID;
-  if (d->dtype != LORA_F32 && d->dtype != LORA_BF16) return LORA_ERR_INVALID;
+  if (d->dtype != LORA_F32 && d->dtype != LORA_BF16 && d->dtype != LORA_BF16_FP8)
+    return LORA_ERR_INVALID;
   if (d->rank <= 0) return LORA_ERR_INVALID;
   if (d->rank > LORA_MAX_RANK || (d->rank % 4) != 0) return LORA_ERR_UNSUPPORTED;
   if ((d->in_dim % 8) != 0 || (d->out_dim % 8) != 0) return LORA_ERR_ALIGN;
@@ -66,6 +67,11 @@ int check_desc(const lora_desc* d, int64_t T, bool multi) {
   if (d->proj_id > 0xFFFFu) return LORA_ERR_INVALID;
   if (d->dora != 0 && d->dora != 1) return LORA_ERR_INVALID;
   if (multi && d->dora) return LORA_ERR_UNSUPPORTED;
+  if (d->dtype == LORA_BF16_FP8) {
+    // E4M3 rows are K bytes (16-byte TMA strides); a row is quantised from registers
+    if ((d->in_dim % 16) != 0 || (d->out_dim % 16) != 0) return LORA_ERR_ALIGN;
+    if (multi || d->dora || d->in_dim > 16384 || d->out_dim > 16384) return LORA_ERR_UNSUPPORTED;
+  }
   if (!multi && !std::isfinite(d->scale)) return LORA_ERR_INVALID;
   if (T >= (int64_t(1) << 31) - kRedTileT) return LORA_ERR_UNSUPPORTED;
   return LORA_OK;
@@ -211,14 +217,44 @@ struct Layout {
   TokenItem* items_db; int32_t* count_db; int64_t max_db; int span_db;
   TokenItem* items_da; int32_t* count_da; int64_t max_da; int span_da;
   float* red_part;     // [items][rmax][N]
+  // FP8 frozen base
+  uint8_t* Aq;         // [T, max(in, out)] E4M3 codes of X (forward) or dY' (backward)
+  float* sq;           // [T] their row scales
+  float* Pq;           // [T, rank] Hs or Gs divided by sq
+  float* Qq;           // [max(in, out), rank] B divided by the W row scales, or A^T by W^T's
   size_t bytes;
 };
+
+// E4M3 prepared weight: [W8 (out x in) | sw (out) | WT8 (in x out) | swT (in)], 16-byte sections
+struct Fp8Prep {
+  const uint8_t* W8;
+  const float* sw;
+  const uint8_t* WT8;
+  const float* swT;
+};
+size_t al16_up(size_t b) { return (b + 15) / 16 * 16; }
+size_t fp8_prep_bytes(int64_t out, int64_t in) {
+  return al16_up((size_t)out * in) + al16_up((size_t)out * 4) + al16_up((size_t)in * out) +
+         al16_up((size_t)in * 4);
+}
+Fp8Prep fp8_prep(const void* Wp, int64_t out, int64_t in) {
+  const uint8_t* b = static_cast<const uint8_t*>(Wp);
+  Fp8Prep f;
+  f.W8 = b;
+  b += al16_up((size_t)out * in);
+  f.sw = reinterpret_cast<const float*>(b);
+  b += al16_up((size_t)out * 4);
+  f.WT8 = b;
+  b += al16_up((size_t)in * out);
+  f.swT = reinterpret_cast<const float*>(b);
+  return f;
+}
 
 Layout carve(const lora_desc* d, int64_t T, int32_t n_seg, int n_slots, int64_t rank_sum,
              bool backward, void* ws) {
   Layout L{};
   Carve c(ws);
-  const bool tc = d->dtype == LORA_BF16;
+  const bool tc = d->dtype != LORA_F32;
   L.gmax = max_gemm_items(T, n_seg);
   L.rmax = max_red_items(T, n_seg);
   L.gitems = c.take<TokenItem>((size_t)L.gmax);
@@ -258,6 +294,13 @@ Layout carve(const lora_desc* d, int64_t T, int32_t n_seg, int n_slots, int64_t 
   } else if (!tc) {
     L.ritems = c.take<TokenItem>((size_t)L.rmax);
     L.rcount = c.take<int32_t>(4);
+  }
+  if (d->dtype == LORA_BF16_FP8) {
+    const int64_t kmax = d->in_dim > d->out_dim ? d->in_dim : d->out_dim;
+    L.Aq = c.take<uint8_t>((size_t)T * kmax);
+    L.sq = c.take<float>((size_t)T);
+    L.Pq = c.take<float>((size_t)T * d->rank);
+    L.Qq = c.take<float>((size_t)kmax * d->rank);
   }
   if (!tc) {
     const int64_t kmax = d->in_dim > d->out_dim ? d->in_dim : d->out_dim;
@@ -331,9 +374,9 @@ int tc_shrink(const lora_desc* d, const DropParams& dp, int64_t T, const void* X
 
 // forward, bf16 activations: shrink and frozen product on tensor cores
 int run_forward_tc(const lora_desc* d, const DropParams& dp, int64_t T, const void* X,
-                   const void* W, int32_t n_seg, const int32_t* seg_start, const int32_t* seg_slot,
-                   const Slots& s, const float* ratio_src_m, const float* ratio_src_n, void* Y,
-                   float* H, void* ws, cudaStream_t st) {
+                   const void* W, const void* Wprep, int32_t n_seg, const int32_t* seg_start,
+                   const int32_t* seg_slot, const Slots& s, const float* ratio_src_m,
+                   const float* ratio_src_n, void* Y, float* H, void* ws, cudaStream_t st) {
   Layout L = carve(d, T, n_seg, s.n, s.rank_sum, false, ws);
   clear_stale();
   if (n_seg < 0)
@@ -346,6 +389,9 @@ int run_forward_tc(const lora_desc* d, const DropParams& dp, int64_t T, const vo
     LORA_TRY(launch_ratio(ratio_src_m, ratio_src_n, d->out_dim, L.ratio, st));
     ratio = L.ratio;
   }
+  const bool fp8 = d->dtype == LORA_BF16_FP8;
+  if (fp8)   // E4M3 codes and per-token scales of X for the frozen product
+    LORA_TRY(launch_quant_rows_e4m3(X, T, d->in_dim, L.Aq, L.sq, st));
   int rc = tc_shrink(d, dp, T, X, n_seg, s, L, H, st);
   if (rc) return rc;
   TcGemmArgs t{};
@@ -353,6 +399,15 @@ int run_forward_tc(const lora_desc* d, const DropParams& dp, int64_t T, const vo
   t.p = H; t.ldp = d->rank; t.n_slots = s.n;
   for (int k = 0; k < s.n; ++k) { t.q[k] = s.B[k]; t.q_rank[k] = s.rank[k]; }
   t.n_colscale = ratio; t.out = Y; t.ldo = d->out_dim;
+  if (fp8) {
+    // Y = sx sw (X8 W8^T) + Hs B^T = sx sw (X8 W8^T + (Hs / sx)(B / sw)^T): one accumulator
+    const Fp8Prep f = fp8_prep(Wprep, d->out_dim, d->in_dim);
+    LORA_TRY(launch_div_rows(H, d->rank, L.sq, T, d->rank, L.Pq, d->rank, st));
+    LORA_TRY(launch_div_rows(s.B[0], d->rank, f.sw, d->out_dim, d->rank, L.Qq, d->rank, st));
+    t.a = L.Aq; t.b = f.W8; t.fp8 = 1;
+    t.p = L.Pq; t.q[0] = L.Qq;
+    t.m_rowscale = L.sq; t.n_colscale = f.sw;
+  }
   t.items = L.gitems; t.n_items = L.gcount; t.max_items = (int)L.gmax; t.drop = dp;
   LORA_TRY(launch_tc_gemm(t, st, LORA_PROF_FROZEN_FWD));
   return LORA_OK;
@@ -433,6 +488,16 @@ int run_backward_tc(const lora_desc* d, const DropParams& dp, int64_t T, const v
     for (int k = 0; k < s.n; ++k) { t.q[k] = At[k]; t.q_rank[k] = s.rank[k]; }
     t.lora_separate = dp.enabled; t.out = dX; t.ldo = d->in_dim;
     t.items = L.gitems; t.n_items = L.gcount; t.max_items = (int)L.gmax; t.drop = dp;
+    if (d->dtype == LORA_BF16_FP8) {
+      // dX = sd swT (dY8 WT8^T) + Gs A: the LoRA operands divided by the same scales
+      const Fp8Prep f = fp8_prep(Wt, d->out_dim, d->in_dim);
+      LORA_TRY(launch_quant_rows_e4m3(dYp, T, d->out_dim, L.Aq, L.sq, st));
+      LORA_TRY(launch_div_rows(L.Gs, d->rank, L.sq, T, d->rank, L.Pq, d->rank, st));
+      LORA_TRY(launch_div_rows(At[0], d->rank, f.swT, d->in_dim, d->rank, L.Qq, d->rank, st));
+      t.a = L.Aq; t.b = f.WT8; t.fp8 = 1;
+      t.p = L.Pq; t.q[0] = L.Qq;
+      t.m_rowscale = L.sq; t.n_colscale = f.swT;
+    }
     LORA_TRY(launch_tc_gemm(t, st, LORA_PROF_FROZEN_DX));
   }
   const size_t split_bytes = (size_t)2 * s.rank_sum * L.ldt * sizeof(uint16_t);
@@ -477,8 +542,8 @@ int run_forward(const lora_desc* d, const DropParams& dp, int64_t T, const void*
                 const void* Wprep, int32_t n_seg, const int32_t* seg_start, const int32_t* seg_slot, const Slots& s,
                 const float* ratio_src_m, const float* ratio_src_n, void* Y, float* H, void* ws,
                 cudaStream_t st) {
-  if (d->dtype == LORA_BF16)
-    return run_forward_tc(d, dp, T, X, W, n_seg, seg_start, seg_slot, s, ratio_src_m,
+  if (d->dtype != LORA_F32)
+    return run_forward_tc(d, dp, T, X, W, Wprep, n_seg, seg_start, seg_slot, s, ratio_src_m,
                           ratio_src_n, Y, H, ws, st);
   Layout L = carve(d, T, n_seg, s.n, s.rank_sum, false, ws);
   clear_stale();
@@ -531,7 +596,7 @@ int run_backward(const lora_desc* d, const DropParams& dp, int64_t T, const void
                  int32_t n_seg, const int32_t* seg_start, const int32_t* seg_slot, const Slots& s,
                  const void* dY, const float* H, const float* dora_m, const float* dora_n,
                  const void* Y_save, void* dX, float* dm, void* ws, cudaStream_t st) {
-  if (d->dtype == LORA_BF16)
+  if (d->dtype != LORA_F32)
     return run_backward_tc(d, dp, T, X, Wt, n_seg, seg_start, seg_slot, s, dY, H, dora_m, dora_n,
                            Y_save, dX, dm, ws, st);
   Layout L = carve(d, T, n_seg, s.n, s.rank_sum, true, ws);
@@ -753,6 +818,7 @@ size_t multi_lora_workspace_size(const lora_desc* d, int64_t T, int32_t n_seg, i
 size_t lora_prepared_weight_size(const lora_desc* d) {
   if (check_desc(d, 0, false) != LORA_OK) return 0;
   const size_t n = (size_t)d->out_dim * (size_t)d->in_dim;
+  if (d->dtype == LORA_BF16_FP8) return fp8_prep_bytes(d->out_dim, d->in_dim);
   return d->dtype == LORA_F32 ? 16 * n : 2 * n;
 }
 
@@ -762,6 +828,16 @@ int lora_prepare_weight(const lora_desc* d, const void* W, void* W_prep, void* s
   if (!W || !W_prep) return LORA_ERR_INVALID;
   if (!al16(W) || !al16(W_prep)) return LORA_ERR_ALIGN;
   clear_stale();
+  if (d->dtype == LORA_BF16_FP8) {
+    // W8: W's rows (forward: K = in), WT8: W's columns as rows (dX: K = out)
+    const Fp8Prep f = fp8_prep(W_prep, d->out_dim, d->in_dim);
+    cudaError_t e = launch_quant_rows_e4m3(W, d->out_dim, d->in_dim, const_cast<uint8_t*>(f.W8),
+                                           const_cast<float*>(f.sw), (cudaStream_t)stream);
+    if (e == cudaSuccess)
+      e = launch_quant_cols_e4m3(W, d->out_dim, d->in_dim, const_cast<uint8_t*>(f.WT8),
+                                 const_cast<float*>(f.swT), (cudaStream_t)stream);
+    return cuda_status(e);
+  }
   return cuda_status(launch_prepare_weight(d->dtype, W, W_prep, d->out_dim, d->in_dim,
                                            (cudaStream_t)stream));
 }
@@ -1031,6 +1107,16 @@ int lora_retire(float* params, float* grads, float* m, float* v, int32_t n_group
   const int flags = kMaintZeroG | kMaintZeroMV | (clear_params ? kMaintZeroDst : 0);
   return cuda_status(launch_group_maint(params, nullptr, grads, m, v, g, flags,
                                         (cudaStream_t)stream));
+}
+
+int lora_quantize_e4m3(const void* src, int64_t rows, int64_t K, uint8_t* codes, float* scales,
+                       void* stream) {
+  if (rows < 0 || K <= 0 || !src || !codes || !scales) return LORA_ERR_INVALID;
+  if (K % 16) return LORA_ERR_ALIGN;
+  if (K > 16384) return LORA_ERR_UNSUPPORTED;
+  if (!al16(src) || !al16(codes) || (reinterpret_cast<uintptr_t>(scales) & 3u)) return LORA_ERR_ALIGN;
+  clear_stale();
+  return cuda_status(launch_quant_rows_e4m3(src, rows, K, codes, scales, (cudaStream_t)stream));
 }
 
 int lora_dropout_mask(const lora_desc* d, const lora_ctx* c, int64_t T, uint8_t* d_mask,

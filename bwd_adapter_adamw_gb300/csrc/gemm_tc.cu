@@ -70,6 +70,7 @@ struct GemmCfg {
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*barriers*/ + 1024 /*alignment*/;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
   static constexpr uint32_t kIdescBF16 = tc::idesc(tc::kFmtBF16, kBM, BN);
+  static constexpr uint32_t kIdescE4M3 = tc::idesc(tc::kFmtE4M3, kBM, BN);
   static constexpr uint32_t kIdescTF32 = tc::idesc(tc::kFmtTF32, kBM, BN);
   static_assert(kStageBytes % 1024 == 0, "stage alignment of the 128-byte swizzle");
 };
@@ -92,6 +93,7 @@ struct TcParams {
   int32_t lora_separate;
   int32_t q_rank[LORA_MAX_SLOTS];
   const float* n_colscale;
+  const float* m_rowscale;
   void* out;
   int64_t ldo;
   int64_t n_out;
@@ -118,7 +120,10 @@ __device__ __forceinline__ bool decode_tile(const TcParams& p, int t, TokenItem&
   return get_item(p.items, p.n_items, first + idx % gsize, p.T, it);
 }
 
-template <int BN>
+// F8: the main K-blocks are E4M3 codes (128 per 128-byte row, kind::f8f6f4); the accumulator is
+// then in code units and the epilogue multiplies by the row and column scales. The LoRA K-blocks
+// arrive pre-divided by the same scales, so that they share the accumulator.
+template <int BN, bool F8>
 __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__ TcParams p) {
   grid_dep_sync();
   using C = GemmCfg<BN>;
@@ -174,8 +179,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
           uint8_t* sb = sa + kABytes;
           mbar_expect_tx(&full_bar[s], kStageBytes);
           if (kb < p.nk_main) {
-            tma_load_2d(sa, &p.ta, &full_bar[s], kb * 64, it.t0);
-            tma_load_2d(sb, &p.tb, &full_bar[s], kb * 64, n0);
+            constexpr int kKBlock = F8 ? 128 : 64;   // elements in one 128-byte row
+            tma_load_2d(sa, &p.ta, &full_bar[s], kb * kKBlock, it.t0);
+            tma_load_2d(sb, &p.tb, &full_bar[s], kb * kKBlock, n0);
           } else {
             const int j = kb - p.nk_main;
             tma_load_2d(sa, &p.tp, &full_bar[s], j * 32, it.t0);
@@ -214,7 +220,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
           if (kb < p.nk_main) {
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-              umma_f16(dm, da + 2 * k, db + 2 * k, C::kIdescBF16, (kb > 0 || k > 0) ? 1u : 0u);
+              if constexpr (F8)
+                umma_f8(dm, da + 2 * k, db + 2 * k, C::kIdescE4M3, (kb > 0 || k > 0) ? 1u : 0u);
+              else
+                umma_f16(dm, da + 2 * k, db + 2 * k, C::kIdescBF16, (kb > 0 || k > 0) ? 1u : 0u);
           } else {
             const uint32_t d = sep ? tmem + 256u : dm;
             const bool first = sep && kb == p.nk_main;
@@ -276,6 +285,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
             if ((keep[c] >> jj) & 1u) v[jj] += w[jj];
         }
         const int64_t nb = (int64_t)n0 + c * 32;
+        if (p.m_rowscale && row_ok) {
+          const float rs = __ldg(p.m_rowscale + m);
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) v[jj] *= rs;
+        }
         if (p.n_colscale) {
 #pragma unroll
           for (int jj = 0; jj < 32; ++jj)
@@ -350,16 +364,17 @@ bool make_map_2d(CUtensorMap* map, const void* ptr, CUtensorMapDataType dt, int 
 }  // namespace tc
 
 namespace {
-template <int BN>
+template <int BN, bool F8>
 cudaError_t launch_gemm_bn(unsigned grid, cudaStream_t st, const TcParams& prm) {
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k_tc_gemm<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(k_tc_gemm<BN, F8>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          GemmCfg<BN>::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  return launch_kernel(k_tc_gemm<BN>, grid, kThreads, GemmCfg<BN>::kSmemBytes, st, prm);
+  return launch_kernel(k_tc_gemm<BN, F8>, grid, kThreads, GemmCfg<BN>::kSmemBytes, st, prm);
 }
 
 // Tile width: the fewest tile-columns of MMA work per SM, rounds x BN x (relative cost of a
@@ -390,8 +405,11 @@ cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st, int prof_kind) 
   const int sms = tc::sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
   const int bn = pick_tile_n(a.n_rows, a.max_items, sms);
-  if (!tc::make_map_2d(&prm.ta, a.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.K, a.T, a.K, 64, kBM) ||
-      !tc::make_map_2d(&prm.tb, a.b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.K, a.n_rows, a.K, 64, bn))
+  // one 128-byte row per K-block: 64 bf16 or 128 E4M3 codes
+  const CUtensorMapDataType adt = a.fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const int esz = a.fp8 ? 1 : 2, kblk = a.fp8 ? 128 : 64;
+  if (!tc::make_map_2d(&prm.ta, a.a, adt, esz, a.K, a.T, a.K, kblk, kBM) ||
+      !tc::make_map_2d(&prm.tb, a.b, adt, esz, a.K, a.n_rows, a.K, kblk, bn))
     return cudaErrorInvalidValue;
   prm.has_lora = a.p != nullptr;
   if (a.p) {
@@ -409,9 +427,10 @@ cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st, int prof_kind) 
   prm.T = a.T;
   prm.err = tc::error_word();
   if (!prm.err) return cudaErrorInvalidDevice;
-  prm.nk_main = (int32_t)((a.K + 63) / 64);
+  prm.nk_main = (int32_t)((a.K + kblk - 1) / kblk);
   prm.lora_separate = a.lora_separate;
   prm.n_colscale = a.n_colscale;
+  prm.m_rowscale = a.m_rowscale;
   prm.out = a.out;
   prm.ldo = a.ldo;
   prm.n_out = a.n_rows;
@@ -426,10 +445,13 @@ cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st, int prof_kind) 
   const unsigned grid = (unsigned)(total < sms ? total : sms);   // one persistent CTA per SM
   prof_begin(prof_kind, st);
   cudaError_t e = cudaErrorInvalidValue;
-  switch (bn) {
-    case 256: e = launch_gemm_bn<256>(grid, st, prm); break;
-    case 224: e = launch_gemm_bn<224>(grid, st, prm); break;
-    case 192: e = launch_gemm_bn<192>(grid, st, prm); break;
+  switch (bn * 2 + (a.fp8 ? 1 : 0)) {
+    case 512: e = launch_gemm_bn<256, false>(grid, st, prm); break;
+    case 448: e = launch_gemm_bn<224, false>(grid, st, prm); break;
+    case 384: e = launch_gemm_bn<192, false>(grid, st, prm); break;
+    case 513: e = launch_gemm_bn<256, true>(grid, st, prm); break;
+    case 449: e = launch_gemm_bn<224, true>(grid, st, prm); break;
+    case 385: e = launch_gemm_bn<192, true>(grid, st, prm); break;
   }
   if (e != cudaSuccess) return e;
   prof_end(prof_kind, st);

@@ -53,7 +53,9 @@ struct TcGemmArgs {
   int32_t n_slots;
   int32_t lora_separate;     // LoRA term in its own accumulator, masked by dropout at (t, n)
   DropParams drop;
-  const float* n_colscale;   // per output column scale (DoRA m / n), nullable
+  const float* n_colscale;   // per output column scale (DoRA m / n, or the FP8 W scales), nullable
+  const float* m_rowscale;   // per token-row scale (the FP8 activation scales), nullable
+  int32_t fp8;               // 1: A and B are E4M3 codes (kind::f8f6f4), 0: bf16
   void* out;                 // [T, ldo] in the activation dtype
   int64_t ldo;
   const TokenItem* items;     // null: uniform 128-token tiles of a single-adapter call
@@ -135,6 +137,18 @@ cudaError_t launch_make_red_items_tc(int64_t T, int32_t n_seg, const int32_t* se
                                      cudaStream_t st);
 cudaError_t launch_mask_bf16(const void* X, int64_t T, int64_t in_dim, const DropParams& dp,
                              void* Xd, cudaStream_t st);
+
+// ---- fp8.cu: E4M3 frozen base ----
+// rows of src [rows, K] bf16 -> dst [rows, K] E4M3 codes, scale[r] = amax_r / 448 (K % 8 == 0,
+// K <= 16384)
+cudaError_t launch_quant_rows_e4m3(const void* src, int64_t rows, int64_t K, uint8_t* dst,
+                                   float* scale, cudaStream_t st);
+// columns of W [rows, cols] bf16 -> dst [cols, rows] E4M3 codes (the rows of W^T), scale[c]
+cudaError_t launch_quant_cols_e4m3(const void* W, int64_t rows, int64_t cols, uint8_t* dst,
+                                   float* scale, cudaStream_t st);
+// dst[r, :] = src[r, :] / scale[r] (fp32)
+cudaError_t launch_div_rows(const float* src, int64_t lds, const float* scale, int64_t rows,
+                            int64_t cols, float* dst, int64_t ldd, cudaStream_t st);
 
 // ---- lowrank_simt.cu: streaming CUDA-core low-rank products (fp32 activations) ----
 struct RowDotArgs {                 // out[t, j] = alpha_slot * sum_k A'[t, k] S_slot[j, k]

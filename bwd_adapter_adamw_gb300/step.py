@@ -20,7 +20,7 @@ import torch
 
 from . import binding as L
 
-_DT = {"f32": L.LORA_F32, "bf16": L.LORA_BF16}
+_DT = {"f32": L.LORA_F32, "bf16": L.LORA_BF16, "bf16fp8": L.LORA_BF16_FP8}
 
 
 def _ws(nbytes: int, device) -> torch.Tensor:

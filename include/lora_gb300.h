@@ -27,7 +27,8 @@
  *   - The library allocates no device memory. Scratch comes from a caller workspace whose size
  *     the matching *_workspace_size call gives; a smaller workspace returns LORA_ERR_WORKSPACE.
  *   - Calls are not thread-safe on one workspace; two calls in flight need two workspaces.
- *   - Activations X, dY, Y, dX and the frozen W share one dtype (LORA_F32 or LORA_BF16).
+ *   - Activations X, dY, Y, dX and the frozen W share one dtype (LORA_F32 or LORA_BF16;
+ *     LORA_BF16_FP8 is bf16 with an E4M3 frozen product, see its definition).
  *     A, B, their gradients, the Adam moments, H and the DoRA vectors are always fp32.
  *   - Shapes: 1 <= rank <= LORA_MAX_RANK and rank % 4 == 0; in and out multiples of 8;
  *     all pointers 16-byte aligned (LORA_ERR_ALIGN otherwise).
@@ -54,6 +55,15 @@ extern "C" {
 /* ---- enums ----------------------------------------------------------------------------------*/
 #define LORA_F32 0
 #define LORA_BF16 1
+/* bf16 activations and frozen W whose frozen products (forward and dX) run on E4M3 tensor
+ * cores: W quantised once by lora_prepare_weight (per output row for the forward, per input
+ * column for dX), X and dY' per token inside each call, every row scaled so that its largest
+ * magnitude maps to 448 (r = 448 / amax, codes = e4m3(x * r) rounded to nearest even and
+ * saturated, scale = amax / 448, all in fp32; r = scale = 1 for an all-zero row). The adapter
+ * branch (shrink, G, dA, dB) reads the bf16 tensors unchanged ("LoRA Training and Serving",
+ * Quantized rollout: an FP8 base under a bf16-trained adapter). Single-adapter calls without
+ * DoRA; in_dim and out_dim multiples of 16 and at most 16384 (LORA_ERR_UNSUPPORTED otherwise). */
+#define LORA_BF16_FP8 2
 
 #define LORA_SCHED_CONSTANT 0
 #define LORA_SCHED_WARMUP_COSINE 1
@@ -69,7 +79,7 @@ typedef struct lora_desc {
   int64_t out_dim;
   int32_t rank;        /* r; for multi-LoRA calls: the largest slot rank (H row stride) */
   float scale;         /* s = lora_scale(alpha, rank, rslora); ignored by multi-LoRA calls */
-  int32_t dtype;       /* LORA_F32 | LORA_BF16 for X, W, dY, Y, dX */
+  int32_t dtype;       /* LORA_F32 | LORA_BF16 | LORA_BF16_FP8 for X, W, dY, Y, dX */
   float dropout_p;     /* 0 <= p < 1; applies to the adapter branch input only */
   uint64_t seed;       /* dropout seed */
   uint32_t layer_id;   /* dropout key fields */
@@ -147,7 +157,10 @@ size_t lora_workspace_size(const lora_desc* d, int64_t T);
  *         (2 * in_dim * out_dim bytes);
  *   fp32: the tf32 split of W and of W^T for the 3xTF32 tensor-core products, four fp32 arrays
  *         [W_hi | W_lo | W^T_hi | W^T_lo], each element x stored as x_hi = x rounded to tf32
- *         (nearest, ties away from zero) and x_lo = x - x_hi (16 * in_dim * out_dim bytes).
+ *         (nearest, ties away from zero) and x_lo = x - x_hi (16 * in_dim * out_dim bytes);
+ *   bf16 with the E4M3 frozen product: [W8 (out x in codes) | sw (out fp32 row scales) |
+ *         WT8 (in x out codes of W's columns) | swT (in fp32)], each section starting on a
+ *         16-byte boundary (about 2 * in_dim * out_dim bytes).
  * Returns 0 for an invalid descriptor. */
 size_t lora_prepared_weight_size(const lora_desc* d);
 
@@ -282,6 +295,10 @@ int multi_lora_backward(const lora_desc* d, const lora_ctx* c, int64_t T, const 
 
 /* ---- test hooks (not part of the timed path) ------------------------------------------------*/
 /* Keep mask M [T, in_dim] as uint8 (1 = kept), exactly as the kernels regenerate it. */
+/* Test hook: the per-row E4M3 quantisation of LORA_BF16_FP8 (see its definition) applied to a bf16
+ * [rows, K] matrix: codes [rows, K] uint8 and scales [rows] fp32. K % 16 == 0, K <= 16384. */
+int lora_quantize_e4m3(const void* src, int64_t rows, int64_t K, uint8_t* codes, float* scales,
+                       void* stream);
 int lora_dropout_mask(const lora_desc* d, const lora_ctx* c, int64_t T, uint8_t* d_mask,
                       void* stream);
 

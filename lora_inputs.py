@@ -47,7 +47,7 @@ class LoraConfig:
     rank: int
     alpha: float
     rslora: bool
-    dtype: str                 # "f32" or "bf16": frozen W and activations
+    dtype: str                 # "f32", "bf16", or "bf16fp8" (bf16 with an E4M3 frozen product)
     tokens: int                # tokens per optimizer step
     chunks: int                # accumulation chunks per step
     x_var: float = 1.0
@@ -119,6 +119,9 @@ CONFIGS: Dict[str, LoraConfig] = {
                      tokens=8192, chunks=8, dy_var=1e-2),
     "c4dora": LoraConfig("c4dora", 4, LLAMA_PROJS, 32, rank=64, alpha=128, rslora=True,
                          dtype="bf16", tokens=8192, chunks=8, dy_var=1e-2, dora=True),
+    # c4's workload (same seeded inputs) with the frozen products on E4M3 tensor cores.
+    "c4fp8": LoraConfig("c4fp8", 4, LLAMA_PROJS, 32, rank=64, alpha=128, rslora=True,
+                        dtype="bf16fp8", tokens=8192, chunks=8, dy_var=1e-2),
     # Slot-keyed multi-LoRA on one Qwen3-4B-shaped layer, 8 slots.
     "c5": LoraConfig("c5", 5, QWEN3_4B_PROJS, 1, rank=64, alpha=128, rslora=False, dtype="bf16",
                      tokens=16384, chunks=1, dy_var=1e-2,

@@ -240,46 +240,46 @@ def e4m3_decode(codes) -> np.ndarray:
 
 def e4m3_encode(x) -> np.ndarray:
     """float32 values -> uint8 codes: round to nearest, ties to even, finite values beyond the
-    largest code saturate to +-448, NaN -> 0x7F with the sign bit of x."""
+    largest code saturate to +-448, NaN -> 0x7F with the sign bit of x.
+
+    Element-wise on the value's binade: below 2^-6 the grid is the subnormal step 2^-9 (q = 8
+    steps is 2^-6 itself, the smallest normal); in the binade [2^e, 2^(e+1)) it is 2^(e-3), the
+    value is q steps with q in 8..16 (16 carries into the next binade), and the code is
+    ((e + 7) << 3) | (q - 8)."""
     x = np.asarray(x, dtype=np.float32)
-    out = np.zeros(x.shape, dtype=np.uint8)
-    flat, of = x.reshape(-1), out.reshape(-1)
-    for i, v in enumerate(flat.astype(np.float64)):
-        sign = 0x80 if math.copysign(1.0, v) < 0 else 0
-        if math.isnan(v):
-            of[i] = sign | 0x7F
-            continue
-        a = abs(v)
-        if a >= E4M3_MAX:
-            of[i] = sign | 0x7E
-            continue
-        if a < 2.0 ** -6:                  # subnormal grid: spacing 2^-9 (q = 8 is 2^-6)
-            q = round(a / 2.0 ** -9)       # Python round: ties to even
-            of[i] = sign | q
-            continue
-        e = math.floor(math.log2(a))
-        while 2.0 ** e > a:                # guard the log against rounding
-            e -= 1
-        while 2.0 ** (e + 1) <= a:
-            e += 1
-        q = round(a / 2.0 ** (e - 3))      # 8 .. 16 steps of 2^(e-3)
-        if q == 16:
-            e, q = e + 1, 8
-        code = ((e + 7) << 3) | (q - 8)
-        of[i] = sign | min(code, 0x7E)     # 464 and above round past 448: saturate
-    return out
+    a = np.abs(x.astype(np.float64))
+    sign = np.where(np.signbit(x), 0x80, 0).astype(np.int64)
+    nan = np.isnan(a)
+    a = np.where(nan, 0.0, a)
+    sub = a < 2.0 ** -6
+    q_sub = np.round(a / 2.0 ** -9)                     # numpy rounds half to even
+    _, ex = np.frexp(np.where(sub, 1.0, a))             # a = f * 2^ex, f in [0.5, 1)
+    e = ex.astype(np.int64) - 1                          # a in [2^e, 2^(e+1))
+    q = np.round(np.where(sub, 0.0, a) / np.power(2.0, (e - 3).astype(np.float64)))
+    carry = q >= 16
+    e = np.where(carry, e + 1, e)
+    q = np.where(carry, 8, q).astype(np.int64)
+    code = np.where(sub, q_sub.astype(np.int64), ((e + 7) << 3) | (q - 8))
+    code = np.where(a >= E4M3_MAX, 0x7E, np.minimum(code, 0x7E))
+    code = np.where(nan, 0x7F, code)
+    return (sign | code).astype(np.uint8)
 
 
 def quantize_rows_e4m3(M):
-    """Per-row scaled E4M3 codes of an fp32 (or bf16-valued) matrix: s_r = amax_r / 448 in fp32
-    (1 when that is not positive), codes = e4m3(M[r, :] / s_r) with the division in fp32.
+    """Per-row scaled E4M3 codes of an fp32 (or bf16-valued) matrix, all arithmetic in fp32:
+    with amax_r = max |M[r, :]|, the row is multiplied by r_r = 448 / amax_r and encoded
+    (codes = e4m3(M[r, :] * r_r)), and s_r = amax_r / 448 is the scale that multiplies the
+    decoded codes back; r_r = s_r = 1 when amax_r is 0 or 448 / amax_r is not finite.
     Returns (codes uint8 [R, K], scales float32 [R])."""
     M = np.asarray(M, dtype=np.float32)
     amax = np.max(np.abs(M), axis=1) if M.shape[1] else np.zeros(M.shape[0], np.float32)
-    sc = (amax / np.float32(E4M3_MAX)).astype(np.float32)
-    sc = np.where(sc > 0, sc, np.float32(1.0)).astype(np.float32)
-    q = (M / sc[:, None]).astype(np.float32)
-    return e4m3_encode(q), sc
+    with np.errstate(divide="ignore", over="ignore"):
+        rcp = (np.float32(E4M3_MAX) / amax).astype(np.float32)
+    ok = (amax > 0) & np.isfinite(rcp)
+    rcp = np.where(ok, rcp, np.float32(1.0)).astype(np.float32)
+    sc = np.where(ok, (amax / np.float32(E4M3_MAX)).astype(np.float32), np.float32(1.0))
+    q = (M * rcp[:, None]).astype(np.float32)
+    return e4m3_encode(q), sc.astype(np.float32)
 
 
 def fp8_product(Xc, sx, Wc, sw) -> np.ndarray:
