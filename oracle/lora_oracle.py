@@ -597,6 +597,35 @@ def run_single_step(problems: Dict[object, dict], state: Dict[object, AdapterSta
 
 
 @dataclass
+class FusedResult:
+    Y: np.ndarray                      # [T, sum out_p]
+    H: np.ndarray                      # [T, P * r] unscaled shrinks, projection p in columns p*r..
+    dX: np.ndarray                     # [T, in] summed over the projections
+    grads: List[Tuple[np.ndarray, np.ndarray]]   # per projection (dA_p, dB_p)
+
+
+def fused_forward_backward(X, Ws: Sequence, As: Sequence, Bs: Sequence, dYs: Sequence, s: float,
+                           keep=None, q: float = 1.0) -> FusedResult:
+    """Projections that share one input, run as one fused linear ("LoRA Training and Serving",
+    --lora-type: `lora` fuses the projections, `canonical_lora` keeps one adapter per projection;
+    here one fused frozen weight W_cat = [W_0; W_1; ...] with one adapter per projection). The
+    output is the projections' outputs side by side, and the input gradient is their sum:
+        Y_cat = [Y_0 | Y_1 | ...],  Y_p = X W_p^T + s q (Xd A_p^T) B_p^T
+        dX    = sum_p (dY_p W_p + s q (G_p A_p) * M),  G_p = dY_p B_p
+    with one dropout mask M shared by the projections (they read the same input)."""
+    ys, hs, grads = [], [], []
+    dX = None
+    for W, A, B, dY in zip(Ws, As, Bs, dYs):
+        f = lora_forward(X, W, A, B, s, keep, q)
+        b = lora_backward(X, W, A, B, dY, s, keep, q)
+        ys.append(f.Y)
+        hs.append(f.H)
+        grads.append((b.dA, b.dB))
+        dX = b.dX if dX is None else dX + b.dX
+    return FusedResult(np.concatenate(ys, axis=1), np.concatenate(hs, axis=1), dX, grads)
+
+
+@dataclass
 class ChainResult:
     Y: np.ndarray                      # [T, d_L] output of the last layer
     dX: np.ndarray                     # [T, d_0] gradient of the first layer's input

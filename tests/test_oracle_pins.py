@@ -654,3 +654,24 @@ def test_fp8_forward_with_zero_adapter_is_the_fp8_product():
     Xc, sx = O.quantize_rows_e4m3(X)
     Wc, sw = O.quantize_rows_e4m3(W)
     np.testing.assert_array_equal(f.Y, O.fp8_product(Xc, sx, Wc, sw))
+
+
+# ---- fused projections ("LoRA Training and Serving", --lora-type lora / canonical_lora) ----
+def test_fused_projections_equal_the_stacked_effective_weight():
+    # one fused linear with the effective weight W_eff = [W_p + s B_p A_p]_p stacked by rows:
+    # Y_cat = X W_eff^T and dX = dY_cat W_eff (closed forms, p = 0)
+    rng = np.random.default_rng(17)
+    T, d_in, outs, r, s = 5, 12, (8, 4, 4), 3, 0.5
+    X = rng.standard_normal((T, d_in))
+    Ws = [rng.standard_normal((o, d_in)) for o in outs]
+    As = [rng.standard_normal((r, d_in)) for _ in outs]
+    Bs = [rng.standard_normal((o, r)) for o in outs]
+    dYs = [rng.standard_normal((T, o)) for o in outs]
+    res = O.fused_forward_backward(X, Ws, As, Bs, dYs, s)
+    W_eff = np.concatenate([W + s * B @ A for W, A, B in zip(Ws, As, Bs)], axis=0)
+    np.testing.assert_allclose(res.Y, X @ W_eff.T, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(res.dX, np.concatenate(dYs, axis=1) @ W_eff, rtol=1e-12, atol=1e-12)
+    # each projection's adapter gradient sees only its own output columns
+    for (gA, gB), W, A, B, dY in zip(res.grads, Ws, As, Bs, dYs):
+        np.testing.assert_allclose(gB, s * dY.T @ (X @ A.T), rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(gA, s * (dY @ B).T @ X, rtol=1e-12, atol=1e-12)
