@@ -55,6 +55,11 @@ class lora_slot(C.Structure):
                 ("rank", C.c_int32), ("scale", C.c_float)]
 
 
+class lora_proj(C.Structure):
+    _fields_ = [("A", C.c_void_p), ("B", C.c_void_p), ("dA", C.c_void_p), ("dB", C.c_void_p),
+                ("out_dim", C.c_int64)]
+
+
 class lora_group(C.Structure):
     _fields_ = [("offset", C.c_int64), ("n_a", C.c_int64), ("n_b", C.c_int64),
                 ("n_mag", C.c_int64), ("grad_scale", C.c_double), ("max_norm", C.c_float),
@@ -94,6 +99,11 @@ def _load() -> C.CDLL:
         "lora_restore": (C.c_int, [P, P, P, P, P, I32, C.POINTER(lora_group), I32, P]),
         "lora_retire": (C.c_int, [P, P, P, P, I32, C.POINTER(lora_group), I32, P]),
         "multi_lora_workspace_size": (SZ, [DP, I64, I32, I32, C.POINTER(lora_slot)]),
+        "lora_fused_workspace_size": (SZ, [DP, I64, I32, C.POINTER(lora_proj)]),
+        "lora_fused_forward": (C.c_int, [DP, CP, I64, P, P, I32, C.POINTER(lora_proj), P, P, P,
+                                         SZ, P]),
+        "lora_fused_backward": (C.c_int, [DP, CP, I64, P, P, I32, C.POINTER(lora_proj), P, P, P,
+                                          P, SZ, P]),
         "multi_lora_forward": (C.c_int, [DP, CP, I64, P, P, P, I32, P, P, I32,
                                          C.POINTER(lora_slot), P, P, P, SZ, P]),
         "multi_lora_backward": (C.c_int, [DP, CP, I64, P, P, I32, P, P, I32,
@@ -121,6 +131,7 @@ EXPORTED = ("lora_status_string", "lora_scale", "lora_lr_at", "lora_workspace_si
             "lora_grad_prepare_workspace_size", "lora_grad_prepare", "lora_grad_prepare_noalloc",
             "lora_adamw_step", "lora_snapshot", "lora_restore", "lora_retire",
             "multi_lora_workspace_size", "multi_lora_forward", "multi_lora_backward",
+            "lora_fused_workspace_size", "lora_fused_forward", "lora_fused_backward",
             "lora_dropout_mask", "lora_quantize_e4m3", "multi_lora_token_slots", "lora_profile_arm",
             "lora_profile_used", "lora_launch_counter", "lora_last_cuda_error",
             "lora_device_error")
@@ -312,6 +323,36 @@ def make_slots(slots: Sequence[dict]):
 
 def multi_lora_workspace_size(d: lora_desc, T: int, n_seg: int, slots) -> int:
     return _lib.multi_lora_workspace_size(C.byref(d), T, n_seg, len(slots), slots)
+
+
+def make_projs(projs: Sequence[dict]):
+    arr = (lora_proj * len(projs))()
+    for i, p in enumerate(projs):
+        arr[i] = lora_proj(_ptr(p["A"]), _ptr(p["B"]), _ptr(p.get("dA")), _ptr(p.get("dB")),
+                           p["out"])
+    return arr
+
+
+def lora_fused_workspace_size(d: lora_desc, T: int, projs) -> int:
+    return _lib.lora_fused_workspace_size(C.byref(d), T, len(projs), projs)
+
+
+def lora_fused_forward(d, c, T, X, W, projs, Y, H_save, ws, ws_bytes=None, stream=None,
+                       check=True):
+    nbytes = ws_bytes if ws_bytes is not None else ws.numel() * ws.element_size()
+    st = _lib.lora_fused_forward(C.byref(d), C.byref(c) if c is not None else None, T, _ptr(X),
+                                 _ptr(W), len(projs), projs, _ptr(Y), _ptr(H_save), _ptr(ws),
+                                 nbytes, _stream(stream))
+    return _check(st, "lora_fused_forward") if check else st
+
+
+def lora_fused_backward(d, c, T, X, W_prep, projs, dY, H_save, dX, ws, ws_bytes=None,
+                        stream=None, check=True):
+    nbytes = ws_bytes if ws_bytes is not None else ws.numel() * ws.element_size()
+    st = _lib.lora_fused_backward(C.byref(d), C.byref(c) if c is not None else None, T,
+                                  _ptr(X), _ptr(W_prep), len(projs), projs, _ptr(dY),
+                                  _ptr(H_save), _ptr(dX), _ptr(ws), nbytes, _stream(stream))
+    return _check(st, "lora_fused_backward") if check else st
 
 
 def multi_lora_forward(d, c, T, X, W, W_prep, n_seg, seg_start, seg_slot, slots, Y, H_save, ws,

@@ -505,7 +505,7 @@ int run_backward_tc(const lora_desc* d, const DropParams& dp, int64_t T, const v
   for (int k = 0; k < s.n; ++k) rt.rank[k] = s.rank[k];
   // dB_k += dY'^T Hs over the slot's tokens (as dB^T rows of the transposed Hs split)
   {
-    LORA_TRY(launch_split_rows_t(H, d->rank, L.ldt, L.gitems, L.gcount, (int)L.gmax, si, L.HsT,
+    LORA_TRY(launch_split_rows_t(H, d->rank, d->rank, L.ldt, L.gitems, L.gcount, (int)L.gmax, si, L.HsT,
                                  split_bytes, T, st));
     TcRedArgs a{};
     for (int k = 0; k < s.n; ++k) {
@@ -760,6 +760,208 @@ cudaError_t run_dora_norm_tc(const lora_desc* d, const void* W, const float* A, 
   if (e != cudaSuccess) return e;
   return launch_dora_gram_combine(W, L.H, A, B, d->scale, d->out_dim, d->in_dim, d->rank, L.C,
                                   norm_out, st);
+}
+
+// ---- fused projections: one frozen product over stacked weights, one adapter per projection --
+// ("LoRA Training and Serving", --lora-type: fused projections versus one adapter per q/k/v and
+// gate/up projection). Projection k owns output columns [off_k, off_k + out_k) of the fused
+// linear; its LoRA operands sit in columns k r .. k r + r - 1 of H (Hs) and G.
+struct FusedProjs {
+  int n = 0;
+  const float* A[LORA_MAX_SLOTS];
+  const float* B[LORA_MAX_SLOTS];
+  float* dA[LORA_MAX_SLOTS];
+  float* dB[LORA_MAX_SLOTS];
+  int64_t out[LORA_MAX_SLOTS];
+  int64_t off[LORA_MAX_SLOTS];
+  int64_t out_max = 0;
+};
+
+int fused_from_table(const lora_desc* d, int32_t n_proj, const lora_proj* tab, bool need_grads,
+                     FusedProjs& f) {
+  if (!tab || n_proj < 1 || n_proj > LORA_MAX_SLOTS) return LORA_ERR_INVALID;
+  if (d->dtype != LORA_BF16 || d->dora) return LORA_ERR_UNSUPPORTED;
+  int64_t sum = 0;
+  for (int k = 0; k < n_proj; ++k) {
+    const lora_proj& e = tab[k];
+    if (!e.A || !e.B || e.out_dim <= 0) return LORA_ERR_INVALID;
+    if (need_grads && (!e.dA || !e.dB)) return LORA_ERR_INVALID;
+    if (e.out_dim % 256) return LORA_ERR_UNSUPPORTED;   // column groups start on 256-wide tiles
+    if (!al16(e.A) || !al16(e.B) || (need_grads && (!al16(e.dA) || !al16(e.dB))))
+      return LORA_ERR_ALIGN;
+    f.A[k] = e.A;
+    f.B[k] = e.B;
+    f.dA[k] = e.dA;
+    f.dB[k] = e.dB;
+    f.out[k] = e.out_dim;
+    f.off[k] = sum;
+    sum += e.out_dim;
+    if (e.out_dim > f.out_max) f.out_max = e.out_dim;
+  }
+  if (sum != d->out_dim) return LORA_ERR_INVALID;
+  f.n = n_proj;
+  return LORA_OK;
+}
+
+// The per-projection low-rank products run one projection after the other in stream order and
+// reuse one projection's scratch, sized for the widest projection; G and A^T of all the
+// projections sit side by side after it.
+struct FusedLayout {
+  Layout L;
+  float* Gcat;    // [T, n r]
+  float* Atcat;   // [in, n r]
+  size_t bytes;
+};
+
+FusedLayout fused_carve(const lora_desc* d, int64_t T, const FusedProjs& f, void* ws) {
+  lora_desc sd = *d;
+  sd.out_dim = f.out_max;
+  FusedLayout F;
+  F.L = carve(&sd, T, -1, 1, d->rank, true, ws);
+  Carve c(ws);
+  c.off = F.L.bytes;
+  F.Gcat = c.take<float>((size_t)T * f.n * d->rank);
+  F.Atcat = c.take<float>((size_t)d->in_dim * f.n * d->rank);
+  F.bytes = c.off + kWsAlign;
+  return F;
+}
+
+SlotInfo fused_slot_info(const lora_desc* d) {
+  Slots one;
+  one.n = 1;
+  one.rank[0] = d->rank;
+  one.scale[0] = d->scale;
+  return slot_info(one, dropout_q(d));
+}
+
+int run_fused_forward(const lora_desc* d, const DropParams& dp, int64_t T, const void* X,
+                      const void* W, const FusedProjs& f, void* Y, float* H, void* ws,
+                      cudaStream_t st) {
+  FusedLayout F = fused_carve(d, T, f, ws);
+  Layout& L = F.L;
+  clear_stale();
+  use_uniform_items(L, T);
+  const int64_t r = d->rank, ldh = (int64_t)f.n * r;
+  const SlotInfo si = fused_slot_info(d);
+  const void* Xin = X;
+  if (dp.enabled) {   // one mask for the projections: they read the same input
+    LORA_TRY(launch_mask_bf16(X, T, d->in_dim, dp, L.Xd, st));
+    Xin = L.Xd;
+  }
+  for (int k = 0; k < f.n; ++k) {   // Hs_k = s' Xd A_k^T into columns k r .. of H
+    SplitTab sp{};
+    sp.K = d->in_dim;
+    sp.src[0] = f.A[k];
+    sp.dst[0] = L.Sa;
+    sp.rank[0] = (int32_t)r;
+    LORA_TRY(launch_split(sp, 1, st));
+    TcRowsArgs a{};
+    a.a = Xin; a.T = T; a.K = d->in_dim; a.n_slots = 1;
+    a.s[0] = L.Sa; a.rank[0] = (int32_t)r;
+    a.NP = np_for((int)r);
+    a.splits = row_splits(T, -1, d->in_dim);
+    a.part = L.rows_part; a.si = si;
+    a.out = H + k * r; a.ldo = r; a.ld_out = ldh;
+    a.items = nullptr; a.n_items = nullptr; a.max_items = (int)L.gmax;
+    LORA_TRY(launch_tc_rows(a, st, LORA_PROF_SHRINK));
+  }
+  TcGemmArgs t{};
+  t.a = X; t.T = T; t.b = W; t.n_rows = d->out_dim; t.K = d->in_dim;
+  t.p = H; t.ldp = ldh; t.n_slots = f.n; t.n_col_groups = f.n;
+  for (int k = 0; k < f.n; ++k) {
+    t.q[k] = f.B[k];
+    t.q_rank[k] = (int32_t)r;
+    t.col_end[k] = f.off[k] + f.out[k];
+    t.p_col[k] = (int32_t)(k * r);
+  }
+  t.out = Y; t.ldo = d->out_dim;
+  t.items = nullptr; t.n_items = nullptr; t.max_items = (int)L.gmax; t.drop = dp;
+  LORA_TRY(launch_tc_gemm(t, st, LORA_PROF_FROZEN_FWD));
+  return LORA_OK;
+}
+
+int run_fused_backward(const lora_desc* d, const DropParams& dp, int64_t T, const void* X,
+                       const void* Wt, const FusedProjs& f, const void* dY, const float* H,
+                       void* dX, void* ws, cudaStream_t st) {
+  FusedLayout F = fused_carve(d, T, f, ws);
+  Layout& L = F.L;
+  clear_stale();
+  use_uniform_items(L, T);
+  const int64_t r = d->rank, ldh = (int64_t)f.n * r;
+  const SlotInfo si = fused_slot_info(d);
+  {   // A_k^T into columns k r .. of A^T_cat [in, n r] for the dX product's LoRA term
+    TransposeTab ta{};
+    for (int k = 0; k < f.n; ++k) {
+      ta.src[k] = f.A[k];
+      ta.dst[k] = F.Atcat + k * r;
+      ta.rows[k] = r;
+      ta.cols[k] = d->in_dim;
+      ta.ld_dst[k] = ldh;
+    }
+    LORA_TRY(launch_transpose_slots(ta, f.n, r, d->in_dim, st));
+  }
+  const void* Xin = X;
+  if (dp.enabled) {
+    LORA_TRY(launch_mask_bf16(X, T, d->in_dim, dp, L.Xd, st));
+    Xin = L.Xd;
+  }
+  const size_t split_bytes = (size_t)2 * r * L.ldt * sizeof(uint16_t);
+  const uint16_t* dYb = static_cast<const uint16_t*>(dY);
+  ReduceTab rt{};
+  rt.rank[0] = (int32_t)r;
+  for (int k = 0; k < f.n; ++k) {
+    // G_k = s' dY_k B_k (projection k's columns of dY) into columns k r .. of G, with its
+    // transposed split for dA_k
+    SplitTab sp{};
+    sp.K = f.out[k];
+    sp.transposed = 1;
+    sp.src[0] = f.B[k];
+    sp.dst[0] = L.Sb;
+    sp.rank[0] = (int32_t)r;
+    LORA_TRY(launch_split(sp, 1, st));
+    TcRowsArgs g{};
+    g.a = dYb + f.off[k]; g.lda = d->out_dim; g.T = T; g.K = f.out[k]; g.n_slots = 1;
+    g.s[0] = L.Sb; g.rank[0] = (int32_t)r;
+    g.NP = np_for((int)r);
+    g.splits = row_splits(T, -1, f.out[k]);
+    g.part = L.rows_part; g.si = si;
+    g.out = F.Gcat + k * r; g.ldo = r; g.ld_out = ldh;
+    g.outT = L.GsT; g.ldt = L.ldt; g.outT_bytes = split_bytes;
+    g.items = nullptr; g.n_items = nullptr; g.max_items = (int)L.gmax;
+    LORA_TRY(launch_tc_rows(g, st, LORA_PROF_G));
+    // dA_k += Gs_k^T Xd
+    TcRedArgs a{};
+    a.st[0] = L.GsT; a.rank[0] = (int32_t)r; a.n_slots = 1; a.max_rank = (int32_t)r;
+    a.T = T; a.ldt = L.ldt; a.b = Xin; a.N = d->in_dim; a.part = L.red_part;
+    rt.out[0] = f.dA[k];
+    a.tab = rt; a.transposed = 0;
+    a.items = nullptr; a.n_items = nullptr; a.max_items = (int)L.max_da;
+    a.span_tokens = (int64_t)L.span_da * 64;
+    LORA_TRY(launch_tc_red(a, st, LORA_PROF_RED_DA));
+    // dB_k += dY_k^T Hs_k
+    LORA_TRY(launch_split_rows_t(H + k * r, ldh, r, L.ldt, nullptr, nullptr, (int)L.gmax, si,
+                                 L.HsT, split_bytes, T, st));
+    TcRedArgs b{};
+    b.st[0] = L.HsT; b.rank[0] = (int32_t)r; b.n_slots = 1; b.max_rank = (int32_t)r;
+    b.T = T; b.ldt = L.ldt; b.b = dYb + f.off[k]; b.ldb = d->out_dim; b.N = f.out[k];
+    b.part = L.red_part;
+    rt.out[0] = f.dB[k];
+    b.tab = rt; b.transposed = 1;
+    b.items = nullptr; b.n_items = nullptr; b.max_items = (int)L.max_db;
+    b.span_tokens = (int64_t)L.span_db * 64;
+    LORA_TRY(launch_tc_red(b, st, LORA_PROF_RED_DB));
+  }
+  // dX = dY_cat W_cat + (G_cat A_cat) * M: the projections' input gradients summed in one product
+  if (dX) {
+    TcGemmArgs t{};
+    t.a = dY; t.T = T; t.b = Wt; t.n_rows = d->in_dim; t.K = d->out_dim;
+    t.p = F.Gcat; t.ldp = ldh; t.n_slots = 1;
+    t.q[0] = F.Atcat; t.q_rank[0] = (int32_t)ldh;
+    t.lora_separate = dp.enabled; t.out = dX; t.ldo = d->in_dim;
+    t.items = nullptr; t.n_items = nullptr; t.max_items = (int)L.gmax; t.drop = dp;
+    LORA_TRY(launch_tc_gemm(t, st, LORA_PROF_FROZEN_DX));
+  }
+  return LORA_OK;
 }
 
 }  // namespace
@@ -1107,6 +1309,49 @@ int lora_retire(float* params, float* grads, float* m, float* v, int32_t n_group
   const int flags = kMaintZeroG | kMaintZeroMV | (clear_params ? kMaintZeroDst : 0);
   return cuda_status(launch_group_maint(params, nullptr, grads, m, v, g, flags,
                                         (cudaStream_t)stream));
+}
+
+size_t lora_fused_workspace_size(const lora_desc* d, int64_t T, int32_t n_proj,
+                                 const lora_proj* projs) {
+  if (check_desc(d, T, false) != LORA_OK) return 0;
+  FusedProjs f;
+  if (fused_from_table(d, n_proj, projs, false, f) != LORA_OK) return 0;
+  return fused_carve(d, T, f, nullptr).bytes;
+}
+
+int lora_fused_forward(const lora_desc* d, const lora_ctx* c, int64_t T, const void* X,
+                       const void* W, int32_t n_proj, const lora_proj* projs, void* Y,
+                       float* H_save, void* ws, size_t ws_bytes, void* stream) {
+  int rc = check_desc(d, T, false);
+  if (rc) return rc;
+  FusedProjs f;
+  if ((rc = fused_from_table(d, n_proj, projs, false, f))) return rc;
+  DropParams dp;
+  if ((rc = build_drop(d, c, T, dp))) return rc;
+  if (!X || !W || !Y || !H_save || !ws) return LORA_ERR_INVALID;
+  if (!al16(X) || !al16(W) || !al16(Y) || !al16(H_save) || !al16(ws)) return LORA_ERR_ALIGN;
+  if (ws_bytes < fused_carve(d, T, f, nullptr).bytes) return LORA_ERR_WORKSPACE;
+  if (T == 0) return LORA_OK;
+  return run_fused_forward(d, dp, T, X, W, f, Y, H_save, ws, (cudaStream_t)stream);
+}
+
+int lora_fused_backward(const lora_desc* d, const lora_ctx* c, int64_t T, const void* X,
+                        const void* W_prep, int32_t n_proj, const lora_proj* projs,
+                        const void* dY, const float* H_save, void* dX, void* ws, size_t ws_bytes,
+                        void* stream) {
+  int rc = check_desc(d, T, false);
+  if (rc) return rc;
+  FusedProjs f;
+  if ((rc = fused_from_table(d, n_proj, projs, true, f))) return rc;
+  DropParams dp;
+  if ((rc = build_drop(d, c, T, dp))) return rc;
+  if (!X || !W_prep || !dY || !H_save || !ws) return LORA_ERR_INVALID;
+  if (!al16(X) || !al16(W_prep) || !al16(dY) || !al16(H_save) || !al16(ws) ||
+      (dX && !al16(dX)))
+    return LORA_ERR_ALIGN;
+  if (ws_bytes < fused_carve(d, T, f, nullptr).bytes) return LORA_ERR_WORKSPACE;
+  if (T == 0) return LORA_OK;
+  return run_fused_backward(d, dp, T, X, W_prep, f, dY, H_save, dX, ws, (cudaStream_t)stream);
 }
 
 int lora_quantize_e4m3(const void* src, int64_t rows, int64_t K, uint8_t* codes, float* scales,

@@ -92,6 +92,9 @@ struct TcParams {
   int32_t has_lora;
   int32_t lora_separate;
   int32_t q_rank[LORA_MAX_SLOTS];
+  int32_t n_col_groups;                 // > 0: the adapter is chosen by output column, not token
+  int32_t col_end[LORA_MAX_SLOTS];      // group k covers columns [col_end[k-1], col_end[k])
+  int32_t p_col[LORA_MAX_SLOTS];        // group k's LoRA operand starts at column p_col[k] of P
   const float* n_colscale;
   const float* m_rowscale;
   void* out;
@@ -109,6 +112,21 @@ struct TcParams {
 // 256-column TMEM accumulators alternate between tiles, so that the epilogue of one tile drains
 // and stores while the MMAs of the next run. With a dropout-masked LoRA term the second 256
 // columns hold that term instead, and tiles take turns on one accumulator.
+// The adapter of a tile, the column of P where its LoRA operand starts and the first output
+// column of its Q: the item's slot, or, for fused projections, the column group that holds the
+// tile's first output column (whose Q rows count from the group's first column).
+__device__ __forceinline__ int tile_slot(const TcParams& p, const TokenItem& it, int32_t n0,
+                                         int& pcol, int& qcol0) {
+  pcol = 0;
+  qcol0 = 0;
+  if (p.n_col_groups <= 0) return it.slot;
+  int k = 0;
+  while (k + 1 < p.n_col_groups && n0 >= p.col_end[k]) ++k;
+  pcol = p.p_col[k];
+  qcol0 = k > 0 ? p.col_end[k - 1] : 0;
+  return k;
+}
+
 template <int BN>
 __device__ __forceinline__ bool decode_tile(const TcParams& p, int t, TokenItem& it, int32_t& n0) {
   const int per_group = p.group_m * p.n_tiles;
@@ -169,7 +187,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
         TokenItem it;
         int32_t n0;
         if (!decode_tile<BN>(p, t, it, n0)) continue;
-        const int slot = it.slot;
+        int pcol, qcol0;
+        const int slot = tile_slot(p, it, n0, pcol, qcol0);
         const int nk = p.nk_main + ((p.has_lora && slot >= 0) ? (p.q_rank[slot] + 31) / 32 : 0);
         for (int kb = 0; kb < nk; ++kb, ++g) {
           const int s = g % kStages;
@@ -184,8 +203,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
             tma_load_2d(sb, &p.tb, &full_bar[s], kb * kKBlock, n0);
           } else {
             const int j = kb - p.nk_main;
-            tma_load_2d(sa, &p.tp, &full_bar[s], j * 32, it.t0);
-            tma_load_2d(sb, &p.tq[slot], &full_bar[s], j * 32, n0);
+            tma_load_2d(sa, &p.tp, &full_bar[s], pcol + j * 32, it.t0);
+            tma_load_2d(sb, &p.tq[slot], &full_bar[s], j * 32, n0 - qcol0);
           }
         }
       }
@@ -201,7 +220,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
         TokenItem it;
         int32_t n0;
         if (!decode_tile<BN>(p, t, it, n0)) continue;
-        const int slot = it.slot;
+        int pcol, qcol0;
+        const int slot = tile_slot(p, it, n0, pcol, qcol0);
         const int nk_lora = (p.has_lora && slot >= 0) ? (p.q_rank[slot] + 31) / 32 : 0;
         const int nk = p.nk_main + nk_lora;
         const bool sep = p.lora_separate && nk_lora > 0;
@@ -248,7 +268,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
       TokenItem it;
       int32_t n0;
       if (!decode_tile<BN>(p, t, it, n0)) continue;
-      const int slot = it.slot;
+      int pcol, qcol0;
+      const int slot = tile_slot(p, it, n0, pcol, qcol0);
       const bool sep = p.lora_separate && p.has_lora && slot >= 0 && p.q_rank[slot] > 0;
       const int b = j % nbuf, use = j / nbuf;
       const int64_t m = (int64_t)it.t0 + row;
@@ -404,7 +425,15 @@ cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st, int prof_kind) 
   std::memset(&prm, 0, sizeof(prm));
   const int sms = tc::sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
-  const int bn = pick_tile_n(a.n_rows, a.max_items, sms);
+  // column groups must start on tile boundaries: fused projections use 256-wide tiles
+  const int bn = a.n_col_groups > 0 ? 256 : pick_tile_n(a.n_rows, a.max_items, sms);
+  if (a.n_col_groups > 0) {
+    if (a.n_col_groups > LORA_MAX_SLOTS || a.n_col_groups != a.n_slots) return cudaErrorInvalidValue;
+    for (int k = 0; k < a.n_col_groups; ++k)
+      if (a.col_end[k] % 256 || (k > 0 && a.col_end[k] <= a.col_end[k - 1]) || a.p_col[k] % 4)
+        return cudaErrorInvalidValue;
+    if (a.col_end[a.n_col_groups - 1] != a.n_rows) return cudaErrorInvalidValue;
+  }
   // one 128-byte row per K-block: 64 bf16 or 128 E4M3 codes
   const CUtensorMapDataType adt = a.fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const int esz = a.fp8 ? 1 : 2, kblk = a.fp8 ? 128 : 64;
@@ -417,7 +446,11 @@ cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st, int prof_kind) 
       return cudaErrorInvalidValue;
     for (int k = 0; k < a.n_slots; ++k) {
       prm.q_rank[k] = a.q_rank[k];
-      if (!tc::make_map_2d(&prm.tq[k], a.q[k], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.q_rank[k], a.n_rows,
+      // Q_k has the output rows of its column group (fused projections) or all of them
+      const int64_t q_rows = a.n_col_groups > 0
+                                 ? a.col_end[k] - (k > 0 ? a.col_end[k - 1] : 0)
+                                 : a.n_rows;
+      if (!tc::make_map_2d(&prm.tq[k], a.q[k], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.q_rank[k], q_rows,
                     a.q_rank[k], 32, bn))
         return cudaErrorInvalidValue;
     }
@@ -431,6 +464,11 @@ cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st, int prof_kind) 
   prm.lora_separate = a.lora_separate;
   prm.n_colscale = a.n_colscale;
   prm.m_rowscale = a.m_rowscale;
+  prm.n_col_groups = a.n_col_groups;
+  for (int k = 0; k < a.n_col_groups; ++k) {
+    prm.col_end[k] = (int32_t)a.col_end[k];
+    prm.p_col[k] = a.p_col[k];
+  }
   prm.out = a.out;
   prm.ldo = a.ldo;
   prm.n_out = a.n_rows;

@@ -55,6 +55,9 @@ struct TcGemmArgs {
   DropParams drop;
   const float* n_colscale;   // per output column scale (DoRA m / n, or the FP8 W scales), nullable
   const float* m_rowscale;   // per token-row scale (the FP8 activation scales), nullable
+  int32_t n_col_groups;      // > 0: fused projections, adapter k covers output columns
+  int64_t col_end[LORA_MAX_SLOTS];   //   [col_end[k-1], col_end[k]) (multiples of 256), its
+  int32_t p_col[LORA_MAX_SLOTS];     //   LoRA operand in columns p_col[k].. of P
   int32_t fp8;               // 1: A and B are E4M3 codes (kind::f8f6f4), 0: bf16
   void* out;                 // [T, ldo] in the activation dtype
   int64_t ldo;
@@ -90,8 +93,10 @@ struct TcRowsArgs {                 // out[t, j] = alpha * (A[t, :] . (S_hi[j] +
   int32_t splits;                   // K splits
   float* part;                      // [splits][T][ldo] scratch
   SlotInfo si;
-  float* out;                       // [T, ldo] fp32 (ldo = largest rank)
-  int64_t ldo;
+  float* out;                       // [T, ld_out] fp32 (columns < ldo written)
+  int64_t ldo;                      // partial row stride (largest rank)
+  int64_t ld_out;                   // out row stride (0: ldo)
+  int64_t lda;                      // A row stride in elements (0: K)
   uint16_t* outT;                   // optional per slot [2 r, ldt] bf16 transposed split of out
   int64_t ldt;
   size_t outT_bytes;                // zeroed first when an item table routes several slots
@@ -106,8 +111,9 @@ struct TcRedArgs {                  // dst_slot += (ST_hi + ST_lo)[., t] x B[t, 
   int32_t max_rank;
   int64_t T;
   int64_t ldt;
-  const void* b;                    // [T, N] bf16 (dY' or Xd)
+  const void* b;                    // [T, N] bf16 (dY' or Xd), row stride ldb
   int64_t N;
+  int64_t ldb;                      // 0: N
   float* part;                      // [items][max_rank][N] scratch
   ReduceTab tab;
   int32_t transposed;               // 1: dst is [N, r] (dB); 0: dst is [r, N] (dA)
@@ -126,7 +132,9 @@ struct SplitTab {
 cudaError_t launch_tc_rows(const TcRowsArgs& a, cudaStream_t st, int prof_kind);
 cudaError_t launch_tc_red(const TcRedArgs& a, cudaStream_t st, int prof_kind);
 cudaError_t launch_split(const SplitTab& t, int n, cudaStream_t st);
-cudaError_t launch_split_rows_t(const float* src, int64_t lds, int64_t ldt, const TokenItem* items,
+// src [T, lds] fp32, columns 0 .. ncols - 1 (the largest rank); dst per slot [2 r, ldt] bf16
+cudaError_t launch_split_rows_t(const float* src, int64_t lds, int64_t ncols, int64_t ldt,
+                                const TokenItem* items,
                                 const int32_t* n_items, int max_items, const SlotInfo& si,
                                 uint16_t* dst, size_t dst_bytes, int64_t T, cudaStream_t st);
 // count[0] = the number of items; count[1 + k] (k = 0 .. n_slots) = the first item of slot k, the
@@ -222,6 +230,7 @@ struct TransposeTab {
   float* dst[LORA_MAX_SLOTS];
   int64_t rows[LORA_MAX_SLOTS];   // src rows
   int64_t cols[LORA_MAX_SLOTS];   // src cols
+  int64_t ld_dst[LORA_MAX_SLOTS]; // dst row stride (0: rows)
 };
 cudaError_t launch_transpose_slots(const TransposeTab& t, int n, int64_t max_rows, int64_t max_cols,
                                    cudaStream_t st);

@@ -62,9 +62,10 @@ __global__ void k_transpose_slots(const TransposeTab tab) {
     if (r < rows && c < cols) tile[i][threadIdx.x] = src[r * cols + c];
   }
   __syncthreads();
+  const int64_t ldd = tab.ld_dst[z] > 0 ? tab.ld_dst[z] : rows;
   for (int i = threadIdx.y; i < 32; i += 8) {
     const int64_t c = c0 + i, r = r0 + threadIdx.x;
-    if (r < rows && c < cols) dst[c * rows + r] = tile[threadIdx.x][i];
+    if (r < rows && c < cols) dst[c * ldd + r] = tile[threadIdx.x][i];
   }
 }
 

@@ -182,8 +182,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_tc_rows(const __grid_constant__
   }
 }
 
-// out[t, j] = alpha_slot * sum_z part[z][t][j] for j < r, 0 for r <= j < ldp (alpha_slot = 1
-// when use_alpha is 0; out may be null). With outT, also the transposed bf16 split that the token
+// out[t, j] = alpha_slot * sum_z part[z][t][j] for j < r, 0 for r <= j < ncols (alpha_slot = 1
+// when use_alpha is 0; out may be null); ldp and ld_out are the row strides of part and out. With outT, also the transposed bf16 split that the token
 // reductions take as their K-major operand:
 // outT[region_slot + j][t] = hi(out[t, j]), outT[region_slot + r + j][t] = lo(out[t, j]).
 // CTA (item, blockIdx.y) covers kFinishTok tokens of the item; every thread issues all of its
@@ -193,9 +193,10 @@ constexpr int kFinishThreads = 256;
 constexpr int kFinishVec = kFinishTok * LORA_MAX_RANK / 4 / kFinishThreads;
 constexpr int kMaxSplitsRows = 8;   // K splits of the rows kernel (the launcher rejects more)
 __global__ void __launch_bounds__(kFinishThreads) k_rows_finish(
-    const float* __restrict__ part, int32_t splits, int64_t T, int32_t ldp, int use_alpha,
+    const float* __restrict__ part, int32_t splits, int64_t T, int64_t ldp, int32_t ncols,
+    int use_alpha,
     const TokenItem* __restrict__ items, const int32_t* __restrict__ n_items, const SlotInfo si,
-    float* __restrict__ out, uint16_t* __restrict__ outT, int64_t ldt) {
+    float* __restrict__ out, int64_t ld_out, uint16_t* __restrict__ outT, int64_t ldt) {
   grid_dep_sync();
   __shared__ float tile[kFinishTok][LORA_MAX_RANK + 1];
   TokenItem it;
@@ -205,7 +206,7 @@ __global__ void __launch_bounds__(kFinishThreads) k_rows_finish(
   const int32_t r = it.slot >= 0 ? si.rank[it.slot] : 0;
   const float alpha = !use_alpha ? 1.f : it.slot >= 0 ? si.alpha[it.slot] : 0.f;
   const int nt = (int)min((int64_t)kFinishTok, (int64_t)it.t1 - tb);
-  const int c4n = ldp / 4;
+  const int c4n = ncols / 4;   // float4 groups per token: columns 0 .. ncols - 1
   const int n4 = nt * c4n;
   const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
   float4 pz[kFinishVec][kMaxSplitsRows];
@@ -240,7 +241,7 @@ __global__ void __launch_bounds__(kFinishThreads) k_rows_finish(
       tile[i][4 * c + 2] = v.z;
       tile[i][4 * c + 3] = v.w;
     }
-    if (out) reinterpret_cast<float4*>(out + (tb + i) * ldp)[c] = v;
+    if (out) reinterpret_cast<float4*>(out + (tb + i) * ld_out)[c] = v;
   }
   if (!outT || it.slot < 0) return;   // uniform over the CTA
   __syncthreads();
@@ -611,7 +612,8 @@ cudaError_t launch_tc_rows(const TcRowsArgs& a, cudaStream_t st, int prof_kind) 
   std::lock_guard<std::mutex> lk(mu);
   std::memset(&prm, 0, sizeof(prm));
   const int NP = a.NP;
-  if (!tc::make_map_2d(&prm.ta, a.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.K, a.T, a.K, 64, kBM))
+  if (!tc::make_map_2d(&prm.ta, a.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.K, a.T,
+                       a.lda > 0 ? a.lda : a.K, 64, kBM))
     return cudaErrorInvalidValue;
   for (int k = 0; k < a.n_slots; ++k)
     if (!tc::make_map_2d(&prm.ts[k], a.s[k], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.K,
@@ -663,7 +665,8 @@ cudaError_t launch_tc_rows(const TcRowsArgs& a, cudaStream_t st, int prof_kind) 
   }
   prof_begin(0, st);
   launch_kernel(k_rows_finish, dim3((unsigned)a.max_items, (unsigned)(kBM / kFinishTok)), kFinishThreads, 0, st, 
-      a.part, a.splits, a.T, (int32_t)a.ldo, 1, a.items, a.n_items, a.si, a.out, a.outT, a.ldt);
+      a.part, a.splits, a.T, a.ldo, (int32_t)a.ldo, 1, a.items, a.n_items, a.si, a.out,
+      a.ld_out > 0 ? a.ld_out : a.ldo, a.outT, a.ldt);
   prof_end(prof_kind, st);   // the class's time spans the product and its split-K finish
   return cudaGetLastError();
 }
@@ -679,7 +682,8 @@ cudaError_t launch_tc_red(const TcRedArgs& a, cudaStream_t st, int prof_kind) {
       return cudaErrorInvalidValue;
     prm.rank[k] = a.rank[k];
   }
-  if (!tc::make_map_2d(&prm.tb, a.b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.N, a.T, a.N, 64, 64))
+  if (!tc::make_map_2d(&prm.tb, a.b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.N, a.T,
+                       a.ldb > 0 ? a.ldb : a.N, 64, 64))
     return cudaErrorInvalidValue;
   prm.items = a.items;
   prm.n_items = a.n_items;
@@ -720,7 +724,8 @@ cudaError_t launch_split(const SplitTab& t, int n, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_split_rows_t(const float* src, int64_t lds, int64_t ldt, const TokenItem* items,
+cudaError_t launch_split_rows_t(const float* src, int64_t lds, int64_t ncols, int64_t ldt,
+                                const TokenItem* items,
                                 const int32_t* n_items, int max_items, const SlotInfo& si,
                                 uint16_t* dst, size_t dst_bytes, int64_t T, cudaStream_t st) {
   if (max_items <= 0) return cudaSuccess;
@@ -730,10 +735,10 @@ cudaError_t launch_split_rows_t(const float* src, int64_t lds, int64_t ldt, cons
     cudaError_t e = cudaMemsetAsync(dst, 0, dst_bytes, st);
     if (e != cudaSuccess) return e;
   }
-  if (lds % 4 || lds > LORA_MAX_RANK) return cudaErrorInvalidValue;
+  if (lds % 4 || ncols % 4 || ncols > LORA_MAX_RANK || ncols > lds) return cudaErrorInvalidValue;
   prof_begin(0, st);
   launch_kernel(k_rows_finish, dim3((unsigned)max_items, (unsigned)(kBM / kFinishTok)), kFinishThreads, 0, st, 
-      src, 1, T, (int32_t)lds, 0, items, n_items, si, nullptr, dst, ldt);
+      src, 1, T, lds, (int32_t)ncols, 0, items, n_items, si, nullptr, (int64_t)0, dst, ldt);
   return cudaGetLastError();
 }
 

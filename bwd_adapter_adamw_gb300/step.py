@@ -225,6 +225,126 @@ class LoraStep:
                        self.groups(0.0, 0), zero_grads)
 
 
+@dataclass
+class FusedGroup:
+    """Projections that read one input, run as one fused linear: the stacked frozen weight
+    W [sum out_k, in] and output gradient dY [T, sum out_k], projection k in columns
+    [off_k, off_k + out_k)."""
+    layer: int
+    proj_id: int                 # dropout key of the group (one mask for its projections)
+    X: torch.Tensor              # [T, in]
+    W: torch.Tensor              # [sum out_k, in]
+    dY: torch.Tensor             # [T, sum out_k]
+    outs: Tuple[int, ...]        # out_k
+    Wp: Optional[torch.Tensor] = None
+    Y: Optional[torch.Tensor] = None
+    dX: Optional[torch.Tensor] = None
+    H: Optional[torch.Tensor] = None            # [T, n rank]
+    A: Optional[List[torch.Tensor]] = None      # arena views per projection
+    B: Optional[List[torch.Tensor]] = None
+    gA: Optional[List[torch.Tensor]] = None
+    gB: Optional[List[torch.Tensor]] = None
+
+    @property
+    def in_dim(self) -> int:
+        return self.W.shape[1]
+
+    @property
+    def out_dim(self) -> int:
+        return self.W.shape[0]
+
+
+class FusedLoraStep:
+    """One optimizer step over groups of fused projections ("LoRA Training and Serving",
+    --lora-type: fused projections, one adapter per projection): each group is one fused
+    forward and one fused backward call (one frozen product over the stacked weight each, and
+    one input gradient summed over the group's projections); the arena, the global clip and
+    AdamW are LoraStep's."""
+
+    def __init__(self, groups: Sequence[FusedGroup], *, rank: int, scale: float, dtype: str,
+                 tokens: int, chunks: int, dropout_p: float = 0.0, seed: int = 0,
+                 max_norm: float = 1.0, hp: Optional[L.lora_adamw_hp] = None,
+                 n_streams: int = 1, device="cuda"):
+        self.fgroups = list(groups)
+        self.rank, self.scale, self.dtype = rank, scale, _DT[dtype]
+        self.T, self.chunks = tokens, chunks
+        self.dropout_p, self.seed, self.dora = dropout_p, seed, False
+        self.max_norm = max_norm
+        self.hp = hp if hp is not None else L.make_hp()
+        self.device = torch.device(device)
+        na = sum(rank * g.in_dim * len(g.outs) for g in self.fgroups)
+        nb = sum(g.out_dim * rank for g in self.fgroups)
+        self.n_a, self.n_b, self.n_mag = na, nb, 0
+        self.arena = Arena(na + nb, self.device)
+        oa, ob = 0, na
+        for g in self.fgroups:
+            if sum(g.outs) != g.out_dim:
+                raise ValueError("the projections' widths must add up to the stacked weight's rows")
+            g.A, g.gA, g.B, g.gB = [], [], [], []
+            for o in g.outs:
+                g.A.append(self.arena.view("params", oa, (rank, g.in_dim)))
+                g.gA.append(self.arena.view("grads", oa, (rank, g.in_dim)))
+                oa += rank * g.in_dim
+                g.B.append(self.arena.view("params", ob, (o, rank)))
+                g.gB.append(self.arena.view("grads", ob, (o, rank)))
+                ob += o * rank
+            act = g.X.dtype
+            if g.Y is None:
+                g.Y = torch.empty((self.T, g.out_dim), dtype=act, device=self.device)
+            if g.dX is None:
+                g.dX = torch.empty((self.T, g.in_dim), dtype=act, device=self.device)
+            if g.H is None:
+                g.H = torch.empty((self.T, rank * len(g.outs)), dtype=torch.float32,
+                                  device=self.device)
+        self.n_streams = max(1, n_streams)
+        self.streams = [torch.cuda.Stream(device=self.device) for _ in range(self.n_streams)] \
+            if self.n_streams > 1 else []
+        self.active_streams = self.n_streams
+        need = max(L.lora_fused_workspace_size(self.desc(g), self.T, self.projs(g))
+                   for g in self.fgroups)
+        if need == 0:
+            raise L.LoraError(L.LORA_ERR_INVALID, "lora_fused_workspace_size")
+        self.ws = [_ws(need, self.device) for _ in range(self.n_streams)]
+        self.scale_norm = torch.zeros(2, dtype=torch.float64, device=self.device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
+
+    def desc(self, g: FusedGroup) -> L.lora_desc:
+        return L.make_desc(g.in_dim, g.out_dim, self.rank, self.scale, self.dtype, self.dropout_p,
+                           self.seed, g.layer, g.proj_id, False)
+
+    def projs(self, g: FusedGroup):
+        return L.make_projs([dict(A=a, B=b, dA=ga, dB=gb, out=o)
+                             for a, b, ga, gb, o in zip(g.A, g.B, g.gA, g.gB, g.outs)])
+
+    def prepare_weights(self, stream=None):
+        for g in self.fgroups:
+            if g.Wp is None:
+                g.Wp = torch.empty(L.lora_prepared_weight_size(self.desc(g)), dtype=torch.uint8,
+                                   device=self.device)
+            L.lora_prepare_weight(self.desc(g), g.W, g.Wp, stream)
+
+    def forward_backward(self, opt_step: int, per_chunk_calls: bool = False):
+        main = torch.cuda.current_stream(self.device)
+        k, use = _streams_in_use(self)
+        _fork(main, use)
+        ct = self.T // self.chunks
+        for i, g in enumerate(self.fgroups):
+            st = use[i % k] if use else main
+            ws = self.ws[i % k]
+            d, pj = self.desc(g), self.projs(g)
+            ctx = L.make_ctx(opt_step, 0, ct)
+            L.lora_fused_forward(d, ctx, self.T, g.X, g.W, pj, g.Y, g.H, ws, stream=st)
+            L.lora_fused_backward(d, ctx, self.T, g.X, g.Wp, pj, g.dY, g.H, g.dX, ws, stream=st)
+        _join(main, use)
+
+    groups = LoraStep.groups
+    prepare_ws = LoraStep.prepare_ws
+    optimizer_step = LoraStep.optimizer_step
+    run = LoraStep.run
+    snapshot = LoraStep.snapshot
+    restore = LoraStep.restore
+
+
 class ChainStep(LoraStep):
     """One optimizer step over a stack of adapted linears in which layer l's output is layer
     l + 1's input ("4.3. Training Guide", Truncated BPTT: the backward window is one chunk of

@@ -246,6 +246,36 @@ int lora_adamw_step(float* params, float* grads, float* m, float* v, int32_t n_g
                     const lora_group* groups, const lora_adamw_hp* hp, const double* d_scale_norm,
                     const int32_t* d_status, int32_t zero_grads, void* stream);
 
+/* ---- fused projections ----------------------------------------------------------------------*/
+/* Projections that read one input (q/k/v, gate/up) run as one fused linear: one frozen product
+ * over the stacked weight W_cat = [W_0; W_1; ...] ([sum out_k, in]) and one output
+ * Y_cat [T, sum out_k] whose columns [off_k, off_k + out_k) (off_k = out_0 + ... + out_{k-1})
+ * are projection k's, while every projection keeps its own adapter ("LoRA Training and Serving",
+ * --lora-type: fused projections, and canonical adapters per q/k/v and gate/up projection):
+ *   Y_k = X W_k^T + s' (Xd A_k^T) B_k^T,   dX = sum_k (dY_k W_k + s' (G_k A_k) * M),
+ *   dA_k += s' G_k^T Xd,  dB_k += s' dY_k^T (Xd A_k^T),  G_k = dY_k B_k.
+ * desc: in_dim, out_dim = sum out_k, the shared rank and scale, dtype LORA_BF16, no DoRA; one
+ * dropout mask (desc.layer_id / proj_id) for all the projections. Every out_k is a multiple of
+ * 256 (LORA_ERR_UNSUPPORTED otherwise); 1 <= n_proj <= LORA_MAX_SLOTS. W_prep is
+ * lora_prepare_weight of W_cat (desc above). H_save [T, n_proj * rank] fp32 holds
+ * Hs_k = s' Xd A_k^T in columns k rank .. k rank + rank - 1. dX may be NULL. */
+typedef struct lora_proj {
+  const float* A;   /* [rank, in_dim] */
+  const float* B;   /* [out_dim, rank] */
+  float* dA;        /* [rank, in_dim], accumulated (+=) by lora_fused_backward */
+  float* dB;        /* [out_dim, rank], accumulated (+=) */
+  int64_t out_dim;  /* out_k */
+} lora_proj;
+size_t lora_fused_workspace_size(const lora_desc* d, int64_t T, int32_t n_proj,
+                                 const lora_proj* projs);
+int lora_fused_forward(const lora_desc* d, const lora_ctx* c, int64_t T, const void* X,
+                       const void* W, int32_t n_proj, const lora_proj* projs, void* Y,
+                       float* H_save, void* ws, size_t ws_bytes, void* stream);
+int lora_fused_backward(const lora_desc* d, const lora_ctx* c, int64_t T, const void* X,
+                        const void* W_prep, int32_t n_proj, const lora_proj* projs,
+                        const void* dY, const float* H_save, void* dX, void* ws, size_t ws_bytes,
+                        void* stream);
+
 /* ---- adapter-state maintenance --------------------------------------------------------------*/
 /* Snapshot, restore and retirement of adapter state over the groups' ranges
  * [offset, offset + n_a + n_b + n_mag) of the flat fp32 arenas ("4.3. Training Guide",
