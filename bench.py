@@ -42,6 +42,9 @@ def parse():
     p.add_argument("--chain", action="store_true",
                    help="stack the config's first square projection over its layers, each "
                         "layer's output feeding the next (one stream)")
+    p.add_argument("--fused", action="store_true",
+                   help="run projections that share an input (q/k/v, gate/up) as one fused "
+                        "linear each")
     p.add_argument("--no-graph", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--prof-class", type=int, default=0, help="kernel class to time (0 = auto)")
@@ -283,6 +286,55 @@ def make_chain(cfg, layers, device):
     return step, run, [X0, dY], [step.scale_norm, step.status]
 
 
+def fused_groups(cfg):
+    """The config's projections grouped by the input they read (q/k/v, gate/up), in order."""
+    groups = []
+    for pi, pr in enumerate(cfg.projs):
+        if groups and cfg.projs[groups[-1][0]].x_group == pr.x_group:
+            groups[-1].append(pi)
+        else:
+            groups.append([pi])
+    return groups
+
+
+def make_fused(cfg, layers, streams, device):
+    import torch
+    from bwd_adapter_adamw_gb300 import binding as L
+    from bwd_adapter_adamw_gb300.step import FusedGroup, FusedLoraStep
+    if cfg.multi or cfg.dora or cfg.dtype != "bf16":
+        raise SystemExit(f"--fused needs a single-adapter bf16 config without DoRA ({cfg.name})")
+    groups, xs = [], []
+    for l in range(layers):
+        for idx in fused_groups(cfg):
+            prs = [cfg.projs[i] for i in idx]
+            X = LI.make_x(cfg, l, prs[0], device=device)
+            W = torch.cat([LI.make_w(cfg, l, pr, device=device) for pr in prs], 0)
+            dY = torch.cat([LI.make_dy(cfg, l, pr, device=device) for pr in prs], 1)
+            groups.append(FusedGroup(l, idx[0], X, W, dY, tuple(pr.out_dim for pr in prs)))
+            xs.append(X)
+    hp = L.make_hp(cfg.beta1, cfg.beta2, cfg.eps, cfg.wd, cfg.plus_ratio)
+    step = FusedLoraStep(groups, rank=cfg.rank, scale=_scale(cfg, L), dtype=cfg.dtype,
+                         tokens=cfg.tokens, chunks=cfg.chunks, dropout_p=cfg.dropout_p,
+                         seed=cfg.dropout_seed, max_norm=cfg.max_norm, hp=hp, n_streams=streams,
+                         device=device)
+    members = {idx[0]: idx for idx in fused_groups(cfg)}   # group key: its first projection
+    for g in step.fgroups:
+        for k, i in enumerate(members[g.proj_id]):
+            g.A[k].copy_(LI.make_a(cfg, g.layer, cfg.projs[i], device=device))
+            g.B[k].copy_(LI.make_b(cfg, g.layer, cfg.projs[i], device=device))
+    m, v = LI.make_adam_state(cfg, step.arena.n, "all", device=device)
+    step.arena.m.copy_(m)
+    step.arena.v.copy_(v)
+    step.prepare_weights()
+    lr = L.lora_lr_at(1 if cfg.sched == "cosine" else 0, cfg.lr, cfg.opt_step, cfg.warmup,
+                      cfg.total, cfg.min_lr)
+
+    def run():
+        step.run(cfg.opt_step, lr)
+
+    return step, run, xs + [g.dY for g in step.fgroups], [step.scale_norm, step.status]
+
+
 def make_multi(cfg, streams, device):
     import torch
     from bwd_adapter_adamw_gb300 import binding as L
@@ -404,7 +456,7 @@ def step_stats(per_step):
     return {"median": statistics.median(xs), "p10": q[0], "p90": q[8], "n": len(xs)}
 
 
-def workload_name(cfg, layers, chained=False):
+def workload_name(cfg, layers, chained=False, fused=False):
     projs = "+".join(f"{p.name}:{p.in_dim}->{p.out_dim}" for p in cfg.projs)
     extra = []
     if cfg.multi:
@@ -417,6 +469,9 @@ def workload_name(cfg, layers, chained=False):
         extra.append(f"dropout {cfg.dropout_p}")
     if chained:
         extra.append("chained: layer l's output is layer l+1's input")
+    if fused:
+        names = ["+".join(cfg.projs[i].name for i in g) for g in fused_groups(cfg)]
+        extra.append("fused projections " + ", ".join(names))
     return (f"{cfg.name}: {layers} layers x [{projs}], {cfg.dtype} frozen W, "
             f"{', '.join(extra)}, T={cfg.tokens} in {cfg.chunks} chunks")
 
@@ -437,6 +492,8 @@ def run_ours(args):
     if args.chain:
         cfg = chain_config(cfg)
         step, run, inputs, results = make_chain(cfg, layers, device)
+    elif args.fused:
+        step, run, inputs, results = make_fused(cfg, layers, args.streams, device)
     elif cfg.multi:
         step, run, inputs, results = make_multi(cfg, args.streams, device)
     else:
@@ -573,6 +630,8 @@ def run_ours(args):
             else cnt["dx_flops_per_launch"]
         if args.chain:   # the chained step launches each product once per chunk
             per_launch /= cfg.chunks
+        if args.fused:   # one product per group of projections
+            per_launch *= len(cfg.projs) / len(fused_groups(cfg))
         avg_kern = statistics.mean(kern_ms) if kern_ms else None
         if cfg.dtype == "f32":
             # 3xTF32 on tensor cores: three tf32 products per fp32 product; tf32 dense rate is
@@ -622,7 +681,7 @@ def run_ours(args):
             "scaling": "weak", "vs_baseline": None,
             "dtype": {"f32": "f32", "bf16": "bf16"}.get(cfg.dtype, "e4m3 frozen, bf16 adapter"),
             "data": "synthetic",
-            "config": {"workload": workload_name(cfg, layers, args.chain),
+            "config": {"workload": workload_name(cfg, layers, args.chain, args.fused),
                        "tokens_per_step": tokens,
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                        "l2": "inputs larger than L2 (frozen W alone exceeds 129 MB)"
