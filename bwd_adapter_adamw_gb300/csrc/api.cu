@@ -222,8 +222,23 @@ struct Layout {
   float* sq;           // [T] their row scales
   float* Pq;           // [T, rank] Hs or Gs divided by sq
   float* Qq;           // [max(in, out), rank] B divided by the W row scales, or A^T by W^T's
+  // routed calls (bf16): frozen products on uniform 128-token tiles with per-tile slot sets
+  uint32_t* tmask;     // [ceil(T / 128)] slots present in each tile
+  float* Px;           // [T, ldx] Hs or Gs expanded: token t's values in its slot's column block
+  float* Atx;          // [in, ldx] every slot's A^T side by side, blocks 32-column aligned
+  int64_t ldx;         // upper bound of the padded column blocks' total
   size_t bytes;
 };
+
+// first column of each slot's 32-aligned block in the expanded operands, and their total
+int32_t expanded_cols(const Slots& s, int32_t* pcol) {
+  int32_t c = 0;
+  for (int k = 0; k < s.n; ++k) {
+    pcol[k] = c;
+    c += (s.rank[k] + 31) / 32 * 32;
+  }
+  return c;
+}
 
 // E4M3 prepared weight: [W8 (out x in) | sw (out) | WT8 (in x out) | swT (in)], 16-byte sections
 struct Fp8Prep {
@@ -295,6 +310,13 @@ Layout carve(const lora_desc* d, int64_t T, int32_t n_seg, int n_slots, int64_t 
     L.ritems = c.take<TokenItem>((size_t)L.rmax);
     L.rcount = c.take<int32_t>(4);
   }
+  if (tc && n_seg >= 0) {
+    // 32-aligned column blocks: each rank (a multiple of 4) pads by at most 28 columns
+    L.ldx = rank_sum + 28 * (int64_t)n_slots;
+    L.tmask = c.take<uint32_t>((size_t)((T + kGemmTileT - 1) / kGemmTileT));
+    L.Px = c.take<float>((size_t)T * L.ldx);
+    if (backward) L.Atx = c.take<float>((size_t)d->in_dim * L.ldx);
+  }
   if (d->dtype == LORA_BF16_FP8) {
     const int64_t kmax = d->in_dim > d->out_dim ? d->in_dim : d->out_dim;
     L.Aq = c.take<uint8_t>((size_t)T * kmax);
@@ -325,6 +347,7 @@ SlotInfo slot_info(const Slots& s, float q) {
     si.region[k] = region;
     region += 2 * s.rank[k];
   }
+  expanded_cols(s, si.pcol);
   return si;
 }
 
@@ -341,7 +364,7 @@ void use_uniform_items(Layout& L, int64_t T) {
 
 // shrink on tensor cores: Hs[t, j] = s_k q (Xd[t, :] . A_k[j, :]) via the hi/lo split of A_k
 int tc_shrink(const lora_desc* d, const DropParams& dp, int64_t T, const void* X, int32_t n_seg,
-              const Slots& s, const Layout& L, float* H, cudaStream_t st) {
+              const Slots& s, const Layout& L, float* H, float* Hx, cudaStream_t st) {
   const float q = dropout_q(d);
   const void* Xin = X;
   if (dp.enabled) {
@@ -367,9 +390,41 @@ int tc_shrink(const lora_desc* d, const DropParams& dp, int64_t T, const void* X
   r.part = L.rows_part;
   r.si = slot_info(s, q);
   r.out = H; r.ldo = d->rank;
+  r.out2 = Hx; r.ld2 = L.ldx;   // routed calls: the slot-expanded copy for the frozen product
   r.items = L.gitems; r.n_items = L.gcount; r.max_items = (int)L.gmax;
   LORA_TRY(launch_tc_rows(r, st, LORA_PROF_SHRINK));
   return LORA_OK;
+}
+
+// Routed call: the frozen products run on uniform 128-token tiles, each tile adding the LoRA
+// terms of the slots present in it from the slot-expanded operand (zeroed first: a token's row is
+// zero outside its slot's column block).
+int routed_tiles(int64_t T, int32_t n_seg, const int32_t* seg_start, const int32_t* seg_slot,
+                 const Slots& s, const Layout& L, cudaStream_t st) {
+  LORA_TRY(launch_tile_slot_masks(T, n_seg, seg_start, seg_slot, s.n, L.tmask, st));
+  LORA_TRY(cudaMemsetAsync(L.Px, 0, (size_t)T * L.ldx * sizeof(float), st));
+  return LORA_OK;
+}
+
+void set_routed_gemm(TcGemmArgs& t, const Slots& s, const Layout& L, int64_t T, bool dx) {
+  int32_t pcol[LORA_MAX_SLOTS];
+  expanded_cols(s, pcol);
+  t.items = nullptr;
+  t.n_items = nullptr;
+  t.max_items = (int)((T + kGemmTileT - 1) / kGemmTileT);
+  t.tile_mask = L.tmask;
+  t.p = L.Px;
+  t.ldp = L.ldx;
+  for (int k = 0; k < s.n; ++k) {
+    t.slot_pcol[k] = pcol[k];
+    t.slot_qx[k] = dx ? pcol[k] : 0;     // dX: one A^T map, the slot's block of columns
+    t.slot_qmap[k] = dx ? 0 : k;         // forward: slot k's own B map
+  }
+  if (dx) {
+    t.q[0] = L.Atx;
+    t.q_inner[0] = L.ldx;
+    t.n_q_maps = 1;
+  }
 }
 
 // forward, bf16 activations: shrink and frozen product on tensor cores
@@ -392,7 +447,12 @@ int run_forward_tc(const lora_desc* d, const DropParams& dp, int64_t T, const vo
   const bool fp8 = d->dtype == LORA_BF16_FP8;
   if (fp8)   // E4M3 codes and per-token scales of X for the frozen product
     LORA_TRY(launch_quant_rows_e4m3(X, T, d->in_dim, L.Aq, L.sq, st));
-  int rc = tc_shrink(d, dp, T, X, n_seg, s, L, H, st);
+  const bool routed = n_seg >= 0;
+  if (routed) {
+    int rr = routed_tiles(T, n_seg, seg_start, seg_slot, s, L, st);
+    if (rr) return rr;
+  }
+  int rc = tc_shrink(d, dp, T, X, n_seg, s, L, H, routed ? L.Px : nullptr, st);
   if (rc) return rc;
   TcGemmArgs t{};
   t.a = X; t.T = T; t.b = W; t.n_rows = d->out_dim; t.K = d->in_dim;
@@ -409,6 +469,7 @@ int run_forward_tc(const lora_desc* d, const DropParams& dp, int64_t T, const vo
     t.m_rowscale = L.sq; t.n_colscale = f.sw;
   }
   t.items = L.gitems; t.n_items = L.gcount; t.max_items = (int)L.gmax; t.drop = dp;
+  if (routed) set_routed_gemm(t, s, L, T, false);
   LORA_TRY(launch_tc_gemm(t, st, LORA_PROF_FROZEN_FWD));
   return LORA_OK;
 }
@@ -430,7 +491,10 @@ int run_backward_tc(const lora_desc* d, const DropParams& dp, int64_t T, const v
                                       L.count_db, (int32_t)L.max_db, st));
     LORA_TRY(launch_make_red_items_tc(T, n_seg, seg_start, seg_slot, s.n, L.span_da, L.items_da,
                                       L.count_da, (int32_t)L.max_da, st));
+    int rr = routed_tiles(T, n_seg, seg_start, seg_slot, s, L, st);
+    if (rr) return rr;
   }
+  const bool routed = n_seg >= 0;
   const float q = dropout_q(d);
   const SlotInfo si = slot_info(s, q);
   // A^T (fp32) for the LoRA K-steps of dX; hi/lo split of B^T for G
@@ -446,6 +510,13 @@ int run_backward_tc(const lora_desc* d, const DropParams& dp, int64_t T, const v
       ta.src[k] = s.A[k]; ta.dst[k] = At[k]; ta.rows[k] = s.rank[k]; ta.cols[k] = d->in_dim;
       sp.src[k] = s.B[k]; sp.dst[k] = L.Sb + ob; sp.rank[k] = s.rank[k];
       ob += 2 * (int64_t)s.rank[k] * d->out_dim;
+    }
+    if (routed) {   // every slot's A^T side by side in one operand, 32-aligned blocks
+      LORA_TRY(cudaMemsetAsync(L.Atx, 0, (size_t)d->in_dim * L.ldx * sizeof(float), st));
+      for (int k = 0; k < s.n; ++k) {
+        ta.dst[k] = L.Atx + si.pcol[k];
+        ta.ld_dst[k] = L.ldx;
+      }
     }
     LORA_TRY(launch_transpose_slots(ta, s.n, d->rank, d->in_dim, st));
     LORA_TRY(launch_split(sp, s.n, st));
@@ -477,6 +548,10 @@ int run_backward_tc(const lora_desc* d, const DropParams& dp, int64_t T, const v
     r.si = si;
     r.out = L.Gs; r.ldo = d->rank;
     r.outT = L.GsT; r.ldt = L.ldt; r.outT_bytes = (size_t)2 * s.rank_sum * L.ldt * sizeof(uint16_t);
+    if (routed) {   // the slot-expanded Gs for the dX product's uniform tiles
+      r.out2 = L.Px;
+      r.ld2 = L.ldx;
+    }
     r.items = L.gitems; r.n_items = L.gcount; r.max_items = (int)L.gmax;
     LORA_TRY(launch_tc_rows(r, st, LORA_PROF_G));
   }
@@ -488,6 +563,7 @@ int run_backward_tc(const lora_desc* d, const DropParams& dp, int64_t T, const v
     for (int k = 0; k < s.n; ++k) { t.q[k] = At[k]; t.q_rank[k] = s.rank[k]; }
     t.lora_separate = dp.enabled; t.out = dX; t.ldo = d->in_dim;
     t.items = L.gitems; t.n_items = L.gcount; t.max_items = (int)L.gmax; t.drop = dp;
+    if (routed) set_routed_gemm(t, s, L, T, true);
     if (d->dtype == LORA_BF16_FP8) {
       // dX = sd swT (dY8 WT8^T) + Gs A: the LoRA operands divided by the same scales
       const Fp8Prep f = fp8_prep(Wt, d->out_dim, d->in_dim);

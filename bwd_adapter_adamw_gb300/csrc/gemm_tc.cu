@@ -92,6 +92,10 @@ struct TcParams {
   int32_t has_lora;
   int32_t lora_separate;
   int32_t q_rank[LORA_MAX_SLOTS];
+  const uint32_t* tile_mask;            // routed uniform tiles: slots present per 128-token tile
+  int32_t slot_pcol[LORA_MAX_SLOTS];
+  int32_t slot_qx[LORA_MAX_SLOTS];
+  int32_t slot_qmap[LORA_MAX_SLOTS];
   int32_t n_col_groups;                 // > 0: the adapter is chosen by output column, not token
   int32_t col_end[LORA_MAX_SLOTS];      // group k covers columns [col_end[k-1], col_end[k])
   int32_t p_col[LORA_MAX_SLOTS];        // group k's LoRA operand starts at column p_col[k] of P
@@ -125,6 +129,59 @@ __device__ __forceinline__ int tile_slot(const TcParams& p, const TokenItem& it,
   pcol = p.p_col[k];
   qcol0 = k > 0 ? p.col_end[k - 1] : 0;
   return k;
+}
+
+// LoRA K-blocks of a tile: from the item's slot (token-routed items), the column group holding
+// the tile (fused projections), or every slot present in a uniform tile of a routed call
+// (tile_mask: each slot's operand occupies its own column block of P, zero at the other slots'
+// tokens, so the slots' terms add up in one accumulator).
+struct LoraTile {
+  uint32_t mask;
+  int slot;
+  int pcol;
+  int qrow0;
+};
+
+__device__ __forceinline__ int lora_tile(const TcParams& p, const TokenItem& it, int32_t n0,
+                                         LoraTile& lt) {
+  lt.mask = 0;
+  lt.slot = -1;
+  lt.pcol = 0;
+  lt.qrow0 = 0;
+  if (!p.has_lora) return 0;
+  if (p.tile_mask) {
+    lt.mask = p.tile_mask[it.t0 / kBM];
+    int nb = 0;
+    for (uint32_t m = lt.mask; m; m &= m - 1) nb += (p.q_rank[__ffs(m) - 1] + 31) / 32;
+    return nb;
+  }
+  lt.slot = tile_slot(p, it, n0, lt.pcol, lt.qrow0);
+  return lt.slot >= 0 ? (p.q_rank[lt.slot] + 31) / 32 : 0;
+}
+
+// Tensor map and coordinates of LoRA K-block jj of a tile.
+__device__ __forceinline__ void lora_block(const TcParams& p, const LoraTile& lt, int jj,
+                                           int& qmap, int& px, int& qx, int& qrow0) {
+  if (!lt.mask) {
+    qmap = lt.slot;
+    px = lt.pcol + 32 * jj;
+    qx = 32 * jj;
+    qrow0 = lt.qrow0;
+    return;
+  }
+  uint32_t m = lt.mask;
+  int sl = __ffs(m) - 1;
+  for (;;) {
+    const int nb = (p.q_rank[sl] + 31) / 32;
+    if (jj < nb) break;
+    jj -= nb;
+    m &= m - 1;
+    sl = __ffs(m) - 1;
+  }
+  qmap = p.slot_qmap[sl];
+  px = p.slot_pcol[sl] + 32 * jj;
+  qx = p.slot_qx[sl] + 32 * jj;
+  qrow0 = 0;
 }
 
 template <int BN>
@@ -187,9 +244,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
         TokenItem it;
         int32_t n0;
         if (!decode_tile<BN>(p, t, it, n0)) continue;
-        int pcol, qcol0;
-        const int slot = tile_slot(p, it, n0, pcol, qcol0);
-        const int nk = p.nk_main + ((p.has_lora && slot >= 0) ? (p.q_rank[slot] + 31) / 32 : 0);
+        LoraTile lt;
+        const int nk = p.nk_main + lora_tile(p, it, n0, lt);
         for (int kb = 0; kb < nk; ++kb, ++g) {
           const int s = g % kStages;
           const uint32_t ph = (uint32_t)(g / kStages) & 1u;
@@ -202,9 +258,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
             tma_load_2d(sa, &p.ta, &full_bar[s], kb * kKBlock, it.t0);
             tma_load_2d(sb, &p.tb, &full_bar[s], kb * kKBlock, n0);
           } else {
-            const int j = kb - p.nk_main;
-            tma_load_2d(sa, &p.tp, &full_bar[s], pcol + j * 32, it.t0);
-            tma_load_2d(sb, &p.tq[slot], &full_bar[s], j * 32, n0 - qcol0);
+            int qmap, px, qx, qrow0;
+            lora_block(p, lt, kb - p.nk_main, qmap, px, qx, qrow0);
+            tma_load_2d(sa, &p.tp, &full_bar[s], px, it.t0);
+            tma_load_2d(sb, &p.tq[qmap], &full_bar[s], qx, n0 - qrow0);
           }
         }
       }
@@ -220,9 +277,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
         TokenItem it;
         int32_t n0;
         if (!decode_tile<BN>(p, t, it, n0)) continue;
-        int pcol, qcol0;
-        const int slot = tile_slot(p, it, n0, pcol, qcol0);
-        const int nk_lora = (p.has_lora && slot >= 0) ? (p.q_rank[slot] + 31) / 32 : 0;
+        LoraTile lt;
+        const int nk_lora = lora_tile(p, it, n0, lt);
         const int nk = p.nk_main + nk_lora;
         const bool sep = p.lora_separate && nk_lora > 0;
         const int b = j % nbuf, use = j / nbuf;
@@ -268,9 +324,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
       TokenItem it;
       int32_t n0;
       if (!decode_tile<BN>(p, t, it, n0)) continue;
-      int pcol, qcol0;
-      const int slot = tile_slot(p, it, n0, pcol, qcol0);
-      const bool sep = p.lora_separate && p.has_lora && slot >= 0 && p.q_rank[slot] > 0;
+      LoraTile lt;
+      const bool sep = p.lora_separate && lora_tile(p, it, n0, lt) > 0;
       const int b = j % nbuf, use = j / nbuf;
       const int64_t m = (int64_t)it.t0 + row;
       const bool row_ok = m < it.t1;
@@ -444,14 +499,16 @@ cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st, int prof_kind) 
   if (a.p) {
     if (!tc::make_map_2d(&prm.tp, a.p, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.ldp, a.T, a.ldp, 32, kBM))
       return cudaErrorInvalidValue;
-    for (int k = 0; k < a.n_slots; ++k) {
-      prm.q_rank[k] = a.q_rank[k];
+    for (int k = 0; k < a.n_slots; ++k) prm.q_rank[k] = a.q_rank[k];
+    const int n_maps = a.n_q_maps > 0 ? a.n_q_maps : a.n_slots;
+    for (int k = 0; k < n_maps; ++k) {
+      const int64_t q_in = a.q_inner[k] > 0 ? a.q_inner[k] : a.q_rank[k];
       // Q_k has the output rows of its column group (fused projections) or all of them
       const int64_t q_rows = a.n_col_groups > 0
                                  ? a.col_end[k] - (k > 0 ? a.col_end[k - 1] : 0)
                                  : a.n_rows;
-      if (!tc::make_map_2d(&prm.tq[k], a.q[k], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.q_rank[k], q_rows,
-                    a.q_rank[k], 32, bn))
+      if (!tc::make_map_2d(&prm.tq[k], a.q[k], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, q_in, q_rows,
+                    q_in, 32, bn))
         return cudaErrorInvalidValue;
     }
   }
@@ -464,6 +521,18 @@ cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st, int prof_kind) 
   prm.lora_separate = a.lora_separate;
   prm.n_colscale = a.n_colscale;
   prm.m_rowscale = a.m_rowscale;
+  prm.tile_mask = a.tile_mask;
+  if (a.tile_mask) {
+    if (a.items) return cudaErrorInvalidValue;   // slot sets need uniform tiles
+    for (int k = 0; k < a.n_slots; ++k) {
+      prm.slot_pcol[k] = a.slot_pcol[k];
+      prm.slot_qx[k] = a.slot_qx[k];
+      prm.slot_qmap[k] = a.slot_qmap[k];
+      if (a.slot_pcol[k] % 4 || a.slot_qx[k] % 4 || a.slot_qmap[k] < 0 ||
+          a.slot_qmap[k] >= (a.n_q_maps > 0 ? a.n_q_maps : a.n_slots))
+        return cudaErrorInvalidValue;
+    }
+  }
   prm.n_col_groups = a.n_col_groups;
   for (int k = 0; k < a.n_col_groups; ++k) {
     prm.col_end[k] = (int32_t)a.col_end[k];

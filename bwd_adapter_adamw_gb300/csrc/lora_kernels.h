@@ -55,6 +55,12 @@ struct TcGemmArgs {
   DropParams drop;
   const float* n_colscale;   // per output column scale (DoRA m / n, or the FP8 W scales), nullable
   const float* m_rowscale;   // per token-row scale (the FP8 activation scales), nullable
+  const uint32_t* tile_mask; // routed calls on uniform 128-token tiles: the slots of each tile;
+  int32_t slot_pcol[LORA_MAX_SLOTS];   //   slot s's LoRA operand: P columns slot_pcol[s] ..,
+  int32_t slot_qx[LORA_MAX_SLOTS];     //   Q map slot_qmap[s] from column slot_qx[s]
+  int32_t slot_qmap[LORA_MAX_SLOTS];
+  int32_t n_q_maps;          // Q tensor maps to build (0: n_slots)
+  int64_t q_inner[LORA_MAX_SLOTS];     // Q_k row length (0: q_rank[k])
   int32_t n_col_groups;      // > 0: fused projections, adapter k covers output columns
   int64_t col_end[LORA_MAX_SLOTS];   //   [col_end[k-1], col_end[k]) (multiples of 256), its
   int32_t p_col[LORA_MAX_SLOTS];     //   LoRA operand in columns p_col[k].. of P
@@ -81,6 +87,7 @@ struct SlotInfo {
   int32_t rank[LORA_MAX_SLOTS];
   float alpha[LORA_MAX_SLOTS];
   int32_t region[LORA_MAX_SLOTS];   // first row of the slot in a per-slot [sum 2 r, ldt] buffer
+  int32_t pcol[LORA_MAX_SLOTS];     // first column of the slot in a slot-expanded [T, ld2] copy
 };
 struct TcRowsArgs {                 // out[t, j] = alpha * (A[t, :] . (S_hi[j] + S_lo[j]))
   const void* a;                    // [T, K] bf16
@@ -97,6 +104,8 @@ struct TcRowsArgs {                 // out[t, j] = alpha * (A[t, :] . (S_hi[j] +
   int64_t ldo;                      // partial row stride (largest rank)
   int64_t ld_out;                   // out row stride (0: ldo)
   int64_t lda;                      // A row stride in elements (0: K)
+  float* out2;                      // optional slot-expanded copy [T, ld2]: token t's values in
+  int64_t ld2;                      //   columns si.pcol[slot(t)] .. + r (other columns untouched)
   uint16_t* outT;                   // optional per slot [2 r, ldt] bf16 transposed split of out
   int64_t ldt;
   size_t outT_bytes;                // zeroed first when an item table routes several slots
@@ -220,6 +229,10 @@ cudaError_t launch_colred(int dtype, const ColRedArgs& a, int max_items, cudaStr
 // ---- lowrank.cu ----
 cudaError_t launch_colscale_bf16(const void* src, const float* scale, int64_t rows, int64_t cols,
                                  void* dst, cudaStream_t st);
+// masks[i] = bitmask of the slots routed any token of 128-token tile i (i < ceil(T / 128))
+cudaError_t launch_tile_slot_masks(int64_t T, int32_t n_seg, const int32_t* seg_start,
+                                   const int32_t* seg_slot, int32_t n_slots, uint32_t* masks,
+                                   cudaStream_t st);
 cudaError_t launch_make_items(int64_t T, int32_t n_seg, const int32_t* seg_start,
                               const int32_t* seg_slot, int32_t n_slots, TokenItem* gitems,
                               int32_t* gcount, int32_t gmax, TokenItem* ritems, int32_t* rcount,

@@ -220,6 +220,50 @@ cudaError_t launch_make_items(int64_t T, int32_t n_seg, const int32_t* seg_start
   return cudaGetLastError();
 }
 
+// Slot bitmask of every 128-token tile: bit s is set when a token of the tile is routed to slot s
+// (segments taken in order, each covering [max(start, coverage so far), end) clamped to [0, T),
+// exactly as for the token items). One thread per tile scans the staged segment table.
+__global__ void __launch_bounds__(256) k_tile_slot_masks(int64_t T, int32_t n_seg,
+                                                         const int32_t* __restrict__ seg_start,
+                                                         const int32_t* __restrict__ seg_slot,
+                                                         int32_t n_slots, uint32_t* masks,
+                                                         int64_t n_tiles) {
+  grid_dep_sync();
+  __shared__ int32_t s_start[kSegSmem + 1], s_slot[kSegSmem];
+  const SegView sv = stage_segments(n_seg, seg_start, seg_slot, s_start, s_slot);
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_tiles;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t lo = i * kGemmTileT, hi = min(T, lo + kGemmTileT);
+    uint32_t m = 0;
+    int64_t cursor = 0;
+    for (int32_t k = 0; k < sv.n; ++k) {
+      int64_t a = sv.start[k], b = sv.start[k + 1];
+      a = max((int64_t)0, min(a, T));
+      b = max((int64_t)0, min(b, T));
+      if (a < cursor) a = cursor;
+      if (b <= a) continue;
+      cursor = b;
+      if (a >= hi) break;   // this and every later segment start after the tile
+      const int32_t slot = sv.slot[k];
+      if (slot >= 0 && slot < n_slots && b > lo) m |= 1u << slot;
+    }
+    masks[i] = m;
+  }
+}
+
+cudaError_t launch_tile_slot_masks(int64_t T, int32_t n_seg, const int32_t* seg_start,
+                                   const int32_t* seg_slot, int32_t n_slots, uint32_t* masks,
+                                   cudaStream_t st) {
+  const int64_t n_tiles = (T + kGemmTileT - 1) / kGemmTileT;
+  if (n_tiles <= 0) return cudaSuccess;
+  int64_t blocks = (n_tiles + 255) / 256;
+  if (blocks > 1024) blocks = 1024;
+  prof_begin(0, st);
+  launch_kernel(k_tile_slot_masks, (unsigned)blocks, 256, 0, st, T, n_seg, seg_start, seg_slot,
+                n_slots, masks, n_tiles);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_transpose_slots(const TransposeTab& t, int n, int64_t max_rows, int64_t max_cols,
                                    cudaStream_t st) {
   if (n <= 0) return cudaSuccess;

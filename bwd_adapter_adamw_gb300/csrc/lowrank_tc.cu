@@ -196,7 +196,8 @@ __global__ void __launch_bounds__(kFinishThreads) k_rows_finish(
     const float* __restrict__ part, int32_t splits, int64_t T, int64_t ldp, int32_t ncols,
     int use_alpha,
     const TokenItem* __restrict__ items, const int32_t* __restrict__ n_items, const SlotInfo si,
-    float* __restrict__ out, int64_t ld_out, uint16_t* __restrict__ outT, int64_t ldt) {
+    float* __restrict__ out, int64_t ld_out, float* __restrict__ out2, int64_t ld2,
+    uint16_t* __restrict__ outT, int64_t ldt) {
   grid_dep_sync();
   __shared__ float tile[kFinishTok][LORA_MAX_RANK + 1];
   TokenItem it;
@@ -242,6 +243,8 @@ __global__ void __launch_bounds__(kFinishThreads) k_rows_finish(
       tile[i][4 * c + 3] = v.w;
     }
     if (out) reinterpret_cast<float4*>(out + (tb + i) * ld_out)[c] = v;
+    if (out2 && 4 * c < r)   // the slot-expanded copy: the slot's own column block
+      reinterpret_cast<float4*>(out2 + (tb + i) * ld2 + si.pcol[it.slot])[c] = v;
   }
   if (!outT || it.slot < 0) return;   // uniform over the CTA
   __syncthreads();
@@ -666,7 +669,7 @@ cudaError_t launch_tc_rows(const TcRowsArgs& a, cudaStream_t st, int prof_kind) 
   prof_begin(0, st);
   launch_kernel(k_rows_finish, dim3((unsigned)a.max_items, (unsigned)(kBM / kFinishTok)), kFinishThreads, 0, st, 
       a.part, a.splits, a.T, a.ldo, (int32_t)a.ldo, 1, a.items, a.n_items, a.si, a.out,
-      a.ld_out > 0 ? a.ld_out : a.ldo, a.outT, a.ldt);
+      a.ld_out > 0 ? a.ld_out : a.ldo, a.out2, a.ld2, a.outT, a.ldt);
   prof_end(prof_kind, st);   // the class's time spans the product and its split-K finish
   return cudaGetLastError();
 }
@@ -738,7 +741,8 @@ cudaError_t launch_split_rows_t(const float* src, int64_t lds, int64_t ncols, in
   if (lds % 4 || ncols % 4 || ncols > LORA_MAX_RANK || ncols > lds) return cudaErrorInvalidValue;
   prof_begin(0, st);
   launch_kernel(k_rows_finish, dim3((unsigned)max_items, (unsigned)(kBM / kFinishTok)), kFinishThreads, 0, st, 
-      src, 1, T, lds, (int32_t)ncols, 0, items, n_items, si, nullptr, (int64_t)0, dst, ldt);
+      src, 1, T, lds, (int32_t)ncols, 0, items, n_items, si, nullptr, (int64_t)0, nullptr,
+      (int64_t)0, dst, ldt);
   return cudaGetLastError();
 }
 

@@ -132,6 +132,31 @@ def test_fullsize_single_sampled(L, name, layers):
         assert n_clause == 0
 
 
+def test_fullsize_fp8_sampled(L):
+    """c4 with the E4M3 frozen product, layer 0's wq at full size (T 8192, 4096 x 4096): the
+    per-token outputs on sampled tokens against the oracle's E4M3 product (codes per token row,
+    so a sampled row quantises as it does in the full batch), the adapter gradients in full."""
+    cfg = LI.CONFIGS["c4fp8"]
+    _warm_library(L)
+    step, problems, state, s, hp_o = build_single(cfg, [0], [0], n_streams=4)
+    _replay_once(lambda: step.run(cfg.opt_step, hp_o.lr, zero_grads=False))
+    assert int(step.status.item()) == O.STATUS_OK
+    rows = _sample_rows(cfg.tokens, 11)
+    lin = step.linears[0]
+    pr, st = problems[(0, 0)], state[(0, 0)]
+    X = _rows_of(pr["X"], rows).float().numpy()
+    dY = _rows_of(pr["dY"], rows).float().numpy()
+    W = pr["W"].float().numpy()
+    f = O.lora_forward_fp8(X, W, st.A, st.B, s)
+    b = O.lora_backward(X, W, st.A, st.B, dY, s)
+    assert rel_err(_rows_of(lin.Y, rows), f.Y) <= TOL_BF16
+    assert rel_err(_rows_of(lin.H, rows), s * f.H) <= TOL_BF16
+    assert rel_err(_rows_of(lin.dX, rows), O.lora_dx_fp8(dY, W, st.A, b.G, s)) <= TOL_BF16
+    gA, gB = O.lora_adapter_grads(pr["X"], st.A, st.B, pr["dY"], s)
+    assert rel_err(lin.gA, gA) <= TOL_BF16
+    assert rel_err(lin.gB, gB) <= TOL_BF16
+
+
 def test_fullsize_multi_sampled(L):
     from bwd_adapter_adamw_gb300.step import MultiLinear, MultiLoraStep
     cfg = LI.CONFIGS["c5"]
