@@ -90,13 +90,13 @@ def counts(cfg: LI.LoraConfig, layers: int):
 
 def memory_counts(cfg: LI.LoraConfig, layers: int):
     """Algorithmic HBM bytes per step of the memory-bound kernel classes (each array the class
-    must touch, once): shrink reads X and A and writes Hs (and, on the fp32 path, the tf32 split
+    must touch, once): shrink reads X and A and writes Hs (and, on the fp32 path, the bf16 split
     of X); G reads dY' and B and writes Gs (and the split of dY'); the dB / dA reductions read dY'
     or X and Hs or Gs and update dB / dA; grad-prepare reads 4 B and AdamW moves 32 B per
     parameter (p, g, m, v read; p, m, v written; g cleared)."""
     T = cfg.tokens
     a = 4 if cfg.dtype == "f32" else 2
-    split = 8 if cfg.dtype == "f32" else 0
+    split = 4 if cfg.dtype == "f32" else 0   # bf16 hi + lo per element
     if cfg.multi:
         ranks = list(LI.make_routing(cfg).slot_rank)
         r_all, layers = sum(ranks), 1
@@ -659,13 +659,11 @@ def run_ours(args):
             per_launch *= len(cfg.projs) / len(fused_groups(cfg))
         avg_kern = statistics.mean(kern_ms) if kern_ms else None
         if cfg.dtype == "f32":
-            # 3xTF32 on tensor cores: three tf32 products per fp32 product; tf32 dense rate is
-            # the measured bf16 rate x the nominal tf32 : bf16 ratio (1.1 : 2.25)
-            tf32 = peaks["bf16_tflops"] * 1.1 / 2.25
-            peak = tf32 / 3.0
+            # fp32 products as three bf16 products of the split operands
+            peak = peaks["bf16_tflops"] / 3.0
             bound, punit = "tensor", "TFLOP/s"
-            note = (f"3xTF32 effective: measured bf16 {peaks['bf16_tflops']:.0f} x 1.1/2.25 "
-                    f"= {tf32:.0f} tf32 TF/s, / 3 products ({peak_src})")
+            note = (f"split-bf16 effective: measured bf16 {peaks['bf16_tflops']:.0f} / 3 products "
+                    f"({peak_src})")
         elif cfg.dtype == "bf16fp8":
             # E4M3 products: the measured bf16 rate x the nominal fp8 : bf16 ratio (4.5 : 2.25)
             peak = peaks["bf16_tflops"] * 4.5 / 2.25

@@ -203,8 +203,8 @@ struct Layout {
   float* partA;        // [rmax_items][in][rank] (fp32 path)
   uint16_t* dYs;       // [T, out] bf16 dY * (m / n) for the DoRA tensor-core products
   float* rd_part;      // [K chunks][T][16] partials of the CUDA-core shrink / G (fp32 path)
-  float* Ah;           // [T, K] tf32 split of X (forward) or dY' (backward): hi ... (fp32 path)
-  float* Al;           // ... and lo
+  uint16_t* Ah;        // [T, K] bf16 split of X (forward) or dY' (backward): hi ... (fp32 path)
+  uint16_t* Al;        // ... and lo
 
   // tensor-core path
   uint16_t* Xd;        // [T, in] bf16 masked input (dropout)
@@ -327,8 +327,8 @@ Layout carve(const lora_desc* d, int64_t T, int32_t n_seg, int n_slots, int64_t 
   if (!tc) {
     const int64_t kmax = d->in_dim > d->out_dim ? d->in_dim : d->out_dim;
     L.rd_part = c.take<float>((size_t)((kmax + kRowChunk - 1) / kRowChunk) * T * kRowPartCols);
-    L.Ah = c.take<float>((size_t)T * kmax);
-    L.Al = c.take<float>((size_t)T * kmax);
+    L.Ah = c.take<uint16_t>((size_t)T * kmax);
+    L.Al = c.take<uint16_t>((size_t)T * kmax);
   }
   L.bytes = c.off + kWsAlign;
   return L;
@@ -651,13 +651,13 @@ int run_forward(const lora_desc* d, const DropParams& dp, int64_t T, const void*
     a.split_hi = L.Ah; a.split_lo = L.Al;
     LORA_TRY(launch_rowdot(d->dtype, a, max_items, st, LORA_PROF_SHRINK));
   }
-  // frozen product + Hs B_k^T, times m/n per column in DoRA mode (3xTF32 tensor cores); the
-  // prepared weight holds [W_hi | W_lo | W^T_hi | W^T_lo]
+  // frozen product + Hs B_k^T, times m/n per column in DoRA mode (three bf16 products of the
+  // split operands); the prepared weight holds bf16 [W_hi | W_lo | W^T_hi | W^T_lo]
   {
     const int64_t n = d->out_dim * d->in_dim;
     TcGemmArgs t{};
     t.a = L.Ah; t.a_lo = L.Al; t.T = T;
-    t.b = Wprep; t.b_lo = static_cast<const float*>(Wprep) + n;
+    t.b = Wprep; t.b_lo = static_cast<const uint16_t*>(Wprep) + n;
     t.n_rows = d->out_dim; t.K = d->in_dim;
     t.p = H; t.ldp = d->rank; t.n_slots = s.n;
     for (int k = 0; k < s.n; ++k) { t.q[k] = s.B[k]; t.q_rank[k] = s.rank[k]; }
@@ -734,7 +734,7 @@ int run_backward(const lora_desc* d, const DropParams& dp, int64_t T, const void
     const int64_t n = d->out_dim * d->in_dim;
     TcGemmArgs t{};
     t.a = L.Ah; t.a_lo = L.Al; t.T = T;
-    t.b = static_cast<const float*>(Wt) + 2 * n; t.b_lo = static_cast<const float*>(Wt) + 3 * n;
+    t.b = static_cast<const uint16_t*>(Wt) + 2 * n; t.b_lo = static_cast<const uint16_t*>(Wt) + 3 * n;
     t.n_rows = d->in_dim; t.K = d->out_dim;
     t.p = L.Gs; t.ldp = d->rank; t.n_slots = s.n;
     for (int k = 0; k < s.n; ++k) { t.q[k] = At[k]; t.q_rank[k] = s.rank[k]; }
@@ -1097,7 +1097,7 @@ size_t lora_prepared_weight_size(const lora_desc* d) {
   if (check_desc(d, 0, false) != LORA_OK) return 0;
   const size_t n = (size_t)d->out_dim * (size_t)d->in_dim;
   if (d->dtype == LORA_BF16_FP8) return fp8_prep_bytes(d->out_dim, d->in_dim);
-  return d->dtype == LORA_F32 ? 16 * n : 2 * n;
+  return d->dtype == LORA_F32 ? 8 * n : 2 * n;
 }
 
 int lora_prepare_weight(const lora_desc* d, const void* W, void* W_prep, void* stream) {

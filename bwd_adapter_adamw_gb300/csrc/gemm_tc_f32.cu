@@ -1,19 +1,23 @@
-// Tensor-core frozen products for fp32 activations (sm_103a), 3xTF32:
+// Tensor-core frozen products for fp32 activations (sm_103a), as three bf16 products:
 //
 //   out[t, n] = ( sum_k A[t, k] B[n, k] + [mask(t, n)] * sum_j P[t, j] Q_slot[n, j] ) * colscale[n]
 //
-// with every fp32 operand x split into x_hi = tf32(x) (round to nearest) and x_lo = x - x_hi, and
-// each product formed as A_hi B_hi + A_hi B_lo + A_lo B_hi with tcgen05.mma kind::tf32. The
-// dropped A_lo B_lo term and the tf32 reading of x_lo are both O(2^-22) relative, so the result
-// stays at fp32-level accuracy. (Same roles as the bf16 kernel: frozen forward X W^T + Hs B^T,
-// frozen dX dY' W + (Gs A) * M; "8. LoRA Fundamentals", How it works; "Backward Bug Hunts and
-// Vulkan Tiled GEMM", Bug #1.)
+// with every fp32 operand x of the main product split into x_hi = bf16(x) and x_lo =
+// bf16(x - x_hi), and the product formed as A_hi B_hi + A_hi B_lo + A_lo B_hi with tcgen05.mma
+// kind::f16 (bf16 operands, fp32 accumulation). The split keeps 16 significant bits of every
+// operand (|x - x_hi - x_lo| <= 2^-16 |x|) and the dropped A_lo B_lo term is of the same order,
+// so the result stays within the fp32 paths' 1e-5 relative bound (about 4e-6 on the TinyLlama
+// shapes), at a third of the bf16 tensor rate, where three tf32 products would run at a sixth.
+// The short LoRA K-blocks (P = Hs or Gs, Q = B or A^T, at most two 32-wide blocks) land raw and
+// are split in shared memory by two converter warps into tf32 hi / lo (three kind::tf32 products,
+// about 2^-21 relative). (Same roles as the bf16 kernel: frozen forward X W^T + Hs B^T, frozen
+// dX dY' W + (Gs A) * M; "8. LoRA Fundamentals", How it works; "Backward Bug Hunts and Vulkan
+// Tiled GEMM", Bug #1.)
 //
 // The frozen operands arrive already split in HBM: B (W or W^T) by the weight preparation, once,
 // and A (X or dY') by the streaming shrink / G kernel, which reads A anyway. So the main K-loop
-// is a plain TMA -> MMA pipeline of four tiles per stage (A_hi, A_lo, B_hi, B_lo). Only the
-// short LoRA K-blocks (P = Hs or Gs, Q = B or A^T, at most two 32-wide blocks) land raw and are
-// split in shared memory by two converter warps.
+// is a plain TMA -> MMA pipeline of four bf16 tiles per stage (A_hi, A_lo, B_hi, B_lo), 64
+// elements of K each.
 //
 // Per K-step two MMAs: A_hi x [B_hi; B_lo] as one N = 256 instruction (the stage holds B_hi and
 // B_lo back to back), whose first 128 columns take A_hi B_hi and last 128 A_hi B_lo, then
@@ -22,14 +26,13 @@
 //
 // The tensor core's fp32 accumulation loses a little at every MMA, so no accumulation chain is
 // allowed to grow with K: two 256-column TMEM regions take turns, each holding the partial sum of
-// 8 K-blocks (a period), and while one fills, the epilogue warps drain the other into fp32
-// registers with ordinary round-to-nearest adds. The LoRA K-blocks form a period of their own,
-// masked element-wise when the LoRA term is dropout-masked.
+// 256 elements of K (a period: 4 main K-blocks), and while one fills, the epilogue warps drain
+// the other into fp32 registers with ordinary round-to-nearest adds. The LoRA K-blocks form a
+// period of their own, masked element-wise when the LoRA term is dropout-masked.
 //
 // CTA (384 threads): warp 0 TMA, warp 1 TMEM + MMA issue, warps 2..9 epilogue, warps 10..11 LoRA
-// split. Tile 128 x 128; K-block 32 fp32 = one 128-byte swizzled row; three stages of four tiles.
-// (Seven stages of 16-wide K-blocks in the 64-byte swizzle measured slower: the TMA engine moves
-// 64-byte rows at a lower byte rate than 128-byte rows.)
+// split. Tile 128 x 128; every K-block is one 128-byte swizzled row (64 bf16 of the main
+// product, 32 fp32 of the LoRA term); three stages of four tiles.
 #include <cstring>
 #include <mutex>
 
@@ -42,10 +45,11 @@ using namespace tc;
 
 constexpr int kBM = 128;
 constexpr int kBN = 128;
-constexpr int kBK = 32;                        // fp32 K per K-block: one 128-byte swizzled row
+constexpr int kBK = 32;                        // LoRA K-block: 32 fp32, one 128-byte swizzled row
+constexpr int kBKm = 64;                       // main K-block: 64 bf16, one 128-byte swizzled row
 constexpr int kStages = 3;
 constexpr int kTile = 128 * kBK * 4;           // 128 rows x 128 bytes
-constexpr int kStageBytes = 4 * kTile;         // A, A_lo, B, B_lo
+constexpr int kStageBytes = 4 * kTile;         // A_hi, A_lo, B_hi, B_lo
 constexpr int kEpiWarps = 8;     // two per TMEM lane quarter, 64 columns each
 constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kConvThreads = 64;
@@ -58,9 +62,11 @@ static_assert(kSmemBytes <= 232448, "dynamic shared memory per CTA");
 __device__ __forceinline__ uint64_t kdesc(uint32_t saddr) {
   return kBK == 32 ? smem_desc_sw128(saddr) : smem_desc_sw64(saddr);
 }
-constexpr uint32_t kIdesc = idesc(kFmtTF32, kBM, kBN);            // lo x B_hi into the big half
-constexpr uint32_t kIdesc2 = idesc(kFmtTF32, kBM, 2 * kBN);       // hi x [B_hi; B_lo]
-constexpr int kPeriod = 8;   // K-blocks accumulated in one TMEM region before it is drained
+constexpr uint32_t kIdesc = idesc(kFmtTF32, kBM, kBN);            // LoRA: lo x Q_hi into the big half
+constexpr uint32_t kIdesc2 = idesc(kFmtTF32, kBM, 2 * kBN);       // LoRA: hi x [Q_hi; Q_lo]
+constexpr uint32_t kIdescB = idesc(kFmtBF16, kBM, kBN);           // main: lo x B_hi
+constexpr uint32_t kIdescB2 = idesc(kFmtBF16, kBM, 2 * kBN);      // main: hi x [B_hi; B_lo]
+constexpr int kPeriod = 4;   // main K-blocks (256 elements) accumulated in one TMEM region
 constexpr int kPartLd = kBN + 4;   // row stride (floats) of a split-K partial tile in shared memory
 constexpr int kMaxSplits = 8;      // portable cluster size
 static_assert(kBM * kPartLd * 4 <= kStages * kStageBytes, "partial tile fits the stage buffers");
@@ -79,8 +85,8 @@ __device__ __forceinline__ float4 ld_peer4(const float* local, uint32_t rank) {
 }
 
 struct F32Params {
-  CUtensorMap tah, tal;               // A hi / lo [T, K] fp32, box {32, 128}
-  CUtensorMap tbh, tbl;               // B hi / lo [N, K] fp32, box {32, 128}
+  CUtensorMap tah, tal;               // A hi / lo [T, K] bf16, box {64, 128}
+  CUtensorMap tbh, tbl;               // B hi / lo [N, K] bf16, box {64, 128}
   CUtensorMap tp;                     // P [T, ldp] fp32, box {32, 128}
   CUtensorMap tq[LORA_MAX_SLOTS];     // Q_slot [N, r] fp32, box {32, 128}
   CUtensorMap to;                     // out [T, ldo] fp32, box {32, 32} (the epilogue's stores)
@@ -180,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm_f32(const __grid_consta
         if (kb >= kStages && !mbar_wait(&empty_bar[s], ph ^ 1u, 1u, p.err)) break;
         uint8_t* st = base + s * kStageBytes;
         if (kb < nml) {
-          const int x = (kb_lo + kb) * kBK;
+          const int x = (kb_lo + kb) * kBKm;
           mbar_expect_tx(&full_bar[s], 4 * kTile);
           tma_load_2d(st, &p.tah, &full_bar[s], x, m0);
           tma_load_2d(st + kTile, &p.tal, &full_bar[s], x, m0);
@@ -229,10 +235,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm_f32(const __grid_consta
         fence_after();
         const uint32_t sa = smem_u32(base + s * kStageBytes);
         const uint64_t ah = kdesc(sa), al = kdesc(sa + kTile), bh = kdesc(sa + 2 * kTile);
+        // four 32-byte K-steps per 128-byte row: K 16 of bf16 (main) or K 8 of tf32 (LoRA)
+        if (lora) {
 #pragma unroll
-        for (int k = 0; k < kBK / 8; ++k) {
-          umma_tf32(d, ah + 2 * k, bh + 2 * k, kIdesc2, (start && k == 0) ? 0u : 1u);
-          umma_tf32(d, al + 2 * k, bh + 2 * k, kIdesc, 1u);
+          for (int k = 0; k < 4; ++k) {
+            umma_tf32(d, ah + 2 * k, bh + 2 * k, kIdesc2, (start && k == 0) ? 0u : 1u);
+            umma_tf32(d, al + 2 * k, bh + 2 * k, kIdesc, 1u);
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            umma_f16(d, ah + 2 * k, bh + 2 * k, kIdescB2, (start && k == 0) ? 0u : 1u);
+            umma_f16(d, al + 2 * k, bh + 2 * k, kIdescB, 1u);
+          }
         }
         umma_commit(&empty_bar[s]);
       }
@@ -392,11 +407,12 @@ cudaError_t launch_tc_gemm_f32(const TcGemmArgs& a, cudaStream_t st, int prof_ki
   std::lock_guard<std::mutex> lk(mu);
   std::memset(&prm, 0, sizeof(prm));
   const auto F32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  const auto BF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   if (!a.a_lo || !a.b_lo) return cudaErrorInvalidValue;
-  if (!tc::make_map_2d(&prm.tah, a.a, F32, 4, a.K, a.T, a.K, kBK, kBM) ||
-      !tc::make_map_2d(&prm.tal, a.a_lo, F32, 4, a.K, a.T, a.K, kBK, kBM) ||
-      !tc::make_map_2d(&prm.tbh, a.b, F32, 4, a.K, a.n_rows, a.K, kBK, kBN) ||
-      !tc::make_map_2d(&prm.tbl, a.b_lo, F32, 4, a.K, a.n_rows, a.K, kBK, kBN))
+  if (!tc::make_map_2d(&prm.tah, a.a, BF16, 2, a.K, a.T, a.K, kBKm, kBM) ||
+      !tc::make_map_2d(&prm.tal, a.a_lo, BF16, 2, a.K, a.T, a.K, kBKm, kBM) ||
+      !tc::make_map_2d(&prm.tbh, a.b, BF16, 2, a.K, a.n_rows, a.K, kBKm, kBN) ||
+      !tc::make_map_2d(&prm.tbl, a.b_lo, BF16, 2, a.K, a.n_rows, a.K, kBKm, kBN))
     return cudaErrorInvalidValue;
   prm.has_lora = a.p != nullptr;
   if (a.p) {
@@ -415,7 +431,7 @@ cudaError_t launch_tc_gemm_f32(const TcGemmArgs& a, cudaStream_t st, int prof_ki
     return cudaErrorInvalidValue;
   prm.err = tc::error_word();
   if (!prm.err) return cudaErrorInvalidDevice;
-  prm.nk_main = (int32_t)((a.K + kBK - 1) / kBK);
+  prm.nk_main = (int32_t)((a.K + kBKm - 1) / kBKm);
   // Split the K-blocks over a cluster when the tile grid alone would leave most SMs idle (few
   // output tiles, long K): up to 8 splits, at least 4 K-blocks each, and at most ~80 CTAs in
   // all. (Measured at T 1024, K 2048, N 256: 35 us unsplit, 14 us as 4 splits over 64 CTAs,

@@ -118,6 +118,23 @@ __device__ __forceinline__ float tf32_hi(float x) {
   return __uint_as_float(r);
 }
 
+// bf16 split for the fp32 frozen products: hi = x rounded to bf16 (nearest even) and lo = the
+// remainder x - hi (exact in fp32) rounded to bf16. Each rounding keeps 8 significant bits, so
+// |x - hi - lo| <= 2^-16 |x|, and a product formed on bf16 tensor cores as
+// hi*hi' + hi*lo' + lo*hi' (the dropped lo*lo' is below 2^-16 too) stays within a few 2^-16 of
+// the fp32 product, relative, for every term; over a dot product the errors partly cancel.
+__device__ __forceinline__ void bf16_split4(const float (&x)[4], uint2& hi, uint2& lo) {
+  const __nv_bfloat162 h01 = __floats2bfloat162_rn(x[0], x[1]);
+  const __nv_bfloat162 h23 = __floats2bfloat162_rn(x[2], x[3]);
+  const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
+  const __nv_bfloat162 l01 = __floats2bfloat162_rn(x[0] - f01.x, x[1] - f01.y);
+  const __nv_bfloat162 l23 = __floats2bfloat162_rn(x[2] - f23.x, x[3] - f23.y);
+  hi.x = *reinterpret_cast<const uint32_t*>(&h01);
+  hi.y = *reinterpret_cast<const uint32_t*>(&h23);
+  lo.x = *reinterpret_cast<const uint32_t*>(&l01);
+  lo.y = *reinterpret_cast<const uint32_t*>(&l23);
+}
+
 // A token range handled by one CTA, with the adapter slot of those tokens (-1: none).
 struct TokenItem {
   int32_t t0, t1, slot, pad;

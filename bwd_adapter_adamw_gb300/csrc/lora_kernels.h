@@ -39,11 +39,11 @@ void prof_end(int kind, cudaStream_t st);
 
 // ---- gemm_tc.cu: tcgen05 frozen products (bf16 activations) ----
 struct TcGemmArgs {
-  const void* a;             // [T, K] K-contiguous: bf16, or the tf32-rounded hi part (fp32 kernel)
-  const void* a_lo;          // fp32 kernel: [T, K] remainders a - hi
+  const void* a;             // [T, K] K-contiguous: bf16, or the bf16 hi part (fp32 kernel)
+  const void* a_lo;          // fp32 kernel: [T, K] bf16 remainders bf16(a - hi)
   int64_t T;
-  const void* b;             // [n_rows, K] K-contiguous: bf16, or the hi part (fp32 kernel)
-  const void* b_lo;          // fp32 kernel: [n_rows, K] remainders
+  const void* b;             // [n_rows, K] K-contiguous: bf16, or the bf16 hi part (fp32 kernel)
+  const void* b_lo;          // fp32 kernel: [n_rows, K] bf16 remainders
   int64_t n_rows;
   int64_t K;
   const float* p;            // LoRA term P [T, ldp] fp32 (nullptr: no LoRA term)
@@ -193,8 +193,8 @@ struct RowDotArgs {                 // out[t, j] = alpha_slot * sum_k A'[t, k] S
   const float* t_src;
   float* t_dst;
   int64_t t_rows, t_cols;
-  float* split_hi;                  // fp32, nullable: A' (colscaled, unmasked) rounded to tf32 ...
-  float* split_lo;                  // ... and A' - hi, both [T, K]: the 3xTF32 product's operands
+  uint16_t* split_hi;               // bf16, nullable: A' (colscaled, unmasked) rounded to bf16 ...
+  uint16_t* split_lo;               // ... and bf16(A' - hi), both [T, K]: the split product's operands
 };
 struct ColRedArgs {                 // part[item][n][j] = sum_{t in item} P[t, j] B'[t, n]
   const float* p;                   // [T, ldp] fp32

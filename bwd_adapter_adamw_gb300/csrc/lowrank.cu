@@ -86,9 +86,16 @@ __global__ void k_transpose_w(const T* __restrict__ src, T* __restrict__ dst, in
   }
 }
 
-// fp32 prepared weight: W [rows, cols] -> [W_hi | W_lo | W^T_hi | W^T_lo] (tf32 split, above)
-__global__ void k_prepare_w_f32(const float* __restrict__ src, float* __restrict__ dst, int64_t rows,
-                                int64_t cols) {
+// fp32 prepared weight: W [rows, cols] -> bf16 [W_hi | W_lo | W^T_hi | W^T_lo] (the bf16 split
+// of every element: hi = bf16(x), lo = bf16(x - hi))
+__device__ __forceinline__ void split_one(float x, uint16_t* hi, uint16_t* lo) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(x);
+  *hi = __bfloat16_as_ushort(h);
+  *lo = __bfloat16_as_ushort(__float2bfloat16_rn(x - __bfloat162float(h)));
+}
+
+__global__ void k_prepare_w_f32(const float* __restrict__ src, uint16_t* __restrict__ dst,
+                                int64_t rows, int64_t cols) {
   grid_dep_sync();
   __shared__ float tile[32][33];
   const int64_t n = rows * cols;
@@ -97,21 +104,14 @@ __global__ void k_prepare_w_f32(const float* __restrict__ src, float* __restrict
     const int64_t r = r0 + i, c = c0 + threadIdx.x;
     if (r < rows && c < cols) {
       const float x = src[r * cols + c];
-      const float h = tf32_hi(x);
-      dst[r * cols + c] = h;
-      dst[n + r * cols + c] = x - h;
+      split_one(x, dst + r * cols + c, dst + n + r * cols + c);
       tile[i][threadIdx.x] = x;
     }
   }
   __syncthreads();
   for (int i = threadIdx.y; i < 32; i += 8) {
     const int64_t c = c0 + i, r = r0 + threadIdx.x;
-    if (r < rows && c < cols) {
-      const float x = tile[threadIdx.x][i];
-      const float h = tf32_hi(x);
-      dst[2 * n + c * rows + r] = h;
-      dst[3 * n + c * rows + r] = x - h;
-    }
+    if (r < rows && c < cols) split_one(tile[threadIdx.x][i], dst + 2 * n + c * rows + r, dst + 3 * n + c * rows + r);
   }
 }
 
@@ -276,7 +276,7 @@ cudaError_t launch_prepare_weight(int dtype, const void* W, void* Wt, int64_t ro
                                   cudaStream_t st) {
   dim3 grid((unsigned)((cols + 31) / 32), (unsigned)((rows + 31) / 32));
   if (dtype == LORA_F32)
-    { prof_begin(0, st); launch_kernel(k_prepare_w_f32, grid, dim3(32, 8), 0, st, (const float*)W, (float*)Wt, rows, cols); }
+    { prof_begin(0, st); launch_kernel(k_prepare_w_f32, grid, dim3(32, 8), 0, st, (const float*)W, (uint16_t*)Wt, rows, cols); }
   else
     { prof_begin(0, st); launch_kernel(k_transpose_w<__nv_bfloat16>, grid, dim3(32, 8), 0, st, (const __nv_bfloat16*)W,
                                                                 (__nv_bfloat16*)Wt, rows, cols); }

@@ -5,8 +5,8 @@
 //  k_rowdot:  out[t, j] = alpha_slot * sum_k A'[t, k] S_slot[j, k]   (shrink with S = A,
 //             G with S = B^T); one warp per token, lanes stride over K with 16-byte loads, the
 //             slot's S staged in shared memory one K-chunk at a time, warp-shuffle reduction.
-//             Since it reads every A'[t, k] anyway, it also writes the tf32 hi / lo split of A'
-//             that the 3xTF32 frozen product consumes (X in the forward, dY' in the backward).
+//             Since it reads every A'[t, k] anyway, it also writes the bf16 hi / lo split of A'
+//             that the split fp32 frozen product consumes (X in the forward, dY' in the backward).
 //  k_colred:  part[item][n][j] = sum_{t in item} P[t, j] B'[t, n]   (dB with P = Hs, B' = dY';
 //             dA^T with P = Gs, B' = Xd); every thread owns CPT adjacent columns, the item's P
 //             rows are staged in shared memory, one partial per work item, reduced in order.
@@ -18,7 +18,8 @@ namespace lora {
 
 namespace {
 
-// hi / lo of A'[t, k .. k + 3] for the tokens t = t0 + u < t1 (the 3xTF32 frozen product's operand)
+// bf16 hi / lo of A'[t, k .. k + 3] for the tokens t = t0 + u < t1 (the split frozen product's
+// operands)
 template <int U>
 __device__ __forceinline__ void write_split(const RowDotArgs& a, const float (&x)[U][4], int64_t t0,
                                             int64_t t1, int64_t k) {
@@ -26,11 +27,10 @@ __device__ __forceinline__ void write_split(const RowDotArgs& a, const float (&x
   for (int u = 0; u < U; ++u) {
     if (t0 + u >= t1) continue;
     const int64_t o = (t0 + u) * a.K + k;
-    float4 h, l;
-    h.x = tf32_hi(x[u][0]); h.y = tf32_hi(x[u][1]); h.z = tf32_hi(x[u][2]); h.w = tf32_hi(x[u][3]);
-    l.x = x[u][0] - h.x; l.y = x[u][1] - h.y; l.z = x[u][2] - h.z; l.w = x[u][3] - h.w;
-    *reinterpret_cast<float4*>(a.split_hi + o) = h;
-    *reinterpret_cast<float4*>(a.split_lo + o) = l;
+    uint2 h, l;
+    bf16_split4(x[u], h, l);
+    *reinterpret_cast<uint2*>(a.split_hi + o) = h;
+    *reinterpret_cast<uint2*>(a.split_lo + o) = l;
   }
 }
 

@@ -155,9 +155,9 @@ size_t lora_workspace_size(const lora_desc* d, int64_t T);
  * once and kept resident beside W):
  *   bf16: W^T [in_dim, out_dim] bf16, the K-contiguous operand of the dX product
  *         (2 * in_dim * out_dim bytes);
- *   fp32: the tf32 split of W and of W^T for the 3xTF32 tensor-core products, four fp32 arrays
- *         [W_hi | W_lo | W^T_hi | W^T_lo], each element x stored as x_hi = x rounded to tf32
- *         (nearest, ties away from zero) and x_lo = x - x_hi (16 * in_dim * out_dim bytes);
+ *   fp32: the bf16 split of W and of W^T for the split tensor-core products, four bf16 arrays
+ *         [W_hi | W_lo | W^T_hi | W^T_lo], each element x stored as x_hi = x rounded to bf16
+ *         (nearest even) and x_lo = (x - x_hi) rounded to bf16 (8 * in_dim * out_dim bytes);
  *   bf16 with the E4M3 frozen product: [W8 (out x in codes) | sw (out fp32 row scales) |
  *         WT8 (in x out codes of W's columns) | swT (in fp32)], each section starting on a
  *         16-byte boundary (about 2 * in_dim * out_dim bytes).

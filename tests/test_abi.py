@@ -92,7 +92,7 @@ def test_forward_argument_errors(L):
 
 
 def test_prepared_weight_size(L):
-    assert L.lora_prepared_weight_size(L.make_desc(2048, 256, 8, 2.0, L.LORA_F32)) == 16 * 2048 * 256
+    assert L.lora_prepared_weight_size(L.make_desc(2048, 256, 8, 2.0, L.LORA_F32)) == 8 * 2048 * 256
     assert L.lora_prepared_weight_size(L.make_desc(1536, 4096, 16, 2.0, L.LORA_BF16)) == 2 * 1536 * 4096
     assert L.lora_prepared_weight_size(L.make_desc(1536, 4096, 0, 2.0, L.LORA_BF16)) == 0
 
