@@ -88,12 +88,14 @@ def counts(cfg: LI.LoraConfig, layers: int):
                 opt_bytes=32 * params, act_bytes=a)
 
 
-def memory_counts(cfg: LI.LoraConfig, layers: int):
+def memory_counts(cfg: LI.LoraConfig, layers: int, groups=None):
     """Algorithmic HBM bytes per step of the memory-bound kernel classes (each array the class
     must touch, once): shrink reads X and A and writes Hs (and, on the fp32 path, the bf16 split
     of X); G reads dY' and B and writes Gs (and the split of dY'); the dB / dA reductions read dY'
     or X and Hs or Gs and update dB / dA; grad-prepare reads 4 B and AdamW moves 32 B per
-    parameter (p, g, m, v read; p, m, v written; g cleared)."""
+    parameter (p, g, m, v read; p, m, v written; g cleared). With `groups` (fused projections:
+    lists of projection indices that read one input), a group's input and output gradient are
+    counted once, with the group's adapters side by side."""
     T = cfg.tokens
     a = 4 if cfg.dtype == "f32" else 2
     split = 4 if cfg.dtype == "f32" else 0   # bf16 hi + lo per element
@@ -104,12 +106,14 @@ def memory_counts(cfg: LI.LoraConfig, layers: int):
     else:
         r_all = r_row = cfg.rank
     out = {"shrink": 0, "G": 0, "redB": 0, "redA": 0}
-    for p in cfg.projs:
-        i, o = p.in_dim, p.out_dim
-        out["shrink"] += T * i * a + r_all * i * 4 + T * r_row * 4 + split * T * i
-        out["G"] += T * o * a + r_all * o * 4 + T * r_row * 4 + split * T * o
-        out["redB"] += T * o * a + T * r_row * 4 + 2 * r_all * o * 4
-        out["redA"] += T * i * a + T * r_row * 4 + 2 * r_all * i * 4
+    for idx in (groups or [[k] for k in range(len(cfg.projs))]):
+        i = cfg.projs[idx[0]].in_dim
+        o = sum(cfg.projs[k].out_dim for k in idx)
+        n = len(idx)   # adapters of the group: n r columns of Hs / G, n A's of [r, in]
+        out["shrink"] += T * i * a + n * r_all * i * 4 + T * n * r_row * 4 + split * T * i
+        out["G"] += T * o * a + r_all * o * 4 + T * n * r_row * 4 + split * T * o
+        out["redB"] += T * o * a + T * n * r_row * 4 + 2 * r_all * o * 4
+        out["redA"] += T * i * a + T * n * r_row * 4 + 2 * n * r_all * i * 4
     out = {k: v * layers for k, v in out.items()}
     r_step = r_all
     if cfg.multi:   # only the slots whose adapter batch is full take a step
@@ -127,10 +131,10 @@ def memory_counts(cfg: LI.LoraConfig, layers: int):
 # value. Captured with `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum` on
 # `python bench.py --layers 1 --steps 2 --warmup 3 --no-cpu-baseline --streams 1`.
 NCU_TRAFFIC = {
-    ("c2", 1): {"source": "gemm_tc_f32.cu", "sha256_16": "deb64ff3168e75dd",
-                "bytes": (50.48e6 + 21.06e6) / 2,
-                "note": "wq fwd 50.48 MB, wv fwd (4-way split K) 21.06 MB read, ~0 written "
-                        "(outputs stay in L2)"},
+    ("c2", 1): {"source": "gemm_tc_f32.cu", "sha256_16": "0cfe552134b8e004",
+                "bytes": (25.32e6 + 10.58e6) / 2,
+                "note": "wq fwd 25.32 MB, wv fwd (4-way split K) 10.58 MB read (the bf16 hi / lo "
+                        "splits of X and W, once), ~0 written (outputs stay in L2)"},
 }
 
 
@@ -207,6 +211,26 @@ class Clocks:
 
 
 # --------------------------------------------------------------------------------- workload
+def pack_inputs(inputs, device):
+    """Rebind every input tensor (same values) to a view of one flat device buffer, so that a
+    step's whole input batch moves host -> device in one copy. Drops repeated tensors from
+    `inputs` (in place) and returns the flat buffer."""
+    import torch
+    uniq = {id(t): t for t in inputs}
+    inputs[:] = list(uniq.values())
+    offs, total = [], 0
+    for t in inputs:
+        offs.append(total)
+        total += (t.numel() * t.element_size() + 255) // 256 * 256
+    flat = torch.empty(total, dtype=torch.uint8, device=device)
+    for t, o in zip(inputs, offs):
+        nb = t.numel() * t.element_size()
+        v = flat[o:o + nb].view(t.dtype).view(t.shape)
+        v.copy_(t)
+        t.set_(v.untyped_storage(), v.storage_offset(), v.shape, v.stride())
+    return flat
+
+
 def _scale(cfg, L):
     return L.lora_scale(cfg.alpha, cfg.rank, cfg.rslora)
 
@@ -301,8 +325,9 @@ def make_fused(cfg, layers, streams, device):
     import torch
     from bwd_adapter_adamw_gb300 import binding as L
     from bwd_adapter_adamw_gb300.step import FusedGroup, FusedLoraStep
-    if cfg.multi or cfg.dora or cfg.dtype != "bf16":
-        raise SystemExit(f"--fused needs a single-adapter bf16 config without DoRA ({cfg.name})")
+    if cfg.multi or cfg.dora or cfg.dtype not in ("bf16", "f32"):
+        raise SystemExit(f"--fused needs a single-adapter bf16 or fp32 config without DoRA "
+                         f"({cfg.name})")
     groups, xs = [], []
     for l in range(layers):
         for idx in fused_groups(cfg):
@@ -498,6 +523,7 @@ def run_ours(args):
         step, run, inputs, results = make_multi(cfg, args.streams, device)
     else:
         step, run, inputs, results = make_single(cfg, layers, args.streams, device)
+    flat_in = pack_inputs(inputs, device)
     torch.cuda.synchronize()
 
     # launches per step (eager), then warm-up
@@ -561,15 +587,19 @@ def run_ours(args):
     per_step = [(ev0 if i == 0 else step_ev[i - 1]).elapsed_time(step_ev[i]) for i in range(K)]
     # dominant-kernel durations from the last replay
     kern_ms = [a.elapsed_time(b) for a, b in zip(starts[:used], stops[:used])] if used else []
-    # end-to-end through host buffers: H2D of the step's inputs, the step, D2H of the result
-    pinned = [t.detach().to("cpu").pin_memory() for t in inputs]
+    # end-to-end through host buffers: H2D of the step's inputs, the step, D2H of the result.
+    # The inputs live in one flat device buffer (pack_inputs), so the batch is one pinned host
+    # buffer and one copy (one large copy runs near the host link's rate; 88 separate 1-8 MB
+    # copies measured about 15% slower).
+    pinned = torch.empty(flat_in.numel(), dtype=torch.uint8, pin_memory=True)
+    pinned.copy_(flat_in)
     res_host = [torch.empty(r.shape, dtype=r.dtype, pin_memory=True) for r in results]
-    h2d = sum(t.numel() * t.element_size() for t in pinned)
+    h2d = sum(t.numel() * t.element_size() for t in inputs)
     d2h = sum(t.numel() * t.element_size() for t in res_host)
     # As a training loop would, the next step's batch is copied host -> device on a second stream
     # while the current step runs (into a staging copy, moved into place at the step's start);
     # every step still copies its whole input from pinned host memory and reads its result back.
-    staging = [torch.empty_like(t) for t in inputs]
+    staging = torch.empty_like(flat_in)
     copy_stream = torch.cuda.Stream(device=device)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     Ke = max(3, K // 2)
@@ -583,8 +613,7 @@ def run_ours(args):
         else:
             copy_stream.wait_event(after)   # the staging copy has been moved into place
         with torch.cuda.stream(copy_stream):
-            for st_, src in zip(staging, pinned):
-                st_.copy_(src, non_blocking=True)
+            staging.copy_(pinned, non_blocking=True)
         done = torch.cuda.Event()
         done.record(copy_stream)
         return done
@@ -592,8 +621,7 @@ def run_ours(args):
     h2d_done = h2d_into_staging()
     for k in range(Ke):
         stream.wait_event(h2d_done)
-        for dst, st_ in zip(inputs, staging):
-            dst.copy_(st_, non_blocking=True)
+        flat_in.copy_(staging, non_blocking=True)
         moved = torch.cuda.Event()
         moved.record(stream)
         if k + 1 < Ke:
@@ -676,7 +704,8 @@ def run_ours(args):
             note = f"dense bf16 cuBLAS burst, {peak_src}"
         achieved = per_launch / (avg_kern / 1e3) / 1e12 if avg_kern else None
         avg_serial = statistics.mean(kern_serial) if kern_serial else None
-        mem = memory_counts(cfg, layers if not cfg.multi else 1)
+        mem = memory_counts(cfg, layers if not cfg.multi else 1,
+                            fused_groups(cfg) if args.fused else None)
         memory_bound = {}
         for name, ts in mem_times.items():
             if ts:

@@ -100,8 +100,8 @@ def _load() -> C.CDLL:
         "lora_retire": (C.c_int, [P, P, P, P, I32, C.POINTER(lora_group), I32, P]),
         "multi_lora_workspace_size": (SZ, [DP, I64, I32, I32, C.POINTER(lora_slot)]),
         "lora_fused_workspace_size": (SZ, [DP, I64, I32, C.POINTER(lora_proj)]),
-        "lora_fused_forward": (C.c_int, [DP, CP, I64, P, P, I32, C.POINTER(lora_proj), P, P, P,
-                                         SZ, P]),
+        "lora_fused_forward": (C.c_int, [DP, CP, I64, P, P, P, I32, C.POINTER(lora_proj), P, P,
+                                         P, SZ, P]),
         "lora_fused_backward": (C.c_int, [DP, CP, I64, P, P, I32, C.POINTER(lora_proj), P, P, P,
                                           P, SZ, P]),
         "multi_lora_forward": (C.c_int, [DP, CP, I64, P, P, P, I32, P, P, I32,
@@ -337,12 +337,12 @@ def lora_fused_workspace_size(d: lora_desc, T: int, projs) -> int:
     return _lib.lora_fused_workspace_size(C.byref(d), T, len(projs), projs)
 
 
-def lora_fused_forward(d, c, T, X, W, projs, Y, H_save, ws, ws_bytes=None, stream=None,
+def lora_fused_forward(d, c, T, X, W, W_prep, projs, Y, H_save, ws, ws_bytes=None, stream=None,
                        check=True):
     nbytes = ws_bytes if ws_bytes is not None else ws.numel() * ws.element_size()
     st = _lib.lora_fused_forward(C.byref(d), C.byref(c) if c is not None else None, T, _ptr(X),
-                                 _ptr(W), len(projs), projs, _ptr(Y), _ptr(H_save), _ptr(ws),
-                                 nbytes, _stream(stream))
+                                 _ptr(W), _ptr(W_prep), len(projs), projs, _ptr(Y), _ptr(H_save),
+                                 _ptr(ws), nbytes, _stream(stream))
     return _check(st, "lora_fused_forward") if check else st
 
 

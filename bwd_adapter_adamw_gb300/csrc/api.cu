@@ -856,13 +856,16 @@ struct FusedProjs {
 int fused_from_table(const lora_desc* d, int32_t n_proj, const lora_proj* tab, bool need_grads,
                      FusedProjs& f) {
   if (!tab || n_proj < 1 || n_proj > LORA_MAX_SLOTS) return LORA_ERR_INVALID;
-  if (d->dtype != LORA_BF16 || d->dora) return LORA_ERR_UNSUPPORTED;
+  if ((d->dtype != LORA_BF16 && d->dtype != LORA_F32) || d->dora) return LORA_ERR_UNSUPPORTED;
+  // fp32: the group runs as one adapter of rank n_proj * rank
+  if (d->dtype == LORA_F32 && (int64_t)n_proj * d->rank > LORA_MAX_RANK) return LORA_ERR_UNSUPPORTED;
   int64_t sum = 0;
   for (int k = 0; k < n_proj; ++k) {
     const lora_proj& e = tab[k];
     if (!e.A || !e.B || e.out_dim <= 0) return LORA_ERR_INVALID;
     if (need_grads && (!e.dA || !e.dB)) return LORA_ERR_INVALID;
-    if (e.out_dim % 256) return LORA_ERR_UNSUPPORTED;   // column groups start on 256-wide tiles
+    // bf16: column groups start on 256-wide tiles
+    if (d->dtype == LORA_BF16 && e.out_dim % 256) return LORA_ERR_UNSUPPORTED;
     if (!al16(e.A) || !al16(e.B) || (need_grads && (!al16(e.dA) || !al16(e.dB))))
       return LORA_ERR_ALIGN;
     f.A[k] = e.A;
@@ -908,6 +911,92 @@ SlotInfo fused_slot_info(const lora_desc* d) {
   one.rank[0] = d->rank;
   one.scale[0] = d->scale;
   return slot_info(one, dropout_q(d));
+}
+
+// fp32 fused projections: the group runs as one single-adapter linear of rank n r whose adapter
+// is A_cat = [A_0; ...; A_{n-1}] and the block-diagonal B_cat (CatTab). Then
+// Y = X W_cat^T + s' (Xd A_cat^T) B_cat^T is every projection's forward at once, with
+// Hs_cat = s' Xd A_cat^T holding Hs_k in columns k r ..; G_cat = s' dY' B_cat holds G_k in its
+// columns k r .., so that the dX product's LoRA term is sum_k G_k A_k and dA_cat = G_cat^T Xd
+// holds dA_k in its rows k r ..; dB_cat = dY'^T Hs_cat holds dB_k in its diagonal blocks. The
+// shrink reads X once and the G pass dY once for the whole group, and the frozen products run
+// once over the stacked weight.
+struct FusedF32Layout {
+  float* Acat;    // [n r, in]
+  float* Bcat;    // [sum out_k, n r]
+  float* dAcat;   // [n r, in]
+  float* dBcat;   // [sum out_k, n r]
+  void* inner;    // workspace of the rank-n r linear
+  size_t bytes;
+};
+
+lora_desc cat_desc(const lora_desc* d, const FusedProjs& f) {
+  lora_desc c = *d;
+  c.rank = f.n * d->rank;
+  return c;
+}
+
+FusedF32Layout fused_f32_carve(const lora_desc* d, int64_t T, const FusedProjs& f, void* ws) {
+  const lora_desc cd = cat_desc(d, f);
+  const size_t nr = (size_t)cd.rank;
+  FusedF32Layout F;
+  Carve c(ws);
+  F.Acat = c.take<float>(nr * d->in_dim);
+  F.Bcat = c.take<float>((size_t)d->out_dim * nr);
+  F.dAcat = c.take<float>(nr * d->in_dim);
+  F.dBcat = c.take<float>((size_t)d->out_dim * nr);
+  F.inner = c.take<uint8_t>(ws_size(&cd, T, -1, 1, cd.rank));
+  F.bytes = c.off + kWsAlign;
+  return F;
+}
+
+size_t fused_ws_bytes(const lora_desc* d, int64_t T, const FusedProjs& f) {
+  return d->dtype == LORA_F32 ? fused_f32_carve(d, T, f, nullptr).bytes
+                              : fused_carve(d, T, f, nullptr).bytes;
+}
+
+CatTab cat_tab(const lora_desc* d, const FusedProjs& f) {
+  CatTab t{};
+  t.n = f.n;
+  t.r = d->rank;
+  t.in = d->in_dim;
+  for (int k = 0; k < f.n; ++k) {
+    t.A[k] = f.A[k];
+    t.B[k] = f.B[k];
+    t.dA[k] = f.dA[k];
+    t.dB[k] = f.dB[k];
+    t.off[k] = f.off[k];
+  }
+  t.off[f.n] = d->out_dim;
+  return t;
+}
+
+int run_fused_forward_f32(const lora_desc* d, const DropParams& dp, int64_t T, const void* X,
+                          const void* W, const void* Wprep, const FusedProjs& f, void* Y, float* H,
+                          void* ws, cudaStream_t st) {
+  const FusedF32Layout F = fused_f32_carve(d, T, f, ws);
+  const lora_desc cd = cat_desc(d, f);
+  LORA_TRY(launch_pack_cat(cat_tab(d, f), F.Acat, F.Bcat, nullptr, nullptr, st));
+  Slots s;
+  single_slot(&cd, F.Acat, F.Bcat, nullptr, nullptr, s);
+  return run_forward(&cd, dp, T, X, W, Wprep, -1, nullptr, nullptr, s, nullptr, nullptr, Y, H,
+                     F.inner, st);
+}
+
+int run_fused_backward_f32(const lora_desc* d, const DropParams& dp, int64_t T, const void* X,
+                           const void* Wt, const FusedProjs& f, const void* dY, const float* H,
+                           void* dX, void* ws, cudaStream_t st) {
+  const FusedF32Layout F = fused_f32_carve(d, T, f, ws);
+  const lora_desc cd = cat_desc(d, f);
+  const CatTab tab = cat_tab(d, f);
+  LORA_TRY(launch_pack_cat(tab, F.Acat, F.Bcat, F.dAcat, F.dBcat, st));
+  Slots s;
+  single_slot(&cd, F.Acat, F.Bcat, F.dAcat, F.dBcat, s);
+  const int rc = run_backward(&cd, dp, T, X, Wt, -1, nullptr, nullptr, s, dY, H, nullptr, nullptr,
+                              nullptr, dX, nullptr, F.inner, st);
+  if (rc) return rc;
+  LORA_TRY(launch_add_cat_grads(tab, F.dAcat, F.dBcat, st));
+  return LORA_OK;
 }
 
 int run_fused_forward(const lora_desc* d, const DropParams& dp, int64_t T, const void* X,
@@ -1392,22 +1481,25 @@ size_t lora_fused_workspace_size(const lora_desc* d, int64_t T, int32_t n_proj,
   if (check_desc(d, T, false) != LORA_OK) return 0;
   FusedProjs f;
   if (fused_from_table(d, n_proj, projs, false, f) != LORA_OK) return 0;
-  return fused_carve(d, T, f, nullptr).bytes;
+  return fused_ws_bytes(d, T, f);
 }
 
 int lora_fused_forward(const lora_desc* d, const lora_ctx* c, int64_t T, const void* X,
-                       const void* W, int32_t n_proj, const lora_proj* projs, void* Y,
-                       float* H_save, void* ws, size_t ws_bytes, void* stream) {
+                       const void* W, const void* W_prep, int32_t n_proj, const lora_proj* projs,
+                       void* Y, float* H_save, void* ws, size_t ws_bytes, void* stream) {
   int rc = check_desc(d, T, false);
   if (rc) return rc;
   FusedProjs f;
   if ((rc = fused_from_table(d, n_proj, projs, false, f))) return rc;
   DropParams dp;
   if ((rc = build_drop(d, c, T, dp))) return rc;
-  if (!X || !W || !Y || !H_save || !ws) return LORA_ERR_INVALID;
-  if (!al16(X) || !al16(W) || !al16(Y) || !al16(H_save) || !al16(ws)) return LORA_ERR_ALIGN;
-  if (ws_bytes < fused_carve(d, T, f, nullptr).bytes) return LORA_ERR_WORKSPACE;
+  if (!X || !W || !W_prep || !Y || !H_save || !ws) return LORA_ERR_INVALID;
+  if (!al16(X) || !al16(W) || !al16(W_prep) || !al16(Y) || !al16(H_save) || !al16(ws))
+    return LORA_ERR_ALIGN;
+  if (ws_bytes < fused_ws_bytes(d, T, f)) return LORA_ERR_WORKSPACE;
   if (T == 0) return LORA_OK;
+  if (d->dtype == LORA_F32)
+    return run_fused_forward_f32(d, dp, T, X, W, W_prep, f, Y, H_save, ws, (cudaStream_t)stream);
   return run_fused_forward(d, dp, T, X, W, f, Y, H_save, ws, (cudaStream_t)stream);
 }
 
@@ -1425,8 +1517,10 @@ int lora_fused_backward(const lora_desc* d, const lora_ctx* c, int64_t T, const 
   if (!al16(X) || !al16(W_prep) || !al16(dY) || !al16(H_save) || !al16(ws) ||
       (dX && !al16(dX)))
     return LORA_ERR_ALIGN;
-  if (ws_bytes < fused_carve(d, T, f, nullptr).bytes) return LORA_ERR_WORKSPACE;
+  if (ws_bytes < fused_ws_bytes(d, T, f)) return LORA_ERR_WORKSPACE;
   if (T == 0) return LORA_OK;
+  if (d->dtype == LORA_F32)
+    return run_fused_backward_f32(d, dp, T, X, W_prep, f, dY, H_save, dX, ws, (cudaStream_t)stream);
   return run_fused_backward(d, dp, T, X, W_prep, f, dY, H_save, dX, ws, (cudaStream_t)stream);
 }
 

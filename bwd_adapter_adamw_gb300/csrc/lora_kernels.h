@@ -247,7 +247,26 @@ struct TransposeTab {
 };
 cudaError_t launch_transpose_slots(const TransposeTab& t, int n, int64_t max_rows, int64_t max_cols,
                                    cudaStream_t st);
-// prepared copy of a frozen W [rows, cols]: bf16 W^T, or fp32 [W_hi | W_lo | W^T_hi | W^T_lo]
+// fp32 fused projections as one adapter of rank n r: A_cat = [A_0; ...; A_{n-1}] ([n r, in]) and
+// the block-diagonal B_cat ([off[n], n r]: B_k in rows off[k].., columns k r..; zeros elsewhere)
+struct CatTab {
+  const float* A[LORA_MAX_SLOTS];
+  const float* B[LORA_MAX_SLOTS];
+  float* dA[LORA_MAX_SLOTS];
+  float* dB[LORA_MAX_SLOTS];
+  int64_t off[LORA_MAX_SLOTS + 1];   // projection k's first output row; off[n] = sum out_k
+  int32_t n, r;
+  int64_t in;
+};
+// (dA_cat and dB_cat, when given, are cleared in the same launch)
+cudaError_t launch_pack_cat(const CatTab& t, float* Acat, float* Bcat, float* dAcat, float* dBcat,
+                            cudaStream_t st);
+// dA_k += rows k r .. of dA_cat; dB_k += the diagonal block k of dB_cat (the off-diagonal blocks
+// are cross terms of one projection's dY with another's Hs, not gradients)
+cudaError_t launch_add_cat_grads(const CatTab& t, const float* dAcat, const float* dBcat,
+                                 cudaStream_t st);
+
+// prepared copy of a frozen W [rows, cols]: bf16 W^T, or fp32 bf16-split [W_hi | W_lo | W^T_hi | W^T_lo]
 cudaError_t launch_prepare_weight(int dtype, const void* W, void* Wt, int64_t rows, int64_t cols,
                                   cudaStream_t st);
 

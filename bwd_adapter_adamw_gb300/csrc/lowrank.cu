@@ -1,4 +1,6 @@
 // Token work items, adapter transposes, ordered split reductions and the test hooks.
+#include <algorithm>
+
 #include "lora_kernels.h"
 
 namespace lora {
@@ -112,6 +114,54 @@ __global__ void k_prepare_w_f32(const float* __restrict__ src, uint16_t* __restr
   for (int i = threadIdx.y; i < 32; i += 8) {
     const int64_t c = c0 + i, r = r0 + threadIdx.x;
     if (r < rows && c < cols) split_one(tile[threadIdx.x][i], dst + 2 * n + c * rows + r, dst + 3 * n + c * rows + r);
+  }
+}
+
+// A_cat and the block-diagonal B_cat of an fp32 fused group (CatTab), one element per thread;
+// with `zero`, the gradient scratch dA_cat, dB_cat (same sizes, after them) is cleared too
+__global__ void k_pack_cat(const CatTab t, float* __restrict__ Acat, float* __restrict__ Bcat,
+                           float* __restrict__ dAcat, float* __restrict__ dBcat, int zero) {
+  grid_dep_sync();
+  const int64_t nr = (int64_t)t.n * t.r;
+  const int64_t na = nr * t.in, nb = t.off[t.n] * nr;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int64_t total = zero ? 2 * (na + nb) : na + nb;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += stride) {
+    if (e >= na + nb) {
+      const int64_t z = e - (na + nb);
+      if (z < na) dAcat[z] = 0.f;
+      else dBcat[z - na] = 0.f;
+    } else if (e < na) {
+      const int64_t row = e / t.in, i = e - row * t.in;
+      const int k = (int)(row / t.r);
+      Acat[e] = t.A[k][(row - (int64_t)k * t.r) * t.in + i];
+    } else {
+      const int64_t f = e - na, o = f / nr, c = f - o * nr;
+      int k = 0;
+      while (k + 1 < t.n && o >= t.off[k + 1]) ++k;
+      const int kc = (int)(c / t.r);
+      Bcat[f] = kc == k ? t.B[k][(o - t.off[k]) * t.r + (c - (int64_t)kc * t.r)] : 0.f;
+    }
+  }
+}
+
+__global__ void k_add_cat_grads(const CatTab t, const float* __restrict__ dAcat,
+                                const float* __restrict__ dBcat) {
+  grid_dep_sync();
+  const int64_t nr = (int64_t)t.n * t.r;
+  const int64_t na = nr * t.in, nb = t.off[t.n] * t.r;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < na + nb; e += stride) {
+    if (e < na) {
+      const int64_t row = e / t.in, i = e - row * t.in;
+      const int k = (int)(row / t.r);
+      t.dA[k][(row - (int64_t)k * t.r) * t.in + i] += dAcat[e];
+    } else {
+      const int64_t f = e - na, o = f / t.r, j = f - o * t.r;
+      int k = 0;
+      while (k + 1 < t.n && o >= t.off[k + 1]) ++k;
+      t.dB[k][(o - t.off[k]) * t.r + j] += dBcat[o * nr + (int64_t)k * t.r + j];
+    }
   }
 }
 
@@ -269,6 +319,29 @@ cudaError_t launch_transpose_slots(const TransposeTab& t, int n, int64_t max_row
   if (n <= 0) return cudaSuccess;
   dim3 grid((unsigned)((max_cols + 31) / 32), (unsigned)((max_rows + 31) / 32), (unsigned)n);
   { prof_begin(0, st); launch_kernel(k_transpose_slots, grid, dim3(32, 8), 0, st, t); }
+  return cudaGetLastError();
+}
+
+static unsigned elementwise_blocks(int64_t n) {
+  return (unsigned)std::max<int64_t>(1, std::min<int64_t>((n + 255) / 256, 152 * 8));
+}
+
+cudaError_t launch_pack_cat(const CatTab& t, float* Acat, float* Bcat, float* dAcat, float* dBcat,
+                            cudaStream_t st) {
+  const int64_t nr = (int64_t)t.n * t.r;
+  const int zero = dAcat != nullptr && dBcat != nullptr;
+  const int64_t n = (nr * t.in + t.off[t.n] * nr) * (zero ? 2 : 1);
+  prof_begin(0, st);
+  launch_kernel(k_pack_cat, elementwise_blocks(n), 256, 0, st, t, Acat, Bcat, dAcat, dBcat, zero);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_add_cat_grads(const CatTab& t, const float* dAcat, const float* dBcat,
+                                 cudaStream_t st) {
+  const int64_t nr = (int64_t)t.n * t.r;
+  prof_begin(0, st);
+  launch_kernel(k_add_cat_grads, elementwise_blocks(nr * t.in + t.off[t.n] * t.r), 256, 0, st, t,
+                dAcat, dBcat);
   return cudaGetLastError();
 }
 

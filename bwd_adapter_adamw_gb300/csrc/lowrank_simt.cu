@@ -477,9 +477,11 @@ __device__ __forceinline__ void rowdot_load(const RowDotArgs& a, const float* S,
 }
 
 // out[t, j] = alpha * sum_k A'[t, k] S[j, k] for TOK tokens per CTA over the whole K (256 threads
-// x 4 columns per pass, per-thread sums kept across passes), then one warp / CTA reduction.
+// x 4 columns per pass, per-thread sums kept across passes), then one warp / CTA reduction. Two
+// CTAs per SM (at most 128 registers): with TOK tokens per CTA the grid is several CTAs per SM,
+// and one resident CTA would leave each SM waiting on a single CTA's load latency.
 template <typename TA, int R, int TOK>
-__global__ void __launch_bounds__(256) k_rowdot_full(const RowDotArgs a) {
+__global__ void __launch_bounds__(256, 2) k_rowdot_full(const RowDotArgs a) {
   grid_dep_sync();
   constexpr int V = TOK * R;
   static_assert(V % 32 == 0, "per-thread values must fill the warp reduction");

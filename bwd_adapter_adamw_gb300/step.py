@@ -333,7 +333,7 @@ class FusedLoraStep:
             ws = self.ws[i % k]
             d, pj = self.desc(g), self.projs(g)
             ctx = L.make_ctx(opt_step, 0, ct)
-            L.lora_fused_forward(d, ctx, self.T, g.X, g.W, pj, g.Y, g.H, ws, stream=st)
+            L.lora_fused_forward(d, ctx, self.T, g.X, g.W, g.Wp, pj, g.Y, g.H, ws, stream=st)
             L.lora_fused_backward(d, ctx, self.T, g.X, g.Wp, pj, g.dY, g.H, g.dX, ws, stream=st)
         _join(main, use)
 

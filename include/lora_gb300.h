@@ -254,11 +254,14 @@ int lora_adamw_step(float* params, float* grads, float* m, float* v, int32_t n_g
  * --lora-type: fused projections, and canonical adapters per q/k/v and gate/up projection):
  *   Y_k = X W_k^T + s' (Xd A_k^T) B_k^T,   dX = sum_k (dY_k W_k + s' (G_k A_k) * M),
  *   dA_k += s' G_k^T Xd,  dB_k += s' dY_k^T (Xd A_k^T),  G_k = dY_k B_k.
- * desc: in_dim, out_dim = sum out_k, the shared rank and scale, dtype LORA_BF16, no DoRA; one
- * dropout mask (desc.layer_id / proj_id) for all the projections. Every out_k is a multiple of
- * 256 (LORA_ERR_UNSUPPORTED otherwise); 1 <= n_proj <= LORA_MAX_SLOTS. W_prep is
- * lora_prepare_weight of W_cat (desc above). H_save [T, n_proj * rank] fp32 holds
- * Hs_k = s' Xd A_k^T in columns k rank .. k rank + rank - 1. dX may be NULL. */
+ * desc: in_dim, out_dim = sum out_k, the shared rank and scale, dtype LORA_BF16 or LORA_F32, no
+ * DoRA; one dropout mask (desc.layer_id / proj_id) for all the projections;
+ * 1 <= n_proj <= LORA_MAX_SLOTS. LORA_BF16: every out_k is a multiple of 256. LORA_F32:
+ * n_proj * rank <= LORA_MAX_RANK (the group runs as one adapter of that rank whose up-projection
+ * is block-diagonal). LORA_ERR_UNSUPPORTED otherwise. W_prep is lora_prepare_weight of W_cat
+ * (desc above); the forward reads W (bf16) or W_prep (fp32), as lora_forward does.
+ * H_save [T, n_proj * rank] fp32 holds Hs_k = s' Xd A_k^T in columns k rank .. k rank + rank - 1.
+ * dX may be NULL. */
 typedef struct lora_proj {
   const float* A;   /* [rank, in_dim] */
   const float* B;   /* [out_dim, rank] */
@@ -269,8 +272,8 @@ typedef struct lora_proj {
 size_t lora_fused_workspace_size(const lora_desc* d, int64_t T, int32_t n_proj,
                                  const lora_proj* projs);
 int lora_fused_forward(const lora_desc* d, const lora_ctx* c, int64_t T, const void* X,
-                       const void* W, int32_t n_proj, const lora_proj* projs, void* Y,
-                       float* H_save, void* ws, size_t ws_bytes, void* stream);
+                       const void* W, const void* W_prep, int32_t n_proj, const lora_proj* projs,
+                       void* Y, float* H_save, void* ws, size_t ws_bytes, void* stream);
 int lora_fused_backward(const lora_desc* d, const lora_ctx* c, int64_t T, const void* X,
                         const void* W_prep, int32_t n_proj, const lora_proj* projs,
                         const void* dY, const float* H_save, void* dX, void* ws, size_t ws_bytes,

@@ -91,6 +91,21 @@ def test_forward_argument_errors(L):
     assert st == L.LORA_ERR_INVALID
 
 
+def test_fused_workspace_dtypes(L):
+    """Fused projections: bf16 needs 256-wide projections; fp32 runs the group as one adapter of
+    rank n_proj * rank, at most 64 (host-side checks only, no launch)."""
+    import torch
+    A = torch.zeros(8, 256)
+    B1, B2 = torch.zeros(384, 8), torch.zeros(128, 8)
+    projs = L.make_projs([dict(A=A, B=B1, out=384), dict(A=A, B=B2, out=128)])
+    assert L.lora_fused_workspace_size(L.make_desc(256, 512, 8, 1.0, L.LORA_F32), 64, projs) > 0
+    assert L.lora_fused_workspace_size(L.make_desc(256, 512, 8, 1.0, L.LORA_BF16), 64, projs) == 0
+    A40 = torch.zeros(40, 256)
+    B40 = torch.zeros(384, 40)
+    projs = L.make_projs([dict(A=A40, B=B40, out=384), dict(A=A40, B=B40, out=128)])
+    assert L.lora_fused_workspace_size(L.make_desc(256, 512, 40, 1.0, L.LORA_F32), 64, projs) == 0
+
+
 def test_prepared_weight_size(L):
     assert L.lora_prepared_weight_size(L.make_desc(2048, 256, 8, 2.0, L.LORA_F32)) == 8 * 2048 * 256
     assert L.lora_prepared_weight_size(L.make_desc(1536, 4096, 16, 2.0, L.LORA_BF16)) == 2 * 1536 * 4096
