@@ -52,6 +52,11 @@ constexpr int kBM = 128;
 constexpr int kABytes = kBM * 128;   // 16 KB: 128 rows x 128 bytes
 constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
+// Epilogue store boxes: each epilogue warp stages 32 rows x 32 bf16 columns (64-byte rows,
+// 64-byte swizzle) and writes them with one bulk tensor store, alternating between two boxes so
+// that one store can still be reading while the next box fills.
+constexpr int kEpiBox = 32 * 64;
+constexpr int kEpiBytes = 4 * 2 * kEpiBox;
 // Items per tile group (rasterization for L2 reuse): 16 when W spans more than 16 N tiles; with
 // fewer, the N tile runs fastest (group of 1), so that the CTAs of one wave read all of W
 // together. Measured at T 8192 (us): N 4096 / K 4096: 152 (N fastest), 152 (8), 162 (16);
@@ -68,9 +73,11 @@ struct GemmCfg {
   static_assert(BN % 32 == 0 && BN >= 128 && BN <= 256, "tile width");
   static constexpr int kBBytes = BN * 128;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  // as many stages as fit 225 KB of shared memory (4 at BN 256, 5 at 224 and 192)
-  static constexpr int kStages = (225 * 1024 / kStageBytes) < 6 ? (225 * 1024 / kStageBytes) : 6;
-  static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*barriers*/ + 1024 /*alignment*/;
+  // as many stages as fit beside the epilogue's store boxes (4 at BN 256 and 224, 5 at 192)
+  static constexpr int kStageRoom = 227 * 1024 - kEpiBytes - 2048;
+  static constexpr int kStages = (kStageRoom / kStageBytes) < 6 ? (kStageRoom / kStageBytes) : 6;
+  static constexpr int kSmemBytes =
+      kStages * kStageBytes + kEpiBytes + 1024 /*barriers*/ + 1024 /*alignment*/;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
   static constexpr uint32_t kIdescBF16 = tc::idesc(tc::kFmtBF16, kBM, BN);
   static constexpr uint32_t kIdescE4M3 = tc::idesc(tc::kFmtE4M3, kBM, BN);
@@ -83,6 +90,7 @@ struct TcParams {
   CUtensorMap tb;                       // B [N, K] bf16, box {64, BN}
   CUtensorMap tp;                       // P [T, ldp] fp32, box {32, 128}
   CUtensorMap tq[LORA_MAX_SLOTS];       // Q_slot [N, r] fp32, box {32, BN}
+  CUtensorMap to;                       // out [T, N] bf16, box {32, 32} (the epilogue's stores)
   const TokenItem* items;               // null: uniform 128-token tiles, slot 0
   const int32_t* n_items;
   int64_t T;
@@ -235,7 +243,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* tiles = base;
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(base + kStages * kStageBytes);
+  uint8_t* epi_boxes = base + kStages * kStageBytes;
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(epi_boxes + kEpiBytes);
   uint64_t* empty_bar = full_bar + kStages;
   uint64_t* acc_full = empty_bar + kStages;   // [2]: a tile's accumulation is complete
   uint64_t* acc_empty = acc_full + 2;         // [2]: the epilogue has drained the accumulator
@@ -363,6 +372,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
     const int q = warp & 3;
     const int row = q * 32 + lane;
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+    uint8_t* boxes = epi_boxes + (warp - 2) * 2 * kEpiBox;
+    int nbox = 0;   // boxes filled so far by this warp
     int j = 0;
     for (int t = t_first; t < p.total_tiles; t += t_step) {
       TokenItem it;
@@ -393,6 +404,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
       if (!ready) break;
       fence_after();
       const uint32_t acc = tmem + ((uint32_t)(q * 32) << 16) + 256u * (uint32_t)b;
+      // This warp's 32 rows leave through bulk tensor stores when they all lie in the item, or
+      // when the end of the tensor clips them; a partial item of a routed call stores row by
+      // row (the rows past it belong to other CTAs).
+      const int64_t wrow0 = (int64_t)it.t0 + q * 32;
+      const bool box_store = wrow0 < it.t1 && (wrow0 + 32 <= it.t1 || (int64_t)it.t1 == p.T);
 #pragma unroll
       for (int c = 0; c < BN / 32; ++c) {
         float v[32];
@@ -415,7 +431,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
           for (int jj = 0; jj < 32; ++jj)
             v[jj] *= (nb + jj < p.n_out) ? __ldg(p.n_colscale + nb + jj) : 0.f;
         }
-        if (row_ok) {
+        if (box_store) {
+          // the store issued from this box two boxes ago has read it
+          uint8_t* box = boxes + (nbox & 1) * kEpiBox;
+          ++nbox;
+          if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+          __syncwarp();
+          uint8_t* rowp = box + lane * 64;
+#pragma unroll
+          for (int gq = 0; gq < 4; ++gq)
+            store8(reinterpret_cast<__nv_bfloat16*>(rowp + ((gq ^ ((lane >> 1) & 3)) << 4)), v + gq * 8);
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&p.to, box, (int32_t)nb, (int32_t)wrow0);
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+          }
+        } else if (row_ok) {
 #pragma unroll
           for (int gq = 0; gq < 4; ++gq)
             if (nb + gq * 8 + 8 <= p.n_out) store8(out + m * p.ldo + nb + gq * 8, v + gq * 8);
@@ -425,6 +457,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
       asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&acc_empty[b])) : "memory");
       ++j;
     }
+    // the bulk stores have written their rows before the kernel completes
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    __syncwarp();
     fence_before();
   }
   __syncthreads();
@@ -641,6 +676,9 @@ cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st, int prof_kind) 
   prm.items = a.items;
   prm.n_items = a.n_items;
   prm.T = a.T;
+  if (!tc::make_map_2d(&prm.to, a.out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.n_rows, a.T, a.ldo, 32,
+                       32))
+    return cudaErrorInvalidValue;
   prm.err = tc::error_word();
   if (!prm.err) return cudaErrorInvalidDevice;
   prm.nk_main = (int32_t)((a.K + kblk - 1) / kblk);
