@@ -214,7 +214,7 @@ class Clocks:
 def pack_inputs(inputs, device):
     """Rebind every input tensor (same values) to a view of one flat device buffer, so that a
     step's whole input batch moves host -> device in one copy. Drops repeated tensors from
-    `inputs` (in place) and returns the flat buffer."""
+    `inputs` (in place) and returns the flat buffer and each tensor's byte offset in it."""
     import torch
     uniq = {id(t): t for t in inputs}
     inputs[:] = list(uniq.values())
@@ -225,10 +225,17 @@ def pack_inputs(inputs, device):
     flat = torch.empty(total, dtype=torch.uint8, device=device)
     for t, o in zip(inputs, offs):
         nb = t.numel() * t.element_size()
+        flat[o:o + nb].view(t.dtype).view(t.shape).copy_(t)
+    rebind_inputs(inputs, flat, offs)
+    return flat, offs
+
+
+def rebind_inputs(inputs, flat, offs):
+    """Point every input tensor at its slice of the flat buffer `flat` (pack_inputs' layout)."""
+    for t, o in zip(inputs, offs):
+        nb = t.numel() * t.element_size()
         v = flat[o:o + nb].view(t.dtype).view(t.shape)
-        v.copy_(t)
         t.set_(v.untyped_storage(), v.storage_offset(), v.shape, v.stride())
-    return flat
 
 
 def _scale(cfg, L):
@@ -523,7 +530,7 @@ def run_ours(args):
         step, run, inputs, results = make_multi(cfg, args.streams, device)
     else:
         step, run, inputs, results = make_single(cfg, layers, args.streams, device)
-    flat_in = pack_inputs(inputs, device)
+    flat_in, in_offs = pack_inputs(inputs, device)
     torch.cuda.synchronize()
 
     # launches per step (eager), then warm-up
@@ -593,47 +600,111 @@ def run_ours(args):
     # copies measured about 15% slower).
     pinned = torch.empty(flat_in.numel(), dtype=torch.uint8, pin_memory=True)
     pinned.copy_(flat_in)
-    res_host = [torch.empty(r.shape, dtype=r.dtype, pin_memory=True) for r in results]
+    # two pinned result sets: the host reads step k's result while step k + 1 is queued
+    res_host = [[torch.empty(r.shape, dtype=r.dtype, pin_memory=True) for r in results]
+                for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in inputs)
-    d2h = sum(t.numel() * t.element_size() for t in res_host)
+    d2h = sum(t.numel() * t.element_size() for t in res_host[0])
     # As a training loop would, the next step's batch is copied host -> device on a second stream
-    # while the current step runs (into a staging copy, moved into place at the step's start);
-    # every step still copies its whole input from pinned host memory and reads its result back.
-    staging = torch.empty_like(flat_in)
+    # while the current step runs: two input buffers take turns, each with its own captured step
+    # (the second capture reads the second buffer), so the copy lands in the idle buffer. Every
+    # step still copies its whole input from pinned host memory and reads its result back.
+    flat_b = torch.empty_like(flat_in)
+    flat_b.copy_(flat_in)
+    if graph is not None:
+        rebind_inputs(inputs, flat_b, in_offs)
+        graph_b = torch.cuda.CUDAGraph()
+        sb = torch.cuda.Stream(device=device)
+        sb.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(sb):
+            with torch.cuda.graph(graph_b, stream=sb):
+                run()
+        torch.cuda.current_stream().wait_stream(sb)
+        graph_b.replay()   # warm: the first replay of a capture does one-time work
+        torch.cuda.synchronize()
+        rebind_inputs(inputs, flat_in, in_offs)
+        steps_on = [graph.replay, graph_b.replay]
+    else:
+        def eager_on(buf):
+            def go():
+                rebind_inputs(inputs, buf, in_offs)
+                run()
+            return go
+        steps_on = [eager_on(flat_in), eager_on(flat_b)]
+    bufs = [flat_in, flat_b]
     copy_stream = torch.cuda.Stream(device=device)
+    # the host link's rate for this batch, alone (context for the e2e number)
+    h0, h1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    h2d_alone_ms = []
+    for _ in range(2):
+        h0.record(copy_stream)
+        with torch.cuda.stream(copy_stream):
+            flat_b.copy_(pinned, non_blocking=True)
+        h1.record(copy_stream)
+        h1.synchronize()
+        h2d_alone_ms.append(h0.elapsed_time(h1))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     Ke = max(3, K // 2)
     torch.cuda.synchronize()
     t_host0 = time.perf_counter()
     e0.record(stream)
 
-    def h2d_into_staging(after=None):
-        if after is None:
-            copy_stream.wait_stream(stream)
-        else:
-            copy_stream.wait_event(after)   # the staging copy has been moved into place
+    copy_ev = []       # (start, end) of every timed host -> device copy
+    step_ev_e2e = []   # (start, end) of every step in the loop
+
+    def h2d_into(buf, after):
+        # `after`: the end of the step that last read `buf`
+        if after is not None:
+            copy_stream.wait_event(after)
+        c0 = torch.cuda.Event(enable_timing=True)
+        c0.record(copy_stream)
         with torch.cuda.stream(copy_stream):
-            staging.copy_(pinned, non_blocking=True)
-        done = torch.cuda.Event()
+            buf.copy_(pinned, non_blocking=True)
+        done = torch.cuda.Event(enable_timing=True)
         done.record(copy_stream)
+        copy_ev.append((c0, done))
         return done
 
-    h2d_done = h2d_into_staging()
+    # Step k: wait for its batch, queue the next batch's copy into the other buffer (after the
+    # step that last read it), run, copy the result to host memory; the host then reads step
+    # k - 1's result, so that step k is already queued while the host waits (a training loop
+    # that logs each step's loss one step late).
+    step_end = [None, None]
+    check = 0.0
+    h2d_done = h2d_into(bufs[0], None)
     for k in range(Ke):
         stream.wait_event(h2d_done)
-        flat_in.copy_(staging, non_blocking=True)
-        moved = torch.cuda.Event()
-        moved.record(stream)
         if k + 1 < Ke:
-            h2d_done = h2d_into_staging(after=moved)
-        replay()
-        for dst, src in zip(res_host, results):
+            h2d_done = h2d_into(bufs[(k + 1) % 2], step_end[(k + 1) % 2])
+        s0 = torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        steps_on[k % 2]()
+        s1 = torch.cuda.Event(enable_timing=True)
+        s1.record(stream)
+        step_ev_e2e.append((s0, s1))
+        for dst, src in zip(res_host[k % 2], results):
             dst.copy_(src, non_blocking=True)
-        stream.synchronize()
+        ev = torch.cuda.Event()
+        ev.record(stream)
+        if k >= 1:
+            step_end[(k - 1) % 2].synchronize()
+            check += float(res_host[(k - 1) % 2][0].double().sum())
+        step_end[k % 2] = ev
+    step_end[(Ke - 1) % 2].synchronize()
+    check += float(res_host[(Ke - 1) % 2][0].double().sum())
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
-    del staging
+    copy_ms = [a.elapsed_time(b) for a, b in copy_ev]
+    loop_step_ms = [a.elapsed_time(b) for a, b in step_ev_e2e]
+    # step-end to step-end periods of the loop (a single slow host copy, for instance from other
+    # traffic on the host link, shows up as one long period)
+    ends = [b for _, b in step_ev_e2e]
+    periods = [(e0 if k == 0 else ends[k - 1]).elapsed_time(ends[k]) for k in range(len(ends))]
+    rebind_inputs(inputs, flat_in, in_offs)
+    if graph is not None:
+        del graph_b
+    del flat_b, bufs
     clk = clocks.stop()
 
     # the kernel classes once more with every linear on one stream (a capture per class after
@@ -757,7 +828,13 @@ def run_ours(args):
                                      "single-stream capture"} if memory_bound else None,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
+                    "d2h_bytes_per_step": d2h,
+                    "h2d_alone_gbs": h2d / (min(h2d_alone_ms) / 1e3) / 1e9 if h2d_alone_ms else None,
+                    "h2d_in_loop_ms": sorted(copy_ms)[len(copy_ms) // 2] if copy_ms else None,
+                    "step_in_loop_ms": sorted(loop_step_ms)[len(loop_step_ms) // 2]
+                    if loop_step_ms else None,
+                    "period_ms": {"median": statistics.median(periods), "max": max(periods)}
+                    if periods else None},
             "gpu_launches": launches_per_step * K,
             "clocks": clk,
         }
