@@ -54,9 +54,11 @@ constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
 // Epilogue store boxes: each epilogue warp stages 32 rows x 32 bf16 columns (64-byte rows,
 // 64-byte swizzle) and writes them with one bulk tensor store, alternating between two boxes so
-// that one store can still be reading while the next box fills.
+// that one store can still be reading while the next box fills. At BN 224 the boxes would cost
+// the fifth pipeline stage, which is worth more: that width stores row by row.
 constexpr int kEpiBox = 32 * 64;
-constexpr int kEpiBytes = 4 * 2 * kEpiBox;
+template <int BN>
+constexpr int epi_bytes() { return BN == 224 ? 0 : 4 * 2 * kEpiBox; }
 // Items per tile group (rasterization for L2 reuse): 16 when W spans more than 16 N tiles; with
 // fewer, the N tile runs fastest (group of 1), so that the CTAs of one wave read all of W
 // together. Measured at T 8192 (us): N 4096 / K 4096: 152 (N fastest), 152 (8), 162 (16);
@@ -73,7 +75,8 @@ struct GemmCfg {
   static_assert(BN % 32 == 0 && BN >= 128 && BN <= 256, "tile width");
   static constexpr int kBBytes = BN * 128;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  // as many stages as fit beside the epilogue's store boxes (4 at BN 256 and 224, 5 at 192)
+  static constexpr int kEpiBytes = epi_bytes<BN>();
+  // as many stages as fit beside the epilogue's store boxes (4 at BN 256, 5 at 224 and 192)
   static constexpr int kStageRoom = 227 * 1024 - kEpiBytes - 2048;
   static constexpr int kStages = (kStageRoom / kStageBytes) < 6 ? (kStageRoom / kStageBytes) : 6;
   static constexpr int kSmemBytes =
@@ -232,7 +235,8 @@ __device__ __forceinline__ bool decode_tile(const TcParams& p, int t, uint32_t r
 // arrive pre-divided by the same scales, so that they share the accumulator.
 template <int BN, bool F8, bool MC>
 __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__ TcParams p) {
-  grid_dep_sync();
+  // The set-up below (barriers, TMEM, tensor-map prefetch) touches nothing that an earlier kernel
+  // writes, so it runs before grid_dep_sync() and overlaps the previous kernel's tail.
   using C = GemmCfg<BN>;
   constexpr int kHalfB = (BN / 2) * 128;   // pair mode: bytes of one half of the B tile
   const uint32_t rank = MC ? cluster_ctarank() : 0u;
@@ -244,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* tiles = base;
   uint8_t* epi_boxes = base + kStages * kStageBytes;
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(epi_boxes + kEpiBytes);
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(epi_boxes + C::kEpiBytes);
   uint64_t* empty_bar = full_bar + kStages;
   uint64_t* acc_full = empty_bar + kStages;   // [2]: a tile's accumulation is complete
   uint64_t* acc_empty = acc_full + 2;         // [2]: the epilogue has drained the accumulator
@@ -256,6 +260,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
   const int nbuf = p.lora_separate ? 1 : 2;
 
   if (threadIdx.x == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.ta)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tb)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.to)) : "memory");
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], MC ? 2 : 1);   // pair mode: both CTAs' MMAs release a stage
@@ -273,6 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
   if constexpr (MC) cluster_sync_all();   // the peer's barriers exist before any multicast
   fence_after();
   const uint32_t tmem = *tmem_slot;
+  grid_dep_sync();   // from here on, the earlier kernels' outputs are visible
 
   if (warp == 0) {
     if (lane == 0) {
@@ -408,7 +416,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
       // when the end of the tensor clips them; a partial item of a routed call stores row by
       // row (the rows past it belong to other CTAs).
       const int64_t wrow0 = (int64_t)it.t0 + q * 32;
-      const bool box_store = wrow0 < it.t1 && (wrow0 + 32 <= it.t1 || (int64_t)it.t1 == p.T);
+      const bool box_store = C::kEpiBytes > 0 && wrow0 < it.t1 &&
+                             (wrow0 + 32 <= it.t1 || (int64_t)it.t1 == p.T);
 #pragma unroll
       for (int c = 0; c < BN / 32; ++c) {
         float v[32];
