@@ -13,9 +13,12 @@
 // Tiled GEMM", Bug #1: the activation gradient through the frozen weight).
 //
 // CTA layout (192 threads): warp 0 issues TMA loads, warp 1 allocates TMEM and issues the MMAs
-// (one thread), warps 2..5 drain the accumulator (one TMEM lane = one output row per thread).
-// Tile 128 x 256, K-block 64 bf16 (32 fp32 for the LoRA blocks) = one 128-byte swizzled row.
-// Every mbarrier wait is bounded; on timeout the kernel records an error bit and unwinds.
+// (one thread), warps 2..5 drain the accumulator (one TMEM lane = one output row per thread)
+// and store it through shared-memory boxes with bulk tensor stores. Tile 128 x BN (BN 256, 224
+// or 192), K-block 64 bf16 / 128 E4M3 (32 fp32 for the LoRA blocks) = one 128-byte swizzled
+// row. Persistent CTAs; for uniform token tiles they run as 2-CTA clusters that share each B
+// tile through TMA multicast (pair mode, below). Every mbarrier wait is bounded; on timeout the
+// kernel records an error bit and unwinds.
 #include <cudaTypedefs.h>
 
 #include <cstdlib>

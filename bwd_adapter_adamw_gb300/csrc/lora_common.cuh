@@ -109,9 +109,10 @@ __device__ __forceinline__ void store4(__nv_bfloat16* p, const float* v) {
   *reinterpret_cast<uint2*>(p) = u;
 }
 
-// tf32 split for the 3xTF32 products: hi = x rounded to tf32 (nearest, ties away from zero),
-// lo = x - hi (exact in fp32). The tensor core reads lo as tf32 too, so a product formed as
-// hi*hi' + hi*lo' + lo*hi' is within about 2^-21 of the fp32 product, relative.
+// tf32 split for the LoRA K-blocks of the fp32 products (three tf32 products): hi = x rounded to
+// tf32 (nearest, ties away from zero), lo = x - hi (exact in fp32). The tensor core reads lo as
+// tf32 too, so a product formed as hi*hi' + hi*lo' + lo*hi' is within about 2^-21 of the fp32
+// product, relative.
 __device__ __forceinline__ float tf32_hi(float x) {
   uint32_t r;
   asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));

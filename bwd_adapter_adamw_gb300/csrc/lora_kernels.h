@@ -72,7 +72,8 @@ struct TcGemmArgs {
   int max_items;
 };
 cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st, int prof_kind);
-// gemm_tc_f32.cu: the same products for fp32 activations, 3xTF32 on operands split beforehand
+// gemm_tc_f32.cu: the same products for fp32 activations, as three bf16 products of operands
+// split beforehand (bf16 hi / lo)
 cudaError_t launch_tc_gemm_f32(const TcGemmArgs& a, cudaStream_t st, int prof_kind);
 cudaError_t read_tc_error(uint32_t* out, bool reset);
 
