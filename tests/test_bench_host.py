@@ -1,0 +1,74 @@
+"""Host-side logic of the benchmark: the flat input buffer behind the end-to-end copies, the
+per-group byte model, and the chained workload's stability caps (CPU only)."""
+import math
+
+import pytest
+import torch
+
+import bench
+import lora_inputs as LI
+
+
+def test_pack_inputs_keeps_values_and_aliases():
+    gen = torch.Generator().manual_seed(3)
+    a = torch.randn(5, 7, generator=gen)
+    b = torch.randn(3, 8, generator=gen).to(torch.bfloat16)
+    c = torch.randn(11, generator=gen)
+    ref = [a.clone(), b.clone(), c.clone()]
+    holder = {"x": a}   # another reference to the same tensor object
+    inputs = [a, b, a, c]
+    flat, offs = bench.pack_inputs(inputs, "cpu")
+    assert len(inputs) == 3            # the repeated tensor is packed once
+    for t, r in zip(inputs, ref):
+        assert torch.equal(t, r)
+    assert holder["x"].data_ptr() == a.data_ptr()
+    # every input is a view of the flat buffer at a 256-byte aligned offset
+    base = flat.data_ptr()
+    for t, o in zip(inputs, offs):
+        assert o % 256 == 0
+        assert t.data_ptr() == base + o
+    # writing the flat buffer is writing the inputs
+    flat.zero_()
+    assert all(float(t.float().abs().sum()) == 0.0 for t in inputs)
+
+
+def test_rebind_moves_inputs_to_a_second_buffer():
+    a = torch.arange(12, dtype=torch.float32).reshape(3, 4)
+    b = torch.arange(6, dtype=torch.float32)
+    inputs = [a, b]
+    flat, offs = bench.pack_inputs(inputs, "cpu")
+    second = flat.clone()
+    second.view(torch.uint8).zero_()
+    bench.rebind_inputs(inputs, second, offs)
+    assert a.data_ptr() == second.data_ptr() + offs[0]
+    assert float(a.sum()) == 0.0 and float(b.sum()) == 0.0
+    bench.rebind_inputs(inputs, flat, offs)
+    assert torch.equal(a, torch.arange(12, dtype=torch.float32).reshape(3, 4))
+    assert torch.equal(b, torch.arange(6, dtype=torch.float32))
+
+
+def test_memory_counts_groups_count_shared_inputs_once():
+    cfg = LI.CONFIGS["c4"]
+    per_proj = bench.memory_counts(cfg, 1)
+    grouped = bench.memory_counts(cfg, 1, bench.fused_groups(cfg))
+    T = cfg.tokens
+    # q/k/v and gate/up share X: the grouped shrink reads X 4 times instead of 7
+    x_reads = lambda m: m["shrink"]
+    saved = (3 - 1) * T * 4096 * 2 + (2 - 1) * T * 4096 * 2
+    # the adapters and Hs columns are the same in both counts; only the X reads differ
+    assert x_reads(per_proj) - x_reads(grouped) == saved
+    # the output-gradient side is unchanged in total width
+    assert per_proj["redB"] == grouped["redB"]
+    assert per_proj["adamw"] == grouped["adamw"]
+
+
+@pytest.mark.parametrize("name", ["c2", "c4"])
+def test_chain_config_caps_the_adapter_gain(name):
+    base = LI.CONFIGS[name]
+    cfg = bench.chain_config(base)
+    assert len(cfg.projs) == 1 and cfg.projs[0].in_dim == cfg.projs[0].out_dim
+    s = cfg.alpha / (math.sqrt(cfg.rank) if cfg.rslora else cfg.rank)
+    assert 2.0 * s * s * cfg.rank * cfg.b_var <= 0.01 * (1 + 1e-9)
+    assert cfg.lr <= base.lr
+    # Adam moves an entry by about lr per update: 50 replayed updates stay near B's scale
+    assert 50 * cfg.lr * max(1.0, cfg.plus_ratio) <= 1.0 * math.sqrt(cfg.b_var) + 1e-12
