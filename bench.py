@@ -656,7 +656,6 @@ def run_ours(args):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     Ke = max(3, K // 2)
     torch.cuda.synchronize()
-    t_host0 = time.perf_counter()
     e0.record(stream)
 
     copy_ev = []       # (start, end) of every timed host -> device copy
@@ -845,7 +844,9 @@ def run_ours(args):
                     "step_in_loop_ms": sorted(loop_step_ms)[len(loop_step_ms) // 2]
                     if loop_step_ms else None,
                     "period_ms": {"median": statistics.median(periods), "max": max(periods)}
-                    if periods else None},
+                    if periods else None,
+                    # every step's result (clip scale and norm) was read on the host
+                    "results_finite": math.isfinite(check)},
             "gpu_launches": launches_per_step * K,
             # the last step's optimizer status (0: every group updated; non-zero: a group's
             # gradients were non-finite and its update was skipped) and gradient norm
