@@ -160,3 +160,27 @@ def test_optimizer_argument_errors(L):
     assert L.lora_adamw_step(FAKE, FAKE, FAKE, FAKE, g3, hp, FAKE, FAKE, stream=0, check=False) == \
         L.LORA_ERR_INVALID
     assert L.lora_grad_prepare_workspace_size(g3) > 0
+
+
+def test_fused_entries_check_arguments_before_launch(L):
+    """Host-side argument checks of the fused entries (no launch happens on these paths)."""
+    import torch
+    A = torch.zeros(8, 256)
+    B1, B2 = torch.zeros(384, 8), torch.zeros(128, 8)
+    projs = L.make_projs([dict(A=A, B=B1, dA=A, dB=B1, out=384), dict(A=A, B=B2, dA=A, dB=B2, out=128)])
+    d = L.make_desc(256, 512, 8, 1.0, L.LORA_F32)
+    c = L.make_ctx(0, 0, 64)
+    args = dict(X=FAKE, W=FAKE, Wp=FAKE, Y=FAKE, H=FAKE, ws=FAKE)
+
+    def fwd(**kw):
+        a = dict(args, **kw)
+        return L.lora_fused_forward(d, c, 64, a["X"], a["W"], a["Wp"], projs, a["Y"], a["H"],
+                                    a["ws"], ws_bytes=1 << 30, stream=0, check=False)
+
+    assert fwd(Wp=None) == L.LORA_ERR_INVALID       # the fp32 forward reads the prepared weight
+    assert fwd(X=None) == L.LORA_ERR_INVALID
+    assert L.lora_fused_forward(d, c, 64, FAKE, FAKE, FAKE, projs, FAKE, FAKE, FAKE, ws_bytes=16,
+                                stream=0, check=False) == L.LORA_ERR_WORKSPACE
+    st = L.lora_fused_backward(d, c, 64, FAKE, None, projs, FAKE, FAKE, None, FAKE,
+                               ws_bytes=1 << 30, stream=0, check=False)
+    assert st == L.LORA_ERR_INVALID                 # W_prep missing
