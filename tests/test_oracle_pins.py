@@ -675,3 +675,134 @@ def test_fused_projections_equal_the_stacked_effective_weight():
     for (gA, gB), W, A, B, dY in zip(res.grads, Ws, As, Bs, dYs):
         np.testing.assert_allclose(gB, s * dY.T @ (X @ A.T), rtol=1e-12, atol=1e-12)
         np.testing.assert_allclose(gA, s * (dY @ B).T @ X, rtol=1e-12, atol=1e-12)
+
+
+# ---- FP8 dX ("LoRA Training and Serving", Quantized rollout: E4M3 frozen base) ----
+def _e4m3_col_scaled(W):
+    """Independent per-input-column quantisation of W (the layout the dX product contracts
+    over the output rows of W): amax_i = max_o |W[o, i]|, codes e4m3(W[o, i] * 448 / amax_i)."""
+    W = np.asarray(W, np.float32)
+    amax = np.max(np.abs(W), axis=0)
+    rcp = (np.float32(448.0) / amax).astype(np.float32)
+    codes = O.e4m3_encode((W * rcp[None, :]).astype(np.float32))
+    return codes, (amax / np.float32(448.0)).astype(np.float32)
+
+
+def _fp8_dx_problem(seed=21, T=3, n_out=24, n_in=5, r=2):
+    rng = np.random.default_rng(seed)
+    dY = rng.standard_normal((T, n_out)).astype(np.float32)
+    # input columns of W with scales 10^-5 .. 10^1: a per-output-row quantisation of W (the
+    # forward's layout, wrong for dX) flushes the small columns to zero, far outside the
+    # per-column bound below
+    W = (rng.standard_normal((n_out, n_in)) * np.logspace(-5, 1, n_in)[None, :]).astype(np.float32)
+    A = rng.standard_normal((r, n_in)).astype(np.float32)
+    B = rng.standard_normal((n_out, r)).astype(np.float32)
+    return dY, W, A, B
+
+
+def test_fp8_dx_brute_force_over_decoded_codes():
+    dY, W, A, B = _fp8_dx_problem()
+    s = 1.5
+    G = dY.astype(np.float64) @ B.astype(np.float64)
+    got = O.lora_dx_fp8(dY, W, A, G, s)
+    Dc, sd = O.quantize_rows_e4m3(dY)          # per token (row of dY)
+    Wc, sw = _e4m3_col_scaled(W)                 # per input column of W
+    T, n_out = dY.shape
+    n_in = W.shape[1]
+    for t in range(T):
+        for i in range(n_in):
+            acc = 0.0
+            for o in range(n_out):
+                acc += float(O.e4m3_decode([Dc[t, o]])[0]) * float(O.e4m3_decode([Wc[o, i]])[0])
+            lora = sum(G[t, j] * float(A[j, i]) for j in range(A.shape[0]))
+            want = float(sd[t]) * acc * float(sw[i]) + s * lora
+            assert abs(got[t, i] - want) <= 1e-12 * max(1.0, abs(want)), (t, i)
+
+
+def test_fp8_dx_with_zero_adapter_is_the_fp8_product_of_dY_and_W_transposed():
+    dY, W, A, _ = _fp8_dx_problem(seed=22)
+    G0 = np.zeros((dY.shape[0], A.shape[0]))
+    got = O.lora_dx_fp8(dY, W, A, G0, 2.0)
+    Dc, sd = O.quantize_rows_e4m3(dY)
+    Wtc, swt = O.quantize_rows_e4m3(np.ascontiguousarray(W.T))
+    np.testing.assert_array_equal(got, O.fp8_product(Dc, sd, Wtc, swt))
+
+
+def test_fp8_dx_within_the_e4m3_bound_of_the_exact_backward():
+    dY, W, A, B = _fp8_dx_problem(seed=23, T=4)
+    rng = np.random.default_rng(24)
+    X = rng.standard_normal((dY.shape[0], W.shape[1])).astype(np.float32)
+    s, p = 0.75, 0.3
+    keep = O.dropout_keep(p, 5, 1, 0, 2, 1, X.shape[0], X.shape[1])
+    q = O.dropout_q(p)
+    ref = O.lora_backward(X, W, A, B, dY, s, keep, q)
+    got = O.lora_dx_fp8(dY, W, A, ref.G, s, keep, q)
+    # each quantised operand is within 2^-4 of its value (relative) or half a subnormal step
+    # (2^-10 in code units) of it; the adapter term is exact in both
+    sd = np.max(np.abs(dY), axis=1) / 448.0
+    sw = np.max(np.abs(W), axis=0) / 448.0
+    bound = (np.abs(dY).astype(np.float64) @ np.abs(W)) * (2 * 2.0 ** -4 + 2.0 ** -8) \
+        + 2.0 ** -10 * (sd[:, None] * np.abs(W).sum(0)[None, :] + np.abs(dY).sum(1)[:, None] * sw[None, :])
+    assert np.all(np.abs(got - ref.dX) <= bound + 1e-12)
+    # and a per-output-row quantisation of W would not be: its small input columns lose
+    # everything, so the same bound fails there
+    Wc_row, sw_row = O.quantize_rows_e4m3(W)
+    Dc, sdq = O.quantize_rows_e4m3(dY)
+    wrong = (sdq[:, None] * (O.e4m3_decode(Dc) @ (O.e4m3_decode(Wc_row) * sw_row[:, None].astype(np.float64))))
+    frozen = dY.astype(np.float64) @ W.astype(np.float64)
+    assert np.any(np.abs(wrong - frozen) > bound)
+
+
+# ---- adapter gradients alone ("Backward Bug Hunts and Vulkan Tiled GEMM", Bug #1 / #2) ----
+@pytest.mark.parametrize("p", [0.0, 0.35])
+def test_adapter_grads_equal_the_full_backward(p):
+    X, W, A, B, dY = _problem(T=7, n_in=6, n_out=5, r=3, seed=31)
+    s = 1.7
+    keep = O.dropout_keep(p, 9, 4, 1, 3, 2, X.shape[0], X.shape[1]) if p > 0 else None
+    q = O.dropout_q(p) if p > 0 else 1.0
+    dA, dB = O.lora_adapter_grads(X, A, B, dY, s, keep, q)
+    ref = O.lora_backward(X, W, A, B, dY, s, keep, q)
+    np.testing.assert_allclose(dA, ref.dA, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(dB, ref.dB, rtol=1e-13, atol=1e-13)
+
+
+def test_adapter_grads_match_central_finite_differences():
+    X, W, A, B, dY = _problem(T=5, n_in=4, n_out=3, r=2, seed=32)
+    s, p = 0.9, 0.5
+    keep = O.dropout_keep(p, 2, 0, 1, 0, 4, X.shape[0], X.shape[1])
+    q = O.dropout_q(p)
+    dA, dB = O.lora_adapter_grads(X, A, B, dY, s, keep, q)
+    h = 1e-3
+
+    def L(A_, B_):
+        return _loss(O.lora_forward(X, W, A_, B_, s, keep, q).Y, dY)
+
+    for arr, grad, which in ((A, dA, "A"), (B, dB, "B")):
+        fd = np.zeros_like(arr)
+        for idx in np.ndindex(arr.shape):
+            plus, minus = arr.copy(), arr.copy()
+            plus[idx] += h
+            minus[idx] -= h
+            fd[idx] = ((L(plus, B) - L(minus, B)) if which == "A" else (L(A, plus) - L(A, minus))) / (2 * h)
+        np.testing.assert_allclose(grad, fd, rtol=1e-8, atol=1e-9, err_msg=which)
+
+
+# ---- Adam bias correction at k > 1 ("4.3. Training Guide", Optimizer) ----
+def test_adam_constant_gradient_gives_the_normalised_sign_step_at_every_k():
+    # from zero moments and a constant g_hat, after k updates m = (1 - b1^k) g_hat and
+    # v = (1 - b2^k) g_hat^2, so the corrected moments are g_hat and g_hat^2 and every update is
+    # -lr g_hat / (|g_hat| + eps); a bias correction with the wrong power (or none) breaks this
+    g = np.array([3e-2, -1.5, 4e-6, 0.25], np.float64)
+    lr = 1e-2
+    p = np.zeros(4, np.float32)
+    m = np.zeros(4, np.float32)
+    v = np.zeros(4, np.float32)
+    want = -lr * g / (np.abs(g) + 1e-8)
+    for k in range(12):
+        hp = O.AdamHP(lr=lr, wd=0.0, step=k)
+        p1, m, v = O.adamw_update(p, g, m, v, O.KIND_B, 1.0, hp)
+        np.testing.assert_allclose(p1.astype(np.float64) - p.astype(np.float64), want,
+                                   rtol=2e-5, atol=1e-12, err_msg=f"update {k + 1}")
+        np.testing.assert_allclose(m, (1 - 0.9 ** (k + 1)) * g, rtol=1e-5)
+        np.testing.assert_allclose(v, (1 - 0.999 ** (k + 1)) * g * g, rtol=1e-5)
+        p = p1
