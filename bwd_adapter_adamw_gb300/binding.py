@@ -21,6 +21,7 @@ LORA_ERR_UNSUPPORTED = 3
 LORA_ERR_WORKSPACE = 4
 LORA_ERR_CUDA = 5
 LORA_ERR_NONFINITE = 6
+LORA_ERR_TIMEOUT = 7
 
 LORA_F32 = 0
 LORA_BF16 = 1
@@ -116,6 +117,8 @@ def _load() -> C.CDLL:
         "lora_launch_counter": (U64, []),
         "lora_last_cuda_error": (C.c_char_p, []),
         "lora_device_error": (C.c_int, [C.POINTER(C.c_uint32), I32]),
+        "lora_device_check": (C.c_int, [P]),
+        "lora_set_wait_limit": (C.c_int, [U64]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -134,7 +137,7 @@ EXPORTED = ("lora_status_string", "lora_scale", "lora_lr_at", "lora_workspace_si
             "lora_fused_workspace_size", "lora_fused_forward", "lora_fused_backward",
             "lora_dropout_mask", "lora_quantize_e4m3", "multi_lora_token_slots", "lora_profile_arm",
             "lora_profile_used", "lora_launch_counter", "lora_last_cuda_error",
-            "lora_device_error")
+            "lora_device_error", "lora_device_check", "lora_set_wait_limit")
 
 LORA_PROF_NONE = 0
 LORA_PROF_FROZEN_FWD = 1
@@ -405,6 +408,17 @@ def lora_profile_used() -> int:
 
 def lora_launch_counter() -> int:
     return _lib.lora_launch_counter()
+
+
+def lora_device_check(stream=None) -> int:
+    """Synchronise the stream and return the device status (LORA_OK, or LORA_ERR_TIMEOUT when a
+    kernel's pipeline wait ran out of its bound) without raising."""
+    return _lib.lora_device_check(_stream(stream))
+
+
+def lora_set_wait_limit(cycles: int) -> None:
+    """Test hook: bound of the frozen products' pipeline waits (0 = the default)."""
+    _check(_lib.lora_set_wait_limit(int(cycles)), "lora_set_wait_limit")
 
 
 def lora_device_error(reset: bool = False) -> int:

@@ -1140,6 +1140,20 @@ int lora_device_error(uint32_t* flags, int32_t reset) {
   return cuda_status(read_tc_error(flags, reset != 0));
 }
 
+int lora_device_check(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_status(e);
+  uint32_t flags = 0;
+  e = read_tc_error(&flags, false);
+  if (e != cudaSuccess) return cuda_status(e);
+  return flags ? LORA_ERR_TIMEOUT : LORA_OK;
+}
+
+int lora_set_wait_limit(uint64_t cycles) {
+  set_tc_wait_limit((unsigned long long)cycles);
+  return LORA_OK;
+}
+
 const char* lora_status_string(int status) {
   switch (status) {
     case LORA_OK: return "ok";
@@ -1149,6 +1163,7 @@ const char* lora_status_string(int status) {
     case LORA_ERR_WORKSPACE: return "workspace too small";
     case LORA_ERR_CUDA: return "CUDA launch or runtime error";
     case LORA_ERR_NONFINITE: return "non-finite gradient: update rejected";
+    case LORA_ERR_TIMEOUT: return "a device pipeline wait ran out of its bound: outputs invalid";
     default: return "unknown status";
   }
 }

@@ -16,12 +16,11 @@
 // (one thread), warps 2..5 drain the accumulator (one TMEM lane = one output row per thread)
 // and store it through shared-memory boxes with bulk tensor stores. Tile 128 x BN (BN 256, 224
 // or 192), K-block 64 bf16 / 128 E4M3 (32 fp32 for the LoRA blocks) = one 128-byte swizzled
-// row. Persistent CTAs; for uniform token tiles they run as 2-CTA clusters that share each B
-// tile through TMA multicast (pair mode, below). Every mbarrier wait is bounded; on timeout the
-// kernel records an error bit and unwinds.
+// row. Persistent CTAs, one per SM. Every mbarrier wait is bounded; on timeout the kernel records
+// an error bit and unwinds.
 #include <cudaTypedefs.h>
 
-#include <cstdlib>
+#include <atomic>
 #include <cstring>
 #include <mutex>
 
@@ -103,9 +102,9 @@ struct TcParams {
   int32_t n_tiles;                      // N tiles per item
   int32_t max_items;                    // item slots
   int32_t group_m;                      // items per tile group
-  int32_t total_tiles;                  // n_tiles x item slots (x item pairs in pair mode)
-  int32_t n_pairs;                      // pair mode: item pairs, ceil(item slots / 2)
+  int32_t total_tiles;                  // n_tiles x item slots
   uint32_t* err;
+  unsigned long long wait_limit;        // bound of the pipeline waits (cycles); drains keep kWaitCycles
   int32_t nk_main;
   int32_t has_lora;
   int32_t lora_separate;
@@ -202,28 +201,9 @@ __device__ __forceinline__ void lora_block(const TcParams& p, const LoraTile& lt
   qrow0 = 0;
 }
 
-// Pair mode (MC): the two CTAs of a cluster take the same N tile of two consecutive 128-token
-// tiles (uniform tiles only) and share its B tile, each loading one half of the B rows into both
-// CTAs' shared memory (TMA multicast), which halves the L2 reads of B. Pair tile t covers items
-// 2 ip and 2 ip + 1; a CTA whose tile lies past T still takes part in the loads and MMAs (its A
-// rows read as zeros) and stores nothing, so that both CTAs run the same stage sequence.
-template <int BN, bool MC>
-__device__ __forceinline__ bool decode_tile(const TcParams& p, int t, uint32_t rank, TokenItem& it,
-                                            int32_t& n0) {
-  if constexpr (MC) {
-    const int per_group = p.group_m * p.n_tiles;
-    const int group = t / per_group;
-    const int first = group * p.group_m;
-    const int gsize = min(p.group_m, p.n_pairs - first);
-    const int idx = t - group * per_group;
-    n0 = (idx / gsize) * BN;
-    const int64_t t0 = (int64_t)(2 * (first + idx % gsize) + (int)rank) * kBM;
-    it.t0 = (int32_t)t0;
-    it.t1 = (int32_t)(t0 >= p.T ? t0 : (p.T < t0 + kBM ? p.T : t0 + kBM));
-    it.slot = 0;
-    it.pad = 0;
-    return true;
-  }
+// Tile t of the persistent schedule: its work item and first output column.
+template <int BN>
+__device__ __forceinline__ bool decode_tile(const TcParams& p, int t, TokenItem& it, int32_t& n0) {
   const int per_group = p.group_m * p.n_tiles;
   const int group = t / per_group;
   const int first = group * p.group_m;
@@ -236,15 +216,13 @@ __device__ __forceinline__ bool decode_tile(const TcParams& p, int t, uint32_t r
 // F8: the main K-blocks are E4M3 codes (128 per 128-byte row, kind::f8f6f4); the accumulator is
 // then in code units and the epilogue multiplies by the row and column scales. The LoRA K-blocks
 // arrive pre-divided by the same scales, so that they share the accumulator.
-template <int BN, bool F8, bool MC>
+template <int BN, bool F8>
 __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__ TcParams p) {
   // The set-up below (barriers, TMEM, tensor-map prefetch) touches nothing that an earlier kernel
   // writes, so it runs before grid_dep_sync() and overlaps the previous kernel's tail.
   using C = GemmCfg<BN>;
-  constexpr int kHalfB = (BN / 2) * 128;   // pair mode: bytes of one half of the B tile
-  const uint32_t rank = MC ? cluster_ctarank() : 0u;
-  const int t_first = MC ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
-  const int t_step = MC ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  const int t_first = (int)blockIdx.x;
+  const int t_step = (int)gridDim.x;
   constexpr int kStages = C::kStages;
   constexpr int kStageBytes = C::kStageBytes;
   extern __shared__ uint8_t smem_raw[];
@@ -255,7 +233,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
   uint64_t* empty_bar = full_bar + kStages;
   uint64_t* acc_full = empty_bar + kStages;   // [2]: a tile's accumulation is complete
   uint64_t* acc_empty = acc_full + 2;         // [2]: the epilogue has drained the accumulator
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  uint64_t* mma_done = acc_empty + 2;         // every MMA this CTA issued has completed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -268,19 +247,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.to)) : "memory");
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], MC ? 2 : 1);   // pair mode: both CTAs' MMAs release a stage
+      mbar_init(&empty_bar[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
       mbar_init(&acc_empty[b], kEpiThreads);
     }
+    mbar_init(mma_done, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   if (warp == 1) tmem_alloc(tmem_slot, ncols);
   fence_before();
   __syncthreads();
-  if constexpr (MC) cluster_sync_all();   // the peer's barriers exist before any multicast
   fence_after();
   const uint32_t tmem = *tmem_slot;
   grid_dep_sync();   // from here on, the earlier kernels' outputs are visible
@@ -292,42 +271,35 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
       for (int t = t_first; t < p.total_tiles && ok; t += t_step) {
         TokenItem it;
         int32_t n0;
-        if (!decode_tile<BN, MC>(p, t, rank, it, n0)) continue;
+        if (!decode_tile<BN>(p, t, it, n0)) continue;
         LoraTile lt;
         const int nk = p.nk_main + lora_tile(p, it, n0, lt);
         for (int kb = 0; kb < nk; ++kb, ++g) {
           const int s = g % kStages;
           const uint32_t ph = (uint32_t)(g / kStages) & 1u;
-          if (g >= kStages && !mbar_wait(&empty_bar[s], ph ^ 1u, 1u, p.err)) { ok = false; break; }
+          if (g >= kStages && !mbar_wait_for(&empty_bar[s], ph ^ 1u, 1u, p.err, p.wait_limit)) {
+            ok = false;
+            break;
+          }
           uint8_t* sa = tiles + s * kStageBytes;
           uint8_t* sb = sa + kABytes;
           mbar_expect_tx(&full_bar[s], kStageBytes);
           if (kb < p.nk_main) {
             constexpr int kKBlock = F8 ? 128 : 64;   // elements in one 128-byte row
             tma_load_2d(sa, &p.ta, &full_bar[s], kb * kKBlock, it.t0);
-            if constexpr (MC)
-              tma_load_2d_mc(sb + rank * kHalfB, &p.tb, &full_bar[s], kb * kKBlock,
-                             n0 + (int32_t)rank * (BN / 2), (uint16_t)0x3);
-            else
-              tma_load_2d(sb, &p.tb, &full_bar[s], kb * kKBlock, n0);
+            tma_load_2d(sb, &p.tb, &full_bar[s], kb * kKBlock, n0);
           } else {
             int qmap, px, qx, qrow0;
             lora_block(p, lt, kb - p.nk_main, qmap, px, qx, qrow0);
             tma_load_2d(sa, &p.tp, &full_bar[s], px, it.t0);
-            if constexpr (MC)
-              tma_load_2d_mc(sb + rank * kHalfB, &p.tq[qmap], &full_bar[s], qx,
-                             n0 - qrow0 + (int32_t)rank * (BN / 2), (uint16_t)0x3);
-            else
-              tma_load_2d(sb, &p.tq[qmap], &full_bar[s], qx, n0 - qrow0);
+            tma_load_2d(sb, &p.tq[qmap], &full_bar[s], qx, n0 - qrow0);
           }
         }
       }
-      // drain: every issued load must have landed before the CTA may exit; in pair mode, also
-      // every release of the last stages by both CTAs' MMAs (the peer's arrivals on this CTA's
-      // barriers), which implies the former
+      // drain: every issued load must have landed before the CTA may exit
       for (int gg = (g > kStages ? g - kStages : 0); gg < g; ++gg) {
         const uint32_t par = (uint32_t)(gg / kStages) & 1u;
-        if (!mbar_wait(MC ? &empty_bar[gg % kStages] : &full_bar[gg % kStages], par, 1u, p.err)) break;
+        if (!mbar_wait(&full_bar[gg % kStages], par, 1u, p.err)) break;
       }
     }
   } else if (warp == 1) {
@@ -337,19 +309,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
       for (int t = t_first; t < p.total_tiles && ok; t += t_step) {
         TokenItem it;
         int32_t n0;
-        if (!decode_tile<BN, MC>(p, t, rank, it, n0)) continue;
+        if (!decode_tile<BN>(p, t, it, n0)) continue;
         LoraTile lt;
         const int nk_lora = lora_tile(p, it, n0, lt);
         const int nk = p.nk_main + nk_lora;
         const bool sep = p.lora_separate && nk_lora > 0;
         const int b = j % nbuf, use = j / nbuf;
-        if (use >= 1 && !mbar_wait(&acc_empty[b], (uint32_t)(use - 1) & 1u, 2u, p.err)) break;
+        if (use >= 1 && !mbar_wait_for(&acc_empty[b], (uint32_t)(use - 1) & 1u, 2u, p.err, p.wait_limit))
+          break;
         fence_after();
         const uint32_t dm = tmem + 256u * (uint32_t)b;
         for (int kb = 0; kb < nk; ++kb, ++g) {
           const int s = g % kStages;
           const uint32_t ph = (uint32_t)(g / kStages) & 1u;
-          if (!mbar_wait(&full_bar[s], ph, 2u, p.err)) { ok = false; break; }
+          if (!mbar_wait_for(&full_bar[s], ph, 2u, p.err, p.wait_limit)) { ok = false; break; }
           fence_after();
           const uint32_t sa = smem_u32(tiles + s * kStageBytes);
           const uint32_t sb = sa + kABytes;
@@ -368,15 +341,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
             for (int k = 0; k < 4; ++k)
               umma_tf32(d, da + 2 * k, db + 2 * k, C::kIdescTF32, (first && k == 0) ? 0u : 1u);
           }
-          if constexpr (MC)
-            umma_commit_mc(&empty_bar[s], (uint16_t)0x3);
-          else
-            umma_commit(&empty_bar[s]);
+          umma_commit(&empty_bar[s]);
         }
         if (!ok) break;
         umma_commit(&acc_full[b]);
         ++j;
       }
+      // every MMA issued above has completed before the tensor memory is freed (after an early
+      // exit nothing else waits for them)
+      umma_commit(mma_done);
+      mbar_wait(mma_done, 0u, 2u, p.err);
     }
   } else {
     // epilogue: warp w drains TMEM lanes 32*(w % 4) .. +31 (one output row per thread)
@@ -389,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
     for (int t = t_first; t < p.total_tiles; t += t_step) {
       TokenItem it;
       int32_t n0;
-      if (!decode_tile<BN, MC>(p, t, rank, it, n0)) continue;
+      if (!decode_tile<BN>(p, t, it, n0)) continue;
       LoraTile lt;
       const bool sep = p.lora_separate && lora_tile(p, it, n0, lt) > 0;
       const int b = j % nbuf, use = j / nbuf;
@@ -411,7 +385,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
         }
       }
       // warp-uniform decision: the TMEM loads below are .sync.aligned
-      const bool ready = __all_sync(0xffffffffu, mbar_wait(&acc_full[b], (uint32_t)use & 1u, 4u, p.err));
+      const bool ready =
+          __all_sync(0xffffffffu, mbar_wait_for(&acc_full[b], (uint32_t)use & 1u, 4u, p.err, p.wait_limit));
       if (!ready) break;
       fence_after();
       const uint32_t acc = tmem + ((uint32_t)(q * 32) << 16) + 256u * (uint32_t)b;
@@ -475,9 +450,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
     fence_before();
   }
   __syncthreads();
-  // pair mode: neither CTA leaves while the other may still write its shared memory or
-  // barriers (every role above ends after bounded waits, so both CTAs arrive)
-  if constexpr (MC) cluster_sync_all();
   if (warp == 1) {
     fence_after();
     tmem_dealloc(tmem, ncols);
@@ -534,90 +506,17 @@ bool make_map_2d(CUtensorMap* map, const void* ptr, CUtensorMapDataType dt, int 
 }  // namespace tc
 
 namespace {
-template <int BN, bool F8, bool MC>
-cudaError_t set_smem_attr() {
+template <int BN, bool F8>
+cudaError_t launch_gemm_bn(unsigned grid, cudaStream_t st, const TcParams& prm) {
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k_tc_gemm<BN, F8, MC>,
+    cudaError_t e = cudaFuncSetAttribute(k_tc_gemm<BN, F8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          GemmCfg<BN>::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  return cudaSuccess;
-}
-
-// Pair mode: clusters of two CTAs that can be resident at once (an SM left over in a GPC with an
-// odd count of free SMs cannot host a pair), cached per variant.
-template <int BN, bool F8>
-int pair_clusters(int sms) {
-  static int cached = -1;
-  if (cached < 0) {
-    if (set_smem_attr<BN, F8, true>() != cudaSuccess) return 0;
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3((unsigned)(sms & ~1));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = GemmCfg<BN>::kSmemBytes;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, k_tc_gemm<BN, F8, true>, &cfg) != cudaSuccess) n = 0;
-    cudaGetLastError();
-    cached = n;
-  }
-  return cached;
-}
-
-template <int BN, bool F8>
-cudaError_t launch_gemm_bn(unsigned grid, cudaStream_t st, const TcParams& prm, bool pair) {
-  if (!pair) {
-    cudaError_t e = set_smem_attr<BN, F8, false>();
-    if (e != cudaSuccess) return e;
-    return launch_kernel(k_tc_gemm<BN, F8, false>, grid, kThreads, GemmCfg<BN>::kSmemBytes, st, prm);
-  }
-  cudaError_t e = set_smem_attr<BN, F8, true>();
-  if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = GemmCfg<BN>::kSmemBytes;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = add_pdl_attr(attr, 1);
-  return cudaLaunchKernelEx(&cfg, k_tc_gemm<BN, F8, true>, prm);
-}
-
-int pair_clusters_bn(int bn, bool f8, int sms) {
-  switch (bn * 2 + (f8 ? 1 : 0)) {
-    case 512: return pair_clusters<256, false>(sms);
-    case 448: return pair_clusters<224, false>(sms);
-    case 384: return pair_clusters<192, false>(sms);
-    case 513: return pair_clusters<256, true>(sms);
-    case 449: return pair_clusters<224, true>(sms);
-    case 385: return pair_clusters<192, true>(sms);
-  }
-  return 0;
-}
-
-// Pair mode (B tiles shared by two CTAs through TMA multicast) for uniform token tiles, where
-// both CTAs of a pair run the same K-blocks; LORA_GEMM_PAIRS=0 turns it off.
-bool pairs_enabled() {
-  static int v = -1;
-  if (v < 0) {
-    const char* e = std::getenv("LORA_GEMM_PAIRS");
-    v = (e && e[0] == '0') ? 0 : 1;
-  }
-  return v == 1;
+  return launch_kernel(k_tc_gemm<BN, F8>, grid, kThreads, GemmCfg<BN>::kSmemBytes, st, prm);
 }
 
 // Tile width: the fewest tile-columns of MMA work per SM, rounds x BN x (relative cost of a
@@ -638,7 +537,11 @@ int pick_tile_n(int64_t n_rows, int64_t items, int sms) {
   }
   return best;
 }
+
+std::atomic<unsigned long long> g_wait_limit{0};   // pipeline-wait bound in cycles; 0: the default
 }  // namespace
+
+void set_tc_wait_limit(unsigned long long cycles) { g_wait_limit.store(cycles); }
 
 cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st, int prof_kind) {
   static TcParams prm;   // large: filled per call on the host, copied into the launch
@@ -659,12 +562,7 @@ cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st, int prof_kind) 
   // one 128-byte row per K-block: 64 bf16 or 128 E4M3 codes
   const CUtensorMapDataType adt = a.fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const int esz = a.fp8 ? 1 : 2, kblk = a.fp8 ? 128 : 64;
-  // pair mode: uniform tiles (every tile of a pair has the same K-blocks), two or more tiles
-  int clusters = 0;
-  if (pairs_enabled() && !a.items && !a.tile_mask && a.max_items >= 2)
-    clusters = pair_clusters_bn(bn, a.fp8 != 0, sms);
-  const bool pair = clusters > 0;
-  const uint32_t b_rows = pair ? (uint32_t)bn / 2 : (uint32_t)bn;   // each CTA loads half of B
+  const uint32_t b_rows = (uint32_t)bn;
   if (!tc::make_map_2d(&prm.ta, a.a, adt, esz, a.K, a.T, a.K, kblk, kBM) ||
       !tc::make_map_2d(&prm.tb, a.b, adt, esz, a.K, a.n_rows, a.K, kblk, b_rows))
     return cudaErrorInvalidValue;
@@ -693,6 +591,8 @@ cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st, int prof_kind) 
     return cudaErrorInvalidValue;
   prm.err = tc::error_word();
   if (!prm.err) return cudaErrorInvalidDevice;
+  const unsigned long long lim = g_wait_limit.load();
+  prm.wait_limit = lim ? lim : tc::kWaitCycles;
   prm.nk_main = (int32_t)((a.K + kblk - 1) / kblk);
   prm.lora_separate = a.lora_separate;
   prm.n_colscale = a.n_colscale;
@@ -721,24 +621,22 @@ cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st, int prof_kind) 
   if (a.max_items <= 0) return cudaSuccess;
   prm.n_tiles = (int32_t)((a.n_rows + bn - 1) / bn);
   prm.max_items = a.max_items;
-  prm.n_pairs = (a.max_items + 1) / 2;
-  // tile groups for L2 reuse, counted in items (pairs of items in pair mode)
-  prm.group_m = prm.n_tiles > kGroupMinTiles ? (pair ? kGroupWide / 2 : kGroupWide) : 1;
-  const int64_t total = (int64_t)prm.n_tiles * (pair ? prm.n_pairs : a.max_items);
+  // tile groups for L2 reuse, counted in items
+  prm.group_m = prm.n_tiles > kGroupMinTiles ? kGroupWide : 1;
+  const int64_t total = (int64_t)prm.n_tiles * a.max_items;
   if (total > INT32_MAX) return cudaErrorInvalidValue;
   prm.total_tiles = (int32_t)total;
-  // one persistent CTA per SM, or one persistent pair per resident cluster
-  const unsigned grid = pair ? 2u * (unsigned)(total < clusters ? total : clusters)
-                             : (unsigned)(total < sms ? total : sms);
+  // one persistent CTA per SM
+  const unsigned grid = (unsigned)(total < sms ? total : sms);
   prof_begin(prof_kind, st);
   cudaError_t e = cudaErrorInvalidValue;
   switch (bn * 2 + (a.fp8 ? 1 : 0)) {
-    case 512: e = launch_gemm_bn<256, false>(grid, st, prm, pair); break;
-    case 448: e = launch_gemm_bn<224, false>(grid, st, prm, pair); break;
-    case 384: e = launch_gemm_bn<192, false>(grid, st, prm, pair); break;
-    case 513: e = launch_gemm_bn<256, true>(grid, st, prm, pair); break;
-    case 449: e = launch_gemm_bn<224, true>(grid, st, prm, pair); break;
-    case 385: e = launch_gemm_bn<192, true>(grid, st, prm, pair); break;
+    case 512: e = launch_gemm_bn<256, false>(grid, st, prm); break;
+    case 448: e = launch_gemm_bn<224, false>(grid, st, prm); break;
+    case 384: e = launch_gemm_bn<192, false>(grid, st, prm); break;
+    case 513: e = launch_gemm_bn<256, true>(grid, st, prm); break;
+    case 449: e = launch_gemm_bn<224, true>(grid, st, prm); break;
+    case 385: e = launch_gemm_bn<192, true>(grid, st, prm); break;
   }
   if (e != cudaSuccess) return e;
   prof_end(prof_kind, st);

@@ -76,6 +76,10 @@ cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st, int prof_kind);
 // split beforehand (bf16 hi / lo)
 cudaError_t launch_tc_gemm_f32(const TcGemmArgs& a, cudaStream_t st, int prof_kind);
 cudaError_t read_tc_error(uint32_t* out, bool reset);
+// Bound (cycles) of the frozen products' pipeline waits for the launches that follow; 0 restores
+// the default. Their drain waits (copies in flight, MMAs before the tensor memory is freed) keep
+// the default bound.
+void set_tc_wait_limit(unsigned long long cycles);
 
 // out_slot[j, i] (+)= sum over items of `slot` of part[item][...]; see lowrank.cu
 struct ReduceTab {

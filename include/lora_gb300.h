@@ -51,6 +51,7 @@ extern "C" {
 #define LORA_ERR_WORKSPACE 4    /* workspace too small */
 #define LORA_ERR_CUDA 5         /* a CUDA launch or runtime call failed */
 #define LORA_ERR_NONFINITE 6    /* device status: a gradient element is NaN or +-Inf */
+#define LORA_ERR_TIMEOUT 7      /* device status: a tensor-core pipeline wait ran out of its bound */
 
 /* ---- enums ----------------------------------------------------------------------------------*/
 #define LORA_F32 0
@@ -370,6 +371,21 @@ const char* lora_last_cuda_error(void);
  * work, released its tensor memory and returned, so the output is invalid. Synchronous (reads
  * a device word of the current device); reset != 0 clears it. */
 int lora_device_error(uint32_t* flags, int32_t reset);
+/* Synchronises `stream`, then reports the device error word: LORA_ERR_TIMEOUT if any bit is set
+ * (left set for lora_device_error), LORA_ERR_CUDA if the stream holds a CUDA error, else LORA_OK.
+ * This is how a caller learns, after the fact, that an asynchronous call's outputs are invalid
+ * because one of its kernels gave up waiting and returned early (no hang, the context stays
+ * usable). The bound of each wait guards against a pipeline that can no longer make progress
+ * ("4.3. Training Guide", Gradient clipping: a bad step is detected and rejected before any
+ * state changes; here the same rule for a stalled kernel). */
+int lora_device_check(void* stream);
+/* Test hook: bound, in SM clock cycles, of the pipeline waits of the frozen-product kernels
+ * (bf16 and E4M3) launched after this call; 0 restores the default (2^33 cycles, seconds).
+ * Process-wide, not thread-safe with concurrent launches. A small bound makes a correct launch
+ * give up: its error bits are set and its outputs are invalid. Waits that drain work already
+ * issued (copies in flight, MMAs before the tensor memory is freed) keep the default bound, so
+ * a kernel that gives up still leaves nothing running behind it. */
+int lora_set_wait_limit(uint64_t cycles);
 
 #ifdef __cplusplus
 }
