@@ -1,9 +1,10 @@
 """Benchmark: one optimizer step of LoRA-adapted linears (forward + backward over every
 accumulation chunk, two-pass clip, A-only AdamW) through the C ABI on GB300.
 
-Default workload: TinyLlama-1.1B-shaped wq + wv adapters over 22 layers, fp32 frozen W, rank 8,
-alpha 16, T = 1024 tokens per step in 4 accumulation chunks, clip 1.0, constant lr 2e-4.
-`--config c3|c4|c4dora|c5` selects the other workloads. Inputs are seeded synthetic tensors.
+Default workload: the Llama-style layer, all seven projections (wq, wk, wv, wo, wgate, wup,
+wdown; hidden 4096, kv 1024, intermediate 14336) over 32 layers, bf16 frozen W, rank 64, alpha 128
+(rsLoRA), T = 8192 tokens per step in 8 accumulation chunks, global clip 1.0. `--config
+c2|c3|c4dora|c5|...` selects the other workloads. Inputs are seeded synthetic tensors.
 
 Prints ONE JSON line (rank 0). `--impl reference` times the CPU oracle instead.
 """
@@ -35,7 +36,7 @@ def parse():
     p.add_argument("--steps", type=int, default=20)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    p.add_argument("--config", default="c2", choices=sorted(LI.CONFIGS))
+    p.add_argument("--config", default="c4", choices=sorted(LI.CONFIGS))
     p.add_argument("--layers", type=int, default=0, help="override the layer count (0 = config's)")
     p.add_argument("--streams", type=int, default=4,
                    help="CUDA streams over the independent adapted linears of the step")
@@ -48,6 +49,7 @@ def parse():
     p.add_argument("--no-graph", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--prof-class", type=int, default=0, help="kernel class to time (0 = auto)")
+    p.add_argument("--oracle-single-thread", action="store_true", help=argparse.SUPPRESS)
     return p.parse_args()
 
 
@@ -412,51 +414,123 @@ def make_multi(cfg, streams, device):
 
 
 # --------------------------------------------------------------------------------- CPU baseline
-def cpu_baseline(cfg: LI.LoraConfig, layers: int, budget_s: float = 20.0):
-    """The oracle, as it stands, on a bounded sample of the workload: whole steps over a subset of
-    the layers (all chunks, all projections), extrapolated to the full layer count."""
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), or None."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu model")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return None
+
+
+def _oracle_problem(cfg, layer, tokens):
+    """One layer's problems and adapter state for the oracle (inputs from lora_inputs)."""
     import numpy as np
+    from oracle import lora_oracle as O
+    problems, state = {}, {}
+    for pi, pr in enumerate(cfg.projs):
+        A = LI.make_a(cfg, layer, pr)
+        B = LI.make_b(cfg, layer, pr)
+        problems[pi] = dict(X=LI.make_x(cfg, layer, pr, tokens=tokens),
+                            W=LI.make_w(cfg, layer, pr),
+                            dY=LI.make_dy(cfg, layer, pr, tokens=tokens), layer=layer, proj=pi)
+        z = lambda a: np.zeros(tuple(a.shape), np.float32)
+        st = O.AdapterState(A.numpy(), B.numpy(), z(A), z(A), z(B), z(B))
+        if cfg.dora:
+            st.mag = LI.dora_magnitude_init(problems[pi]["W"]).numpy()
+            st.mM, st.vM = np.zeros_like(st.mag), np.zeros_like(st.mag)
+        state[pi] = st
+    return problems, state
+
+
+def _oracle_step_seconds(cfg, problems, state, chunks):
     from oracle import lora_oracle as O
     s = O.lora_scale(cfg.alpha, cfg.rank, cfg.rslora)
     hp = O.AdamHP(lr=O.lr_at(cfg.sched, cfg.lr, cfg.opt_step, cfg.warmup, cfg.total, cfg.min_lr),
                   beta1=cfg.beta1, beta2=cfg.beta2, eps=cfg.eps, wd=cfg.wd,
                   plus_ratio=cfg.plus_ratio, step=cfg.opt_step)
+    t0 = time.perf_counter()
+    O.run_single_step(problems, state, s=s, chunks=chunks, p=cfg.dropout_p,
+                      seed=cfg.dropout_seed, opt_step=cfg.opt_step, max_norm=cfg.max_norm,
+                      hp=hp, dora=cfg.dora, keep_outputs=False)
+    return time.perf_counter() - t0
+
+
+def oracle_single_thread():
+    """Single-thread oracle times of two whole workloads: the tiny fp32 linear (64 x 64, T 32 in
+    two chunks) and one rank-16 projection (1536 -> 4096, T 4096, dropout 0.1). Run in a child
+    process whose BLAS is limited to one thread before numpy loads."""
+    out = {}
+    for name in ("c1", "c3"):
+        cfg = LI.CONFIGS[name]
+        problems, state = _oracle_problem(cfg, 0, cfg.tokens)
+        sec = _oracle_step_seconds(cfg, problems, state, cfg.chunks)
+        out[name] = {"seconds": sec, "tokens_per_s": cfg.tokens / sec,
+                     "workload": f"{name}: 1 layer x {cfg.projs[0].in_dim}->{cfg.projs[0].out_dim}, "
+                                 f"T={cfg.tokens}, whole step"}
+    return out
+
+
+def run_single_thread_probe():
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS",
+              "VECLIB_MAXIMUM_THREADS", "NUMEXPR_NUM_THREADS"):
+        env[k] = "1"
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    try:
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-single-thread"],
+                           capture_output=True, text=True, timeout=300, env=env)
+        return json.loads(r.stdout.strip().splitlines()[-1]) if r.returncode == 0 else None
+    except (OSError, subprocess.SubprocessError, ValueError, IndexError):
+        return None
+
+
+def cpu_baseline(cfg: LI.LoraConfig, layers: int, budget_s: float = 20.0, single_thread=True):
+    """The oracle, as it stands, on a bounded sample of the workload: whole steps over a subset of
+    the layers (all chunks, all projections; large workloads also a token sample). `value` is the
+    sample's time scaled to the whole step (per layer x layers, x tokens / sampled tokens), and
+    the measured part and the scale factor are reported beside it."""
     done_layers, elapsed = 0, 0.0
     tokens = cfg.tokens
     if cfg.multi or cfg.tokens * max(p.in_dim for p in cfg.projs) > 8192 * 4096:
         tokens = 512   # large workloads: a token sample, scaled by tokens
     t_all = time.perf_counter()
     while done_layers < layers:
-        problems, state = {}, {}
-        for pi, pr in enumerate(cfg.projs):
-            X = LI.make_x(cfg, done_layers, pr, tokens=tokens)
-            A = LI.make_a(cfg, done_layers, pr)
-            B = LI.make_b(cfg, done_layers, pr)
-            problems[pi] = dict(X=X, W=LI.make_w(cfg, done_layers, pr),
-                                dY=LI.make_dy(cfg, done_layers, pr, tokens=tokens),
-                                layer=done_layers, proj=pi)
-            z = lambda a: np.zeros(tuple(a.shape), np.float32)
-            st = O.AdapterState(A.numpy(), B.numpy(), z(A), z(A), z(B), z(B))
-            if cfg.dora:
-                st.mag = LI.dora_magnitude_init(problems[pi]["W"]).numpy()
-                st.mM, st.vM = np.zeros_like(st.mag), np.zeros_like(st.mag)
-            state[pi] = st
+        problems, state = _oracle_problem(cfg, done_layers, tokens)
         chunks = cfg.chunks if tokens == cfg.tokens else 1
-        t0 = time.perf_counter()
-        O.run_single_step(problems, state, s=s, chunks=chunks, p=cfg.dropout_p,
-                          seed=cfg.dropout_seed, opt_step=cfg.opt_step, max_norm=cfg.max_norm,
-                          hp=hp, dora=cfg.dora, keep_outputs=False)
-        elapsed += time.perf_counter() - t0
+        elapsed += _oracle_step_seconds(cfg, problems, state, chunks)
         done_layers += 1
         if time.perf_counter() - t_all > budget_s:
             break
-    per_step = elapsed / done_layers * layers * (cfg.tokens / tokens)
+    scale = (layers / done_layers) * (cfg.tokens / tokens)
+    per_step = elapsed * scale
     cores = len(os.sched_getaffinity(0))
-    return {"value": cfg.tokens / per_step, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": (f"{done_layers} of {layers} layers x {len(cfg.projs)} projections, "
-                       f"{tokens} of {cfg.tokens} tokens, float64 numpy oracle (BLAS threads "
-                       f"= all {cores} cores), whole step per layer, extrapolated linearly"),
-            "seconds": elapsed}
+    out = {"value": cfg.tokens / per_step, "unit": UNIT, "cores": cores, "kind": "oracle",
+           "cpu_model": cpu_model(),
+           "sample": (f"{done_layers} of {layers} layers x {len(cfg.projs)} projections, "
+                      f"{tokens} of {cfg.tokens} tokens, float64 numpy oracle (BLAS threads "
+                      f"= all {cores} cores), whole step per layer"),
+           "measured": {"seconds": elapsed, "layers": done_layers, "tokens": tokens,
+                        "tokens_per_s": done_layers * tokens / elapsed / layers
+                        if elapsed > 0 else None},
+           "extrapolation": {"factor": scale,
+                             "rule": f"x {layers}/{done_layers} layers x {cfg.tokens}/{tokens} "
+                                     "tokens (the oracle's cost is linear in both)",
+                             "per_step_s": per_step},
+           "seconds": elapsed}
+    if single_thread:
+        out["single_thread"] = run_single_thread_probe()
+    return out
 
 
 # --------------------------------------------------------------------------------- reference arm
@@ -471,7 +545,7 @@ def run_reference(args):
     budget = 240.0 / max(1, args.steps + args.warmup)
     vals = []
     for i in range(args.warmup + args.steps):
-        r = cpu_baseline(cfg, layers, budget_s=min(budget, 20.0))
+        r = cpu_baseline(cfg, layers, budget_s=min(budget, 20.0), single_thread=False)
         if i >= args.warmup:
             vals.append(r)
     value = statistics.median(v["value"] for v in vals)
@@ -482,7 +556,9 @@ def run_reference(args):
             "config": {"workload": workload_name(cfg, layers, args.chain),
                        "tokens_per_step": cfg.tokens},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": vals[0]["cores"],
-                             "kind": "oracle", "sample": vals[0]["sample"]},
+                             "kind": "oracle", "sample": vals[0]["sample"],
+                             "cpu_model": vals[0]["cpu_model"],
+                             "extrapolation": vals[0]["extrapolation"]["rule"]},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -783,8 +859,14 @@ def run_ours(args):
             peak = peaks["bf16_tflops"]
             bound, punit = "tensor", "TFLOP/s"
             note = f"dense bf16 cuBLAS burst, {peak_src}"
-        achieved = per_launch / (avg_kern / 1e3) / 1e12 if avg_kern else None
         avg_serial = statistics.mean(kern_serial) if kern_serial else None
+        # the roofline takes the kernel's own launch durations: from the single-stream capture
+        # when the step runs on several streams (there, concurrent launches stretch each
+        # other's event brackets), else from the timed step itself
+        own = kern_serial if kern_serial else kern_ms
+        avg_own = statistics.mean(own) if own else None
+        achieved = per_launch / (avg_own / 1e3) / 1e12 if avg_own else None
+        achieved_overlap = per_launch / (avg_kern / 1e3) / 1e12 if avg_kern else None
         mem = memory_counts(cfg, layers if not cfg.multi else 1,
                             fused_groups(cfg) if args.fused else None)
         memory_bound = {}
@@ -794,7 +876,6 @@ def run_ours(args):
                 memory_bound[name] = {"achieved_gbs": gbs, "frac": gbs / peaks["hbm_gbs"],
                                       "launches": len(ts), "ms_total": sum(ts),
                                       "bytes_per_step": mem[name]}
-        achieved_serial = per_launch / (avg_serial / 1e3) / 1e12 if avg_serial else None
         # step-level bound: every frozen product at the tensor peak plus every memory-bound
         # class's algorithmic bytes at the HBM peak, against the measured step
         t_tensor = (cnt["fwd_flops"] + cnt["dx_flops"]) / (peak * 1e12) * 1e3
@@ -826,13 +907,18 @@ def run_ours(args):
                          "traffic_note": traffic_note,
                          "kernel": {1: "frozen forward GEMM", 2: "frozen dX GEMM"}.get(
                              prof_class, f"class {prof_class}"),
-                         "launches_timed": len(kern_ms), "avg_launch_ms": avg_kern,
+                         "launches_timed": len(own), "avg_launch_ms": avg_own,
+                         "sum_launch_ms": sum(own) if own else None,
+                         "flops_per_launch": per_launch,
+                         "timing": "single-stream capture of the same step (CUDA events on the "
+                                   "launching stream around every launch of the class)"
+                                   if kern_serial else "the timed step's launches (one stream)",
                          "peak_source": note},
-            "roofline_serial": None if achieved_serial is None else {
-                "achieved": achieved_serial, "peak": peak, "unit": punit,
-                "frac": achieved_serial / peak, "avg_launch_ms": avg_serial,
-                "launches_timed": len(kern_serial),
-                "note": "same kernel class, same step captured with every linear on one stream"},
+            "roofline_overlapped": None if not kern_serial or achieved_overlap is None else {
+                "achieved": achieved_overlap, "frac": achieved_overlap / peak,
+                "avg_launch_ms": avg_kern, "launches_timed": len(kern_ms),
+                "note": "event brackets inside the multi-stream timed step, where concurrent "
+                        "launches overlap: not the kernel's own duration"},
             "memory_bound": {"peak_gbs": peaks["hbm_gbs"], "kernels": memory_bound,
                              "note": "algorithmic bytes per step / summed launch times, "
                                      "single-stream capture"} if memory_bound else None,
@@ -862,6 +948,9 @@ def run_ours(args):
 
 def main():
     args = parse()
+    if args.oracle_single_thread:
+        print(json.dumps(oracle_single_thread()), flush=True)
+        return 0
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)
