@@ -158,32 +158,27 @@ int np_for(int rmax) {           // MMA N covering hi + lo rows of the largest s
   return n <= 16 ? 16 : n <= 32 ? 32 : n <= 64 ? 64 : 128;
 }
 
-// Resident CTAs of the skinny tensor-core products: two per SM on the 152-SM part. A shape choice
-// only (any count is correct); it is a constant so that workspace sizes do not depend on the device.
-constexpr int64_t kLowRankSlots = 2 * 152;
+// Resident CTAs of the skinny tensor-core products: one per SM on the 152-SM part (each holds
+// about 192 KB of stages). A shape choice only (any count is correct).
+constexpr int64_t kLowRankSlots = 152;
 
-// K splits of the skinny token-row products: as many as keep every CTA resident in one wave.
+// K splits of the skinny token-row products (the CTAs of one cluster, a power of two that divides
+// the 128-token tile): as many as keep every CTA resident in one wave.
 int row_splits(int64_t T, int32_t n_seg, int64_t K) {
   const int64_t items = max_gemm_items(T, n_seg);
   int64_t s = kLowRankSlots / items;
   const int64_t nk = (K + 63) / 64;
   if (s > nk / 2) s = nk / 2;
   if (s > kMaxRowSplits) s = kMaxRowSplits;
-  return s < 1 ? 1 : (int)s;
+  int p2 = 1;
+  while (2 * p2 <= s) p2 *= 2;
+  return p2;
 }
 
-// 64-token blocks per reduction work item: as few items as fill the resident CTA slots over the
-// N tiles, but at least 4 blocks so that the per-item partial ([r, 256] fp32 per tile) stays small
-// next to the streamed input (256 tokens x 256 columns bf16 per tile).
-int red_span_blocks(int64_t T, int64_t N) {
-  const int64_t tiles = (N + 255) / 256;
-  int64_t items = kLowRankSlots / tiles;
-  if (items < 1) items = 1;
-  int64_t blocks = ((T + 63) / 64 + items - 1) / items;
-  if (blocks < 4) blocks = 4;
-  if (blocks > 64) blocks = 64;
-  return (int)blocks;
-}
+// 64-token blocks per reduction work item: short runs, so that the CTAs of a reduction cluster,
+// which split a slot's items evenly, get nearly equal token counts. The single-adapter form walks
+// the same runs over [0, T), so that one slot routed every token gives the same sums bit for bit.
+int red_span_blocks(int64_t, int64_t) { return kRedSpanBlocks; }
 
 int64_t red_items_bound(int64_t T, int32_t n_seg, int n_slots, int span) {
   const int64_t ns = n_seg < 1 ? 1 : n_seg;
@@ -210,13 +205,11 @@ struct Layout {
   uint16_t* Xd;        // [T, in] bf16 masked input (dropout)
   uint16_t* Sa;        // per slot [2 r, in] bf16 split of A
   uint16_t* Sb;        // per slot [2 r, out] bf16 split of B^T
-  float* rows_part;    // [splits][T][rmax]
   int64_t ldt;         // padded token stride of the transposed splits
   uint16_t* HsT;       // per slot [2 r, ldt] bf16
   uint16_t* GsT;       // per slot [2 r, ldt] bf16
   TokenItem* items_db; int32_t* count_db; int64_t max_db; int span_db;
   TokenItem* items_da; int32_t* count_da; int64_t max_da; int span_da;
-  float* red_part;     // [items][rmax][N]
   // FP8 frozen base
   uint8_t* Aq;         // [T, max(in, out)] E4M3 codes of X (forward) or dY' (backward)
   float* sq;           // [T] their row scales
@@ -278,7 +271,6 @@ Layout carve(const lora_desc* d, int64_t T, int32_t n_seg, int n_slots, int64_t 
   if (tc) {
     if (d->dropout_p > 0.f) L.Xd = c.take<uint16_t>((size_t)T * d->in_dim);
     L.Sa = c.take<uint16_t>((size_t)2 * rank_sum * d->in_dim);
-    L.rows_part = c.take<float>((size_t)kMaxRowSplits * T * d->rank);
   }
   if (backward) {
     L.Gs = c.take<float>((size_t)T * d->rank);
@@ -297,8 +289,6 @@ Layout carve(const lora_desc* d, int64_t T, int32_t n_seg, int n_slots, int64_t 
       L.count_db = c.take<int32_t>(LORA_MAX_SLOTS + 8);   // total, then per-slot item ranges
       L.items_da = c.take<TokenItem>((size_t)L.max_da);
       L.count_da = c.take<int32_t>(LORA_MAX_SLOTS + 8);
-      const int64_t a = L.max_db * d->out_dim, b = L.max_da * d->in_dim;
-      L.red_part = c.take<float>((size_t)(a > b ? a : b) * d->rank);
     } else {
       L.ritems = c.take<TokenItem>((size_t)L.rmax);
       L.rcount = c.take<int32_t>(4);
@@ -387,7 +377,6 @@ int tc_shrink(const lora_desc* d, const DropParams& dp, int64_t T, const void* X
   r.a = Xin; r.T = T; r.K = d->in_dim; r.n_slots = s.n;
   r.NP = np_for(d->rank);
   r.splits = row_splits(T, n_seg, d->in_dim);
-  r.part = L.rows_part;
   r.si = slot_info(s, q);
   r.out = H; r.ldo = d->rank;
   r.out2 = Hx; r.ld2 = L.ldx;   // routed calls: the slot-expanded copy for the frozen product
@@ -544,7 +533,6 @@ int run_backward_tc(const lora_desc* d, const DropParams& dp, int64_t T, const v
     r.a = dYp; r.T = T; r.K = d->out_dim; r.n_slots = s.n;
     r.NP = np_for(d->rank);
     r.splits = row_splits(T, n_seg, d->out_dim);
-    r.part = L.rows_part;
     r.si = si;
     r.out = L.Gs; r.ldo = d->rank;
     r.outT = L.GsT; r.ldt = L.ldt; r.outT_bytes = (size_t)2 * s.rank_sum * L.ldt * sizeof(uint16_t);
@@ -590,9 +578,8 @@ int run_backward_tc(const lora_desc* d, const DropParams& dp, int64_t T, const v
       rt.out[k] = s.dB[k];
     }
     a.n_slots = s.n; a.max_rank = d->rank; a.T = T; a.ldt = L.ldt;
-    a.b = dYp; a.N = d->out_dim; a.part = L.red_part; a.tab = rt; a.transposed = 1;
-    a.items = L.items_db; a.n_items = L.count_db; a.max_items = (int)L.max_db;
-    a.span_tokens = (int64_t)L.span_db * 64;
+    a.b = dYp; a.N = d->out_dim; a.tab = rt; a.transposed = 1;
+    a.items = L.items_db; a.n_items = L.count_db;
     LORA_TRY(launch_tc_red(a, st, LORA_PROF_RED_DB));
   }
   // dA_k += Gs^T Xd over the slot's tokens (GsT was written by the G product's finish)
@@ -604,9 +591,8 @@ int run_backward_tc(const lora_desc* d, const DropParams& dp, int64_t T, const v
       rt.out[k] = s.dA[k];
     }
     a.n_slots = s.n; a.max_rank = d->rank; a.T = T; a.ldt = L.ldt;
-    a.b = Xin; a.N = d->in_dim; a.part = L.red_part; a.tab = rt; a.transposed = 0;
-    a.items = L.items_da; a.n_items = L.count_da; a.max_items = (int)L.max_da;
-    a.span_tokens = (int64_t)L.span_da * 64;
+    a.b = Xin; a.N = d->in_dim; a.tab = rt; a.transposed = 0;
+    a.items = L.items_da; a.n_items = L.count_da;
     LORA_TRY(launch_tc_red(a, st, LORA_PROF_RED_DA));
   }
   if (dm) LORA_TRY(launch_dora_dm(d->dtype, dY, Y_save, dora_m, T, d->out_dim, dm, st));
@@ -793,7 +779,6 @@ int run_backward(const lora_desc* d, const DropParams& dp, int64_t T, const void
 // lo bf16 split of A), then ||W_o||^2 + 2 s H_o . B_o + s^2 B_o (A A^T) B_o^T per row.
 struct NormLayout {
   uint16_t* Sa;        // [2 r, in] bf16 split of A
-  float* part;         // [splits][out][r]
   float* H;            // [out, r]
   float* C;            // [r, r]
   size_t bytes;
@@ -804,7 +789,6 @@ NormLayout dora_norm_carve(const lora_desc* d, void* ws) {
   Carve c(ws);
   if (d->dtype == LORA_BF16) {
     L.Sa = c.take<uint16_t>((size_t)2 * d->rank * d->in_dim);
-    L.part = c.take<float>((size_t)kMaxRowSplits * d->out_dim * d->rank);
     L.H = c.take<float>((size_t)d->out_dim * d->rank);
     L.C = c.take<float>((size_t)d->rank * d->rank);
   }
@@ -827,7 +811,6 @@ cudaError_t run_dora_norm_tc(const lora_desc* d, const void* W, const float* A, 
   r.s[0] = L.Sa; r.rank[0] = d->rank;
   r.NP = np_for(d->rank);
   r.splits = row_splits(d->out_dim, -1, d->in_dim);
-  r.part = L.part;
   r.si.rank[0] = d->rank; r.si.alpha[0] = 1.f; r.si.region[0] = 0;
   r.out = L.H; r.ldo = d->rank;
   r.items = nullptr; r.n_items = nullptr;   // uniform 128-row tiles of W
@@ -1025,7 +1008,7 @@ int run_fused_forward(const lora_desc* d, const DropParams& dp, int64_t T, const
     a.s[0] = L.Sa; a.rank[0] = (int32_t)r;
     a.NP = np_for((int)r);
     a.splits = row_splits(T, -1, d->in_dim);
-    a.part = L.rows_part; a.si = si;
+    a.si = si;
     a.out = H + k * r; a.ldo = r; a.ld_out = ldh;
     a.items = nullptr; a.n_items = nullptr; a.max_items = (int)L.gmax;
     LORA_TRY(launch_tc_rows(a, st, LORA_PROF_SHRINK));
@@ -1089,7 +1072,7 @@ int run_fused_backward(const lora_desc* d, const DropParams& dp, int64_t T, cons
     g.s[0] = L.Sb; g.rank[0] = (int32_t)r;
     g.NP = np_for((int)r);
     g.splits = row_splits(T, -1, f.out[k]);
-    g.part = L.rows_part; g.si = si;
+    g.si = si;
     g.out = F.Gcat + k * r; g.ldo = r; g.ld_out = ldh;
     g.outT = L.GsT; g.ldt = L.ldt; g.outT_bytes = split_bytes;
     g.items = nullptr; g.n_items = nullptr; g.max_items = (int)L.gmax;
@@ -1097,11 +1080,10 @@ int run_fused_backward(const lora_desc* d, const DropParams& dp, int64_t T, cons
     // dA_k += Gs_k^T Xd
     TcRedArgs a{};
     a.st[0] = L.GsT; a.rank[0] = (int32_t)r; a.n_slots = 1; a.max_rank = (int32_t)r;
-    a.T = T; a.ldt = L.ldt; a.b = Xin; a.N = d->in_dim; a.part = L.red_part;
+    a.T = T; a.ldt = L.ldt; a.b = Xin; a.N = d->in_dim;
     rt.out[0] = f.dA[k];
     a.tab = rt; a.transposed = 0;
-    a.items = nullptr; a.n_items = nullptr; a.max_items = (int)L.max_da;
-    a.span_tokens = (int64_t)L.span_da * 64;
+    a.items = nullptr; a.n_items = nullptr;
     LORA_TRY(launch_tc_red(a, st, LORA_PROF_RED_DA));
     // dB_k += dY_k^T Hs_k
     LORA_TRY(launch_split_rows_t(H + k * r, ldh, r, L.ldt, nullptr, nullptr, (int)L.gmax, si,
@@ -1109,11 +1091,9 @@ int run_fused_backward(const lora_desc* d, const DropParams& dp, int64_t T, cons
     TcRedArgs b{};
     b.st[0] = L.HsT; b.rank[0] = (int32_t)r; b.n_slots = 1; b.max_rank = (int32_t)r;
     b.T = T; b.ldt = L.ldt; b.b = dYb + f.off[k]; b.ldb = d->out_dim; b.N = f.out[k];
-    b.part = L.red_part;
     rt.out[0] = f.dB[k];
     b.tab = rt; b.transposed = 1;
-    b.items = nullptr; b.n_items = nullptr; b.max_items = (int)L.max_db;
-    b.span_tokens = (int64_t)L.span_db * 64;
+    b.items = nullptr; b.n_items = nullptr;
     LORA_TRY(launch_tc_red(b, st, LORA_PROF_RED_DB));
   }
   // dX = dY_cat W_cat + (G_cat A_cat) * M: the projections' input gradients summed in one product

@@ -102,8 +102,7 @@ struct TcRowsArgs {                 // out[t, j] = alpha * (A[t, :] . (S_hi[j] +
   int32_t rank[LORA_MAX_SLOTS];
   int32_t n_slots;
   int32_t NP;                       // MMA N: 16, 32, 64 or 128 (>= 2 * max rank)
-  int32_t splits;                   // K splits
-  float* part;                      // [splits][T][ldo] scratch
+  int32_t splits;                   // K splits: CTAs of one cluster (1, 2, 4 or 8)
   SlotInfo si;
   float* out;                       // [T, ld_out] fp32 (columns < ldo written)
   int64_t ldo;                      // partial row stride (largest rank)
@@ -118,6 +117,7 @@ struct TcRowsArgs {                 // out[t, j] = alpha * (A[t, :] . (S_hi[j] +
   const int32_t* n_items;
   int max_items;
 };
+constexpr int kRedSpanBlocks = 2;   // 64-token blocks per reduction work item
 struct TcRedArgs {                  // dst_slot += (ST_hi + ST_lo)[., t] x B[t, .] over the slot's tokens
   const uint16_t* st[LORA_MAX_SLOTS];  // per slot [2 r, ldt] bf16 transposed split
   int32_t rank[LORA_MAX_SLOTS];
@@ -128,13 +128,10 @@ struct TcRedArgs {                  // dst_slot += (ST_hi + ST_lo)[., t] x B[t, 
   const void* b;                    // [T, N] bf16 (dY' or Xd), row stride ldb
   int64_t N;
   int64_t ldb;                      // 0: N
-  float* part;                      // [items][max_rank][N] scratch
   ReduceTab tab;
   int32_t transposed;               // 1: dst is [N, r] (dB); 0: dst is [r, N] (dA)
-  const TokenItem* items;           // 64-token aligned runs (launch_make_red_items_tc)
-  const int32_t* n_items;
-  int max_items;
-  int64_t span_tokens;              // tokens per uniform item when items is null (single adapter)
+  const TokenItem* items;           // 64-token aligned runs grouped by slot
+  const int32_t* n_items;           //   (launch_make_red_items_tc); null: slot 0 over all T
 };
 struct SplitTab {
   const float* src[LORA_MAX_SLOTS];

@@ -44,11 +44,16 @@ struct RowsParams {
   const TokenItem* items;
   const int32_t* n_items;
   uint32_t* err;
-  int32_t rank[LORA_MAX_SLOTS];
+  SlotInfo si;
   int32_t nk;                        // K blocks in total
   int32_t nk_per_split;
-  int32_t ldp;                       // partial row stride (largest rank)
-  float* part;                       // [splits][T][ldp]
+  int32_t ncols;                     // columns of out written per token (zeros past the rank)
+  float* out;                        // [T, ld_out] (nullable)
+  int64_t ld_out;
+  float* out2;                       // slot-expanded copy [T, ld2] (nullable)
+  int64_t ld2;
+  uint16_t* outT;                    // per slot [2 r, ldt] transposed bf16 split (nullable)
+  int64_t ldt;
   int64_t T;
 };
 
@@ -56,41 +61,55 @@ template <int NP>
 struct RowsCfg {
   static constexpr int kBBytes = NP * 128;
   static constexpr int kStageBytes = 16384 + kBBytes;
-  // about 100 KB of stages, so that two CTAs fit one SM
-  static constexpr int kStages = (100 * 1024 / kStageBytes) < 8 ? (100 * 1024 / kStageBytes) : 8;
+  // one CTA per SM with about 192 KB of stages in flight
+  static constexpr int kStages = (192 * 1024 / kStageBytes) < 10 ? (192 * 1024 / kStageBytes) : 10;
   static constexpr int kSmem = kStages * kStageBytes + 1024 + 1024;
-  static constexpr int kLdb = NP + 4;   // staging row stride of the epilogue (floats)
+  static constexpr int kLdb = NP + 4;   // staging row stride of the partial tile (floats)
   static_assert(kStages >= 2, "pipeline depth");
-  static_assert(kBM * kLdb * 4 <= kStages * kStageBytes, "epilogue staging fits the stages");
+  static_assert(kBM * kLdb * 4 <= kStages * kStageBytes, "partial tile fits the stages");
   static constexpr uint32_t kCols = NP < 32 ? 32u : (uint32_t)NP;
   static constexpr uint32_t kIdesc = idesc(kFmtBF16, kBM, NP);
 };
 
+// One work item (<= 128 tokens, one slot) per cluster of `splits` CTAs along y; CTA z multiplies
+// the item's rows by its share of the K-blocks into TMEM and leaves the partial tile (hi and lo
+// columns added) in its shared memory. The cluster then adds the partials in split order through
+// distributed shared memory (reruns are bitwise equal): CTA z finishes token rows
+// [z R, z R + R), R = 128 / splits, scales them by the slot's alpha and writes out, the
+// slot-expanded copy and the transposed bf16 split (no partials reach global memory).
 template <int NP>
-__global__ void __launch_bounds__(kThreads, 2) k_tc_rows(const __grid_constant__ RowsParams p) {
+__global__ void __launch_bounds__(kThreads, 1) k_tc_rows(const __grid_constant__ RowsParams p) {
   grid_dep_sync();
   using C = RowsCfg<NP>;
   extern __shared__ uint8_t smem_raw[];
   TokenItem it;
-  if (!get_item(p.items, p.n_items, blockIdx.x, p.T, it)) return;
-  const int z = blockIdx.y;
-  const int kb0 = z * p.nk_per_split;
-  const int kb1 = min(p.nk, kb0 + p.nk_per_split);
-  float* part = p.part + (int64_t)z * p.T * p.ldp;
+  if (!get_item(p.items, p.n_items, blockIdx.x, p.T, it)) return;   // the same for the cluster
+  const int z = blockIdx.y;   // == rank in the cluster (cluster dims 1 x splits)
+  const int splits = gridDim.y;
+  const int R = kBM / splits;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (it.slot < 0 || kb0 >= kb1) {
-    // no adapter for these tokens (or an empty split): the partial rows are zero
-    float4* dst = reinterpret_cast<float4*>(part + (int64_t)it.t0 * p.ldp);
-    const int n4 = (it.t1 - it.t0) * (p.ldp / 4);
-    for (int e = threadIdx.x; e < n4; e += kThreads) dst[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (it.slot < 0) {
+    // no adapter for these tokens: their rows of out are zero (the same for the whole cluster)
+    if (p.out) {
+      const int c4n = p.ncols / 4;
+      for (int e = threadIdx.x; e < R * c4n; e += kThreads) {
+        const int64_t t = (int64_t)it.t0 + z * R + e / c4n;
+        if (t < it.t1)
+          reinterpret_cast<float4*>(p.out + t * p.ld_out)[e % c4n] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
     return;
   }
-  const int nk = kb1 - kb0;
+  const int r = p.si.rank[it.slot];
+  const int kb0 = z * p.nk_per_split;
+  const int kb1 = min(p.nk, kb0 + p.nk_per_split);
+  const int nk = kb1 > kb0 ? kb1 - kb0 : 0;
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(base + C::kStages * C::kStageBytes);
   uint64_t* empty_bar = full_bar + C::kStages;
   uint64_t* acc_bar = empty_bar + C::kStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_bar + 1);
+  float* buf = reinterpret_cast<float*>(base);   // partial tile [128][kLdb], over the idle stages
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full_bar[s], 1);
@@ -106,6 +125,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_tc_rows(const __grid_constant__
   fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  bool ready = true;
   if (warp == 0) {
     if (lane == 0) {
       int issued = 0;
@@ -119,6 +139,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_tc_rows(const __grid_constant__
         tma_load_2d(sa + 16384, &p.ts[it.slot], &full_bar[s], (kb0 + i) * 64, 0);
         issued = i + 1;
       }
+      // every issued load has landed before the stages are reused as the partial tile
       for (int i = (issued > C::kStages ? issued - C::kStages : 0); i < issued; ++i)
         if (!mbar_wait(&full_bar[i % C::kStages], (uint32_t)(i / C::kStages) & 1u, 1u, p.err)) break;
     }
@@ -135,47 +156,77 @@ __global__ void __launch_bounds__(kThreads, 2) k_tc_rows(const __grid_constant__
           umma_f16(tmem, da + 2 * k, db + 2 * k, C::kIdesc, (i > 0 || k > 0) ? 1u : 0u);
         umma_commit(&empty_bar[s]);
       }
-      umma_commit(acc_bar);
+      if (nk > 0) umma_commit(acc_bar);   // with no K-blocks the epilogue does not wait
     }
   } else {
-    // epilogue: the accumulator rows go through shared memory (the stages are idle once acc_bar
-    // has fired), then hi + lo columns are added and the item's [n, ldp] partial block, which is
-    // contiguous in memory, is written with coalesced float4 stores
+    // epilogue: this thread's accumulator row (one token) -> its staging row, then hi + lo
     const int q = warp & 3;
     const int row = q * 32 + lane;
-    float* buf = reinterpret_cast<float*>(base);
-    const bool ready = __all_sync(0xffffffffu, mbar_wait(acc_bar, 0u, 4u, p.err));
-    if (ready) {
-      fence_after();
+    ready = nk == 0 || __all_sync(0xffffffffu, mbar_wait(acc_bar, 0u, 4u, p.err));
+    if (ready) fence_after();
+    float* br = buf + row * C::kLdb;
+    if (ready && nk > 0) {
 #pragma unroll
       for (int c = 0; c < NP / 16; ++c) {
         float v[16];
         tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * 16), v);
-        float4* dst = reinterpret_cast<float4*>(buf + row * C::kLdb + c * 16);
+        float4* dst = reinterpret_cast<float4*>(br + c * 16);
 #pragma unroll
         for (int g = 0; g < 4; ++g) dst[g] = make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
       }
+      for (int j = 0; j < r; j += 4) {
+        const float4 h = *reinterpret_cast<const float4*>(br + j);
+        const float4 l = *reinterpret_cast<const float4*>(br + r + j);
+        *reinterpret_cast<float4*>(br + j) = make_float4(h.x + l.x, h.y + l.y, h.z + l.z, h.w + l.w);
+      }
+    } else {
+      for (int j = 0; j < r; j += 4) *reinterpret_cast<float4*>(br + j) = make_float4(0.f, 0.f, 0.f, 0.f);
     }
     fence_before();
-    asm volatile("bar.sync 1, 128;" ::: "memory");   // the four epilogue warps
-    if (ready) {
-      const int r = p.rank[it.slot];
-      const int r4 = r / 4, l4 = p.ldp / 4;
-      const int n4 = (it.t1 - it.t0) * l4;
-      float4* dst = reinterpret_cast<float4*>(part + (int64_t)it.t0 * p.ldp);
-      for (int e = threadIdx.x - 64; e < n4; e += 128) {
-        const int i = e / l4, c = e - i * l4;
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (c < r4) {
-          const float4 h = *reinterpret_cast<const float4*>(buf + i * C::kLdb + 4 * c);
-          const float4 l = *reinterpret_cast<const float4*>(buf + i * C::kLdb + r + 4 * c);
-          v = make_float4(h.x + l.x, h.y + l.y, h.z + l.z, h.w + l.w);
-        }
-        dst[e] = v;
-      }
-    }
   }
   __syncthreads();
+  cluster_sync_all();   // every CTA's partial tile is in its shared memory
+  // CTA z: token rows [z R, z R + R) summed over the splits in split order
+  const float alpha = p.si.alpha[it.slot];
+  const int r4 = r / 4, c4n = p.ncols / 4;
+  for (int e = threadIdx.x; e < R * c4n; e += kThreads) {
+    const int i = z * R + e / c4n, c = e - (e / c4n) * c4n;
+    const int64_t t = (int64_t)it.t0 + i;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (c < r4) {
+      float4 pz[8];
+#pragma unroll
+      for (int zz = 0; zz < 8; ++zz)
+        if (zz < splits) pz[zz] = dsmem_ld4(buf + i * C::kLdb + 4 * c, (uint32_t)zz);
+#pragma unroll
+      for (int zz = 0; zz < 8; ++zz)
+        if (zz < splits) {
+          v.x += pz[zz].x; v.y += pz[zz].y; v.z += pz[zz].z; v.w += pz[zz].w;
+        }
+      v = make_float4(v.x * alpha, v.y * alpha, v.z * alpha, v.w * alpha);
+    }
+    if (t < it.t1) {
+      if (p.out) reinterpret_cast<float4*>(p.out + t * p.ld_out)[c] = v;
+      if (p.out2 && c < r4) reinterpret_cast<float4*>(p.out2 + t * p.ld2 + p.si.pcol[it.slot])[c] = v;
+    }
+    // the finished values, for the transposed split below: only this CTA reads rows
+    // [z R, z R + R) of its own tile, and each element is rewritten by the thread that read it
+    if (c < r4) *reinterpret_cast<float4*>(buf + i * C::kLdb + 4 * c) = v;
+  }
+  if (p.outT) {
+    __syncthreads();
+    const int64_t tb = (int64_t)it.t0 + z * R;
+    const int nt = (int)max((int64_t)0, min((int64_t)R, (int64_t)it.t1 - tb));
+    uint16_t* d = p.outT + (int64_t)p.si.region[it.slot] * p.ldt + tb;
+    for (int e = threadIdx.x; e < nt * r; e += kThreads) {
+      const int j = e / nt, i = e - j * nt;
+      const float x = buf[(z * R + i) * C::kLdb + j];
+      const uint16_t hb = bf16_bits(x);
+      d[(int64_t)j * p.ldt + i] = hb;
+      d[(int64_t)(r + j) * p.ldt + i] = bf16_bits(x - bf16_val(hb));
+    }
+  }
+  cluster_sync_all();   // peers' shared memory stays alive until every CTA has read it
   if (warp == 1) {
     fence_after();
     tmem_dealloc(tmem, C::kCols);
@@ -264,42 +315,87 @@ __global__ void __launch_bounds__(kFinishThreads) k_rows_finish(
 struct RedParams {
   CUtensorMap tst[LORA_MAX_SLOTS];   // ST_slot [2 r, T] bf16 (tokens contiguous), box {64, 128}
   CUtensorMap tb;                    // B [T, N] bf16, box {64 (n), 64 (t)}
-  const TokenItem* items;
-  const int32_t* n_items;
+  const TokenItem* items;            // 64-token aligned runs grouped by slot (null: the uniform
+                                     // runs of kRedSpanBlocks blocks over [0, T), slot 0)
+  const int32_t* counts;             // counts[1 + slot] .. counts[2 + slot]: the slot's items
   uint32_t* err;
   int32_t rank[LORA_MAX_SLOTS];
-  int32_t rstride;                   // partial rows per item (largest rank)
-  float* part;                       // [items][rstride][N]
+  float* dst[LORA_MAX_SLOTS];        // dB_slot [N, r] (transposed) or dA_slot [r, N]
+  int32_t transposed;
   int64_t N;
   int64_t T;
-  int64_t span;                      // tokens per uniform item (null item table)
 };
 
-constexpr int kRedBN = 256;
-constexpr int kRedStageBytes = 16384 + 32768;
-constexpr int kRedStages = 2;       // about 100 KB of stages, so that two CTAs fit one SM
-constexpr int kRedSmem = kRedStages * kRedStageBytes + 1024 + 1024;
-constexpr int kRedHalf = kRedBN / 2;   // epilogue columns staged per pass
-constexpr int kRedLdb = kRedHalf + 4;
-static_assert(kBM * kRedLdb * 4 <= kRedStages * kRedStageBytes, "epilogue staging fits the stages");
-constexpr uint32_t kRedIdesc = idesc(kFmtBF16, kBM, kRedBN, false, true);
+// Tile: M = 128 split rows (2 r used), N = BN columns of B (256 or 128), K = 64 tokens per stage;
+// one CTA per SM with about 192 KB of stages in flight.
+template <int BN>
+struct RedCfg {
+  static constexpr int kStageBytes = 16384 + BN * 128;
+  static constexpr int kStages = (192 * 1024) / kStageBytes;
+  static constexpr int kSmem = kStages * kStageBytes + 1024 + 1024;
+  static constexpr int kLdA = BN + 4;                 // staging [r][kLdA] (dA)
+  static constexpr int kLdB = LORA_MAX_RANK + 4;      // staging [BN][kLdB] (dB, transposed)
+  static_assert(LORA_MAX_RANK * kLdA * 4 <= kStages * kStageBytes, "dA staging fits");
+  static_assert(BN * kLdB * 4 <= kStages * kStageBytes, "dB staging fits");
+  static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
+  static constexpr uint32_t kIdesc = idesc(kFmtBF16, kBM, BN, false, true);
+};
+constexpr int kRedMaxSplits = 16;
 
-__global__ void __launch_bounds__(kThreads, 2) k_tc_red(const __grid_constant__ RedParams p) {
+// dst_slot += (ST_hi + ST_lo) Bmn over the slot's tokens, for one BN-column tile of B.
+// A cluster of `splits` CTAs along y shares the tile; CTA z accumulates its share of the slot's
+// 64-token blocks in TMEM (M = 2 r split rows, N = BN columns, K = tokens) and leaves its partial
+// (hi and lo rows added) in shared memory; the cluster then adds the partials in split order
+// through distributed shared memory (reruns are bitwise equal) and CTA z adds columns
+// [z W, z W + W), W = BN / splits, into dst. No partials reach global memory.
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1) k_tc_red(const __grid_constant__ RedParams p) {
   grid_dep_sync();
+  using C = RedCfg<BN>;
+  constexpr int kRedStages = C::kStages;
+  constexpr int kRedStageBytes = C::kStageBytes;
+  constexpr int kRedLdA = C::kLdA;
+  constexpr int kRedLdB = C::kLdB;
+  constexpr int kRedBN = BN;
   extern __shared__ uint8_t smem_raw[];
-  const int item = blockIdx.y;
-  TokenItem it;
-  if (!get_span_item(p.items, p.n_items, item, p.T, p.span, it)) return;
-  if (it.slot < 0) return;
-  const int32_t n0 = blockIdx.x * kRedBN;
-  const int32_t tb0 = it.t0 & ~63;                  // 64-token blocks covering [t0, t1)
-  const int nk = (it.t1 - tb0 + 63) / 64;
+  const int slot = blockIdx.z;
+  const int z = blockIdx.y;   // == rank in the cluster (cluster dims 1 x splits)
+  const int splits = gridDim.y;
+  const int32_t n0 = blockIdx.x * BN;
+  const int r = p.rank[slot];
+  // this CTA's work: items [w0, w1) of the slot's items, split evenly over the cluster (the
+  // uniform runs of a single-adapter call are the items of one segment covering [0, T))
+  const int32_t nb_all = (int32_t)((p.T + 63) / 64);
+  int32_t ia = 0, ib = (nb_all + kRedSpanBlocks - 1) / kRedSpanBlocks;
+  if (p.items) {
+    ia = p.counts[1 + slot];
+    ib = p.counts[2 + slot];
+  }
+  const int32_t w0 = ia + (int32_t)((int64_t)(ib - ia) * z / splits);
+  const int32_t w1 = ia + (int32_t)((int64_t)(ib - ia) * (z + 1) / splits);
+  auto blocks_of = [&](int32_t w, int32_t& tb0, int32_t& nblk) {
+    if (p.items) {
+      const TokenItem it = p.items[w];
+      tb0 = it.t0 & ~63;
+      nblk = (it.t1 - tb0 + 63) / 64;
+    } else {
+      tb0 = w * kRedSpanBlocks * 64;
+      nblk = min(kRedSpanBlocks, nb_all - w * kRedSpanBlocks);
+    }
+  };
+  int nk = 0;
+  for (int32_t w = w0; w < w1; ++w) {
+    int32_t tb0, nb;
+    blocks_of(w, tb0, nb);
+    nk += nb;
+  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(base + kRedStages * kRedStageBytes);
   uint64_t* empty_bar = full_bar + kRedStages;
   uint64_t* acc_bar = empty_bar + kRedStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_bar + 1);
+  float* buf = reinterpret_cast<float*>(base);   // staging over the idle stages
   if (threadIdx.x == 0) {
     for (int s = 0; s < kRedStages; ++s) {
       mbar_init(&full_bar[s], 1);
@@ -309,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_tc_red(const __grid_constant__ 
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
-  if (warp == 1) tmem_alloc(tmem_slot, 256u);
+  if (warp == 1) tmem_alloc(tmem_slot, (uint32_t)BN);
   fence_before();
   __syncthreads();
   fence_after();
@@ -317,21 +413,27 @@ __global__ void __launch_bounds__(kThreads, 2) k_tc_red(const __grid_constant__ 
 
   if (warp == 0) {
     if (lane == 0) {
-      int issued = 0;
-      for (int i = 0; i < nk; ++i) {
-        const int s = i % kRedStages;
-        const uint32_t ph = (uint32_t)(i / kRedStages) & 1u;
-        if (i >= kRedStages && !mbar_wait(&empty_bar[s], ph ^ 1u, 1u, p.err)) break;
-        uint8_t* sa = base + s * kRedStageBytes;
-        mbar_expect_tx(&full_bar[s], kRedStageBytes);
-        const int32_t t = tb0 + i * 64;
-        tma_load_2d(sa, &p.tst[it.slot], &full_bar[s], t, 0);
+      int i = 0;
+      bool ok = true;
+      for (int32_t w = w0; w < w1 && ok; ++w) {
+        int32_t tb0, nb;
+        blocks_of(w, tb0, nb);
+        for (int b = 0; b < nb; ++b, ++i) {
+          const int s = i % kRedStages;
+          const uint32_t ph = (uint32_t)(i / kRedStages) & 1u;
+          if (i >= kRedStages && !mbar_wait(&empty_bar[s], ph ^ 1u, 1u, p.err)) { ok = false; break; }
+          uint8_t* sa = base + s * kRedStageBytes;
+          mbar_expect_tx(&full_bar[s], kRedStageBytes);
+          const int32_t t = tb0 + b * 64;
+          tma_load_2d(sa, &p.tst[slot], &full_bar[s], t, 0);
 #pragma unroll
-        for (int b = 0; b < 4; ++b) tma_load_2d(sa + 16384 + b * 8192, &p.tb, &full_bar[s], n0 + 64 * b, t);
-        issued = i + 1;
+          for (int q = 0; q < BN / 64; ++q)
+            tma_load_2d(sa + 16384 + q * 8192, &p.tb, &full_bar[s], n0 + 64 * q, t);
+        }
       }
-      for (int i = (issued > kRedStages ? issued - kRedStages : 0); i < issued; ++i)
-        if (!mbar_wait(&full_bar[i % kRedStages], (uint32_t)(i / kRedStages) & 1u, 1u, p.err)) break;
+      // every issued load has landed before the stages are reused as the staging tile
+      for (int k = (i > kRedStages ? i - kRedStages : 0); k < i; ++k)
+        if (!mbar_wait(&full_bar[k % kRedStages], (uint32_t)(k / kRedStages) & 1u, 1u, p.err)) break;
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -345,148 +447,109 @@ __global__ void __launch_bounds__(kThreads, 2) k_tc_red(const __grid_constant__ 
         // K step of 16 tokens: +32 bytes in the K-major A rows, +2 KB (two 8-row atoms) in B
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          umma_f16(tmem, da + 2 * k, db + 128 * k, kRedIdesc, (i > 0 || k > 0) ? 1u : 0u);
+          umma_f16(tmem, da + 2 * k, db + 128 * k, C::kIdesc, (i > 0 || k > 0) ? 1u : 0u);
         umma_commit(&empty_bar[s]);
       }
-      umma_commit(acc_bar);
+      if (nk > 0) umma_commit(acc_bar);   // with no K-blocks the epilogue does not wait
     }
   } else {
-    // epilogue, in two passes of 128 columns: the accumulator rows go through shared memory (the
-    // stages are idle once acc_bar has fired), then row j (hi) and row r + j (lo) are added and
-    // written along n with coalesced float4 stores
+    // epilogue: accumulator row `row` is split row j = row (hi, row < r) or j = row - r (lo,
+    // r <= row < 2 r); hi rows are staged first, then lo rows are added onto them.
+    // dA stages [j][n] (rows along dst's rows), dB stages [n][j] (dst is [N, r]).
     const int q = warp & 3;
     const int row = q * 32 + lane;
-    const int r = p.rank[it.slot];
-    float* buf = reinterpret_cast<float*>(base);
-    float* part = p.part + (int64_t)item * p.rstride * p.N;
-    const bool ready = __all_sync(0xffffffffu, mbar_wait(acc_bar, 0u, 4u, p.err));
+    const bool ready = nk == 0 || __all_sync(0xffffffffu, mbar_wait(acc_bar, 0u, 4u, p.err));
     if (ready) fence_after();
-    for (int h = 0; h < kRedBN / kRedHalf; ++h) {
-      if (ready) {
+    const bool live = ready && nk > 0;
+    for (int phase = 0; phase < 2; ++phase) {
+      const bool mine = phase == 0 ? row < r : (row >= r && row < 2 * r);
+      const int j = phase == 0 ? row : row - r;
+#pragma unroll 1
+      for (int c = 0; c < kRedBN / 32; ++c) {
+        float v[32];
+        if (live) {
+          tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * 32), v);
+        } else {
 #pragma unroll
-        for (int c = 0; c < kRedHalf / 32; ++c) {
-          float v[32];
-          tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * kRedHalf + c * 32), v);
-          float4* dst = reinterpret_cast<float4*>(buf + row * kRedLdb + c * 32);
-#pragma unroll
-          for (int g = 0; g < 8; ++g) dst[g] = make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+          for (int k = 0; k < 32; ++k) v[k] = 0.f;
         }
-      }
-      asm volatile("bar.sync 1, 128;" ::: "memory");
-      if (ready) {
-        constexpr int kC4 = kRedHalf / 4;
-        for (int e = threadIdx.x - 64; e < r * kC4; e += 128) {
-          const int j = e / kC4, c = e - j * kC4;
-          const int64_t nb = (int64_t)n0 + h * kRedHalf + 4 * c;
-          if (nb + 4 <= p.N) {
-            const float4 hi = *reinterpret_cast<const float4*>(buf + j * kRedLdb + 4 * c);
-            const float4 lo = *reinterpret_cast<const float4*>(buf + (r + j) * kRedLdb + 4 * c);
-            *reinterpret_cast<float4*>(part + (int64_t)j * p.N + nb) =
-                make_float4(hi.x + lo.x, hi.y + lo.y, hi.z + lo.z, hi.w + lo.w);
+        if (!mine) continue;
+        if (!p.transposed) {
+          float* d = buf + j * kRedLdA + c * 32;
+#pragma unroll
+          for (int g = 0; g < 8; ++g) {
+            float4 x = make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+            if (phase == 1) {
+              const float4 h = reinterpret_cast<const float4*>(d)[g];
+              x = make_float4(h.x + x.x, h.y + x.y, h.z + x.z, h.w + x.w);
+            }
+            reinterpret_cast<float4*>(d)[g] = x;
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            float* d = buf + (c * 32 + k) * kRedLdB + j;
+            *d = phase == 0 ? v[k] : *d + v[k];
           }
         }
       }
-      asm volatile("bar.sync 1, 128;" ::: "memory");   // the staging rows are reused next pass
+      asm volatile("bar.sync 1, 128;" ::: "memory");   // the four epilogue warps
     }
     fence_before();
   }
   __syncthreads();
+  cluster_sync_all();   // every CTA's partial tile is in its shared memory
+  const int W = kRedBN / splits;
+  float* dst = p.dst[slot];
+  if (!p.transposed) {
+    // dA [r, N]: rows j, columns n0 + z W ..
+    const int w4 = W / 4;
+    for (int e = threadIdx.x; e < r * w4; e += kThreads) {
+      const int j = e / w4, c = z * W + 4 * (e - (e / w4) * w4);
+      const int64_t n = (int64_t)n0 + c;
+      if (n >= p.N) continue;
+      float4 pz[kRedMaxSplits];
+#pragma unroll
+      for (int zz = 0; zz < kRedMaxSplits; ++zz)
+        if (zz < splits) pz[zz] = dsmem_ld4(buf + j * kRedLdA + c, (uint32_t)zz);
+      float4* o = reinterpret_cast<float4*>(dst + (int64_t)j * p.N + n);
+      float4 acc = *o;
+      float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int zz = 0; zz < kRedMaxSplits; ++zz)
+        if (zz < splits) {
+          sum.x += pz[zz].x; sum.y += pz[zz].y; sum.z += pz[zz].z; sum.w += pz[zz].w;
+        }
+      acc.x += sum.x; acc.y += sum.y; acc.z += sum.z; acc.w += sum.w;
+      *o = acc;
+    }
+  } else {
+    // dB [N, r]: rows n0 + z W .., columns j
+    const int r4 = r / 4;
+    for (int e = threadIdx.x; e < W * r4; e += kThreads) {
+      const int c = z * W + e / r4, j = 4 * (e - (e / r4) * r4);
+      const int64_t n = (int64_t)n0 + c;
+      if (n >= p.N) continue;
+      float4 pz[kRedMaxSplits];
+#pragma unroll
+      for (int zz = 0; zz < kRedMaxSplits; ++zz)
+        if (zz < splits) pz[zz] = dsmem_ld4(buf + c * kRedLdB + j, (uint32_t)zz);
+      float4* o = reinterpret_cast<float4*>(dst + n * r + j);
+      float4 acc = *o;
+      float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int zz = 0; zz < kRedMaxSplits; ++zz)
+        if (zz < splits) {
+          sum.x += pz[zz].x; sum.y += pz[zz].y; sum.z += pz[zz].z; sum.w += pz[zz].w;
+        }
+      acc.x += sum.x; acc.y += sum.y; acc.z += sum.z; acc.w += sum.w;
+      *o = acc;
+    }
+  }
+  cluster_sync_all();   // peers' shared memory stays alive until every CTA has read it
   if (warp == 1) {
     fence_after();
-    tmem_dealloc(tmem, 256u);
-  }
-}
-
-// dst_slot += sum over the slot's items (in item order) of their partial rows:
-// transposed == 0: dst[j * N + n] (dA [r, N]); transposed == 1: dst[n * r + j] (dB [N, r]).
-// The slot's items are contiguous in the table, from counts[1 + slot] to counts[2 + slot] (a null
-// table is the uniform runs of a single-adapter call, all of slot 0). CTA (blockIdx.x, slot)
-// covers kRedFinCols columns; each thread holds kRedFinVec float4 groups and loads four items'
-// partials before adding them.
-constexpr int kRedFinCols = 32;
-constexpr int kRedFinC4 = kRedFinCols / 4;
-constexpr int kRedFinVec = LORA_MAX_RANK * kRedFinC4 / kFinishThreads;
-__global__ void __launch_bounds__(kFinishThreads) k_red_finish(
-    const float* __restrict__ part, const TokenItem* __restrict__ items,
-    const int32_t* __restrict__ counts, int64_t N, int32_t rstride, int transposed,
-    const ReduceTab tab, int64_t T, int64_t span) {
-  grid_dep_sync();
-  __shared__ float tile[kRedFinCols][LORA_MAX_RANK + 1];
-  const int slot = blockIdx.y;
-  const int32_t r = tab.rank[slot];
-  float* dst = tab.out[slot];
-  int32_t i0 = 0, i1 = 0;
-  if (items) {
-    i0 = counts[1 + slot];
-    i1 = counts[2 + slot];
-  } else if (slot == 0) {
-    i1 = (int32_t)((T + span - 1) / span);
-  }
-  if (i1 <= i0) return;
-  const int64_t n0 = (int64_t)blockIdx.x * kRedFinCols;
-  const int nc = (int)min((int64_t)kRedFinCols, N - n0);
-  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
-  float4 acc[kRedFinVec];
-  int64_t off[kRedFinVec];
-  bool live[kRedFinVec];
-#pragma unroll
-  for (int u = 0; u < kRedFinVec; ++u) {
-    const int q = threadIdx.x + u * kFinishThreads;
-    const int j = q / kRedFinC4, c = q - j * kRedFinC4;
-    live[u] = j < r && 4 * c < nc;
-    off[u] = (int64_t)j * N + n0 + 4 * c;
-    acc[u] = zero;
-  }
-  const int64_t istride = (int64_t)rstride * N;
-  for (int32_t i = i0; i < i1; i += 4) {
-    float4 v[4][kRedFinVec];
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-#pragma unroll
-      for (int u = 0; u < kRedFinVec; ++u)
-        v[k][u] = (live[u] && i + k < i1)
-                      ? *reinterpret_cast<const float4*>(part + (int64_t)(i + k) * istride + off[u])
-                      : zero;
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-#pragma unroll
-      for (int u = 0; u < kRedFinVec; ++u)
-        if (i + k < i1) {
-          acc[u].x += v[k][u].x;
-          acc[u].y += v[k][u].y;
-          acc[u].z += v[k][u].z;
-          acc[u].w += v[k][u].w;
-        }
-  }
-  if (!transposed) {
-#pragma unroll
-    for (int u = 0; u < kRedFinVec; ++u) {
-      if (!live[u]) continue;
-      float4* p = reinterpret_cast<float4*>(dst + off[u]);
-      float4 d = *p;
-      d.x += acc[u].x;
-      d.y += acc[u].y;
-      d.z += acc[u].z;
-      d.w += acc[u].w;
-      *p = d;
-    }
-    return;
-  }
-  // dB [N, r]: through shared memory so that the row-major writes are coalesced
-#pragma unroll
-  for (int u = 0; u < kRedFinVec; ++u) {
-    if (!live[u]) continue;
-    const int q = threadIdx.x + u * kFinishThreads;
-    const int j = q / kRedFinC4, c = q - j * kRedFinC4;
-    tile[4 * c][j] = acc[u].x;
-    tile[4 * c + 1][j] = acc[u].y;
-    tile[4 * c + 2][j] = acc[u].z;
-    tile[4 * c + 3][j] = acc[u].w;
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e < nc * r; e += kFinishThreads) {
-    const int n = e / r, j = e - n * r;
-    dst[(n0 + n) * r + j] += tile[n][j];
+    tmem_dealloc(tmem, (uint32_t)BN);
   }
 }
 
@@ -609,6 +672,24 @@ cudaError_t set_smem(K kernel, int bytes) {
 }  // namespace
 
 // ---------------------------------------------------------------------------------------------
+template <typename... KArgs, typename... Args>
+cudaError_t launch_cluster_y(void (*kernel)(KArgs...), dim3 grid, int cluster_y, int smem,
+                             cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = (unsigned)cluster_y;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = add_pdl_attr(attr, 1);
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 cudaError_t launch_tc_rows(const TcRowsArgs& a, cudaStream_t st, int prof_kind) {
   static RowsParams prm;
   static std::mutex mu;
@@ -622,35 +703,47 @@ cudaError_t launch_tc_rows(const TcRowsArgs& a, cudaStream_t st, int prof_kind) 
     if (!tc::make_map_2d(&prm.ts[k], a.s[k], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.K,
                          2 * (uint64_t)a.rank[k], a.K, 64, (uint32_t)NP))
       return cudaErrorInvalidValue;
-  for (int k = 0; k < a.n_slots; ++k) {
-    if (2 * a.rank[k] > NP || a.rank[k] > a.ldo || a.rank[k] % 4) return cudaErrorInvalidValue;
-    prm.rank[k] = a.rank[k];
-  }
-  if (a.splits < 1 || a.splits > kMaxSplitsRows || a.ldo % 4 || a.ldo > LORA_MAX_RANK)
+  for (int k = 0; k < a.n_slots; ++k)
+    if (2 * a.rank[k] > NP || a.rank[k] > a.ldo || a.rank[k] % 4 || a.si.rank[k] != a.rank[k])
+      return cudaErrorInvalidValue;
+  // the cluster splits the 128 token rows evenly: 1, 2, 4 or 8 CTAs
+  if (a.splits < 1 || a.splits > kMaxSplitsRows || (a.splits & (a.splits - 1)) || a.ldo % 4 ||
+      a.ldo > LORA_MAX_RANK)
     return cudaErrorInvalidValue;
   prm.items = a.items;
   prm.n_items = a.n_items;
   prm.err = tc::error_word();
   if (!prm.err) return cudaErrorInvalidDevice;
+  prm.si = a.si;
   prm.nk = (int32_t)((a.K + 63) / 64);
   prm.nk_per_split = (prm.nk + a.splits - 1) / a.splits;
-  prm.ldp = (int32_t)a.ldo;
-  prm.part = a.part;
+  prm.ncols = (int32_t)a.ldo;
+  prm.out = a.out;
+  prm.ld_out = a.ld_out > 0 ? a.ld_out : a.ldo;
+  prm.out2 = a.out2;
+  prm.ld2 = a.ld2;
+  prm.outT = a.outT;
+  prm.ldt = a.ldt;
   prm.T = a.T;
+  if (a.max_items <= 0) return cudaSuccess;
+  if (a.outT && a.items) {   // tokens of other slots read as zero in each slot's rows
+    cudaError_t e = cudaMemsetAsync(a.outT, 0, a.outT_bytes, st);
+    if (e != cudaSuccess) return e;
+  }
   dim3 grid((unsigned)a.max_items, (unsigned)a.splits);
   cudaError_t e = cudaSuccess;
   prof_begin(prof_kind, st);
   switch (NP) {
-#define LORA_ROWS_CASE(NPV)                                                        \
-  case NPV: {                                                                      \
-    static bool attr = false;                                                      \
-    if (!attr) {                                                                   \
-      e = set_smem(k_tc_rows<NPV>, RowsCfg<NPV>::kSmem);                           \
-      if (e != cudaSuccess) return e;                                              \
-      attr = true;                                                                 \
-    }                                                                              \
-    launch_kernel(k_tc_rows<NPV>, grid, kThreads, RowsCfg<NPV>::kSmem, st, prm);              \
-    break;                                                                         \
+#define LORA_ROWS_CASE(NPV)                                                             \
+  case NPV: {                                                                           \
+    static bool attr = false;                                                           \
+    if (!attr) {                                                                        \
+      e = set_smem(k_tc_rows<NPV>, RowsCfg<NPV>::kSmem);                                \
+      if (e != cudaSuccess) return e;                                                   \
+      attr = true;                                                                      \
+    }                                                                                   \
+    e = launch_cluster_y(k_tc_rows<NPV>, grid, a.splits, RowsCfg<NPV>::kSmem, st, prm); \
+    break;                                                                              \
   }
     LORA_ROWS_CASE(16)
     LORA_ROWS_CASE(32)
@@ -660,18 +753,69 @@ cudaError_t launch_tc_rows(const TcRowsArgs& a, cudaStream_t st, int prof_kind) 
     default:
       return cudaErrorInvalidValue;
   }
-  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (a.outT && a.items) {   // tokens of other slots read as zero in each slot's rows
-    e = cudaMemsetAsync(a.outT, 0, a.outT_bytes, st);
-    if (e != cudaSuccess) return e;
-  }
-  prof_begin(0, st);
-  launch_kernel(k_rows_finish, dim3((unsigned)a.max_items, (unsigned)(kBM / kFinishTok)), kFinishThreads, 0, st, 
-      a.part, a.splits, a.T, a.ldo, (int32_t)a.ldo, 1, a.items, a.n_items, a.si, a.out,
-      a.ld_out > 0 ? a.ld_out : a.ldo, a.out2, a.ld2, a.outT, a.ldt);
-  prof_end(prof_kind, st);   // the class's time spans the product and its split-K finish
+  prof_end(prof_kind, st);
   return cudaGetLastError();
+}
+
+// Clusters of `size` CTAs of a kernel that can be resident at once (0 when the size cannot be
+// hosted). Sizes above 8 need the non-portable cluster attribute.
+template <typename K>
+int resident_clusters(K kernel, int smem, int size) {
+  int n = 0;
+  bool ok = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) ==
+            cudaSuccess;
+  if (ok && size > 8)
+    ok = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+         cudaSuccess;
+  if (ok) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(1, (unsigned)size, 1);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = (unsigned)size;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) n = 0;
+  }
+  cudaGetLastError();
+  return n;
+}
+
+// resident clusters of k_tc_red<BN> per cluster size 1, 2, 4, 8, 16 (cached per device)
+template <int BN>
+int red_resident(int size) {
+  static int cache[64][5];
+  static bool done[64] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!done[dev]) {
+    for (int i = 0; i < 5; ++i) cache[dev][i] = resident_clusters(k_tc_red<BN>, RedCfg<BN>::kSmem, 1 << i);
+    done[dev] = true;
+  }
+  int i = 0;
+  while (i < 4 && (1 << i) < size) ++i;
+  return (1 << i) == size ? cache[dev][i] : 0;
+}
+
+template <int BN>
+cudaError_t launch_red_bn(dim3 grid, int splits, cudaStream_t st, const RedParams& prm) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = set_smem(k_tc_red<BN>, RedCfg<BN>::kSmem);
+    if (e != cudaSuccess) return e;
+    if (cudaFuncSetAttribute(k_tc_red<BN>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+        cudaSuccess)
+      cudaGetLastError();
+    attr = true;
+  }
+  return launch_cluster_y(k_tc_red<BN>, grid, splits, RedCfg<BN>::kSmem, st, prm);
 }
 
 cudaError_t launch_tc_red(const TcRedArgs& a, cudaStream_t st, int prof_kind) {
@@ -679,40 +823,54 @@ cudaError_t launch_tc_red(const TcRedArgs& a, cudaStream_t st, int prof_kind) {
   static std::mutex mu;
   std::lock_guard<std::mutex> lk(mu);
   std::memset(&prm, 0, sizeof(prm));
+  if (a.T <= 0 || a.n_slots <= 0) return cudaSuccess;
+  // Tile width and token splits (CTAs of one cluster): the most CTAs, one per SM at most, whose
+  // clusters are all resident at once, with at least two 64-token blocks of T per split; the
+  // wider tile on ties (it re-reads the split operand less).
+  const int sms = tc::sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  int best_bn = 256, best_splits = 1;
+  int64_t best_ctas = -1;
+  for (int bn : {256, 128}) {
+    const int64_t tiles = (a.N + bn - 1) / bn;
+    for (int c = 1; c <= kRedMaxSplits; c *= 2) {
+      const int64_t clusters = tiles * a.n_slots;
+      if (clusters * c > sms || (c > 1 && (a.T + 63) / 64 < 2 * (int64_t)c)) break;
+      const int res = bn == 256 ? red_resident<256>(c) : red_resident<128>(c);
+      if (clusters > res) continue;
+      if (clusters * c > best_ctas) {
+        best_ctas = clusters * c;
+        best_bn = bn;
+        best_splits = c;
+      }
+    }
+  }
+  const int bn = best_bn, splits = best_splits;
   for (int k = 0; k < a.n_slots; ++k) {
     if (!tc::make_map_2d(&prm.tst[k], a.st[k], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T,
                          2 * (uint64_t)a.rank[k], a.ldt, 64, kBM))
       return cudaErrorInvalidValue;
+    if (a.rank[k] % 4 || a.rank[k] > LORA_MAX_RANK) return cudaErrorInvalidValue;
     prm.rank[k] = a.rank[k];
+    prm.dst[k] = a.tab.out[k];
   }
   if (!tc::make_map_2d(&prm.tb, a.b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.N, a.T,
                        a.ldb > 0 ? a.ldb : a.N, 64, 64))
     return cudaErrorInvalidValue;
+  if (a.N % 4) return cudaErrorInvalidValue;
   prm.items = a.items;
-  prm.n_items = a.n_items;
+  prm.counts = a.n_items;
   prm.err = tc::error_word();
   if (!prm.err) return cudaErrorInvalidDevice;
-  prm.part = a.part;
+  prm.transposed = a.transposed;
   prm.N = a.N;
   prm.T = a.T;
-  prm.span = a.span_tokens;
-  prm.rstride = a.max_rank;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = set_smem(k_tc_red, kRedSmem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
-  dim3 grid((unsigned)((a.N + kRedBN - 1) / kRedBN), (unsigned)a.max_items);
+  dim3 grid((unsigned)((a.N + bn - 1) / bn), (unsigned)splits, (unsigned)a.n_slots);
   prof_begin(prof_kind, st);
-  launch_kernel(k_tc_red, grid, kThreads, kRedSmem, st, prm);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = bn == 256 ? launch_red_bn<256>(grid, splits, st, prm)
+                            : launch_red_bn<128>(grid, splits, st, prm);
   if (e != cudaSuccess) return e;
-  const int64_t blocks = (a.N + kRedFinCols - 1) / kRedFinCols;
-  prof_begin(0, st);
-  launch_kernel(k_red_finish, dim3((unsigned)blocks, (unsigned)a.n_slots), kFinishThreads, 0, st, 
-      a.part, a.items, a.n_items, a.N, a.max_rank, a.transposed, a.tab, a.T, a.span_tokens);
-  prof_end(prof_kind, st);   // the class's time spans the product and its item reduction
+  prof_end(prof_kind, st);
   return cudaGetLastError();
 }
 
