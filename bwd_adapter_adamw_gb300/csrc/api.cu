@@ -507,8 +507,7 @@ int run_backward_tc(const lora_desc* d, const DropParams& dp, int64_t T, const v
         ta.ld_dst[k] = L.ldx;
       }
     }
-    LORA_TRY(launch_transpose_slots(ta, s.n, d->rank, d->in_dim, st));
-    LORA_TRY(launch_split(sp, s.n, st));
+    LORA_TRY(launch_adapter_prep(ta, sp, s.n, st));
   }
   const void* dYp = dY;
   if (dora_m) {   // DoRA: dY' = dY * (m / n), materialised once in bf16 for every product
@@ -536,6 +535,7 @@ int run_backward_tc(const lora_desc* d, const DropParams& dp, int64_t T, const v
     r.si = si;
     r.out = L.Gs; r.ldo = d->rank;
     r.outT = L.GsT; r.ldt = L.ldt; r.outT_bytes = (size_t)2 * s.rank_sum * L.ldt * sizeof(uint16_t);
+    r.side_h = H; r.side_ldh = d->rank; r.side_outT = L.HsT;   // the saved Hs for dB
     if (routed) {   // the slot-expanded Gs for the dX product's uniform tiles
       r.out2 = L.Px;
       r.ld2 = L.ldx;
@@ -564,13 +564,11 @@ int run_backward_tc(const lora_desc* d, const DropParams& dp, int64_t T, const v
     }
     LORA_TRY(launch_tc_gemm(t, st, LORA_PROF_FROZEN_DX));
   }
-  const size_t split_bytes = (size_t)2 * s.rank_sum * L.ldt * sizeof(uint16_t);
   ReduceTab rt{};
   for (int k = 0; k < s.n; ++k) rt.rank[k] = s.rank[k];
-  // dB_k += dY'^T Hs over the slot's tokens (as dB^T rows of the transposed Hs split)
+  // dB_k += dY'^T Hs over the slot's tokens (as dB^T rows of the transposed Hs split, written by
+  // the G product's CTAs)
   {
-    LORA_TRY(launch_split_rows_t(H, d->rank, d->rank, L.ldt, L.gitems, L.gcount, (int)L.gmax, si, L.HsT,
-                                 split_bytes, T, st));
     TcRedArgs a{};
     for (int k = 0; k < s.n; ++k) {
       a.st[k] = L.HsT + (int64_t)si.region[k] * L.ldt;

@@ -113,6 +113,9 @@ struct TcRowsArgs {                 // out[t, j] = alpha * (A[t, :] . (S_hi[j] +
   uint16_t* outT;                   // optional per slot [2 r, ldt] bf16 transposed split of out
   int64_t ldt;
   size_t outT_bytes;                // zeroed first when an item table routes several slots
+  const float* side_h;              // optional [T, side_ldh] fp32: its transposed bf16 split
+  int64_t side_ldh;                 //   goes to side_outT (per slot [2 r, ldt], same layout and
+  uint16_t* side_outT;              //   size as outT), written by the same CTAs
   const TokenItem* items;
   const int32_t* n_items;
   int max_items;
@@ -249,6 +252,14 @@ struct TransposeTab {
 };
 cudaError_t launch_transpose_slots(const TransposeTab& t, int n, int64_t max_rows, int64_t max_cols,
                                    cudaStream_t st);
+// bf16 backward: A_slot^T (TransposeTab, n slots) and the split of B_slot^T (SplitTab with
+// transposed = 1) in one launch
+struct AdapterPrepTiles {
+  int32_t n, n_t;                       // (task, slot) units; the first n_t are transposes
+  int32_t first[2 * LORA_MAX_SLOTS];    // first tile of each unit
+};
+cudaError_t launch_adapter_prep(const TransposeTab& ta, const SplitTab& sb, int n,
+                                cudaStream_t st);
 // fp32 fused projections as one adapter of rank n r: A_cat = [A_0; ...; A_{n-1}] ([n r, in]) and
 // the block-diagonal B_cat ([off[n], n r]: B_k in rows off[k].., columns k r..; zeros elsewhere)
 struct CatTab {
@@ -311,7 +322,7 @@ struct GroupTab {
 constexpr int kPrepThreads = 256;
 constexpr int kPrepElemsWs = kPrepThreads * 16;         // per CTA, workspace form (more CTAs)
 constexpr int kPrepElemsPerBlock = kPrepThreads * 64;   // per CTA, allocation-free form
-constexpr int64_t kPrepTargetBlocks = 8 * 152;          // CTAs of the workspace form, large arenas
+constexpr int64_t kPrepTargetBlocks = 4 * 152;          // CTAs of the workspace form, large arenas (one wave)
 // adapter-state maintenance (launch_group_maint flags)
 constexpr int kMaintCopy = 1;     // dst = src
 constexpr int kMaintZeroDst = 2;  // dst = 0

@@ -54,6 +54,11 @@ struct RowsParams {
   int64_t ld2;
   uint16_t* outT;                    // per slot [2 r, ldt] transposed bf16 split (nullable)
   int64_t ldt;
+  // side task: the transposed bf16 split of another [T, ldh] fp32 operand of the same tokens
+  // into side_outT (per slot [2 r, ldt]), e.g. the saved Hs next to the G product
+  const float* side_h;
+  int64_t side_ldh;
+  uint16_t* side_outT;
   int64_t T;
 };
 
@@ -162,6 +167,28 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_rows(const __grid_constant__
     // epilogue: this thread's accumulator row (one token) -> its staging row, then hi + lo
     const int q = warp & 3;
     const int row = q * 32 + lane;
+    if (p.side_h) {
+      // side task while the K-blocks stream: the transposed split of the side operand's rows
+      // [z R, z R + R) of this item, straight from global memory (a thread per token and half
+      // of the columns; a warp's stores of one row are 32 consecutive tokens)
+      const int64_t sb0 = (int64_t)it.t0 + z * R;
+      const int e0 = threadIdx.x - 64;   // 0 .. 127
+      const int halves = 128 / R;        // threads per token
+      const int i = e0 % R, hpart = e0 / R;
+      const int64_t t = sb0 + i;
+      if (t < it.t1) {
+        const int per = (r + halves - 1) / halves;
+        const int j0 = hpart * per, j1 = min(r, j0 + per);
+        const float* src = p.side_h + t * p.side_ldh;
+        uint16_t* d = p.side_outT + (int64_t)p.si.region[it.slot] * p.ldt + t;
+        for (int j = j0; j < j1; ++j) {
+          const float x = __ldg(src + j);
+          const uint16_t hb = bf16_bits(x);
+          d[(int64_t)j * p.ldt] = hb;
+          d[(int64_t)(r + j) * p.ldt] = bf16_bits(x - bf16_val(hb));
+        }
+      }
+    }
     ready = nk == 0 || __all_sync(0xffffffffu, mbar_wait(acc_bar, 0u, 4u, p.err));
     if (ready) fence_after();
     float* br = buf + row * C::kLdb;
@@ -213,11 +240,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_rows(const __grid_constant__
     // [z R, z R + R) of its own tile, and each element is rewritten by the thread that read it
     if (c < r4) *reinterpret_cast<float4*>(buf + i * C::kLdb + 4 * c) = v;
   }
-  if (p.outT) {
-    __syncthreads();
-    const int64_t tb = (int64_t)it.t0 + z * R;
-    const int nt = (int)max((int64_t)0, min((int64_t)R, (int64_t)it.t1 - tb));
-    uint16_t* d = p.outT + (int64_t)p.si.region[it.slot] * p.ldt + tb;
+  const int64_t tb = (int64_t)it.t0 + z * R;
+  const int nt = (int)max((int64_t)0, min((int64_t)R, (int64_t)it.t1 - tb));
+  // transposed split of rows [z R, z R + nt) of this CTA's tile into d (per slot [2 r, ldt])
+  auto write_split_t = [&](uint16_t* d) {
     for (int e = threadIdx.x; e < nt * r; e += kThreads) {
       const int j = e / nt, i = e - j * nt;
       const float x = buf[(z * R + i) * C::kLdb + j];
@@ -225,7 +251,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_rows(const __grid_constant__
       d[(int64_t)j * p.ldt + i] = hb;
       d[(int64_t)(r + j) * p.ldt + i] = bf16_bits(x - bf16_val(hb));
     }
+  };
+  if (p.outT) {
+    __syncthreads();
+    write_split_t(p.outT + (int64_t)p.si.region[it.slot] * p.ldt + tb);
   }
+
   cluster_sync_all();   // peers' shared memory stays alive until every CTA has read it
   if (warp == 1) {
     fence_after();
@@ -556,6 +587,44 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_red(const __grid_constant__ 
 // ---------------------------------------------------------------------------------------------
 // split helpers
 // ---------------------------------------------------------------------------------------------
+// The backward's adapter operands in one launch of 32 x 32 shared-memory tiles: A_slot^T (fp32,
+// the dX product's LoRA operand) and the bf16 hi / lo split of B_slot^T (the G product's operand),
+// both read and written along rows. Flat tile index: the tiles of every (task, slot) in turn.
+__global__ void __launch_bounds__(256) k_adapter_prep(const TransposeTab ta, const SplitTab sb,
+                                                      const AdapterPrepTiles pt) {
+  grid_dep_sync();
+  __shared__ float tile[32][33];
+  int u = 0;
+  while (u + 1 < pt.n && (int)blockIdx.x >= pt.first[u + 1]) ++u;
+  const bool split = u >= pt.n_t;                 // tasks: transposes first, then splits
+  const int k = split ? u - pt.n_t : u;           // slot
+  const int local = (int)blockIdx.x - pt.first[u];
+  const int64_t rows = split ? sb.K : ta.rows[k];          // src rows (B: out, A: r)
+  const int64_t cols = split ? sb.rank[k] : ta.cols[k];    // src cols (B: r, A: in)
+  const int64_t ncb = (cols + 31) / 32;
+  const int64_t r0 = (int64_t)(local / ncb) * 32, c0 = (int64_t)(local % ncb) * 32;
+  const float* src = split ? sb.src[k] : ta.src[k];
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  for (int i = ty; i < 32; i += 8) {
+    const int64_t r = r0 + i, c = c0 + tx;
+    tile[i][tx] = (r < rows && c < cols) ? src[r * cols + c] : 0.f;
+  }
+  __syncthreads();
+  for (int i = ty; i < 32; i += 8) {
+    const int64_t c = c0 + i, r = r0 + tx;   // dst row c (a src column), dst column r
+    if (r >= rows || c >= cols) continue;
+    const float x = tile[tx][i];
+    if (!split) {
+      const int64_t ldd = ta.ld_dst[k] > 0 ? ta.ld_dst[k] : rows;
+      ta.dst[k][c * ldd + r] = x;
+    } else {
+      const uint16_t hb = bf16_bits(x);
+      sb.dst[k][c * rows + r] = hb;
+      sb.dst[k][(cols + c) * rows + r] = bf16_bits(x - bf16_val(hb));
+    }
+  }
+}
+
 // dst [2 r, K] bf16: rows j < r = hi(src[j, :]), rows r + j = lo(src[j, :]); src [r, K] fp32.
 // transposed: src is [K, r] and row j of dst takes column j of src.
 __global__ void k_split(const SplitTab tab) {
@@ -724,11 +793,22 @@ cudaError_t launch_tc_rows(const TcRowsArgs& a, cudaStream_t st, int prof_kind) 
   prm.ld2 = a.ld2;
   prm.outT = a.outT;
   prm.ldt = a.ldt;
+  prm.side_h = a.side_h;
+  prm.side_ldh = a.side_ldh;
+  prm.side_outT = a.side_outT;
   prm.T = a.T;
+  if (a.side_h && (!a.side_outT || a.side_ldh % 4 || a.side_ldh < a.ldo || a.ldt <= 0))
+    return cudaErrorInvalidValue;
   if (a.max_items <= 0) return cudaSuccess;
-  if (a.outT && a.items) {   // tokens of other slots read as zero in each slot's rows
-    cudaError_t e = cudaMemsetAsync(a.outT, 0, a.outT_bytes, st);
-    if (e != cudaSuccess) return e;
+  if (a.items) {   // tokens of other slots read as zero in each slot's rows
+    if (a.outT) {
+      cudaError_t e = cudaMemsetAsync(a.outT, 0, a.outT_bytes, st);
+      if (e != cudaSuccess) return e;
+    }
+    if (a.side_outT) {
+      cudaError_t e = cudaMemsetAsync(a.side_outT, 0, a.outT_bytes, st);
+      if (e != cudaSuccess) return e;
+    }
   }
   dim3 grid((unsigned)a.max_items, (unsigned)a.splits);
   cudaError_t e = cudaSuccess;
@@ -871,6 +951,28 @@ cudaError_t launch_tc_red(const TcRedArgs& a, cudaStream_t st, int prof_kind) {
                             : launch_red_bn<128>(grid, splits, st, prm);
   if (e != cudaSuccess) return e;
   prof_end(prof_kind, st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_adapter_prep(const TransposeTab& ta, const SplitTab& sb, int n,
+                                cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  if (!sb.transposed || n > LORA_MAX_SLOTS) return cudaErrorInvalidValue;
+  AdapterPrepTiles pt{};
+  pt.n_t = n;
+  pt.n = 2 * n;
+  int total = 0;
+  for (int u = 0; u < 2 * n; ++u) {
+    const bool split = u >= n;
+    const int k = split ? u - n : u;
+    const int64_t rows = split ? sb.K : ta.rows[k];
+    const int64_t cols = split ? sb.rank[k] : ta.cols[k];
+    pt.first[u] = total;
+    total += (int)(((rows + 31) / 32) * ((cols + 31) / 32));
+  }
+  if (total <= 0) return cudaSuccess;
+  prof_begin(0, st);
+  launch_kernel(k_adapter_prep, dim3((unsigned)total), dim3(256), 0, st, ta, sb, pt);
   return cudaGetLastError();
 }
 

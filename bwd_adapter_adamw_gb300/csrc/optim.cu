@@ -56,7 +56,7 @@ __device__ __forceinline__ int find_group(const GroupTab& g, int b) {
   return lo;
 }
 
-__global__ void __launch_bounds__(kPrepThreads, 8) k_grad_prepare(const float* __restrict__ grads,
+__global__ void __launch_bounds__(kPrepThreads, 4) k_grad_prepare(const float* __restrict__ grads,
                                                                const GroupTab gt,
                                                                double* __restrict__ scale_norm,
                                                                int32_t* __restrict__ status,
@@ -70,19 +70,36 @@ __global__ void __launch_bounds__(kPrepThreads, 8) k_grad_prepare(const float* _
   const int64_t begin = (int64_t)(b - gt.block_begin[g]) * per_block;
   const int64_t n = min(per_block, gt.count[g] - begin);
   const float* p = grads + gt.offset[g] + begin;
-  float hi = 0.f, lo = 0.f;
+  // Two independent float-float accumulators per thread (x, y and z, w of each float4) halve the
+  // dependent chain, and each batch issues kPrepBatch independent 16-byte loads before any add,
+  // so that enough bytes are in flight to stream at the memory's rate.
+  constexpr int kPrepBatch = 8;
+  float hi0 = 0.f, lo0 = 0.f, hi1 = 0.f, lo1 = 0.f;
   double big = 0.0;
   const int64_t nv = n >> 2;
-#pragma unroll 4
-  for (int64_t v = threadIdx.x; v < nv; v += kPrepThreads) {
-    const float4 x = __ldcs(reinterpret_cast<const float4*>(p) + v);
-    sq_accum(x.x, hi, lo, big);
-    sq_accum(x.y, hi, lo, big);
-    sq_accum(x.z, hi, lo, big);
-    sq_accum(x.w, hi, lo, big);
+  const float4* p4 = reinterpret_cast<const float4*>(p);
+  int64_t v = threadIdx.x;
+  for (; v + (kPrepBatch - 1) * kPrepThreads < nv; v += kPrepBatch * kPrepThreads) {
+    float4 x[kPrepBatch];
+#pragma unroll
+    for (int u = 0; u < kPrepBatch; ++u) x[u] = __ldcs(p4 + v + u * kPrepThreads);
+#pragma unroll
+    for (int u = 0; u < kPrepBatch; ++u) {
+      sq_accum(x[u].x, hi0, lo0, big);
+      sq_accum(x[u].y, hi0, lo0, big);
+      sq_accum(x[u].z, hi1, lo1, big);
+      sq_accum(x[u].w, hi1, lo1, big);
+    }
   }
-  for (int64_t e = (nv << 2) + threadIdx.x; e < n; e += kPrepThreads) sq_accum(p[e], hi, lo, big);
-  const double mine = ((double)hi + (double)lo) + big;
+  for (; v < nv; v += kPrepThreads) {
+    const float4 x = __ldcs(p4 + v);
+    sq_accum(x.x, hi0, lo0, big);
+    sq_accum(x.y, hi0, lo0, big);
+    sq_accum(x.z, hi1, lo1, big);
+    sq_accum(x.w, hi1, lo1, big);
+  }
+  for (int64_t e = (nv << 2) + threadIdx.x; e < n; e += kPrepThreads) sq_accum(p[e], hi0, lo0, big);
+  const double mine = (((double)hi0 + (double)lo0) + ((double)hi1 + (double)lo1)) + big;
   const double tot = block_sum_double(mine, sh);
   if (threadIdx.x == 0) {
     part[b] = tot;
