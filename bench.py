@@ -860,10 +860,10 @@ def run_ours(args):
         bf16_peak = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
         kind = ("sustained (timed region %.1f s)" % (ms / 1e3)) if sustained else "burst"
         if cfg.dtype == "f32":
-            # fp32 products as three bf16 products of the split operands
-            peak = bf16_peak / 3.0
+            # fp32 products as four bf16 products of the split operands
+            peak = bf16_peak / 4.0
             bound, punit = "tensor", "TFLOP/s"
-            note = (f"split-bf16 effective: measured bf16 {kind} {bf16_peak:.0f} / 3 products "
+            note = (f"split-bf16 effective: measured bf16 {kind} {bf16_peak:.0f} / 4 products "
                     f"({peak_src})")
         elif cfg.dtype == "bf16fp8":
             # E4M3 products: the measured bf16 rate x the nominal fp8 : bf16 ratio (4.5 : 2.25)

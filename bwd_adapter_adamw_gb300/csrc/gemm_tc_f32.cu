@@ -1,13 +1,14 @@
-// Tensor-core frozen products for fp32 activations (sm_103a), as three bf16 products:
+// Tensor-core frozen products for fp32 activations (sm_103a), as bf16 products of split operands:
 //
 //   out[t, n] = ( sum_k A[t, k] B[n, k] + [mask(t, n)] * sum_j P[t, j] Q_slot[n, j] ) * colscale[n]
 //
 // with every fp32 operand x of the main product split into x_hi = bf16(x) and x_lo =
-// bf16(x - x_hi), and the product formed as A_hi B_hi + A_hi B_lo + A_lo B_hi with tcgen05.mma
-// kind::f16 (bf16 operands, fp32 accumulation). The split keeps 16 significant bits of every
-// operand (|x - x_hi - x_lo| <= 2^-16 |x|) and the dropped A_lo B_lo term is of the same order,
-// so the result stays within the fp32 paths' 1e-5 relative bound (about 4e-6 on the TinyLlama
-// shapes), at a third of the bf16 tensor rate, where three tf32 products would run at a sixth.
+// bf16(x - x_hi), and the product formed as A_hi B_hi + A_hi B_lo + A_lo B_hi + A_lo B_lo with
+// tcgen05.mma kind::f16 (bf16 operands, fp32 accumulation). The split keeps 16 significant bits
+// of every operand (|x - x_hi - x_lo| <= 2^-16 |x|). The fourth product costs one N = 128 MMA
+// more per K-step and keeps heavy-tailed operands over long K inside the fp32 paths' 1e-5
+// relative bound (with three products a Student-t upstream gradient over K = 1024 measured
+// 1.4e-5).
 // The short LoRA K-blocks (P = Hs or Gs, Q = B or A^T, at most two 32-wide blocks) land raw and
 // are split in shared memory by two converter warps into tf32 hi / lo (three kind::tf32 products,
 // about 2^-21 relative). (Same roles as the bf16 kernel: frozen forward X W^T + Hs B^T, frozen
@@ -19,10 +20,10 @@
 // is a plain TMA -> MMA pipeline of four bf16 tiles per stage (A_hi, A_lo, B_hi, B_lo), 64
 // elements of K each.
 //
-// Per K-step two MMAs: A_hi x [B_hi; B_lo] as one N = 256 instruction (the stage holds B_hi and
-// B_lo back to back), whose first 128 columns take A_hi B_hi and last 128 A_hi B_lo, then
-// A_lo x B_hi (N = 128) into the first 128 columns. N = 256 MMAs run about 1.3x faster per flop
-// than N = 128 ones.
+// Per K-step two N = 256 MMAs (the stage holds B_hi and B_lo back to back): A_hi x [B_hi; B_lo],
+// whose first 128 columns take A_hi B_hi and last 128 A_hi B_lo, then A_lo x [B_hi; B_lo] into
+// the same columns (A_lo B_hi, A_lo B_lo); the epilogue adds the two halves. N = 256 MMAs run
+// about 1.3x faster per flop than N = 128 ones.
 //
 // The tensor core's fp32 accumulation loses a little at every MMA, so no accumulation chain is
 // allowed to grow with K: two 256-column TMEM regions take turns, each holding the partial sum of
@@ -64,8 +65,7 @@ __device__ __forceinline__ uint64_t kdesc(uint32_t saddr) {
 }
 constexpr uint32_t kIdesc = idesc(kFmtTF32, kBM, kBN);            // LoRA: lo x Q_hi into the big half
 constexpr uint32_t kIdesc2 = idesc(kFmtTF32, kBM, 2 * kBN);       // LoRA: hi x [Q_hi; Q_lo]
-constexpr uint32_t kIdescB = idesc(kFmtBF16, kBM, kBN);           // main: lo x B_hi
-constexpr uint32_t kIdescB2 = idesc(kFmtBF16, kBM, 2 * kBN);      // main: hi x [B_hi; B_lo]
+constexpr uint32_t kIdescB2 = idesc(kFmtBF16, kBM, 2 * kBN);      // main: hi or lo x [B_hi; B_lo]
 constexpr int kPeriod = 4;   // main K-blocks (256 elements) accumulated in one TMEM region
 constexpr int kPartLd = kBN + 4;   // row stride (floats) of a split-K partial tile in shared memory
 constexpr int kMaxSplits = 8;      // portable cluster size
@@ -210,9 +210,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm_f32(const __grid_consta
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      // Per K-step: hi x [B_hi; B_lo] as one N = 256 MMA (big half: hi x B_hi, small half:
-      // hi x B_lo), then lo x B_hi into the big half. Regions alternate per period; a region is
-      // reused only after the epilogue has drained it.
+      // Per K-step: hi x [B_hi; B_lo] and lo x [B_hi; B_lo] as N = 256 MMAs (first half: x B_hi,
+      // second half: x B_lo); the LoRA K-blocks take hi x [Q_hi; Q_lo] and lo x Q_hi (tf32).
+      // Regions alternate per period; a region is reused only after the epilogue has drained it.
       int per = -1;
       uint32_t d = tmem;
       bool ok = true;
@@ -246,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm_f32(const __grid_consta
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             umma_f16(d, ah + 2 * k, bh + 2 * k, kIdescB2, (start && k == 0) ? 0u : 1u);
-            umma_f16(d, al + 2 * k, bh + 2 * k, kIdescB, 1u);
+            umma_f16(d, al + 2 * k, bh + 2 * k, kIdescB2, 1u);
           }
         }
         umma_commit(&empty_bar[s]);

@@ -54,6 +54,14 @@ extern "C" {
 #define LORA_ERR_TIMEOUT 7      /* device status: a tensor-core pipeline wait ran out of its bound */
 
 /* ---- enums ----------------------------------------------------------------------------------*/
+/* fp32 activations and frozen W. The frozen products (forward and dX) run on bf16 tensor cores as
+ * four products of a two-term bf16 split of each operand (hi = bf16(x), lo = bf16(x - hi);
+ * hi*hi' + hi*lo' + lo*hi' + lo*lo'), accumulated in fp32 in periods of 256 K-elements; the
+ * adapter terms and the low-rank products run in fp32. Each output of the split products is
+ * within 2^-17 of sum_k |a_k w_k| of the exact product. Against a float64 reference the
+ * per-tensor max relative error is shown below 1e-5 for N(0, 1)-scaled operands with
+ * K <= 14336 and for heavy-tailed ones (Student-t, 3 degrees of freedom) up to K = 8192 on the
+ * GPU and K = 14336 in the split arithmetic alone. */
 #define LORA_F32 0
 #define LORA_BF16 1
 /* bf16 activations and frozen W whose frozen products (forward and dX) run on E4M3 tensor

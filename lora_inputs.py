@@ -52,6 +52,7 @@ class LoraConfig:
     chunks: int                # accumulation chunks per step
     x_var: float = 1.0
     dy_var: float = 1.0
+    dy_tail: int = 0           # 0: dY normal; k > 0: Student-t with k degrees of freedom, scaled by sqrt(dy_var)
     b_var: float = 0.01
     b_zero: bool = False
     dropout_p: float = 0.0
@@ -159,6 +160,21 @@ def _normal(shape, var, seed, device, dtype) -> torch.Tensor:
     return t.to(dtype)
 
 
+def _student_t(shape, dof: int, var, seed, device, dtype) -> torch.Tensor:
+    """Student-t with `dof` degrees of freedom times sqrt(var): z / sqrt(chi2_dof / dof), the
+    chi-square drawn as a sum of dof squared normals from the same seeded generator."""
+    g = _gen(seed, device)
+    z = torch.randn(tuple(shape), generator=g, device=device, dtype=torch.float32)
+    chi = torch.zeros(tuple(shape), device=device, dtype=torch.float32)
+    for _ in range(dof):
+        u = torch.randn(tuple(shape), generator=g, device=device, dtype=torch.float32)
+        chi.add_(u * u)
+    t = z / torch.sqrt(chi / dof)
+    if var != 1.0:
+        t.mul_(math.sqrt(var))
+    return t.to(dtype)
+
+
 def _uniform(shape, bound, seed, device) -> torch.Tensor:
     g = _gen(seed, device)
     t = torch.rand(tuple(shape), generator=g, device=device, dtype=torch.float32)
@@ -202,10 +218,13 @@ def make_b(cfg: LoraConfig, layer: int, proj: Proj, rank: Optional[int] = None, 
 
 
 def make_dy(cfg: LoraConfig, layer: int, proj: Proj, device="cpu", tokens: Optional[int] = None):
-    """Upstream gradient dY [T, out]: N(0, dy_var) in the activation dtype."""
+    """Upstream gradient dY [T, out]: N(0, dy_var) in the activation dtype (or, with dy_tail = k,
+    a heavy-tailed Student-t with k degrees of freedom at the same scale)."""
     T = cfg.tokens if tokens is None else tokens
-    return _normal((T, proj.out_dim), cfg.dy_var, tensor_seed(cfg.seed, layer, "dY", proj.name),
-                   device, act_dtype(cfg))
+    seed = tensor_seed(cfg.seed, layer, "dY", proj.name)
+    if cfg.dy_tail > 0:
+        return _student_t((T, proj.out_dim), cfg.dy_tail, cfg.dy_var, seed, device, act_dtype(cfg))
+    return _normal((T, proj.out_dim), cfg.dy_var, seed, device, act_dtype(cfg))
 
 
 def make_adam_state(cfg: LoraConfig, n: int, tag: str, device="cpu"):

@@ -159,6 +159,10 @@ SINGLE_CASES = {
     "c2_two_layers": ("c2", [0, 21], [0, 1], None, {}),
     "c4_small": ("c4", [0], [1, 6], 512, {}),
     "c4dora_small": ("c4dora", [3], [2, 4], 256, dict(chunks=2)),
+    # fp32 split products over long contractions with a heavy-tailed upstream gradient
+    # (Student-t, 3 degrees of freedom): K = 8192 in the forward, then in the dX product
+    "longK_fwd_f32": ("c1", [0], [0], 64, dict(projs=(LI.Proj("lin", 8192, 1024, "x"),), dy_tail=3)),
+    "longK_dx_f32": ("c1", [0], [0], 64, dict(projs=(LI.Proj("lin", 512, 8192, "x"),), dy_tail=3)),
 }
 
 

@@ -1,9 +1,10 @@
-"""The fp32 frozen products run as three bf16 products of a two-term bf16 split of each operand
-(hi = bf16(x), lo = bf16(x - hi); the product is hi*hi' + hi*lo' + lo*hi'). This checks, in
-float64 on the CPU and independently of the CUDA path, that the arithmetic this reading rests on
-holds: the split keeps 16 significant bits, and on the fp32 workloads' shapes and value
-distributions the three-product form stays well inside the fp32 paths' 1e-5 relative bound
-(max |diff| / max |ref|), leaving room for the tensor core's fp32 accumulation."""
+"""The fp32 frozen products run as four bf16 products of a two-term bf16 split of each operand
+(hi = bf16(x), lo = bf16(x - hi); the product is hi*hi' + hi*lo' + lo*hi' + lo*lo'). This checks,
+in float64 on the CPU and independently of the CUDA path, that the arithmetic this reading rests
+on holds: the split keeps 16 significant bits, every output of the four-product form is within
+2^-17 of sum_k |a_k w_k| of the exact product, and on the fp32 workloads' shapes, on long
+contractions and with heavy-tailed operands it stays well inside the fp32 paths' 1e-5 relative
+bound (max |diff| / max |ref|), leaving room for the tensor core's fp32 accumulation."""
 import numpy as np
 import pytest
 
@@ -22,6 +23,18 @@ def _split(x):
     return hi.astype(np.float64), lo.astype(np.float64)
 
 
+def _student_t3(rng, shape):
+    z = rng.standard_normal(shape)
+    chi = sum(rng.standard_normal(shape) ** 2 for _ in range(3))
+    return z / np.sqrt(chi / 3)
+
+
+def _four(A, W):
+    ah, al = _split(A)
+    wh, wl = _split(W)
+    return ah @ wh + ah @ wl + al @ wh + al @ wl
+
+
 def test_two_term_split_keeps_sixteen_bits():
     rng = np.random.default_rng(0)
     x = np.concatenate([rng.standard_normal(200000), rng.uniform(-1e3, 1e3, 200000),
@@ -35,19 +48,50 @@ def test_two_term_split_keeps_sixteen_bits():
 
 @pytest.mark.parametrize("T,K,N", [(256, 2048, 512), (256, 2048, 256), (256, 256, 1024),
                                    (32, 64, 64)])
-def test_three_product_form_within_fp32_bound(T, K, N):
+def test_four_product_form_within_fp32_bound(T, K, N):
     """Shapes of the fp32 workloads (TinyLlama wq / wv forward and dX, the tiny linear) at a
     reduced token count; X ~ N(0, 1), W ~ N(0, 1/K)."""
     rng = np.random.default_rng(T + K + N)
     X = rng.standard_normal((T, K)).astype(np.float32)
     W = (rng.standard_normal((N, K)) / np.sqrt(K)).astype(np.float32)
     ref = X.astype(np.float64) @ W.astype(np.float64).T
-    xh, xl = _split(X)
-    wh, wl = _split(W)
-    three = xh @ wh.T + xh @ wl.T + xl @ wh.T
-    err = np.max(np.abs(three - ref)) / np.max(np.abs(ref))
-    assert err <= 6e-6, err
+    err = np.max(np.abs(_four(X, W.T) - ref)) / np.max(np.abs(ref))
+    assert err <= 5e-6, err
     # dropping the lo terms altogether (a plain bf16 product) is far outside the bound, so the
     # check above can fail
-    plain = xh @ wh.T
-    assert np.max(np.abs(plain - ref)) / np.max(np.abs(ref)) > 1e-4
+    xh, _ = _split(X)
+    wh, _ = _split(W)
+    assert np.max(np.abs(xh @ wh.T - ref)) / np.max(np.abs(ref)) > 1e-4
+
+
+@pytest.mark.parametrize("T,K,N,tail", [(64, 8192, 256, False), (64, 14336, 128, False),
+                                        (64, 1024, 512, True), (64, 8192, 256, True),
+                                        (64, 14336, 128, True)])
+def test_four_product_form_at_long_contractions(T, K, N, tail):
+    """Long contractions (a 8192- or 14336-long K, as in a dX product over a wide output) with
+    the upstream operand N(0, 1) or heavy-tailed (Student-t, 3 degrees of freedom): every output
+    is within 2^-17 of sum_k |a_k w_k| (the split's representation error of both operands), and
+    the per-tensor error stays inside the fp32 paths' 1e-5 bar."""
+    rng = np.random.default_rng(K + N + int(tail))
+    A = (_student_t3(rng, (T, K)) if tail else rng.standard_normal((T, K))).astype(np.float32)
+    W = (rng.standard_normal((K, N)) / np.sqrt(K)).astype(np.float32)
+    ref = A.astype(np.float64) @ W.astype(np.float64)
+    diff = np.abs(_four(A, W) - ref)
+    assert np.all(diff <= 2.0 ** -17 * (np.abs(A).astype(np.float64) @ np.abs(W).astype(np.float64)))
+    err = np.max(diff) / np.max(np.abs(ref))
+    assert err <= 8e-6, err
+
+
+def test_three_products_are_not_enough_for_heavy_tails():
+    """Why the fourth product: without lo x lo' a Student-t(3) operand over K = 14336 takes the
+    error above the 1e-5 bar for some draws (seed 3 here), while the four-product form of the
+    same draw stays inside it."""
+    rng = np.random.default_rng(3)
+    A = _student_t3(rng, (64, 14336)).astype(np.float32)
+    W = (rng.standard_normal((14336, 128)) / np.sqrt(14336)).astype(np.float32)
+    ref = A.astype(np.float64) @ W.astype(np.float64)
+    ah, al = _split(A)
+    wh, wl = _split(W)
+    three = ah @ wh + ah @ wl + al @ wh
+    assert np.max(np.abs(three - ref)) / np.max(np.abs(ref)) > 1e-5
+    assert np.max(np.abs(three + al @ wl - ref)) / np.max(np.abs(ref)) <= 8e-6
