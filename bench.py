@@ -137,12 +137,12 @@ def memory_counts(cfg: LI.LoraConfig, layers: int, groups=None):
 # value. Captured with `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum` on
 # `python bench.py --layers 1 --steps 2 --warmup 3 --no-cpu-baseline --streams 1`.
 NCU_TRAFFIC = {
-    ("c4", 1): {"source": "gemm_tc.cu", "sha256_16": "d18ed8a10b97a935",
-                "bytes": 447.4e6,
+    ("c4", 1): {"source": "gemm_tc.cu", "sha256_16": "4819c92179bf6c02",
+                "bytes": 385.8e6,
                 "note": "one-layer capture (profiles/launch_list_c4_llama_bf16.md): the seven "
-                        "forward launches move 154, 78.6, 78.1, 153.3, 766, 765.4 and 1136 MB "
-                        "(read + write); the wide and long shapes re-read their operands about "
-                        "3x while compute-bound"},
+                        "forward launches move 154.5, 78.6, 78.1, 154.0, 548.9, 550.5 and "
+                        "1136.2 MB (read + write); the wide and long shapes re-read operands "
+                        "while compute-bound"},
     ("c2", 1): {"source": "gemm_tc_f32.cu", "sha256_16": "0cfe552134b8e004",
                 "bytes": (25.32e6 + 10.58e6) / 2,
                 "note": "wq fwd 25.32 MB, wv fwd (4-way split K) 10.58 MB read (the bf16 hi / lo "

@@ -478,8 +478,14 @@ int run_backward_tc(const lora_desc* d, const DropParams& dp, int64_t T, const v
                                (int32_t)L.gmax, nullptr, nullptr, 0, st));
     LORA_TRY(launch_make_red_items_tc(T, n_seg, seg_start, seg_slot, s.n, L.span_db, L.items_db,
                                       L.count_db, (int32_t)L.max_db, st));
-    LORA_TRY(launch_make_red_items_tc(T, n_seg, seg_start, seg_slot, s.n, L.span_da, L.items_da,
-                                      L.count_da, (int32_t)L.max_da, st));
+    if (L.span_da == L.span_db) {   // the same runs serve both reductions
+      L.items_da = L.items_db;
+      L.count_da = L.count_db;
+      L.max_da = L.max_db;
+    } else {
+      LORA_TRY(launch_make_red_items_tc(T, n_seg, seg_start, seg_slot, s.n, L.span_da, L.items_da,
+                                        L.count_da, (int32_t)L.max_da, st));
+    }
     int rr = routed_tiles(T, n_seg, seg_start, seg_slot, s, L, st);
     if (rr) return rr;
   }

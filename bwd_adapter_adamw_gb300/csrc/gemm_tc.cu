@@ -61,12 +61,15 @@ constexpr int kEpiThreads = 128;
 constexpr int kEpiBox = 32 * 64;
 template <int BN>
 constexpr int epi_bytes() { return BN == 224 ? 0 : 4 * 2 * kEpiBox; }
-// Items per tile group (rasterization for L2 reuse): 16 when W spans more than 16 N tiles; with
+// Items per tile group (rasterization for L2 reuse): 32 when W spans more than 16 N tiles; with
 // fewer, the N tile runs fastest (group of 1), so that the CTAs of one wave read all of W
 // together. Measured at T 8192 (us): N 4096 / K 4096: 152 (N fastest), 152 (8), 162 (16);
-// N 14336 / K 4096: 688, 585, 550; N 4096 / K 14336: 542, 566, 557. (A threshold of 32 tiles
-// left c3, T 4096 / N 4096 at 19 tiles of 224, unchanged.)
-constexpr int kGroupWide = 16;
+// N 14336 / K 4096: 688, 585, 550 (16); N 4096 / K 14336: 542, 566, 557. Later, cold in one
+// capture, N 14336 / K 4096 (and the dX of K 14336 back to N 14336): 577 us and 555 MB of DRAM
+// reads with groups of 16, 566 / 436 MB with 24, 564 / 330 MB with 32, 603 / 1399 MB with 64
+// (the band of W no longer fits L2). (A threshold of 32 tiles left c3, T 4096 / N 4096 at 19
+// tiles of 224, unchanged.)
+constexpr int kGroupWide = 32;
 constexpr int kGroupMinTiles = 16;
 
 // Tile 128 x BN. BN = 256 is the fastest MMA shape per flop; 224 and 192 (the same kernel with
