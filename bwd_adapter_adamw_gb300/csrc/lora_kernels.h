@@ -157,6 +157,11 @@ cudaError_t launch_make_red_items_tc(int64_t T, int32_t n_seg, const int32_t* se
                                      const int32_t* seg_slot, int32_t n_slots, int32_t span_blocks,
                                      TokenItem* items, int32_t* count, int32_t max_items,
                                      cudaStream_t st);
+// the same table built by a parallel coverage pass (lowrank.cu), for 1 .. 2048 segments
+cudaError_t launch_make_red_items_par(int64_t T, int32_t n_seg, const int32_t* seg_start,
+                                      const int32_t* seg_slot, int32_t n_slots,
+                                      int32_t span_blocks, TokenItem* items, int32_t* count,
+                                      int32_t max_items, cudaStream_t st);
 cudaError_t launch_mask_bf16(const void* X, int64_t T, int64_t in_dim, const DropParams& dp,
                              void* Xd, cudaStream_t st);
 

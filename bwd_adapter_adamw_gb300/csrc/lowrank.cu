@@ -367,7 +367,103 @@ __global__ void __launch_bounds__(kItemThreads) k_make_items_par(
   }
 }
 
+// Reduction work items of the tensor-core dA / dB products (the serial walk is
+// k_make_red_items_tc in lowrank_tc.cu): per slot, the 64-token blocks of its segments merged
+// into runs and cut into spans of span_blocks blocks, the slots' items one after the other. The
+// segments' coverage is computed in parallel (as in k_make_items_par), so that each slot's walker
+// thread only tests a staged slot id per segment and merges its own segments' block ranges.
+__global__ void __launch_bounds__(kItemThreads) k_make_red_items_par(
+    int64_t T, int32_t n_seg, const int32_t* __restrict__ seg_start,
+    const int32_t* __restrict__ seg_slot, int32_t n_slots, int32_t span_blocks, TokenItem* items,
+    int32_t* count, int32_t max_items) {
+  grid_dep_sync();
+  __shared__ int32_t s_ba[kItemSegs], s_bb[kItemSegs], s_cur[kItemSegs];
+  __shared__ int8_t s_sl[kItemSegs];
+  __shared__ int32_t s_count[LORA_MAX_SLOTS + 1];
+  const int n = n_seg;   // 1 .. kItemSegs (the launcher checks)
+  const int64_t TT = T;
+  int32_t a_[2], b_[2], sl_[2];
+  for (int u = 0; u < 2; ++u) {
+    const int k = threadIdx.x + u * kItemThreads;
+    a_[u] = b_[u] = 0;
+    sl_[u] = -1;
+    if (k >= n) continue;
+    int64_t a = seg_start[k], b = seg_start[k + 1];
+    int32_t slot = seg_slot[k];
+    if (slot < 0 || slot >= n_slots) slot = -1;
+    a = max((int64_t)0, min(a, TT));
+    b = max((int64_t)0, min(b, TT));
+    a_[u] = (int32_t)a;
+    b_[u] = (int32_t)b;
+    sl_[u] = slot;
+    s_cur[k] = b > a ? (int32_t)b : 0;
+  }
+  __syncthreads();
+  block_scan2(s_cur, n, true);
+  for (int u = 0; u < 2; ++u) {
+    const int k = threadIdx.x + u * kItemThreads;
+    if (k >= n) continue;
+    const int32_t cur = k > 0 ? max(0, s_cur[k - 1]) : 0;
+    const int32_t ea = max(a_[u], cur);
+    const bool acc = b_[u] > ea;
+    s_ba[k] = (acc && sl_[u] >= 0) ? ea / 64 : -1;
+    s_bb[k] = (b_[u] + 63) / 64;
+    s_sl[k] = (int8_t)sl_[u];
+  }
+  __syncthreads();
+  const int s = threadIdx.x;
+  auto walk = [&](bool write, int32_t base) {
+    int32_t cnt = 0;
+    auto emit_run = [&](int32_t b0, int32_t b1) {
+      for (int32_t b = b0; b < b1; b += span_blocks) {
+        if (write && base + cnt < max_items)
+          items[base + cnt] = TokenItem{b * 64, min(b1, b + span_blocks) * 64, s, 0};
+        ++cnt;
+      }
+    };
+    int32_t rb = -1, re = -1;
+    for (int k = 0; k < n; ++k) {
+      if (s_sl[k] != s) continue;
+      const int32_t ba = s_ba[k];
+      if (ba < 0) continue;
+      const int32_t bb = s_bb[k];
+      if (re >= 0 && ba <= re) {
+        re = max(re, bb);
+      } else {
+        if (re >= 0) emit_run(rb, re);
+        rb = ba;
+        re = bb;
+      }
+    }
+    if (re >= 0) emit_run(rb, re);
+    return cnt;
+  };
+  if (s < n_slots) s_count[s + 1] = walk(false, 0);
+  __syncthreads();
+  if (s == 0) {
+    s_count[0] = 0;
+    for (int k = 1; k <= n_slots; ++k) s_count[k] += s_count[k - 1];
+    *count = min(s_count[n_slots], max_items);
+    for (int k = 0; k <= n_slots; ++k) count[1 + k] = min(s_count[k], max_items);   // slot ranges
+  }
+  __syncthreads();
+  if (s < n_slots) walk(true, s_count[s]);
+}
+
 }  // namespace
+
+cudaError_t launch_make_red_items_par(int64_t T, int32_t n_seg, const int32_t* seg_start,
+                                      const int32_t* seg_slot, int32_t n_slots,
+                                      int32_t span_blocks, TokenItem* items, int32_t* count,
+                                      int32_t max_items, cudaStream_t st) {
+  if (!seg_start || !seg_slot || n_seg < 1 || n_seg > kItemSegs || T > INT32_MAX - 64 ||
+      span_blocks < 1 || n_slots > LORA_MAX_SLOTS)
+    return cudaErrorInvalidValue;
+  prof_begin(0, st);
+  launch_kernel(k_make_red_items_par, 1, kItemThreads, 0, st, T, n_seg, seg_start, seg_slot,
+                n_slots, span_blocks, items, count, max_items);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_make_items(int64_t T, int32_t n_seg, const int32_t* seg_start,
                               const int32_t* seg_slot, int32_t n_slots, TokenItem* gitems,

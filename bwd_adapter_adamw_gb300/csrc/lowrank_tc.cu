@@ -1010,6 +1010,9 @@ cudaError_t launch_make_red_items_tc(int64_t T, int32_t n_seg, const int32_t* se
                                      const int32_t* seg_slot, int32_t n_slots, int32_t span_blocks,
                                      TokenItem* items, int32_t* count, int32_t max_items,
                                      cudaStream_t st) {
+  if (seg_start && seg_slot && n_seg >= 1 && n_seg <= 2048 && T <= INT32_MAX - 64)
+    return launch_make_red_items_par(T, n_seg, seg_start, seg_slot, n_slots, span_blocks, items,
+                                     count, max_items, st);
   prof_begin(0, st);
   launch_kernel(k_make_red_items_tc, 1, 128, 0, st, T, n_seg, seg_start, seg_slot, n_slots, span_blocks,
                                          items, count, max_items);
