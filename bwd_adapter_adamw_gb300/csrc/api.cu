@@ -874,8 +874,10 @@ int fused_from_table(const lora_desc* d, int32_t n_proj, const lora_proj* tab, b
 // projections sit side by side after it.
 struct FusedLayout {
   Layout L;
-  float* Gcat;    // [T, n r]
-  float* Atcat;   // [in, n r]
+  float* Gcat;     // [T, n r]
+  float* Atcat;    // [in, n r]
+  uint16_t* Sbk;   // per projection [2 r, out_k] bf16 split of B_k^T, one after the other
+  uint16_t* Sacat; // per projection [2 r, in] bf16 split of A_k, one after the other
   size_t bytes;
 };
 
@@ -888,6 +890,8 @@ FusedLayout fused_carve(const lora_desc* d, int64_t T, const FusedProjs& f, void
   c.off = F.L.bytes;
   F.Gcat = c.take<float>((size_t)T * f.n * d->rank);
   F.Atcat = c.take<float>((size_t)d->in_dim * f.n * d->rank);
+  F.Sbk = c.take<uint16_t>((size_t)2 * d->rank * d->out_dim);   // sum of out_k = out_dim
+  F.Sacat = c.take<uint16_t>((size_t)2 * d->rank * f.n * d->in_dim);
   F.bytes = c.off + kWsAlign;
   return F;
 }
@@ -1000,22 +1004,45 @@ int run_fused_forward(const lora_desc* d, const DropParams& dp, int64_t T, const
     LORA_TRY(launch_mask_bf16(X, T, d->in_dim, dp, L.Xd, st));
     Xin = L.Xd;
   }
-  for (int k = 0; k < f.n; ++k) {   // Hs_k = s' Xd A_k^T into columns k r .. of H
+  const int64_t np = 2 * ldh;
+  if ((np == 256 || np == 384 || np == 512) && r % 16 == 0) {
+    // one shrink for the group: X read once against every A_k (their splits side by side), Hs_k
+    // into columns k r .. of H
     SplitTab sp{};
     sp.K = d->in_dim;
-    sp.src[0] = f.A[k];
-    sp.dst[0] = L.Sa;
-    sp.rank[0] = (int32_t)r;
-    LORA_TRY(launch_split(sp, 1, st));
+    for (int k = 0; k < f.n; ++k) {
+      sp.src[k] = f.A[k];
+      sp.dst[k] = F.Sacat + (int64_t)k * 2 * r * d->in_dim;
+      sp.rank[k] = (int32_t)r;
+    }
+    LORA_TRY(launch_split(sp, f.n, st));
     TcRowsArgs a{};
     a.a = Xin; a.T = T; a.K = d->in_dim; a.n_slots = 1;
-    a.s[0] = L.Sa; a.rank[0] = (int32_t)r;
-    a.NP = np_for((int)r);
+    a.s[0] = F.Sacat; a.rank[0] = (int32_t)ldh;
+    a.NP = (int32_t)np; a.pair_r = (int32_t)r;
     a.splits = row_splits(T, -1, d->in_dim);
-    a.si = si;
-    a.out = H + k * r; a.ldo = r; a.ld_out = ldh;
+    a.si = si; a.si.rank[0] = (int32_t)ldh;
+    a.out = H; a.ldo = ldh; a.ld_out = ldh;
     a.items = nullptr; a.n_items = nullptr; a.max_items = (int)L.gmax;
     LORA_TRY(launch_tc_rows(a, st, LORA_PROF_SHRINK));
+  } else {
+    for (int k = 0; k < f.n; ++k) {   // Hs_k = s' Xd A_k^T into columns k r .. of H
+      SplitTab sp{};
+      sp.K = d->in_dim;
+      sp.src[0] = f.A[k];
+      sp.dst[0] = L.Sa;
+      sp.rank[0] = (int32_t)r;
+      LORA_TRY(launch_split(sp, 1, st));
+      TcRowsArgs a{};
+      a.a = Xin; a.T = T; a.K = d->in_dim; a.n_slots = 1;
+      a.s[0] = L.Sa; a.rank[0] = (int32_t)r;
+      a.NP = np_for((int)r);
+      a.splits = row_splits(T, -1, d->in_dim);
+      a.si = si;
+      a.out = H + k * r; a.ldo = r; a.ld_out = ldh;
+      a.items = nullptr; a.n_items = nullptr; a.max_items = (int)L.gmax;
+      LORA_TRY(launch_tc_rows(a, st, LORA_PROF_SHRINK));
+    }
   }
   TcGemmArgs t{};
   t.a = X; t.T = T; t.b = W; t.n_rows = d->out_dim; t.K = d->in_dim;
@@ -1041,16 +1068,30 @@ int run_fused_backward(const lora_desc* d, const DropParams& dp, int64_t T, cons
   use_uniform_items(L, T);
   const int64_t r = d->rank, ldh = (int64_t)f.n * r;
   const SlotInfo si = fused_slot_info(d);
-  {   // A_k^T into columns k r .. of A^T_cat [in, n r] for the dX product's LoRA term
+  // one launch: A_k^T into columns k r .. of A^T_cat [in, n r] for the dX product's LoRA term,
+  // and the bf16 split of every B_k^T for its G product
+  uint16_t* sbk[LORA_MAX_SLOTS];
+  {
     TransposeTab ta{};
+    SplitTab sp{};
+    sp.transposed = 1;
+    sp.K = f.out[0];
+    int64_t kk[LORA_MAX_SLOTS];
+    int64_t ob = 0;
     for (int k = 0; k < f.n; ++k) {
       ta.src[k] = f.A[k];
       ta.dst[k] = F.Atcat + k * r;
       ta.rows[k] = r;
       ta.cols[k] = d->in_dim;
       ta.ld_dst[k] = ldh;
+      sbk[k] = F.Sbk + ob;
+      sp.src[k] = f.B[k];
+      sp.dst[k] = sbk[k];
+      sp.rank[k] = (int32_t)r;
+      kk[k] = f.out[k];
+      ob += 2 * r * f.out[k];
     }
-    LORA_TRY(launch_transpose_slots(ta, f.n, r, d->in_dim, st));
+    LORA_TRY(launch_adapter_prep(ta, sp, f.n, st, kk));
   }
   const void* Xin = X;
   if (dp.enabled) {
@@ -1063,22 +1104,16 @@ int run_fused_backward(const lora_desc* d, const DropParams& dp, int64_t T, cons
   rt.rank[0] = (int32_t)r;
   for (int k = 0; k < f.n; ++k) {
     // G_k = s' dY_k B_k (projection k's columns of dY) into columns k r .. of G, with its
-    // transposed split for dA_k
-    SplitTab sp{};
-    sp.K = f.out[k];
-    sp.transposed = 1;
-    sp.src[0] = f.B[k];
-    sp.dst[0] = L.Sb;
-    sp.rank[0] = (int32_t)r;
-    LORA_TRY(launch_split(sp, 1, st));
+    // transposed split for dA_k and, as a side task, the transposed split of the saved Hs_k
     TcRowsArgs g{};
     g.a = dYb + f.off[k]; g.lda = d->out_dim; g.T = T; g.K = f.out[k]; g.n_slots = 1;
-    g.s[0] = L.Sb; g.rank[0] = (int32_t)r;
+    g.s[0] = sbk[k]; g.rank[0] = (int32_t)r;
     g.NP = np_for((int)r);
     g.splits = row_splits(T, -1, f.out[k]);
     g.si = si;
     g.out = F.Gcat + k * r; g.ldo = r; g.ld_out = ldh;
     g.outT = L.GsT; g.ldt = L.ldt; g.outT_bytes = split_bytes;
+    g.side_h = H + k * r; g.side_ldh = ldh; g.side_outT = L.HsT;
     g.items = nullptr; g.n_items = nullptr; g.max_items = (int)L.gmax;
     LORA_TRY(launch_tc_rows(g, st, LORA_PROF_G));
     // dA_k += Gs_k^T Xd
@@ -1090,8 +1125,6 @@ int run_fused_backward(const lora_desc* d, const DropParams& dp, int64_t T, cons
     a.items = nullptr; a.n_items = nullptr;
     LORA_TRY(launch_tc_red(a, st, LORA_PROF_RED_DA));
     // dB_k += dY_k^T Hs_k
-    LORA_TRY(launch_split_rows_t(H + k * r, ldh, r, L.ldt, nullptr, nullptr, (int)L.gmax, si,
-                                 L.HsT, split_bytes, T, st));
     TcRedArgs b{};
     b.st[0] = L.HsT; b.rank[0] = (int32_t)r; b.n_slots = 1; b.max_rank = (int32_t)r;
     b.T = T; b.ldt = L.ldt; b.b = dYb + f.off[k]; b.ldb = d->out_dim; b.N = f.out[k];

@@ -101,7 +101,10 @@ struct TcRowsArgs {                 // out[t, j] = alpha * (A[t, :] . (S_hi[j] +
   const uint16_t* s[LORA_MAX_SLOTS];   // per slot [2 r, K] bf16 split (hi rows, lo rows)
   int32_t rank[LORA_MAX_SLOTS];
   int32_t n_slots;
-  int32_t NP;                       // MMA N: 16, 32, 64 or 128 (>= 2 * max rank)
+  int32_t NP;                       // MMA N: 16, 32, 64 or 128 (>= 2 * max rank), or 256, 384,
+                                    //   512 for adapters side by side (one slot, rank = their
+                                    //   total, NP = 2 rank, the split of each in turn)
+  int32_t pair_r;                   // NP > 128: rank of each side-by-side adapter
   int32_t splits;                   // K splits: CTAs of one cluster (1, 2, 4 or 8)
   SlotInfo si;
   float* out;                       // [T, ld_out] fp32 (columns < ldo written)
@@ -262,9 +265,10 @@ cudaError_t launch_transpose_slots(const TransposeTab& t, int n, int64_t max_row
 struct AdapterPrepTiles {
   int32_t n, n_t;                       // (task, slot) units; the first n_t are transposes
   int32_t first[2 * LORA_MAX_SLOTS];    // first tile of each unit
+  int64_t split_k[LORA_MAX_SLOTS];      // rows of B_slot (its K) for the splits; 0: SplitTab.K
 };
 cudaError_t launch_adapter_prep(const TransposeTab& ta, const SplitTab& sb, int n,
-                                cudaStream_t st);
+                                cudaStream_t st, const int64_t* split_k = nullptr);
 // fp32 fused projections as one adapter of rank n r: A_cat = [A_0; ...; A_{n-1}] ([n r, in]) and
 // the block-diagonal B_cat ([off[n], n r]: B_k in rows off[k].., columns k r..; zeros elsewhere)
 struct CatTab {

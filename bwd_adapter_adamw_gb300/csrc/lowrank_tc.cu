@@ -59,21 +59,33 @@ struct RowsParams {
   const float* side_h;
   int64_t side_ldh;
   uint16_t* side_outT;
+  int32_t pair_r;                    // wide tiles: hi / lo block width of each adapter
   int64_t T;
 };
 
+// NP <= 128: one adapter, N = NP >= 2 r (hi rows then lo rows), the raw tile staged and its hi
+// and lo columns added in place. NP 256-512: several adapters side by side (the bf16 split of
+// each in turn, hi rows then lo rows of pair_r each), two MMAs of N = NP / 2 per K-step above
+// N 256, hi and lo added while the accumulator is read, so only the NP / 2 result columns are
+// staged.
 template <int NP>
 struct RowsCfg {
+  static constexpr bool kWide = NP > 128;
   static constexpr int kBBytes = NP * 128;
   static constexpr int kStageBytes = 16384 + kBBytes;
   // one CTA per SM with about 192 KB of stages in flight
   static constexpr int kStages = (192 * 1024 / kStageBytes) < 10 ? (192 * 1024 / kStageBytes) : 10;
   static constexpr int kSmem = kStages * kStageBytes + 1024 + 1024;
-  static constexpr int kLdb = NP + 4;   // staging row stride of the partial tile (floats)
+  static constexpr int kLdb = (kWide ? NP / 2 : NP) + 4;   // staging row stride (floats)
   static_assert(kStages >= 2, "pipeline depth");
   static_assert(kBM * kLdb * 4 <= kStages * kStageBytes, "partial tile fits the stages");
-  static constexpr uint32_t kCols = NP < 32 ? 32u : (uint32_t)NP;
-  static constexpr uint32_t kIdesc = idesc(kFmtBF16, kBM, NP);
+  static_assert(NP <= 512, "TMEM columns");
+  // TMEM is allocated in powers of two columns (32 .. 512)
+  static constexpr uint32_t kCols = NP <= 32 ? 32u : NP <= 64 ? 64u : NP <= 128 ? 128u
+                                    : NP <= 256 ? 256u : 512u;
+  static constexpr int kMmaN = NP > 256 ? NP / 2 : NP;   // one or two MMAs per K-step
+  static constexpr uint32_t kIdesc = idesc(kFmtBF16, kBM, kMmaN);
+  static constexpr int kBoxRows = NP > 256 ? NP / 2 : NP;   // TMA boxes hold at most 256 rows
 };
 
 // One work item (<= 128 tokens, one slot) per cluster of `splits` CTAs along y; CTA z multiplies
@@ -141,7 +153,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_rows(const __grid_constant__
         uint8_t* sa = base + s * C::kStageBytes;
         mbar_expect_tx(&full_bar[s], C::kStageBytes);
         tma_load_2d(sa, &p.ta, &full_bar[s], (kb0 + i) * 64, it.t0);
-        tma_load_2d(sa + 16384, &p.ts[it.slot], &full_bar[s], (kb0 + i) * 64, 0);
+#pragma unroll
+        for (int h = 0; h < NP / C::kBoxRows; ++h)
+          tma_load_2d(sa + 16384 + h * C::kBoxRows * 128, &p.ts[it.slot], &full_bar[s],
+                      (kb0 + i) * 64, h * C::kBoxRows);
         issued = i + 1;
       }
       // every issued load has landed before the stages are reused as the partial tile
@@ -157,8 +172,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_rows(const __grid_constant__
         const uint32_t sa = smem_u32(base + s * C::kStageBytes);
         const uint64_t da = smem_desc_sw128(sa), db = smem_desc_sw128(sa + 16384);
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
+        for (int k = 0; k < 4; ++k) {
           umma_f16(tmem, da + 2 * k, db + 2 * k, C::kIdesc, (i > 0 || k > 0) ? 1u : 0u);
+          if constexpr (NP > 256)   // the second half of the rows: 1024-byte atoms, so +NP/2 * 8
+            umma_f16(tmem + (uint32_t)(NP / 2), da + 2 * k, db + (uint64_t)(NP / 2) * 8 + 2 * k,
+                     C::kIdesc, (i > 0 || k > 0) ? 1u : 0u);
+        }
         umma_commit(&empty_bar[s]);
       }
       if (nk > 0) umma_commit(acc_bar);   // with no K-blocks the epilogue does not wait
@@ -192,7 +211,27 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_rows(const __grid_constant__
     ready = nk == 0 || __all_sync(0xffffffffu, mbar_wait(acc_bar, 0u, 4u, p.err));
     if (ready) fence_after();
     float* br = buf + row * C::kLdb;
-    if (ready && nk > 0) {
+    if constexpr (C::kWide) {
+      // output column o: adapter o / pair_r, hi column 2 pair_r (o / pair_r) + o % pair_r, its lo
+      // column pair_r further on; 16 columns at a time
+      const int pr = p.pair_r;
+      for (int o = 0; o < NP / 2; o += 16) {
+        float h[16], l[16];
+        if (ready && nk > 0) {
+          const int hc = 2 * pr * (o / pr) + (o % pr);
+          tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)hc, h);
+          tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(hc + pr), l);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) h[e] = l[e] = 0.f;
+        }
+        float4* dst = reinterpret_cast<float4*>(br + o);
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+          dst[g] = make_float4(h[4 * g] + l[4 * g], h[4 * g + 1] + l[4 * g + 1],
+                               h[4 * g + 2] + l[4 * g + 2], h[4 * g + 3] + l[4 * g + 3]);
+      }
+    } else if (ready && nk > 0) {
 #pragma unroll
       for (int c = 0; c < NP / 16; ++c) {
         float v[16];
@@ -599,7 +638,7 @@ __global__ void __launch_bounds__(256) k_adapter_prep(const TransposeTab ta, con
   const bool split = u >= pt.n_t;                 // tasks: transposes first, then splits
   const int k = split ? u - pt.n_t : u;           // slot
   const int local = (int)blockIdx.x - pt.first[u];
-  const int64_t rows = split ? sb.K : ta.rows[k];          // src rows (B: out, A: r)
+  const int64_t rows = split ? (pt.split_k[k] > 0 ? pt.split_k[k] : sb.K) : ta.rows[k];   // src rows (B: out, A: r)
   const int64_t cols = split ? sb.rank[k] : ta.cols[k];    // src cols (B: r, A: in)
   const int64_t ncb = (cols + 31) / 32;
   const int64_t r0 = (int64_t)(local / ncb) * 32, c0 = (int64_t)(local % ncb) * 32;
@@ -768,17 +807,25 @@ cudaError_t launch_tc_rows(const TcRowsArgs& a, cudaStream_t st, int prof_kind) 
   if (!tc::make_map_2d(&prm.ta, a.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.K, a.T,
                        a.lda > 0 ? a.lda : a.K, 64, kBM))
     return cudaErrorInvalidValue;
+  const bool wide = NP > 128;
+  const uint32_t box_rows = NP > 256 ? (uint32_t)NP / 2 : (uint32_t)NP;
   for (int k = 0; k < a.n_slots; ++k)
     if (!tc::make_map_2d(&prm.ts[k], a.s[k], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.K,
-                         2 * (uint64_t)a.rank[k], a.K, 64, (uint32_t)NP))
+                         2 * (uint64_t)a.rank[k], a.K, 64, box_rows))
       return cudaErrorInvalidValue;
   for (int k = 0; k < a.n_slots; ++k)
     if (2 * a.rank[k] > NP || a.rank[k] > a.ldo || a.rank[k] % 4 || a.si.rank[k] != a.rank[k])
       return cudaErrorInvalidValue;
   // the cluster splits the 128 token rows evenly: 1, 2, 4 or 8 CTAs
   if (a.splits < 1 || a.splits > kMaxSplitsRows || (a.splits & (a.splits - 1)) || a.ldo % 4 ||
-      a.ldo > LORA_MAX_RANK)
+      a.ldo > (wide ? NP / 2 : LORA_MAX_RANK))
     return cudaErrorInvalidValue;
+  // wide tiles: one item table slot whose rank is the adapters' total, NP = twice it, adapters of
+  // pair_r columns (a multiple of 16 dividing the total); no transposed outputs
+  if (wide && (a.n_slots != 1 || 2 * a.rank[0] != NP || a.pair_r < 16 || a.pair_r % 16 ||
+               a.rank[0] % a.pair_r || a.outT || a.side_h || a.items))
+    return cudaErrorInvalidValue;
+  prm.pair_r = wide ? a.pair_r : a.rank[0];
   prm.items = a.items;
   prm.n_items = a.n_items;
   prm.err = tc::error_word();
@@ -829,6 +876,9 @@ cudaError_t launch_tc_rows(const TcRowsArgs& a, cudaStream_t st, int prof_kind) 
     LORA_ROWS_CASE(32)
     LORA_ROWS_CASE(64)
     LORA_ROWS_CASE(128)
+    LORA_ROWS_CASE(256)
+    LORA_ROWS_CASE(384)
+    LORA_ROWS_CASE(512)
 #undef LORA_ROWS_CASE
     default:
       return cudaErrorInvalidValue;
@@ -955,17 +1005,18 @@ cudaError_t launch_tc_red(const TcRedArgs& a, cudaStream_t st, int prof_kind) {
 }
 
 cudaError_t launch_adapter_prep(const TransposeTab& ta, const SplitTab& sb, int n,
-                                cudaStream_t st) {
+                                cudaStream_t st, const int64_t* split_k) {
   if (n <= 0) return cudaSuccess;
   if (!sb.transposed || n > LORA_MAX_SLOTS) return cudaErrorInvalidValue;
   AdapterPrepTiles pt{};
   pt.n_t = n;
   pt.n = 2 * n;
+  for (int k = 0; k < n; ++k) pt.split_k[k] = split_k ? split_k[k] : 0;
   int total = 0;
   for (int u = 0; u < 2 * n; ++u) {
     const bool split = u >= n;
     const int k = split ? u - n : u;
-    const int64_t rows = split ? sb.K : ta.rows[k];
+    const int64_t rows = split ? (pt.split_k[k] > 0 ? pt.split_k[k] : sb.K) : ta.rows[k];
     const int64_t cols = split ? sb.rank[k] : ta.cols[k];
     pt.first[u] = total;
     total += (int)(((rows + 31) / 32) * ((cols + 31) / 32));
