@@ -149,11 +149,6 @@ struct SplitTab {
 cudaError_t launch_tc_rows(const TcRowsArgs& a, cudaStream_t st, int prof_kind);
 cudaError_t launch_tc_red(const TcRedArgs& a, cudaStream_t st, int prof_kind);
 cudaError_t launch_split(const SplitTab& t, int n, cudaStream_t st);
-// src [T, lds] fp32, columns 0 .. ncols - 1 (the largest rank); dst per slot [2 r, ldt] bf16
-cudaError_t launch_split_rows_t(const float* src, int64_t lds, int64_t ncols, int64_t ldt,
-                                const TokenItem* items,
-                                const int32_t* n_items, int max_items, const SlotInfo& si,
-                                uint16_t* dst, size_t dst_bytes, int64_t T, cudaStream_t st);
 // count[0] = the number of items; count[1 + k] (k = 0 .. n_slots) = the first item of slot k, the
 // items being grouped by slot in slot order (count needs n_slots + 2 entries).
 cudaError_t launch_make_red_items_tc(int64_t T, int32_t n_seg, const int32_t* seg_start,

@@ -7,15 +7,15 @@
 // (x = hi + lo + O(2^-16 |x|)); both parts are multiplied against the exact bf16 activations, so
 // the products keep fp32-level accuracy while running on kind::f16 tensor cores.
 //
-//  k_tc_rows: part[z][t][j] = sum_{k in split z} A[t, k] (S_slot[j, k] + S_slot[r + j, k])
-//             (shrink, G). M = 128 tokens of one work item, N = NP >= 2 r (hi rows then lo
-//             rows), K-major; the epilogue adds the hi and lo columns.
-//  k_tc_red:  part[item][j][n] = sum_{t in item} (ST_slot[j, t] + ST_slot[r + j, t]) Bmn[t, n]
-//             (dA, dB^T). M = 128 (2 r rows of the slot's transposed split), N = 256 columns of
-//             dY or X (MN-major tiles), K = the item's tokens in 64-token blocks; the epilogue adds
-//             the hi and lo rows.
-// Both run two CTAs per SM so that one CTA's prologue and epilogue overlap the other's stream.
-// Partials are combined in a fixed order by the finish kernels, so reruns are bitwise equal.
+//  k_tc_rows: out[t, j] = alpha * sum_k A[t, k] (S[j, k] + S[r + j, k]) (shrink, G). M = 128
+//             tokens of one work item, N = NP >= 2 r (hi rows then lo rows; or several adapters'
+//             splits side by side), K split over a thread-block cluster of 1-8 CTAs.
+//  k_tc_red:  dst += sum_t (ST[j, t] + ST[r + j, t]) Bmn[t, n] (dA, dB^T). M = 128 (2 r rows of
+//             the slot's transposed split), N = 256 or 128 columns of dY' or Xd (MN-major
+//             tiles), K = tokens in 64-token blocks split over a cluster of up to 16 CTAs.
+// One CTA per SM with about 192 KB of stages in flight. The split partials stay in shared memory
+// and the cluster adds them in split order through distributed shared memory, so no partial
+// reaches global memory and reruns are bitwise equal.
 #include <cstring>
 #include <mutex>
 
@@ -303,81 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_rows(const __grid_constant__
   }
 }
 
-// out[t, j] = alpha_slot * sum_z part[z][t][j] for j < r, 0 for r <= j < ncols (alpha_slot = 1
-// when use_alpha is 0; out may be null); ldp and ld_out are the row strides of part and out. With outT, also the transposed bf16 split that the token
-// reductions take as their K-major operand:
-// outT[region_slot + j][t] = hi(out[t, j]), outT[region_slot + r + j][t] = lo(out[t, j]).
-// CTA (item, blockIdx.y) covers kFinishTok tokens of the item; every thread issues all of its
-// loads (kFinishVec float4 groups x the splits) before the first add.
-constexpr int kFinishTok = 32;
-constexpr int kFinishThreads = 256;
-constexpr int kFinishVec = kFinishTok * LORA_MAX_RANK / 4 / kFinishThreads;
 constexpr int kMaxSplitsRows = 8;   // K splits of the rows kernel (the launcher rejects more)
-__global__ void __launch_bounds__(kFinishThreads) k_rows_finish(
-    const float* __restrict__ part, int32_t splits, int64_t T, int64_t ldp, int32_t ncols,
-    int use_alpha,
-    const TokenItem* __restrict__ items, const int32_t* __restrict__ n_items, const SlotInfo si,
-    float* __restrict__ out, int64_t ld_out, float* __restrict__ out2, int64_t ld2,
-    uint16_t* __restrict__ outT, int64_t ldt) {
-  grid_dep_sync();
-  __shared__ float tile[kFinishTok][LORA_MAX_RANK + 1];
-  TokenItem it;
-  if (!get_item(items, n_items, blockIdx.x, T, it)) return;
-  const int64_t tb = (int64_t)it.t0 + (int64_t)blockIdx.y * kFinishTok;
-  if (tb >= it.t1) return;
-  const int32_t r = it.slot >= 0 ? si.rank[it.slot] : 0;
-  const float alpha = !use_alpha ? 1.f : it.slot >= 0 ? si.alpha[it.slot] : 0.f;
-  const int nt = (int)min((int64_t)kFinishTok, (int64_t)it.t1 - tb);
-  const int c4n = ncols / 4;   // float4 groups per token: columns 0 .. ncols - 1
-  const int n4 = nt * c4n;
-  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
-  float4 pz[kFinishVec][kMaxSplitsRows];
-#pragma unroll
-  for (int u = 0; u < kFinishVec; ++u) {
-    const int q = threadIdx.x + u * kFinishThreads;
-    const int i = q / c4n, c = q - i * c4n;
-    const bool live = q < n4 && 4 * c < r;
-    const float4* src = reinterpret_cast<const float4*>(part + (tb + i) * ldp) + c;
-#pragma unroll
-    for (int z = 0; z < kMaxSplitsRows; ++z)
-      pz[u][z] = (live && z < splits) ? src[(int64_t)z * T * c4n] : zero;
-  }
-#pragma unroll
-  for (int u = 0; u < kFinishVec; ++u) {
-    const int q = threadIdx.x + u * kFinishThreads;
-    if (q >= n4) continue;
-    const int i = q / c4n, c = q - i * c4n;
-    float4 v = zero;
-    if (4 * c < r) {
-#pragma unroll
-      for (int z = 0; z < kMaxSplitsRows; ++z)
-        if (z < splits) {
-          v.x += pz[u][z].x;
-          v.y += pz[u][z].y;
-          v.z += pz[u][z].z;
-          v.w += pz[u][z].w;
-        }
-      v = make_float4(v.x * alpha, v.y * alpha, v.z * alpha, v.w * alpha);
-      tile[i][4 * c] = v.x;
-      tile[i][4 * c + 1] = v.y;
-      tile[i][4 * c + 2] = v.z;
-      tile[i][4 * c + 3] = v.w;
-    }
-    if (out) reinterpret_cast<float4*>(out + (tb + i) * ld_out)[c] = v;
-    if (out2 && 4 * c < r)   // the slot-expanded copy: the slot's own column block
-      reinterpret_cast<float4*>(out2 + (tb + i) * ld2 + si.pcol[it.slot])[c] = v;
-  }
-  if (!outT || it.slot < 0) return;   // uniform over the CTA
-  __syncthreads();
-  uint16_t* d = outT + (int64_t)si.region[it.slot] * ldt + tb;
-  for (int e = threadIdx.x; e < nt * r; e += kFinishThreads) {
-    const int j = e / nt, i = e - j * nt;
-    const float x = tile[i][j];
-    const uint16_t hb = bf16_bits(x);
-    d[(int64_t)j * ldt + i] = hb;
-    d[(int64_t)(r + j) * ldt + i] = bf16_bits(x - bf16_val(hb));
-  }
-}
 
 // ---------------------------------------------------------------------------------------------
 // k_tc_red
@@ -1035,25 +961,6 @@ cudaError_t launch_split(const SplitTab& t, int n, cudaStream_t st) {
   if (blocks > 4096) blocks = 4096;
   prof_begin(0, st);
   launch_kernel(k_split, dim3((unsigned)blocks, 1, (unsigned)n), 256, 0, st, t);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_split_rows_t(const float* src, int64_t lds, int64_t ncols, int64_t ldt,
-                                const TokenItem* items,
-                                const int32_t* n_items, int max_items, const SlotInfo& si,
-                                uint16_t* dst, size_t dst_bytes, int64_t T, cudaStream_t st) {
-  if (max_items <= 0) return cudaSuccess;
-  // With an item table, tokens of other slots must read as zero in each slot's rows. A null table
-  // (single adapter) writes every token of the one slot, and the tensor maps stop at T.
-  if (items) {
-    cudaError_t e = cudaMemsetAsync(dst, 0, dst_bytes, st);
-    if (e != cudaSuccess) return e;
-  }
-  if (lds % 4 || ncols % 4 || ncols > LORA_MAX_RANK || ncols > lds) return cudaErrorInvalidValue;
-  prof_begin(0, st);
-  launch_kernel(k_rows_finish, dim3((unsigned)max_items, (unsigned)(kBM / kFinishTok)), kFinishThreads, 0, st, 
-      src, 1, T, lds, (int32_t)ncols, 0, items, n_items, si, nullptr, (int64_t)0, nullptr,
-      (int64_t)0, dst, ldt);
   return cudaGetLastError();
 }
 
