@@ -114,9 +114,9 @@ def memory_counts(cfg: LI.LoraConfig, layers: int, groups=None):
         n = len(idx)   # adapters of the group: n r columns of Hs / G, n A's of [r, in]
         out["shrink"] += T * i * a + n * r_all * i * 4 + T * n * r_row * 4 + split * T * i
         out["G"] += T * o * a + r_all * o * 4 + T * n * r_row * 4 + split * T * o
-        if cfg.dtype != "f32" and not groups and not cfg.multi:
+        if cfg.dtype != "f32" and not cfg.multi:
             # the bf16 G product also writes the transposed bf16 split of Gs (for dA) and, as a
-            # side task, reads the saved Hs and writes its transposed split (for dB)
+            # side task, reads the saved Hs and writes its transposed split (for dB), per adapter
             out["G"] += 3 * 4 * T * n * r_row
         out["redB"] += T * o * a + T * n * r_row * 4 + 2 * r_all * o * 4
         out["redA"] += T * i * a + T * n * r_row * 4 + 2 * n * r_all * i * 4

@@ -146,6 +146,17 @@ struct SplitTab {
   int64_t K;
   int32_t transposed;               // src is [K, r] instead of [r, K]
 };
+// dA of n (2 .. 4) adapters of rank r that read one input, the input streamed once:
+// dst[m] [r, N] += sum_t (ST_m[j, t] + ST_m[r + j, t]) B[t, n] over all T tokens
+struct TcRedMultiArgs {
+  const uint16_t* st[LORA_MAX_SLOTS];  // per adapter [2 r, ldt] bf16 transposed split
+  float* dst[LORA_MAX_SLOTS];
+  int32_t n, r;
+  int64_t T, ldt;
+  const void* b;                        // [T, N] bf16, row stride ldb
+  int64_t N, ldb;
+};
+cudaError_t launch_tc_red_multi(const TcRedMultiArgs& a, cudaStream_t st, int prof_kind);
 cudaError_t launch_tc_rows(const TcRowsArgs& a, cudaStream_t st, int prof_kind);
 cudaError_t launch_tc_red(const TcRedArgs& a, cudaStream_t st, int prof_kind);
 cudaError_t launch_split(const SplitTab& t, int n, cudaStream_t st);

@@ -550,6 +550,186 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_red(const __grid_constant__ 
 }
 
 // ---------------------------------------------------------------------------------------------
+// k_tc_red_multi: dA of several adapters that read one input (fused projections)
+// ---------------------------------------------------------------------------------------------
+// dA_m [r, N] += (ST_m[hi] + ST_m[lo])^T-rows x Xd over all tokens, for NA adapters of rank r
+// (2 r <= 128) at once: per 64-token block the stage holds each adapter's [2 r, 64] transposed
+// split (an M = 128 tile each) and one [64, 128] tile of Xd, so Xd is read once for the group;
+// NA MMAs per K-step into TMEM columns m * 128 .. . The token split and its cluster reduction
+// are those of k_tc_red.
+constexpr int kRedMultiBN = 128;
+template <int NA>
+struct RedMultiCfg {
+  static constexpr int kStageBytes = NA * 16384 + kRedMultiBN * 128;
+  static constexpr int kStages = (192 * 1024) / kStageBytes;
+  static constexpr int kSmem = kStages * kStageBytes + 1024 + 1024;
+  static constexpr int kLd = kRedMultiBN + 4;                   // staging [m][r][kLd]
+  static constexpr int kStagingFloats = NA * LORA_MAX_RANK * kLd;
+  static_assert(kStages >= 2, "pipeline depth");
+  static_assert(kStagingFloats * 4 <= kStages * kStageBytes, "staging fits the stages");
+  static_assert(NA * kRedMultiBN <= 512, "TMEM columns");
+  static constexpr uint32_t kCols = NA * kRedMultiBN <= 256 ? 256u : 512u;
+  static constexpr uint32_t kIdesc = idesc(kFmtBF16, kBM, kRedMultiBN, false, true);
+};
+
+struct RedMultiParams {
+  CUtensorMap tst[LORA_MAX_SLOTS];   // ST_m [2 r, T] bf16, box {64, 128}
+  CUtensorMap tb;                    // Xd [T, N] bf16, box {64 (n), 64 (t)}
+  uint32_t* err;
+  float* dst[LORA_MAX_SLOTS];        // dA_m [r, N]
+  int32_t r;
+  int64_t N;
+  int64_t T;
+};
+
+template <int NA>
+__global__ void __launch_bounds__(kThreads, 1) k_tc_red_multi(const __grid_constant__ RedMultiParams p) {
+  grid_dep_sync();
+  using C = RedMultiCfg<NA>;
+  extern __shared__ uint8_t smem_raw[];
+  const int z = blockIdx.y;   // == rank in the cluster (cluster dims 1 x splits)
+  const int splits = gridDim.y;
+  const int32_t n0 = blockIdx.x * kRedMultiBN;
+  const int r = p.r;
+  // this CTA's 64-token blocks: the same runs of kRedSpanBlocks blocks as the single-adapter form
+  const int32_t nb_all = (int32_t)((p.T + 63) / 64);
+  const int32_t n_runs = (nb_all + kRedSpanBlocks - 1) / kRedSpanBlocks;
+  const int32_t w0 = (int32_t)((int64_t)n_runs * z / splits);
+  const int32_t w1 = (int32_t)((int64_t)n_runs * (z + 1) / splits);
+  const int32_t blk0 = w0 * kRedSpanBlocks, blk1 = min(nb_all, w1 * kRedSpanBlocks);
+  const int nk = blk1 > blk0 ? blk1 - blk0 : 0;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(base + C::kStages * C::kStageBytes);
+  uint64_t* empty_bar = full_bar + C::kStages;
+  uint64_t* acc_bar = empty_bar + C::kStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_bar + 1);
+  float* buf = reinterpret_cast<float*>(base);   // staging over the idle stages
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    mbar_init(acc_bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, C::kCols);
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int i = 0;
+      for (; i < nk; ++i) {
+        const int s = i % C::kStages;
+        const uint32_t ph = (uint32_t)(i / C::kStages) & 1u;
+        if (i >= C::kStages && !mbar_wait(&empty_bar[s], ph ^ 1u, 1u, p.err)) break;
+        uint8_t* sa = base + s * C::kStageBytes;
+        mbar_expect_tx(&full_bar[s], C::kStageBytes);
+        const int32_t t = (blk0 + i) * 64;
+#pragma unroll
+        for (int m = 0; m < NA; ++m) tma_load_2d(sa + m * 16384, &p.tst[m], &full_bar[s], t, 0);
+#pragma unroll
+        for (int q = 0; q < kRedMultiBN / 64; ++q)
+          tma_load_2d(sa + NA * 16384 + q * 8192, &p.tb, &full_bar[s], n0 + 64 * q, t);
+      }
+      // every issued load has landed before the stages are reused as the staging tile
+      for (int k = (i > C::kStages ? i - C::kStages : 0); k < i; ++k)
+        if (!mbar_wait(&full_bar[k % C::kStages], (uint32_t)(k / C::kStages) & 1u, 1u, p.err)) break;
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      for (int i = 0; i < nk; ++i) {
+        const int s = i % C::kStages;
+        if (!mbar_wait(&full_bar[s], (uint32_t)(i / C::kStages) & 1u, 2u, p.err)) break;
+        fence_after();
+        const uint32_t sa = smem_u32(base + s * C::kStageBytes);
+        const uint64_t db = smem_desc_sw128_mn(sa + NA * 16384, 8192);
+#pragma unroll
+        for (int m = 0; m < NA; ++m) {
+          const uint64_t da = smem_desc_sw128(sa + m * 16384);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            umma_f16(tmem + (uint32_t)(m * kRedMultiBN), da + 2 * k, db + 128 * k, C::kIdesc,
+                     (i > 0 || k > 0) ? 1u : 0u);
+        }
+        umma_commit(&empty_bar[s]);
+      }
+      if (nk > 0) umma_commit(acc_bar);   // with no K-blocks the epilogue does not wait
+    }
+  } else {
+    // epilogue: per adapter, hi rows staged first, then lo rows added onto them
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    const bool ready = nk == 0 || __all_sync(0xffffffffu, mbar_wait(acc_bar, 0u, 4u, p.err));
+    if (ready) fence_after();
+    const bool live = ready && nk > 0;
+    for (int phase = 0; phase < 2; ++phase) {
+      const bool mine = phase == 0 ? row < r : (row >= r && row < 2 * r);
+      const int j = phase == 0 ? row : row - r;
+      for (int m = 0; m < NA; ++m) {
+#pragma unroll 1
+        for (int c = 0; c < kRedMultiBN / 32; ++c) {
+          float v[32];
+          if (live) {
+            tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(m * kRedMultiBN + c * 32), v);
+          } else {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) v[k] = 0.f;
+          }
+          if (!mine) continue;
+          float* d = buf + ((size_t)m * LORA_MAX_RANK + j) * C::kLd + c * 32;
+#pragma unroll
+          for (int g = 0; g < 8; ++g) {
+            float4 x = make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+            if (phase == 1) {
+              const float4 h = reinterpret_cast<const float4*>(d)[g];
+              x = make_float4(h.x + x.x, h.y + x.y, h.z + x.z, h.w + x.w);
+            }
+            reinterpret_cast<float4*>(d)[g] = x;
+          }
+        }
+      }
+      asm volatile("bar.sync 1, 128;" ::: "memory");   // the four epilogue warps
+    }
+    fence_before();
+  }
+  __syncthreads();
+  cluster_sync_all();   // every CTA's partial tiles are in its shared memory
+  // columns [z W, z W + W) of every adapter's rows, summed over the cluster in split order
+  const int W = kRedMultiBN / splits;
+  const int w4 = W / 4;
+  for (int e = threadIdx.x; e < NA * r * w4; e += kThreads) {
+    const int m = e / (r * w4), rem = e - m * (r * w4);
+    const int j = rem / w4, c = z * W + 4 * (rem - (rem / w4) * w4);
+    const int64_t n = (int64_t)n0 + c;
+    if (n >= p.N) continue;
+    float4 pz[kRedMaxSplits];
+#pragma unroll
+    for (int zz = 0; zz < kRedMaxSplits; ++zz)
+      if (zz < splits) pz[zz] = dsmem_ld4(buf + ((size_t)m * LORA_MAX_RANK + j) * C::kLd + c, (uint32_t)zz);
+    float4* o = reinterpret_cast<float4*>(p.dst[m] + (int64_t)j * p.N + n);
+    float4 acc = *o;
+    float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int zz = 0; zz < kRedMaxSplits; ++zz)
+      if (zz < splits) {
+        sum.x += pz[zz].x; sum.y += pz[zz].y; sum.z += pz[zz].z; sum.w += pz[zz].w;
+      }
+    acc.x += sum.x; acc.y += sum.y; acc.z += sum.z; acc.w += sum.w;
+    *o = acc;
+  }
+  cluster_sync_all();   // peers' shared memory stays alive until every CTA has read it
+  if (warp == 1) {
+    fence_after();
+    tmem_dealloc(tmem, C::kCols);
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
 // split helpers
 // ---------------------------------------------------------------------------------------------
 // The backward's adapter operands in one launch of 32 x 32 shared-memory tiles: A_slot^T (fp32,
@@ -951,6 +1131,80 @@ cudaError_t launch_adapter_prep(const TransposeTab& ta, const SplitTab& sb, int 
   prof_begin(0, st);
   launch_kernel(k_adapter_prep, dim3((unsigned)total), dim3(256), 0, st, ta, sb, pt);
   return cudaGetLastError();
+}
+
+template <int NA>
+int red_multi_resident(int size) {
+  static int cache[64][5];
+  static bool done[64] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!done[dev]) {
+    for (int i = 0; i < 5; ++i)
+      cache[dev][i] = resident_clusters(k_tc_red_multi<NA>, RedMultiCfg<NA>::kSmem, 1 << i);
+    done[dev] = true;
+  }
+  int i = 0;
+  while (i < 4 && (1 << i) < size) ++i;
+  return (1 << i) == size ? cache[dev][i] : 0;
+}
+
+template <int NA>
+cudaError_t launch_red_multi_na(const TcRedMultiArgs& a, cudaStream_t st, int prof_kind) {
+  static RedMultiParams prm;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lk(mu);
+  std::memset(&prm, 0, sizeof(prm));
+  const int sms = tc::sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  const int64_t tiles = (a.N + kRedMultiBN - 1) / kRedMultiBN;
+  int splits = 1;
+  for (int c = 2; c <= kRedMaxSplits; c *= 2) {
+    if (tiles * c > sms || (a.T + 63) / 64 < 2 * (int64_t)c) break;
+    if (tiles <= red_multi_resident<NA>(c)) splits = c;
+  }
+  for (int m = 0; m < NA; ++m) {
+    if (!tc::make_map_2d(&prm.tst[m], a.st[m], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T,
+                         2 * (uint64_t)a.r, a.ldt, 64, kBM))
+      return cudaErrorInvalidValue;
+    prm.dst[m] = a.dst[m];
+  }
+  if (!tc::make_map_2d(&prm.tb, a.b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.N, a.T,
+                       a.ldb > 0 ? a.ldb : a.N, 64, 64))
+    return cudaErrorInvalidValue;
+  prm.err = tc::error_word();
+  if (!prm.err) return cudaErrorInvalidDevice;
+  prm.r = a.r;
+  prm.N = a.N;
+  prm.T = a.T;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = set_smem(k_tc_red_multi<NA>, RedMultiCfg<NA>::kSmem);
+    if (e != cudaSuccess) return e;
+    if (cudaFuncSetAttribute(k_tc_red_multi<NA>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+        cudaSuccess)
+      cudaGetLastError();
+    attr = true;
+  }
+  dim3 grid((unsigned)tiles, (unsigned)splits, 1);
+  prof_begin(prof_kind, st);
+  cudaError_t e = launch_cluster_y(k_tc_red_multi<NA>, grid, splits, RedMultiCfg<NA>::kSmem, st, prm);
+  if (e != cudaSuccess) return e;
+  prof_end(prof_kind, st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tc_red_multi(const TcRedMultiArgs& a, cudaStream_t st, int prof_kind) {
+  if (a.T <= 0) return cudaSuccess;
+  if (a.r < 4 || a.r % 4 || 2 * a.r > kBM || a.r > LORA_MAX_RANK || a.N % 8) return cudaErrorInvalidValue;
+  switch (a.n) {
+    case 2: return launch_red_multi_na<2>(a, st, prof_kind);
+    case 3: return launch_red_multi_na<3>(a, st, prof_kind);
+    case 4: return launch_red_multi_na<4>(a, st, prof_kind);
+  }
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_split(const SplitTab& t, int n, cudaStream_t st) {
