@@ -834,6 +834,7 @@ def run_ours(args):
             kern_serial = serial_times(prof_class, n_prof)
         for name, cls in (("shrink", L.LORA_PROF_SHRINK), ("G", L.LORA_PROF_G),
                           ("redB", L.LORA_PROF_RED_DB), ("redA", L.LORA_PROF_RED_DA),
+                          ("red", L.LORA_PROF_RED),
                           ("prepare", L.LORA_PROF_PREPARE), ("adamw", L.LORA_PROF_ADAMW)):
             # the chained step launches each low-rank class once per chunk and layer
             mem_times[name] = serial_times(cls, max(n_prof, 8) * (cfg.chunks if args.chain else 1))
@@ -886,12 +887,14 @@ def run_ours(args):
         mem = memory_counts(cfg, layers if not cfg.multi else 1,
                             fused_groups(cfg) if args.fused else None)
         memory_bound = {}
+        # "red": the dB and dA reductions of a linear in one launch, both classes' bytes
+        class_bytes = dict(mem, red=mem["redB"] + mem["redA"])
         for name, ts in mem_times.items():
             if ts:
-                gbs = mem[name] / (sum(ts) / 1e3) / 1e9
+                gbs = class_bytes[name] / (sum(ts) / 1e3) / 1e9
                 memory_bound[name] = {"achieved_gbs": gbs, "frac": gbs / peaks["hbm_gbs"],
                                       "launches": len(ts), "ms_total": sum(ts),
-                                      "bytes_per_step": mem[name]}
+                                      "bytes_per_step": class_bytes[name]}
         # step-level bound: every frozen product at the tensor peak plus every memory-bound
         # class's algorithmic bytes at the HBM peak, against the measured step
         t_tensor = (cnt["fwd_flops"] + cnt["dx_flops"]) / (peak * 1e12) * 1e3

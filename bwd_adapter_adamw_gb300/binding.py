@@ -148,6 +148,7 @@ LORA_PROF_RED_DB = 5
 LORA_PROF_RED_DA = 6
 LORA_PROF_PREPARE = 7
 LORA_PROF_ADAMW = 8
+LORA_PROF_RED = 9
 
 
 def library_path() -> str:

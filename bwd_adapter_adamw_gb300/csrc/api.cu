@@ -570,34 +570,31 @@ int run_backward_tc(const lora_desc* d, const DropParams& dp, int64_t T, const v
     }
     LORA_TRY(launch_tc_gemm(t, st, LORA_PROF_FROZEN_DX));
   }
-  ReduceTab rt{};
-  for (int k = 0; k < s.n; ++k) rt.rank[k] = s.rank[k];
   // dB_k += dY'^T Hs over the slot's tokens (as dB^T rows of the transposed Hs split, written by
-  // the G product's CTAs)
-  {
-    TcRedArgs a{};
-    for (int k = 0; k < s.n; ++k) {
-      a.st[k] = L.HsT + (int64_t)si.region[k] * L.ldt;
-      a.rank[k] = s.rank[k];
-      rt.out[k] = s.dB[k];
-    }
-    a.n_slots = s.n; a.max_rank = d->rank; a.T = T; a.ldt = L.ldt;
-    a.b = dYp; a.N = d->out_dim; a.tab = rt; a.transposed = 1;
-    a.items = L.items_db; a.n_items = L.count_db;
-    LORA_TRY(launch_tc_red(a, st, LORA_PROF_RED_DB));
+  // the G product's CTAs) and dA_k += Gs^T Xd (GsT, written by the G product): one launch when
+  // both walk the same run table
+  TcRedArgs rb{}, ra{};
+  for (int k = 0; k < s.n; ++k) {
+    rb.st[k] = L.HsT + (int64_t)si.region[k] * L.ldt;
+    ra.st[k] = L.GsT + (int64_t)si.region[k] * L.ldt;
+    rb.rank[k] = ra.rank[k] = s.rank[k];
+    rb.tab.rank[k] = ra.tab.rank[k] = s.rank[k];
+    rb.tab.out[k] = s.dB[k];
+    ra.tab.out[k] = s.dA[k];
   }
-  // dA_k += Gs^T Xd over the slot's tokens (GsT was written by the G product's finish)
-  {
-    TcRedArgs a{};
-    for (int k = 0; k < s.n; ++k) {
-      a.st[k] = L.GsT + (int64_t)si.region[k] * L.ldt;
-      a.rank[k] = s.rank[k];
-      rt.out[k] = s.dA[k];
-    }
-    a.n_slots = s.n; a.max_rank = d->rank; a.T = T; a.ldt = L.ldt;
-    a.b = Xin; a.N = d->in_dim; a.tab = rt; a.transposed = 0;
-    a.items = L.items_da; a.n_items = L.count_da;
-    LORA_TRY(launch_tc_red(a, st, LORA_PROF_RED_DA));
+  rb.n_slots = ra.n_slots = s.n;
+  rb.max_rank = ra.max_rank = d->rank;
+  rb.T = ra.T = T;
+  rb.ldt = ra.ldt = L.ldt;
+  rb.b = dYp; rb.N = d->out_dim; rb.transposed = 1;
+  ra.b = Xin; ra.N = d->in_dim; ra.transposed = 0;
+  rb.items = L.items_db; rb.n_items = L.count_db;
+  ra.items = L.items_da; ra.n_items = L.count_da;
+  if (rb.items == ra.items && rb.n_items == ra.n_items) {
+    LORA_TRY(launch_tc_red2(rb, ra, st, LORA_PROF_RED));
+  } else {
+    LORA_TRY(launch_tc_red(rb, st, LORA_PROF_RED_DB));
+    LORA_TRY(launch_tc_red(ra, st, LORA_PROF_RED_DA));
   }
   if (dm) LORA_TRY(launch_dora_dm(d->dtype, dY, Y_save, dora_m, T, d->out_dim, dm, st));
   return LORA_OK;
@@ -738,42 +735,34 @@ int run_backward(const lora_desc* d, const DropParams& dp, int64_t T, const void
   // ranks one partial per item
   const int32_t sub = d->rank <= 16 ? kRedSub : 1;
   // dB_k += sum_t dY'[t, o] Hs[t, j]
-  {
-    ColRedArgs a{};
-    a.p = H; a.ldp = d->rank;
-    a.b = dY; a.ldb = d->out_dim; a.N = d->out_dim; a.colscale = ratio;
-    for (int k = 0; k < s.n; ++k) a.rank[k] = s.rank[k];
-    a.max_rank = d->rank; a.drop = dp;
-    a.part = L.partB; a.ldpart = d->rank; a.sub_groups = sub;
-    a.items = L.ritems; a.n_items = L.rcount;
-    if (fused) {
-      a.T = T; a.out = s.dB[0]; a.out_transposed = 0;
-      LORA_TRY(launch_colred(d->dtype, a, 0, st, LORA_PROF_RED_DB));
-    } else {
-      LORA_TRY(launch_colred(d->dtype, a, (int)L.rmax, st, LORA_PROF_RED_DB));
-      for (int k = 0; k < s.n; ++k) rt.out[k] = s.dB[k];
-      LORA_TRY(launch_reduce_parts(L.partB, L.ritems, L.rcount, (int)L.rmax, sub, d->out_dim,
-                                   d->rank, 0, rt, s.n, st));
-    }
-  }
+  ColRedArgs rb{};
+  rb.p = H; rb.ldp = d->rank;
+  rb.b = dY; rb.ldb = d->out_dim; rb.N = d->out_dim; rb.colscale = ratio;
+  for (int k = 0; k < s.n; ++k) rb.rank[k] = s.rank[k];
+  rb.max_rank = d->rank; rb.drop = dp;
+  rb.part = L.partB; rb.ldpart = d->rank; rb.sub_groups = sub;
+  rb.items = L.ritems; rb.n_items = L.rcount;
   // dA_k += sum_t Gs[t, j] M[t, i] X[t, i]   (computed as dA^T partials)
-  {
-    ColRedArgs a{};
-    a.p = L.Gs; a.ldp = d->rank;
-    a.b = X; a.ldb = d->in_dim; a.N = d->in_dim; a.mask = dp.enabled;
-    for (int k = 0; k < s.n; ++k) a.rank[k] = s.rank[k];
-    a.max_rank = d->rank; a.drop = dp;
-    a.part = L.partA; a.ldpart = d->rank; a.sub_groups = sub;
-    a.items = L.ritems; a.n_items = L.rcount;
-    if (fused) {
-      a.T = T; a.out = s.dA[0]; a.out_transposed = 1;
-      LORA_TRY(launch_colred(d->dtype, a, 0, st, LORA_PROF_RED_DA));
-    } else {
-      LORA_TRY(launch_colred(d->dtype, a, (int)L.rmax, st, LORA_PROF_RED_DA));
-      for (int k = 0; k < s.n; ++k) rt.out[k] = s.dA[k];
-      LORA_TRY(launch_reduce_parts(L.partA, L.ritems, L.rcount, (int)L.rmax, sub, d->in_dim,
-                                   d->rank, 1, rt, s.n, st));
-    }
+  ColRedArgs ra{};
+  ra.p = L.Gs; ra.ldp = d->rank;
+  ra.b = X; ra.ldb = d->in_dim; ra.N = d->in_dim; ra.mask = dp.enabled;
+  for (int k = 0; k < s.n; ++k) ra.rank[k] = s.rank[k];
+  ra.max_rank = d->rank; ra.drop = dp;
+  ra.part = L.partA; ra.ldpart = d->rank; ra.sub_groups = sub;
+  ra.items = L.ritems; ra.n_items = L.rcount;
+  if (fused) {   // both in one launch, each cluster adding its fixed-order sum into dB / dA^T
+    rb.T = T; rb.out = s.dB[0]; rb.out_transposed = 0;
+    ra.T = T; ra.out = s.dA[0]; ra.out_transposed = 1;
+    LORA_TRY(launch_colred2(d->dtype, rb, ra, st, LORA_PROF_RED));
+  } else {
+    LORA_TRY(launch_colred(d->dtype, rb, (int)L.rmax, st, LORA_PROF_RED_DB));
+    for (int k = 0; k < s.n; ++k) rt.out[k] = s.dB[k];
+    LORA_TRY(launch_reduce_parts(L.partB, L.ritems, L.rcount, (int)L.rmax, sub, d->out_dim,
+                                 d->rank, 0, rt, s.n, st));
+    LORA_TRY(launch_colred(d->dtype, ra, (int)L.rmax, st, LORA_PROF_RED_DA));
+    for (int k = 0; k < s.n; ++k) rt.out[k] = s.dA[k];
+    LORA_TRY(launch_reduce_parts(L.partA, L.ritems, L.rcount, (int)L.rmax, sub, d->in_dim,
+                                 d->rank, 1, rt, s.n, st));
   }
   if (dm) LORA_TRY(launch_dora_dm(d->dtype, dY, Y_save, dora_m, T, d->out_dim, dm, st));
   return LORA_OK;

@@ -159,6 +159,9 @@ struct TcRedMultiArgs {
 cudaError_t launch_tc_red_multi(const TcRedMultiArgs& a, cudaStream_t st, int prof_kind);
 cudaError_t launch_tc_rows(const TcRowsArgs& a, cudaStream_t st, int prof_kind);
 cudaError_t launch_tc_red(const TcRedArgs& a, cudaStream_t st, int prof_kind);
+// Two reductions over the same tokens, slots, ranks and run table (dB and dA of a linear) in one
+// launch; cudaErrorInvalidValue when they differ in any of these.
+cudaError_t launch_tc_red2(const TcRedArgs& a, const TcRedArgs& b, cudaStream_t st, int prof_kind);
 cudaError_t launch_split(const SplitTab& t, int n, cudaStream_t st);
 // count[0] = the number of items; count[1 + k] (k = 0 .. n_slots) = the first item of slot k, the
 // items being grouped by slot in slot order (count needs n_slots + 2 entries).
@@ -244,6 +247,9 @@ cudaError_t launch_rowdot(int dtype, const RowDotArgs& a, int max_items, cudaStr
                           int prof_kind);
 cudaError_t launch_colred(int dtype, const ColRedArgs& a, int max_items, cudaStream_t st,
                           int prof_kind);
+// Two fused single-adapter reductions (out set) over the same T and rank in one launch.
+cudaError_t launch_colred2(int dtype, const ColRedArgs& a, const ColRedArgs& b, cudaStream_t st,
+                           int prof_kind);
 
 // ---- lowrank.cu ----
 cudaError_t launch_colscale_bf16(const void* src, const float* scale, int64_t rows, int64_t cols,

@@ -557,10 +557,21 @@ __device__ __forceinline__ float ld_peer(const float* local, uint32_t rank) {
 // per lane; the 8 warps take every 8th token of a 128-token chunk, P rows staged in shared
 // memory) and reduces its warps in warp order. Then every CTA of the cluster adds, for 8 of the
 // block's columns, the groups' sums in group order (read from the peers' shared memory) into
-// out, so reruns are bitwise equal and no partials leave the chip.
+// out, so reruns are bitwise equal and no partials leave the chip. Two reductions over the same
+// tokens (dB and dA of a linear) can share a launch: grid x runs over job 0's column blocks, then
+// job 1's.
+struct ColRedJobs {
+  ColRedArgs job[2];
+  int32_t n_jobs;
+  int32_t blocks0;   // job 0's 64-column blocks
+};
+
 template <typename TB, int R>
-__global__ void __launch_bounds__(256) k_colred_fused(const ColRedArgs a) {
+__global__ void __launch_bounds__(256) k_colred_fused(const __grid_constant__ ColRedJobs jobs) {
   grid_dep_sync();
+  const int jb = (jobs.n_jobs > 1 && (int)blockIdx.x >= jobs.blocks0) ? 1 : 0;
+  const ColRedArgs& a = jobs.job[jb];
+  const int bx = (int)blockIdx.x - (jb ? jobs.blocks0 : 0);
   constexpr int kChunk = 128;   // tokens staged per pass (16 per warp, all loads in flight)
   constexpr int U = kChunk / 8;
   __shared__ __align__(16) float sP[kChunk * R];
@@ -568,7 +579,7 @@ __global__ void __launch_bounds__(256) k_colred_fused(const ColRedArgs a) {
   __shared__ float mine[kColBlock * R];   // this group's sums, [col][j]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t N = a.N;
-  const int64_t nb = (int64_t)blockIdx.x * kColBlock;
+  const int64_t nb = (int64_t)bx * kColBlock;
   const int64_t n0 = nb + 2 * lane;
   const bool nok = n0 < N;
   const int g = blockIdx.y;   // == rank in the cluster (cluster dims 1 x kColGroups)
@@ -735,36 +746,58 @@ cudaError_t launch_rowdot(int dtype, const RowDotArgs& a, int max_items, cudaStr
   return e;
 }
 
+namespace {
+// the fused single-adapter form of one or two jobs (ranks <= 16, same rank, T and dtype)
+cudaError_t colred_fused(int dtype, const ColRedArgs* js, int n_jobs, cudaStream_t st,
+                         int prof_kind) {
+  const ColRedArgs& a = js[0];
+  if (a.T <= 0) return cudaSuccess;
+  if (a.max_rank > 16) return cudaErrorInvalidValue;
+  ColRedJobs jobs{};
+  unsigned blocks = 0;
+  for (int q = 0; q < n_jobs; ++q) {
+    jobs.job[q] = js[q];
+    blocks += (unsigned)((js[q].N + kColBlock - 1) / kColBlock);
+  }
+  jobs.n_jobs = n_jobs;
+  jobs.blocks0 = (int32_t)((a.N + kColBlock - 1) / kColBlock);
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(blocks, (unsigned)kColGroups);
+  cfg.blockDim = dim3(256);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = kColGroups;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = add_pdl_attr(attr, 1);
+  cudaError_t e;
+  prof_begin(prof_kind, st);
+  if (dtype == LORA_F32) {
+    if (a.max_rank <= 4) e = cudaLaunchKernelEx(&cfg, k_colred_fused<float, 4>, jobs);
+    else if (a.max_rank <= 8) e = cudaLaunchKernelEx(&cfg, k_colred_fused<float, 8>, jobs);
+    else e = cudaLaunchKernelEx(&cfg, k_colred_fused<float, 16>, jobs);
+  } else {
+    if (a.max_rank <= 4) e = cudaLaunchKernelEx(&cfg, k_colred_fused<__nv_bfloat16, 4>, jobs);
+    else if (a.max_rank <= 8) e = cudaLaunchKernelEx(&cfg, k_colred_fused<__nv_bfloat16, 8>, jobs);
+    else e = cudaLaunchKernelEx(&cfg, k_colred_fused<__nv_bfloat16, 16>, jobs);
+  }
+  prof_end(prof_kind, st);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_colred2(int dtype, const ColRedArgs& a, const ColRedArgs& b, cudaStream_t st,
+                           int prof_kind) {
+  if (!a.out || !b.out || a.T != b.T || a.max_rank != b.max_rank) return cudaErrorInvalidValue;
+  const ColRedArgs js[2] = {a, b};
+  return colred_fused(dtype, js, 2, st, prof_kind);
+}
+
 cudaError_t launch_colred(int dtype, const ColRedArgs& a, int max_items, cudaStream_t st,
                           int prof_kind) {
-  if (a.out) {
-    if (a.T <= 0) return cudaSuccess;
-    if (a.max_rank > 16) return cudaErrorInvalidValue;
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3((unsigned)((a.N + kColBlock - 1) / kColBlock), (unsigned)kColGroups);
-    cfg.blockDim = dim3(256);
-    cfg.stream = st;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 1;
-    attr[0].val.clusterDim.y = kColGroups;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = add_pdl_attr(attr, 1);
-    cudaError_t e;
-    prof_begin(prof_kind, st);
-    if (dtype == LORA_F32) {
-      if (a.max_rank <= 4) e = cudaLaunchKernelEx(&cfg, k_colred_fused<float, 4>, a);
-      else if (a.max_rank <= 8) e = cudaLaunchKernelEx(&cfg, k_colred_fused<float, 8>, a);
-      else e = cudaLaunchKernelEx(&cfg, k_colred_fused<float, 16>, a);
-    } else {
-      if (a.max_rank <= 4) e = cudaLaunchKernelEx(&cfg, k_colred_fused<__nv_bfloat16, 4>, a);
-      else if (a.max_rank <= 8) e = cudaLaunchKernelEx(&cfg, k_colred_fused<__nv_bfloat16, 8>, a);
-      else e = cudaLaunchKernelEx(&cfg, k_colred_fused<__nv_bfloat16, 16>, a);
-    }
-    prof_end(prof_kind, st);
-    return e != cudaSuccess ? e : cudaGetLastError();
-  }
+  if (a.out) return colred_fused(dtype, &a, 1, st, prof_kind);
   if (max_items <= 0) return cudaSuccess;
   // the partial layout must match what the caller reduces: kRedTileT / kCrTok partials per item
   // from the wide kernel (ranks <= 16), one per item otherwise

@@ -308,17 +308,25 @@ constexpr int kMaxSplitsRows = 8;   // K splits of the rows kernel (the launcher
 // ---------------------------------------------------------------------------------------------
 // k_tc_red
 // ---------------------------------------------------------------------------------------------
-struct RedParams {
+struct RedJob {
   CUtensorMap tst[LORA_MAX_SLOTS];   // ST_slot [2 r, T] bf16 (tokens contiguous), box {64, 128}
   CUtensorMap tb;                    // B [T, N] bf16, box {64 (n), 64 (t)}
+  int32_t rank[LORA_MAX_SLOTS];
+  float* dst[LORA_MAX_SLOTS];        // dB_slot [N, r] (transposed) or dA_slot [r, N]
+  int32_t transposed;
+  int32_t tiles;                     // BN-column tiles of B: the job's share of the grid's x
+  int64_t N;
+};
+
+// One or two reductions over the same tokens and run table (dB and dA of a linear) in one
+// launch: grid x runs over job 0's tiles, then job 1's.
+struct RedParams {
+  RedJob job[2];
+  int32_t n_jobs;
   const TokenItem* items;            // 64-token aligned runs grouped by slot (null: the uniform
                                      // runs of kRedSpanBlocks blocks over [0, T), slot 0)
   const int32_t* counts;             // counts[1 + slot] .. counts[2 + slot]: the slot's items
   uint32_t* err;
-  int32_t rank[LORA_MAX_SLOTS];
-  float* dst[LORA_MAX_SLOTS];        // dB_slot [N, r] (transposed) or dA_slot [r, N]
-  int32_t transposed;
-  int64_t N;
   int64_t T;
 };
 
@@ -357,8 +365,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_red(const __grid_constant__ 
   const int slot = blockIdx.z;
   const int z = blockIdx.y;   // == rank in the cluster (cluster dims 1 x splits)
   const int splits = gridDim.y;
-  const int32_t n0 = blockIdx.x * BN;
-  const int r = p.rank[slot];
+  const int jb = (p.n_jobs > 1 && (int)blockIdx.x >= p.job[0].tiles) ? 1 : 0;
+  const RedJob& J = p.job[jb];
+  const int32_t n0 = ((int32_t)blockIdx.x - (jb ? p.job[0].tiles : 0)) * BN;
+  const int r = J.rank[slot];
   // this CTA's work: items [w0, w1) of the slot's items, split evenly over the cluster (the
   // uniform runs of a single-adapter call are the items of one segment covering [0, T))
   const int32_t nb_all = (int32_t)((p.T + 63) / 64);
@@ -421,10 +431,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_red(const __grid_constant__ 
           uint8_t* sa = base + s * kRedStageBytes;
           mbar_expect_tx(&full_bar[s], kRedStageBytes);
           const int32_t t = tb0 + b * 64;
-          tma_load_2d(sa, &p.tst[slot], &full_bar[s], t, 0);
+          tma_load_2d(sa, &J.tst[slot], &full_bar[s], t, 0);
 #pragma unroll
           for (int q = 0; q < BN / 64; ++q)
-            tma_load_2d(sa + 16384 + q * 8192, &p.tb, &full_bar[s], n0 + 64 * q, t);
+            tma_load_2d(sa + 16384 + q * 8192, &J.tb, &full_bar[s], n0 + 64 * q, t);
         }
       }
       // every issued load has landed before the stages are reused as the staging tile
@@ -470,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_red(const __grid_constant__ 
           for (int k = 0; k < 32; ++k) v[k] = 0.f;
         }
         if (!mine) continue;
-        if (!p.transposed) {
+        if (!J.transposed) {
           float* d = buf + j * kRedLdA + c * 32;
 #pragma unroll
           for (int g = 0; g < 8; ++g) {
@@ -496,19 +506,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_red(const __grid_constant__ 
   __syncthreads();
   cluster_sync_all();   // every CTA's partial tile is in its shared memory
   const int W = kRedBN / splits;
-  float* dst = p.dst[slot];
-  if (!p.transposed) {
+  float* dst = J.dst[slot];
+  if (!J.transposed) {
     // dA [r, N]: rows j, columns n0 + z W ..
     const int w4 = W / 4;
     for (int e = threadIdx.x; e < r * w4; e += kThreads) {
       const int j = e / w4, c = z * W + 4 * (e - (e / w4) * w4);
       const int64_t n = (int64_t)n0 + c;
-      if (n >= p.N) continue;
+      if (n >= J.N) continue;
       float4 pz[kRedMaxSplits];
 #pragma unroll
       for (int zz = 0; zz < kRedMaxSplits; ++zz)
         if (zz < splits) pz[zz] = dsmem_ld4(buf + j * kRedLdA + c, (uint32_t)zz);
-      float4* o = reinterpret_cast<float4*>(dst + (int64_t)j * p.N + n);
+      float4* o = reinterpret_cast<float4*>(dst + (int64_t)j * J.N + n);
       float4 acc = *o;
       float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
@@ -525,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_red(const __grid_constant__ 
     for (int e = threadIdx.x; e < W * r4; e += kThreads) {
       const int c = z * W + e / r4, j = 4 * (e - (e / r4) * r4);
       const int64_t n = (int64_t)n0 + c;
-      if (n >= p.N) continue;
+      if (n >= J.N) continue;
       float4 pz[kRedMaxSplits];
 #pragma unroll
       for (int zz = 0; zz < kRedMaxSplits; ++zz)
@@ -1054,11 +1064,32 @@ cudaError_t launch_red_bn(dim3 grid, int splits, cudaStream_t st, const RedParam
   return launch_cluster_y(k_tc_red<BN>, grid, splits, RedCfg<BN>::kSmem, st, prm);
 }
 
-cudaError_t launch_tc_red(const TcRedArgs& a, cudaStream_t st, int prof_kind) {
+namespace {
+bool fill_red_job(RedJob& j, const TcRedArgs& a, int bn) {
+  for (int k = 0; k < a.n_slots; ++k) {
+    if (!tc::make_map_2d(&j.tst[k], a.st[k], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T,
+                         2 * (uint64_t)a.rank[k], a.ldt, 64, kBM))
+      return false;
+    if (a.rank[k] % 4 || a.rank[k] > LORA_MAX_RANK) return false;
+    j.rank[k] = a.rank[k];
+    j.dst[k] = a.tab.out[k];
+  }
+  if (!tc::make_map_2d(&j.tb, a.b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.N, a.T,
+                       a.ldb > 0 ? a.ldb : a.N, 64, 64))
+    return false;
+  if (a.N % 4) return false;
+  j.transposed = a.transposed;
+  j.N = a.N;
+  j.tiles = (int32_t)((a.N + bn - 1) / bn);
+  return true;
+}
+
+cudaError_t launch_tc_red_jobs(const TcRedArgs* jobs, int n_jobs, cudaStream_t st, int prof_kind) {
   static RedParams prm;
   static std::mutex mu;
   std::lock_guard<std::mutex> lk(mu);
   std::memset(&prm, 0, sizeof(prm));
+  const TcRedArgs& a = jobs[0];
   if (a.T <= 0 || a.n_slots <= 0) return cudaSuccess;
   // Tile width and token splits (CTAs of one cluster): the most CTAs, one per SM at most, whose
   // clusters are all resident at once, with at least two 64-token blocks of T per split; the
@@ -1068,7 +1099,8 @@ cudaError_t launch_tc_red(const TcRedArgs& a, cudaStream_t st, int prof_kind) {
   int best_bn = 256, best_splits = 1;
   int64_t best_ctas = -1;
   for (int bn : {256, 128}) {
-    const int64_t tiles = (a.N + bn - 1) / bn;
+    int64_t tiles = 0;
+    for (int q = 0; q < n_jobs; ++q) tiles += (jobs[q].N + bn - 1) / bn;
     for (int c = 1; c <= kRedMaxSplits; c *= 2) {
       const int64_t clusters = tiles * a.n_slots;
       if (clusters * c > sms || (c > 1 && (a.T + 63) / 64 < 2 * (int64_t)c)) break;
@@ -1082,32 +1114,38 @@ cudaError_t launch_tc_red(const TcRedArgs& a, cudaStream_t st, int prof_kind) {
     }
   }
   const int bn = best_bn, splits = best_splits;
-  for (int k = 0; k < a.n_slots; ++k) {
-    if (!tc::make_map_2d(&prm.tst[k], a.st[k], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T,
-                         2 * (uint64_t)a.rank[k], a.ldt, 64, kBM))
-      return cudaErrorInvalidValue;
-    if (a.rank[k] % 4 || a.rank[k] > LORA_MAX_RANK) return cudaErrorInvalidValue;
-    prm.rank[k] = a.rank[k];
-    prm.dst[k] = a.tab.out[k];
+  int64_t tiles = 0;
+  for (int q = 0; q < n_jobs; ++q) {
+    if (!fill_red_job(prm.job[q], jobs[q], bn)) return cudaErrorInvalidValue;
+    tiles += prm.job[q].tiles;
   }
-  if (!tc::make_map_2d(&prm.tb, a.b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.N, a.T,
-                       a.ldb > 0 ? a.ldb : a.N, 64, 64))
-    return cudaErrorInvalidValue;
-  if (a.N % 4) return cudaErrorInvalidValue;
+  prm.n_jobs = n_jobs;
   prm.items = a.items;
   prm.counts = a.n_items;
   prm.err = tc::error_word();
   if (!prm.err) return cudaErrorInvalidDevice;
-  prm.transposed = a.transposed;
-  prm.N = a.N;
   prm.T = a.T;
-  dim3 grid((unsigned)((a.N + bn - 1) / bn), (unsigned)splits, (unsigned)a.n_slots);
+  dim3 grid((unsigned)tiles, (unsigned)splits, (unsigned)a.n_slots);
   prof_begin(prof_kind, st);
   cudaError_t e = bn == 256 ? launch_red_bn<256>(grid, splits, st, prm)
                             : launch_red_bn<128>(grid, splits, st, prm);
   if (e != cudaSuccess) return e;
   prof_end(prof_kind, st);
   return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_tc_red(const TcRedArgs& a, cudaStream_t st, int prof_kind) {
+  return launch_tc_red_jobs(&a, 1, st, prof_kind);
+}
+
+cudaError_t launch_tc_red2(const TcRedArgs& a, const TcRedArgs& b, cudaStream_t st, int prof_kind) {
+  if (a.T != b.T || a.n_slots != b.n_slots || a.items != b.items || a.n_items != b.n_items)
+    return cudaErrorInvalidValue;
+  for (int k = 0; k < a.n_slots; ++k)
+    if (a.rank[k] != b.rank[k]) return cudaErrorInvalidValue;
+  const TcRedArgs jobs[2] = {a, b};
+  return launch_tc_red_jobs(jobs, 2, st, prof_kind);
 }
 
 cudaError_t launch_adapter_prep(const TransposeTab& ta, const SplitTab& sb, int n,

@@ -24,10 +24,24 @@ __device__ __forceinline__ void ff_add_square(float a, float& hi, float& lo) {
   lo = __fadd_rn(lo, __fadd_rn(err, e));
 }
 
-// One element of pass 1. |a| > 2^60 (and +-Inf) goes to a double accumulator so that no finite
-// square overflows; NaN propagates through hi. The block sum is non-finite iff an element is.
+// (ah, al) += (bh, bl) for float-float pairs: TwoSum of the high parts, the low parts and that
+// rounding error added, then renormalised with Fast2Sum.
+__device__ __forceinline__ void ff_add(float& ah, float& al, float bh, float bl) {
+  const float s = __fadd_rn(ah, bh);
+  const float bp = __fsub_rn(s, ah);
+  const float err = __fadd_rn(__fsub_rn(ah, __fsub_rn(s, bp)), __fsub_rn(bh, bp));
+  const float t = __fadd_rn(__fadd_rn(al, bl), err);
+  const float h = __fadd_rn(s, t);
+  al = __fsub_rn(t, __fsub_rn(h, s));
+  ah = h;
+}
+
+// One element of pass 1. |a| > 2^40 (and +-Inf) goes to a double accumulator: a square below
+// 2^80 keeps a CTA's float-float sum (at most 2^24 elements) far inside the float range, so no
+// finite gradient overflows; NaN propagates through hi. The block sum is non-finite iff an
+// element is.
 __device__ __forceinline__ void sq_accum(float a, float& hi, float& lo, double& big) {
-  if (fabsf(a) > 0x1p60f) {
+  if (fabsf(a) > 0x1p40f) {
     const double d = (double)a;
     big = fma(d, d, big);
   } else {
@@ -64,6 +78,7 @@ __global__ void __launch_bounds__(kPrepThreads, 4) k_grad_prepare(const float* _
                                                                int64_t per_block) {
   grid_dep_sync();
   __shared__ double sh[kPrepThreads / 32];
+  __shared__ float2 shf[kPrepThreads / 32];
   __shared__ bool am_last;
   const int b = blockIdx.x;
   const int g = find_group(gt, b);
@@ -71,38 +86,65 @@ __global__ void __launch_bounds__(kPrepThreads, 4) k_grad_prepare(const float* _
   const int64_t n = min(per_block, gt.count[g] - begin);
   const float* p = grads + gt.offset[g] + begin;
   // Two independent float-float accumulators per thread (x, y and z, w of each float4) halve the
-  // dependent chain, and each batch issues kPrepBatch independent 16-byte loads before any add,
-  // so that enough bytes are in flight to stream at the memory's rate.
+  // dependent chain, and every batch issues its kPrepBatch 16-byte loads before any add (the
+  // last batch predicated, zeros past the end), so that a thread's whole run is in flight in one
+  // or two round trips. A zero adds nothing to the pair, so each thread still sums its own
+  // elements in increasing order.
   constexpr int kPrepBatch = 8;
   float hi0 = 0.f, lo0 = 0.f, hi1 = 0.f, lo1 = 0.f;
   double big = 0.0;
   const int64_t nv = n >> 2;
   const float4* p4 = reinterpret_cast<const float4*>(p);
-  int64_t v = threadIdx.x;
-  for (; v + (kPrepBatch - 1) * kPrepThreads < nv; v += kPrepBatch * kPrepThreads) {
+  for (int64_t v0 = 0; v0 < nv; v0 += kPrepBatch * kPrepThreads) {
     float4 x[kPrepBatch];
 #pragma unroll
-    for (int u = 0; u < kPrepBatch; ++u) x[u] = __ldcs(p4 + v + u * kPrepThreads);
-#pragma unroll
     for (int u = 0; u < kPrepBatch; ++u) {
-      sq_accum(x[u].x, hi0, lo0, big);
-      sq_accum(x[u].y, hi0, lo0, big);
-      sq_accum(x[u].z, hi1, lo1, big);
-      sq_accum(x[u].w, hi1, lo1, big);
+      const int64_t v = v0 + threadIdx.x + u * kPrepThreads;
+      x[u] = v < nv ? __ldcs(p4 + v) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    // One warp-uniform test per batch keeps the per-element path in FP32: only a batch of a warp
+    // that holds a value above 2^40 or an infinity takes the per-element test with its double
+    // accumulator (fmaxf passes over NaN, which the float-float pair propagates by itself).
+    float mx = 0.f;
+#pragma unroll
+    for (int u = 0; u < kPrepBatch; ++u)
+      mx = fmaxf(mx, fmaxf(fmaxf(fabsf(x[u].x), fabsf(x[u].y)), fmaxf(fabsf(x[u].z), fabsf(x[u].w))));
+    if (__any_sync(0xffffffffu, mx > 0x1p40f)) {
+#pragma unroll
+      for (int u = 0; u < kPrepBatch; ++u) {
+        sq_accum(x[u].x, hi0, lo0, big);
+        sq_accum(x[u].y, hi0, lo0, big);
+        sq_accum(x[u].z, hi1, lo1, big);
+        sq_accum(x[u].w, hi1, lo1, big);
+      }
+    } else {
+#pragma unroll
+      for (int u = 0; u < kPrepBatch; ++u) {
+        ff_add_square(x[u].x, hi0, lo0);
+        ff_add_square(x[u].y, hi0, lo0);
+        ff_add_square(x[u].z, hi1, lo1);
+        ff_add_square(x[u].w, hi1, lo1);
+      }
     }
   }
-  for (; v < nv; v += kPrepThreads) {
-    const float4 x = __ldcs(p4 + v);
-    sq_accum(x.x, hi0, lo0, big);
-    sq_accum(x.y, hi0, lo0, big);
-    sq_accum(x.z, hi1, lo1, big);
-    sq_accum(x.w, hi1, lo1, big);
-  }
   for (int64_t e = (nv << 2) + threadIdx.x; e < n; e += kPrepThreads) sq_accum(p[e], hi0, lo0, big);
-  const double mine = (((double)hi0 + (double)lo0) + ((double)hi1 + (double)lo1)) + big;
-  const double tot = block_sum_double(mine, sh);
+  // The CTA's pairs are summed in float-float in a fixed tree (lanes by shuffles, then the warps
+  // in order by thread 0): FP64 runs at a small fraction of the FP32 rate on this part, so
+  // double arithmetic is kept to one conversion per CTA (and the rare large-element sum).
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  ff_add(hi0, lo0, hi1, lo1);
+  for (int off = 16; off > 0; off >>= 1) {
+    const float oh = __shfl_down_sync(0xffffffffu, hi0, off);
+    const float ol = __shfl_down_sync(0xffffffffu, lo0, off);
+    ff_add(hi0, lo0, oh, ol);
+  }
+  if (lane == 0) shf[warp] = make_float2(hi0, lo0);
+  const bool any_big = __syncthreads_or(big != 0.0);
+  const double big_sum = any_big ? block_sum_double(big, sh) : 0.0;
   if (threadIdx.x == 0) {
-    part[b] = tot;
+    float th = shf[0].x, tl = shf[0].y;
+    for (int w = 1; w < kPrepThreads / 32; ++w) ff_add(th, tl, shf[w].x, shf[w].y);
+    part[b] = ((double)th + (double)tl) + big_sum;
     __threadfence();
     const uint32_t done = atomicAdd(counter, 1u);
     am_last = (done == gridDim.x - 1);
@@ -110,14 +152,15 @@ __global__ void __launch_bounds__(kPrepThreads, 4) k_grad_prepare(const float* _
   __syncthreads();
   if (!am_last) return;
   __threadfence();
-  // last block: per group, fixed-order reduction of that group's block partials
-  for (int gg = 0; gg < gt.n; ++gg) {
+  // last block: one warp per group, each reducing that group's block partials in a fixed order
+  // (lane l sums partials l, l + 32, ... in turn, then a fixed shuffle tree), all groups at once
+  for (int gg = warp; gg < gt.n; gg += kPrepThreads / 32) {
     const int b0 = gt.block_begin[gg], b1 = gt.block_begin[gg + 1];
-    double acc = 0.0;
-#pragma unroll 4
-    for (int k = b0 + threadIdx.x; k < b1; k += kPrepThreads) acc += __ldcg(part + k);
-    const double S = block_sum_double(acc, sh);
-    if (threadIdx.x == 0) {
+    double S = 0.0;
+#pragma unroll 8
+    for (int k = b0 + lane; k < b1; k += 32) S += __ldcg(part + k);
+    for (int off = 16; off > 0; off >>= 1) S += __shfl_down_sync(0xffffffffu, S, off);
+    if (lane == 0) {
       if (!isfinite(S)) {
         status[gg] = LORA_ERR_NONFINITE;
         scale_norm[2 * gg] = 0.0;
@@ -155,38 +198,58 @@ __global__ void __launch_bounds__(kAdamThreads) k_adamw(float* __restrict__ P, f
                                                         const GroupTab gt, const AdamK hp,
                                                         const double* __restrict__ scale_norm,
                                                         const int32_t* __restrict__ status,
-                                                        int zero_grads) {
+                                                        int zero_grads, int64_t per_block) {
   grid_dep_sync();
   const int b = blockIdx.x;
   const int g = find_group(gt, b);
-  if (status[g] != LORA_OK) return;
-  const float c = (float)scale_norm[2 * g];
+  // the group's verdict and factor are read alongside the first batch, not ahead of it
+  const int32_t verdict = status[g];
+  const double factor = scale_norm[2 * g];
   const float lr = gt.lr[g];
   const float inv_bc1 = 1.f / gt.bc1[g], inv_bc2 = 1.f / gt.bc2[g];
-  const int64_t begin = (int64_t)(b - gt.block_begin[g]) * kAdamElemsPerBlock;
-  const int64_t n = min((int64_t)kAdamElemsPerBlock, gt.count[g] - begin);
+  const int64_t begin = (int64_t)(b - gt.block_begin[g]) * per_block;
+  const int64_t n = min(per_block, gt.count[g] - begin);
   const int64_t base = gt.offset[g] + begin;
   const int64_t na = gt.n_a[g], nab = gt.n_a[g] + gt.n_b[g];
   const int64_t nv = n >> 2;
-  for (int64_t q = threadIdx.x; q < nv; q += kAdamThreads) {
-    const int64_t e = base + (q << 2);
-    float4 p = *reinterpret_cast<float4*>(P + e);
-    float4 gr = *reinterpret_cast<float4*>(G + e);
-    float4 m = *reinterpret_cast<float4*>(Mo + e);
-    float4 v = *reinterpret_cast<float4*>(V + e);
-    float* pp = &p.x; float* gg = &gr.x; float* mm = &m.x; float* vv = &v.x;
-    const int64_t li = begin + (q << 2);
+  // kAdamBatch float4 of each of p, g, m, v per thread in flight before any update
+  constexpr int kAdamBatch = 2;
+  for (int64_t q0 = 0; q0 < nv; q0 += kAdamBatch * kAdamThreads) {
+    float4 p[kAdamBatch], gr[kAdamBatch], m[kAdamBatch], v[kAdamBatch];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int64_t l = li + j;
-      const int kind = (l < na) ? 0 : ((l < nab) ? 1 : 2);
-      adam_elem(pp[j], gg[j], mm[j], vv[j], kind, c, lr, hp, inv_bc1, inv_bc2);
+    for (int u = 0; u < kAdamBatch; ++u) {
+      const int64_t q = q0 + threadIdx.x + u * kAdamThreads;
+      if (q < nv) {
+        const int64_t e = base + (q << 2);
+        p[u] = *reinterpret_cast<const float4*>(P + e);
+        gr[u] = *reinterpret_cast<const float4*>(G + e);
+        m[u] = *reinterpret_cast<const float4*>(Mo + e);
+        v[u] = *reinterpret_cast<const float4*>(V + e);
+      }
     }
-    *reinterpret_cast<float4*>(P + e) = p;
-    *reinterpret_cast<float4*>(Mo + e) = m;
-    *reinterpret_cast<float4*>(V + e) = v;
-    if (zero_grads) *reinterpret_cast<float4*>(G + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (verdict != LORA_OK) return;
+    const float c = (float)factor;
+#pragma unroll
+    for (int u = 0; u < kAdamBatch; ++u) {
+      const int64_t q = q0 + threadIdx.x + u * kAdamThreads;
+      if (q >= nv) continue;
+      const int64_t e = base + (q << 2);
+      float* pp = &p[u].x; float* gg = &gr[u].x; float* mm = &m[u].x; float* vv = &v[u].x;
+      const int64_t li = begin + (q << 2);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int64_t l = li + j;
+        const int kind = (l < na) ? 0 : ((l < nab) ? 1 : 2);
+        adam_elem(pp[j], gg[j], mm[j], vv[j], kind, c, lr, hp, inv_bc1, inv_bc2);
+      }
+      *reinterpret_cast<float4*>(P + e) = p[u];
+      *reinterpret_cast<float4*>(Mo + e) = m[u];
+      *reinterpret_cast<float4*>(V + e) = v[u];
+      if (zero_grads) *reinterpret_cast<float4*>(G + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
   }
+  if (verdict != LORA_OK) return;
+  const float c = (float)factor;
   for (int64_t l = begin + (nv << 2) + threadIdx.x; l < begin + n; l += kAdamThreads) {
     const int64_t e = gt.offset[g] + l;
     const int kind = (l < na) ? 0 : ((l < nab) ? 1 : 2);
@@ -285,10 +348,23 @@ cudaError_t launch_adamw(float* p, float* g, float* m, float* v, const GroupTab&
                          const AdamK& hp, const double* d_scale_norm, const int32_t* d_status,
                          int zero_grads, cudaStream_t st) {
   GroupTab gt = gt_in;
-  const int blocks = set_blocks(gt, kAdamElemsPerBlock);
+  // elements per CTA: about eight CTAs per SM over the whole arena, each thread holding one or
+  // more batches, so that a small arena still has all its loads in flight at once
+  int64_t total = 0;
+  for (int i = 0; i < gt.n; ++i) total += gt.count[i];
+  const int64_t unit = 2 * 4 * kAdamThreads;   // one batch of the kernel
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+    sms = 152;
+  const int64_t target = (int64_t)8 * sms;
+  int64_t per = (total / target + unit - 1) / unit * unit;
+  per = per < unit ? unit : (per > 4 * unit ? 4 * unit : per);
+  const int blocks = set_blocks(gt, per);
   if (blocks == 0) return cudaSuccess;
   prof_begin(LORA_PROF_ADAMW, st);
-  launch_kernel(k_adamw, blocks, kAdamThreads, 0, st, p, g, m, v, gt, hp, d_scale_norm, d_status, zero_grads);
+  launch_kernel(k_adamw, blocks, kAdamThreads, 0, st, p, g, m, v, gt, hp, d_scale_norm, d_status,
+                zero_grads, per);
   prof_end(LORA_PROF_ADAMW, st);
   return cudaGetLastError();
 }

@@ -356,10 +356,11 @@ int multi_lora_token_slots(int64_t T, int32_t n_seg, const int32_t* d_seg_start,
 #define LORA_PROF_FROZEN_DX 2    /* frozen dX product with the fused LoRA dX term */
 #define LORA_PROF_SHRINK 3       /* Hs = s' Xd A^T */
 #define LORA_PROF_G 4            /* Gs = s' dY' B */
-#define LORA_PROF_RED_DB 5       /* dB token-reduction partials */
-#define LORA_PROF_RED_DA 6       /* dA token-reduction partials */
+#define LORA_PROF_RED_DB 5       /* dB token reduction */
+#define LORA_PROF_RED_DA 6       /* dA token reduction */
 #define LORA_PROF_PREPARE 7      /* grad-prepare pass 1 */
 #define LORA_PROF_ADAMW 8        /* fused clip + AdamW */
+#define LORA_PROF_RED 9          /* dB and dA token reductions in one launch */
 
 /* Arm event brackets: the next n launches of `kernel_class` record start_events[i] before and
  * stop_events[i] after launch i on the launching stream (cudaEvent_t handles, caller-owned).
