@@ -97,7 +97,9 @@ def memory_counts(cfg: LI.LoraConfig, layers: int, groups=None):
     or X and Hs or Gs and update dB / dA; grad-prepare reads 4 B and AdamW moves 32 B per
     parameter (p, g, m, v read; p, m, v written; g cleared). With `groups` (fused projections:
     lists of projection indices that read one input), a group's input and output gradient are
-    counted once, with the group's adapters side by side."""
+    counted once, with the group's adapters side by side. The bf16 fused backward times the dB of
+    groups of 2 to 4 projections and their shared dA as classes of their own ("redB", "redA");
+    every other fused group reduces dB and dA in one launch ("red")."""
     T = cfg.tokens
     a = 4 if cfg.dtype == "f32" else 2
     split = 4 if cfg.dtype == "f32" else 0   # bf16 hi + lo per element
@@ -108,6 +110,8 @@ def memory_counts(cfg: LI.LoraConfig, layers: int, groups=None):
     else:
         r_all = r_row = cfg.rank
     out = {"shrink": 0, "G": 0, "redB": 0, "redA": 0}
+    if groups:
+        out["red"] = 0
     for idx in (groups or [[k] for k in range(len(cfg.projs))]):
         i = cfg.projs[idx[0]].in_dim
         o = sum(cfg.projs[k].out_dim for k in idx)
@@ -118,8 +122,13 @@ def memory_counts(cfg: LI.LoraConfig, layers: int, groups=None):
             # the bf16 G product also writes the transposed bf16 split of Gs (for dA) and, as a
             # side task, reads the saved Hs and writes its transposed split (for dB), per adapter
             out["G"] += 3 * 4 * T * n * r_row
-        out["redB"] += T * o * a + T * n * r_row * 4 + 2 * r_all * o * 4
-        out["redA"] += T * i * a + T * n * r_row * 4 + 2 * n * r_all * i * 4
+        red_b = T * o * a + T * n * r_row * 4 + 2 * r_all * o * 4
+        red_a = T * i * a + T * n * r_row * 4 + 2 * n * r_all * i * 4
+        if groups and not (cfg.dtype != "f32" and 2 <= n <= 4 and 2 * r_row <= 128):
+            out["red"] += red_b + red_a
+        else:
+            out["redB"] += red_b
+            out["redA"] += red_a
     out = {k: v * layers for k, v in out.items()}
     r_step = r_all
     if cfg.multi:   # only the slots whose adapter batch is full take a step
@@ -887,8 +896,10 @@ def run_ours(args):
         mem = memory_counts(cfg, layers if not cfg.multi else 1,
                             fused_groups(cfg) if args.fused else None)
         memory_bound = {}
-        # "red": the dB and dA reductions of a linear in one launch, both classes' bytes
-        class_bytes = dict(mem, red=mem["redB"] + mem["redA"])
+        # "red": the dB and dA reductions of a linear in one launch, both classes' bytes (fused
+        # groups count their own)
+        class_bytes = dict(mem)
+        class_bytes.setdefault("red", mem["redB"] + mem["redA"])
         for name, ts in mem_times.items():
             if ts:
                 gbs = class_bytes[name] / (sum(ts) / 1e3) / 1e9

@@ -868,6 +868,7 @@ struct FusedLayout {
   uint16_t* Sbk;   // per projection [2 r, out_k] bf16 split of B_k^T, one after the other
   uint16_t* Sacat; // per projection [2 r, in] bf16 split of A_k, one after the other
   uint16_t* GsTk;  // per projection [2 r, ldt] transposed split of Gs_k, one after the other
+  uint16_t* HsTk;  // per projection [2 r, ldt] transposed split of the saved Hs_k
   size_t bytes;
 };
 
@@ -883,6 +884,7 @@ FusedLayout fused_carve(const lora_desc* d, int64_t T, const FusedProjs& f, void
   F.Sbk = c.take<uint16_t>((size_t)2 * d->rank * d->out_dim);   // sum of out_k = out_dim
   F.Sacat = c.take<uint16_t>((size_t)2 * d->rank * f.n * d->in_dim);
   F.GsTk = c.take<uint16_t>((size_t)2 * d->rank * f.n * F.L.ldt);
+  F.HsTk = c.take<uint16_t>((size_t)2 * d->rank * f.n * F.L.ldt);
   F.bytes = c.off + kWsAlign;
   return F;
 }
@@ -1091,14 +1093,12 @@ int run_fused_backward(const lora_desc* d, const DropParams& dp, int64_t T, cons
   }
   const size_t split_bytes = (size_t)2 * r * L.ldt * sizeof(uint16_t);
   const uint16_t* dYb = static_cast<const uint16_t*>(dY);
-  ReduceTab rt{};
-  rt.rank[0] = (int32_t)r;
   // dA of the whole group in one reduction that reads Xd once, after every G_k
   const bool group_da = f.n >= 2 && f.n <= 4 && 2 * r <= 128 && d->in_dim % 8 == 0;
   for (int k = 0; k < f.n; ++k) {
     // G_k = s' dY_k B_k (projection k's columns of dY) into columns k r .. of G, with its
-    // transposed split for dA_k and, as a side task, the transposed split of the saved Hs_k
-    uint16_t* gst = group_da ? F.GsTk + (int64_t)k * 2 * r * L.ldt : L.GsT;
+    // transposed split for dA_k and, as a side task, the transposed split of the saved Hs_k,
+    // each in the projection's own region
     TcRowsArgs g{};
     g.a = dYb + f.off[k]; g.lda = d->out_dim; g.T = T; g.K = f.out[k]; g.n_slots = 1;
     g.s[0] = sbk[k]; g.rank[0] = (int32_t)r;
@@ -1106,28 +1106,32 @@ int run_fused_backward(const lora_desc* d, const DropParams& dp, int64_t T, cons
     g.splits = row_splits(T, -1, f.out[k]);
     g.si = si;
     g.out = F.Gcat + k * r; g.ldo = r; g.ld_out = ldh;
-    g.outT = gst; g.ldt = L.ldt; g.outT_bytes = split_bytes;
-    g.side_h = H + k * r; g.side_ldh = ldh; g.side_outT = L.HsT;
+    g.outT = F.GsTk + (int64_t)k * 2 * r * L.ldt; g.ldt = L.ldt; g.outT_bytes = split_bytes;
+    g.side_h = H + k * r; g.side_ldh = ldh; g.side_outT = F.HsTk + (int64_t)k * 2 * r * L.ldt;
     g.items = nullptr; g.n_items = nullptr; g.max_items = (int)L.gmax;
     LORA_TRY(launch_tc_rows(g, st, LORA_PROF_G));
-    if (!group_da) {   // dA_k += Gs_k^T Xd
-      TcRedArgs a{};
-      a.st[0] = gst; a.rank[0] = (int32_t)r; a.n_slots = 1; a.max_rank = (int32_t)r;
-      a.T = T; a.ldt = L.ldt; a.b = Xin; a.N = d->in_dim;
-      rt.out[0] = f.dA[k];
-      a.tab = rt; a.transposed = 0;
-      a.items = nullptr; a.n_items = nullptr;
-      LORA_TRY(launch_tc_red(a, st, LORA_PROF_RED_DA));
-    }
-    // dB_k += dY_k^T Hs_k
-    TcRedArgs b{};
-    b.st[0] = L.HsT; b.rank[0] = (int32_t)r; b.n_slots = 1; b.max_rank = (int32_t)r;
-    b.T = T; b.ldt = L.ldt; b.b = dYb + f.off[k]; b.ldb = d->out_dim; b.N = f.out[k];
-    rt.out[0] = f.dB[k];
-    b.tab = rt; b.transposed = 1;
-    b.items = nullptr; b.n_items = nullptr;
-    LORA_TRY(launch_tc_red(b, st, LORA_PROF_RED_DB));
   }
+  // dB_k += dY_k^T Hs_k for every k and, without the group dA, dA_k += Gs_k^T Xd: jobs of shared
+  // reduction launches
+  TcRedArgs jobs[2 * LORA_MAX_SLOTS];
+  int nj = 0;
+  for (int k = 0; k < f.n; ++k) {
+    TcRedArgs& b = jobs[nj++];
+    b = TcRedArgs{};
+    b.st[0] = F.HsTk + (int64_t)k * 2 * r * L.ldt;
+    b.rank[0] = (int32_t)r; b.n_slots = 1; b.max_rank = (int32_t)r;
+    b.T = T; b.ldt = L.ldt; b.b = dYb + f.off[k]; b.ldb = d->out_dim; b.N = f.out[k];
+    b.tab.rank[0] = (int32_t)r; b.tab.out[0] = f.dB[k]; b.transposed = 1;
+    if (!group_da) {
+      TcRedArgs& a = jobs[nj++];
+      a = TcRedArgs{};
+      a.st[0] = F.GsTk + (int64_t)k * 2 * r * L.ldt;
+      a.rank[0] = (int32_t)r; a.n_slots = 1; a.max_rank = (int32_t)r;
+      a.T = T; a.ldt = L.ldt; a.b = Xin; a.N = d->in_dim;
+      a.tab.rank[0] = (int32_t)r; a.tab.out[0] = f.dA[k]; a.transposed = 0;
+    }
+  }
+  LORA_TRY(launch_tc_red_n(jobs, nj, st, group_da ? LORA_PROF_RED_DB : LORA_PROF_RED));
   if (group_da) {   // dA_k += Gs_k^T Xd for every k, Xd streamed once
     TcRedMultiArgs a{};
     for (int k = 0; k < f.n; ++k) {

@@ -159,8 +159,10 @@ struct TcRedMultiArgs {
 cudaError_t launch_tc_red_multi(const TcRedMultiArgs& a, cudaStream_t st, int prof_kind);
 cudaError_t launch_tc_rows(const TcRowsArgs& a, cudaStream_t st, int prof_kind);
 cudaError_t launch_tc_red(const TcRedArgs& a, cudaStream_t st, int prof_kind);
-// Two reductions over the same tokens, slots, ranks and run table (dB and dA of a linear) in one
-// launch; cudaErrorInvalidValue when they differ in any of these.
+// Reductions over the same tokens, slots, ranks and run table (dB and dA of a linear, the dB of
+// every projection of a fused group) sharing launches, up to four jobs per launch;
+// cudaErrorInvalidValue when they differ in any of these.
+cudaError_t launch_tc_red_n(const TcRedArgs* jobs, int n, cudaStream_t st, int prof_kind);
 cudaError_t launch_tc_red2(const TcRedArgs& a, const TcRedArgs& b, cudaStream_t st, int prof_kind);
 cudaError_t launch_split(const SplitTab& t, int n, cudaStream_t st);
 // count[0] = the number of items; count[1 + k] (k = 0 .. n_slots) = the first item of slot k, the

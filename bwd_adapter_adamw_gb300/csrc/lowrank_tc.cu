@@ -318,10 +318,12 @@ struct RedJob {
   int64_t N;
 };
 
-// One or two reductions over the same tokens and run table (dB and dA of a linear) in one
-// launch: grid x runs over job 0's tiles, then job 1's.
+// Up to kRedMaxJobs reductions over the same tokens, slots and run table (dB and dA of a linear,
+// or the dB of every projection of a fused group) in one launch: grid x runs over job 0's tiles,
+// then job 1's, and so on.
+constexpr int kRedMaxJobs = 4;
 struct RedParams {
-  RedJob job[2];
+  RedJob job[kRedMaxJobs];
   int32_t n_jobs;
   const TokenItem* items;            // 64-token aligned runs grouped by slot (null: the uniform
                                      // runs of kRedSpanBlocks blocks over [0, T), slot 0)
@@ -329,6 +331,7 @@ struct RedParams {
   uint32_t* err;
   int64_t T;
 };
+static_assert(sizeof(RedParams) <= 32764, "kernel parameter block");
 
 // Tile: M = 128 split rows (2 r used), N = BN columns of B (256 or 128), K = 64 tokens per stage;
 // one CTA per SM with about 192 KB of stages in flight.
@@ -365,9 +368,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_red(const __grid_constant__ 
   const int slot = blockIdx.z;
   const int z = blockIdx.y;   // == rank in the cluster (cluster dims 1 x splits)
   const int splits = gridDim.y;
-  const int jb = (p.n_jobs > 1 && (int)blockIdx.x >= p.job[0].tiles) ? 1 : 0;
+  int jb = 0, bx = (int)blockIdx.x;
+  while (jb + 1 < p.n_jobs && bx >= p.job[jb].tiles) bx -= p.job[jb++].tiles;
   const RedJob& J = p.job[jb];
-  const int32_t n0 = ((int32_t)blockIdx.x - (jb ? p.job[0].tiles : 0)) * BN;
+  const int32_t n0 = bx * BN;
   const int r = J.rank[slot];
   // this CTA's work: items [w0, w1) of the slot's items, split evenly over the cluster (the
   // uniform runs of a single-adapter call are the items of one segment covering [0, T))
@@ -1085,6 +1089,7 @@ bool fill_red_job(RedJob& j, const TcRedArgs& a, int bn) {
 }
 
 cudaError_t launch_tc_red_jobs(const TcRedArgs* jobs, int n_jobs, cudaStream_t st, int prof_kind) {
+  if (n_jobs < 1 || n_jobs > kRedMaxJobs) return cudaErrorInvalidValue;
   static RedParams prm;
   static std::mutex mu;
   std::lock_guard<std::mutex> lk(mu);
@@ -1139,13 +1144,27 @@ cudaError_t launch_tc_red(const TcRedArgs& a, cudaStream_t st, int prof_kind) {
   return launch_tc_red_jobs(&a, 1, st, prof_kind);
 }
 
+cudaError_t launch_tc_red_n(const TcRedArgs* jobs, int n, cudaStream_t st, int prof_kind) {
+  // in launches of at most kRedMaxJobs jobs
+  for (int q0 = 0; q0 < n; q0 += kRedMaxJobs) {
+    const int m = n - q0 < kRedMaxJobs ? n - q0 : kRedMaxJobs;
+    const TcRedArgs& a = jobs[q0];
+    for (int q = q0 + 1; q < q0 + m; ++q) {
+      const TcRedArgs& b = jobs[q];
+      if (a.T != b.T || a.n_slots != b.n_slots || a.items != b.items || a.n_items != b.n_items)
+        return cudaErrorInvalidValue;
+      for (int k = 0; k < a.n_slots; ++k)
+        if (a.rank[k] != b.rank[k]) return cudaErrorInvalidValue;
+    }
+    cudaError_t e = launch_tc_red_jobs(jobs + q0, m, st, prof_kind);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
 cudaError_t launch_tc_red2(const TcRedArgs& a, const TcRedArgs& b, cudaStream_t st, int prof_kind) {
-  if (a.T != b.T || a.n_slots != b.n_slots || a.items != b.items || a.n_items != b.n_items)
-    return cudaErrorInvalidValue;
-  for (int k = 0; k < a.n_slots; ++k)
-    if (a.rank[k] != b.rank[k]) return cudaErrorInvalidValue;
   const TcRedArgs jobs[2] = {a, b};
-  return launch_tc_red_jobs(jobs, 2, st, prof_kind);
+  return launch_tc_red_n(jobs, 2, st, prof_kind);
 }
 
 cudaError_t launch_adapter_prep(const TransposeTab& ta, const SplitTab& sb, int n,

@@ -57,8 +57,10 @@ def test_memory_counts_groups_count_shared_inputs_once():
     saved = (3 - 1) * T * 4096 * 2 + (2 - 1) * T * 4096 * 2
     # the adapters and Hs columns are the same in both counts; only the X reads differ
     assert x_reads(per_proj) - x_reads(grouped) == saved
-    # the output-gradient side is unchanged in total width
-    assert per_proj["redB"] == grouped["redB"]
+    # the reductions: dY' and the adapters are the same in both counts, and the grouped dA reads
+    # X once per group (the o and down groups reduce dB and dA in one launch, class "red")
+    red = lambda m: m["redB"] + m["redA"] + m.get("red", 0)
+    assert red(per_proj) - red(grouped) == saved
     assert per_proj["adamw"] == grouped["adamw"]
 
 
