@@ -147,9 +147,9 @@ def memory_counts(cfg: LI.LoraConfig, layers: int, groups=None):
 # `python bench.py --layers 1 --steps 2 --warmup 3 --no-cpu-baseline --streams 1`.
 NCU_TRAFFIC = {
     ("c4", 1): {"source": "gemm_tc.cu", "sha256_16": "4819c92179bf6c02",
-                "bytes": 385.8e6,
+                "bytes": 384.9e6,
                 "note": "one-layer capture (profiles/launch_list_c4_llama_bf16.md): the seven "
-                        "forward launches move 154.5, 78.6, 78.1, 154.0, 548.9, 550.5 and "
+                        "forward launches move 152.9, 78.3, 78.3, 153.9, 546.1, 548.6 and "
                         "1136.2 MB (read + write); the wide and long shapes re-read operands "
                         "while compute-bound"},
     ("c2", 1): {"source": "gemm_tc_f32.cu", "sha256_16": "0cfe552134b8e004",
