@@ -509,13 +509,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_red(const __grid_constant__ 
   }
   __syncthreads();
   cluster_sync_all();   // every CTA's partial tile is in its shared memory
-  const int W = kRedBN / splits;
+  // CTA z adds columns [cz0, cz1) of the tile: W (a multiple of 4) each, the last CTAs of a
+  // cluster whose size does not divide BN fewer or none
+  const int W = ((kRedBN + splits - 1) / splits + 3) / 4 * 4;
+  const int cz0 = z * W, cz1 = min(kRedBN, cz0 + W);
+  const int Wz = cz1 > cz0 ? cz1 - cz0 : 0;
   float* dst = J.dst[slot];
   if (!J.transposed) {
-    // dA [r, N]: rows j, columns n0 + z W ..
-    const int w4 = W / 4;
+    // dA [r, N]: rows j, columns n0 + cz0 ..
+    const int w4 = Wz / 4;
     for (int e = threadIdx.x; e < r * w4; e += kThreads) {
-      const int j = e / w4, c = z * W + 4 * (e - (e / w4) * w4);
+      const int j = e / w4, c = cz0 + 4 * (e - (e / w4) * w4);
       const int64_t n = (int64_t)n0 + c;
       if (n >= J.N) continue;
       float4 pz[kRedMaxSplits];
@@ -534,10 +538,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_red(const __grid_constant__ 
       *o = acc;
     }
   } else {
-    // dB [N, r]: rows n0 + z W .., columns j
+    // dB [N, r]: rows n0 + cz0 .., columns j
     const int r4 = r / 4;
-    for (int e = threadIdx.x; e < W * r4; e += kThreads) {
-      const int c = z * W + e / r4, j = 4 * (e - (e / r4) * r4);
+    for (int e = threadIdx.x; e < Wz * r4; e += kThreads) {
+      const int c = cz0 + e / r4, j = 4 * (e - (e / r4) * r4);
       const int64_t n = (int64_t)n0 + c;
       if (n >= J.N) continue;
       float4 pz[kRedMaxSplits];
@@ -1036,22 +1040,22 @@ int resident_clusters(K kernel, int smem, int size) {
   return n;
 }
 
-// resident clusters of k_tc_red<BN> per cluster size 1, 2, 4, 8, 16 (cached per device)
+// resident clusters of k_tc_red<BN> per cluster size 1 .. kRedMaxSplits (cached per device)
 template <int BN>
 int red_resident(int size) {
-  static int cache[64][5];
+  static int cache[64][kRedMaxSplits];
   static bool done[64] = {};
   static std::mutex mu;
   int dev = 0;
+  if (size < 1 || size > kRedMaxSplits) return 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   std::lock_guard<std::mutex> lk(mu);
   if (!done[dev]) {
-    for (int i = 0; i < 5; ++i) cache[dev][i] = resident_clusters(k_tc_red<BN>, RedCfg<BN>::kSmem, 1 << i);
+    for (int i = 0; i < kRedMaxSplits; ++i)
+      cache[dev][i] = resident_clusters(k_tc_red<BN>, RedCfg<BN>::kSmem, i + 1);
     done[dev] = true;
   }
-  int i = 0;
-  while (i < 4 && (1 << i) < size) ++i;
-  return (1 << i) == size ? cache[dev][i] : 0;
+  return cache[dev][size - 1];
 }
 
 template <int BN>
@@ -1096,9 +1100,10 @@ cudaError_t launch_tc_red_jobs(const TcRedArgs* jobs, int n_jobs, cudaStream_t s
   std::memset(&prm, 0, sizeof(prm));
   const TcRedArgs& a = jobs[0];
   if (a.T <= 0 || a.n_slots <= 0) return cudaSuccess;
-  // Tile width and token splits (CTAs of one cluster): the most CTAs, one per SM at most, whose
-  // clusters are all resident at once, with at least two 64-token blocks of T per split; the
-  // wider tile on ties (it re-reads the split operand less).
+  // Tile width and token splits (CTAs of one cluster, any size up to kRedMaxSplits): the most
+  // CTAs, one per SM at most, whose clusters are all resident at once, with at least two 64-token
+  // blocks of T per split; the wider tile and the smaller cluster on ties (the wider tile
+  // re-reads the split operand less).
   const int sms = tc::sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
   int best_bn = 256, best_splits = 1;
@@ -1106,7 +1111,7 @@ cudaError_t launch_tc_red_jobs(const TcRedArgs* jobs, int n_jobs, cudaStream_t s
   for (int bn : {256, 128}) {
     int64_t tiles = 0;
     for (int q = 0; q < n_jobs; ++q) tiles += (jobs[q].N + bn - 1) / bn;
-    for (int c = 1; c <= kRedMaxSplits; c *= 2) {
+    for (int c = 1; c <= kRedMaxSplits; ++c) {
       const int64_t clusters = tiles * a.n_slots;
       if (clusters * c > sms || (c > 1 && (a.T + 63) / 64 < 2 * (int64_t)c)) break;
       const int res = bn == 256 ? red_resident<256>(c) : red_resident<128>(c);
