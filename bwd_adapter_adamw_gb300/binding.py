@@ -109,6 +109,12 @@ def _load() -> C.CDLL:
                                          C.POINTER(lora_slot), P, P, P, SZ, P]),
         "multi_lora_backward": (C.c_int, [DP, CP, I64, P, P, I32, P, P, I32,
                                           C.POINTER(lora_slot), P, P, P, P, SZ, P]),
+        "multi_lora_plan_size": (SZ, [I64, I32, I32]),
+        "multi_lora_plan_build": (C.c_int, [I64, I32, P, P, I32, P, SZ, P]),
+        "multi_lora_forward_planned": (C.c_int, [DP, CP, I64, I32, P, P, P, P, I32,
+                                                 C.POINTER(lora_slot), P, P, P, SZ, P]),
+        "multi_lora_backward_planned": (C.c_int, [DP, CP, I64, I32, P, P, P, I32,
+                                                  C.POINTER(lora_slot), P, P, P, P, SZ, P]),
         "lora_dropout_mask": (C.c_int, [DP, CP, I64, P, P]),
         "lora_quantize_e4m3": (C.c_int, [P, I64, I64, P, P, P]),
         "multi_lora_token_slots": (C.c_int, [I64, I32, P, P, I32, P, P]),
@@ -134,6 +140,8 @@ EXPORTED = ("lora_status_string", "lora_scale", "lora_lr_at", "lora_workspace_si
             "lora_grad_prepare_workspace_size", "lora_grad_prepare", "lora_grad_prepare_noalloc",
             "lora_adamw_step", "lora_snapshot", "lora_restore", "lora_retire",
             "multi_lora_workspace_size", "multi_lora_forward", "multi_lora_backward",
+            "multi_lora_plan_size", "multi_lora_plan_build", "multi_lora_forward_planned",
+            "multi_lora_backward_planned",
             "lora_fused_workspace_size", "lora_fused_forward", "lora_fused_backward",
             "lora_dropout_mask", "lora_quantize_e4m3", "multi_lora_token_slots", "lora_profile_arm",
             "lora_profile_used", "lora_launch_counter", "lora_last_cuda_error",
@@ -376,6 +384,38 @@ def multi_lora_backward(d, c, T, X, W_prep, n_seg, seg_start, seg_slot, slots, d
                                   slots, _ptr(dY), _ptr(H_save), _ptr(dX), _ptr(ws), nbytes,
                                   _stream(stream))
     return _check(st, "multi_lora_backward") if check else st
+
+
+def multi_lora_plan_size(T: int, n_seg: int, n_slots: int) -> int:
+    return _lib.multi_lora_plan_size(T, n_seg, n_slots)
+
+
+def multi_lora_plan_build(T, n_seg, seg_start, seg_slot, n_slots, plan, plan_bytes=None,
+                          stream=None, check=True):
+    nbytes = plan_bytes if plan_bytes is not None else plan.numel() * plan.element_size()
+    st = _lib.multi_lora_plan_build(T, n_seg, _ptr(seg_start), _ptr(seg_slot), n_slots,
+                                    _ptr(plan), nbytes, _stream(stream))
+    return _check(st, "multi_lora_plan_build") if check else st
+
+
+def multi_lora_forward_planned(d, c, T, n_seg, plan, X, W, W_prep, slots, Y, H_save, ws,
+                               ws_bytes=None, stream=None, check=True):
+    nbytes = ws_bytes if ws_bytes is not None else ws.numel() * ws.element_size()
+    st = _lib.multi_lora_forward_planned(C.byref(d), C.byref(c) if c is not None else None, T,
+                                         n_seg, _ptr(plan), _ptr(X), _ptr(W), _ptr(W_prep),
+                                         len(slots), slots, _ptr(Y), _ptr(H_save), _ptr(ws),
+                                         nbytes, _stream(stream))
+    return _check(st, "multi_lora_forward_planned") if check else st
+
+
+def multi_lora_backward_planned(d, c, T, n_seg, plan, X, W_prep, slots, dY, H_save, dX, ws,
+                                ws_bytes=None, stream=None, check=True):
+    nbytes = ws_bytes if ws_bytes is not None else ws.numel() * ws.element_size()
+    st = _lib.multi_lora_backward_planned(C.byref(d), C.byref(c) if c is not None else None, T,
+                                          n_seg, _ptr(plan), _ptr(X), _ptr(W_prep), len(slots),
+                                          slots, _ptr(dY), _ptr(H_save), _ptr(dX), _ptr(ws),
+                                          nbytes, _stream(stream))
+    return _check(st, "multi_lora_backward_planned") if check else st
 
 
 def lora_dropout_mask(d: lora_desc, c: Optional[lora_ctx], T: int, mask, stream=None, check=True):

@@ -328,6 +328,47 @@ size_t ws_size(const lora_desc* d, int64_t T, int32_t n_seg, int n_slots, int64_
   return carve(d, T, n_seg, n_slots, rank_sum, true, nullptr).bytes;
 }
 
+// Routing plan: the token work tables of routed calls over one batch (T, segments, slots), built
+// once and read by every planned call: the row products' items, the fp32 reductions' items, the
+// tensor-core reductions' runs and the slot mask of every 128-token tile. Its layout is a function
+// of (T, n_seg, n_slots) alone.
+struct RoutePlan {
+  TokenItem* gitems; int32_t* gcount; int64_t gmax;
+  TokenItem* ritems; int32_t* rcount; int64_t rmax;
+  TokenItem* items_red; int32_t* count_red; int64_t max_red;
+  uint32_t* tmask;
+  size_t bytes;
+};
+
+RoutePlan plan_carve(int64_t T, int32_t n_seg, int32_t n_slots, void* buf) {
+  RoutePlan P{};
+  Carve c(buf);
+  P.gmax = max_gemm_items(T, n_seg);
+  P.rmax = max_red_items(T, n_seg);
+  P.max_red = red_items_bound(T, n_seg, n_slots, kRedSpanBlocks);
+  P.gitems = c.take<TokenItem>((size_t)P.gmax);
+  P.gcount = c.take<int32_t>(4);
+  P.ritems = c.take<TokenItem>((size_t)P.rmax);
+  P.rcount = c.take<int32_t>(4);
+  P.items_red = c.take<TokenItem>((size_t)P.max_red);
+  P.count_red = c.take<int32_t>(LORA_MAX_SLOTS + 8);
+  P.tmask = c.take<uint32_t>((size_t)((T + kGemmTileT - 1) / kGemmTileT));
+  P.bytes = c.off + kWsAlign;
+  return P;
+}
+
+// The call's tables become the plan's (the workspace copies go unused).
+void apply_plan(Layout& L, const RoutePlan& P) {
+  L.gitems = P.gitems; L.gcount = P.gcount;
+  if (L.ritems) { L.ritems = P.ritems; L.rcount = P.rcount; }
+  if (L.items_db) {
+    L.items_db = L.items_da = P.items_red;
+    L.count_db = L.count_da = P.count_red;
+    L.max_db = L.max_da = P.max_red;
+  }
+  if (L.tmask) L.tmask = P.tmask;
+}
+
 SlotInfo slot_info(const Slots& s, float q) {
   SlotInfo si{};
   int32_t region = 0;
@@ -389,8 +430,9 @@ int tc_shrink(const lora_desc* d, const DropParams& dp, int64_t T, const void* X
 // terms of the slots present in it from the slot-expanded operand (zeroed first: a token's row is
 // zero outside its slot's column block).
 int routed_tiles(int64_t T, int32_t n_seg, const int32_t* seg_start, const int32_t* seg_slot,
-                 const Slots& s, const Layout& L, cudaStream_t st) {
-  LORA_TRY(launch_tile_slot_masks(T, n_seg, seg_start, seg_slot, s.n, L.tmask, st));
+                 const Slots& s, const Layout& L, bool masks_ready, cudaStream_t st) {
+  if (!masks_ready)
+    LORA_TRY(launch_tile_slot_masks(T, n_seg, seg_start, seg_slot, s.n, L.tmask, st));
   LORA_TRY(cudaMemsetAsync(L.Px, 0, (size_t)T * L.ldx * sizeof(float), st));
   return LORA_OK;
 }
@@ -420,11 +462,14 @@ void set_routed_gemm(TcGemmArgs& t, const Slots& s, const Layout& L, int64_t T, 
 int run_forward_tc(const lora_desc* d, const DropParams& dp, int64_t T, const void* X,
                    const void* W, const void* Wprep, int32_t n_seg, const int32_t* seg_start,
                    const int32_t* seg_slot, const Slots& s, const float* ratio_src_m,
-                   const float* ratio_src_n, void* Y, float* H, void* ws, cudaStream_t st) {
+                   const float* ratio_src_n, void* Y, float* H, void* ws, cudaStream_t st,
+                   const RoutePlan* plan = nullptr) {
   Layout L = carve(d, T, n_seg, s.n, s.rank_sum, false, ws);
   clear_stale();
   if (n_seg < 0)
     use_uniform_items(L, T);
+  else if (plan)
+    apply_plan(L, *plan);
   else
     LORA_TRY(launch_make_items(T, n_seg, seg_start, seg_slot, s.n, L.gitems, L.gcount,
                                (int32_t)L.gmax, nullptr, nullptr, 0, st));
@@ -438,7 +483,7 @@ int run_forward_tc(const lora_desc* d, const DropParams& dp, int64_t T, const vo
     LORA_TRY(launch_quant_rows_e4m3(X, T, d->in_dim, L.Aq, L.sq, st));
   const bool routed = n_seg >= 0;
   if (routed) {
-    int rr = routed_tiles(T, n_seg, seg_start, seg_slot, s, L, st);
+    int rr = routed_tiles(T, n_seg, seg_start, seg_slot, s, L, plan != nullptr, st);
     if (rr) return rr;
   }
   int rc = tc_shrink(d, dp, T, X, n_seg, s, L, H, routed ? L.Px : nullptr, st);
@@ -468,11 +513,16 @@ int run_backward_tc(const lora_desc* d, const DropParams& dp, int64_t T, const v
                     const void* Wt, int32_t n_seg, const int32_t* seg_start,
                     const int32_t* seg_slot, const Slots& s, const void* dY, const float* H,
                     const float* dora_m, const float* dora_n, const void* Y_save, void* dX,
-                    float* dm, void* ws, cudaStream_t st) {
+                    float* dm, void* ws, cudaStream_t st, const RoutePlan* plan = nullptr) {
   Layout L = carve(d, T, n_seg, s.n, s.rank_sum, true, ws);
   clear_stale();
   if (n_seg < 0) {
     use_uniform_items(L, T);
+  } else if (plan) {
+    if (L.span_db != kRedSpanBlocks || L.span_da != kRedSpanBlocks) return LORA_ERR_INVALID;
+    apply_plan(L, *plan);
+    int rr = routed_tiles(T, n_seg, seg_start, seg_slot, s, L, true, st);
+    if (rr) return rr;
   } else {
     LORA_TRY(launch_make_items(T, n_seg, seg_start, seg_slot, s.n, L.gitems, L.gcount,
                                (int32_t)L.gmax, nullptr, nullptr, 0, st));
@@ -486,7 +536,7 @@ int run_backward_tc(const lora_desc* d, const DropParams& dp, int64_t T, const v
       LORA_TRY(launch_make_red_items_tc(T, n_seg, seg_start, seg_slot, s.n, L.span_da, L.items_da,
                                         L.count_da, (int32_t)L.max_da, st));
     }
-    int rr = routed_tiles(T, n_seg, seg_start, seg_slot, s, L, st);
+    int rr = routed_tiles(T, n_seg, seg_start, seg_slot, s, L, false, st);
     if (rr) return rr;
   }
   const bool routed = n_seg >= 0;
@@ -604,18 +654,19 @@ int run_backward_tc(const lora_desc* d, const DropParams& dp, int64_t T, const v
 int run_forward(const lora_desc* d, const DropParams& dp, int64_t T, const void* X, const void* W,
                 const void* Wprep, int32_t n_seg, const int32_t* seg_start, const int32_t* seg_slot, const Slots& s,
                 const float* ratio_src_m, const float* ratio_src_n, void* Y, float* H, void* ws,
-                cudaStream_t st) {
+                cudaStream_t st, const RoutePlan* plan = nullptr) {
   if (d->dtype != LORA_F32)
     return run_forward_tc(d, dp, T, X, W, Wprep, n_seg, seg_start, seg_slot, s, ratio_src_m,
-                          ratio_src_n, Y, H, ws, st);
+                          ratio_src_n, Y, H, ws, st, plan);
   Layout L = carve(d, T, n_seg, s.n, s.rank_sum, false, ws);
   clear_stale();
+  if (plan && n_seg >= 0) apply_plan(L, *plan);
   // single adapter, rank <= 16: uniform token tiles computed in the kernels, single-pass shrink
   const bool fused = n_seg < 0 && d->rank <= 16;
   const TokenItem* items = fused ? nullptr : L.gitems;
   const int32_t* n_items = fused ? nullptr : L.gcount;
   const int max_items = fused ? (int)((T + kGemmTileT - 1) / kGemmTileT) : (int)L.gmax;
-  if (!fused)
+  if (!fused && !(plan && n_seg >= 0))
     LORA_TRY(launch_make_items(T, n_seg, seg_start, seg_slot, s.n, L.gitems, L.gcount,
                                (int32_t)L.gmax, L.ritems, L.rcount, (int32_t)L.rmax, st));
   const float q = dropout_q(d);
@@ -658,19 +709,21 @@ int run_forward(const lora_desc* d, const DropParams& dp, int64_t T, const void*
 int run_backward(const lora_desc* d, const DropParams& dp, int64_t T, const void* X, const void* Wt,
                  int32_t n_seg, const int32_t* seg_start, const int32_t* seg_slot, const Slots& s,
                  const void* dY, const float* H, const float* dora_m, const float* dora_n,
-                 const void* Y_save, void* dX, float* dm, void* ws, cudaStream_t st) {
+                 const void* Y_save, void* dX, float* dm, void* ws, cudaStream_t st,
+                 const RoutePlan* plan = nullptr) {
   if (d->dtype != LORA_F32)
     return run_backward_tc(d, dp, T, X, Wt, n_seg, seg_start, seg_slot, s, dY, H, dora_m, dora_n,
-                           Y_save, dX, dm, ws, st);
+                           Y_save, dX, dm, ws, st, plan);
   Layout L = carve(d, T, n_seg, s.n, s.rank_sum, true, ws);
   clear_stale();
+  if (plan && n_seg >= 0) apply_plan(L, *plan);
   // single adapter, rank <= 16: uniform token tiles, single-pass G that also writes A^T, and
   // token reductions that finish inside their thread-block clusters (4 launches)
   const bool fused = n_seg < 0 && d->rank <= 16;
   const TokenItem* items = fused ? nullptr : L.gitems;
   const int32_t* n_items = fused ? nullptr : L.gcount;
   const int max_items = fused ? (int)((T + kGemmTileT - 1) / kGemmTileT) : (int)L.gmax;
-  if (!fused)
+  if (!fused && !(plan && n_seg >= 0))
     LORA_TRY(launch_make_items(T, n_seg, seg_start, seg_slot, s.n, L.gitems, L.gcount,
                                (int32_t)L.gmax, L.ritems, L.rcount, (int32_t)L.rmax, st));
   const float q = dropout_q(d);
@@ -1316,17 +1369,21 @@ int lora_backward(const lora_desc* d, const lora_ctx* c, int64_t T, const void* 
                       d->dora ? dm : nullptr, ws, (cudaStream_t)stream);
 }
 
-int multi_lora_forward(const lora_desc* d, const lora_ctx* c, int64_t T, const void* X,
-                       const void* W, const void* W_prep, int32_t n_seg,
-                       const int32_t* d_seg_start, const int32_t* d_seg_slot, int32_t n_slots,
-                       const lora_slot* slots, void* Y, float* H_save, void* ws, size_t ws_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+int multi_forward(const lora_desc* d, const lora_ctx* c, int64_t T, const void* X, const void* W,
+                  const void* W_prep, int32_t n_seg, const int32_t* d_seg_start,
+                  const int32_t* d_seg_slot, const RoutePlan* plan, int32_t n_slots,
+                  const lora_slot* slots, void* Y, float* H_save, void* ws, size_t ws_bytes,
+                  void* stream) {
   int rc = check_desc(d, T, true);
   if (rc) return rc;
   DropParams dp;
   if ((rc = build_drop(d, c, T, dp))) return rc;
   Slots s;
   if ((rc = slots_from_table(d, n_slots, slots, false, s))) return rc;
-  if (n_seg < 0 || (n_seg > 0 && (!d_seg_start || !d_seg_slot))) return LORA_ERR_INVALID;
+  if (n_seg < 0 || (n_seg > 0 && !plan && (!d_seg_start || !d_seg_slot))) return LORA_ERR_INVALID;
   if (!X || !W || !W_prep || !Y || !H_save || !ws) return LORA_ERR_INVALID;
   if (!al16(X) || !al16(W) || !al16(W_prep) || !al16(Y) || !al16(H_save) || !al16(ws))
     return LORA_ERR_ALIGN;
@@ -1334,21 +1391,21 @@ int multi_lora_forward(const lora_desc* d, const lora_ctx* c, int64_t T, const v
   if (T == 0) return LORA_OK;
   return run_forward(d, dp, T, X, W, W_prep, n_seg, n_seg ? d_seg_start : nullptr,
                      n_seg ? d_seg_slot : nullptr, s, nullptr, nullptr, Y, H_save, ws,
-                     (cudaStream_t)stream);
+                     (cudaStream_t)stream, plan);
 }
 
-int multi_lora_backward(const lora_desc* d, const lora_ctx* c, int64_t T, const void* X,
-                        const void* W_prep, int32_t n_seg, const int32_t* d_seg_start,
-                        const int32_t* d_seg_slot, int32_t n_slots, const lora_slot* slots,
-                        const void* dY, const float* H_save, void* dX, void* ws,
-                        size_t ws_bytes, void* stream) {
+int multi_backward(const lora_desc* d, const lora_ctx* c, int64_t T, const void* X,
+                   const void* W_prep, int32_t n_seg, const int32_t* d_seg_start,
+                   const int32_t* d_seg_slot, const RoutePlan* plan, int32_t n_slots,
+                   const lora_slot* slots, const void* dY, const float* H_save, void* dX, void* ws,
+                   size_t ws_bytes, void* stream) {
   int rc = check_desc(d, T, true);
   if (rc) return rc;
   DropParams dp;
   if ((rc = build_drop(d, c, T, dp))) return rc;
   Slots s;
   if ((rc = slots_from_table(d, n_slots, slots, true, s))) return rc;
-  if (n_seg < 0 || (n_seg > 0 && (!d_seg_start || !d_seg_slot))) return LORA_ERR_INVALID;
+  if (n_seg < 0 || (n_seg > 0 && !plan && (!d_seg_start || !d_seg_slot))) return LORA_ERR_INVALID;
   if (!X || !W_prep || !dY || !H_save || !ws) return LORA_ERR_INVALID;
   if (!al16(X) || !al16(W_prep) || !al16(dY) || !al16(H_save) || !al16(ws) || (dX && !al16(dX)))
     return LORA_ERR_ALIGN;
@@ -1356,7 +1413,84 @@ int multi_lora_backward(const lora_desc* d, const lora_ctx* c, int64_t T, const 
   if (T == 0) return LORA_OK;
   return run_backward(d, dp, T, X, W_prep, n_seg, n_seg ? d_seg_start : nullptr,
                       n_seg ? d_seg_slot : nullptr, s, dY, H_save, nullptr, nullptr, nullptr, dX,
-                      nullptr, ws, (cudaStream_t)stream);
+                      nullptr, ws, (cudaStream_t)stream, plan);
+}
+
+// a plan's tables for (T, n_seg, n_slots), or LORA_ERR_* on bad arguments
+int plan_of(int64_t T, int32_t n_seg, int32_t n_slots, const void* plan, RoutePlan& P) {
+  if (!plan || T < 0 || n_seg < 1 || n_slots < 1 || n_slots > LORA_MAX_SLOTS)
+    return LORA_ERR_INVALID;
+  if (!al16(plan)) return LORA_ERR_ALIGN;
+  P = plan_carve(T, n_seg, n_slots, const_cast<void*>(plan));
+  return LORA_OK;
+}
+}  // namespace
+
+extern "C" {
+
+int multi_lora_forward(const lora_desc* d, const lora_ctx* c, int64_t T, const void* X,
+                       const void* W, const void* W_prep, int32_t n_seg,
+                       const int32_t* d_seg_start, const int32_t* d_seg_slot, int32_t n_slots,
+                       const lora_slot* slots, void* Y, float* H_save, void* ws, size_t ws_bytes, void* stream) {
+  return multi_forward(d, c, T, X, W, W_prep, n_seg, d_seg_start, d_seg_slot, nullptr, n_slots,
+                       slots, Y, H_save, ws, ws_bytes, stream);
+}
+
+int multi_lora_backward(const lora_desc* d, const lora_ctx* c, int64_t T, const void* X,
+                        const void* W_prep, int32_t n_seg, const int32_t* d_seg_start,
+                        const int32_t* d_seg_slot, int32_t n_slots, const lora_slot* slots,
+                        const void* dY, const float* H_save, void* dX, void* ws,
+                        size_t ws_bytes, void* stream) {
+  return multi_backward(d, c, T, X, W_prep, n_seg, d_seg_start, d_seg_slot, nullptr, n_slots,
+                        slots, dY, H_save, dX, ws, ws_bytes, stream);
+}
+
+size_t multi_lora_plan_size(int64_t T, int32_t n_seg, int32_t n_slots) {
+  if (T < 0 || n_seg < 1 || n_slots < 1 || n_slots > LORA_MAX_SLOTS) return 0;
+  return plan_carve(T, n_seg, n_slots, nullptr).bytes;
+}
+
+int multi_lora_plan_build(int64_t T, int32_t n_seg, const int32_t* d_seg_start,
+                          const int32_t* d_seg_slot, int32_t n_slots, void* plan, size_t plan_bytes,
+                          void* stream) {
+  RoutePlan P;
+  int rc = plan_of(T, n_seg, n_slots, plan, P);
+  if (rc) return rc;
+  if (!d_seg_start || !d_seg_slot) return LORA_ERR_INVALID;
+  if (T > INT32_MAX - 256) return LORA_ERR_UNSUPPORTED;
+  if (plan_bytes < P.bytes) return LORA_ERR_WORKSPACE;
+  if (T == 0) return LORA_OK;   // planned calls over no tokens return before reading the plan
+  clear_stale();
+  const cudaStream_t st = (cudaStream_t)stream;
+  LORA_TRY(launch_make_items(T, n_seg, d_seg_start, d_seg_slot, n_slots, P.gitems, P.gcount,
+                             (int32_t)P.gmax, P.ritems, P.rcount, (int32_t)P.rmax, st));
+  LORA_TRY(launch_make_red_items_tc(T, n_seg, d_seg_start, d_seg_slot, n_slots, kRedSpanBlocks,
+                                    P.items_red, P.count_red, (int32_t)P.max_red, st));
+  LORA_TRY(launch_tile_slot_masks(T, n_seg, d_seg_start, d_seg_slot, n_slots, P.tmask, st));
+  return LORA_OK;
+}
+
+int multi_lora_forward_planned(const lora_desc* d, const lora_ctx* c, int64_t T, int32_t n_seg,
+                               const void* plan, const void* X, const void* W, const void* W_prep,
+                               int32_t n_slots, const lora_slot* slots, void* Y, float* H_save,
+                               void* ws, size_t ws_bytes, void* stream) {
+  RoutePlan P;
+  int rc = plan_of(T, n_seg, n_slots, plan, P);
+  if (rc) return rc;
+  return multi_forward(d, c, T, X, W, W_prep, n_seg, nullptr, nullptr, &P, n_slots, slots, Y,
+                       H_save, ws, ws_bytes, stream);
+}
+
+int multi_lora_backward_planned(const lora_desc* d, const lora_ctx* c, int64_t T, int32_t n_seg,
+                                const void* plan, const void* X, const void* W_prep,
+                                int32_t n_slots, const lora_slot* slots, const void* dY,
+                                const float* H_save, void* dX, void* ws, size_t ws_bytes,
+                                void* stream) {
+  RoutePlan P;
+  int rc = plan_of(T, n_seg, n_slots, plan, P);
+  if (rc) return rc;
+  return multi_backward(d, c, T, X, W_prep, n_seg, nullptr, nullptr, &P, n_slots, slots, dY,
+                        H_save, dX, ws, ws_bytes, stream);
 }
 
 size_t lora_grad_prepare_workspace_size(int32_t n_groups, const lora_group* groups) {

@@ -423,7 +423,7 @@ class MultiLoraStep:
                  slot_scales: Sequence[float], dtype: str, tokens: int, seg_start: torch.Tensor,
                  seg_slot: torch.Tensor, dropout_p: float = 0.0, seed: int = 0,
                  max_norm: float = 1.0, hp: Optional[L.lora_adamw_hp] = None, n_streams: int = 1,
-                 device="cuda"):
+                 planned: bool = True, device="cuda"):
         self.linears = list(linears)
         self.ranks, self.scales = list(slot_ranks), list(slot_scales)
         self.n_slots = len(self.ranks)
@@ -472,6 +472,14 @@ class MultiLoraStep:
         if need == 0:
             raise L.LoraError(L.LORA_ERR_INVALID, "multi_lora_workspace_size")
         self.ws = [_ws(need, self.device) for _ in range(self.n_streams)]
+        # the routing plan: the batch's token work tables, built once per forward_backward and
+        # read by every linear's calls
+        self.plan = None
+        if planned and self.n_seg >= 1:
+            nbytes = L.multi_lora_plan_size(self.T, self.n_seg, self.n_slots)
+            if nbytes == 0:
+                raise L.LoraError(L.LORA_ERR_INVALID, "multi_lora_plan_size")
+            self.plan = _ws(nbytes, self.device)
         self.scale_norm = torch.zeros(2 * self.n_slots, dtype=torch.float64, device=self.device)
         self.status = torch.zeros(self.n_slots, dtype=torch.int32, device=self.device)
 
@@ -492,6 +500,9 @@ class MultiLoraStep:
 
     def forward_backward(self, opt_step: int = 0):
         main = torch.cuda.current_stream(self.device)
+        if self.plan is not None:
+            L.multi_lora_plan_build(self.T, self.n_seg, self.seg_start, self.seg_slot,
+                                    self.n_slots, self.plan, stream=main)
         k, use = _streams_in_use(self)
         _fork(main, use)
         for i, l in enumerate(self.linears):
@@ -500,10 +511,16 @@ class MultiLoraStep:
             d = self.desc(l)
             ctx = L.make_ctx(opt_step, 0, 0)
             sl = self.slots(l)
-            L.multi_lora_forward(d, ctx, self.T, l.X, l.W, l.Wp, self.n_seg, self.seg_start,
-                                 self.seg_slot, sl, l.Y, l.H, ws, stream=st)
-            L.multi_lora_backward(d, ctx, self.T, l.X, l.Wp, self.n_seg, self.seg_start,
-                                  self.seg_slot, sl, l.dY, l.H, l.dX, ws, stream=st)
+            if self.plan is not None:
+                L.multi_lora_forward_planned(d, ctx, self.T, self.n_seg, self.plan, l.X, l.W, l.Wp,
+                                             sl, l.Y, l.H, ws, stream=st)
+                L.multi_lora_backward_planned(d, ctx, self.T, self.n_seg, self.plan, l.X, l.Wp, sl,
+                                              l.dY, l.H, l.dX, ws, stream=st)
+            else:
+                L.multi_lora_forward(d, ctx, self.T, l.X, l.W, l.Wp, self.n_seg, self.seg_start,
+                                     self.seg_slot, sl, l.Y, l.H, ws, stream=st)
+                L.multi_lora_backward(d, ctx, self.T, l.X, l.Wp, self.n_seg, self.seg_start,
+                                      self.seg_slot, sl, l.dY, l.H, l.dX, ws, stream=st)
         _join(main, use)
 
     def groups(self, ready: Sequence[int], gbs: Sequence[int], lrs: Sequence[float],

@@ -335,6 +335,35 @@ int multi_lora_backward(const lora_desc* d, const lora_ctx* c, int64_t T, const 
                         const void* dY, const float* H_save, void* dX, void* ws,
                         size_t ws_bytes, void* stream);
 
+/* Routing plan. Every routed call over the same batch (T, segments, slots: the same token
+ * routing for every projection and layer, "Multi-LoRA Training Example", Design: slot-keyed
+ * page table, one routing per batch) needs the same token work tables: the row products' token
+ * items, the token reductions' runs and the slot set of every 128-token tile. A plan holds them
+ * in a caller-owned device buffer of multi_lora_plan_size(T, n_seg, n_slots) bytes (0 for bad
+ * arguments), 16-byte aligned. multi_lora_plan_build fills it from the segment table (the same
+ * rules as multi_lora_forward; three launches on `stream`); the *_planned calls take
+ * (T, n_seg, plan) in place of the segment table, read the plan on their own stream and build
+ * nothing, so any number of calls, on any streams ordered after the build, may share one plan.
+ * A plan stays valid until the caller rewrites its buffer; its contents depend on
+ * (T, n_seg, n_slots) and the segment table only, so a planned call passes the same T, n_seg and
+ * n_slots as the build. Results are bit-identical to the unplanned calls. Errors: LORA_ERR_INVALID
+ * (null pointers, n_seg < 1, n_slots outside 1..LORA_MAX_SLOTS), LORA_ERR_ALIGN,
+ * LORA_ERR_WORKSPACE (plan_bytes too small), LORA_ERR_UNSUPPORTED (T above 2^31 - 257), then
+ * the checks of multi_lora_forward / multi_lora_backward. */
+size_t multi_lora_plan_size(int64_t T, int32_t n_seg, int32_t n_slots);
+int multi_lora_plan_build(int64_t T, int32_t n_seg, const int32_t* d_seg_start,
+                          const int32_t* d_seg_slot, int32_t n_slots, void* plan, size_t plan_bytes,
+                          void* stream);
+int multi_lora_forward_planned(const lora_desc* d, const lora_ctx* c, int64_t T, int32_t n_seg,
+                               const void* plan, const void* X, const void* W, const void* W_prep,
+                               int32_t n_slots, const lora_slot* slots, void* Y, float* H_save,
+                               void* ws, size_t ws_bytes, void* stream);
+int multi_lora_backward_planned(const lora_desc* d, const lora_ctx* c, int64_t T, int32_t n_seg,
+                                const void* plan, const void* X, const void* W_prep,
+                                int32_t n_slots, const lora_slot* slots, const void* dY,
+                                const float* H_save, void* dX, void* ws, size_t ws_bytes,
+                                void* stream);
+
 /* ---- test hooks (not part of the timed path) ------------------------------------------------*/
 /* Keep mask M [T, in_dim] as uint8 (1 = kept), exactly as the kernels regenerate it. */
 /* Test hook: the per-row E4M3 quantisation of LORA_BF16_FP8 (see its definition) applied to a bf16

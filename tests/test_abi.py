@@ -139,6 +139,40 @@ def test_multi_argument_errors(L):
     assert st == L.LORA_ERR_WORKSPACE
 
 
+def test_plan_argument_errors(L):
+    """The routing plan's calls validate their arguments on the host, before any launch."""
+    assert L.multi_lora_plan_size(16384, 30, 8) > 0
+    assert L.multi_lora_plan_size(16384, 0, 8) == 0
+    assert L.multi_lora_plan_size(16384, 30, 0) == 0
+    assert L.multi_lora_plan_size(16384, 30, L.LORA_MAX_SLOTS + 1) == 0
+    # more segments take more room; T = 0 still has a layout
+    assert L.multi_lora_plan_size(16384, 300, 8) > L.multi_lora_plan_size(16384, 30, 8)
+    assert L.multi_lora_plan_size(0, 1, 1) > 0
+    size = L.multi_lora_plan_size(1024, 5, 2)
+    assert L.multi_lora_plan_build(1024, 5, None, FAKE, 2, FAKE, size, stream=0,
+                                   check=False) == L.LORA_ERR_INVALID
+    assert L.multi_lora_plan_build(1024, 5, FAKE, FAKE, 2, None, size, stream=0,
+                                   check=False) == L.LORA_ERR_INVALID
+    assert L.multi_lora_plan_build(1024, 5, FAKE, FAKE, 2, FAKE + 8, size, stream=0,
+                                   check=False) == L.LORA_ERR_ALIGN
+    assert L.multi_lora_plan_build(1024, 5, FAKE, FAKE, 2, FAKE, size - 16, stream=0,
+                                   check=False) == L.LORA_ERR_WORKSPACE
+    assert L.multi_lora_plan_build(0, 5, FAKE, FAKE, 2, FAKE, size, stream=0,
+                                   check=False) == L.LORA_OK   # no tokens: nothing to build
+    d = L.make_desc(2560, 4096, 64, 0.0, L.LORA_BF16)
+    slots = L.make_slots([dict(A=FAKE, B=FAKE, dA=FAKE, dB=FAKE, rank=8, scale=1.0),
+                          dict(A=FAKE, B=FAKE, dA=FAKE, dB=FAKE, rank=64, scale=2.0)])
+    st = L.multi_lora_forward_planned(d, None, 16, 0, FAKE, FAKE, FAKE, FAKE, slots, FAKE, FAKE,
+                                      FAKE, 1 << 30, stream=0, check=False)
+    assert st == L.LORA_ERR_INVALID   # a plan needs at least one segment
+    st = L.multi_lora_forward_planned(d, None, 16, 1, None, FAKE, FAKE, FAKE, slots, FAKE, FAKE,
+                                      FAKE, 1 << 30, stream=0, check=False)
+    assert st == L.LORA_ERR_INVALID
+    st = L.multi_lora_backward_planned(d, None, 16, 1, FAKE, FAKE, FAKE, slots, FAKE, FAKE, None,
+                                       FAKE, 16, stream=0, check=False)
+    assert st == L.LORA_ERR_WORKSPACE
+
+
 def test_optimizer_argument_errors(L):
     g1 = L.make_groups([dict(offset=0, n_a=100, n_b=50, grad_scale=0.1, max_norm=1.0),
                         dict(offset=148, n_a=8, grad_scale=0.1, max_norm=1.0)])

@@ -315,7 +315,7 @@ def test_multi_stream_matches_single_stream(L):
 
 
 # --------------------------------------------------------------------------------- multi-LoRA
-def _build_multi(cfg, proj_idx, T, device="cuda"):
+def _build_multi(cfg, proj_idx, T, device="cuda", planned=True, n_streams=1):
     from bwd_adapter_adamw_gb300 import binding as L
     from bwd_adapter_adamw_gb300.step import MultiLinear, MultiLoraStep
     r = LI.make_routing(cfg, T)
@@ -336,7 +336,7 @@ def _build_multi(cfg, proj_idx, T, device="cuda"):
                          seg_start=torch.tensor(r.seg_start, device=device),
                          seg_slot=torch.tensor(r.seg_slot, device=device),
                          dropout_p=cfg.dropout_p, seed=cfg.dropout_seed, max_norm=cfg.max_norm,
-                         hp=hp, device=device)
+                         hp=hp, planned=planned, n_streams=n_streams, device=device)
     for lin in step.linears:
         for k, (A, B) in enumerate(host[lin.proj_id]["slots"]):
             lin.A[k].copy_(A)
@@ -414,6 +414,25 @@ def test_multi_lora_parity(L, T, proj_idx, p, dtype):
     for k in not_ready:
         o, n = step.slot_off[k], step.slot_na[k] + step.slot_nb[k]
         assert torch.equal(step.arena.params[o:o + n], before[o:o + n])
+
+
+@pytest.mark.parametrize("T,proj_idx,p,dtype,streams", [(1500, [0, 3, 6], 0.25, "bf16", 3),
+                                                        (1500, [1], 0.0, "bf16", 1),
+                                                        (600, [0, 2], 0.25, "f32", 2)])
+def test_multi_planned_equals_unplanned(L, T, proj_idx, p, dtype, streams):
+    """Calls that read a routing plan (built once, shared by every linear and stream) give the
+    same bits as calls that build their own tables from the segment table."""
+    cfg = LI.with_overrides(LI.CONFIGS["c5"], dropout_p=p, dropout_seed=7, dtype=dtype)
+    outs = []
+    for planned in (False, True):
+        step, *_ = _build_multi(cfg, proj_idx, T, planned=planned, n_streams=streams)
+        assert (step.plan is not None) == planned
+        step.forward_backward(0)
+        torch.cuda.synchronize()
+        outs.append([t.clone() for l in step.linears for t in (l.Y, l.H, l.dX)] +
+                    [step.arena.grads.clone()])
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
 
 
 def test_multi_single_slot_equals_single_lora(L):
