@@ -12,7 +12,10 @@
 //             splits side by side), K split over a thread-block cluster of 1-8 CTAs.
 //  k_tc_red:  dst += sum_t (ST[j, t] + ST[r + j, t]) Bmn[t, n] (dA, dB^T). M = 128 (2 r rows of
 //             the slot's transposed split), N = 256 or 128 columns of dY' or Xd (MN-major
-//             tiles), K = tokens in 64-token blocks split over a cluster of up to 16 CTAs.
+//             tiles), K = tokens in 64-token blocks split over a cluster of 1 to 16 CTAs. Up to
+//             four reductions over the same tokens (dB and dA of a linear, the dB of every
+//             projection of a fused group) share one launch as a job table along grid x.
+//  k_tc_red_multi: dA of two to four adapters that read one Xd, each Xd tile streamed once.
 // One CTA per SM with about 192 KB of stages in flight. The split partials stay in shared memory
 // and the cluster adds them in split order through distributed shared memory, so no partial
 // reaches global memory and reruns are bitwise equal.

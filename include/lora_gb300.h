@@ -213,7 +213,9 @@ int lora_backward(const lora_desc* d, const lora_ctx* c, int64_t T, const void* 
 size_t lora_grad_prepare_workspace_size(int32_t n_groups, const lora_group* groups);
 
 /* Pass 1 of the two-pass clip for each group: S_g = sum of squares of grads[offset, offset+n)
- * accumulated in double (per-thread exact float-float partials combined in double), then
+ * accumulated beyond float precision (exact float-float per-thread partials, summed in
+ * float-float within a CTA and in double across CTAs; elements above 2^40 in magnitude go to a
+ * double accumulator, so no finite gradient overflows), then
  *   status[g] = LORA_ERR_NONFINITE if any element is NaN or +-Inf, else LORA_OK;
  *   scale_norm[2g]   = c = gamma * max_norm / norm if max_norm > 0 and norm > max_norm, else gamma
  *   scale_norm[2g+1] = norm = gamma * sqrt(S_g)
