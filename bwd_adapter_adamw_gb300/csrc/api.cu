@@ -496,8 +496,9 @@ int run_forward_tc(const lora_desc* d, const DropParams& dp, int64_t T, const vo
   if (fp8) {
     // Y = sx sw (X8 W8^T) + Hs B^T = sx sw (X8 W8^T + (Hs / sx)(B / sw)^T): one accumulator
     const Fp8Prep f = fp8_prep(Wprep, d->out_dim, d->in_dim);
-    LORA_TRY(launch_div_rows(H, d->rank, L.sq, T, d->rank, L.Pq, d->rank, st));
-    LORA_TRY(launch_div_rows(s.B[0], d->rank, f.sw, d->out_dim, d->rank, L.Qq, d->rank, st));
+    LORA_TRY(launch_div_rows2(DivRowsJob{H, d->rank, L.sq, T, d->rank, L.Pq, d->rank},
+                              DivRowsJob{s.B[0], d->rank, f.sw, d->out_dim, d->rank, L.Qq, d->rank},
+                              st));
     t.a = L.Aq; t.b = f.W8; t.fp8 = 1;
     t.p = L.Pq; t.q[0] = L.Qq;
     t.m_rowscale = L.sq; t.n_colscale = f.sw;
@@ -612,8 +613,9 @@ int run_backward_tc(const lora_desc* d, const DropParams& dp, int64_t T, const v
       // dX = sd swT (dY8 WT8^T) + Gs A: the LoRA operands divided by the same scales
       const Fp8Prep f = fp8_prep(Wt, d->out_dim, d->in_dim);
       LORA_TRY(launch_quant_rows_e4m3(dYp, T, d->out_dim, L.Aq, L.sq, st));
-      LORA_TRY(launch_div_rows(L.Gs, d->rank, L.sq, T, d->rank, L.Pq, d->rank, st));
-      LORA_TRY(launch_div_rows(At[0], d->rank, f.swT, d->in_dim, d->rank, L.Qq, d->rank, st));
+      LORA_TRY(launch_div_rows2(DivRowsJob{L.Gs, d->rank, L.sq, T, d->rank, L.Pq, d->rank},
+                                DivRowsJob{At[0], d->rank, f.swT, d->in_dim, d->rank, L.Qq, d->rank},
+                                st));
       t.a = L.Aq; t.b = f.WT8; t.fp8 = 1;
       t.p = L.Pq; t.q[0] = L.Qq;
       t.m_rowscale = L.sq; t.n_colscale = f.swT;

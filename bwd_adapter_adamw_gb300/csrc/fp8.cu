@@ -130,13 +130,22 @@ __global__ void __launch_bounds__(256) k_quant_cols(const __nv_bfloat16* __restr
 }
 
 // dst[r, :] = src[r, :] / scale[r] for an fp32 [rows, cols] matrix (row strides lds, ldd).
-__global__ void k_div_rows(const float* __restrict__ src, int64_t lds, const float* __restrict__ scale,
-                           int64_t rows, int64_t cols, float* __restrict__ dst, int64_t ldd) {
+// Two row divisions in one launch (the LoRA operands of an E4M3 product: Hs or Gs by the token
+// scales, B or A^T by the weight's scales); the grid-stride index runs over job 0's elements,
+// then job 1's.
+__global__ void k_div_rows(const DivRowsJob j0, const DivRowsJob j1) {
   grid_dep_sync();
-  const int64_t n = rows * cols;
+  const int64_t n0 = j0.rows * j0.cols, n = n0 + j1.rows * j1.cols;
   for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
        e += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = e / cols, c = e - r * cols;
+    const bool second = e >= n0;
+    const int64_t ee = second ? e - n0 : e;
+    const int64_t cols = second ? j1.cols : j0.cols;
+    const int64_t r = ee / cols, c = ee - r * cols;
+    const float* src = second ? j1.src : j0.src;
+    const float* scale = second ? j1.scale : j0.scale;
+    float* dst = second ? j1.dst : j0.dst;
+    const int64_t lds = second ? j1.lds : j0.lds, ldd = second ? j1.ldd : j0.ldd;
     dst[r * ldd + c] = __fdiv_rn(src[r * lds + c], scale[r]);
   }
 }
@@ -167,15 +176,23 @@ cudaError_t launch_quant_cols_e4m3(const void* W, int64_t rows, int64_t cols, ui
   return cudaGetLastError();
 }
 
-cudaError_t launch_div_rows(const float* src, int64_t lds, const float* scale, int64_t rows,
-                            int64_t cols, float* dst, int64_t ldd, cudaStream_t st) {
-  const int64_t n = rows * cols;
+cudaError_t launch_div_rows2(const DivRowsJob& a, const DivRowsJob& b, cudaStream_t st) {
+  const int64_t n = (a.rows > 0 && a.cols > 0 ? a.rows * a.cols : 0) +
+                    (b.rows > 0 && b.cols > 0 ? b.rows * b.cols : 0);
   if (n <= 0) return cudaSuccess;
+  DivRowsJob j0 = a, j1 = b;
+  if (j0.rows <= 0 || j0.cols <= 0) { j0.rows = 0; j0.cols = 1; }
+  if (j1.rows <= 0 || j1.cols <= 0) { j1.rows = 0; j1.cols = 1; }
   int64_t blocks = (n + 255) / 256;
   if (blocks > 4096) blocks = 4096;
   prof_begin(0, st);
-  launch_kernel(k_div_rows, (unsigned)blocks, 256, 0, st, src, lds, scale, rows, cols, dst, ldd);
+  launch_kernel(k_div_rows, (unsigned)blocks, 256, 0, st, j0, j1);
   return cudaGetLastError();
+}
+
+cudaError_t launch_div_rows(const float* src, int64_t lds, const float* scale, int64_t rows,
+                            int64_t cols, float* dst, int64_t ldd, cudaStream_t st) {
+  return launch_div_rows2(DivRowsJob{src, lds, scale, rows, cols, dst, ldd}, DivRowsJob{}, st);
 }
 
 }  // namespace lora

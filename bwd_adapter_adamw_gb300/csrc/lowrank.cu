@@ -208,27 +208,43 @@ __global__ void k_dropout_mask(const DropParams dp, int64_t T, int64_t in_dim, u
 }
 
 // dst[t, o] = bf16(src[t, o] * scale[o]): the DoRA dY' operand of the tensor-core dX product,
-// whose column scale runs along K and so cannot be applied in the epilogue.
-__global__ void k_colscale_bf16(const __nv_bfloat16* __restrict__ src, const float* __restrict__ scale,
-                                int64_t rows, int64_t cols, __nv_bfloat16* __restrict__ dst) {
+// whose column scale runs along K and so cannot be applied in the epilogue. A thread owns 8
+// adjacent columns (their scales loaded once) and walks a band of `band` rows (32, more when the
+// grid's y extent would exceed its limit) with four 16-byte loads in flight; consecutive threads
+// take consecutive 16-byte chunks of a row.
+constexpr int kColscaleThreads = 128;
+constexpr int kColscaleRows = 32;
+__global__ void __launch_bounds__(kColscaleThreads) k_colscale_bf16(
+    const __nv_bfloat16* __restrict__ src, const float* __restrict__ scale, int64_t rows,
+    int64_t cols, int64_t band, __nv_bfloat16* __restrict__ dst) {
   grid_dep_sync();
-  const int64_t n8 = rows * cols / 8;
-  for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < n8;
-       v += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t e = v * 8;
-    const int64_t c = e % cols;
-    float x[8];
-    load16(src + e, x);
+  const int64_t c = ((int64_t)blockIdx.x * kColscaleThreads + threadIdx.x) * 8;
+  if (c >= cols) return;
+  const float4 s0 = __ldg(reinterpret_cast<const float4*>(scale + c));
+  const float4 s1 = __ldg(reinterpret_cast<const float4*>(scale + c + 4));
+  const float sc[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+  const int64_t r0 = (int64_t)blockIdx.y * band;
+  const int64_t r1 = min(rows, r0 + band);
+  for (int64_t r = r0; r < r1; r += 4) {
+    uint4 v[4];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) x[j] *= __ldg(scale + c + j);
-    uint4 u;
-    uint32_t* w = &u.x;
+    for (int u = 0; u < 4; ++u)
+      if (r + u < r1) v[u] = __ldg(reinterpret_cast<const uint4*>(src + (r + u) * cols + c));
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      __nv_bfloat162 h = __floats2bfloat162_rn(x[2 * j], x[2 * j + 1]);
-      w[j] = *reinterpret_cast<uint32_t*>(&h);
+    for (int u = 0; u < 4; ++u) {
+      if (r + u >= r1) continue;
+      const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+      uint4 o;
+      uint32_t* ow = &o.x;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float x0 = __uint_as_float(w[j] << 16) * sc[2 * j];
+        const float x1 = __uint_as_float(w[j] & 0xFFFF0000u) * sc[2 * j + 1];
+        __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+        ow[j] = *reinterpret_cast<uint32_t*>(&h);
+      }
+      *reinterpret_cast<uint4*>(dst + (r + u) * cols + c) = o;
     }
-    *reinterpret_cast<uint4*>(dst + e) = u;
   }
 }
 
@@ -590,13 +606,15 @@ cudaError_t launch_dropout_mask(const DropParams& dp, int64_t T, int64_t in_dim,
 
 cudaError_t launch_colscale_bf16(const void* src, const float* scale, int64_t rows, int64_t cols,
                                  void* dst, cudaStream_t st) {
-  const int64_t n8 = rows * cols / 8;
-  if (n8 <= 0) return cudaSuccess;
-  int64_t blocks = (n8 + 255) / 256;
-  if (blocks > 16384) blocks = 16384;
+  if (rows <= 0 || cols <= 0) return cudaSuccess;
+  if (cols % 8) return cudaErrorInvalidValue;
+  int64_t band = kColscaleRows;
+  while ((rows + band - 1) / band > 65535) band *= 2;
+  const dim3 grid((unsigned)((cols / 8 + kColscaleThreads - 1) / kColscaleThreads),
+                  (unsigned)((rows + band - 1) / band));
   prof_begin(0, st);
-  launch_kernel(k_colscale_bf16, (unsigned)blocks, 256, 0, st, (const __nv_bfloat16*)src, scale, rows, cols,
-                                                    (__nv_bfloat16*)dst);
+  launch_kernel(k_colscale_bf16, grid, kColscaleThreads, 0, st, (const __nv_bfloat16*)src, scale,
+                rows, cols, band, (__nv_bfloat16*)dst);
   return cudaGetLastError();
 }
 
