@@ -435,6 +435,35 @@ def test_multi_planned_equals_unplanned(L, T, proj_idx, p, dtype, streams):
         assert torch.equal(a, b)
 
 
+def test_multi_many_short_segments(L):
+    """More than 2048 segments (lengths 1-8 over 10000 tokens): the item builders take their
+    serial form. The planned and unplanned calls agree bit for bit, and both match the oracle."""
+    cfg = LI.with_overrides(LI.CONFIGS["c5"], dropout_p=0.0, dtype="bf16", seg_len_range=(1, 8))
+    T = 10000
+    outs = []
+    for planned in (False, True):
+        step, host, r, scales = _build_multi(cfg, [1], T, planned=planned)
+        assert step.n_seg > 2048
+        step.forward_backward(0)
+        torch.cuda.synchronize()
+        outs.append([t.clone() for l in step.linears for t in (l.Y, l.H, l.dX)] +
+                    [step.arena.grads.clone()])
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
+    lin = step.linears[0]
+    h = host[lin.proj_id]
+    tok = O.token_slots(T, r.seg_start, r.seg_slot, len(r.slot_rank))
+    slots = [O.SlotTensors(A, B, sc) for (A, B), sc in zip(h["slots"], scales)]
+    Y, _ = O.multi_lora_forward(h["X"], h["W"], slots, tok, None, 1.0)
+    dX, dA, dB = O.multi_lora_backward_vectorised(h["X"], h["W"], h["dY"], slots, tok, None, 1.0)
+    assert rel_err(lin.Y, Y) <= TOL_BF16
+    assert rel_err(lin.dX, dX) <= TOL_BF16
+    for k in range(len(slots)):
+        if np.any(tok == k):
+            assert rel_err(lin.gA[k], dA[k]) <= TOL_BF16, ("dA", k)
+            assert rel_err(lin.gB[k], dB[k]) <= TOL_BF16, ("dB", k)
+
+
 def test_multi_single_slot_equals_single_lora(L):
     """One slot holding one full-T segment gives the single-adapter result (same kernels, same
     reduction order), so the two paths agree bitwise."""
