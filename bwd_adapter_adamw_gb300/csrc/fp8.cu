@@ -190,9 +190,4 @@ cudaError_t launch_div_rows2(const DivRowsJob& a, const DivRowsJob& b, cudaStrea
   return cudaGetLastError();
 }
 
-cudaError_t launch_div_rows(const float* src, int64_t lds, const float* scale, int64_t rows,
-                            int64_t cols, float* dst, int64_t ldd, cudaStream_t st) {
-  return launch_div_rows2(DivRowsJob{src, lds, scale, rows, cols, dst, ldd}, DivRowsJob{}, st);
-}
-
 }  // namespace lora

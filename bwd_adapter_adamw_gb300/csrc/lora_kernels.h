@@ -187,7 +187,8 @@ cudaError_t launch_quant_rows_e4m3(const void* src, int64_t rows, int64_t K, uin
 // columns of W [rows, cols] bf16 -> dst [cols, rows] E4M3 codes (the rows of W^T), scale[c]
 cudaError_t launch_quant_cols_e4m3(const void* W, int64_t rows, int64_t cols, uint8_t* dst,
                                    float* scale, cudaStream_t st);
-// dst[r, :] = src[r, :] / scale[r] (fp32); two such divisions in one launch
+// dst[r, :] = src[r, :] / scale[r] (fp32), two such divisions in one launch (a job with no
+// rows is skipped)
 struct DivRowsJob {
   const float* src;
   int64_t lds;
@@ -196,8 +197,6 @@ struct DivRowsJob {
   float* dst;
   int64_t ldd;
 };
-cudaError_t launch_div_rows(const float* src, int64_t lds, const float* scale, int64_t rows,
-                            int64_t cols, float* dst, int64_t ldd, cudaStream_t st);
 cudaError_t launch_div_rows2(const DivRowsJob& a, const DivRowsJob& b, cudaStream_t st);
 
 // ---- lowrank_simt.cu: streaming CUDA-core low-rank products (fp32 activations) ----
