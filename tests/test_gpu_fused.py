@@ -30,7 +30,10 @@ def _bf16(a):
                                              # one shrink over the group's adapters side by side:
                                              # 3 x 64 and 4 x 64 columns (two MMAs per K-step)
                                              (520, 512, (512, 256, 256), 64, 0.1),
-                                             (300, 256, (256, 256, 256, 256), 64, 0.0)])
+                                             (300, 256, (256, 256, 256, 256), 64, 0.0),
+                                             # five projections: no group dA, ten reduction
+                                             # jobs over three shared launches
+                                             (264, 256, (256, 256, 512, 256, 256), 16, 0.1)])
 def test_fused_projections_match_oracle(L, T, in_d, outs, r, p):
     from bwd_adapter_adamw_gb300.step import FusedGroup, FusedLoraStep
     rng = np.random.default_rng(T + in_d + sum(outs) + r)
