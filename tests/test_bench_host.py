@@ -64,6 +64,30 @@ def test_memory_counts_groups_count_shared_inputs_once():
     assert per_proj["adamw"] == grouped["adamw"]
 
 
+def test_memory_counts_fused_classes_follow_the_launches():
+    """bf16 fused groups of 2 to 4 projections time their dB and their shared dA as classes of
+    their own; every other group (one projection here) reduces dB and dA in one launch ("red").
+    fp32 groups run as one adapter of rank n r, so all of them count as "red"."""
+    cfg = LI.CONFIGS["c4"]
+    groups = bench.fused_groups(cfg)
+    bf = bench.memory_counts(cfg, 1, groups)
+    sizes = sorted(len(g) for g in groups)
+    assert sizes == [1, 1, 2, 3]
+    T, a, r = cfg.tokens, 2, cfg.rank
+    # the o and down groups: dY' and X read once each, Hs and Gs, dB and dA read and written
+    want_red = 0
+    for g in groups:
+        if len(g) == 1:
+            p = cfg.projs[g[0]]
+            want_red += (T * p.out_dim * a + T * r * 4 + 2 * r * p.out_dim * 4 +
+                         T * p.in_dim * a + T * r * 4 + 2 * r * p.in_dim * 4)
+    assert bf["red"] == want_red
+    f32 = bench.memory_counts(LI.with_overrides(cfg, dtype="f32"), 1, groups)
+    assert f32["redB"] == 0 and f32["redA"] == 0 and f32["red"] > 0
+    # the unfused count has no merged class of its own: the bench derives it from dB + dA
+    assert "red" not in bench.memory_counts(cfg, 1)
+
+
 @pytest.mark.parametrize("name", ["c2", "c4"])
 def test_chain_config_caps_the_adapter_gain(name):
     base = LI.CONFIGS[name]
